@@ -1,0 +1,498 @@
+/*
+ * qoracle.c -- plain, slow, single-threaded CPU oracle for weight-only,
+ * group-wise, low-bit quantization and the linear layer y = x . dequant(W)^T.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg may load this library.  It shares no code with the CUDA
+ * library (no headers, tables or helpers); the two meet only through the
+ * seeded inputs the tests hand to both.
+ *
+ * What it computes, and where each step comes from:
+ *
+ *  - Affine asymmetric quantizer: scale = (max - min) / (qmax - qmin),
+ *    zero_point = qmin - round(min / scale), q = round(x / scale) + zero_point,
+ *    x_hat = (q - zero_point) * scale  (m.mzlw.cn 206779 page, section 1.1).
+ *  - Per-group statistics over groups of consecutive weights along K, with the
+ *    top 0.1 % of weights by magnitude excluded and kept as FP16 outliers that
+ *    are added back after the matrix product (bjdmk.com.cn 5414039 page,
+ *    section 2, steps 1-3; group size 128).
+ *  - 2-bit layers use a 4-entry non-uniform codebook found by k-means
+ *    (pwwt.cn page, sections 2.1 table and 4.1).
+ *  - Packing: b-bit codes stored LSB-first in a little-endian bit stream;
+ *    the pages' unpack routines read 3-bit units of 8 values in 3 bytes with
+ *    shifts 0,3,...,21, 6-bit units of 4 values in 3 bytes with shifts
+ *    0,6,12,18, 5-bit units of 8 values in 5 bytes with shifts 5i (pwwt.cn
+ *    page, sections 3.1-3.2), the 4-bit value pair as the low/high half of a
+ *    byte (section 2.1 table).
+ *  - The product accumulates in fp64 here (the pages require at least fp32
+ *    accumulation, pwwt.cn page, section 4.2).
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  round = round-half-to-even; q clamped to [0, 2^b - 1]; the group range is
+ *  widened to include 0; the fp16 scale is rounded toward +infinity from the
+ *  fp32 quotient; zero-point stored as one byte per group; "top 0.1 %" =
+ *  the floor(frac*N*K) largest |w| of the whole matrix (ties by lower linear
+ *  index); the dense code at an outlier contributes 0 (affine) or the
+ *  codebook entry nearest to 0 with the residual stored (2-bit); the codebook
+ *  is 16 Lloyd iterations from a uniform 4-level start with ties to the lower
+ *  entry.  All fp32 arithmetic below is IEEE single precision, round to
+ *  nearest even, evaluated in the order written (build with
+ *  -ffp-contract=off).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_EINVAL -1
+#define ORC_ENOMEM -2
+#define ORC_ENONFINITE -3
+
+/* ------------------------------------------------------------------ */
+/* IEEE 754 binary16 and bfloat16, written from the format definitions */
+/* ------------------------------------------------------------------ */
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double orc_f16_to_f64(uint16_t h)
+{
+    int s = h >> 15, e = (h >> 10) & 0x1F, m = h & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);              /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);  /* (1 + m/1024) * 2^(e-15) */
+    return s ? -v : v;
+}
+
+float orc_f16_to_f32(uint16_t h) { return (float)orc_f16_to_f64(h); }
+
+/* Round a float to binary16.  mode 0: nearest, ties to even.  mode 1: toward
+ * +infinity.  The value is split as q * ulp with ulp the spacing of binary16
+ * numbers in the value's binade (2^-24 below the normal range); q is then
+ * rounded to an integer, which is exactly the rounding of the significand. */
+static uint16_t f32_to_f16(float f, int mode)
+{
+    uint16_t sign = signbit(f) ? 0x8000 : 0;
+    if (isnan(f)) return (uint16_t)(sign | 0x7E00);
+    if (isinf(f)) return (uint16_t)(sign | 0x7C00);
+    double a = fabs((double)f);
+    if (a == 0.0) return sign;
+    int e2;
+    frexp(a, &e2);                 /* a in [2^(e2-1), 2^e2) */
+    int E = e2 - 1;
+    if (E < -14) E = -14;
+    double ulp = ldexp(1.0, E - 10);
+    double q = a / ulp;            /* exact: power-of-two scaling */
+    double qi;
+    if (mode == 0)
+        qi = nearbyint(q);         /* default environment: ties to even */
+    else
+        qi = sign ? floor(q) : ceil(q);   /* toward +inf on the signed value */
+    double r = qi * ulp;
+    if (r >= 65536.0) return (uint16_t)(sign | 0x7C00);   /* overflow */
+    if (r < ldexp(1.0, -14))                            /* subnormal or 0 */
+        return (uint16_t)(sign | (uint16_t)(r / ldexp(1.0, -24)));
+    frexp(r, &e2);
+    int Er = e2 - 1;
+    uint16_t m = (uint16_t)(r / ldexp(1.0, Er - 10) - 1024.0);
+    return (uint16_t)(sign | ((Er + 15) << 10) | m);
+}
+
+uint16_t orc_f32_to_f16_rn(float f) { return f32_to_f16(f, 0); }
+uint16_t orc_f32_to_f16_ru(float f) { return f32_to_f16(f, 1); }
+
+/* bfloat16 is the upper half of a binary32. */
+double orc_bf16_to_f64(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+void orc_f16_to_f32_array(const uint16_t *in, int64_t n, float *out)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = orc_f16_to_f32(in[i]);
+}
+
+void orc_f32_to_f16_array(const float *in, int64_t n, int mode, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = f32_to_f16(in[i], mode);
+}
+
+/* ------------------------------------------------------------------ */
+/* sizes                                                                */
+/* ------------------------------------------------------------------ */
+
+/* Number of outliers: floor(frac * N * K) evaluated in double. */
+int64_t orc_nnz(int64_t N, int64_t K, float frac)
+{
+    if (frac <= 0.0f) return 0;
+    return (int64_t)floor((double)frac * (double)N * (double)K);
+}
+
+static int valid_shape(int64_t N, int64_t K, int bits, int group)
+{
+    if (N <= 0 || K <= 0) return 0;
+    if (bits < 2 || bits > 6) return 0;
+    if (group != 64 && group != 128) return 0;
+    if (K % group) return 0;
+    return 1;
+}
+
+/* Bytes of each buffer of a quantized matrix (packed codes, fp16 scales,
+ * one-byte zero-points, fp16 codebooks, outlier CSR).  out[0..7] =
+ * packed, scale, zp, codebook, nnz, row_ptr, col, val. */
+int orc_sizes(int64_t N, int64_t K, int bits, int group, float frac, int64_t *out)
+{
+    if (!valid_shape(N, K, bits, group) || frac < 0.0f || frac >= 1.0f) return ORC_EINVAL;
+    int64_t ng = K / group;
+    int64_t nnz = orc_nnz(N, K, frac);
+    out[0] = N * K * bits / 8;
+    out[1] = bits == 2 ? 0 : N * ng * 2;
+    out[2] = bits == 2 ? 0 : N * ng;
+    out[3] = bits == 2 ? N * ng * 4 * 2 : 0;
+    out[4] = nnz;
+    out[5] = (N + 1) * 4;
+    out[6] = nnz * 4;
+    out[7] = nnz * 2;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* bit packing: code i occupies stream bits [b*i, b*i + b), bit j of the  */
+/* code at stream bit b*i + j; stream bit t is bit (t mod 8) of byte t/8. */
+/* ------------------------------------------------------------------ */
+void orc_pack(const uint8_t *codes, int64_t n, int bits, uint8_t *out)
+{
+    int64_t nbytes = (n * bits + 7) / 8;
+    memset(out, 0, (size_t)nbytes);
+    for (int64_t i = 0; i < n; i++)
+        for (int j = 0; j < bits; j++)
+            if ((codes[i] >> j) & 1u) {
+                int64_t t = i * bits + j;
+                out[t / 8] |= (uint8_t)(1u << (t % 8));
+            }
+}
+
+void orc_unpack(const uint8_t *in, int64_t n, int bits, uint8_t *codes)
+{
+    for (int64_t i = 0; i < n; i++) {
+        unsigned c = 0;
+        for (int j = 0; j < bits; j++) {
+            int64_t t = i * bits + j;
+            c |= ((in[t / 8] >> (t % 8)) & 1u) << j;
+        }
+        codes[i] = (uint8_t)c;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* outlier selection                                                    */
+/* ------------------------------------------------------------------ */
+typedef struct {
+    uint16_t mag;   /* |w| as the binary16 bit pattern without sign */
+    uint32_t idx;   /* linear index n*K + k */
+} okey;
+
+static int okey_cmp(const void *pa, const void *pb)
+{
+    const okey *a = (const okey *)pa, *b = (const okey *)pb;
+    if (a->mag != b->mag) return a->mag > b->mag ? -1 : 1;   /* larger |w| first */
+    return a->idx < b->idx ? -1 : (a->idx > b->idx);        /* then lower index */
+}
+
+static int finite16(uint16_t h) { return ((h >> 10) & 0x1F) != 31; }
+
+/* Mark the floor(frac*N*K) largest-|w| elements.  mask[n*K+k] = 1 for an
+ * outlier.  Returns nnz or a negative error. */
+static int64_t select_outliers(const uint16_t *W, int64_t N, int64_t K, float frac, uint8_t *mask)
+{
+    int64_t total = N * K, nnz = orc_nnz(N, K, frac);
+    memset(mask, 0, (size_t)total);
+    if (nnz == 0) return 0;
+    if (total > 0xFFFFFFFFll) return ORC_EINVAL;
+    okey *keys = (okey *)malloc(sizeof(okey) * (size_t)total);
+    if (!keys) return ORC_ENOMEM;
+    for (int64_t i = 0; i < total; i++) {
+        keys[i].mag = (uint16_t)(W[i] & 0x7FFF);
+        keys[i].idx = (uint32_t)i;
+    }
+    qsort(keys, (size_t)total, sizeof(okey), okey_cmp);
+    for (int64_t r = 0; r < nnz; r++) mask[keys[r].idx] = 1;
+    free(keys);
+    return nnz;
+}
+
+/* CSR of the outlier positions, columns ascending within a row. */
+int64_t orc_select_outliers(const uint16_t *W, int64_t N, int64_t K, float frac,
+                            int32_t *row_ptr, int32_t *col)
+{
+    uint8_t *mask = (uint8_t *)malloc((size_t)(N * K));
+    if (!mask) return ORC_ENOMEM;
+    int64_t nnz = select_outliers(W, N, K, frac, mask);
+    if (nnz >= 0) {
+        int64_t p = 0;
+        for (int64_t n = 0; n < N; n++) {
+            row_ptr[n] = (int32_t)p;
+            for (int64_t k = 0; k < K; k++)
+                if (mask[n * K + k]) col[p++] = (int32_t)k;
+        }
+        row_ptr[N] = (int32_t)p;
+    }
+    free(mask);
+    return nnz;
+}
+
+/* ------------------------------------------------------------------ */
+/* group quantizers                                                     */
+/* ------------------------------------------------------------------ */
+
+/* Affine asymmetric quantizer of one group (b in 3..6, also 4).
+ * w: g fp16 values, out: g codes.  Writes the fp16 scale and the u8 zp. */
+static void quant_group_affine(const uint16_t *w, const uint8_t *is_out, int g, int bits,
+                               uint8_t *codes, uint16_t *scale16, uint8_t *zp_out)
+{
+    const int qmin = 0, qmax = (1 << bits) - 1;
+    /* range over the non-outlier elements, widened to contain 0 */
+    float mn = 0.0f, mx = 0.0f;
+    for (int i = 0; i < g; i++) {
+        if (is_out[i]) continue;
+        float v = orc_f16_to_f32(w[i]);
+        if (v < mn) mn = v;
+        if (v > mx) mx = v;
+    }
+    uint16_t s16;
+    if (mx == mn) {
+        s16 = 0x3C00; /* 1.0 */
+    } else {
+        float range = mx - mn;
+        float s32 = range / (float)(qmax - qmin);
+        s16 = f32_to_f16(s32, 1);
+    }
+    float s = orc_f16_to_f32(s16);
+    float r = rintf(mn / s);
+    int zp = qmin - (int)r;
+    if (zp < qmin) zp = qmin;
+    if (zp > qmax) zp = qmax;
+    for (int i = 0; i < g; i++) {
+        int q;
+        if (is_out[i]) {
+            q = zp;     /* dense part contributes (zp - zp) * s = 0 */
+        } else {
+            float v = orc_f16_to_f32(w[i]);
+            q = (int)rintf(v / s) + zp;
+            if (q < qmin) q = qmin;
+            if (q > qmax) q = qmax;
+        }
+        codes[i] = (uint8_t)q;
+    }
+    *scale16 = s16;
+    *zp_out = (uint8_t)zp;
+}
+
+/* Index of the entry nearest to v; ties go to the lower index. */
+static int nearest4(float v, const float c[4])
+{
+    int best = 0;
+    float bd = fabsf(v - c[0]);
+    for (int i = 1; i < 4; i++) {
+        float d = fabsf(v - c[i]);
+        if (d < bd) {
+            bd = d;
+            best = i;
+        }
+    }
+    return best;
+}
+
+#define LLOYD_ITERS 16
+
+/* 2-bit non-uniform codebook of one group: 1-D k-means (Lloyd) with four
+ * centroids, started from four evenly spaced levels over the group range.
+ * Writes 4 fp16 entries (ascending) and the codes.  For an outlier the code
+ * is the entry nearest to 0 and *resid receives fp16(w - entry). */
+static void quant_group_codebook(const uint16_t *w, const uint8_t *is_out, int g,
+                                 uint8_t *codes, uint16_t cb16[4], uint16_t *resid)
+{
+    float mn = 0.0f, mx = 0.0f;
+    for (int i = 0; i < g; i++) {
+        if (is_out[i]) continue;
+        float v = orc_f16_to_f32(w[i]);
+        if (v < mn) mn = v;
+        if (v > mx) mx = v;
+    }
+    float c[4];
+    float step = (mx - mn) / 3.0f;
+    for (int i = 0; i < 4; i++) c[i] = mn + (float)i * step;
+
+    for (int it = 0; it < LLOYD_ITERS; it++) {
+        float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        int cnt[4] = {0, 0, 0, 0};
+        for (int i = 0; i < g; i++) {      /* ascending k */
+            if (is_out[i]) continue;
+            float v = orc_f16_to_f32(w[i]);
+            int j = nearest4(v, c);
+            sum[j] = sum[j] + v;
+            cnt[j] += 1;
+        }
+        for (int j = 0; j < 4; j++)
+            if (cnt[j] > 0) c[j] = sum[j] / (float)cnt[j];   /* empty: keep */
+    }
+
+    /* fp16 entries, then a stable ascending sort */
+    uint16_t e[4];
+    for (int i = 0; i < 4; i++) e[i] = f32_to_f16(c[i], 0);
+    for (int i = 1; i < 4; i++) {
+        uint16_t x = e[i];
+        float xv = orc_f16_to_f32(x);
+        int j = i - 1;
+        while (j >= 0 && orc_f16_to_f32(e[j]) > xv) {
+            e[j + 1] = e[j];
+            j--;
+        }
+        e[j + 1] = x;
+    }
+    float ef[4];
+    for (int i = 0; i < 4; i++) ef[i] = orc_f16_to_f32(e[i]);
+    int zero_code = nearest4(0.0f, ef);
+    for (int i = 0; i < g; i++) {
+        if (is_out[i]) {
+            codes[i] = (uint8_t)zero_code;
+            float v = orc_f16_to_f32(w[i]);
+            resid[i] = f32_to_f16(v - ef[zero_code], 0);
+        } else {
+            codes[i] = (uint8_t)nearest4(orc_f16_to_f32(w[i]), ef);
+        }
+    }
+    for (int i = 0; i < 4; i++) cb16[i] = e[i];
+}
+
+/* Quantize and pack a whole matrix W [N, K] (fp16 bit patterns).
+ * Outputs (caller-allocated, sizes from orc_sizes): packed [N, K*bits/8],
+ * scale fp16 [N, K/group] and zp u8 [N, K/group] for bits != 2,
+ * cb fp16 [N, K/group, 4] for bits == 2, outlier CSR row_ptr [N+1],
+ * col [nnz], val fp16 [nnz].  Unused outputs may be NULL. */
+int orc_quantize(const uint16_t *W, int64_t N, int64_t K, int bits, int group, float frac,
+                 uint8_t *packed, uint16_t *scale, uint8_t *zp, uint16_t *cb,
+                 int32_t *row_ptr, int32_t *col, uint16_t *val)
+{
+    if (!valid_shape(N, K, bits, group) || frac < 0.0f || frac >= 1.0f) return ORC_EINVAL;
+    for (int64_t i = 0; i < N * K; i++)
+        if (!finite16(W[i])) return ORC_ENONFINITE;
+    int64_t ng = K / group;
+    uint8_t *mask = (uint8_t *)malloc((size_t)(N * K));
+    uint8_t *codes = (uint8_t *)malloc((size_t)K);
+    uint16_t *resid = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)K);
+    if (!mask || !codes || !resid) {
+        free(mask); free(codes); free(resid);
+        return ORC_ENOMEM;
+    }
+    int64_t nnz = select_outliers(W, N, K, frac, mask);
+    if (nnz < 0) {
+        free(mask); free(codes); free(resid);
+        return (int)nnz;
+    }
+    int64_t p = 0;
+    for (int64_t n = 0; n < N; n++) {
+        const uint16_t *wr = W + n * K;
+        const uint8_t *mr = mask + n * K;
+        for (int64_t j = 0; j < ng; j++) {
+            int64_t k0 = j * group;
+            if (bits == 2)
+                quant_group_codebook(wr + k0, mr + k0, group, codes + k0, cb + (n * ng + j) * 4,
+                                     resid + k0);
+            else
+                quant_group_affine(wr + k0, mr + k0, group, bits, codes + k0, scale + n * ng + j,
+                                   zp + n * ng + j);
+        }
+        orc_pack(codes, K, bits, packed + n * (K * bits / 8));
+        row_ptr[n] = (int32_t)p;
+        for (int64_t k = 0; k < K; k++)
+            if (mr[k]) {
+                col[p] = (int32_t)k;
+                val[p] = bits == 2 ? resid[k] : wr[k];
+                p++;
+            }
+    }
+    row_ptr[N] = (int32_t)p;
+    free(mask); free(codes); free(resid);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* dequantization and the linear layer (fp64)                           */
+/* ------------------------------------------------------------------ */
+typedef struct {
+    int64_t N, K;
+    int32_t bits, group;
+    const uint8_t *packed;
+    const uint16_t *scale;
+    const uint8_t *zp;
+    const uint16_t *cb;
+    int64_t nnz;
+    const int32_t *row_ptr;
+    const int32_t *col;
+    const uint16_t *val;
+} orc_qweight;
+
+/* Row n of x_hat + S in fp64: x_hat = (q - zp) * scale, or cb[q] for 2-bit;
+ * S holds the fp16 outlier values at their positions. */
+static void dequant_row(const orc_qweight *w, int64_t n, uint8_t *codes, double *out)
+{
+    int64_t K = w->K, ng = K / w->group;
+    orc_unpack(w->packed + n * (K * w->bits / 8), K, w->bits, codes);
+    for (int64_t k = 0; k < K; k++) {
+        int64_t j = k / w->group;
+        if (w->bits == 2) {
+            out[k] = orc_f16_to_f64(w->cb[(n * ng + j) * 4 + codes[k]]);
+        } else {
+            double s = orc_f16_to_f64(w->scale[n * ng + j]);
+            out[k] = ((double)codes[k] - (double)w->zp[n * ng + j]) * s;
+        }
+    }
+    if (w->nnz > 0)
+        for (int32_t p = w->row_ptr[n]; p < w->row_ptr[n + 1]; p++)
+            out[w->col[p]] += orc_f16_to_f64(w->val[p]);
+}
+
+int orc_dequant_rows(const orc_qweight *w, int64_t n0, int64_t n1, double *out)
+{
+    if (n0 < 0 || n1 > w->N || n0 > n1) return ORC_EINVAL;
+    uint8_t *codes = (uint8_t *)malloc((size_t)w->K);
+    if (!codes) return ORC_ENOMEM;
+    for (int64_t n = n0; n < n1; n++) dequant_row(w, n, codes, out + (n - n0) * w->K);
+    free(codes);
+    return ORC_OK;
+}
+
+/* y[m, n - n0] = sum_k x[m, k] * (x_hat[n, k] + S[n, k]) for n in [n0, n1),
+ * x bf16 [M, K] with row stride ldx, accumulated in fp64 in ascending k. */
+int orc_linear_rows(const uint16_t *x, int64_t M, int64_t ldx, const orc_qweight *w,
+                    int64_t n0, int64_t n1, double *y)
+{
+    if (n0 < 0 || n1 > w->N || n0 > n1 || ldx < w->K) return ORC_EINVAL;
+    int64_t K = w->K, nn = n1 - n0;
+    double *row = (double *)malloc(sizeof(double) * (size_t)K);
+    double *xd = (double *)malloc(sizeof(double) * (size_t)(M * K));
+    uint8_t *codes = (uint8_t *)malloc((size_t)K);
+    if (!row || !xd || !codes) {
+        free(row); free(xd); free(codes);
+        return ORC_ENOMEM;
+    }
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t k = 0; k < K; k++) xd[m * K + k] = orc_bf16_to_f64(x[m * ldx + k]);
+    for (int64_t n = n0; n < n1; n++) {
+        dequant_row(w, n, codes, row);
+        for (int64_t m = 0; m < M; m++) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; k++) acc += xd[m * K + k] * row[k];
+            y[m * nn + (n - n0)] = acc;
+        }
+    }
+    free(row); free(xd); free(codes);
+    return ORC_OK;
+}

@@ -1,0 +1,418 @@
+"""Pins for the CPU oracle: facts from the pages and from mathematics that the
+oracle must reproduce.  None of these re-states the oracle's own formulas;
+each checks a property a plausible slip (dropped term, wrong sign, wrong
+shift, transposed operand, wrong rounding mode) would break.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([s.strip() for s in line.split("|")])
+    return rows
+
+
+# ---------------------------------------------------------------- packing
+PACK_ROWS = [(int(b), [int(c) for c in cs.split()], bytes.fromhex(h.replace(" ", "")))
+             for b, cs, h in _golden_rows("pack_examples.txt")]
+
+
+@pytest.mark.parametrize("bits,codes,expect", PACK_ROWS)
+def test_pack_matches_hand_worked_units(bits, codes, expect):
+    assert oracle.pack(codes, bits).tobytes() == expect
+    got = oracle.unpack(np.frombuffer(expect, np.uint8), len(codes), bits)
+    assert got.tolist() == codes
+
+
+UNIT = {2: 4, 3: 8, 4: 2, 5: 8, 6: 4}   # values per packing unit (pwwt.cn section 3.1)
+UNIT_BYTES = {2: 1, 3: 3, 4: 1, 5: 5, 6: 3}
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6])
+def test_pack_every_code_at_every_lane(bits):
+    qmax = (1 << bits) - 1
+    for background in (0, qmax):
+        for lane in range(UNIT[bits]):
+            for c in range(qmax + 1):
+                u = [background] * UNIT[bits]
+                u[lane] = c
+                p = oracle.pack(u, bits)
+                assert p.size == UNIT_BYTES[bits]
+                assert oracle.unpack(p, len(u), bits).tolist() == u
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6])
+def test_pack_units_are_independent_and_roundtrip(bits):
+    rng = np.random.default_rng(bits)
+    codes = rng.integers(0, 1 << bits, size=UNIT[bits] * 97).astype(np.uint8)
+    p = oracle.pack(codes, bits)
+    assert p.size == codes.size * bits // 8
+    assert (oracle.unpack(p, codes.size, bits) == codes).all()
+    # the stream is the concatenation of its units
+    ub, uv = UNIT_BYTES[bits], UNIT[bits]
+    for i in range(0, codes.size // uv, 13):
+        assert oracle.pack(codes[i * uv:(i + 1) * uv], bits).tobytes() == p[i * ub:(i + 1) * ub].tobytes()
+
+
+# ---------------------------------------------------------------- fp16 rounding
+def test_f16_round_nearest_even_matches_numpy():
+    rng = np.random.default_rng(7)
+    parts = [rng.standard_normal(100000) * s for s in (1e-7, 1e-5, 1e-3, 1.0, 300.0, 3e4)]
+    # midpoints between neighbouring fp16 values exercise ties-to-even
+    h = np.arange(0, 0x7BFF, 7, dtype=np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    mids = ((lo + hi) / 2).astype(np.float32)
+    edges = np.array([0.0, -0.0, 65504.0, 65519.996, 65520.0, 65536.0, 1e9, 2.0 ** -24,
+                      2.0 ** -25, 2.0 ** -26, 6.1e-5, -65520.0], np.float32)
+    v = np.concatenate(parts + [mids, -mids, edges]).astype(np.float32)
+    with np.errstate(over="ignore"):
+        ref = v.astype(np.float16).view(np.uint16)
+    assert (oracle.f32_to_f16(v, "rn") == ref).all()
+
+
+def test_f16_round_up_is_least_upper_bound():
+    rng = np.random.default_rng(8)
+    v = np.concatenate([np.abs(rng.standard_normal(100000)) * s for s in (1e-6, 1e-3, 0.02, 1.0, 500.0)])
+    v = np.concatenate([v, -v]).astype(np.float32)
+    h = oracle.f32_to_f16(v, "ru").view(np.float16)
+    up = h.astype(np.float64)
+    assert (up >= v.astype(np.float64)).all()
+    below = np.nextafter(h, np.float16(-np.inf)).astype(np.float64)
+    assert (below < v.astype(np.float64)).all()
+    # values already in fp16 are unchanged
+    exact = rng.standard_normal(1000).astype(np.float16)
+    assert (oracle.f32_to_f16(exact.astype(np.float32), "ru") == exact.view(np.uint16)).all()
+
+
+# ---------------------------------------------------------------- sizing
+def _sizing():
+    return {r[0]: (float(r[1]), float(r[2])) for r in _golden_rows("sizing.txt")}
+
+
+def _bytes(layer):
+    s = oracle.sizes(layer.N, layer.K, layer.bits, layer.group, layer.frac)
+    return sum(v for k, v in s.items() if k != "nnz")
+
+
+def test_sizing_4096_layer_at_2p5_bits():
+    v, _ = _sizing()["layer_4096_2p5bit_bytes"]
+    s = oracle.sizes(4096, 4096, 2, 128, 0.0)
+    assert s["packed"] + s["codebook"] == v
+    assert (s["packed"] + s["codebook"]) * 8 / (4096 * 4096) == 2.5
+
+
+def test_sizing_scale_overhead_per_group():
+    g = _sizing()
+    # one fp16 per group: 16 bits spread over the group's weights
+    for group, key in ((64, "scale_overhead_bits_g64"), (128, "scale_overhead_bits_g128")):
+        s = oracle.sizes(4096, 4096, 4, group, 0.0)
+        assert s["scale"] * 8 / (4096 * 4096) == g[key][0]
+
+
+def test_sizing_70b_stack_is_36GB():
+    v, tol = _sizing()["stack70b_int4_outliers_GB"]
+    total = sum(_bytes(L) for L in wl.stack_70b())
+    assert abs(total / 1e9 - v) <= tol, total
+
+
+def test_sizing_7b_mixed_stack_is_a_bit_over_3GB():
+    g = _sizing()
+    total = sum(_bytes(L) for L in wl.stack_7b()) / 1e9
+    assert g["stack7b_mixed_GB_min"][0] < total < g["stack7b_mixed_GB_max"][0], total
+    # average payload width of the stack is about 3.5 bits (pwwt.cn section 2.2: 3.4-3.6)
+    w = sum(L.N * L.K * L.bits for L in wl.stack_7b()) / sum(L.N * L.K for L in wl.stack_7b())
+    assert 3.4 <= w <= 3.7, w
+
+
+def test_nnz_is_floor_of_fraction():
+    assert oracle.nnz(4096, 4096, 0.001) == 16777
+    assert oracle.nnz(11008, 4096, 0.001) == 45088
+    assert oracle.nnz(4096, 4096, 0.0) == 0
+    assert oracle.nnz(10, 10, 0.001) == 0
+
+
+# ---------------------------------------------------------------- outliers
+def test_outliers_recover_the_planted_set():
+    N, K = 96, 1024
+    W = wl.gen_weight(N, K, seed=11, outlier_frac=0.001, outlier_seed=12)
+    n = oracle.nnz(N, K, 0.001)
+    assert n == wl.planted_count(N, K, 0.001) > 0
+    w = W.float().numpy()
+    planted = set(np.flatnonzero(np.abs(w) >= 3.0).tolist())
+    assert len(planted) == n
+    row_ptr, col = oracle.select_outliers(W, 0.001)
+    got = set()
+    for r in range(N):
+        cs = col[row_ptr[r]:row_ptr[r + 1]]
+        assert (np.diff(cs) > 0).all()
+        got |= {r * K + int(c) for c in cs}
+    assert got == planted
+
+
+def test_outlier_ties_break_by_lower_index():
+    rng = np.random.default_rng(3)
+    N, K = 6, 64
+    mags = rng.choice([0.5, 1.0, 2.0], size=(N, K), p=[0.5, 0.4, 0.1])
+    w = (mags * rng.choice([-1.0, 1.0], size=(N, K))).astype(np.float16)
+    frac = 0.2   # cuts inside the block of |w| == 1.0
+    n = oracle.nnz(N, K, frac)
+    flat = np.abs(w.astype(np.float64)).ravel()
+    expect = sorted(range(N * K), key=lambda i: (-flat[i], i))[:n]
+    row_ptr, col = oracle.select_outliers(w, frac)
+    got = sorted(r * K + int(c) for r in range(N) for c in col[row_ptr[r]:row_ptr[r + 1]])
+    assert got == sorted(expect)
+
+
+# ---------------------------------------------------------------- affine quantizer
+def _groups(q: oracle.QWeight):
+    codes = np.stack([oracle.unpack(q.packed[r], q.K, q.bits) for r in range(q.N)])
+    return codes.reshape(q.N, q.K // q.group, q.group)
+
+
+def _outlier_mask(q):
+    m = np.zeros((q.N, q.K), bool)
+    for r in range(q.N):
+        m[r, q.col[q.row_ptr[r]:q.row_ptr[r + 1]]] = True
+    return m
+
+
+@pytest.mark.parametrize("bits", [3, 4, 5, 6])
+@pytest.mark.parametrize("group", [64, 128])
+def test_affine_codes_are_nearest_grid_points(bits, group):
+    N, K, frac = 24, 1024, 0.002
+    W = wl.gen_weight(N, K, seed=100 + bits, outlier_frac=frac, outlier_seed=200 + group)
+    q = oracle.quantize(W, bits, group, frac)
+    qmax = (1 << bits) - 1
+    w = W.double().numpy()
+    xhat = oracle.dequant(q)
+    out = _outlier_mask(q)
+    assert out.sum() == oracle.nnz(N, K, frac)
+    # outliers are reproduced exactly: the dense part is 0 and S holds fp16(w)
+    assert (xhat[out] == w[out]).all()
+    assert (q.val == W.numpy().view(np.uint16)[out]).all()
+    s = oracle.f16_to_f32(q.scale).astype(np.float64)          # [N, ng]
+    zp = q.zp.astype(np.float64)
+    assert (q.zp <= qmax).all()
+    sg = np.repeat(s, group, axis=1)
+    zg = np.repeat(zp, group, axis=1)
+    err = np.abs(w - xhat)
+    # round-trip bound: half a step, plus an fp32 rounding slack of the quotient
+    assert (err[~out] <= sg[~out] * (0.5 + 2.0 ** -20)).all()
+    # brute force over all 2^b grid points: the chosen one is the nearest
+    grid = (np.arange(qmax + 1)[None, None, :] - zg[..., None]) * sg[..., None]
+    best = np.abs(w[..., None] - grid).min(axis=-1)
+    assert (err[~out] <= best[~out] + sg[~out] * 2.0 ** -20).all()
+    # the code at an outlier is the zero point
+    codes = _groups(q).reshape(N, K)
+    assert (codes[out] == zg[out]).all()
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6])
+def test_affine_scale_is_least_fp16_step_covering_the_range(bits):
+    N, K, group = 32, 1024, 128
+    W = wl.gen_weight(N, K, seed=31 + bits)
+    q = oracle.quantize(W, bits, group, 0.0)
+    qmax = (1 << bits) - 1
+    w = W.float().numpy().reshape(N, K // group, group)
+    mn = np.minimum(w.min(-1), 0).astype(np.float32)
+    mx = np.maximum(w.max(-1), 0).astype(np.float32)
+    need = (mx - mn) / np.float32(qmax)                          # fp32 quotient
+    s = q.scale.view(np.float16)
+    assert (s.astype(np.float32) >= need).all()
+    assert (np.nextafter(s, np.float16(0)).astype(np.float32) < need).all()
+
+
+def test_affine_grid_aligned_ramp_is_exact():
+    # values on a 0.25-spaced grid spanning 16 levels reproduce exactly at 4 bits
+    ramp = (np.arange(16) - 5) * 0.25
+    row = np.tile(ramp, 8)                                       # 128 values
+    W = np.stack([row, row[::-1], np.roll(row, 3)]).astype(np.float16)
+    q = oracle.quantize(W, 4, 128, 0.0)
+    assert (oracle.dequant(q) == W.astype(np.float64)).all()
+    assert (q.scale.view(np.float16) == np.float16(0.25)).all()
+    assert (q.zp == 5).all()
+
+
+def test_affine_zero_and_one_signed_groups():
+    W = np.zeros((2, 128), np.float16)
+    W[1, :] = np.float16(0.75)                                   # all positive
+    q = oracle.quantize(W, 4, 128, 0.0)
+    xhat = oracle.dequant(q)
+    assert (xhat[0] == 0).all()
+    assert (q.zp[1] == 0).all()                                  # range widened to include 0
+    assert (np.abs(xhat[1] - 0.75) <= q.scale.view(np.float16)[1, 0] / 2).all()
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6])
+def test_affine_error_is_uniform_noise(bits):
+    # rounding to a grid of step s leaves errors ~ U(-s/2, s/2): E[e^2] = s^2/12
+    N, K, group = 512, 1024, 128
+    W = wl.gen_weight(N, K, seed=55)
+    q = oracle.quantize(W, bits, group, 0.0)
+    e = (W.double().numpy() - oracle.dequant(q)).reshape(N, K // group, group)
+    s = q.scale.view(np.float16).astype(np.float64)
+    ratio = ((e ** 2).mean(-1) / s ** 2).mean()
+    assert abs(ratio - 1 / 12) < 0.1 / 12, ratio
+
+
+# ---------------------------------------------------------------- codebook (2 bit)
+def test_codebook_codes_nearest_and_lloyd_not_worse_than_uniform():
+    N, K, group, frac = 32, 1024, 64, 0.002
+    W = wl.gen_weight(N, K, seed=91, outlier_frac=frac, outlier_seed=92)
+    q = oracle.quantize(W, 2, group, frac)
+    w = W.double().numpy()
+    out = _outlier_mask(q)
+    cb = q.cb.view(np.float16).astype(np.float64)                 # [N, ng, 4]
+    assert (np.diff(cb, axis=-1) >= 0).all()                      # ascending
+    codes = _groups(q)
+    wg = w.reshape(N, -1, group)
+    og = out.reshape(N, -1, group)
+    for r in range(N):
+        for j in range(K // group):
+            keep = ~og[r, j]
+            v = wg[r, j][keep]
+            e = cb[r, j]
+            d = np.abs(v[:, None] - e[None, :])
+            chosen = d[np.arange(v.size), codes[r, j][keep]]
+            assert (chosen <= d.min(1) + 1e-12).all()
+            # Lloyd never increases distortion from its uniform start
+            mn, mx = min(v.min(), 0.0), max(v.max(), 0.0)
+            uni = mn + np.arange(4) * (mx - mn) / 3
+            d_uni = (np.abs(v[:, None] - uni[None, :]).min(1) ** 2).sum()
+            d_cb = (chosen ** 2).sum()
+            assert d_cb <= d_uni * (1 + 1e-3) + 1e-12
+            # outliers: code nearest to 0, residual restores w to fp16 precision
+            for k in np.flatnonzero(og[r, j]):
+                c = codes[r, j][k]
+                assert c == int(np.argmin(np.abs(e)))
+    xhat = oracle.dequant(q)
+    assert (np.abs(xhat[out] - w[out]) <= np.abs(w[out]) * 2.0 ** -10).all()
+
+
+def test_codebook_is_a_lloyd_fixed_point_near_the_gaussian_optimum():
+    # A converged k-means codebook satisfies the centroid condition: each
+    # entry is the mean of the values coded to it (up to fp16 rounding of the
+    # entry).  Max (1960): the 4-level minimum-MSE quantizer of N(0,1) has
+    # levels +-0.4528, +-1.5104 and distortion 0.1175.  Per-group k-means on
+    # 128 samples fits its own sample: its in-sample distortion lies below
+    # the population optimum and its outer levels sit further out.
+    n_groups, group = 3000, 128
+    w = wl.gen_group_values(n_groups, group, seed=5, std=1.0)
+    q = oracle.quantize(w.reshape(1, -1), 2, group, 0.0)
+    cb = q.cb.view(np.float16).astype(np.float64).reshape(n_groups, 4)
+    codes = _groups(q).reshape(n_groups, group)
+    v = w.astype(np.float64)
+    dev = []
+    for gi in range(n_groups):
+        for j in range(4):
+            sel = codes[gi] == j
+            if sel.any():
+                dev.append(abs(v[gi][sel].mean() - cb[gi, j]) / max(abs(cb[gi, j]), 1e-3))
+    dev = np.array(dev)
+    assert np.quantile(dev, 0.95) < 2.0 ** -10, np.quantile(dev, 0.95)
+    xhat = oracle.dequant(q).reshape(n_groups, group)
+    dist = ((v - xhat) ** 2).mean()
+    assert 0.100 < dist < 0.1175, dist
+    lv = cb.mean(0)
+    assert abs(lv.sum()) < 0.05                                   # symmetric input
+    assert 0.40 < -lv[1] < 0.55 and 0.40 < lv[2] < 0.55, lv
+    assert 1.45 < -lv[0] < 1.80 and 1.45 < lv[3] < 1.80, lv
+
+
+def test_codebook_tie_rules_on_a_closed_form_group():
+    # Values -3, -1, 1, 3 (32 each) start Lloyd exactly on its fixed point
+    # [-3, -1, 1, 3].  Two zeros sit exactly between -1 and 1: ties go to
+    # the lower entry, so the -1 cell becomes {31 x -1, 2 x 0} with mean
+    # -31/33, and stays so.  The two largest |w| (the first two 3.0 by
+    # index) are outliers; the entry nearest to 0 is then -31/33.
+    g = np.concatenate([np.full(32, -3.0), np.full(31, -1.0), [0.0, 0.0],
+                        np.full(31, 1.0), np.full(32, 3.0)])
+    W = g.astype(np.float16)[None, :]
+    q = oracle.quantize(W, 2, 128, 0.0)
+    e = q.cb.view(np.float16).astype(np.float64).ravel()
+    assert e[0] == -3.0 and e[2] == 1.0 and e[3] == 3.0
+    assert e[1] == float(np.float16(-31.0 / 33.0))
+    codes = _groups(q).ravel()
+    assert (codes[63:65] == 1).all()
+    # outlier tie: a symmetric codebook has two entries nearest to 0
+    g2 = np.concatenate([np.full(32, -3.0), np.full(32, -1.0), np.full(32, 1.0), np.full(32, 3.0)])
+    W2 = g2.astype(np.float16)[None, :]
+    q2 = oracle.quantize(W2, 2, 128, 2.0 / 128 + 1e-6)
+    assert q2.nnz == 2
+    codes2 = _groups(q2).ravel()
+    assert (q2.col == [0, 1]).all()
+    assert (codes2[q2.col] == 1).all()                            # entry -1, the lower of +-1
+    assert (q2.val.view(np.float16) == np.float16(-2.0)).all()    # -3 - (-1)
+
+
+# ---------------------------------------------------------------- the product
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6])
+def test_linear_is_x_times_dequant_transposed(bits):
+    N, K, M = 8, 128, 3
+    W = wl.gen_weight(N, K, seed=71, outlier_frac=0.02, outlier_seed=72)
+    q = oracle.quantize(W, bits, 64, 0.02)
+    x = wl.gen_x(M, K, seed=73)
+    y = oracle.linear(x, q)
+    ref = oracle.bf16_to_f64(x) @ oracle.dequant(q).T
+    assert y.shape == (M, N)
+    assert np.allclose(y, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_linear_one_hot_selects_a_column():
+    N, K = 8, 256
+    W = wl.gen_weight(N, K, seed=81, outlier_frac=0.01, outlier_seed=82)
+    q = oracle.quantize(W, 5, 128, 0.01)
+    D = oracle.dequant(q)
+    for k in (0, 1, 127, 128, 255):
+        x = np.zeros((1, K), np.uint16)
+        x[0, k] = 0x3F80                                          # bf16 1.0
+        assert (oracle.linear(x, q)[0] == D[:, k]).all()
+
+
+def test_linear_additive_over_disjoint_support_and_zero_weights():
+    N, K = 16, 256
+    W = wl.gen_weight(N, K, seed=83)
+    q = oracle.quantize(W, 3, 64, 0.0)
+    x = oracle.as_u16(wl.gen_x(2, K, seed=84)).copy()
+    x1, x2 = x.copy(), x.copy()
+    x1[:, K // 2:] = 0
+    x2[:, :K // 2] = 0
+    y, y1, y2 = (oracle.linear(a, q) for a in (x, x1, x2))
+    assert np.allclose(y, y1 + y2, rtol=1e-13, atol=1e-13)
+    qz = oracle.quantize(np.zeros((N, K), np.float16), 4, 128, 0.0)
+    assert (oracle.linear(x, qz) == 0).all()
+
+
+def test_linear_row_ranges_agree_with_full():
+    N, K = 40, 128
+    q = oracle.quantize(wl.gen_weight(N, K, seed=85), 6, 128, 0.0)
+    x = wl.gen_x(4, K, seed=86)
+    full = oracle.linear(x, q)
+    assert (oracle.linear(x, q, 7, 23) == full[:, 7:23]).all()
+
+
+def test_moe_routes_each_pair_to_its_expert():
+    E, N, K, T, k = 4, 8, 128, 10, 2
+    experts = [oracle.quantize(wl.gen_weight(N, K, seed=300 + e), 4, 128, 0.0) for e in range(E)]
+    x = wl.gen_x(T, K, seed=310)
+    topk = wl.gen_topk(T, k, E, seed=311).numpy()
+    y = oracle.moe(x, topk, experts)
+    xb = oracle.as_u16(x)
+    for t in range(T):
+        for j in range(k):
+            assert (y[t, j] == oracle.linear(xb[t:t + 1], experts[topk[t, j]])[0]).all()
+    assert all(len(set(r)) == k for r in topk.tolist())
