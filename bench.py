@@ -1,0 +1,478 @@
+#!/usr/bin/env python
+"""Benchmark of the fused-dequantization linear layer on one GB300 (or N
+replicas under torchrun).
+
+Headline (``value``): decode qGEMV weight throughput at M = 1 over the
+70B-shaped stack -- 80 layers x (q, k, v, o, gate, up, down), INT4 group 128
+with 0.1 % FP16 outliers, 36 GB of quantized weights resident in HBM.  One
+step = the 560 products of one token, captured once in a CUDA graph and
+replayed.  The unit is GB/s of packed-weight bytes (codes only); the
+all-bytes figure (codes + scales + zero-points + outlier CSR + x + y) is the
+roofline's ``achieved``.
+
+Secondary lines in the same JSON object: prefill qGEMM TFLOP/s at M = 2048 on
+one layer of the same stack, and the MoE layer (16 experts, 256 tokens, top-2
+Zipf routing) through the grouped entry point.
+
+``--impl reference`` times the CPU oracle (plain C, fp64) on the host cores
+on a bounded sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "qGEMV weight GB/s (% of HBM peak) at M=1; qGEMM TFLOP/s at M=2048"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--layers", type=int, default=80, help="layers of the 70B-shaped stack")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the prefill and MoE lines")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d.get("hbm_gbs", 6800.0), bf16=d.get("bf16_tflops", 1900.0),
+                    bf16_sust=d.get("bf16_tflops_sustained", 1700.0), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class Clocks:
+    """nvidia-smi sampled every 200 ms; only samples whose timestamp falls in
+    the timed region are kept."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        try:
+            self.dev = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        except Exception:
+            self.dev = str(torch.cuda.current_device())
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", self.dev], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        import datetime
+        for line in open(self.path):
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm = float(f[1])
+            except ValueError:
+                continue
+            if t0 <= ts <= t1:
+                rows.append((sm, f))
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "samples": 0, "reasons": [], "note": "no nvidia-smi sample inside the timed region"}
+        reasons = set()
+        for _, f in rows:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        pw = [float(f[3]) for _, f in rows if f[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm for sm, _ in rows), "sm_max_mhz": float(rows[0][1][2]),
+                "samples": len(rows), "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- our arm
+def build_stack(qg, layers, device):
+    """Quantize every matrix of the stack on the device from seeded fp16 W."""
+    ws_bytes = max(qg.qpack_workspace_size(L.N, L.K) for L in layers)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    qws = []
+    for i, L in enumerate(layers):
+        W = wl.gen_weight(L.N, L.K, seed=wl.SEED_W + i, outlier_frac=L.frac, outlier_seed=wl.SEED_OUTLIER + i,
+                          device=device, distinct_positions=False)
+        qws.append(qg.qpack_quantize(W, L.bits, L.group, L.frac, workspace=ws))
+        del W
+    torch.cuda.synchronize()
+    return qws
+
+
+def layer_bytes(qg, L, M):
+    s = qg.qpack_query_sizes(L.N, L.K, L.bits, L.group, L.frac)
+    packed = s["packed"]
+    rest = s["scale"] + s["zp"] + s["codebook"] + (L.N + 1) * 4 + s["nnz"] * 6
+    io = M * L.K * 2 + M * L.N * 4
+    return packed, packed + rest + io
+
+
+def time_graph(g, steps, warmup, world, clocks=False):
+    clk = Clocks() if clocks else None
+    if clk:
+        clk.start()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record(s)
+    for _ in range(steps):
+        g.replay()
+    e1.record(s)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    return ms, (clk.stop(t0, t1) if clk else None)
+
+
+def run_decode(qg, args, world, rank, P):
+    layers = wl.stack_70b(args.layers)
+    dev = torch.device("cuda")
+    t0 = time.time()
+    qws = build_stack(qg, layers, dev)
+    setup_s = time.time() - t0
+    M = 1
+    x_hid = wl.gen_x(M, 8192, device=dev)
+    x_ffn = wl.gen_x(M, 28672, seed=wl.SEED_X + 1, device=dev)
+    xs = [x_ffn if L.K == 28672 else x_hid for L in layers]
+    ys = [torch.empty((M, L.N), dtype=torch.float32, device=dev) for L in layers]
+
+    def step():
+        for x, q, y in zip(xs, qws, ys):
+            qg.qgemm_forward(x, q, out=y)
+
+    step()                      # eager once (lazy module/function loading outside capture)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    torch.cuda.synchronize()
+
+    ms, clocks = time_graph(g, args.steps, args.warmup, world, clocks=True)
+    ms_max = max_over_ranks(ms, world)
+    packed = sum(layer_bytes(qg, L, M)[0] for L in layers)
+    allb = sum(layer_bytes(qg, L, M)[1] for L in layers)
+    per_step_s = ms_max / 1e3 / args.steps
+    value = sum_over_ranks(packed, world) / per_step_s / 1e9
+
+    # end to end: pinned host x -> device, the captured step, final y -> host
+    xh_pin = x_hid.cpu().pin_memory()
+    xf_pin = x_ffn.cpu().pin_memory()
+    y_pin = torch.empty_like(ys[-1], device="cpu").pin_memory()
+    s = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        x_hid.copy_(xh_pin, non_blocking=True)
+        x_ffn.copy_(xf_pin, non_blocking=True)
+        g.replay()
+        y_pin.copy_(ys[-1], non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(args.steps):
+        x_hid.copy_(xh_pin, non_blocking=True)
+        x_ffn.copy_(xf_pin, non_blocking=True)
+        g.replay()
+        y_pin.copy_(ys[-1], non_blocking=True)
+    e1.record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e = {"value": sum_over_ranks(packed, world) / (e2e_ms / 1e3 / args.steps) / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": xh_pin.numel() * 2 + xf_pin.numel() * 2,
+           "d2h_bytes_per_step": y_pin.numel() * 4,
+           "note": "the step's 560 C-ABI calls captured once in a CUDA graph, replayed per step"}
+
+    achieved = allb / per_step_s / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": P["hbm"], "unit": "GB/s",
+            "frac": round(achieved / P["hbm"], 4), "traffic": None,
+            "kernel": "k_gemv<4,128,1> (decode qGEMV, the only kernel of the step)",
+            "peak_source": P["src"] + " hbm_gbs"}
+    out = dict(value=value, ms_per_step=ms_max / args.steps, roofline=roof, e2e=e2e, clocks=clocks,
+               gpu_launches=len(layers) * args.steps, setup_s=round(setup_s, 1),
+               weights_GB=round(sum(q.nbytes() for q in qws) / 1e9, 3), all_bytes_GBps=round(achieved, 1),
+               frac_of_nominal_8TBs=round(value / 8000.0, 4))
+    del qws, g
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_prefill(qg, args, P):
+    """One layer of the 70B stack at M = 2048 (7 products), TFLOP/s."""
+    layers = wl.stack_70b(1)
+    dev = torch.device("cuda")
+    qws = build_stack(qg, layers, dev)
+    M = wl.STACK_70B_PREFILL_M
+    x_hid = wl.gen_x(M, 8192, device=dev)
+    x_ffn = wl.gen_x(M, 28672, seed=wl.SEED_X + 1, device=dev)
+    xs = [x_ffn if L.K == 28672 else x_hid for L in layers]
+    ys = [torch.empty((M, L.N), dtype=torch.float32, device=dev) for L in layers]
+    wsb = max(qg.qgemm_workspace_size(M, q) for q in qws)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+
+    def step():
+        for x, q, y in zip(xs, qws, ys):
+            qg.qgemm_forward(x, q, out=y, workspace=ws)
+
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    steps = max(3, min(20, args.steps // 10))
+    ms, _ = time_graph(g, steps, 3, 1)
+    flops = sum(2.0 * M * L.N * L.K for L in layers)
+    tflops = flops / (ms / 1e3 / steps) / 1e12
+    del qws, g
+    torch.cuda.empty_cache()
+    return {"metric": "qGEMM TFLOP/s at M=2048", "value": round(tflops, 1), "unit": "TFLOP/s",
+            "ms_per_step": ms / steps, "config": "one 70B-shaped layer (7 products), INT4 g128, 0.1% outliers",
+            "frac_of_bf16_peak": round(tflops / P["bf16"], 4)}
+
+
+def run_moe(qg, args):
+    cfg = wl.MoE()
+    dev = torch.device("cuda")
+    projs = cfg.projections()
+    experts = {}
+    for pi, (name, N, K) in enumerate(projs):
+        lay = [wl.Linear(f"{name}{e}", N, K, cfg.bits, cfg.group, cfg.frac) for e in range(cfg.n_experts)]
+        qs = []
+        for e, L in enumerate(lay):
+            W = wl.gen_weight(N, K, seed=wl.SEED_W + 1000 * pi + e, device=dev)
+            qs.append(qg.qpack_quantize(W, L.bits, L.group, L.frac))
+        experts[name] = qs
+    x = wl.gen_x(cfg.tokens, cfg.hidden, device=dev)
+    xd = wl.gen_x(cfg.tokens, cfg.ffn, seed=wl.SEED_X + 2, device=dev)
+    topk = wl.gen_topk(cfg.tokens, cfg.top_k, cfg.n_experts).to(dev)
+    ys = {n: torch.empty((cfg.tokens, cfg.top_k, N), dtype=torch.float32, device=dev) for n, N, _ in projs}
+    wsb = max(qg.qgemm_moe_workspace_size(cfg.tokens, cfg.top_k, experts[n]) for n, _, _ in projs)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+
+    def step():
+        for n, _, K in projs:
+            qg.qgemm_moe_grouped(xd if K == cfg.ffn else x, topk, experts[n], out=ys[n], workspace=ws)
+
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    steps = max(5, min(50, args.steps))
+    # the layer's weights fit in L2; write a buffer larger than L2 between steps
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    s = torch.cuda.current_stream()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    tot = 0.0
+    for _ in range(steps):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        g.replay()
+        e1.record(s)
+        torch.cuda.synchronize()
+        tot += e0.elapsed_time(e1)
+    ms = tot / steps
+    touched = torch.unique(topk).numel()
+    used = sorted(set(topk.flatten().tolist()))
+    wbytes = sum(experts[n][e].nbytes() for n, _, _ in projs for e in used)
+    flops = sum(2.0 * cfg.tokens * cfg.top_k * N * K for _, N, K in projs)
+    return {"metric": "MoE grouped qGEMM", "value": round(wbytes / (ms / 1e3) / 1e9, 1), "unit": "GB/s",
+            "tflops": round(flops / (ms / 1e3) / 1e12, 2), "ms_per_step": ms, "experts_touched": touched,
+            "config": "16 experts gate/up 3072x4096 + down 4096x3072, INT4 g128, 256 tokens top-2 Zipf(1.1)",
+            "l2": "L2 flushed (512 MB write) before each step"}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample():
+    """A bounded sample of the 70B decode workload for the CPU oracle: 128
+    rows of each of the 7 projection shapes of a layer, quantized by the
+    oracle itself (INT4 g128, 0.1 % outliers), M = 1."""
+    import oracle
+    oracle.build()
+    rows = 128
+    qs, xs = [], {}
+    for i, L in enumerate(wl.stack_70b(1)):
+        W = wl.gen_weight(rows, L.K, seed=wl.SEED_W + i, outlier_frac=L.frac, outlier_seed=wl.SEED_OUTLIER + i)
+        qs.append(oracle.quantize(W, L.bits, L.group, L.frac))
+        if L.K not in xs:
+            xs[L.K] = wl.gen_x(1, L.K, seed=wl.SEED_X + L.K)
+    packed = sum(q.packed.nbytes for q in qs)
+    return qs, xs, packed
+
+
+def oracle_pass(sample):
+    """One pass of the oracle's product (fp64, one core) over the sample."""
+    import oracle
+    qs, xs, _ = sample
+    for q in qs:
+        oracle.linear(xs[q.K], q)
+
+
+def oracle_rate(seconds: float):
+    sample = oracle_sample()
+    oracle_pass(sample)                     # warm
+    t0 = time.time()
+    passes = 0
+    while passes == 0 or time.time() - t0 < seconds:
+        oracle_pass(sample)
+        passes += 1
+    dt = time.time() - t0
+    txt = (f"{passes} passes over 128 rows of each of the 7 projection shapes of a 70B-shaped layer "
+           f"(INT4 g128, 0.1% outliers, M=1; {sample[2] / 1e6:.2f} MB packed per pass) in {dt:.1f} s")
+    return sample[2] * passes / dt / 1e9, 1, txt
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    sample = oracle_sample()
+    for _ in range(args.warmup):
+        oracle_pass(sample)
+    t0 = time.time()
+    for _ in range(args.steps):
+        oracle_pass(sample)
+    dt = time.time() - t0
+    value = sample[2] * args.steps / dt / 1e9
+    txt = (f"each step: one pass of the oracle over 128 rows of each of the 7 projection shapes of a "
+           f"70B-shaped layer (INT4 g128, 0.1% outliers, M=1; {sample[2] / 1e6:.2f} MB packed)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "70B-shaped stack decode M=1, INT4 g128, 0.1% outliers (bounded row sample)"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": txt},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    import bit_weight_only_group_gb300 as qg
+    qg.lib()
+    P = peaks()
+    dec = run_decode(qg, args, world, rank, P)
+    line = {"metric": METRIC, "value": round(dec["value"], 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dec["ms_per_step"], 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int4 weights, fp16 x fp16 MMA, fp32 accumulate", "data": "synthetic",
+            "config": {"workload": "70B-shaped stack decode: 80 layers x q/k/v/o/gate/up/down, INT4 group 128, "
+                                   "0.1% FP16 outliers, M=1, y fp32",
+                       "layers": args.layers, "M": 1, "weights_GB_per_gpu": dec["weights_GB"],
+                       "l2": "inputs larger than L2 (weights per step far above 129 MB)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "frac_of_hbm_peak": round(dec["value"] / P["hbm"], 4),
+            "frac_of_nominal_8TBs": dec["frac_of_nominal_8TBs"],
+            "roofline": dec["roofline"], "e2e": dec["e2e"], "clocks": dec["clocks"],
+            "gpu_launches": dec["gpu_launches"], "setup_s": dec["setup_s"]}
+    if not args.no_secondary and rank == 0:
+        try:
+            line["prefill"] = run_prefill(qg, args, P)
+        except Exception as e:  # report, do not hide
+            line["prefill"] = {"error": repr(e)}
+        try:
+            line["moe"] = run_moe(qg, args)
+        except Exception as e:
+            line["moe"] = {"error": repr(e)}
+    if rank == 0:
+        v, cores, txt = oracle_rate(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": txt}
+        print(json.dumps(line))
+    barrier(world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

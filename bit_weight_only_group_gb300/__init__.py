@@ -1,0 +1,237 @@
+"""Python binding of libqgemm: fused-dequantization linear layers over
+weight-only, group-wise, asymmetric low-bit weights on GB300 (sm_103a).
+
+This module only marshals arguments: PyTorch supplies device memory and the
+current CUDA stream, and every step of the computation runs in the library's
+own CUDA kernels, reached through the C ABI declared in ``include/qgemm.h``.
+If ``libqgemm.so`` is missing the functions raise; there is no fallback.
+
+Entry points (same names as the C ABI):
+
+* ``qpack_query_sizes(N, K, bits, group, outlier_frac)`` -> dict of bytes
+* ``qpack_quantize(W, bits, group, outlier_frac)`` -> :class:`QWeight`
+* ``qgemm_forward(x, qw)`` -> y = x . (dequant(W) + outliers)^T
+* ``qgemm_moe_grouped(x, topk_ids, experts)`` -> y [T, k, N]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqgemm.so")
+
+QG_OK = 0
+STATUS_NAMES = {0: "QG_OK", -1: "QG_ERR_INVALID_ARG", -2: "QG_ERR_UNSUPPORTED", -3: "QG_ERR_ALIGNMENT",
+                -4: "QG_ERR_WORKSPACE", -5: "QG_ERR_CUDA", -6: "QG_ERR_TIMEOUT", -7: "QG_ERR_DEVICE_STATUS"}
+Y_F32, Y_BF16 = 0, 1
+
+ABI_FUNCTIONS = ("qpack_query_sizes", "qpack_workspace_size", "qpack_quantize", "qgemm_workspace_size",
+                 "qgemm_forward", "qgemm_moe_workspace_size", "qgemm_moe_grouped", "qgemm_last_error")
+
+
+class QgError(RuntimeError):
+    def __init__(self, status: int, where: str, message: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class QgQWeight(ctypes.Structure):
+    """Mirror of ``qg_qweight`` in include/qgemm.h."""
+    _fields_ = [("N", ctypes.c_int32), ("K", ctypes.c_int32), ("bits", ctypes.c_int32),
+                ("group", ctypes.c_int32), ("packed", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("zp", ctypes.c_void_p), ("codebook", ctypes.c_void_p), ("nnz", ctypes.c_int32),
+                ("out_row_ptr", ctypes.c_void_p), ("out_col", ctypes.c_void_p),
+                ("out_val", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m bit_weight_only_group_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        i32, f32, vp, sz = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+        psz, pi32 = ctypes.POINTER(sz), ctypes.POINTER(i32)
+        pq = ctypes.POINTER(QgQWeight)
+        L.qpack_query_sizes.argtypes = [i32, i32, i32, i32, f32, psz, psz, psz, psz, pi32]
+        L.qpack_workspace_size.argtypes = [i32, i32, psz]
+        L.qpack_quantize.argtypes = [vp, f32, pq, vp, sz, vp]
+        L.qgemm_workspace_size.argtypes = [i32, pq, psz]
+        L.qgemm_forward.argtypes = [vp, i32, i32, pq, vp, i32, ctypes.c_int, vp, sz, vp]
+        L.qgemm_moe_workspace_size.argtypes = [i32, i32, i32, pq, psz]
+        L.qgemm_moe_grouped.argtypes = [vp, i32, vp, i32, pq, i32, vp, ctypes.c_int, vp, sz, vp]
+        for name in ABI_FUNCTIONS[:-1]:
+            getattr(L, name).restype = ctypes.c_int
+        L.qgemm_last_error.argtypes = []
+        L.qgemm_last_error.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().qgemm_last_error().decode()
+
+
+def _check(st: int, where: str):
+    if st != QG_OK:
+        raise QgError(st, where, last_error())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t: torch.Tensor | None):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() else None
+
+
+# --------------------------------------------------------------------- sizes
+def qpack_query_sizes(N: int, K: int, bits: int, group: int, outlier_frac: float = 0.0) -> dict:
+    p, s, z, c = (ctypes.c_size_t() for _ in range(4))
+    n = ctypes.c_int32()
+    _check(lib().qpack_query_sizes(N, K, bits, group, outlier_frac, ctypes.byref(p), ctypes.byref(s),
+                                   ctypes.byref(z), ctypes.byref(c), ctypes.byref(n)), "qpack_query_sizes")
+    return dict(packed=p.value, scale=s.value, zp=z.value, codebook=c.value, nnz=n.value)
+
+
+def qpack_workspace_size(N: int, K: int) -> int:
+    b = ctypes.c_size_t()
+    _check(lib().qpack_workspace_size(N, K, ctypes.byref(b)), "qpack_workspace_size")
+    return b.value
+
+
+# --------------------------------------------------------------------- weights
+@dataclass
+class QWeight:
+    """A quantized matrix in device memory (canonical planar layout)."""
+    N: int
+    K: int
+    bits: int
+    group: int
+    packed: torch.Tensor                 # uint8 [N, K*bits/8]
+    scale: torch.Tensor | None           # int16 (fp16 bits) [N, K/group]
+    zp: torch.Tensor | None              # uint8 [N, K/group]
+    codebook: torch.Tensor | None        # int16 (fp16 bits) [N, K/group, 4]
+    row_ptr: torch.Tensor | None         # int32 [N+1]
+    col: torch.Tensor | None             # int32 [nnz]
+    val: torch.Tensor | None             # int16 (fp16 bits) [nnz]
+    nnz: int = 0
+
+    @staticmethod
+    def empty(N: int, K: int, bits: int, group: int, outlier_frac: float = 0.0, device="cuda") -> "QWeight":
+        sz = qpack_query_sizes(N, K, bits, group, outlier_frac)
+        ng = K // group
+        u8, i16, i32 = torch.uint8, torch.int16, torch.int32
+        nnz = sz["nnz"]
+        return QWeight(
+            N, K, bits, group,
+            packed=torch.empty((N, K * bits // 8), dtype=u8, device=device),
+            scale=torch.empty((N, ng), dtype=i16, device=device) if bits != 2 else None,
+            zp=torch.empty((N, ng), dtype=u8, device=device) if bits != 2 else None,
+            codebook=torch.empty((N, ng, 4), dtype=i16, device=device) if bits == 2 else None,
+            row_ptr=torch.empty(N + 1, dtype=i32, device=device),
+            col=torch.empty(max(nnz, 1), dtype=i32, device=device)[:nnz],
+            val=torch.empty(max(nnz, 1), dtype=i16, device=device)[:nnz],
+            nnz=nnz)
+
+    def desc(self) -> QgQWeight:
+        return QgQWeight(self.N, self.K, self.bits, self.group, _ptr(self.packed), _ptr(self.scale),
+                         _ptr(self.zp), _ptr(self.codebook), self.nnz, _ptr(self.row_ptr),
+                         _ptr(self.col), _ptr(self.val))
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in
+                   (self.packed, self.scale, self.zp, self.codebook, self.row_ptr, self.col, self.val)
+                   if t is not None)
+
+
+def qpack_quantize(W: torch.Tensor, bits: int, group: int, outlier_frac: float = 0.0,
+                   out: QWeight | None = None, workspace: torch.Tensor | None = None, stream=None) -> QWeight:
+    """Quantize and pack W [N, K] (fp16, CUDA) on the device."""
+    if W.dtype != torch.float16 or not W.is_cuda or W.dim() != 2:
+        raise ValueError("W must be a 2-D float16 CUDA tensor")
+    W = W.contiguous()
+    N, K = W.shape
+    qw = out if out is not None else QWeight.empty(N, K, bits, group, outlier_frac, W.device)
+    ws_bytes = qpack_workspace_size(N, K)
+    ws = workspace if workspace is not None else torch.empty(ws_bytes, dtype=torch.uint8, device=W.device)
+    d = qw.desc()
+    _check(lib().qpack_quantize(_ptr(W), outlier_frac, ctypes.byref(d), _ptr(ws), ws.numel(), _stream(stream)),
+           "qpack_quantize")
+    return qw
+
+
+def qgemm_workspace_size(M: int, qw: QWeight) -> int:
+    b = ctypes.c_size_t()
+    d = qw.desc()
+    _check(lib().qgemm_workspace_size(M, ctypes.byref(d), ctypes.byref(b)), "qgemm_workspace_size")
+    return b.value
+
+
+def qgemm_forward(x: torch.Tensor, qw: QWeight, out: torch.Tensor | None = None,
+                  out_dtype: torch.dtype = torch.float32, workspace: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """y [M, N] = x [M, K] (bf16, CUDA) times (dequant(W) + outliers)^T."""
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D bfloat16 CUDA tensor with unit inner stride")
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, qw.N), dtype=out_dtype, device=x.device)
+    yt = Y_BF16 if out.dtype == torch.bfloat16 else Y_F32
+    if out.dtype not in (torch.float32, torch.bfloat16) or out.stride(1) != 1:
+        raise ValueError("out must be float32 or bfloat16 with unit inner stride")
+    need = qgemm_workspace_size(M, qw)
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    d = qw.desc()
+    _check(lib().qgemm_forward(_ptr(x), M, x.stride(0), ctypes.byref(d), _ptr(out), out.stride(0), yt,
+                               _ptr(workspace) if need else None, workspace.numel() if need else 0,
+                               _stream(stream)), "qgemm_forward")
+    return out
+
+
+def _desc_array(experts):
+    arr = (QgQWeight * len(experts))()
+    for i, q in enumerate(experts):
+        arr[i] = q.desc()
+    return arr
+
+
+def qgemm_moe_workspace_size(T: int, k: int, experts) -> int:
+    b = ctypes.c_size_t()
+    arr = _desc_array(experts)
+    _check(lib().qgemm_moe_workspace_size(T, k, len(experts), arr, ctypes.byref(b)), "qgemm_moe_workspace_size")
+    return b.value
+
+
+def qgemm_moe_grouped(x: torch.Tensor, topk_ids: torch.Tensor, experts, out: torch.Tensor | None = None,
+                      out_dtype: torch.dtype = torch.float32, workspace: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """y [T, k, N]: y[t, j] = x[t] . (dequant(W_e) + outliers_e)^T with e = topk_ids[t, j]."""
+    if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bfloat16 CUDA tensor [T, K]")
+    if topk_ids.dtype != torch.int32 or not topk_ids.is_contiguous():
+        raise ValueError("topk_ids must be a contiguous int32 tensor [T, k]")
+    T, k = topk_ids.shape
+    N = experts[0].N
+    if out is None:
+        out = torch.empty((T, k, N), dtype=out_dtype, device=x.device)
+    yt = Y_BF16 if out.dtype == torch.bfloat16 else Y_F32
+    arr = _desc_array(experts)
+    need = qgemm_moe_workspace_size(T, k, experts)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    _check(lib().qgemm_moe_grouped(_ptr(x), T, _ptr(topk_ids), k, arr, len(experts), _ptr(out), yt,
+                                   _ptr(workspace), workspace.numel(), _stream(stream)), "qgemm_moe_grouped")
+    return out

@@ -1,0 +1,222 @@
+// C-ABI entry points of libqgemm: argument validation (host, before any
+// launch), dispatch to the kernels, and per-thread error messages.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "qg_internal.h"
+
+namespace qg {
+
+namespace {
+thread_local char g_err[512] = {0};
+}
+
+void set_error(const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+}
+
+qg_status fail(qg_status st, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+qg_status cuda_fail(cudaError_t e, const char* what)
+{
+    set_error("%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+    return QG_ERR_CUDA;
+}
+
+int num_sms()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    if (dev >= 0 && dev < 64) cache[dev] = v;
+    return v;
+}
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t nnz_of(int64_t N, int64_t K, float frac)
+{
+    if (frac <= 0.0f) return 0;
+    return (int64_t)std::floor((double)frac * (double)N * (double)K);
+}
+
+qg_status check_shape(int64_t N, int64_t K, int bits, int group)
+{
+    if (N <= 0 || K <= 0) return fail(QG_ERR_INVALID_ARG, "N and K must be positive (N=%lld K=%lld)", (long long)N, (long long)K);
+    if (bits < 2 || bits > 6) return fail(QG_ERR_UNSUPPORTED, "bits must be 2..6 (got %d)", bits);
+    if (group != 64 && group != 128) return fail(QG_ERR_UNSUPPORTED, "group must be 64 or 128 (got %d)", group);
+    if (K % group) return fail(QG_ERR_INVALID_ARG, "K=%lld is not a multiple of group=%d", (long long)K, group);
+    if ((int64_t)N * K > (int64_t)1 << 34) return fail(QG_ERR_INVALID_ARG, "N*K too large");
+    return QG_OK;
+}
+
+// Validate a weight descriptor for use by a product kernel.
+qg_status check_qweight(const qg_qweight* w, const char* who)
+{
+    if (!w) return fail(QG_ERR_INVALID_ARG, "%s: null weight descriptor", who);
+    qg_status st = check_shape(w->N, w->K, w->bits, w->group);
+    if (st != QG_OK) return st;
+    if (!w->packed) return fail(QG_ERR_INVALID_ARG, "%s: packed is null", who);
+    if (!aligned(w->packed, 16)) return fail(QG_ERR_ALIGNMENT, "%s: packed must be 16-byte aligned", who);
+    if (w->bits == 2) {
+        if (!w->codebook) return fail(QG_ERR_INVALID_ARG, "%s: codebook is null for bits=2", who);
+        if (!aligned(w->codebook, 8)) return fail(QG_ERR_ALIGNMENT, "%s: codebook must be 8-byte aligned", who);
+    } else {
+        if (!w->scale || !w->zp) return fail(QG_ERR_INVALID_ARG, "%s: scale/zp null for bits=%d", who, w->bits);
+        if (!aligned(w->scale, 2)) return fail(QG_ERR_ALIGNMENT, "%s: scale must be 2-byte aligned", who);
+    }
+    if (w->nnz < 0) return fail(QG_ERR_INVALID_ARG, "%s: nnz < 0", who);
+    if (w->nnz > 0) {
+        if (!w->out_row_ptr || !w->out_col || !w->out_val)
+            return fail(QG_ERR_INVALID_ARG, "%s: outlier arrays null with nnz=%d", who, w->nnz);
+        if (!aligned(w->out_row_ptr, 4) || !aligned(w->out_col, 4) || !aligned(w->out_val, 2))
+            return fail(QG_ERR_ALIGNMENT, "%s: outlier arrays misaligned", who);
+    }
+    return QG_OK;
+}
+
+}  // namespace
+}  // namespace qg
+
+using namespace qg;
+
+extern "C" {
+
+const char* qgemm_last_error(void) { return g_err; }
+
+qg_status qpack_query_sizes(int32_t N, int32_t K, int32_t bits, int32_t group, float outlier_frac,
+                            size_t* packed_bytes, size_t* scale_bytes, size_t* zp_bytes,
+                            size_t* codebook_bytes, int32_t* nnz)
+{
+    qg_status st = check_shape(N, K, bits, group);
+    if (st != QG_OK) return st;
+    if (!(outlier_frac >= 0.0f && outlier_frac < 1.0f))
+        return fail(QG_ERR_INVALID_ARG, "outlier_frac must be in [0, 1)");
+    const int64_t ng = K / group;
+    const int64_t n = nnz_of(N, K, outlier_frac);
+    if (n > INT32_MAX) return fail(QG_ERR_INVALID_ARG, "too many outliers");
+    if (packed_bytes) *packed_bytes = (size_t)N * K * bits / 8;
+    if (scale_bytes) *scale_bytes = bits == 2 ? 0 : (size_t)N * ng * 2;
+    if (zp_bytes) *zp_bytes = bits == 2 ? 0 : (size_t)N * ng;
+    if (codebook_bytes) *codebook_bytes = bits == 2 ? (size_t)N * ng * 8 : 0;
+    if (nnz) *nnz = (int32_t)n;
+    return QG_OK;
+}
+
+qg_status qpack_workspace_size(int32_t N, int32_t K, size_t* bytes)
+{
+    if (!bytes) return fail(QG_ERR_INVALID_ARG, "bytes is null");
+    if (N <= 0 || K <= 0) return fail(QG_ERR_INVALID_ARG, "N and K must be positive");
+    *bytes = quantize_workspace_bytes(N, K);
+    return QG_OK;
+}
+
+qg_status qpack_quantize(const uint16_t* W, float outlier_frac, const qg_qweight* out, void* ws,
+                         size_t ws_bytes, void* stream)
+{
+    if (!W) return fail(QG_ERR_INVALID_ARG, "qpack_quantize: W is null");
+    if (!aligned(W, 16)) return fail(QG_ERR_ALIGNMENT, "qpack_quantize: W must be 16-byte aligned");
+    qg_status st = check_qweight(out, "qpack_quantize");
+    if (st != QG_OK) return st;
+    if (!(outlier_frac >= 0.0f && outlier_frac < 1.0f))
+        return fail(QG_ERR_INVALID_ARG, "qpack_quantize: outlier_frac must be in [0, 1)");
+    const int64_t n = nnz_of(out->N, out->K, outlier_frac);
+    if (n != out->nnz)
+        return fail(QG_ERR_INVALID_ARG, "qpack_quantize: nnz=%d but floor(frac*N*K)=%lld", out->nnz, (long long)n);
+    if (out->nnz > 0 && (int64_t)out->N * out->K > 0xFFFFFFFFll)
+        return fail(QG_ERR_INVALID_ARG, "qpack_quantize: N*K above 2^32 with outliers");
+    const size_t need = quantize_workspace_bytes(out->N, out->K);
+    if (!ws || ws_bytes < need)
+        return fail(QG_ERR_WORKSPACE, "qpack_quantize: workspace %zu bytes < %zu", ws ? ws_bytes : (size_t)0, need);
+    if (!aligned(ws, 256)) return fail(QG_ERR_ALIGNMENT, "qpack_quantize: workspace must be 256-byte aligned");
+    return launch_quantize(W, outlier_frac, *out, ws, static_cast<cudaStream_t>(stream));
+}
+
+qg_status qgemm_workspace_size(int32_t M, const qg_qweight* w, size_t* bytes)
+{
+    if (!bytes) return fail(QG_ERR_INVALID_ARG, "bytes is null");
+    qg_status st = check_qweight(w, "qgemm_workspace_size");
+    if (st != QG_OK) return st;
+    if (M < 0) return fail(QG_ERR_INVALID_ARG, "M < 0");
+    *bytes = M <= kGemvMaxM ? 0 : gemm_workspace_bytes(M, *w);
+    return QG_OK;
+}
+
+qg_status qgemm_forward(const uint16_t* x, int32_t M, int32_t ldx, const qg_qweight* w, void* y,
+                        int32_t ldy, qg_ydtype yt, void* ws, size_t ws_bytes, void* stream)
+{
+    qg_status st = check_qweight(w, "qgemm_forward");
+    if (st != QG_OK) return st;
+    if (M < 0) return fail(QG_ERR_INVALID_ARG, "qgemm_forward: M < 0");
+    if (M == 0) return QG_OK;
+    if (!x || !y) return fail(QG_ERR_INVALID_ARG, "qgemm_forward: x or y is null");
+    if (ldx < w->K) return fail(QG_ERR_INVALID_ARG, "qgemm_forward: ldx=%d < K=%d", ldx, w->K);
+    if (ldy < w->N) return fail(QG_ERR_INVALID_ARG, "qgemm_forward: ldy=%d < N=%d", ldy, w->N);
+    if (yt != QG_Y_F32 && yt != QG_Y_BF16) return fail(QG_ERR_INVALID_ARG, "qgemm_forward: bad y dtype");
+    if (!aligned(x, 2) || !aligned(y, yt == QG_Y_F32 ? 4 : 2))
+        return fail(QG_ERR_ALIGNMENT, "qgemm_forward: x or y misaligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (M <= kGemvMaxM) return launch_gemv(x, M, ldx, *w, y, ldy, yt, s);
+    const size_t need = gemm_workspace_bytes(M, *w);
+    if (need && (!ws || ws_bytes < need))
+        return fail(QG_ERR_WORKSPACE, "qgemm_forward: workspace %zu bytes < %zu", ws ? ws_bytes : (size_t)0, need);
+    if (need && !aligned(ws, 256)) return fail(QG_ERR_ALIGNMENT, "qgemm_forward: workspace must be 256-byte aligned");
+    return launch_gemm(x, M, ldx, *w, y, ldy, yt, ws, ws_bytes, s);
+}
+
+qg_status qgemm_moe_workspace_size(int32_t T, int32_t k, int32_t E, const qg_qweight* experts,
+                                   size_t* bytes)
+{
+    if (!bytes) return fail(QG_ERR_INVALID_ARG, "bytes is null");
+    if (T < 0 || k <= 0 || E <= 0 || E > kMoeMaxExperts || !experts)
+        return fail(QG_ERR_INVALID_ARG, "qgemm_moe_workspace_size: bad T/k/E");
+    *bytes = moe_workspace_bytes(T, k, E, experts);
+    return QG_OK;
+}
+
+qg_status qgemm_moe_grouped(const uint16_t* x, int32_t T, const int32_t* topk_ids, int32_t k,
+                            const qg_qweight* experts, int32_t E, void* y, qg_ydtype yt, void* ws,
+                            size_t ws_bytes, void* stream)
+{
+    if (T < 0 || k <= 0) return fail(QG_ERR_INVALID_ARG, "qgemm_moe_grouped: T < 0 or k <= 0");
+    if (E <= 0 || E > kMoeMaxExperts)
+        return fail(QG_ERR_INVALID_ARG, "qgemm_moe_grouped: E must be in 1..%d", kMoeMaxExperts);
+    if (!experts) return fail(QG_ERR_INVALID_ARG, "qgemm_moe_grouped: experts is null");
+    for (int e = 0; e < E; e++) {
+        qg_status st = check_qweight(&experts[e], "qgemm_moe_grouped");
+        if (st != QG_OK) return st;
+        if (experts[e].N != experts[0].N || experts[e].K != experts[0].K || experts[e].bits != experts[0].bits ||
+            experts[e].group != experts[0].group)
+            return fail(QG_ERR_INVALID_ARG, "qgemm_moe_grouped: experts differ in N/K/bits/group");
+    }
+    if (T == 0) return QG_OK;
+    if (!x || !topk_ids || !y) return fail(QG_ERR_INVALID_ARG, "qgemm_moe_grouped: null x/topk_ids/y");
+    if (yt != QG_Y_F32 && yt != QG_Y_BF16) return fail(QG_ERR_INVALID_ARG, "qgemm_moe_grouped: bad y dtype");
+    if (!aligned(x, 2) || !aligned(topk_ids, 4) || !aligned(y, yt == QG_Y_F32 ? 4 : 2))
+        return fail(QG_ERR_ALIGNMENT, "qgemm_moe_grouped: misaligned x/topk_ids/y");
+    const size_t need = moe_workspace_bytes(T, k, E, experts);
+    if (need && (!ws || ws_bytes < need))
+        return fail(QG_ERR_WORKSPACE, "qgemm_moe_grouped: workspace %zu bytes < %zu", ws ? ws_bytes : (size_t)0, need);
+    if (need && !aligned(ws, 256)) return fail(QG_ERR_ALIGNMENT, "qgemm_moe_grouped: workspace must be 256-byte aligned");
+    return launch_moe(x, T, topk_ids, k, experts, E, y, yt, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

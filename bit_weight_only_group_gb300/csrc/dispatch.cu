@@ -1,0 +1,216 @@
+// Host dispatch of the decode kernels by bit width, and the grouped (MoE)
+// entry: device-side routing (a stable counting sort of the (token, slot)
+// pairs by expert) followed by the grouped decode kernel.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "gemv_impl.cuh"
+#include "qg_internal.h"
+
+namespace qg {
+namespace gemv {
+extern template qg_status launch_dense<2>(const Problem&, int, cudaStream_t);
+extern template qg_status launch_dense<3>(const Problem&, int, cudaStream_t);
+extern template qg_status launch_dense<4>(const Problem&, int, cudaStream_t);
+extern template qg_status launch_dense<5>(const Problem&, int, cudaStream_t);
+extern template qg_status launch_dense<6>(const Problem&, int, cudaStream_t);
+extern template qg_status launch_grouped<2>(const MoeTable&, int, int, int, int, cudaStream_t);
+extern template qg_status launch_grouped<3>(const MoeTable&, int, int, int, int, cudaStream_t);
+extern template qg_status launch_grouped<4>(const MoeTable&, int, int, int, int, cudaStream_t);
+extern template qg_status launch_grouped<5>(const MoeTable&, int, int, int, int, cudaStream_t);
+extern template qg_status launch_grouped<6>(const MoeTable&, int, int, int, int, cudaStream_t);
+}  // namespace gemv
+
+namespace {
+
+gemv::Problem make_problem(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,
+                           qg_ydtype yt)
+{
+    gemv::Problem p;
+    p.x = reinterpret_cast<const __nv_bfloat16*>(x);
+    p.ldx = ldx; p.M = M; p.N = w.N; p.K = w.K;
+    p.rowmap = nullptr; p.xdiv = 1;
+    p.packed = w.packed;
+    p.scale = w.scale;
+    p.zp = w.zp;
+    p.cb = reinterpret_cast<const uint2*>(w.codebook);
+    p.row_ptr = w.out_row_ptr;
+    p.col = w.out_col;
+    p.val = w.out_val;
+    p.nnz = w.nnz;
+    p.y = y; p.ldy = ldy; p.y_bf16 = yt == QG_Y_BF16;
+    return p;
+}
+
+qg_status dense_by_bits(const gemv::Problem& p, int bits, int group, cudaStream_t s)
+{
+    switch (bits) {
+        case 2: return gemv::launch_dense<2>(p, group, s);
+        case 3: return gemv::launch_dense<3>(p, group, s);
+        case 4: return gemv::launch_dense<4>(p, group, s);
+        case 5: return gemv::launch_dense<5>(p, group, s);
+        default: return gemv::launch_dense<6>(p, group, s);
+    }
+}
+
+// ---------------------------------------------------------------- routing
+// One block.  counts -> exclusive offsets -> stable placement: pair i goes
+// to offsets[e] + (number of earlier pairs with the same expert).
+constexpr int kRouteThreads = 1024;
+
+__global__ void __launch_bounds__(kRouteThreads) k_route(const int* __restrict__ topk, int P, int E, int chunk,
+                                                         int* __restrict__ offsets, int* __restrict__ perm,
+                                                         int2* __restrict__ items, int* __restrict__ n_items)
+{
+    __shared__ int cnt[kMoeMaxExperts];
+    __shared__ int off[kMoeMaxExperts];
+    __shared__ int carry[kMoeMaxExperts];
+    __shared__ int wtab[kRouteThreads / 32][kMoeMaxExperts];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e < E; e += kRouteThreads) cnt[e] = 0, carry[e] = 0;
+    __syncthreads();
+    for (int i = tid; i < P; i += kRouteThreads) {
+        const int e = topk[i];
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0, ni = 0;
+        for (int e = 0; e < E; e++) {
+            off[e] = acc;
+            offsets[e] = acc;
+            acc += cnt[e];
+            for (int c = 0; c * chunk < cnt[e]; c++) items[ni++] = make_int2(e, c);
+        }
+        offsets[E] = acc;
+        *n_items = ni;
+    }
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = 0; base < P; base += kRouteThreads) {
+        for (int q = tid; q < (kRouteThreads / 32) * E; q += kRouteThreads) wtab[q / E][q % E] = 0;
+        __syncthreads();
+        const int i = base + tid;
+        const int e = i < P ? topk[i] : -1;
+        const bool valid = e >= 0 && e < E;
+        const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+        const int wrank = __popc(peers & lt);
+        if (valid && wrank == 0) wtab[warp][e] = __popc(peers);
+        __syncthreads();
+        if (valid) {
+            int before = carry[e];
+            for (int w = 0; w < warp; w++) before += wtab[w][e];
+            perm[off[e] + before + wrank] = i;
+        }
+        __syncthreads();
+        for (int q = tid; q < E; q += kRouteThreads) {
+            int s = 0;
+            for (int w = 0; w < kRouteThreads / 32; w++) s += wtab[w][q];
+            carry[q] += s;
+        }
+        __syncthreads();
+    }
+}
+
+struct MoeWs {
+    int* offsets;
+    int* perm;
+    int2* items;
+    int* n_items;
+};
+
+// Upper bound on work items: sum over experts of ceil(count / chunk) with the
+// smallest chunk (8 pairs).
+inline int max_items_for(int P, int E, int chunk) { return (int)ceil_div(P, chunk) + E; }
+
+size_t moe_ws_layout(int T, int k, int E, MoeWs* p, void* base)
+{
+    const size_t P = (size_t)T * k;
+    const size_t o_off = 0;
+    const size_t o_n = align_up(sizeof(int) * ((size_t)E + 1), 256);
+    const size_t o_perm = o_n + 256;
+    const size_t o_items = align_up(o_perm + sizeof(int) * P, 256);
+    const size_t total = align_up(o_items + sizeof(int2) * (size_t)max_items_for((int)P, E, 8), 256);
+    if (p && base) {
+        char* b = static_cast<char*>(base);
+        p->offsets = reinterpret_cast<int*>(b + o_off);
+        p->n_items = reinterpret_cast<int*>(b + o_n);
+        p->perm = reinterpret_cast<int*>(b + o_perm);
+        p->items = reinterpret_cast<int2*>(b + o_items);
+    }
+    return total;
+}
+
+}  // namespace
+
+qg_status launch_gemv(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,
+                      qg_ydtype yt, cudaStream_t s)
+{
+    return dense_by_bits(make_problem(x, M, ldx, w, y, ldy, yt), w.bits, w.group, s);
+}
+
+// Products with M above the decode kernel's range, in 64-row passes of the
+// decode kernel.  (The tensor-core kernel takes these over where built.)
+qg_status launch_gemv_chunked(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,
+                              qg_ydtype yt, cudaStream_t s)
+{
+    const size_t esz = yt == QG_Y_BF16 ? 2 : 4;
+    for (int m0 = 0; m0 < M; m0 += kGemvMaxM) {
+        const int mc = std::min(kGemvMaxM, M - m0);
+        qg_status st = launch_gemv(x + (size_t)m0 * ldx, mc, ldx, w, static_cast<char*>(y) + (size_t)m0 * ldy * esz,
+                                   ldy, yt, s);
+        if (st != QG_OK) return st;
+    }
+    return QG_OK;
+}
+
+size_t moe_workspace_bytes(int T, int k, int E, const qg_qweight*) { return moe_ws_layout(T, k, E, nullptr, nullptr); }
+
+qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const qg_qweight* experts, int E,
+                     void* y, qg_ydtype yt, void* ws, size_t, cudaStream_t s)
+{
+    MoeWs p;
+    moe_ws_layout(T, k, E, &p, ws);
+    const int P = T * k;
+    const qg_qweight& w0 = experts[0];
+    // tokens per CTA chunk from the mean load per expert
+    const int mean = (P + E - 1) / E;
+    const int nt = gemv::nt_for(std::max(1, mean));
+    k_route<<<1, kRouteThreads, 0, s>>>(topk, P, E, 8 * nt, p.offsets, p.perm, p.items, p.n_items);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
+
+    gemv::MoeTable t;
+    memset(&t, 0, sizeof(t));
+    t.x = reinterpret_cast<const __nv_bfloat16*>(x);
+    t.ldx = w0.K; t.N = w0.N; t.K = w0.K; t.topk = k;
+    t.chunk = 8 * nt;
+    t.offsets = p.offsets;
+    t.perm = p.perm;
+    t.items = p.items;
+    t.n_items = p.n_items;
+    t.y = y;
+    t.y_bf16 = yt == QG_Y_BF16;
+    for (int i = 0; i < E; i++) {
+        t.packed[i] = experts[i].packed;
+        t.scale[i] = experts[i].scale;
+        t.zp[i] = experts[i].zp;
+        t.cb[i] = reinterpret_cast<const uint2*>(experts[i].codebook);
+        t.row_ptr[i] = experts[i].out_row_ptr;
+        t.col[i] = experts[i].out_col;
+        t.val[i] = experts[i].out_val;
+        t.nnz[i] = experts[i].nnz;
+    }
+    const int maxi = max_items_for(P, E, t.chunk);
+    const int expect = std::min(maxi, (int)ceil_div(P, t.chunk) + E / 2);
+    switch (w0.bits) {
+        case 2: return gemv::launch_grouped<2>(t, maxi, expect, w0.group, nt, s);
+        case 3: return gemv::launch_grouped<3>(t, maxi, expect, w0.group, nt, s);
+        case 4: return gemv::launch_grouped<4>(t, maxi, expect, w0.group, nt, s);
+        case 5: return gemv::launch_grouped<5>(t, maxi, expect, w0.group, nt, s);
+        default: return gemv::launch_grouped<6>(t, maxi, expect, w0.group, nt, s);
+    }
+}
+
+}  // namespace qg

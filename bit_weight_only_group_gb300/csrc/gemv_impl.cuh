@@ -1,0 +1,613 @@
+// Decode-side fused dequantization product for small M (M <= 64):
+//     y[m, n] = sum_k x[m, k] * (w_hat[n, k] + S[n, k])
+// Memory-bound: every packed weight byte is read from HBM once, unpacked in
+// registers (never written back as fp16 -- pwwt.cn page, section 4.1: unpack
+// and multiply-accumulate in one loop, the value lives only in registers),
+// and consumed by warp-level tensor-core MMAs with fp32 accumulation
+// (section 4.2 requires fp32 accumulation).
+//
+// Layout of the work (GB300, 152 SMs):
+//  * a CTA = 4 warps = 64 consecutive weight rows; a warp owns 16 rows and
+//    issues mma.sync.m16n8k16 with the weights as the A operand (rows = W
+//    rows, "swap AB") and up to 8 tokens per n8 tile as B;
+//  * K is split across the CTAs of a thread-block cluster (1, S, 1); their
+//    fp32 partials are summed in rank order through distributed shared
+//    memory -- deterministic, no global workspace, no spin-waits;
+//  * each thread owns, per group and row, one contiguous quarter of the
+//    group's codes ("chunk").  Inside an MMA the 16 k positions may be
+//    permuted freely as long as A and B agree, so each thread turns its chunk
+//    into fp16 pairs with one AND+OR (LOP3) per pair: a b-bit code placed at
+//    mantissa bits [p, p+b) of the fp16 value 1024 reads as 1024 + 2^p * q;
+//    one packed FMA (HFMA2) by (2^-p, -1024*2^-p - zp) turns the pair into the
+//    exact integers q - zp.  The MMA sums (q - zp) * x exactly per product in
+//    fp32, and the group's fp16 scale is applied to that fp32 partial.
+//    (Magic-number int->fp16 conversion after Kim et al. 2022, "Who Says
+//    Elephants Can't Run"; the per-width pair plans are this library's own.)
+//  * 2-bit groups hold 4 fp16 codebook entries; two byte-permutes (PRMT)
+//    look up a pair of entries at once from a 2-register table.
+//  * the FP16 outliers (bjdmk.com.cn 5414039 page, section 2, step 3: added
+//    back after the product) are applied in the cluster epilogue from CSR.
+#pragma once
+
+#include <cooperative_groups.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+#include <type_traits>
+
+#include "qg_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace qg {
+namespace gemv {
+
+constexpr int kWarps = 4;
+constexpr int kRowsPerCta = 16 * kWarps;
+
+// ---------------------------------------------------------------- pair plans
+// Entry e of a thread chunk with NC codes: codes `lo` and `hi` of the chunk
+// go to the low and high fp16 half; in the 32-bit window that starts at
+// chunk bit S, code lo sits at bit plo and code hi at bit 16 + phi
+// (plo, phi <= 10 - bits, so 1024 + 2^p * q stays an exact fp16 integer).
+// For bits == 2 the entry only names the two codes of a PRMT lookup.
+struct PairE {
+    int lo, hi, plo, phi, S;
+};
+
+__host__ __device__ constexpr PairE plan_entry(int bits, int nc, int e)
+{
+    if (bits == 4) {   // (i, i+4) within each 8-code word; windows at 0, 8
+        const int j = e / 4, q = e % 4;
+        return PairE{8 * j + q, 8 * j + q + 4, (q & 1) * 4, (q & 1) * 4, 32 * j + (q / 2) * 8};
+    }
+    if (bits == 2) {   // PRMT pairs: (j, j+4) and (j+8, j+12) within each 16-code word
+        const int w = e / 8, j = (e % 8) / 2, h = e % 2;
+        const int lo = 16 * w + (h ? 8 : 0) + j;
+        return PairE{lo, lo + 4, 0, 0, 0};
+    }
+    if (bits == 6) {   // (i, i+2) within each 4-code unit (3 bytes)
+        const int m = e / 2, q = e % 2;
+        const int lo = 4 * m + q;
+        return PairE{lo, lo + 2, 4, 0, 6 * lo - 4};
+    }
+    if (bits == 3) {   // four pairs per 8-code unit (3 bytes), two windows
+        const int u = e / 4, q = e % 4;
+        const int lo = 8 * u + q;
+        return PairE{lo, lo + 4, (q & 1) ? 7 : 4, (q & 1) ? 3 : 0, 24 * u + (q < 2 ? -4 : 2)};
+    }
+    // bits == 5: one pair per window, found by an exhaustive search
+    if (nc == 16) {
+        constexpr PairE t[8] = {{0, 3, 5, 4, -5},  {1, 4, 5, 4, 0},   {2, 6, 1, 5, 9},
+                                {5, 8, 5, 4, 20},  {7, 10, 5, 4, 30}, {9, 13, 1, 5, 44},
+                                {11, 14, 5, 4, 50}, {12, 15, 5, 4, 55}};
+        return t[e];
+    }
+    constexpr PairE t[16] = {{0, 3, 5, 4, -5},    {1, 4, 5, 4, 0},     {2, 5, 5, 4, 5},
+                             {6, 9, 5, 4, 25},    {7, 10, 5, 4, 30},   {8, 11, 5, 4, 35},
+                             {12, 15, 5, 4, 55},  {13, 16, 5, 4, 60},  {14, 17, 5, 4, 65},
+                             {18, 21, 5, 4, 85},  {19, 22, 5, 4, 90},  {20, 23, 5, 4, 95},
+                             {24, 27, 5, 4, 115}, {25, 29, 1, 5, 124}, {26, 30, 1, 5, 129},
+                             {28, 31, 5, 4, 135}};
+    return t[e];
+}
+
+template <int I, int N, typename F>
+__device__ __forceinline__ void static_for(F&& f)
+{
+    if constexpr (I < N) {
+        f(std::integral_constant<int, I>{});
+        static_for<I + 1, N>(f);
+    }
+}
+
+// 32 bits of the chunk stream starting at bit S (S may be negative).
+template <int S, int NW>
+__device__ __forceinline__ uint32_t window(const uint32_t (&w)[NW])
+{
+    if constexpr (S < 0) {
+        return w[0] << (-S);
+    } else {
+        constexpr int q = S / 32, r = S % 32;
+        if constexpr (r == 0) {
+            return w[q];
+        } else if constexpr (q + 1 < NW) {
+            return __funnelshift_r(w[q], w[q + 1], r);
+        } else {
+            return w[q] >> r;
+        }
+    }
+}
+
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
+{
+    return (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
+}
+
+// fp16 pair (q_lo - zp, q_hi - zp) of entry E, exact: the LOP3 gives
+// (1024 + 2^plo q_lo, 1024 + 2^phi q_hi); the HFMA2 scales by 2^-p (exact)
+// and adds -1024*2^-p - zp (an exact fp16 integer).
+template <int BITS, int NC, int E, int NW>
+__device__ __forceinline__ uint32_t deq_affine(const uint32_t (&w)[NW], float zp)
+{
+    constexpr PairE p = plan_entry(BITS, NC, E);
+    constexpr uint32_t cm = (1u << BITS) - 1u;
+    constexpr uint32_t mask = (cm << p.plo) | (cm << (16 + p.phi));
+    const uint32_t raw = (window<p.S, NW>(w) & mask) | 0x64006400u;
+    constexpr uint32_t mul = (uint32_t)(0x3C00 - 0x400 * p.plo) | ((uint32_t)(0x3C00 - 0x400 * p.phi) << 16);
+    const uint32_t add = pack_h2(-1024.0f * pow2f(-p.plo) - zp, -1024.0f * pow2f(-p.phi) - zp);
+    return hfma2_u32(raw, mul, add);
+}
+
+// ---------------------------------------------------------------- loads
+__device__ __forceinline__ uint4 ldg_stream128(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ldg_stream64(const void* p)
+{
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg_stream32(const void* p)
+{
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// Load the CB = NC*BITS/8 bytes of one chunk into NW little-endian words.
+template <int BITS, int G>
+struct Chunk {
+    static constexpr int NC = G / 4;
+    static constexpr int CB = NC * BITS / 8;
+    static constexpr int NW = (NC * BITS + 31) / 32;
+    __device__ __forceinline__ static void load(const uint8_t* p, uint32_t (&w)[NW])
+    {
+        if constexpr (CB % 16 == 0) {
+#pragma unroll
+            for (int i = 0; i < CB / 16; i++) {
+                const uint4 v = ldg_stream128(p + 16 * i);
+                w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+            }
+        } else if constexpr (CB % 8 == 0) {
+#pragma unroll
+            for (int i = 0; i < CB / 8; i++) {
+                const uint2 v = ldg_stream64(p + 8 * i);
+                w[2 * i] = v.x; w[2 * i + 1] = v.y;
+            }
+        } else if constexpr (CB % 4 == 0) {
+#pragma unroll
+            for (int i = 0; i < CB / 4; i++) w[i] = ldg_stream32(p + 4 * i);
+        } else {
+            // 2-byte aligned chunk (group 64, odd width): aligned words, then
+            // shift by 16 bits when the chunk starts mid-word.  Every word read
+            // holds at least one byte of this group.
+            constexpr int NWL = (CB + 2 + 3) / 4;
+            const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+            const uint8_t* base = reinterpret_cast<const uint8_t*>(a & ~uintptr_t(3));
+            uint32_t raw[NWL + 1];
+#pragma unroll
+            for (int i = 0; i < NWL; i++) raw[i] = ldg_stream32(base + 4 * i);
+            raw[NWL] = 0u;
+            const int sh = (int)(a & 3u) * 8;   // 0 or 16
+#pragma unroll
+            for (int i = 0; i < NW; i++) w[i] = __funnelshift_r(raw[i], raw[i + 1], sh);
+        }
+    }
+};
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint16_t x_f16(__nv_bfloat16 v)
+{
+    return __half_as_ushort(__float2half_rn(__bfloat162float(v)));
+}
+
+__device__ __forceinline__ float h2f(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+
+// One product on one weight matrix.  Token m reads x row
+// (rowmap ? rowmap[m] / xdiv : m) and writes y row (rowmap ? rowmap[m] : m).
+struct Problem {
+    const __nv_bfloat16* x;
+    int ldx, M, N, K;
+    const int* rowmap;
+    int xdiv;
+    const uint8_t* packed;
+    const uint16_t* scale;
+    const uint8_t* zp;
+    const uint2* cb;
+    const int* row_ptr;
+    const int* col;
+    const uint16_t* val;
+    int nnz;
+    void* y;
+    int ldy;
+    int y_bf16;
+};
+
+__device__ __forceinline__ int x_row(const Problem& p, int m) { return p.rowmap ? p.rowmap[m] / p.xdiv : m; }
+__device__ __forceinline__ int y_row(const Problem& p, int m) { return p.rowmap ? p.rowmap[m] : m; }
+
+template <int BITS, int G, int NT>
+struct Cfg {
+    static constexpr int NC = G / 4;
+    static constexpr int NW = Chunk<BITS, G>::NW;
+    static constexpr int STEPS = G / 16;
+    static constexpr int NTOK = 8 * NT;
+    static constexpr int D = NT <= 2 ? 4 : 2;                    // prefetch depth (groups)
+    static constexpr int XG_RAW = 2048 / (G * NT);               // x-block groups (32 KB)
+    static constexpr int XG = XG_RAW < D ? D : XG_RAW;
+    static constexpr int XS_BYTES = XG * STEPS * NT * 32 * 8;
+    static constexpr int RED_BYTES = kRowsPerCta * NTOK * 4;
+    static constexpr int SMEM = XS_BYTES > RED_BYTES ? XS_BYTES : RED_BYTES;
+};
+
+// Stage x[:, kbase : kbase + ngr*G] as fp16 in MMA B-fragment order: item
+// (group, step, n8 tile, lane) holds the 4 values whose k positions match the
+// A-fragment codes of thread lane%4 in that step.
+template <int BITS, int G, int NT>
+__device__ void stage_x(const Problem& a, int kbase, int ngr, uint2* xs)
+{
+    using C = Cfg<BITS, G, NT>;
+    const int items = ngr * NT * 32;
+    for (int it = threadIdx.x; it < items; it += blockDim.x) {
+        const int gi = it / (NT * 32), rem = it % (NT * 32);
+        const int nt = rem / 32, ln = rem % 32;
+        const int m = nt * 8 + (ln >> 2), t = ln & 3;
+        const bool live = m < a.M;
+        const __nv_bfloat16* xr = a.x + (size_t)(live ? x_row(a, m) : 0) * a.ldx + kbase + gi * G + t * C::NC;
+        static_for<0, C::STEPS>([&](auto sc) {
+            constexpr int s = decltype(sc)::value;
+            constexpr PairE e0 = plan_entry(BITS, C::NC, 2 * s);
+            constexpr PairE e1 = plan_entry(BITS, C::NC, 2 * s + 1);
+            uint2 v = make_uint2(0u, 0u);
+            if (live) {
+                v.x = (uint32_t)x_f16(xr[e0.lo]) | ((uint32_t)x_f16(xr[e0.hi]) << 16);
+                v.y = (uint32_t)x_f16(xr[e1.lo]) | ((uint32_t)x_f16(xr[e1.hi]) << 16);
+            }
+            xs[((gi * C::STEPS + s) * NT + nt) * 32 + ln] = v;
+        });
+    }
+}
+
+template <int BITS, int G, int NT>
+__device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsplit)
+{
+    using C = Cfg<BITS, G, NT>;
+    constexpr int NW = C::NW, D = C::D;
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint2* xs = reinterpret_cast<uint2*>(smem);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = lane & 3, gq = lane >> 2;
+    const int row_base = blockIdx.x * kRowsPerCta + warp * 16 + gq;
+    const int r0 = min(row_base, a.N - 1), r1 = min(row_base + 8, a.N - 1);
+    const int ng = a.K / G;
+    const int g_begin = blockIdx.y * gpsplit;
+    const int ngrp = max(0, min(ng, g_begin + gpsplit) - g_begin);
+
+    constexpr int GB = G * BITS / 8;   // bytes per group
+    const size_t rowbytes = (size_t)a.K * BITS / 8;
+    const uint8_t* src0 = a.packed + (size_t)r0 * rowbytes + (size_t)g_begin * GB + t * Chunk<BITS, G>::CB;
+    const uint8_t* src1 = a.packed + (size_t)r1 * rowbytes + (size_t)g_begin * GB + t * Chunk<BITS, G>::CB;
+    const size_t pidx0 = (size_t)r0 * ng + g_begin, pidx1 = (size_t)r1 * ng + g_begin;
+
+    float yacc[NT][4];
+#pragma unroll
+    for (int i = 0; i < NT; i++) yacc[i][0] = yacc[i][1] = yacc[i][2] = yacc[i][3] = 0.0f;
+
+    uint32_t wr[D][2][NW];
+    uint32_t prm[D][2][2];   // affine: scale bits, zp; codebook: two words of 4 fp16
+
+    auto issue = [&](int slot, int j) {
+        Chunk<BITS, G>::load(src0 + (size_t)j * GB, wr[slot][0]);
+        Chunk<BITS, G>::load(src1 + (size_t)j * GB, wr[slot][1]);
+        if constexpr (BITS == 2) {
+            const uint2 c0 = __ldg(a.cb + pidx0 + j), c1 = __ldg(a.cb + pidx1 + j);
+            prm[slot][0][0] = c0.x; prm[slot][0][1] = c0.y;
+            prm[slot][1][0] = c1.x; prm[slot][1][1] = c1.y;
+        } else {
+            prm[slot][0][0] = __ldg(a.scale + pidx0 + j);
+            prm[slot][1][0] = __ldg(a.scale + pidx1 + j);
+            prm[slot][0][1] = __ldg(a.zp + pidx0 + j);
+            prm[slot][1][1] = __ldg(a.zp + pidx1 + j);
+        }
+    };
+
+#pragma unroll
+    for (int d = 0; d < D; d++)
+        if (d < ngrp) issue(d, d);
+
+    for (int jj = 0; jj < ngrp; jj += D) {
+#pragma unroll
+        for (int d = 0; d < D; d++) {
+            const int j = jj + d;
+            if (j >= ngrp) break;
+            if (j % C::XG == 0) {
+                __syncthreads();
+                stage_x<BITS, G, NT>(a, (g_begin + j) * G, min(C::XG, ngrp - j), xs);
+                __syncthreads();
+            }
+            const int xg = j % C::XG;
+            const uint2* xb = xs + (size_t)xg * C::STEPS * NT * 32 + lane;
+
+            if constexpr (BITS == 2) {
+                // per-row lookup tables: low bytes and high bytes of the 4 entries
+                const uint32_t L0 = __byte_perm(prm[d][0][0], prm[d][0][1], 0x6420);
+                const uint32_t H0 = __byte_perm(prm[d][0][0], prm[d][0][1], 0x7531);
+                const uint32_t L1 = __byte_perm(prm[d][1][0], prm[d][1][1], 0x6420);
+                const uint32_t H1 = __byte_perm(prm[d][1][0], prm[d][1][1], 0x7531);
+                static_for<0, NW>([&](auto wc) {
+                    constexpr int wi = decltype(wc)::value;
+                    static_for<0, 4>([&](auto jc) {
+                        constexpr int jf = decltype(jc)::value;
+                        const uint32_t f0 = (wr[d][0][wi] >> (2 * jf)) & 0x03030303u;
+                        const uint32_t f1 = (wr[d][1][wi] >> (2 * jf)) & 0x03030303u;
+                        const uint32_t s0l = f0 * 0x11u + 0x4040u, s0h = __umulhi(f0, 0x00110000u) + 0x4040u;
+                        const uint32_t s1l = f1 * 0x11u + 0x4040u, s1h = __umulhi(f1, 0x00110000u) + 0x4040u;
+                        const uint32_t a0 = __byte_perm(L0, H0, s0l), a2 = __byte_perm(L0, H0, s0h);
+                        const uint32_t a1 = __byte_perm(L1, H1, s1l), a3 = __byte_perm(L1, H1, s1h);
+                        constexpr int s = 4 * wi + jf;   // entries 2s (lo) and 2s+1 (hi)
+#pragma unroll
+                        for (int nt = 0; nt < NT; nt++) {
+                            const uint2 b = xb[(s * NT + nt) * 32];
+                            mma16816(yacc[nt], a0, a1, a2, a3, b.x, b.y);
+                        }
+                    });
+                });
+            } else {
+                float acc[NT][4];
+#pragma unroll
+                for (int i = 0; i < NT; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+                const float z0 = (float)prm[d][0][1], z1 = (float)prm[d][1][1];
+                static_for<0, C::STEPS>([&](auto sc) {
+                    constexpr int s = decltype(sc)::value;
+                    const uint32_t a0 = deq_affine<BITS, C::NC, 2 * s>(wr[d][0], z0);
+                    const uint32_t a1 = deq_affine<BITS, C::NC, 2 * s>(wr[d][1], z1);
+                    const uint32_t a2 = deq_affine<BITS, C::NC, 2 * s + 1>(wr[d][0], z0);
+                    const uint32_t a3 = deq_affine<BITS, C::NC, 2 * s + 1>(wr[d][1], z1);
+#pragma unroll
+                    for (int nt = 0; nt < NT; nt++) {
+                        const uint2 b = xb[(s * NT + nt) * 32];
+                        mma16816(acc[nt], a0, a1, a2, a3, b.x, b.y);
+                    }
+                });
+                const float s0 = h2f((uint16_t)prm[d][0][0]), s1 = h2f((uint16_t)prm[d][1][0]);
+#pragma unroll
+                for (int nt = 0; nt < NT; nt++) {
+                    yacc[nt][0] = fmaf(s0, acc[nt][0], yacc[nt][0]);
+                    yacc[nt][1] = fmaf(s0, acc[nt][1], yacc[nt][1]);
+                    yacc[nt][2] = fmaf(s1, acc[nt][2], yacc[nt][2]);
+                    yacc[nt][3] = fmaf(s1, acc[nt][3], yacc[nt][3]);
+                }
+            }
+            if (j + D < ngrp) issue(d, j + D);
+        }
+    }
+
+    // ------------------------------------------------ split-K reduction + epilogue
+    __syncthreads();
+    float* yp = reinterpret_cast<float*>(smem);   // [64 rows][NTOK]
+    const int rl0 = warp * 16 + gq;
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++) {
+        const int c = nt * 8 + 2 * t;
+        yp[rl0 * C::NTOK + c] = yacc[nt][0];
+        yp[rl0 * C::NTOK + c + 1] = yacc[nt][1];
+        yp[(rl0 + 8) * C::NTOK + c] = yacc[nt][2];
+        yp[(rl0 + 8) * C::NTOK + c + 1] = yacc[nt][3];
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    const int S = splits;
+    if (S > 1) cluster.sync();
+    else __syncthreads();
+    const int rank = S > 1 ? (int)cluster.block_rank() : 0;
+    const int rows_per = kRowsPerCta / S;
+    const int Mv = min(a.M, C::NTOK);
+    for (int it = threadIdx.x; it < rows_per * Mv; it += blockDim.x) {
+        const int m = it / rows_per, rl = rank * rows_per + it % rows_per;
+        const int n = blockIdx.x * kRowsPerCta + rl;
+        float v = 0.0f;
+        for (int r = 0; r < S; r++) {
+            const float* src = S > 1 ? cluster.map_shared_rank(yp, r) : yp;
+            v += src[rl * C::NTOK + m];
+        }
+        if (n < a.N) {
+            if (a.nnz > 0) {
+                const int pe = a.row_ptr[n + 1];
+                const __nv_bfloat16* xm = a.x + (size_t)x_row(a, m) * a.ldx;
+                for (int p = a.row_ptr[n]; p < pe; p++)
+                    v += __bfloat162float(xm[a.col[p]]) * h2f(a.val[p]);
+            }
+            const size_t yo = (size_t)y_row(a, m) * a.ldy + n;
+            if (a.y_bf16)
+                reinterpret_cast<__nv_bfloat16*>(a.y)[yo] = __float2bfloat16_rn(v);
+            else
+                reinterpret_cast<float*>(a.y)[yo] = v;
+        }
+    }
+    if (S > 1) cluster.sync();   // keep this CTA's partials alive until every rank has read them
+}
+
+
+template <int BITS, int G, int NT>
+__global__ void __launch_bounds__(kWarps * 32) k_gemv(const Problem p, int splits, int gpsplit)
+{
+    gemv_body<BITS, G, NT>(p, splits, gpsplit);
+}
+
+// Grouped product over routed experts.  Pairs (token, slot) are sorted by
+// expert on the device (offsets[e] .. offsets[e+1] index `perm`, which holds
+// pair ids t*k + j).  The routing kernel also lists the work items
+// (expert, chunk of `chunk` pairs); blockIdx.z picks one item.
+struct MoeTable {
+    const __nv_bfloat16* x;
+    int ldx, N, K, topk;
+    int chunk;
+    const int* offsets;
+    const int* perm;
+    const int2* items;
+    const int* n_items;
+    void* y;
+    int y_bf16;
+    const uint8_t* packed[kMoeMaxExperts];
+    const uint16_t* scale[kMoeMaxExperts];
+    const uint8_t* zp[kMoeMaxExperts];
+    const uint2* cb[kMoeMaxExperts];
+    const int* row_ptr[kMoeMaxExperts];
+    const int* col[kMoeMaxExperts];
+    const uint16_t* val[kMoeMaxExperts];
+    int nnz[kMoeMaxExperts];
+};
+
+template <int BITS, int G, int NT>
+__global__ void __launch_bounds__(kWarps * 32) k_gemv_moe(const __grid_constant__ MoeTable t, int splits,
+                                                          int gpsplit)
+{
+    if ((int)blockIdx.z >= *t.n_items) return;   // uniform across the cluster (same blockIdx.z)
+    const int2 item = t.items[blockIdx.z];
+    const int e = item.x;
+    const int end = t.offsets[e + 1];
+    const int m0 = t.offsets[e] + item.y * t.chunk;
+    Problem p;
+    p.x = t.x; p.ldx = t.ldx; p.M = min(t.chunk, end - m0); p.N = t.N; p.K = t.K;
+    p.rowmap = t.perm + m0; p.xdiv = t.topk;
+    p.packed = t.packed[e]; p.scale = t.scale[e]; p.zp = t.zp[e]; p.cb = t.cb[e];
+    p.row_ptr = t.row_ptr[e]; p.col = t.col[e]; p.val = t.val[e]; p.nnz = t.nnz[e];
+    p.y = t.y; p.ldy = t.N; p.y_bf16 = t.y_bf16;
+    gemv_body<BITS, G, NT>(p, splits, gpsplit);
+}
+
+// K split: the cluster size S in {1, 2, 4, 8} that best fills the SMs with
+// whole waves of CTAs; near-ties go to at least two CTAs per SM, then to the
+// smaller S.
+inline int choose_splits(long long ctas_per_split, int ng)
+{
+    const int sms = num_sms();
+    int best = 1;
+    double best_eff = -1.0;
+    bool best_two = false;
+    for (int S = 1; S <= 8; S *= 2) {
+        if (S > 1 && ng / S < 2) break;
+        const double u = (double)ctas_per_split * S / sms;
+        const double eff = u < 1.0 ? u : u / std::ceil(u);
+        const bool two = u >= 2.0;
+        if (eff > best_eff + 0.03 || (eff > best_eff - 0.03 && two && !best_two)) {
+            best = S;
+            best_eff = eff;
+            best_two = two;
+        }
+    }
+    return best;
+}
+
+inline int nt_for(int M) { return M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8; }
+
+template <int BITS, int G, int NT, typename K, typename A>
+qg_status launch_cluster(K kernel, const A& args, dim3 grid, int S, int gpsplit, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)Cfg<BITS, G, NT>::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)S;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args, S, gpsplit);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+    return QG_OK;
+}
+
+template <int BITS, int G, int NT>
+qg_status dense_nt(const Problem& p, cudaStream_t s)
+{
+    const int ng = p.K / G;
+    const int tiles = (int)ceil_div(p.N, kRowsPerCta);
+    const int S = choose_splits(tiles, ng);
+    return launch_cluster<BITS, G, NT>(k_gemv<BITS, G, NT>, p, dim3((unsigned)tiles, (unsigned)S, 1), S,
+                                       (int)ceil_div(ng, S), s);
+}
+
+template <int BITS, int G, int NT>
+qg_status grouped_nt(const MoeTable& t, int max_items, int expect_items, cudaStream_t s)
+{
+    const int ng = t.K / G;
+    const int tiles = (int)ceil_div(t.N, kRowsPerCta);
+    const int S = choose_splits((long long)tiles * std::max(1, expect_items), ng);
+    return launch_cluster<BITS, G, NT>(k_gemv_moe<BITS, G, NT>, t,
+                                       dim3((unsigned)tiles, (unsigned)S, (unsigned)max_items), S,
+                                       (int)ceil_div(ng, S), s);
+}
+
+template <int BITS>
+qg_status launch_dense(const Problem& p, int G, cudaStream_t s)
+{
+    const int nt = nt_for(p.M);
+    if (G == 64) {
+        switch (nt) {
+            case 1: return dense_nt<BITS, 64, 1>(p, s);
+            case 2: return dense_nt<BITS, 64, 2>(p, s);
+            case 4: return dense_nt<BITS, 64, 4>(p, s);
+            default: return dense_nt<BITS, 64, 8>(p, s);
+        }
+    }
+    switch (nt) {
+        case 1: return dense_nt<BITS, 128, 1>(p, s);
+        case 2: return dense_nt<BITS, 128, 2>(p, s);
+        case 4: return dense_nt<BITS, 128, 4>(p, s);
+        default: return dense_nt<BITS, 128, 8>(p, s);
+    }
+}
+
+// t.chunk must be 8 * nt.  max_items bounds the device-built item count;
+// expect_items is the typical count (for choosing the K split).
+template <int BITS>
+qg_status launch_grouped(const MoeTable& t, int max_items, int expect_items, int G, int nt, cudaStream_t s)
+{
+    if (G == 64) {
+        switch (nt) {
+            case 1: return grouped_nt<BITS, 64, 1>(t, max_items, expect_items, s);
+            case 2: return grouped_nt<BITS, 64, 2>(t, max_items, expect_items, s);
+            case 4: return grouped_nt<BITS, 64, 4>(t, max_items, expect_items, s);
+            default: return grouped_nt<BITS, 64, 8>(t, max_items, expect_items, s);
+        }
+    }
+    switch (nt) {
+        case 1: return grouped_nt<BITS, 128, 1>(t, max_items, expect_items, s);
+        case 2: return grouped_nt<BITS, 128, 2>(t, max_items, expect_items, s);
+        case 4: return grouped_nt<BITS, 128, 4>(t, max_items, expect_items, s);
+        default: return grouped_nt<BITS, 128, 8>(t, max_items, expect_items, s);
+    }
+}
+
+}  // namespace gemv
+}  // namespace qg

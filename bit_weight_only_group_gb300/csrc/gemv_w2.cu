@@ -1,0 +1,9 @@
+// Instantiation of the decode / grouped kernels for 2-bit weights.
+#include "gemv_impl.cuh"
+
+namespace qg {
+namespace gemv {
+template qg_status launch_dense<2>(const Problem&, int, cudaStream_t);
+template qg_status launch_grouped<2>(const MoeTable&, int, int, int, int, cudaStream_t);
+}  // namespace gemv
+}  // namespace qg

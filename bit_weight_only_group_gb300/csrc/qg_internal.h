@@ -1,0 +1,45 @@
+// Internal declarations shared by the translation units of libqgemm.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "qgemm.h"
+
+namespace qg {
+
+// Thread-local message behind qgemm_last_error().
+void set_error(const char* fmt, ...);
+qg_status fail(qg_status st, const char* fmt, ...);
+qg_status cuda_fail(cudaError_t e, const char* what);
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- quantizer
+size_t quantize_workspace_bytes(int N, int K);
+qg_status launch_quantize(const uint16_t* W, float frac, const qg_qweight& w, void* ws,
+                          cudaStream_t s);
+
+// ---------------------------------------------------------------- decode GEMV
+// Largest M the register-dequant kernel handles in one pass.
+constexpr int kGemvMaxM = 64;
+qg_status launch_gemv(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,
+                      qg_ydtype yt, cudaStream_t s);
+
+// ---------------------------------------------------------------- tensor-core GEMM
+size_t gemm_workspace_bytes(int M, const qg_qweight& w);
+qg_status launch_gemm(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,
+                      qg_ydtype yt, void* ws, size_t ws_bytes, cudaStream_t s);
+
+// ---------------------------------------------------------------- grouped MoE
+constexpr int kMoeMaxExperts = 256;
+size_t moe_workspace_bytes(int T, int k, int E, const qg_qweight* experts);
+qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const qg_qweight* experts,
+                     int E, void* y, qg_ydtype yt, void* ws, size_t ws_bytes, cudaStream_t s);
+
+}  // namespace qg

@@ -1,0 +1,191 @@
+/*
+ * qgemm.h -- C ABI of the fused-dequantization linear layer for weight-only,
+ * group-wise, asymmetric low-bit weights, built for NVIDIA GB300 (sm_103a).
+ *
+ *     y = x . dequant(W)^T  (+ FP16 outliers added back)
+ *
+ * The method (from the pages this library follows):
+ *  - affine asymmetric quantizer: scale = (max - min) / (qmax - qmin),
+ *    zero_point = qmin - round(min / scale), q = round(w / scale) +
+ *    zero_point, w_hat = (q - zero_point) * scale  (m.mzlw.cn 206779 page,
+ *    section 1.1 "quantization is a lossy mapping");
+ *  - statistics per group of consecutive weights along K (64 or 128), after
+ *    excluding the largest-magnitude 0.1 % of weights, which are kept in FP16
+ *    and added back after the product  (bjdmk.com.cn 5414039 page, section 2,
+ *    "group-wise outlier-aware quantization", steps 1-3);
+ *  - widths 2, 3, 4, 5, 6 bits; 2-bit groups use a 4-entry non-uniform
+ *    codebook found by k-means  (pwwt.cn page, section 2.1 table and 4.1);
+ *  - codes packed LSB-first in a little-endian bit stream: 3-bit 8 values
+ *    in 3 bytes, 5-bit 8 values in 5 bytes, 6-bit 4 values in 3 bytes,
+ *    2-bit 4 values per byte, 4-bit two per byte with the even index in the
+ *    low half  (pwwt.cn page, sections 3.1-3.2 and the 2.1 table);
+ *  - unpacking happens on the computing device, fused into the product,
+ *    with fp32 accumulation  (pwwt.cn page, sections 1.2 and 4.1-4.2;
+ *    bjdmk.com.cn 5414039 page, section 3 "kernel fusion").
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer in a qg_qweight, every x / y / topk_ids / W argument and
+ *    the workspace are DEVICE memory owned by the caller.  The library never
+ *    allocates, frees or retains them past the call.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is
+ *    enqueued on it; the calls never synchronize the stream or the device.
+ *  - Arguments are validated on the host before anything is launched; a
+ *    rejected call launches nothing and returns a negative qg_status.  No
+ *    call throws.  qgemm_last_error() returns a human-readable message for
+ *    the calling thread's last failure.
+ *  - Inputs must not alias outputs.
+ */
+#ifndef QGEMM_H_
+#define QGEMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QG_API __attribute__((visibility("default")))
+#else
+#define QG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QG_OK = 0,
+    QG_ERR_INVALID_ARG = -1,   /* a null pointer, a bad size, an out-of-range value */
+    QG_ERR_UNSUPPORTED = -2,   /* valid in principle, not built (e.g. bits = 7) */
+    QG_ERR_ALIGNMENT = -3,     /* a pointer or leading dimension is misaligned */
+    QG_ERR_WORKSPACE = -4,     /* workspace missing or smaller than the size query */
+    QG_ERR_CUDA = -5,          /* a CUDA runtime call or launch failed */
+    QG_ERR_TIMEOUT = -6,       /* reserved: a bounded device-side wait gave up */
+    QG_ERR_DEVICE_STATUS = -7  /* reserved: a device-side check reported an error */
+} qg_status;
+
+typedef enum { QG_Y_F32 = 0, QG_Y_BF16 = 1 } qg_ydtype;
+
+/*
+ * A quantized weight matrix W [N, K] in the planar layout (codes in one
+ * array, per-group parameters in others; pwwt.cn page, section 3.3).
+ *
+ *  N, K        output and input features.  K % group == 0.
+ *  bits        2, 3, 4, 5 or 6.
+ *  group       64 or 128 consecutive weights along K share a scale/zp
+ *              (or, at 2 bits, a codebook).  ng = K / group.
+ *  packed      uint8 [N, K*bits/8], row-major; row n holds the K codes of
+ *              row n as one LSB-first stream.  16-byte aligned.
+ *  scale       fp16 [N, ng]  (bits != 2; NULL at 2 bits).  2-byte aligned.
+ *  zp          uint8 [N, ng] (bits != 2; NULL at 2 bits).
+ *  codebook    fp16 [N, ng, 4], ascending per group (bits == 2; NULL
+ *              otherwise).  8-byte aligned.
+ *  nnz         number of FP16 outliers = floor(outlier_frac * N * K).
+ *  out_row_ptr int32 [N+1] CSR row pointer (may be NULL when nnz == 0).
+ *  out_col     int32 [nnz] column of each outlier, ascending within a row.
+ *  out_val     fp16 [nnz]  the value added back at (row, col): the weight
+ *              itself (bits 3..6) or the residual w - codebook entry (2 bits).
+ */
+typedef struct {
+    int32_t N, K, bits, group;
+    uint8_t* packed;
+    uint16_t* scale;
+    uint8_t* zp;
+    uint16_t* codebook;
+    int32_t nnz;
+    int32_t* out_row_ptr;
+    int32_t* out_col;
+    uint16_t* out_val;
+} qg_qweight;
+
+/*
+ * Bytes of every buffer of a quantized [N, K] matrix.  Host-only, no GPU.
+ * nnz = floor(outlier_frac * N * K) evaluated in double; the outlier arrays
+ * take (N+1)*4 + nnz*4 + nnz*2 bytes.  Any output pointer may be NULL.
+ * Effective bits per weight = bits + 24/group (fp16 scale + u8 zp) or
+ * 2 + 64/group (2-bit codebook of 4 fp16 entries); pwwt.cn page, section 2.3
+ * gives the same accounting for the scale overhead.
+ * Errors: QG_ERR_INVALID_ARG for N, K <= 0, K % group, outlier_frac outside
+ * [0, 1); QG_ERR_UNSUPPORTED for bits outside 2..6 or group not 64/128.
+ */
+QG_API qg_status qpack_query_sizes(int32_t N, int32_t K, int32_t bits, int32_t group, float outlier_frac,
+                            size_t* packed_bytes, size_t* scale_bytes, size_t* zp_bytes,
+                            size_t* codebook_bytes, int32_t* nnz);
+
+/* Workspace bytes qpack_quantize needs for an [N, K] matrix.  Host-only. */
+QG_API qg_status qpack_workspace_size(int32_t N, int32_t K, size_t* bytes);
+
+/*
+ * Quantize and pack W [N, K] (fp16, row-major, DEVICE, 16-byte aligned, all
+ * values finite) into the buffers of `out`, whose N, K, bits, group and nnz
+ * the caller fills (nnz from qpack_query_sizes) and whose pointers the
+ * caller allocates.  Steps (bjdmk.com.cn 5414039 page, section 2; m.mzlw.cn
+ * 206779 page, section 1.1; pwwt.cn page, sections 3-4):
+ *   1. outliers: the nnz largest |w| of the whole matrix (ties: lower
+ *      linear index n*K + k), stored as CSR, columns ascending;
+ *   2. per (row, group): min/max over the non-outliers with 0 included;
+ *      bits 3..6: scale = fp16 rounded up of (max-min)/(2^bits - 1) (1.0 if
+ *      max == min), zp = clamp(-rint(min/scale), 0, 2^bits-1),
+ *      q = clamp(rint(w/scale) + zp, 0, 2^bits - 1), q = zp at outliers;
+ *      bits 2: 16 Lloyd iterations from 4 evenly spaced levels, entries
+ *      rounded to fp16 and sorted, q = nearest entry (ties: lower index),
+ *      the entry nearest 0 at an outlier, whose stored value becomes the
+ *      residual fp16(w - entry);
+ *   3. codes packed LSB-first along K.
+ * All rounding is IEEE round-to-nearest-even except the scale (toward +inf);
+ * the results are bit-exact and deterministic.
+ * `ws` must hold qpack_workspace_size bytes (256-byte aligned).  Errors:
+ * QG_ERR_INVALID_ARG (nulls, sizes, nnz mismatch), QG_ERR_ALIGNMENT,
+ * QG_ERR_WORKSPACE, QG_ERR_CUDA.  Non-finite W gives unspecified output.
+ */
+QG_API qg_status qpack_quantize(const uint16_t* W, float outlier_frac, const qg_qweight* out, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/* Workspace bytes qgemm_forward needs for M rows of x against w.  Host-only. */
+QG_API qg_status qgemm_workspace_size(int32_t M, const qg_qweight* w, size_t* bytes);
+
+/*
+ * y[m, n] = sum_k x[m, k] * (w_hat[n, k] + S[n, k])   for m < M, n < N,
+ * with w_hat the dequantized weight and S the FP16 outliers (bjdmk.com.cn
+ * 5414039 page, sections 2-3).  Dequantization happens in registers / on-chip
+ * memory inside the product; accumulation is fp32.
+ *   x   bf16 [M, K] row-major with row stride ldx >= K elements (DEVICE).
+ *   y   [M, N] row-major with row stride ldy >= N elements, fp32 or bf16
+ *       per `yt` (DEVICE).
+ * M = 0 is a no-op.  M <= 64 runs the decode kernel (register dequant, split
+ * K across a thread-block cluster); larger M runs the tensor-core kernel
+ * (tcgen05 with TMEM accumulators), which converts x to fp16 in the workspace.
+ * `ws` may be NULL when qgemm_workspace_size reports 0.
+ * Errors: QG_ERR_INVALID_ARG, QG_ERR_ALIGNMENT, QG_ERR_WORKSPACE, QG_ERR_CUDA.
+ */
+QG_API qg_status qgemm_forward(const uint16_t* x, int32_t M, int32_t ldx, const qg_qweight* w, void* y,
+                        int32_t ldy, qg_ydtype yt, void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes qgemm_moe_grouped needs.  Host-only. */
+QG_API qg_status qgemm_moe_workspace_size(int32_t T, int32_t k, int32_t E, const qg_qweight* experts,
+                                   size_t* bytes);
+
+/*
+ * Grouped product over top-k routed experts (bjdmk.com.cn 5648983 page,
+ * sections 1-2: each token activates its top-k of the experts):
+ *   y[t, j, :] = x[t, :] . (w_hat + S)_{e}^T   with e = topk_ids[t, j],
+ * for t < T, j < k.  No gate weights are applied.
+ *   x         bf16 [T, K] row-major, contiguous (DEVICE).
+ *   topk_ids  int32 [T, k] expert ids in [0, E) (DEVICE).
+ *   experts   HOST array of E descriptors; all share N, K, bits and group.
+ *   y         [T, k, N] contiguous, fp32 or bf16 per `yt` (DEVICE).
+ * Routing (a counting sort of the T*k pairs by expert) runs on the device.
+ * Ids outside [0, E) are skipped (their y rows are left untouched).
+ * E <= 256.  Errors: QG_ERR_INVALID_ARG, QG_ERR_ALIGNMENT, QG_ERR_WORKSPACE,
+ * QG_ERR_CUDA.
+ */
+QG_API qg_status qgemm_moe_grouped(const uint16_t* x, int32_t T, const int32_t* topk_ids, int32_t k,
+                            const qg_qweight* experts, int32_t E, void* y, qg_ydtype yt, void* ws,
+                            size_t ws_bytes, void* stream);
+
+/* Message describing the calling thread's most recent failure ("" if none). */
+QG_API const char* qgemm_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMM_H_ */

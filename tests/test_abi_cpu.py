@@ -1,0 +1,142 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol
+the header declares, answers the host-only size queries like the oracle, and
+rejects bad arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def qg():
+    from bit_weight_only_group_gb300 import build
+    build.build()
+    import bit_weight_only_group_gb300 as qg
+    return qg
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "qgemm.h")).read()
+    return re.findall(r"QG_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+
+
+def test_every_declared_symbol_is_exported(qg):
+    names = _declared()
+    assert set(names) == set(qg.ABI_FUNCTIONS)
+    L = qg.lib()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+@pytest.mark.parametrize("N,K,bits,group,frac", [
+    (4096, 4096, 4, 128, 0.0), (4096, 4096, 2, 128, 0.001), (11008, 4096, 3, 64, 0.001),
+    (4096, 11008, 5, 128, 0.001), (1024, 8192, 6, 64, 0.002), (7, 64, 2, 64, 0.5)])
+def test_sizes_match_oracle(qg, N, K, bits, group, frac):
+    got = qg.qpack_query_sizes(N, K, bits, group, frac)
+    ref = oracle.sizes(N, K, bits, group, frac)
+    for k in ("packed", "scale", "zp", "codebook", "nnz"):
+        assert got[k] == ref[k], k
+
+
+def test_sizes_reject_bad_shapes(qg):
+    with pytest.raises(qg.QgError) as e:
+        qg.qpack_query_sizes(64, 100, 4, 64)
+    assert e.value.status == -1
+    with pytest.raises(qg.QgError) as e:
+        qg.qpack_query_sizes(64, 128, 7, 64)
+    assert e.value.status == -2
+    with pytest.raises(qg.QgError) as e:
+        qg.qpack_query_sizes(64, 128, 4, 32)
+    assert e.value.status == -2
+    with pytest.raises(qg.QgError) as e:
+        qg.qpack_query_sizes(64, 128, 4, 64, 1.0)
+    assert e.value.status == -1
+    with pytest.raises(qg.QgError):
+        qg.qpack_query_sizes(0, 128, 4, 64)
+
+
+def _fake_desc(qg, N=64, K=128, bits=4, group=64, nnz=0, base=0x100000):
+    d = qg.QgQWeight(N, K, bits, group, base, base + 0x10000, base + 0x20000, 0, nnz, None, None, None)
+    if bits == 2:
+        d.scale = None
+        d.zp = None
+        d.codebook = base + 0x30000
+    return d
+
+
+def test_host_validation_without_gpu(qg):
+    L = qg.lib()
+    d = _fake_desc(qg)
+    y = ctypes.c_void_p(0x200000)
+    x = ctypes.c_void_p(0x300000)
+    # null x
+    assert L.qgemm_forward(None, 1, 128, ctypes.byref(d), y, 64, 0, None, 0, None) == -1
+    assert "null" in qg.last_error()
+    # ldx < K, ldy < N
+    assert L.qgemm_forward(x, 1, 64, ctypes.byref(d), y, 64, 0, None, 0, None) == -1
+    assert L.qgemm_forward(x, 1, 128, ctypes.byref(d), y, 32, 0, None, 0, None) == -1
+    # M = 0 is a no-op
+    assert L.qgemm_forward(None, 0, 128, ctypes.byref(d), None, 64, 0, None, 0, None) == 0
+    # misaligned packed
+    bad = _fake_desc(qg, base=0x100004)
+    assert L.qgemm_forward(x, 1, 128, ctypes.byref(bad), y, 64, 0, None, 0, None) == -3
+    # unsupported width and group
+    for dd in (_fake_desc(qg, bits=7), _fake_desc(qg, group=32)):
+        assert L.qgemm_forward(x, 1, 128, ctypes.byref(dd), y, 64, 0, None, 0, None) == -2
+    # outliers declared but arrays missing
+    assert L.qgemm_forward(x, 1, 128, ctypes.byref(_fake_desc(qg, nnz=3)), y, 64, 0, None, 0, None) == -1
+    # 2-bit needs a codebook
+    d2 = _fake_desc(qg, bits=2)
+    d2.codebook = None
+    assert L.qgemm_forward(x, 1, 128, ctypes.byref(d2), y, 64, 0, None, 0, None) == -1
+
+
+def test_quantize_validation_without_gpu(qg):
+    L = qg.lib()
+    W = ctypes.c_void_p(0x400000)
+    d = _fake_desc(qg, N=64, K=1024, nnz=oracle.nnz(64, 1024, 0.001))
+    d.out_row_ptr, d.out_col, d.out_val = 0x500000, 0x510000, 0x520000
+    ws_need = qg.qpack_workspace_size(64, 1024)
+    ws = ctypes.c_void_p(0x600000)
+    # nnz must equal floor(frac*N*K)
+    assert L.qpack_quantize(W, 0.002, ctypes.byref(d), ws, ws_need, None) == -1
+    # workspace too small / missing
+    assert L.qpack_quantize(W, 0.001, ctypes.byref(d), ws, ws_need - 1, None) == -4
+    assert L.qpack_quantize(W, 0.001, ctypes.byref(d), None, ws_need, None) == -4
+    # misaligned W and workspace
+    assert L.qpack_quantize(ctypes.c_void_p(0x400002), 0.001, ctypes.byref(d), ws, ws_need, None) == -3
+    assert L.qpack_quantize(W, 0.001, ctypes.byref(d), ctypes.c_void_p(0x600010), ws_need, None) == -3
+
+
+def test_valid_call_without_a_device_reports_cuda_error(qg):
+    # every argument passes host validation; the first CUDA call then fails
+    # (no device here) and the status says so instead of crashing
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    L = qg.lib()
+    d = _fake_desc(qg)
+    st = L.qgemm_forward(ctypes.c_void_p(0x300000), 1, 128, ctypes.byref(d), ctypes.c_void_p(0x200000), 64, 0,
+                         None, 0, None)
+    assert st == -5
+    assert qg.last_error()
+
+
+def test_moe_validation_without_gpu(qg):
+    L = qg.lib()
+    arr = (qg.QgQWeight * 2)(_fake_desc(qg), _fake_desc(qg, N=128))
+    x, ids, y = ctypes.c_void_p(0x300000), ctypes.c_void_p(0x310000), ctypes.c_void_p(0x320000)
+    assert L.qgemm_moe_grouped(x, 4, ids, 2, arr, 2, y, 0, None, 0, None) == -1   # N differs
+    arr2 = (qg.QgQWeight * 1)(_fake_desc(qg))
+    assert L.qgemm_moe_grouped(x, 4, ids, 2, arr2, 300, y, 0, None, 0, None) == -1  # E too large
+    assert L.qgemm_moe_grouped(x, 0, ids, 2, arr2, 1, y, 0, None, 0, None) == 0     # T = 0
+    b = ctypes.c_size_t()
+    assert L.qgemm_moe_workspace_size(256, 2, 1, arr2, ctypes.byref(b)) == 0 and b.value > 0
+    assert L.qgemm_moe_grouped(x, 4, ids, 2, arr2, 1, y, 0, None, 0, None) == -4    # no workspace

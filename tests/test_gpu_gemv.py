@@ -1,0 +1,104 @@
+"""The fused product on the GPU against the fp64 oracle, for every width,
+group size and M path, with outliers, ragged N, strided x / y."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from _parity import check_product, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qg():
+    import bit_weight_only_group_gb300 as qg
+    qg.lib()
+    return qg
+
+
+_cache = {}
+
+
+def _weights(N, K, bits, group, frac, seed):
+    key = (N, K, bits, group, frac, seed)
+    if key not in _cache:
+        W = wl.gen_weight(N, K, seed=seed, outlier_frac=frac, outlier_seed=seed + 1)
+        q = oracle.quantize(W, bits, group, frac)
+        _cache[key] = (q, np.abs(oracle.dequant(q)).max())
+    return _cache[key]
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6])
+@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("M", [1, 5, 8, 16, 27, 64])
+def test_product_small(qg, bits, group, M):
+    N, K, frac = 200, 1024, 0.002            # N not a multiple of the 64-row tile
+    q, wmax = _weights(N, K, bits, group, frac, seed=17 * bits + group)
+    x = wl.gen_x(M, K, seed=M)
+    y = qg.qgemm_forward(x.cuda(), to_device(q))
+    torch.cuda.synchronize()
+    check_product(y, oracle.linear(x, q), x, wmax)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 6])
+@pytest.mark.parametrize("M", [65, 130])
+def test_product_above_decode_range(qg, bits, M):
+    N, K = 136, 512
+    q, wmax = _weights(N, K, bits, 128, 0.002, seed=5)
+    x = wl.gen_x(M, K, seed=M)
+    y = qg.qgemm_forward(x.cuda(), to_device(q))
+    torch.cuda.synchronize()
+    check_product(y, oracle.linear(x, q), x, wmax)
+
+
+def test_product_strided_and_bf16_output(qg):
+    N, K, M = 192, 768, 9
+    q, wmax = _weights(N, K, 5, 64, 0.003, seed=9)
+    xbig = wl.gen_x(M, K + 40, seed=3).cuda()
+    x = xbig[:, 16:16 + K]                     # row stride K + 40, unaligned start
+    ybig = torch.full((M, N + 8), 7.0, device="cuda")
+    y = ybig[:, :N]
+    qd = to_device(q)
+    qg.qgemm_forward(x, qd, out=y)
+    yb = qg.qgemm_forward(x, qd, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    check_product(y, oracle.linear(x.cpu(), q), x.cpu(), wmax)
+    assert (ybig[:, N:] == 7.0).all()          # nothing written past N
+    assert torch.equal(yb, y.to(torch.bfloat16))
+
+
+def test_zero_weights_and_zero_x_give_exact_zero(qg):
+    N, K = 64, 256
+    for bits in (2, 4, 5):
+        q = oracle.quantize(np.zeros((N, K), np.float16), bits, 128, 0.0)
+        y = qg.qgemm_forward(wl.gen_x(3, K).cuda(), to_device(q))
+        assert (y == 0).all()
+    q, _ = _weights(N, K, 3, 64, 0.0, seed=4)
+    y = qg.qgemm_forward(torch.zeros((2, K), dtype=torch.bfloat16, device="cuda"), to_device(q))
+    assert (y == 0).all()
+
+
+def test_one_hot_x_reads_back_dequantized_columns(qg):
+    N, K = 128, 512
+    q, _ = _weights(N, K, 6, 128, 0.004, seed=21)
+    D = oracle.dequant(q)
+    ks = [0, 1, 63, 64, 127, 300, 511]
+    x = torch.zeros((len(ks), K), dtype=torch.bfloat16)
+    for i, k in enumerate(ks):
+        x[i, k] = 1.0
+    y = qg.qgemm_forward(x.cuda(), to_device(q)).double().cpu().numpy()
+    ref = D[:, ks].T
+    assert np.allclose(y, ref, rtol=2 ** -10, atol=0), np.abs(y - ref).max()
+
+
+@pytest.mark.parametrize("bits,group,M", [(4, 128, 1), (2, 128, 8), (3, 64, 32), (5, 128, 1), (6, 64, 8),
+                                          (2, 64, 32)])
+def test_product_4096(qg, bits, group, M):
+    frac = 0.0 if bits == 4 else 0.001
+    q, wmax = _weights(4096, 4096, bits, group, frac, seed=1234)
+    x = wl.gen_x(M, 4096)
+    y = qg.qgemm_forward(x.cuda(), to_device(q))
+    torch.cuda.synchronize()
+    check_product(y, oracle.linear(x, q), x, wmax)

@@ -1,0 +1,75 @@
+"""Grouped product over top-k routed experts against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from _parity import check_product, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qg():
+    import bit_weight_only_group_gb300 as qg
+    qg.lib()
+    return qg
+
+
+def _experts(E, N, K, bits, group, frac, seed):
+    qs = [oracle.quantize(wl.gen_weight(N, K, seed=seed + e, outlier_frac=frac, outlier_seed=seed + 100 + e),
+                          bits, group, frac) for e in range(E)]
+    wmax = max(np.abs(oracle.dequant(q)).max() for q in qs)
+    return qs, wmax
+
+
+@pytest.mark.parametrize("bits,group", [(4, 128), (2, 64), (5, 128)])
+@pytest.mark.parametrize("T,k,E", [(37, 2, 4), (128, 2, 8), (3, 3, 5)])
+def test_moe_small(qg, bits, group, T, k, E):
+    N, K = 136, 512
+    qs, wmax = _experts(E, N, K, bits, group, 0.002, seed=40)
+    x = wl.gen_x(T, K, seed=T)
+    topk = wl.gen_topk(T, k, E, seed=T + 1)
+    y = qg.qgemm_moe_grouped(x.cuda(), topk.cuda(), [to_device(q) for q in qs])
+    torch.cuda.synchronize()
+    ref = oracle.moe(x, topk.numpy(), qs)
+    check_product(y.reshape(T * k, N), ref.reshape(T * k, N), x.repeat_interleave(k, 0), wmax)
+
+
+def test_moe_skips_invalid_ids_and_handles_empty_experts(qg):
+    N, K, E, T, k = 64, 256, 6, 20, 2
+    qs, wmax = _experts(E, N, K, 4, 128, 0.0, seed=70)
+    x = wl.gen_x(T, K, seed=1)
+    topk = torch.full((T, k), 1, dtype=torch.int32)
+    topk[:, 1] = 3
+    topk[5, 0] = -1                            # invalid ids are skipped
+    topk[6, 1] = E
+    y = torch.full((T, k, N), 9.0, device="cuda")
+    qg.qgemm_moe_grouped(x.cuda(), topk.cuda(), [to_device(q) for q in qs], out=y)
+    torch.cuda.synchronize()
+    yc = y.double().cpu().numpy()
+    assert (yc[5, 0] == 9.0).all() and (yc[6, 1] == 9.0).all()
+    valid = np.ones((T, k), bool)
+    valid[5, 0] = valid[6, 1] = False
+    tk = topk.numpy().copy()
+    tk[~valid] = 0
+    ref = oracle.moe(x, tk, qs)
+    check_product(torch.from_numpy(yc[valid]), ref[valid], x.repeat_interleave(k, 0)[valid.ravel()], wmax)
+
+
+def test_moe_layer_4096_experts(qg):
+    # the MoE workload: hidden 4096, 16 experts, 3072x4096 gate projection,
+    # 256 tokens, top-2 from a Zipf(1.1) popularity; a sample of tokens is
+    # checked against the oracle
+    cfg = wl.MoE()
+    qs, wmax = _experts(cfg.n_experts, cfg.ffn, cfg.hidden, 4, 128, 0.0, seed=500)
+    x = wl.gen_x(cfg.tokens, cfg.hidden)
+    topk = wl.gen_topk(cfg.tokens, cfg.top_k, cfg.n_experts)
+    y = qg.qgemm_moe_grouped(x.cuda(), topk.cuda(), [to_device(q) for q in qs])
+    torch.cuda.synchronize()
+    sample = np.arange(0, cfg.tokens, 16)
+    ref = oracle.moe(x[sample], topk.numpy()[sample], qs)
+    got = y[torch.from_numpy(sample).cuda()]
+    k = cfg.top_k
+    check_product(got.reshape(-1, cfg.ffn), ref.reshape(-1, cfg.ffn), x[sample].repeat_interleave(k, 0), wmax)
