@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "QG_OK", -1: "QG_ERR_INVALID_ARG", -2: "QG_ERR_UNSUPPORTED", 
                 -4: "QG_ERR_WORKSPACE", -5: "QG_ERR_CUDA", -6: "QG_ERR_TIMEOUT", -7: "QG_ERR_DEVICE_STATUS"}
 Y_F32, Y_BF16 = 0, 1
 
-ABI_FUNCTIONS = ("qpack_query_sizes", "qpack_workspace_size", "qpack_quantize", "qgemm_workspace_size",
+ABI_FUNCTIONS = ("qpack_query_sizes", "qpack_workspace_size", "qpack_quantize", "qpack_quantize_noalloc",
+                 "qgemm_workspace_size",
                  "qgemm_forward", "qgemm_moe_workspace_size", "qgemm_moe_grouped", "qgemm_last_error")
 
 
@@ -169,6 +170,23 @@ def qpack_quantize(W: torch.Tensor, bits: int, group: int, outlier_frac: float =
     d = qw.desc()
     _check(lib().qpack_quantize(_ptr(W), outlier_frac, ctypes.byref(d), _ptr(ws), ws.numel(), _stream(stream)),
            "qpack_quantize")
+    return qw
+
+
+def qpack_quantize_noalloc(W: torch.Tensor, bits: int, group: int, outlier_frac: float = 0.0,
+                           out: QWeight | None = None, stream=None) -> QWeight:
+    """qpack_quantize for callers that cannot allocate device memory: the
+    library uses its own fixed scratch array (see include/qgemm.h).  Pass
+    ``out`` (allocated beforehand) to keep this call allocation-free."""
+    if W.dtype != torch.float16 or not W.is_cuda or W.dim() != 2 or not W.is_contiguous():
+        raise ValueError("W must be a contiguous 2-D float16 CUDA tensor")
+    N, K = W.shape
+    qw = out if out is not None else QWeight.empty(N, K, bits, group, outlier_frac, W.device)
+    f = lib().qpack_quantize_noalloc
+    f.argtypes = [ctypes.c_void_p, ctypes.c_float, ctypes.POINTER(QgQWeight), ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    d = qw.desc()
+    _check(f(_ptr(W), outlier_frac, ctypes.byref(d), _stream(stream)), "qpack_quantize_noalloc")
     return qw
 
 

@@ -139,6 +139,30 @@ QG_API qg_status qpack_workspace_size(int32_t N, int32_t K, size_t* bytes);
 QG_API qg_status qpack_quantize(const uint16_t* W, float outlier_frac, const qg_qweight* out, void* ws,
                          size_t ws_bytes, void* stream);
 
+/*
+ * qpack_quantize without a workspace argument, for callers that cannot
+ * allocate device memory when they quantize: code inside a host application
+ * that owns the device allocator (a plugin, a server that reserves its memory
+ * pool up front), code where cudaMalloc's implicit device synchronization is
+ * not acceptable, or code running after a fixed memory budget is frozen.
+ * The pages have no counterpart to this entry point; it exists for such
+ * callers only.  Same operation, arguments and results as qpack_quantize
+ * (bit-identical output).
+ *  - Scratch: a fixed 1 MiB array in the library's own device memory, held
+ *    by every GPU that loads the library until the process exits.  Matrices
+ *    whose scratch need (qpack_workspace_size) exceeds it -- more than about
+ *    76,000 rows -- are rejected with QG_ERR_WORKSPACE before anything runs.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make
+ *    that first call before any stream capture.
+ *  - Every call shares the array and it keeps the last call's contents; each
+ *    call clears what must start at zero.  Calls that overlap on the GPU
+ *    (e.g. on two unordered streams) race on the array: order them.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+QG_API qg_status qpack_quantize_noalloc(const uint16_t* W, float outlier_frac, const qg_qweight* out,
+                                        void* stream);
+
 /* Workspace bytes qgemm_forward needs for M rows of x against w.  Host-only. */
 QG_API qg_status qgemm_workspace_size(int32_t M, const qg_qweight* w, size_t* bytes);
 
