@@ -121,7 +121,7 @@ struct MoeWs {
 };
 
 // Upper bound on work items: sum over experts of ceil(count / chunk) with the
-// smallest chunk (8 pairs).
+// smallest chunk (1 pair).
 inline int max_items_for(int P, int E, int chunk) { return (int)ceil_div(P, chunk) + E; }
 
 size_t moe_ws_layout(int T, int k, int E, MoeWs* p, void* base)
@@ -131,7 +131,7 @@ size_t moe_ws_layout(int T, int k, int E, MoeWs* p, void* base)
     const size_t o_n = align_up(sizeof(int) * ((size_t)E + 1), 256);
     const size_t o_perm = o_n + 256;
     const size_t o_items = align_up(o_perm + sizeof(int) * P, 256);
-    const size_t total = align_up(o_items + sizeof(int2) * (size_t)max_items_for((int)P, E, 8), 256);
+    const size_t total = align_up(o_items + sizeof(int2) * (size_t)max_items_for((int)P, E, 1), 256);
     if (p && base) {
         char* b = static_cast<char*>(base);
         p->offsets = reinterpret_cast<int*>(b + o_off);
@@ -176,8 +176,8 @@ qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const
     const qg_qweight& w0 = experts[0];
     // tokens per CTA chunk from the mean load per expert
     const int mean = (P + E - 1) / E;
-    const int nt = gemv::nt_for(std::max(1, mean));
-    k_route<<<1, kRouteThreads, 0, s>>>(topk, P, E, 8 * nt, p.offsets, p.perm, p.items, p.n_items);
+    const int mp = gemv::mp_for(std::max(1, mean));
+    k_route<<<1, kRouteThreads, 0, s>>>(topk, P, E, mp, p.offsets, p.perm, p.items, p.n_items);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
 
@@ -185,7 +185,7 @@ qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const
     memset(&t, 0, sizeof(t));
     t.x = reinterpret_cast<const __nv_bfloat16*>(x);
     t.ldx = w0.K; t.N = w0.N; t.K = w0.K; t.topk = k;
-    t.chunk = 8 * nt;
+    t.chunk = mp;
     t.offsets = p.offsets;
     t.perm = p.perm;
     t.items = p.items;
@@ -205,11 +205,11 @@ qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const
     const int maxi = max_items_for(P, E, t.chunk);
     const int expect = std::min(maxi, (int)ceil_div(P, t.chunk) + E / 2);
     switch (w0.bits) {
-        case 2: return gemv::launch_grouped<2>(t, maxi, expect, w0.group, nt, s);
-        case 3: return gemv::launch_grouped<3>(t, maxi, expect, w0.group, nt, s);
-        case 4: return gemv::launch_grouped<4>(t, maxi, expect, w0.group, nt, s);
-        case 5: return gemv::launch_grouped<5>(t, maxi, expect, w0.group, nt, s);
-        default: return gemv::launch_grouped<6>(t, maxi, expect, w0.group, nt, s);
+        case 2: return gemv::launch_grouped<2>(t, maxi, expect, w0.group, mp, s);
+        case 3: return gemv::launch_grouped<3>(t, maxi, expect, w0.group, mp, s);
+        case 4: return gemv::launch_grouped<4>(t, maxi, expect, w0.group, mp, s);
+        case 5: return gemv::launch_grouped<5>(t, maxi, expect, w0.group, mp, s);
+        default: return gemv::launch_grouped<6>(t, maxi, expect, w0.group, mp, s);
     }
 }
 

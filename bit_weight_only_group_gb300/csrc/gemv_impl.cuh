@@ -129,31 +129,37 @@ __device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c
     return d;
 }
 
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
-{
-    return (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
-}
-
 // fp16 pair (q_lo - zp, q_hi - zp) of entry E, exact: the LOP3 gives
 // (1024 + 2^plo q_lo, 1024 + 2^phi q_hi); the HFMA2 scales by 2^-p (exact)
-// and adds -1024*2^-p - zp (an exact fp16 integer).
+// and adds -(1024*2^-p + zp).  Because zp < 2^bits <= 1024*2^-p, the value
+// 1024*2^-p + zp stays in the binade of 1024*2^-p, where one fp16 step is
+// 2^-p: its bit pattern is bits(1024*2^-p) + zp*2^p, so the addend is one
+// integer multiply-add on zp.
+template <int BITS, int NC, int E>
+__device__ __forceinline__ uint32_t zp_addend(uint32_t zp)
+{
+    constexpr PairE p = plan_entry(BITS, NC, E);
+    constexpr uint32_t base = (uint32_t)(0xE400 - 0x400 * p.plo) | ((uint32_t)(0xE400 - 0x400 * p.phi) << 16);
+    constexpr uint32_t mul = (1u << p.plo) | ((1u << p.phi) << 16);
+    return zp * mul + base;
+}
+
 template <int BITS, int NC, int E, int NW>
-__device__ __forceinline__ uint32_t deq_affine(const uint32_t (&w)[NW], float zp)
+__device__ __forceinline__ uint32_t deq_affine(const uint32_t (&w)[NW], uint32_t zp)
 {
     constexpr PairE p = plan_entry(BITS, NC, E);
     constexpr uint32_t cm = (1u << BITS) - 1u;
     constexpr uint32_t mask = (cm << p.plo) | (cm << (16 + p.phi));
     const uint32_t raw = (window<p.S, NW>(w) & mask) | 0x64006400u;
     constexpr uint32_t mul = (uint32_t)(0x3C00 - 0x400 * p.plo) | ((uint32_t)(0x3C00 - 0x400 * p.phi) << 16);
-    const uint32_t add = pack_h2(-1024.0f * pow2f(-p.plo) - zp, -1024.0f * pow2f(-p.phi) - zp);
-    return hfma2_u32(raw, mul, add);
+    return hfma2_u32(raw, mul, zp_addend<BITS, NC, E>(zp));
 }
 
 // ---------------------------------------------------------------- loads
 __device__ __forceinline__ uint4 ldg_stream128(const void* p)
 {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
@@ -161,13 +167,13 @@ __device__ __forceinline__ uint4 ldg_stream128(const void* p)
 __device__ __forceinline__ uint2 ldg_stream64(const void* p)
 {
     uint2 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
     return v;
 }
 __device__ __forceinline__ uint32_t ldg_stream32(const void* p)
 {
     uint32_t v;
-    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.u32 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
 }
 
@@ -252,55 +258,84 @@ struct Problem {
 __device__ __forceinline__ int x_row(const Problem& p, int m) { return p.rowmap ? p.rowmap[m] / p.xdiv : m; }
 __device__ __forceinline__ int y_row(const Problem& p, int m) { return p.rowmap ? p.rowmap[m] : m; }
 
-template <int BITS, int G, int NT>
+// MP = padded token count (1, 2, 4, 8, 16, 32 or 64): the staged-x layout
+// [group][step][token < MP][t < 4] (8 bytes each) has compile-time strides.
+template <int BITS, int G, int MP>
 struct Cfg {
     static constexpr int NC = G / 4;
     static constexpr int NW = Chunk<BITS, G>::NW;
     static constexpr int STEPS = G / 16;
+    static constexpr int NT = (MP + 7) / 8;                       // n8 token tiles
     static constexpr int NTOK = 8 * NT;
-    static constexpr int D = NT <= 2 ? 4 : 2;                    // prefetch depth (groups)
-    static constexpr int XG_RAW = 2048 / (G * NT);               // x-block groups (32 KB)
-    static constexpr int XG = XG_RAW < D ? D : XG_RAW;
-    static constexpr int XS_BYTES = XG * STEPS * NT * 32 * 8;
+    // prefetch depth (groups) of the register ring
+    static constexpr int D_CLAMP = MP <= 16 ? 4 : 2;
+    static constexpr int TSTRIDE = 32;                            // bytes per token per step
+    static constexpr int SSTRIDE = MP * TSTRIDE;                  // bytes per step
+    static constexpr int GSTRIDE = STEPS * SSTRIDE;               // bytes per group
+    static constexpr int XS_BUDGET = 49152;
+    static constexpr int D = D_CLAMP < XS_BUDGET / GSTRIDE ? D_CLAMP : XS_BUDGET / GSTRIDE;
+    static constexpr int XG = (XS_BUDGET / GSTRIDE) / D * D;      // groups per x block
     static constexpr int RED_BYTES = kRowsPerCta * NTOK * 4;
-    static constexpr int SMEM = XS_BYTES > RED_BYTES ? XS_BYTES : RED_BYTES;
+    static_assert(XG >= D, "x block smaller than the prefetch ring");
+    // dynamic shared memory for a split of gpsplit groups
+    static int smem(int gpsplit)
+    {
+        const int xs = (gpsplit < XG ? gpsplit : XG) * GSTRIDE;
+        return xs > RED_BYTES ? xs : RED_BYTES;
+    }
 };
 
-// Stage x[:, kbase : kbase + ngr*G] as fp16 in MMA B-fragment order: item
-// (group, step, n8 tile, lane) holds the 4 values whose k positions match the
-// A-fragment codes of thread lane%4 in that step.
-template <int BITS, int G, int NT>
-__device__ void stage_x(const Problem& a, int kbase, int ngr, uint2* xs)
+// Stage x[:, kbase : kbase + ngr*G] as fp16 in MMA B-fragment order: the
+// 8-byte entry (group, step, token m, t) holds the 4 values of token m whose k
+// positions match the A-fragment codes of thread t in that step.  One item
+// = (group, token, t): 16-byte loads of the thread's NC contiguous bf16
+// values, then one 8-byte store per step.  Tokens M..MP-1 are not written:
+// the MMA columns that read them are never stored.
+template <int BITS, int G, int MP>
+__device__ void stage_x(const Problem& a, int kbase, int ngr, unsigned char* xs)
 {
-    using C = Cfg<BITS, G, NT>;
-    const int items = ngr * NT * 32;
+    using C = Cfg<BITS, G, MP>;
+    const int M = a.M;
+    const int items = ngr * M * 4;
     for (int it = threadIdx.x; it < items; it += blockDim.x) {
-        const int gi = it / (NT * 32), rem = it % (NT * 32);
-        const int nt = rem / 32, ln = rem % 32;
-        const int m = nt * 8 + (ln >> 2), t = ln & 3;
-        const bool live = m < a.M;
-        const __nv_bfloat16* xr = a.x + (size_t)(live ? x_row(a, m) : 0) * a.ldx + kbase + gi * G + t * C::NC;
+        const int t = it & 3, m = (it >> 2) % M, gi = (it >> 2) / M;
+        const __nv_bfloat16* xr = a.x + (size_t)x_row(a, m) * a.ldx + kbase + gi * G + t * C::NC;
+        uint32_t v[C::NC / 2];
+        if ((reinterpret_cast<uintptr_t>(xr) & 15u) == 0) {
+#pragma unroll
+            for (int i = 0; i < C::NC / 8; i++) {
+                const uint4 q = __ldg(reinterpret_cast<const uint4*>(xr) + i);
+                v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+            }
+        } else {
+            const unsigned short* x16 = reinterpret_cast<const unsigned short*>(xr);
+#pragma unroll
+            for (int i = 0; i < C::NC / 2; i++)
+                v[i] = (uint32_t)__ldg(x16 + 2 * i) | ((uint32_t)__ldg(x16 + 2 * i + 1) << 16);
+        }
+        auto f16 = [&](int c) -> uint32_t {   // bf16 -> fp32 (exact) -> fp16
+            const uint32_t bits = (c & 1) ? (v[c >> 1] & 0xFFFF0000u) : (v[c >> 1] << 16);
+            return __half_as_ushort(__float2half_rn(__uint_as_float(bits)));
+        };
+        unsigned char* dst = xs + (size_t)gi * C::GSTRIDE + m * C::TSTRIDE + t * 8;
         static_for<0, C::STEPS>([&](auto sc) {
             constexpr int s = decltype(sc)::value;
             constexpr PairE e0 = plan_entry(BITS, C::NC, 2 * s);
             constexpr PairE e1 = plan_entry(BITS, C::NC, 2 * s + 1);
-            uint2 v = make_uint2(0u, 0u);
-            if (live) {
-                v.x = (uint32_t)x_f16(xr[e0.lo]) | ((uint32_t)x_f16(xr[e0.hi]) << 16);
-                v.y = (uint32_t)x_f16(xr[e1.lo]) | ((uint32_t)x_f16(xr[e1.hi]) << 16);
-            }
-            xs[((gi * C::STEPS + s) * NT + nt) * 32 + ln] = v;
+            *reinterpret_cast<uint2*>(dst + s * C::SSTRIDE) =
+                make_uint2(f16(e0.lo) | (f16(e0.hi) << 16), f16(e1.lo) | (f16(e1.hi) << 16));
         });
     }
 }
 
-template <int BITS, int G, int NT>
+template <int BITS, int G, int MP>
 __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsplit)
 {
-    using C = Cfg<BITS, G, NT>;
-    constexpr int NW = C::NW, D = C::D;
+    using C = Cfg<BITS, G, MP>;
+    constexpr int NW = C::NW, D = C::D, NT = C::NT;
+    constexpr int GB = G * BITS / 8;   // packed bytes per group
+    constexpr int CB = Chunk<BITS, G>::CB;
     extern __shared__ __align__(16) unsigned char smem[];
-    uint2* xs = reinterpret_cast<uint2*>(smem);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = lane & 3, gq = lane >> 2;
@@ -310,11 +345,22 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     const int g_begin = blockIdx.y * gpsplit;
     const int ngrp = max(0, min(ng, g_begin + gpsplit) - g_begin);
 
-    constexpr int GB = G * BITS / 8;   // bytes per group
+    // streaming pointers of this thread, advanced by D groups per iteration
     const size_t rowbytes = (size_t)a.K * BITS / 8;
-    const uint8_t* src0 = a.packed + (size_t)r0 * rowbytes + (size_t)g_begin * GB + t * Chunk<BITS, G>::CB;
-    const uint8_t* src1 = a.packed + (size_t)r1 * rowbytes + (size_t)g_begin * GB + t * Chunk<BITS, G>::CB;
+    const uint8_t* p0 = a.packed + (size_t)r0 * rowbytes + (size_t)g_begin * GB + t * CB;
+    const uint8_t* p1 = a.packed + (size_t)r1 * rowbytes + (size_t)g_begin * GB + t * CB;
     const size_t pidx0 = (size_t)r0 * ng + g_begin, pidx1 = (size_t)r1 * ng + g_begin;
+    const uint16_t* sp0 = a.scale + pidx0;
+    const uint16_t* sp1 = a.scale + pidx1;
+    const uint8_t* zq0 = a.zp + pidx0;
+    const uint8_t* zq1 = a.zp + pidx1;
+    const uint2* cq0 = a.cb + pidx0;
+    const uint2* cq1 = a.cb + pidx1;
+
+    // this lane's B-fragment slot (token clamped to MP-1; its column is discarded)
+    uint32_t xlo[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++) xlo[nt] = min(nt * 8 + gq, MP - 1) * C::TSTRIDE + t * 8;
 
     float yacc[NT][4];
 #pragma unroll
@@ -323,90 +369,105 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     uint32_t wr[D][2][NW];
     uint32_t prm[D][2][2];   // affine: scale bits, zp; codebook: two words of 4 fp16
 
-    auto issue = [&](int slot, int j) {
-        Chunk<BITS, G>::load(src0 + (size_t)j * GB, wr[slot][0]);
-        Chunk<BITS, G>::load(src1 + (size_t)j * GB, wr[slot][1]);
+    // load group (current base + REL) into ring slot SLOT
+    auto issue = [&](auto slot_c, auto rel_c) {
+        constexpr int SLOT = decltype(slot_c)::value, REL = decltype(rel_c)::value;
+        Chunk<BITS, G>::load(p0 + REL * GB, wr[SLOT][0]);
+        Chunk<BITS, G>::load(p1 + REL * GB, wr[SLOT][1]);
         if constexpr (BITS == 2) {
-            const uint2 c0 = __ldg(a.cb + pidx0 + j), c1 = __ldg(a.cb + pidx1 + j);
-            prm[slot][0][0] = c0.x; prm[slot][0][1] = c0.y;
-            prm[slot][1][0] = c1.x; prm[slot][1][1] = c1.y;
+            const uint2 c0 = __ldg(cq0 + REL), c1 = __ldg(cq1 + REL);
+            prm[SLOT][0][0] = c0.x; prm[SLOT][0][1] = c0.y;
+            prm[SLOT][1][0] = c1.x; prm[SLOT][1][1] = c1.y;
         } else {
-            prm[slot][0][0] = __ldg(a.scale + pidx0 + j);
-            prm[slot][1][0] = __ldg(a.scale + pidx1 + j);
-            prm[slot][0][1] = __ldg(a.zp + pidx0 + j);
-            prm[slot][1][1] = __ldg(a.zp + pidx1 + j);
+            prm[SLOT][0][0] = __ldg(sp0 + REL);
+            prm[SLOT][1][0] = __ldg(sp1 + REL);
+            prm[SLOT][0][1] = __ldg(zq0 + REL);
+            prm[SLOT][1][1] = __ldg(zq1 + REL);
         }
     };
+    auto advance = [&]() {
+        p0 += D * GB; p1 += D * GB;
+        if constexpr (BITS == 2) { cq0 += D; cq1 += D; }
+        else { sp0 += D; sp1 += D; zq0 += D; zq1 += D; }
+    };
 
-#pragma unroll
-    for (int d = 0; d < D; d++)
-        if (d < ngrp) issue(d, d);
+    static_for<0, D>([&](auto dc) {
+        constexpr int d = decltype(dc)::value;
+        if (d < ngrp) issue(dc, dc);
+    });
 
+    int xnext = 0;          // group index (relative) at which x is staged next
+    uint32_t xoff = 0;      // byte offset of group jj inside the x block
     for (int jj = 0; jj < ngrp; jj += D) {
+        if (jj == xnext) {
+            __syncthreads();
+            stage_x<BITS, G, MP>(a, (g_begin + jj) * G, min(C::XG, ngrp - jj), smem);
+            __syncthreads();
+            xnext += C::XG;
+            xoff = 0;
+        }
+        const unsigned char* xb[NT];
 #pragma unroll
-        for (int d = 0; d < D; d++) {
-            const int j = jj + d;
-            if (j >= ngrp) break;
-            if (j % C::XG == 0) {
-                __syncthreads();
-                stage_x<BITS, G, NT>(a, (g_begin + j) * G, min(C::XG, ngrp - j), xs);
-                __syncthreads();
-            }
-            const int xg = j % C::XG;
-            const uint2* xb = xs + (size_t)xg * C::STEPS * NT * 32 + lane;
+        for (int nt = 0; nt < NT; nt++) xb[nt] = smem + xoff + xlo[nt];
 
-            if constexpr (BITS == 2) {
-                // per-row lookup tables: low bytes and high bytes of the 4 entries
-                const uint32_t L0 = __byte_perm(prm[d][0][0], prm[d][0][1], 0x6420);
-                const uint32_t H0 = __byte_perm(prm[d][0][0], prm[d][0][1], 0x7531);
-                const uint32_t L1 = __byte_perm(prm[d][1][0], prm[d][1][1], 0x6420);
-                const uint32_t H1 = __byte_perm(prm[d][1][0], prm[d][1][1], 0x7531);
-                static_for<0, NW>([&](auto wc) {
-                    constexpr int wi = decltype(wc)::value;
-                    static_for<0, 4>([&](auto jc) {
-                        constexpr int jf = decltype(jc)::value;
-                        const uint32_t f0 = (wr[d][0][wi] >> (2 * jf)) & 0x03030303u;
-                        const uint32_t f1 = (wr[d][1][wi] >> (2 * jf)) & 0x03030303u;
-                        const uint32_t s0l = f0 * 0x11u + 0x4040u, s0h = __umulhi(f0, 0x00110000u) + 0x4040u;
-                        const uint32_t s1l = f1 * 0x11u + 0x4040u, s1h = __umulhi(f1, 0x00110000u) + 0x4040u;
-                        const uint32_t a0 = __byte_perm(L0, H0, s0l), a2 = __byte_perm(L0, H0, s0h);
-                        const uint32_t a1 = __byte_perm(L1, H1, s1l), a3 = __byte_perm(L1, H1, s1h);
-                        constexpr int s = 4 * wi + jf;   // entries 2s (lo) and 2s+1 (hi)
+        static_for<0, D>([&](auto dc) {
+            constexpr int d = decltype(dc)::value;
+            if (jj + d < ngrp) {
+                if constexpr (BITS == 2) {
+                    // per-row lookup tables: low bytes and high bytes of the 4 entries
+                    const uint32_t L0 = __byte_perm(prm[d][0][0], prm[d][0][1], 0x6420);
+                    const uint32_t H0 = __byte_perm(prm[d][0][0], prm[d][0][1], 0x7531);
+                    const uint32_t L1 = __byte_perm(prm[d][1][0], prm[d][1][1], 0x6420);
+                    const uint32_t H1 = __byte_perm(prm[d][1][0], prm[d][1][1], 0x7531);
+                    static_for<0, NW>([&](auto wc) {
+                        constexpr int wi = decltype(wc)::value;
+                        static_for<0, 4>([&](auto jc) {
+                            constexpr int jf = decltype(jc)::value;
+                            const uint32_t f0 = (wr[d][0][wi] >> (2 * jf)) & 0x03030303u;
+                            const uint32_t f1 = (wr[d][1][wi] >> (2 * jf)) & 0x03030303u;
+                            const uint32_t s0l = f0 * 0x11u + 0x4040u, s0h = __umulhi(f0, 0x00110000u) + 0x4040u;
+                            const uint32_t s1l = f1 * 0x11u + 0x4040u, s1h = __umulhi(f1, 0x00110000u) + 0x4040u;
+                            const uint32_t a0 = __byte_perm(L0, H0, s0l), a2 = __byte_perm(L0, H0, s0h);
+                            const uint32_t a1 = __byte_perm(L1, H1, s1l), a3 = __byte_perm(L1, H1, s1h);
+                            constexpr int s = 4 * wi + jf;   // entries 2s (lo) and 2s+1 (hi)
+#pragma unroll
+                            for (int nt = 0; nt < NT; nt++) {
+                                const uint2 b = *reinterpret_cast<const uint2*>(xb[nt] + d * C::GSTRIDE + s * C::SSTRIDE);
+                                mma16816(yacc[nt], a0, a1, a2, a3, b.x, b.y);
+                            }
+                        });
+                    });
+                } else {
+                    float acc[NT][4];
+#pragma unroll
+                    for (int i = 0; i < NT; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+                    const uint32_t z0 = prm[d][0][1], z1 = prm[d][1][1];
+                    static_for<0, C::STEPS>([&](auto sc) {
+                        constexpr int s = decltype(sc)::value;
+                        const uint32_t a0 = deq_affine<BITS, C::NC, 2 * s>(wr[d][0], z0);
+                        const uint32_t a1 = deq_affine<BITS, C::NC, 2 * s>(wr[d][1], z1);
+                        const uint32_t a2 = deq_affine<BITS, C::NC, 2 * s + 1>(wr[d][0], z0);
+                        const uint32_t a3 = deq_affine<BITS, C::NC, 2 * s + 1>(wr[d][1], z1);
 #pragma unroll
                         for (int nt = 0; nt < NT; nt++) {
-                            const uint2 b = xb[(s * NT + nt) * 32];
-                            mma16816(yacc[nt], a0, a1, a2, a3, b.x, b.y);
+                            const uint2 b = *reinterpret_cast<const uint2*>(xb[nt] + d * C::GSTRIDE + s * C::SSTRIDE);
+                            mma16816(acc[nt], a0, a1, a2, a3, b.x, b.y);
                         }
                     });
-                });
-            } else {
-                float acc[NT][4];
-#pragma unroll
-                for (int i = 0; i < NT; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
-                const float z0 = (float)prm[d][0][1], z1 = (float)prm[d][1][1];
-                static_for<0, C::STEPS>([&](auto sc) {
-                    constexpr int s = decltype(sc)::value;
-                    const uint32_t a0 = deq_affine<BITS, C::NC, 2 * s>(wr[d][0], z0);
-                    const uint32_t a1 = deq_affine<BITS, C::NC, 2 * s>(wr[d][1], z1);
-                    const uint32_t a2 = deq_affine<BITS, C::NC, 2 * s + 1>(wr[d][0], z0);
-                    const uint32_t a3 = deq_affine<BITS, C::NC, 2 * s + 1>(wr[d][1], z1);
+                    const float s0 = h2f((uint16_t)prm[d][0][0]), s1 = h2f((uint16_t)prm[d][1][0]);
 #pragma unroll
                     for (int nt = 0; nt < NT; nt++) {
-                        const uint2 b = xb[(s * NT + nt) * 32];
-                        mma16816(acc[nt], a0, a1, a2, a3, b.x, b.y);
+                        yacc[nt][0] = fmaf(s0, acc[nt][0], yacc[nt][0]);
+                        yacc[nt][1] = fmaf(s0, acc[nt][1], yacc[nt][1]);
+                        yacc[nt][2] = fmaf(s1, acc[nt][2], yacc[nt][2]);
+                        yacc[nt][3] = fmaf(s1, acc[nt][3], yacc[nt][3]);
                     }
-                });
-                const float s0 = h2f((uint16_t)prm[d][0][0]), s1 = h2f((uint16_t)prm[d][1][0]);
-#pragma unroll
-                for (int nt = 0; nt < NT; nt++) {
-                    yacc[nt][0] = fmaf(s0, acc[nt][0], yacc[nt][0]);
-                    yacc[nt][1] = fmaf(s0, acc[nt][1], yacc[nt][1]);
-                    yacc[nt][2] = fmaf(s1, acc[nt][2], yacc[nt][2]);
-                    yacc[nt][3] = fmaf(s1, acc[nt][3], yacc[nt][3]);
                 }
+                if (jj + d + D < ngrp) issue(dc, std::integral_constant<int, D + d>{});
             }
-            if (j + D < ngrp) issue(d, j + D);
-        }
+        });
+        advance();
+        xoff += D * C::GSTRIDE;
     }
 
     // ------------------------------------------------ split-K reduction + epilogue
@@ -427,7 +488,7 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     else __syncthreads();
     const int rank = S > 1 ? (int)cluster.block_rank() : 0;
     const int rows_per = kRowsPerCta / S;
-    const int Mv = min(a.M, C::NTOK);
+    const int Mv = min(a.M, MP);
     for (int it = threadIdx.x; it < rows_per * Mv; it += blockDim.x) {
         const int m = it / rows_per, rl = rank * rows_per + it % rows_per;
         const int n = blockIdx.x * kRowsPerCta + rl;
@@ -453,11 +514,10 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     if (S > 1) cluster.sync();   // keep this CTA's partials alive until every rank has read them
 }
 
-
-template <int BITS, int G, int NT>
+template <int BITS, int G, int MP>
 __global__ void __launch_bounds__(kWarps * 32) k_gemv(const Problem p, int splits, int gpsplit)
 {
-    gemv_body<BITS, G, NT>(p, splits, gpsplit);
+    gemv_body<BITS, G, MP>(p, splits, gpsplit);
 }
 
 // Grouped product over routed experts.  Pairs (token, slot) are sorted by
@@ -484,7 +544,7 @@ struct MoeTable {
     int nnz[kMoeMaxExperts];
 };
 
-template <int BITS, int G, int NT>
+template <int BITS, int G, int MP>
 __global__ void __launch_bounds__(kWarps * 32) k_gemv_moe(const __grid_constant__ MoeTable t, int splits,
                                                           int gpsplit)
 {
@@ -499,7 +559,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_gemv_moe(const __grid_constant_
     p.packed = t.packed[e]; p.scale = t.scale[e]; p.zp = t.zp[e]; p.cb = t.cb[e];
     p.row_ptr = t.row_ptr[e]; p.col = t.col[e]; p.val = t.val[e]; p.nnz = t.nnz[e];
     p.y = t.y; p.ldy = t.N; p.y_bf16 = t.y_bf16;
-    gemv_body<BITS, G, NT>(p, splits, gpsplit);
+    gemv_body<BITS, G, MP>(p, splits, gpsplit);
 }
 
 // K split: the cluster size S in {1, 2, 4, 8} that best fills the SMs with
@@ -525,15 +585,16 @@ inline int choose_splits(long long ctas_per_split, int ng)
     return best;
 }
 
-inline int nt_for(int M) { return M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8; }
+// Padded token count of a launch.
+inline int mp_for(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : 64; }
 
-template <int BITS, int G, int NT, typename K, typename A>
+template <int BITS, int G, int MP, typename K, typename A>
 qg_status launch_cluster(K kernel, const A& args, dim3 grid, int S, int gpsplit, cudaStream_t s)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kWarps * 32, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)Cfg<BITS, G, NT>::SMEM;
+    cfg.dynamicSmemBytes = (size_t)Cfg<BITS, G, MP>::smem(gpsplit);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -547,66 +608,65 @@ qg_status launch_cluster(K kernel, const A& args, dim3 grid, int S, int gpsplit,
     return QG_OK;
 }
 
-template <int BITS, int G, int NT>
-qg_status dense_nt(const Problem& p, cudaStream_t s)
+template <int BITS, int G, int MP>
+qg_status dense_mp(const Problem& p, cudaStream_t s)
 {
     const int ng = p.K / G;
     const int tiles = (int)ceil_div(p.N, kRowsPerCta);
     const int S = choose_splits(tiles, ng);
-    return launch_cluster<BITS, G, NT>(k_gemv<BITS, G, NT>, p, dim3((unsigned)tiles, (unsigned)S, 1), S,
+    return launch_cluster<BITS, G, MP>(k_gemv<BITS, G, MP>, p, dim3((unsigned)tiles, (unsigned)S, 1), S,
                                        (int)ceil_div(ng, S), s);
 }
 
-template <int BITS, int G, int NT>
-qg_status grouped_nt(const MoeTable& t, int max_items, int expect_items, cudaStream_t s)
+template <int BITS, int G, int MP>
+qg_status grouped_mp(const MoeTable& t, int max_items, int expect_items, cudaStream_t s)
 {
     const int ng = t.K / G;
     const int tiles = (int)ceil_div(t.N, kRowsPerCta);
     const int S = choose_splits((long long)tiles * std::max(1, expect_items), ng);
-    return launch_cluster<BITS, G, NT>(k_gemv_moe<BITS, G, NT>, t,
+    return launch_cluster<BITS, G, MP>(k_gemv_moe<BITS, G, MP>, t,
                                        dim3((unsigned)tiles, (unsigned)S, (unsigned)max_items), S,
                                        (int)ceil_div(ng, S), s);
 }
 
-template <int BITS>
-qg_status launch_dense(const Problem& p, int G, cudaStream_t s)
+template <int BITS, int G, template <int, int, int> class F, typename... Args>
+qg_status by_mp(int mp, Args&&... args)
 {
-    const int nt = nt_for(p.M);
-    if (G == 64) {
-        switch (nt) {
-            case 1: return dense_nt<BITS, 64, 1>(p, s);
-            case 2: return dense_nt<BITS, 64, 2>(p, s);
-            case 4: return dense_nt<BITS, 64, 4>(p, s);
-            default: return dense_nt<BITS, 64, 8>(p, s);
-        }
-    }
-    switch (nt) {
-        case 1: return dense_nt<BITS, 128, 1>(p, s);
-        case 2: return dense_nt<BITS, 128, 2>(p, s);
-        case 4: return dense_nt<BITS, 128, 4>(p, s);
-        default: return dense_nt<BITS, 128, 8>(p, s);
+    switch (mp) {
+        case 1: return F<BITS, G, 1>::run(args...);
+        case 2: return F<BITS, G, 2>::run(args...);
+        case 4: return F<BITS, G, 4>::run(args...);
+        case 8: return F<BITS, G, 8>::run(args...);
+        case 16: return F<BITS, G, 16>::run(args...);
+        case 32: return F<BITS, G, 32>::run(args...);
+        default: return F<BITS, G, 64>::run(args...);
     }
 }
 
-// t.chunk must be 8 * nt.  max_items bounds the device-built item count;
-// expect_items is the typical count (for choosing the K split).
+template <int BITS, int G, int MP>
+struct DenseF {
+    static qg_status run(const Problem& p, cudaStream_t s) { return dense_mp<BITS, G, MP>(p, s); }
+};
+template <int BITS, int G, int MP>
+struct GroupedF {
+    static qg_status run(const MoeTable& t, int mi, int ei, cudaStream_t s) { return grouped_mp<BITS, G, MP>(t, mi, ei, s); }
+};
+
 template <int BITS>
-qg_status launch_grouped(const MoeTable& t, int max_items, int expect_items, int G, int nt, cudaStream_t s)
+qg_status launch_dense(const Problem& p, int G, cudaStream_t s)
 {
-    if (G == 64) {
-        switch (nt) {
-            case 1: return grouped_nt<BITS, 64, 1>(t, max_items, expect_items, s);
-            case 2: return grouped_nt<BITS, 64, 2>(t, max_items, expect_items, s);
-            case 4: return grouped_nt<BITS, 64, 4>(t, max_items, expect_items, s);
-            default: return grouped_nt<BITS, 64, 8>(t, max_items, expect_items, s);
-        }
-    }
-    switch (nt) {
-        case 1: return grouped_nt<BITS, 128, 1>(t, max_items, expect_items, s);
-        case 2: return grouped_nt<BITS, 128, 2>(t, max_items, expect_items, s);
-        case 4: return grouped_nt<BITS, 128, 4>(t, max_items, expect_items, s);
-        default: return grouped_nt<BITS, 128, 8>(t, max_items, expect_items, s);
-    }
+    const int mp = mp_for(p.M);
+    return G == 64 ? by_mp<BITS, 64, DenseF>(mp, p, s) : by_mp<BITS, 128, DenseF>(mp, p, s);
+}
+
+// t.chunk must equal the padded token count mp.  max_items bounds the
+// device-built item count; expect_items is the typical count (for choosing
+// the K split).
+template <int BITS>
+qg_status launch_grouped(const MoeTable& t, int max_items, int expect_items, int G, int mp, cudaStream_t s)
+{
+    return G == 64 ? by_mp<BITS, 64, GroupedF>(mp, t, max_items, expect_items, s)
+                   : by_mp<BITS, 128, GroupedF>(mp, t, max_items, expect_items, s);
 }
 
 }  // namespace gemv

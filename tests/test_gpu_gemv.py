@@ -32,7 +32,7 @@ def _weights(N, K, bits, group, frac, seed):
 
 @pytest.mark.parametrize("bits", [2, 3, 4, 5, 6])
 @pytest.mark.parametrize("group", [64, 128])
-@pytest.mark.parametrize("M", [1, 5, 8, 16, 27, 64])
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8, 16, 27, 64])
 def test_product_small(qg, bits, group, M):
     N, K, frac = 200, 1024, 0.002            # N not a multiple of the 64-row tile
     q, wmax = _weights(N, K, bits, group, frac, seed=17 * bits + group)
