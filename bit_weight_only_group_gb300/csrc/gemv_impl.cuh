@@ -487,10 +487,11 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     if (S > 1) cluster.sync();
     else __syncthreads();
     const int rank = S > 1 ? (int)cluster.block_rank() : 0;
-    const int rows_per = kRowsPerCta / S;
+    // rank r finishes rows [r*64/S, (r+1)*64/S) of the tile
+    const int row_lo = rank * kRowsPerCta / S, rows_per = (rank + 1) * kRowsPerCta / S - row_lo;
     const int Mv = min(a.M, MP);
     for (int it = threadIdx.x; it < rows_per * Mv; it += blockDim.x) {
-        const int m = it / rows_per, rl = rank * rows_per + it % rows_per;
+        const int m = it / rows_per, rl = row_lo + it % rows_per;
         const int n = blockIdx.x * kRowsPerCta + rl;
         float v = 0.0f;
         for (int r = 0; r < S; r++) {
@@ -562,27 +563,17 @@ __global__ void __launch_bounds__(kWarps * 32) k_gemv_moe(const __grid_constant_
     gemv_body<BITS, G, MP>(p, splits, gpsplit);
 }
 
-// K split: the cluster size S in {1, 2, 4, 8} that best fills the SMs with
-// whole waves of CTAs; near-ties go to at least two CTAs per SM, then to the
-// smaller S.
+// K split: the cluster size S (1..8) that brings the grid closest to three
+// CTAs per SM (measured best for these streaming CTAs: fewer leave HBM idle,
+// more pay the per-CTA start-up and reduction latency more often), keeping
+// at least two groups per split.
 inline int choose_splits(long long ctas_per_split, int ng)
 {
-    const int sms = num_sms();
-    int best = 1;
-    double best_eff = -1.0;
-    bool best_two = false;
-    for (int S = 1; S <= 8; S *= 2) {
-        if (S > 1 && ng / S < 2) break;
-        const double u = (double)ctas_per_split * S / sms;
-        const double eff = u < 1.0 ? u : u / std::ceil(u);
-        const bool two = u >= 2.0;
-        if (eff > best_eff + 0.03 || (eff > best_eff - 0.03 && two && !best_two)) {
-            best = S;
-            best_eff = eff;
-            best_two = two;
-        }
-    }
-    return best;
+    const double target = 3.0 * num_sms();
+    int S = (int)std::lround(target / (double)std::max<long long>(1, ctas_per_split));
+    S = std::max(1, std::min(8, S));
+    while (S > 1 && ng / S < 2) S--;
+    return S;
 }
 
 // Padded token count of a launch.
