@@ -102,3 +102,35 @@ def test_product_4096(qg, bits, group, M):
     y = qg.qgemm_forward(x.cuda(), to_device(q))
     torch.cuda.synchronize()
     check_product(y, oracle.linear(x, q), x, wmax)
+
+
+@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("M,N,K", [(300, 600, 1024), (129, 256, 384), (1000, 700, 512)])
+def test_tensor_core_path_against_oracle(qg, group, M, N, K):
+    # M above the decode range runs the tcgen05 kernel (128 x 256 tiles, K in
+    # blocks of 64); ragged M and N exercise the zero-filled TMA edges
+    q, wmax = _weights(N, K, 4, group, 0.003, seed=M + N)
+    x = wl.gen_x(M, K, seed=M)
+    qd = to_device(q)
+    assert qg.qgemm_workspace_size(M, qd) > 0
+    y = qg.qgemm_forward(x.cuda(), qd)
+    yb = qg.qgemm_forward(x.cuda(), qd, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    check_product(y, oracle.linear(x, q), x, wmax)
+    assert torch.equal(yb, y.to(torch.bfloat16))
+
+
+def test_tensor_core_path_full_size_sampled(qg):
+    # the prefill shape of the 70B-shaped stack (M = 2048, 8192 x 8192, INT4
+    # group 128, 0.1 % outliers); the oracle checks sampled tokens and rows
+    M, N, K = 2048, 8192, 8192
+    W = wl.gen_weight(N, K, outlier_frac=0.001)
+    q = oracle.quantize(W, 4, 128, 0.001)
+    x = wl.gen_x(M, K)
+    y = qg.qgemm_forward(x.cuda(), to_device(q))
+    torch.cuda.synchronize()
+    toks = torch.arange(0, M, 97)
+    for n0 in (0, 4096 - 32, N - 64):
+        n1 = n0 + 64
+        wmax = float(np.abs(oracle.dequant(q, n0, n1)).max())
+        check_product(y[toks.cuda(), n0:n1], oracle.linear(x[toks], q, n0, n1), x[toks], wmax)
