@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--layers", type=int, default=80, help="layers of the 70B-shaped stack")
     ap.add_argument("--no-secondary", action="store_true", help="skip the prefill and MoE lines")
+    ap.add_argument("--mode", choices=("all", "prefill", "moe"), default="all",
+                    help="'prefill' / 'moe': run only that measurement and print its object (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
     return ap.parse_args()
 
@@ -469,6 +471,11 @@ def main():
     import bit_weight_only_group_gb300 as qg
     qg.lib()
     P = peaks()
+    if args.mode != "all":
+        out = run_prefill(qg, args, P) if args.mode == "prefill" else run_moe(qg, args)
+        if rank == 0:
+            print(json.dumps(out))
+        return 0
     dec = run_decode(qg, args, world, rank, P)
     line = {"metric": METRIC, "value": round(dec["value"], 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dec["ms_per_step"], 4),

@@ -7,18 +7,22 @@
 // that structure written for sm_103a:
 //  * one CTA computes a 128 x 256 tile of y (128 tokens x 256 weight rows)
 //    with its fp32 accumulator in tensor memory (256 TMEM columns);
-//  * warp 8 (one lane) streams, per K block of 64, the fp16 x tile (TMA,
-//    128-byte swizzle) and the packed 4-bit weight tile (TMA, 256 rows x
-//    32 bytes) into a 3-stage shared-memory ring;
-//  * warps 0-7 (one weight row per thread) unpack the codes with byte
-//    permutes and masks into fp16 1024 + 2^p q, turn them into the exact
-//    integers q - zp with one packed FMA and multiply by the fp16 group scale
-//    (one rounding), patch the FP16 outliers of the block in place, and
-//    store the 256 x 64 fp16 tile in the K-major 128-byte-swizzled layout the
-//    tensor core reads;
-//  * warp 9 (one lane) issues four tcgen05.mma (M=128, N=256, K=16) per
-//    stage and commits them to the stage's "empty" barrier;
-//  * warps 0-7 then read the accumulator with tcgen05.ld and store y.
+//  * warp 16 (one lane) streams the fp16 x tiles (TMA, 128-byte swizzle,
+//    K blocks of 64) into a 3-deep ring and warp 17 the packed 4-bit weight
+//    tiles (TMA, 256 rows x 128 bytes = 4 K blocks, 128-byte swizzle) into a
+//    3-deep ring; each ring has its own full/empty mbarriers, so loads run
+//    ahead of the consumers;
+//  * warps 0-15 (two threads per weight row, 32 k each) unpack the codes with
+//    masks into fp16 1024 + 2^p q, turn them into the exact integers q - zp
+//    with one packed FMA and multiply by the fp16 group scale (one
+//    rounding), patch the FP16 outliers of the block in place, and store the
+//    256 x 64 fp16 tile in the K-major 128-byte-swizzled layout the tensor
+//    core reads (K order permuted inside blocks of 8, matching x);
+//    the fp16 tiles go to a 2-deep ring (the packed slot is released once
+//    the stores that consumed its codes are issued);
+//  * warp 18 (one lane) issues four tcgen05.mma (M=128, N=256, K=16) per K
+//    block and commits them to the x and fp16 rings' "empty" barriers;
+//  * warps 0-15 then read the accumulator with tcgen05.ld and store y.
 // Every mbarrier wait is bounded (a wait that gives up writes QG_ERR_TIMEOUT
 // into the workspace status word).  x is first converted bf16 -> fp16 into
 // the workspace (exact in fp16's normal range).
@@ -39,17 +43,23 @@ qg_status launch_gemv_chunked(const uint16_t* x, int M, int ldx, const qg_qweigh
 
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 3;
-constexpr int kDeqWarps = 8, kThreads = (kDeqWarps + 2) * 32;
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int SA = 3, SP = 3, SB = 2;   // ring depths: x tiles, packed tiles, fp16 weight tiles
+constexpr int PK = 4;                   // K blocks per packed tile (128-byte rows at 4 bits)
+constexpr int kDeqWarps = 16;
+constexpr int kWarpA = kDeqWarps, kWarpP = kDeqWarps + 1, kWarpMma = kDeqWarps + 2;
+constexpr int kThreads = (kDeqWarps + 3) * 32;
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB fp16
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB fp16
 
 template <int BITS>
 struct Cfg {
-    static constexpr int P_BYTES = BN * BK * BITS / 8;    // packed tile
+    static constexpr int P_BYTES = BN * PK * BK * BITS / 8;   // packed tile: 256 rows x 128 bytes
     static constexpr int P_ALIGNED = (P_BYTES + 1023) / 1024 * 1024;
-    static constexpr int STAGE = A_BYTES + B_BYTES + P_ALIGNED;
-    static constexpr int SMEM = STAGES * STAGE + 1024 /* barriers */ + 1024 /* alignment */;
+    static constexpr int OFF_B = SA * A_BYTES;
+    static constexpr int OFF_P = OFF_B + SB * B_BYTES;
+    static constexpr int OFF_BAR = OFF_P + SP * P_ALIGNED;
+    static constexpr int SMEM = OFF_BAR + 1024 /* barriers */ + 1024 /* alignment */;
 };
 
 struct Args {
@@ -73,21 +83,27 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b)
     return d;
 }
 
-// 8 consecutive 4-bit codes (one 32-bit word, code i at bits 4i) ->
-// 4 fp16 pairs ((q_2j - zp) * s, (q_2j+1 - zp) * s) in k order.
-__device__ __forceinline__ uint4 deq8_u4(uint32_t v, uint32_t zp_add, uint32_t s2)
+// 8 consecutive 4-bit codes (one 32-bit word, code i at bits 4i) -> 4 fp16
+// pairs (q - zp) * s in the order (c0, c4, c1, c5, c2, c6, c3, c7): masks
+// pick two codes 16 bits apart straight into fp16 1024 + 2^p q (p = 0 or 4),
+// one packed FMA makes them the exact integers q - zp and one packed multiply
+// applies the scale.  x is staged with its K positions permuted the same way
+// inside each block of 8 (the product does not depend on the order of k as
+// long as both operands agree).
+__device__ __forceinline__ uint4 deq8_u4(uint32_t v, uint32_t add_lo, uint32_t add_hi, uint32_t s2)
 {
-    constexpr uint32_t mul = 0x3C00u | (0x2C00u << 16);   // (1, 1/16)
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-        // byte j into bytes 0 and 2: low nibble -> low half, high nibble -> high half (<< 4)
-        const uint32_t u = __byte_perm(v, 0u, 0x4040u | (uint32_t)j | ((uint32_t)j << 8));
-        const uint32_t raw = (u & 0x00F0000Fu) | 0x64006400u;
-        o[j] = hmul2_u32(gemv::hfma2_u32(raw, mul, zp_add), s2);
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
+    constexpr uint32_t one = 0x3C003C00u, sixteenth = 0x2C002C00u;   // 1, 1/16
+    const uint32_t v8 = v >> 8;
+    const uint32_t r0 = (v & 0x000F000Fu) | 0x64006400u;
+    const uint32_t r1 = (v & 0x00F000F0u) | 0x64006400u;
+    const uint32_t r2 = (v8 & 0x000F000Fu) | 0x64006400u;
+    const uint32_t r3 = (v8 & 0x00F000F0u) | 0x64006400u;
+    return make_uint4(hmul2_u32(gemv::hfma2_u32(r0, one, add_lo), s2), hmul2_u32(gemv::hfma2_u32(r1, sixteenth, add_hi), s2),
+                      hmul2_u32(gemv::hfma2_u32(r2, one, add_lo), s2), hmul2_u32(gemv::hfma2_u32(r3, sixteenth, add_hi), s2));
 }
+
+// position of k (mod 8) inside a permuted block of 8: inverse of (0,4,1,5,2,6,3,7)
+__device__ __forceinline__ int perm8_pos(int k) { return ((k & 3) << 1) | ((k >> 2) & 1); }
 
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -99,34 +115,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_u32(smem);
-    const uint32_t bars = sbase + STAGES * C::STAGE;
+    const uint32_t bars = sbase + C::OFF_BAR;
+    // barriers: full/empty per ring slot, then the accumulator-ready barrier
     auto full_a = [&](int s) { return bars + 8 * s; };
-    auto full_b = [&](int s) { return bars + 8 * (STAGES + s); };
-    auto empty = [&](int s) { return bars + 8 * (2 * STAGES + s); };
-    const uint32_t acc_full = bars + 8 * (3 * STAGES);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + STAGES * C::STAGE + 8 * (3 * STAGES + 1));
-    auto a_tile = [&](int s) { return sbase + s * C::STAGE; };
-    auto b_tile = [&](int s) { return sbase + s * C::STAGE + A_BYTES; };
-    auto p_tile = [&](int s) { return smem + s * C::STAGE + A_BYTES + B_BYTES; };
+    auto empty_a = [&](int s) { return bars + 8 * (SA + s); };
+    auto full_p = [&](int s) { return bars + 8 * (2 * SA + s); };
+    auto empty_p = [&](int s) { return bars + 8 * (2 * SA + SP + s); };
+    auto full_b = [&](int s) { return bars + 8 * (2 * SA + 2 * SP + s); };
+    auto empty_b = [&](int s) { return bars + 8 * (2 * SA + 2 * SP + SB + s); };
+    const uint32_t acc_full = bars + 8 * (2 * SA + 2 * SP + 2 * SB);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * (2 * SA + 2 * SP + 2 * SB + 1));
+    auto a_tile = [&](int s) { return sbase + s * A_BYTES; };
+    auto b_tile = [&](int s) { return sbase + C::OFF_B + s * B_BYTES; };
+    auto p_tile = [&](int s) { return smem + C::OFF_P + s * C::P_ALIGNED; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
     const int KB = a.K / BK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; s++) {
-            ptx::mbar_init(full_a(s), 1);
-            ptx::mbar_init(full_b(s), kDeqWarps);
-            ptx::mbar_init(empty(s), 1);
-        }
+        for (int s = 0; s < SA; s++) { ptx::mbar_init(full_a(s), 1); ptx::mbar_init(empty_a(s), 1); }
+        for (int s = 0; s < SP; s++) { ptx::mbar_init(full_p(s), 1); ptx::mbar_init(empty_p(s), kDeqWarps); }
+        for (int s = 0; s < SB; s++) { ptx::mbar_init(full_b(s), kDeqWarps); ptx::mbar_init(empty_b(s), 1); }
         ptx::mbar_init(acc_full, 1);
         ptx::fence_mbar_init();
     }
-    if (warp == kDeqWarps + 1) {
+    if (warp == kWarpMma) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 256);
         ptx::tmem_relinquish();
     }
-    if (warp == kDeqWarps && lane == 0) {
+    if (warp == kWarpA && lane == 0) {
         ptx::prefetch_tensormap(&xmap);
         ptx::prefetch_tensormap(&wmap);
     }
@@ -136,53 +154,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
 
-    if (warp == kDeqWarps) {
-        // ------------------------------------------------ TMA producer
+    if (warp == kWarpA) {
+        // ------------------------------------------------ x tiles (TMA)
         if (lane == 0) {
             for (int kb = 0; kb < KB; kb++) {
-                const int s = kb % STAGES;
-                const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-                if (!ptx::mbar_wait(empty(s), ph ^ 1u)) { ok = false; break; }
-                ptx::mbar_expect_tx(full_a(s), A_BYTES + C::P_BYTES);
+                const int s = kb % SA;
+                const uint32_t ph = (uint32_t)(kb / SA) & 1u;
+                if (!ptx::mbar_wait(empty_a(s), ph ^ 1u)) { ok = false; break; }
+                ptx::mbar_expect_tx(full_a(s), A_BYTES);
                 ptx::tma_load_2d(a_tile(s), &xmap, kb * BK, m0, full_a(s));
-                ptx::tma_load_2d(ptx::smem_u32(p_tile(s)), &wmap, kb * (BK * BITS / 8), n0, full_a(s));
             }
         }
-    } else if (warp == kDeqWarps + 1) {
+    } else if (warp == kWarpP) {
+        // ------------------------------------------------ packed weight tiles (TMA, PK K blocks each)
+        if (lane == 0) {
+            const int KP = (KB + PK - 1) / PK;
+            for (int kp = 0; kp < KP; kp++) {
+                const int s = kp % SP;
+                const uint32_t ph = (uint32_t)(kp / SP) & 1u;
+                if (!ptx::mbar_wait(empty_p(s), ph ^ 1u)) { ok = false; break; }
+                ptx::mbar_expect_tx(full_p(s), C::P_BYTES);
+                ptx::tma_load_2d(ptx::smem_u32(p_tile(s)), &wmap, kp * (PK * BK * BITS / 8), n0, full_p(s));
+            }
+        }
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_f16_f32(BM, BN);
             for (int kb = 0; kb < KB; kb++) {
-                const int s = kb % STAGES;
-                const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-                if (!ptx::mbar_wait(full_a(s), ph) || !ptx::mbar_wait(full_b(s), ph)) { ok = false; break; }
+                const int sa = kb % SA, sb = kb % SB;
+                if (!ptx::mbar_wait(full_a(sa), (uint32_t)(kb / SA) & 1u) ||
+                    !ptx::mbar_wait(full_b(sb), (uint32_t)(kb / SB) & 1u)) { ok = false; break; }
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; kk++)
-                    ptx::mma_f16(tmem, ptx::sw128_desc(a_tile(s) + 32 * kk), ptx::sw128_desc(b_tile(s) + 32 * kk), idesc,
-                                 (kb | kk) != 0);
-                ptx::tc_commit(empty(s));
+                    ptx::mma_f16(tmem, ptx::sw128_desc(a_tile(sa) + 32 * kk), ptx::sw128_desc(b_tile(sb) + 32 * kk),
+                                 idesc, (kb | kk) != 0);
+                ptx::tc_commit(empty_a(sa));
+                ptx::tc_commit(empty_b(sb));
             }
             ptx::tc_commit(acc_full);
         }
     } else {
-        // ------------------------------------------------ dequantization (one row per thread)
-        const int r = threadIdx.x;                      // 0..255
+        // ------------------------------------------------ dequantization (two threads per row)
+        // with SB == 2 and PK == 4, the fp16 slot (kb % 2) and its parity
+        // ((kb / 2) & 1) depend only on sub = kb % 4: compile-time below
+        static_assert(SB == 2 && PK == 4, "fp16 ring indices below assume SB == 2, PK == 4");
+        const int r = threadIdx.x >> 1;                 // 0..255
+        const int hk = threadIdx.x & 1;                 // which 32 k of the block
         const int nr = n0 + r;
         const int n = min(nr, a.N - 1);
-        const size_t pbase = (size_t)n * a.ng;
-        // per-group parameters, fetched two groups ahead
+        const uint16_t* sp_row = a.scale + (size_t)n * a.ng;
+        const uint8_t* zp_row = a.zp + (size_t)n * a.ng;
         constexpr int KB_PER_G = G / BK;                // 1 or 2
         const int ng = a.ng;
-        uint32_t sc[3], zq[3];
-        auto fetch = [&](int gi, int slot) {
-            if (gi < ng) {
-                sc[slot] = __ldg(a.scale + pbase + gi);
-                zq[slot] = __ldg(a.zp + pbase + gi);
-            }
-        };
-        fetch(0, 0);
-        fetch(1, 1);
+        // parameters of the current group and the next one (prefetched)
+        uint32_t sc_cur = __ldg(sp_row), zq_cur = __ldg(zp_row);
+        uint32_t sc_nxt = ng > 1 ? __ldg(sp_row + 1) : 0u, zq_nxt = ng > 1 ? __ldg(zp_row + 1) : 0u;
         // outlier cursor of this row
         int op = 0, oe = 0, ocol = 0x7FFFFFFF;
         uint16_t oval = 0;
@@ -194,51 +222,80 @@ __global__ void __launch_bounds__(kThreads, 1)
                 oval = a.val[op];
             }
         }
-        const uint32_t brow = r * 128, bsw = r & 7;
-        for (int kb = 0; kb < KB; kb++) {
-            const int s = kb % STAGES;
-            const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-            const int gi = kb / KB_PER_G;
-            const int slot = gi % 3;
-            if (kb % KB_PER_G == 0) fetch(gi + 2, (gi + 2) % 3);
-            const uint32_t zp = zq[slot];
-            const uint32_t zp_add = zp * (1u | (16u << 16)) + (0xE400u | (0xD400u << 16));
-            const uint32_t s1 = sc[slot] & 0xFFFFu;
-            const uint32_t s2 = s1 | (s1 << 16);
-            if (!ptx::mbar_wait(full_a(s), ph)) { ok = false; break; }
-            const uint4* prow = reinterpret_cast<const uint4*>(p_tile(s) + r * 32);
-            const uint4 w01 = prow[0], w23 = prow[1];
-            const uint32_t wv[8] = {w01.x, w01.y, w01.z, w01.w, w23.x, w23.y, w23.z, w23.w};
-            unsigned char* bt = smem + s * C::STAGE + A_BYTES;
+        // swizzled offsets, fixed per thread: source chunk (2*sub + hk) of the
+        // packed row, destination chunks (4*hk + j) of the fp16 row
+        const uint32_t rsw = r & 7;
+        uint32_t src_off[PK], dst_off[4];
 #pragma unroll
-            for (int c = 0; c < 8; c++) {
-                const uint4 h = deq8_u4(wv[c], zp_add, s2);
-                *reinterpret_cast<uint4*>(bt + brow + ((c ^ bsw) << 4)) = h;
-            }
-            // FP16 outliers of this block: the dense value there is exactly 0
-            const int k0 = kb * BK;
-            while (ocol < k0 + BK) {
-                const int kk = ocol - k0;
-                *reinterpret_cast<uint16_t*>(bt + brow + (((kk >> 3) ^ bsw) << 4) + ((kk & 7) << 1)) = oval;
-                if (++op < oe) {
-                    ocol = a.col[op];
-                    oval = a.val[op];
-                } else {
-                    ocol = 0x7FFFFFFF;
+        for (int sub = 0; sub < PK; sub++) src_off[sub] = r * 128 + (((2 * sub + hk) ^ rsw) << 4);
+#pragma unroll
+        for (int j = 0; j < 4; j++) dst_off[j] = r * 128 + (((4 * hk + j) ^ rsw) << 4);
+        unsigned char* const btile0 = smem + C::OFF_B;
+        const int KP = (KB + PK - 1) / PK;
+        for (int kp = 0; kp < KP && ok; kp++) {
+            const int sp = kp % SP;
+            const unsigned char* pt = p_tile(sp);
+            if (!ptx::mbar_wait(full_p(sp), (uint32_t)(kp / SP) & 1u)) { ok = false; break; }
+#pragma unroll
+            for (int sub = 0; sub < PK; sub++) {
+                const int kb = kp * PK + sub;
+                if (kb >= KB) break;
+                const int sb = sub % SB;                 // kb % 2 == sub % 2
+                const uint32_t eparity = ((uint32_t)(sub / SB) & 1u) ^ 1u;   // ((kb / 2) & 1) ^ 1
+                if (kb > 0 && kb % KB_PER_G == 0) {      // next group
+                    const int gi = kb / KB_PER_G;
+                    sc_cur = sc_nxt;
+                    zq_cur = zq_nxt;
+                    if (gi + 1 < ng) {
+                        sc_nxt = __ldg(sp_row + gi + 1);
+                        zq_nxt = __ldg(zp_row + gi + 1);
+                    }
+                }
+                const uint32_t add_lo = zq_cur * 0x00010001u + 0xE400E400u;   // -(1024 + zp)
+                const uint32_t add_hi = zq_cur * 0x00100010u + 0xD400D400u;   // -(64 + zp)
+                const uint32_t s2 = __byte_perm(sc_cur, 0u, 0x1010u);
+                const uint4 w = *reinterpret_cast<const uint4*>(pt + src_off[sub]);
+                if (!ptx::mbar_wait(empty_b(sb), eparity)) { ok = false; break; }
+                unsigned char* bt = btile0 + sb * B_BYTES;
+                *reinterpret_cast<uint4*>(bt + dst_off[0]) = deq8_u4(w.x, add_lo, add_hi, s2);
+                *reinterpret_cast<uint4*>(bt + dst_off[1]) = deq8_u4(w.y, add_lo, add_hi, s2);
+                *reinterpret_cast<uint4*>(bt + dst_off[2]) = deq8_u4(w.z, add_lo, add_hi, s2);
+                *reinterpret_cast<uint4*>(bt + dst_off[3]) = deq8_u4(w.w, add_lo, add_hi, s2);
+                // FP16 outliers in this thread's 32 k: the dense value there is exactly 0
+                const int k0 = kb * BK + 32 * hk;
+                while (ocol < k0 + 32) {
+                    if (ocol >= k0) {
+                        const int kk = ocol - kb * BK;
+                        *reinterpret_cast<uint16_t*>(bt + r * 128 + (((kk >> 3) ^ rsw) << 4) + (perm8_pos(kk) << 1)) = oval;
+                    }
+                    if (++op < oe) {
+                        ocol = a.col[op];
+                        oval = a.val[op];
+                    } else {
+                        ocol = 0x7FFFFFFF;
+                    }
+                }
+                ptx::fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::mbar_arrive(full_b(sb));
+                    // the packed slot goes back to its producer only after the
+                    // stores that consumed its codes: a shared load of the
+                    // whole warp completes in several wavefronts, and a
+                    // release right after issuing it let the next TMA tile
+                    // overwrite rows that the later lanes had not read yet
+                    if (sub == PK - 1 || kb == KB - 1) ptx::mbar_arrive(empty_p(sp));
                 }
             }
-            ptx::fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(full_b(s));
         }
         // ------------------------------------------------ epilogue: TMEM -> y
         if (ok && ptx::mbar_wait(acc_full, 0)) {
             ptx::tc_fence_after();
-            const int q = warp & 3, half = warp >> 2;
+            const int q = warp & 3, quarter = warp >> 2;   // TMEM lanes 32q.., columns 64*quarter..
             const int m = m0 + 32 * q + lane;
 #pragma unroll 1
-            for (int i = 0; i < 8; i++) {
-                const int cb = 128 * half + 16 * i;
+            for (int i = 0; i < 4; i++) {
+                const int cb = 64 * quarter + 16 * i;
                 uint32_t v[16];
                 ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)cb, v);
                 ptx::tmem_ld_wait();
@@ -273,10 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (warp == kDeqWarps + 1) ptx::tmem_dealloc(tmem, 256);
+    if (warp == kWarpMma) ptx::tmem_dealloc(tmem, 256);
 }
 
-// bf16 [M, ldx] -> fp16 [M, K] (exact for |x| in fp16's normal range)
+// bf16 [M, ldx] -> fp16 [M, K] (exact for |x| in fp16's normal range), with
+// the K positions of every block of 8 in the order (0,4,1,5,2,6,3,7) the
+// weight operand uses.
 __global__ void k_x_to_f16(const __nv_bfloat16* __restrict__ x, int M, int K, int ldx, __half* __restrict__ out)
 {
     const long long total8 = (long long)M * K / 8;
@@ -285,9 +344,10 @@ __global__ void k_x_to_f16(const __nv_bfloat16* __restrict__ x, int M, int K, in
         const long long e = i * 8;
         const int m = (int)(e / K), k = (int)(e % K);
         const __nv_bfloat16* src = x + (size_t)m * ldx + k;
+        constexpr int perm[8] = {0, 4, 1, 5, 2, 6, 3, 7};
         __half h[8];
 #pragma unroll
-        for (int j = 0; j < 8; j++) h[j] = __float2half_rn(__bfloat162float(src[j]));
+        for (int j = 0; j < 8; j++) h[j] = __float2half_rn(__bfloat162float(src[perm[j]]));
         *reinterpret_cast<uint4*>(out + e) = *reinterpret_cast<const uint4*>(h);
     }
 }
@@ -349,7 +409,7 @@ qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, i
                              (uint64_t)w.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != QG_OK) return st;
     st = encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.packed, (uint64_t)w.K / 2, (uint64_t)w.N,
-                   (uint64_t)w.K / 2, BK / 2, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+                   (uint64_t)w.K / 2, PK * BK / 2, BN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != QG_OK) return st;
     Args a;
     a.M = M; a.N = w.N; a.K = w.K; a.ng = w.K / G;

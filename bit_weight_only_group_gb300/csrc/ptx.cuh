@@ -8,11 +8,12 @@
 namespace qg {
 namespace ptx {
 
-// Upper bound on polls of one mbarrier wait.  try_wait itself suspends the
-// thread for a while between polls, so this is many seconds: a wait that
-// runs out means something is broken, and the caller reports it instead of
-// hanging.
-constexpr uint32_t kSpinLimit = 1u << 24;
+// Upper bound on polls of one mbarrier wait.  Each poll may suspend the
+// thread for up to kSuspendNs while the phase is incomplete, so the bound is
+// seconds: a wait that runs out means something is broken, and the caller
+// reports it instead of hanging.
+constexpr uint32_t kSpinLimit = 1u << 16;
+constexpr uint32_t kSuspendNs = 100000;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
@@ -45,9 +46,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     for (uint32_t it = 0; it < kSpinLimit; it++) {
         uint32_t ok;
         asm volatile(
-            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
             : "=r"(ok)
-            : "r"(bar), "r"(parity)
+            : "r"(bar), "r"(parity), "r"(kSuspendNs)
             : "memory");
         if (ok) return true;
     }
