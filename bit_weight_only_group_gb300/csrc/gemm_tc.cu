@@ -5,23 +5,25 @@
 // The pages' fused kernel dequantizes INT4 tiles into shared memory and runs
 // the tensor cores on them (bjdmk.com.cn 5414039 page, section 3); this is
 // that structure written for sm_103a:
-//  * one CTA computes a 128 x 256 tile of y (128 tokens x 256 weight rows)
-//    with its fp32 accumulator in tensor memory (256 TMEM columns);
+//  * one CTA computes a 256 x 256 tile of y (256 tokens x 256 weight rows)
+//    as two fp32 accumulators of 128 tokens in tensor memory (all 512 TMEM
+//    columns), so every dequantized weight tile feeds 256 tokens;
 //  * warp 16 (one lane) streams the fp16 x tiles (TMA, 128-byte swizzle,
-//    K blocks of 64) into a 3-deep ring and warp 17 the packed 4-bit weight
-//    tiles (TMA, 256 rows x 128 bytes = 4 K blocks, 128-byte swizzle) into a
-//    3-deep ring; each ring has its own full/empty mbarriers, so loads run
-//    ahead of the consumers;
+//    256 x 64) into a 2-deep ring and warp 17 the packed 4-bit weight tiles
+//    (TMA, 256 rows x 128 bytes = 4 K blocks, 128-byte swizzle) into a 2-deep
+//    ring; each ring has its own full/empty mbarriers, so loads run ahead of
+//    the consumers;
 //  * warps 0-15 (two threads per weight row, 32 k each) unpack the codes with
 //    masks into fp16 1024 + 2^p q, turn them into the exact integers q - zp
 //    with one packed FMA and multiply by the fp16 group scale (one
 //    rounding), patch the FP16 outliers of the block in place, and store the
 //    256 x 64 fp16 tile in the K-major 128-byte-swizzled layout the tensor
 //    core reads (K order permuted inside blocks of 8, matching x);
-//    the fp16 tiles go to a 2-deep ring (the packed slot is released once
+//    the fp16 tiles go to a 3-deep ring (the packed slot is released once
 //    the stores that consumed its codes are issued);
-//  * warp 18 (one lane) issues four tcgen05.mma (M=128, N=256, K=16) per K
-//    block and commits them to the x and fp16 rings' "empty" barriers;
+//  * warp 18 (one lane) issues eight tcgen05.mma (M=128, N=256, K=16) per K
+//    block, four per accumulator, and commits them to the x and fp16
+//    rings' "empty" barriers;
 //  * warps 0-15 then read the accumulator with tcgen05.ld and store y.
 // Every mbarrier wait is bounded (a wait that gives up writes QG_ERR_TIMEOUT
 // into the workspace status word).  x is first converted bf16 -> fp16 into
@@ -43,13 +45,15 @@ qg_status launch_gemv_chunked(const uint16_t* x, int M, int ldx, const qg_qweigh
 
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int SA = 3, SP = 3, SB = 2;   // ring depths: x tiles, packed tiles, fp16 weight tiles
+constexpr int BM = 256, BN = 256, BK = 64;
+constexpr int MH = 128;                 // tokens per accumulator (one tcgen05.mma covers M = 128)
+constexpr int SA = 2, SP = 2, SB = 3;   // ring depths: x tiles, packed tiles, fp16 weight tiles
+constexpr int TMEM_COLS = 2 * BN;       // two fp32 accumulators of 128 x 256
 constexpr int PK = 4;                   // K blocks per packed tile (128-byte rows at 4 bits)
 constexpr int kDeqWarps = 16;
 constexpr int kWarpA = kDeqWarps, kWarpP = kDeqWarps + 1, kWarpMma = kDeqWarps + 2;
 constexpr int kThreads = (kDeqWarps + 3) * 32;
-constexpr int A_BYTES = BM * BK * 2;   // 16 KB fp16
+constexpr int A_BYTES = BM * BK * 2;   // 32 KB fp16
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB fp16
 
 template <int BITS>
@@ -141,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_mbar_init();
     }
     if (warp == kWarpMma) {
-        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 256);
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
         ptx::tmem_relinquish();
     }
     if (warp == kWarpA && lane == 0) {
@@ -157,49 +161,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpA) {
         // ------------------------------------------------ x tiles (TMA)
         if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
             for (int kb = 0; kb < KB; kb++) {
-                const int s = kb % SA;
-                const uint32_t ph = (uint32_t)(kb / SA) & 1u;
                 if (!ptx::mbar_wait(empty_a(s), ph ^ 1u)) { ok = false; break; }
                 ptx::mbar_expect_tx(full_a(s), A_BYTES);
                 ptx::tma_load_2d(a_tile(s), &xmap, kb * BK, m0, full_a(s));
+                if (++s == SA) { s = 0; ph ^= 1u; }
             }
         }
     } else if (warp == kWarpP) {
         // ------------------------------------------------ packed weight tiles (TMA, PK K blocks each)
         if (lane == 0) {
             const int KP = (KB + PK - 1) / PK;
+            int s = 0;
+            uint32_t ph = 0;
             for (int kp = 0; kp < KP; kp++) {
-                const int s = kp % SP;
-                const uint32_t ph = (uint32_t)(kp / SP) & 1u;
                 if (!ptx::mbar_wait(empty_p(s), ph ^ 1u)) { ok = false; break; }
                 ptx::mbar_expect_tx(full_p(s), C::P_BYTES);
                 ptx::tma_load_2d(ptx::smem_u32(p_tile(s)), &wmap, kp * (PK * BK * BITS / 8), n0, full_p(s));
+                if (++s == SP) { s = 0; ph ^= 1u; }
             }
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = ptx::idesc_f16_f32(BM, BN);
+            constexpr uint32_t idesc = ptx::idesc_f16_f32(MH, BN);
+            int sa = 0, sb = 0;
+            uint32_t pa = 0, pb = 0;
             for (int kb = 0; kb < KB; kb++) {
-                const int sa = kb % SA, sb = kb % SB;
-                if (!ptx::mbar_wait(full_a(sa), (uint32_t)(kb / SA) & 1u) ||
-                    !ptx::mbar_wait(full_b(sb), (uint32_t)(kb / SB) & 1u)) { ok = false; break; }
+                if (!ptx::mbar_wait(full_a(sa), pa) || !ptx::mbar_wait(full_b(sb), pb)) { ok = false; break; }
                 ptx::tc_fence_after();
+                // tokens [0, 128) into columns [0, 256), tokens [128, 256) into [256, 512):
+                // the fp16 weight tile is read by both
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; kk++)
-                    ptx::mma_f16(tmem, ptx::sw128_desc(a_tile(sa) + 32 * kk), ptx::sw128_desc(b_tile(sb) + 32 * kk),
-                                 idesc, (kb | kk) != 0);
+                for (int kk = 0; kk < BK / 16; kk++) {
+                    const uint64_t bd = ptx::sw128_desc(b_tile(sb) + 32 * kk);
+                    ptx::mma_f16(tmem, ptx::sw128_desc(a_tile(sa) + 32 * kk), bd, idesc, (kb | kk) != 0);
+                    ptx::mma_f16(tmem + BN, ptx::sw128_desc(a_tile(sa) + MH * 128 + 32 * kk), bd, idesc, (kb | kk) != 0);
+                }
                 ptx::tc_commit(empty_a(sa));
                 ptx::tc_commit(empty_b(sb));
+                if (++sa == SA) { sa = 0; pa ^= 1u; }
+                if (++sb == SB) { sb = 0; pb ^= 1u; }
             }
             ptx::tc_commit(acc_full);
         }
     } else {
         // ------------------------------------------------ dequantization (two threads per row)
-        // with SB == 2 and PK == 4, the fp16 slot (kb % 2) and its parity
-        // ((kb / 2) & 1) depend only on sub = kb % 4: compile-time below
-        static_assert(SB == 2 && PK == 4, "fp16 ring indices below assume SB == 2, PK == 4");
         const int r = threadIdx.x >> 1;                 // 0..255
         const int hk = threadIdx.x & 1;                 // which 32 k of the block
         const int nr = n0 + r;
@@ -232,16 +241,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 4; j++) dst_off[j] = r * 128 + (((4 * hk + j) ^ rsw) << 4);
         unsigned char* const btile0 = smem + C::OFF_B;
         const int KP = (KB + PK - 1) / PK;
+        int sp = 0, sb = 0;
+        uint32_t pp = 0, pb = 1;   // parities: full_p to wait for, empty_b to wait for
         for (int kp = 0; kp < KP && ok; kp++) {
-            const int sp = kp % SP;
             const unsigned char* pt = p_tile(sp);
-            if (!ptx::mbar_wait(full_p(sp), (uint32_t)(kp / SP) & 1u)) { ok = false; break; }
+            if (!ptx::mbar_wait(full_p(sp), pp)) { ok = false; break; }
 #pragma unroll
             for (int sub = 0; sub < PK; sub++) {
                 const int kb = kp * PK + sub;
                 if (kb >= KB) break;
-                const int sb = sub % SB;                 // kb % 2 == sub % 2
-                const uint32_t eparity = ((uint32_t)(sub / SB) & 1u) ^ 1u;   // ((kb / 2) & 1) ^ 1
                 if (kb > 0 && kb % KB_PER_G == 0) {      // next group
                     const int gi = kb / KB_PER_G;
                     sc_cur = sc_nxt;
@@ -255,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t add_hi = zq_cur * 0x00100010u + 0xD400D400u;   // -(64 + zp)
                 const uint32_t s2 = __byte_perm(sc_cur, 0u, 0x1010u);
                 const uint4 w = *reinterpret_cast<const uint4*>(pt + src_off[sub]);
-                if (!ptx::mbar_wait(empty_b(sb), eparity)) { ok = false; break; }
+                if (!ptx::mbar_wait(empty_b(sb), pb)) { ok = false; break; }
                 unsigned char* bt = btile0 + sb * B_BYTES;
                 *reinterpret_cast<uint4*>(bt + dst_off[0]) = deq8_u4(w.x, add_lo, add_hi, s2);
                 *reinterpret_cast<uint4*>(bt + dst_off[1]) = deq8_u4(w.y, add_lo, add_hi, s2);
@@ -286,18 +294,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // overwrite rows that the later lanes had not read yet
                     if (sub == PK - 1 || kb == KB - 1) ptx::mbar_arrive(empty_p(sp));
                 }
+                if (++sb == SB) { sb = 0; pb ^= 1u; }
             }
+            if (++sp == SP) { sp = 0; pp ^= 1u; }
         }
         // ------------------------------------------------ epilogue: TMEM -> y
         if (ok && ptx::mbar_wait(acc_full, 0)) {
             ptx::tc_fence_after();
-            const int q = warp & 3, quarter = warp >> 2;   // TMEM lanes 32q.., columns 64*quarter..
-            const int m = m0 + 32 * q + lane;
+            // warp w reads TMEM lanes 32 (w % 4) .. (the lanes a warp may
+            // access) and a quarter of the 512 columns
+            const int q = warp & 3, quarter = warp >> 2;
 #pragma unroll 1
-            for (int i = 0; i < 4; i++) {
-                const int cb = 64 * quarter + 16 * i;
+            for (int i = 0; i < 8; i++) {
+                const int col = 128 * quarter + 16 * i;       // 0..511
+                const int half = col / BN, cb = col % BN;
+                const int m = m0 + MH * half + 32 * q + lane;
                 uint32_t v[16];
-                ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)cb, v);
+                ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, v);
                 ptx::tmem_ld_wait();
                 if (m < a.M) {
                     const int nb = n0 + cb;
@@ -330,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (warp == kWarpMma) ptx::tmem_dealloc(tmem, 256);
+    if (warp == kWarpMma) ptx::tmem_dealloc(tmem, TMEM_COLS);
 }
 
 // bf16 [M, ldx] -> fp16 [M, K] (exact for |x| in fp16's normal range), with
