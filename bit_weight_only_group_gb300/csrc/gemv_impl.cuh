@@ -272,17 +272,22 @@ struct Cfg {
     static constexpr int TSTRIDE = 32;                            // bytes per token per step
     static constexpr int SSTRIDE = MP * TSTRIDE;                  // bytes per step
     static constexpr int GSTRIDE = STEPS * SSTRIDE;               // bytes per group
-    static constexpr int XS_BUDGET = 49152;
+    static constexpr int RED_BYTES = kRowsPerCta * NTOK * 4;     // this CTA's partial sums [64 rows][NTOK]
+    // split-K slots: rank r receives [S][ceil(64/S)][NTOK] partials of its rows (S <= 8)
+    static constexpr int SLOT_BYTES = (kRowsPerCta + 8) * NTOK * 4;
+    static constexpr int XS_BUDGET = 49152 - SLOT_BYTES;
     static constexpr int D = D_CLAMP < XS_BUDGET / GSTRIDE ? D_CLAMP : XS_BUDGET / GSTRIDE;
     static constexpr int XG = (XS_BUDGET / GSTRIDE) / D * D;      // groups per x block
-    static constexpr int RED_BYTES = kRowsPerCta * NTOK * 4;
     static_assert(XG >= D, "x block smaller than the prefetch ring");
-    // dynamic shared memory for a split of gpsplit groups
-    static int smem(int gpsplit)
+    // dynamic shared memory for a split of gpsplit groups: the x block (reused
+    // for the partial sums after the main loop), then the split-K slots,
+    // which other ranks may write while this CTA still reads x
+    __host__ __device__ static int slot_offset(int gpsplit)
     {
         const int xs = (gpsplit < XG ? gpsplit : XG) * GSTRIDE;
-        return xs > RED_BYTES ? xs : RED_BYTES;
+        return ((xs > RED_BYTES ? xs : RED_BYTES) + 15) / 16 * 16;
     }
+    static int smem(int gpsplit, int S) { return slot_offset(gpsplit) + (S > 1 ? SLOT_BYTES : 0); }
 };
 
 // Stage x[:, kbase : kbase + ngr*G] as fp16 in MMA B-fragment order: the
@@ -295,12 +300,12 @@ template <int BITS, int G, int MP>
 __device__ void stage_x(const Problem& a, int kbase, int ngr, unsigned char* xs)
 {
     using C = Cfg<BITS, G, MP>;
+    constexpr int NV = C::NC / 2;
     const int M = a.M;
     const int items = ngr * M * 4;
-    for (int it = threadIdx.x; it < items; it += blockDim.x) {
+    auto load = [&](int it, uint32_t (&v)[NV]) {
         const int t = it & 3, m = (it >> 2) % M, gi = (it >> 2) / M;
         const __nv_bfloat16* xr = a.x + (size_t)x_row(a, m) * a.ldx + kbase + gi * G + t * C::NC;
-        uint32_t v[C::NC / 2];
         if ((reinterpret_cast<uintptr_t>(xr) & 15u) == 0) {
 #pragma unroll
             for (int i = 0; i < C::NC / 8; i++) {
@@ -310,9 +315,12 @@ __device__ void stage_x(const Problem& a, int kbase, int ngr, unsigned char* xs)
         } else {
             const unsigned short* x16 = reinterpret_cast<const unsigned short*>(xr);
 #pragma unroll
-            for (int i = 0; i < C::NC / 2; i++)
+            for (int i = 0; i < NV; i++)
                 v[i] = (uint32_t)__ldg(x16 + 2 * i) | ((uint32_t)__ldg(x16 + 2 * i + 1) << 16);
         }
+    };
+    auto store = [&](int it, const uint32_t (&v)[NV]) {
+        const int t = it & 3, m = (it >> 2) % M, gi = (it >> 2) / M;
         auto f16 = [&](int c) -> uint32_t {   // bf16 -> fp32 (exact) -> fp16
             const uint32_t bits = (c & 1) ? (v[c >> 1] & 0xFFFF0000u) : (v[c >> 1] << 16);
             return __half_as_ushort(__float2half_rn(__uint_as_float(bits)));
@@ -325,7 +333,31 @@ __device__ void stage_x(const Problem& a, int kbase, int ngr, unsigned char* xs)
             *reinterpret_cast<uint2*>(dst + s * C::SSTRIDE) =
                 make_uint2(f16(e0.lo) | (f16(e0.hi) << 16), f16(e1.lo) | (f16(e1.hi) << 16));
         });
+    };
+    for (int it = threadIdx.x; it < items; it += blockDim.x) {
+        uint32_t v[NV];
+        load(it, v);
+        store(it, v);
     }
+}
+
+// Cluster barrier in two halves, and an fp32 add into another CTA's shared
+// memory (distributed shared memory of the thread-block cluster).
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_v4(const void* local_addr, int rank, float4 v)
+{
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local_addr));
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(r), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
 }
 
 template <int BITS, int G, int MP>
@@ -396,7 +428,35 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
         if (d < ngrp) issue(dc, dc);
     });
 
-    int xnext = 0;          // group index (relative) at which x is staged next
+    // FP16 outliers of the tile's rows: two threads per row, and the S CTAs of
+    // a cluster take every S-th pair of the row's entries, so the add-back is
+    // spread over every thread of the cluster.  The CSR bounds are read now
+    // and the first OU entries of each thread right after x is staged; only
+    // the x values they multiply are read after the main loop.
+    static_assert(kWarps * 32 == 2 * kRowsPerCta, "two threads per tile row");
+    constexpr int OU = 4;
+    const int o_row = threadIdx.x >> 1;
+    const int o_n = blockIdx.x * kRowsPerCta + o_row;
+    const int o_stride = 2 * splits;
+    int o_p = 0, o_end = 0;
+    if (a.nnz > 0 && o_n < a.N) {
+        o_p = __ldg(a.row_ptr + o_n) + 2 * (int)blockIdx.y + (int)(threadIdx.x & 1);
+        o_end = __ldg(a.row_ptr + o_n + 1);
+    }
+    int o_col[OU];
+    uint32_t o_val[OU];
+
+    const int S = splits;
+    if (ngrp > 0) stage_x<BITS, G, MP>(a, g_begin * G, min(C::XG, ngrp), smem);
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < OU; u++) {
+        const int p = o_p + u * o_stride;
+        o_col[u] = p < o_end ? __ldg(a.col + p) : -1;
+        o_val[u] = p < o_end ? __ldg(a.val + p) : 0u;
+    }
+
+    int xnext = C::XG;      // group index (relative) at which x is staged next
     uint32_t xoff = 0;      // byte offset of group jj inside the x block
     for (int jj = 0; jj < ngrp; jj += D) {
         if (jj == xnext) {
@@ -471,8 +531,15 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     }
 
     // ------------------------------------------------ split-K reduction + epilogue
+    // Partial sums of the tile go to shared memory (the x block is dead now)
+    // and the CTA's share of the outliers is added to them.  With a K split,
+    // rank r owns rows [r*64/S, (r+1)*64/S): every rank writes its partials of
+    // those rows into its own slot in rank r's shared memory (plain 16-byte
+    // remote stores), and after one cluster barrier the owner adds the S
+    // slots and stores its rows.
+    const int Mv = min(a.M, MP);
     __syncthreads();
-    float* yp = reinterpret_cast<float*>(smem);   // [64 rows][NTOK]
+    float* const yp = reinterpret_cast<float*>(smem);   // [64 rows][NTOK]
     const int rl0 = warp * 16 + gq;
 #pragma unroll
     for (int nt = 0; nt < NT; nt++) {
@@ -482,28 +549,65 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
         yp[(rl0 + 8) * C::NTOK + c] = yacc[nt][2];
         yp[(rl0 + 8) * C::NTOK + c + 1] = yacc[nt][3];
     }
-    cg::cluster_group cluster = cg::this_cluster();
-    const int S = splits;
-    if (S > 1) cluster.sync();
-    else __syncthreads();
-    const int rank = S > 1 ? (int)cluster.block_rank() : 0;
-    // rank r finishes rows [r*64/S, (r+1)*64/S) of the tile
-    const int row_lo = rank * kRowsPerCta / S, rows_per = (rank + 1) * kRowsPerCta / S - row_lo;
-    const int Mv = min(a.M, MP);
-    for (int it = threadIdx.x; it < rows_per * Mv; it += blockDim.x) {
-        const int m = it / rows_per, rl = row_lo + it % rows_per;
-        const int n = blockIdx.x * kRowsPerCta + rl;
-        float v = 0.0f;
-        for (int r = 0; r < S; r++) {
-            const float* src = S > 1 ? cluster.map_shared_rank(yp, r) : yp;
-            v += src[rl * C::NTOK + m];
+    __syncthreads();
+    for (int p = o_p;;) {
+        if (o_col[0] < 0) break;   // entries fill the slots in order
+        // tokens four at a time, so that all the x loads of a round are in flight together
+        constexpr int OM = MP < 4 ? MP : 4;
+        for (int mb = 0; mb < Mv; mb += OM) {
+            float xv[OM][OU];
+#pragma unroll
+            for (int i = 0; i < OM; i++) {
+                const int m = mb + i;
+                const __nv_bfloat16* xm = a.x + (size_t)x_row(a, min(m, Mv - 1)) * a.ldx;
+#pragma unroll
+                for (int u = 0; u < OU; u++) xv[i][u] = (m < Mv && o_col[u] >= 0) ? __bfloat162float(xm[o_col[u]]) : 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < OM; i++) {
+                float sum = 0.0f;
+#pragma unroll
+                for (int u = 0; u < OU; u++) sum = fmaf(xv[i][u], h2f((uint16_t)o_val[u]), sum);
+                if (mb + i < Mv) atomicAdd(&yp[o_row * C::NTOK + mb + i], sum);
+            }
         }
+        p += OU * o_stride;
+        if (p >= o_end) break;
+#pragma unroll
+        for (int u = 0; u < OU; u++) {
+            const int q = p + u * o_stride;
+            o_col[u] = q < o_end ? __ldg(a.col + q) : -1;
+            o_val[u] = q < o_end ? __ldg(a.val + q) : 0u;
+        }
+    }
+    __syncthreads();
+    const int rows_cap = (kRowsPerCta + S - 1) / S;
+    const float* slots = reinterpret_cast<const float*>(smem + C::slot_offset(gpsplit));   // [S][rows_cap][NTOK]
+    if (S > 1) {
+        const int me = (int)cluster_rank();
+        constexpr int Q = C::NTOK / 4;   // float4 per row
+        for (int j = threadIdx.x; j < kRowsPerCta * Q; j += blockDim.x) {
+            const int rl = j / Q, c4 = j % Q;
+            const int owner = (S * (rl + 1) - 1) / kRowsPerCta;
+            const int lr = rl - owner * kRowsPerCta / S;
+            const float4 v = *reinterpret_cast<const float4*>(yp + rl * C::NTOK + 4 * c4);
+            st_cluster_v4(slots + ((size_t)(me * rows_cap + lr) * C::NTOK + 4 * c4), owner, v);
+        }
+        cluster_arrive();
+        cluster_wait();
+    }
+    const int rank = S > 1 ? (int)cluster_rank() : 0;
+    const int row_lo = rank * kRowsPerCta / S, rows_per = (rank + 1) * kRowsPerCta / S - row_lo;
+    for (int it = threadIdx.x; it < rows_per * Mv; it += blockDim.x) {
+        const int m = it / rows_per, lr = it % rows_per, rl = row_lo + lr;
+        const int n = blockIdx.x * kRowsPerCta + rl;
         if (n < a.N) {
-            if (a.nnz > 0) {
-                const int pe = a.row_ptr[n + 1];
-                const __nv_bfloat16* xm = a.x + (size_t)x_row(a, m) * a.ldx;
-                for (int p = a.row_ptr[n]; p < pe; p++)
-                    v += __bfloat162float(xm[a.col[p]]) * h2f(a.val[p]);
+            float v;
+            if (S > 1) {
+                v = 0.0f;
+                for (int r = 0; r < S; r++) v += slots[(size_t)(r * rows_cap + lr) * C::NTOK + m];
+            } else {
+                v = yp[rl * C::NTOK + m];
             }
             const size_t yo = (size_t)y_row(a, m) * a.ldy + n;
             if (a.y_bf16)
@@ -512,7 +616,6 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
                 reinterpret_cast<float*>(a.y)[yo] = v;
         }
     }
-    if (S > 1) cluster.sync();   // keep this CTA's partials alive until every rank has read them
 }
 
 template <int BITS, int G, int MP>
@@ -585,7 +688,7 @@ qg_status launch_cluster(K kernel, const A& args, dim3 grid, int S, int gpsplit,
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kWarps * 32, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)Cfg<BITS, G, MP>::smem(gpsplit);
+    cfg.dynamicSmemBytes = (size_t)Cfg<BITS, G, MP>::smem(gpsplit, S);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
