@@ -217,18 +217,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* zp_row = a.zp + (size_t)n * a.ng;
         constexpr int KB_PER_G = G / BK;                // 1 or 2
         const int ng = a.ng;
-        // parameters of the current group and the next one (prefetched)
+        // parameters of the current group and of the next two (loads in flight)
         uint32_t sc_cur = __ldg(sp_row), zq_cur = __ldg(zp_row);
-        uint32_t sc_nxt = ng > 1 ? __ldg(sp_row + 1) : 0u, zq_nxt = ng > 1 ? __ldg(zp_row + 1) : 0u;
-        // outlier cursor of this row
-        int op = 0, oe = 0, ocol = 0x7FFFFFFF;
-        uint16_t oval = 0;
+        uint32_t sc_n1 = ng > 1 ? __ldg(sp_row + 1) : 0u, zq_n1 = ng > 1 ? __ldg(zp_row + 1) : 0u;
+        uint32_t sc_n2 = ng > 2 ? __ldg(sp_row + 2) : 0u, zq_n2 = ng > 2 ? __ldg(zp_row + 2) : 0u;
+        // outlier cursor of this row: the next entry (ocol, oval) and the one
+        // after it (ncol, nval), so that consuming an entry never waits for a load
+        int op = 0, oe = 0, ocol = 0x7FFFFFFF, ncol = 0x7FFFFFFF;
+        uint16_t oval = 0, nval = 0;
         if (a.nnz > 0 && nr < a.N) {
             op = a.row_ptr[n];
             oe = a.row_ptr[n + 1];
             if (op < oe) {
                 ocol = a.col[op];
                 oval = a.val[op];
+            }
+            if (op + 1 < oe) {
+                ncol = a.col[op + 1];
+                nval = a.val[op + 1];
             }
         }
         // swizzled offsets, fixed per thread: source chunk (2*sub + hk) of the
@@ -252,11 +258,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kb >= KB) break;
                 if (kb > 0 && kb % KB_PER_G == 0) {      // next group
                     const int gi = kb / KB_PER_G;
-                    sc_cur = sc_nxt;
-                    zq_cur = zq_nxt;
-                    if (gi + 1 < ng) {
-                        sc_nxt = __ldg(sp_row + gi + 1);
-                        zq_nxt = __ldg(zp_row + gi + 1);
+                    sc_cur = sc_n1;
+                    zq_cur = zq_n1;
+                    sc_n1 = sc_n2;
+                    zq_n1 = zq_n2;
+                    if (gi + 2 < ng) {
+                        sc_n2 = __ldg(sp_row + gi + 2);
+                        zq_n2 = __ldg(zp_row + gi + 2);
                     }
                 }
                 const uint32_t add_lo = zq_cur * 0x00010001u + 0xE400E400u;   // -(1024 + zp)
@@ -276,11 +284,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int kk = ocol - kb * BK;
                         *reinterpret_cast<uint16_t*>(bt + r * 128 + (((kk >> 3) ^ rsw) << 4) + (perm8_pos(kk) << 1)) = oval;
                     }
-                    if (++op < oe) {
-                        ocol = a.col[op];
-                        oval = a.val[op];
+                    ocol = ncol;
+                    oval = nval;
+                    if (++op + 1 < oe) {
+                        ncol = a.col[op + 1];
+                        nval = a.val[op + 1];
                     } else {
-                        ocol = 0x7FFFFFFF;
+                        ncol = 0x7FFFFFFF;
                     }
                 }
                 ptx::fence_proxy_async();
