@@ -22,6 +22,7 @@ on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -53,6 +54,22 @@ def parse():
                     help="'prefill' / 'moe': run only that measurement and print its object (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
     return ap.parse_args()
+
+
+# DRAM bytes (read + written) per 70B-shaped layer of the decode step, from one
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum over the 7
+# launches of a layer, profiles/k_gemv_decode_70b_stack_m1.md), valid only
+# for the kernel source it was taken on.
+DECODE_TRAFFIC = {"kernel_sha256": "9e7abb4bbec6f55570aacc0650cc7e5292300641869cfbf4e1f17552675fa5ca",
+                  "bytes_per_layer": 454.208e6}
+
+
+def decode_traffic(n_layers):
+    src = os.path.join(ROOT, "bit_weight_only_group_gb300", "csrc", "gemv_impl.cuh")
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != DECODE_TRAFFIC["kernel_sha256"]:
+            return None
+    return DECODE_TRAFFIC["bytes_per_layer"] * n_layers
 
 
 def peaks():
@@ -299,7 +316,8 @@ def run_decode(qg, args, world, rank, P):
 
     achieved = allb / per_step_s / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": P["hbm"], "unit": "GB/s",
-            "frac": round(achieved / P["hbm"], 4), "traffic": None,
+            "frac": round(achieved / P["hbm"], 4), "traffic": decode_traffic(len(layers) // 7),
+            "traffic_unit": "bytes per step (the achieved figure is per step: the step is 560 launches of this kernel)",
             "kernel": "k_gemv<4,128,1> (decode qGEMV, the only kernel of the step)",
             "peak_source": P["src"] + " hbm_gbs"}
     out = dict(value=value, ms_per_step=ms_max / args.steps, roofline=roof, e2e=e2e, clocks=clocks,
