@@ -40,6 +40,7 @@ gemv::Problem make_problem(const uint16_t* x, int M, int ldx, const qg_qweight& 
     p.val = w.out_val;
     p.nnz = w.nnz;
     p.y = y; p.ldy = ldy; p.y_bf16 = yt == QG_Y_BF16;
+    p.magic = gemv::kF16Magic;
     return p;
 }
 
@@ -192,6 +193,7 @@ qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const
     t.n_items = p.n_items;
     t.y = y;
     t.y_bf16 = yt == QG_Y_BF16;
+    t.magic = gemv::kF16Magic;
     for (int i = 0; i < E; i++) {
         t.packed[i] = experts[i].packed;
         t.scale[i] = experts[i].scale;

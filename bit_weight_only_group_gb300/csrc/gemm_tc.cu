@@ -78,6 +78,7 @@ struct Args {
     int ldy;
     int y_bf16;
     int* status;
+    uint32_t magic;   // gemv::kF16Magic, a run-time value (one logic op per code pair)
 };
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b)
@@ -94,14 +95,14 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b)
 // applies the scale.  x is staged with its K positions permuted the same way
 // inside each block of 8 (the product does not depend on the order of k as
 // long as both operands agree).
-__device__ __forceinline__ uint4 deq8_u4(uint32_t v, uint32_t add_lo, uint32_t add_hi, uint32_t s2)
+__device__ __forceinline__ uint4 deq8_u4(uint32_t v, uint32_t add_lo, uint32_t add_hi, uint32_t s2, uint32_t magic)
 {
     constexpr uint32_t one = 0x3C003C00u, sixteenth = 0x2C002C00u;   // 1, 1/16
     const uint32_t v8 = v >> 8;
-    const uint32_t r0 = (v & 0x000F000Fu) | 0x64006400u;
-    const uint32_t r1 = (v & 0x00F000F0u) | 0x64006400u;
-    const uint32_t r2 = (v8 & 0x000F000Fu) | 0x64006400u;
-    const uint32_t r3 = (v8 & 0x00F000F0u) | 0x64006400u;
+    const uint32_t r0 = gemv::and_or<0x000F000Fu>(v, magic);
+    const uint32_t r1 = gemv::and_or<0x00F000F0u>(v, magic);
+    const uint32_t r2 = gemv::and_or<0x000F000Fu>(v8, magic);
+    const uint32_t r3 = gemv::and_or<0x00F000F0u>(v8, magic);
     return make_uint4(hmul2_u32(gemv::hfma2_u32(r0, one, add_lo), s2), hmul2_u32(gemv::hfma2_u32(r1, sixteenth, add_hi), s2),
                       hmul2_u32(gemv::hfma2_u32(r2, one, add_lo), s2), hmul2_u32(gemv::hfma2_u32(r3, sixteenth, add_hi), s2));
 }
@@ -209,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------ dequantization (two threads per row)
+        const uint32_t magic = a.magic;
         const int r = threadIdx.x >> 1;                 // 0..255
         const int hk = threadIdx.x & 1;                 // which 32 k of the block
         const int nr = n0 + r;
@@ -273,10 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint4 w = *reinterpret_cast<const uint4*>(pt + src_off[sub]);
                 if (!ptx::mbar_wait(empty_b(sb), pb)) { ok = false; break; }
                 unsigned char* bt = btile0 + sb * B_BYTES;
-                *reinterpret_cast<uint4*>(bt + dst_off[0]) = deq8_u4(w.x, add_lo, add_hi, s2);
-                *reinterpret_cast<uint4*>(bt + dst_off[1]) = deq8_u4(w.y, add_lo, add_hi, s2);
-                *reinterpret_cast<uint4*>(bt + dst_off[2]) = deq8_u4(w.z, add_lo, add_hi, s2);
-                *reinterpret_cast<uint4*>(bt + dst_off[3]) = deq8_u4(w.w, add_lo, add_hi, s2);
+                *reinterpret_cast<uint4*>(bt + dst_off[0]) = deq8_u4(w.x, add_lo, add_hi, s2, magic);
+                *reinterpret_cast<uint4*>(bt + dst_off[1]) = deq8_u4(w.y, add_lo, add_hi, s2, magic);
+                *reinterpret_cast<uint4*>(bt + dst_off[2]) = deq8_u4(w.z, add_lo, add_hi, s2, magic);
+                *reinterpret_cast<uint4*>(bt + dst_off[3]) = deq8_u4(w.w, add_lo, add_hi, s2, magic);
                 // FP16 outliers in this thread's 32 k: the dense value there is exactly 0
                 const int k0 = kb * BK + 32 * hk;
                 while (ocol < k0 + 32) {
@@ -440,6 +442,7 @@ qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, i
     a.row_ptr = w.out_row_ptr; a.col = w.out_col; a.val = w.out_val; a.nnz = w.nnz;
     a.y = y; a.ldy = ldy; a.y_bf16 = yt == QG_Y_BF16;
     a.status = p.status;
+    a.magic = gemv::kF16Magic;
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(k_gemm_tc_u4<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);

@@ -144,13 +144,28 @@ __device__ __forceinline__ uint32_t zp_addend(uint32_t zp)
     return zp * mul + base;
 }
 
+// Exponent pattern of fp16 1024 in both halves.  The kernels receive it as a
+// run-time value (Problem::magic, Args::magic) so that it stays in a register:
+// (v & mask) | magic is then one three-input logic op, where two compile-time
+// 32-bit constants would not fit one instruction and cost two.
+constexpr uint32_t kF16Magic = 0x64006400u;
+
+// (a & MASK) | c in one lop3 (truth table 0xEA = (A & B) | C).
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c)
+{
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
+    return d;
+}
+
 template <int BITS, int NC, int E, int NW>
-__device__ __forceinline__ uint32_t deq_affine(const uint32_t (&w)[NW], uint32_t zp)
+__device__ __forceinline__ uint32_t deq_affine(const uint32_t (&w)[NW], uint32_t zp, uint32_t magic)
 {
     constexpr PairE p = plan_entry(BITS, NC, E);
     constexpr uint32_t cm = (1u << BITS) - 1u;
     constexpr uint32_t mask = (cm << p.plo) | (cm << (16 + p.phi));
-    const uint32_t raw = (window<p.S, NW>(w) & mask) | 0x64006400u;
+    const uint32_t raw = and_or<mask>(window<p.S, NW>(w), magic);
     constexpr uint32_t mul = (uint32_t)(0x3C00 - 0x400 * p.plo) | ((uint32_t)(0x3C00 - 0x400 * p.phi) << 16);
     return hfma2_u32(raw, mul, zp_addend<BITS, NC, E>(zp));
 }
@@ -253,6 +268,7 @@ struct Problem {
     void* y;
     int ldy;
     int y_bf16;
+    uint32_t magic;   // kF16Magic
 };
 
 __device__ __forceinline__ int x_row(const Problem& p, int m) { return p.rowmap ? p.rowmap[m] / p.xdiv : m; }
@@ -371,6 +387,7 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = lane & 3, gq = lane >> 2;
+    const uint32_t magic = a.magic;
     const int row_base = blockIdx.x * kRowsPerCta + warp * 16 + gq;
     const int r0 = min(row_base, a.N - 1), r1 = min(row_base + 8, a.N - 1);
     const int ng = a.K / G;
@@ -504,10 +521,10 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
                     const uint32_t z0 = prm[d][0][1], z1 = prm[d][1][1];
                     static_for<0, C::STEPS>([&](auto sc) {
                         constexpr int s = decltype(sc)::value;
-                        const uint32_t a0 = deq_affine<BITS, C::NC, 2 * s>(wr[d][0], z0);
-                        const uint32_t a1 = deq_affine<BITS, C::NC, 2 * s>(wr[d][1], z1);
-                        const uint32_t a2 = deq_affine<BITS, C::NC, 2 * s + 1>(wr[d][0], z0);
-                        const uint32_t a3 = deq_affine<BITS, C::NC, 2 * s + 1>(wr[d][1], z1);
+                        const uint32_t a0 = deq_affine<BITS, C::NC, 2 * s>(wr[d][0], z0, magic);
+                        const uint32_t a1 = deq_affine<BITS, C::NC, 2 * s>(wr[d][1], z1, magic);
+                        const uint32_t a2 = deq_affine<BITS, C::NC, 2 * s + 1>(wr[d][0], z0, magic);
+                        const uint32_t a3 = deq_affine<BITS, C::NC, 2 * s + 1>(wr[d][1], z1, magic);
 #pragma unroll
                         for (int nt = 0; nt < NT; nt++) {
                             const uint2 b = *reinterpret_cast<const uint2*>(xb[nt] + d * C::GSTRIDE + s * C::SSTRIDE);
@@ -638,6 +655,7 @@ struct MoeTable {
     const int* n_items;
     void* y;
     int y_bf16;
+    uint32_t magic;   // kF16Magic
     const uint8_t* packed[kMoeMaxExperts];
     const uint16_t* scale[kMoeMaxExperts];
     const uint8_t* zp[kMoeMaxExperts];
@@ -663,6 +681,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_gemv_moe(const __grid_constant_
     p.packed = t.packed[e]; p.scale = t.scale[e]; p.zp = t.zp[e]; p.cb = t.cb[e];
     p.row_ptr = t.row_ptr[e]; p.col = t.col[e]; p.val = t.val[e]; p.nnz = t.nnz[e];
     p.y = t.y; p.ldy = t.N; p.y_bf16 = t.y_bf16;
+    p.magic = t.magic;
     gemv_body<BITS, G, MP>(p, splits, gpsplit);
 }
 
