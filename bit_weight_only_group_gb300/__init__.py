@@ -31,7 +31,8 @@ Y_F32, Y_BF16 = 0, 1
 
 ABI_FUNCTIONS = ("qpack_query_sizes", "qpack_workspace_size", "qpack_quantize", "qpack_quantize_noalloc",
                  "qgemm_workspace_size",
-                 "qgemm_forward", "qgemm_moe_workspace_size", "qgemm_moe_grouped", "qgemm_last_error")
+                 "qgemm_forward", "qgemm_moe_workspace_size", "qgemm_moe_grouped", "qgemm_device_status",
+                 "qgemm_last_error")
 
 
 class QgError(RuntimeError):
@@ -70,6 +71,7 @@ def lib() -> ctypes.CDLL:
         L.qgemm_forward.argtypes = [vp, i32, i32, pq, vp, i32, ctypes.c_int, vp, sz, vp]
         L.qgemm_moe_workspace_size.argtypes = [i32, i32, i32, pq, psz]
         L.qgemm_moe_grouped.argtypes = [vp, i32, vp, i32, pq, i32, vp, ctypes.c_int, vp, sz, vp]
+        L.qgemm_device_status.argtypes = [pi32, i32]
         for name in ABI_FUNCTIONS[:-1]:
             getattr(L, name).restype = ctypes.c_int
         L.qgemm_last_error.argtypes = []
@@ -253,3 +255,11 @@ def qgemm_moe_grouped(x: torch.Tensor, topk_ids: torch.Tensor, experts, out: tor
     _check(lib().qgemm_moe_grouped(_ptr(x), T, _ptr(topk_ids), k, arr, len(experts), _ptr(out), yt,
                                    _ptr(workspace), workspace.numel(), _stream(stream)), "qgemm_moe_grouped")
     return out
+
+
+def qgemm_device_status(reset: bool = False) -> int:
+    """Status word of the decode kernels on the current device (0 = QG_OK,
+    QG_ERR_TIMEOUT after a bounded wait gave up).  Synchronizes the device."""
+    v = ctypes.c_int32(0)
+    _check(lib().qgemm_device_status(ctypes.byref(v), 1 if reset else 0), "qgemm_device_status")
+    return v.value

@@ -102,6 +102,16 @@ extern "C" {
 
 const char* qgemm_last_error(void) { return g_err; }
 
+qg_status qgemm_device_status(int32_t* status, int32_t reset)
+{
+    if (!status) return fail(QG_ERR_INVALID_ARG, "qgemm_device_status: status is NULL");
+    int v = 0;
+    qg_status st = read_device_status(&v, reset);
+    if (st != QG_OK) return st;
+    *status = v;
+    return QG_OK;
+}
+
 qg_status qpack_query_sizes(int32_t N, int32_t K, int32_t bits, int32_t group, float outlier_frac,
                             size_t* packed_bytes, size_t* scale_bytes, size_t* zp_bytes,
                             size_t* codebook_bytes, int32_t* nnz)

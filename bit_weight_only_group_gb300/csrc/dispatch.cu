@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "gemv_impl.cuh"
 #include "qg_internal.h"
@@ -21,6 +22,46 @@ extern template qg_status launch_grouped<4>(const MoeTable&, int, int, int, int,
 extern template qg_status launch_grouped<5>(const MoeTable&, int, int, int, int, cudaStream_t);
 extern template qg_status launch_grouped<6>(const MoeTable&, int, int, int, int, cudaStream_t);
 }  // namespace gemv
+
+// Device status word of the library's kernels (QG_OK, or QG_ERR_TIMEOUT after
+// a bounded wait gave up), one per device; kernels write it through a pointer
+// argument, qgemm_device_status() reads and clears it.
+__device__ int g_device_status;
+
+namespace {
+constexpr int kMaxStatusDevices = 64;
+std::mutex g_status_mu;
+int* g_status_addr[kMaxStatusDevices];
+}  // namespace
+
+int* device_status_ptr()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxStatusDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    if (!g_status_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        g_status_addr[dev] = static_cast<int*>(p);
+    }
+    return g_status_addr[dev];
+}
+
+qg_status read_device_status(int* out, int reset)
+{
+    int* p = device_status_ptr();
+    if (!p) return fail(QG_ERR_CUDA, "qgemm_device_status: no device status word on the current device");
+    int v = 0;
+    cudaError_t e = cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "qgemm_device_status: read");
+    if (reset && v != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "qgemm_device_status: reset");
+    }
+    *out = v;
+    return QG_OK;
+}
 
 namespace {
 

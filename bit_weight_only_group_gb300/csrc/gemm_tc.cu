@@ -26,8 +26,8 @@
 //    rings' "empty" barriers;
 //  * warps 0-15 then read the accumulator with tcgen05.ld and store y.
 // Every mbarrier wait is bounded (a wait that gives up writes QG_ERR_TIMEOUT
-// into the workspace status word).  x is first converted bf16 -> fp16 into
-// the workspace (exact in fp16's normal range).
+// into the device status word read by qgemm_device_status).  x is first
+// converted bf16 -> fp16 into the workspace (exact in fp16's normal range).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
@@ -42,6 +42,29 @@ namespace qg {
 
 qg_status launch_gemv_chunked(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,
                               qg_ydtype yt, cudaStream_t s);
+
+qg_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f)
+            return fail(QG_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(QG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return QG_OK;
+}
+
 
 namespace tc {
 
@@ -351,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
         }
     }
-    if (!ok) atomicExch(a.status, (int)QG_ERR_TIMEOUT);
+    if (!ok && a.status) atomicExch(a.status, (int)QG_ERR_TIMEOUT);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -377,41 +400,15 @@ __global__ void k_x_to_f16(const __nv_bfloat16* __restrict__ x, int M, int K, in
     }
 }
 
-qg_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
-                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw)
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
-        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f)
-            return fail(QG_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(QG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-    return QG_OK;
-}
-
+// Workspace: x converted to fp16 (K order permuted), M x K.
 struct Ws {
-    int* status;
     __half* x16;
 };
 
 size_t ws_layout(int M, int K, Ws* w, void* base)
 {
-    const size_t o_x = 256;
-    const size_t total = align_up(o_x + (size_t)M * K * 2, 256);
-    if (w && base) {
-        w->status = reinterpret_cast<int*>(base);
-        w->x16 = reinterpret_cast<__half*>(static_cast<char*>(base) + o_x);
-    }
+    const size_t total = align_up((size_t)M * K * 2, 256);
+    if (w && base) w->x16 = reinterpret_cast<__half*>(base);
     return total;
 }
 
@@ -441,13 +438,11 @@ qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, i
     a.scale = w.scale; a.zp = w.zp;
     a.row_ptr = w.out_row_ptr; a.col = w.out_col; a.val = w.out_val; a.nnz = w.nnz;
     a.y = y; a.ldy = ldy; a.y_bf16 = yt == QG_Y_BF16;
-    a.status = p.status;
+    a.status = device_status_ptr();
     a.magic = gemv::kF16Magic;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc_u4<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel: shared memory attribute");
-        attr = true;
+    {
+        qg_status st2 = gemv::allow_smem(k_gemm_tc_u4<G>, C::SMEM);
+        if (st2 != QG_OK) return st2;
     }
     dim3 grid((unsigned)ceil_div(M, BM), (unsigned)ceil_div(w.N, BN), 1);
     k_gemm_tc_u4<G><<<grid, kThreads, C::SMEM, s>>>(xmap, wmap, a);

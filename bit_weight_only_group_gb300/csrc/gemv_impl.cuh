@@ -34,13 +34,16 @@
 #include <cuda_fp16.h>
 
 #include <cmath>
+#include <mutex>
 #include <type_traits>
 
+#include "ptx.cuh"
 #include "qg_internal.h"
 
 namespace cg = cooperative_groups;
 
 namespace qg {
+
 namespace gemv {
 
 constexpr int kWarps = 4;
@@ -313,7 +316,7 @@ struct Cfg {
 // values, then one 8-byte store per step.  Tokens M..MP-1 are not written:
 // the MMA columns that read them are never stored.
 template <int BITS, int G, int MP>
-__device__ void stage_x(const Problem& a, int kbase, int ngr, unsigned char* xs)
+__device__ void stage_x(const Problem& a, int kbase, int ngr, unsigned char* xs, int nthr)
 {
     using C = Cfg<BITS, G, MP>;
     constexpr int NV = C::NC / 2;
@@ -350,10 +353,75 @@ __device__ void stage_x(const Problem& a, int kbase, int ngr, unsigned char* xs)
                 make_uint2(f16(e0.lo) | (f16(e0.hi) << 16), f16(e1.lo) | (f16(e1.hi) << 16));
         });
     };
-    for (int it = threadIdx.x; it < items; it += blockDim.x) {
+    for (int it = threadIdx.x; it < items; it += nthr) {
         uint32_t v[NV];
         load(it, v);
         store(it, v);
+    }
+}
+
+// One group of two weight rows (w0: row r0, w1: row r1 of the thread's
+// A-fragment rows, NW words each) against the staged x block of that group:
+// dequantize to fp16 MMA operands and accumulate into yacc.  pr holds the
+// rows' parameters: affine (scale bits, zero-point), codebook (two words of
+// four fp16 entries).
+template <int BITS, int G, int MP>
+__device__ __forceinline__ void mma_group(const uint32_t (&w0)[Chunk<BITS, G>::NW], const uint32_t (&w1)[Chunk<BITS, G>::NW],
+                                          const uint32_t (&pr)[2][2],
+                                          const unsigned char* const (&xg)[Cfg<BITS, G, MP>::NT],
+                                          float (&yacc)[Cfg<BITS, G, MP>::NT][4], uint32_t magic)
+{
+    using C = Cfg<BITS, G, MP>;
+    constexpr int NW = C::NW, NT = C::NT;
+    if constexpr (BITS == 2) {
+        // per-row lookup tables: low bytes and high bytes of the 4 entries
+        const uint32_t L0 = __byte_perm(pr[0][0], pr[0][1], 0x6420);
+        const uint32_t H0 = __byte_perm(pr[0][0], pr[0][1], 0x7531);
+        const uint32_t L1 = __byte_perm(pr[1][0], pr[1][1], 0x6420);
+        const uint32_t H1 = __byte_perm(pr[1][0], pr[1][1], 0x7531);
+        static_for<0, NW>([&](auto wc) {
+            constexpr int wi = decltype(wc)::value;
+            static_for<0, 4>([&](auto jc) {
+                constexpr int jf = decltype(jc)::value;
+                const uint32_t f0 = (w0[wi] >> (2 * jf)) & 0x03030303u;
+                const uint32_t f1 = (w1[wi] >> (2 * jf)) & 0x03030303u;
+                const uint32_t s0l = f0 * 0x11u + 0x4040u, s0h = __umulhi(f0, 0x00110000u) + 0x4040u;
+                const uint32_t s1l = f1 * 0x11u + 0x4040u, s1h = __umulhi(f1, 0x00110000u) + 0x4040u;
+                const uint32_t a0 = __byte_perm(L0, H0, s0l), a2 = __byte_perm(L0, H0, s0h);
+                const uint32_t a1 = __byte_perm(L1, H1, s1l), a3 = __byte_perm(L1, H1, s1h);
+                constexpr int s = 4 * wi + jf;   // entries 2s (lo) and 2s+1 (hi)
+#pragma unroll
+                for (int nt = 0; nt < NT; nt++) {
+                    const uint2 b = *reinterpret_cast<const uint2*>(xg[nt] + s * C::SSTRIDE);
+                    mma16816(yacc[nt], a0, a1, a2, a3, b.x, b.y);
+                }
+            });
+        });
+    } else {
+        float acc[NT][4];
+#pragma unroll
+        for (int i = 0; i < NT; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+        const uint32_t z0 = pr[0][1], z1 = pr[1][1];
+        static_for<0, C::STEPS>([&](auto sc) {
+            constexpr int s = decltype(sc)::value;
+            const uint32_t a0 = deq_affine<BITS, C::NC, 2 * s>(w0, z0, magic);
+            const uint32_t a1 = deq_affine<BITS, C::NC, 2 * s>(w1, z1, magic);
+            const uint32_t a2 = deq_affine<BITS, C::NC, 2 * s + 1>(w0, z0, magic);
+            const uint32_t a3 = deq_affine<BITS, C::NC, 2 * s + 1>(w1, z1, magic);
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++) {
+                const uint2 b = *reinterpret_cast<const uint2*>(xg[nt] + s * C::SSTRIDE);
+                mma16816(acc[nt], a0, a1, a2, a3, b.x, b.y);
+            }
+        });
+        const float s0 = h2f((uint16_t)pr[0][0]), s1 = h2f((uint16_t)pr[1][0]);
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+            yacc[nt][0] = fmaf(s0, acc[nt][0], yacc[nt][0]);
+            yacc[nt][1] = fmaf(s0, acc[nt][1], yacc[nt][1]);
+            yacc[nt][2] = fmaf(s1, acc[nt][2], yacc[nt][2]);
+            yacc[nt][3] = fmaf(s1, acc[nt][3], yacc[nt][3]);
+        }
     }
 }
 
@@ -374,6 +442,149 @@ __device__ __forceinline__ void st_cluster_v4(const void* local_addr, int rank, 
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(r), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
                  : "memory");
+}
+
+// Cursor over the FP16 outliers a thread adds back: two threads per tile row
+// (threads 2r, 2r+1 take row r; threads beyond the 64 rows take none), and
+// the S CTAs of a cluster take every S-th pair of the row's CSR entries, so
+// the add-back is spread over every thread of the cluster.  init() reads the
+// CSR bounds, fetch() the first OU entries; only the x values they multiply
+// are read after the main loop.
+struct OutCursor {
+    static constexpr int OU = 4;
+    int p, end, row, stride;
+    int col[OU];
+    uint32_t val[OU];
+    __device__ __forceinline__ void init(const Problem& a, int splits)
+    {
+        row = (int)(threadIdx.x >> 1);
+        stride = 2 * splits;
+        p = 0;
+        end = 0;
+#pragma unroll
+        for (int u = 0; u < OU; u++) {
+            col[u] = -1;
+            val[u] = 0u;
+        }
+        const int n = blockIdx.x * kRowsPerCta + row;
+        if (a.nnz > 0 && threadIdx.x < 2 * kRowsPerCta && n < a.N) {
+            p = __ldg(a.row_ptr + n) + 2 * (int)blockIdx.y + (int)(threadIdx.x & 1);
+            end = __ldg(a.row_ptr + n + 1);
+        }
+    }
+    __device__ __forceinline__ void fetch(const Problem& a)
+    {
+#pragma unroll
+        for (int u = 0; u < OU; u++) {
+            const int q = p + u * stride;
+            col[u] = q < end ? __ldg(a.col + q) : -1;
+            val[u] = q < end ? __ldg(a.val + q) : 0u;
+        }
+    }
+};
+
+// Split-K reduction, outlier add-back and store of one 64-row tile; every
+// thread of the CTA calls it (threads of warps >= kWarps contribute no
+// partial sums).  yacc holds the thread's MMA accumulators of the tile; the
+// x block at the start of shared memory is reused for the partial sums, and
+// the split-K slots start at byte slot_off.
+template <int BITS, int G, int MP>
+__device__ __forceinline__ void tile_epilogue(const Problem& a, int splits, int slot_off,
+                                              const float (&yacc)[Cfg<BITS, G, MP>::NT][4], OutCursor& oc)
+{
+    using C = Cfg<BITS, G, MP>;
+    constexpr int NT = C::NT;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = lane & 3, gq = lane >> 2;
+    const int S = splits;
+    // ------------------------------------------------ split-K reduction + epilogue
+    // Partial sums of the tile go to shared memory (the x block is dead now)
+    // and the CTA's share of the outliers is added to them.  With a K split,
+    // rank r owns rows [r*64/S, (r+1)*64/S): every rank writes its partials of
+    // those rows into its own slot in rank r's shared memory (plain 16-byte
+    // remote stores), and after one cluster barrier the owner adds the S
+    // slots and stores its rows.
+    const int Mv = min(a.M, MP);
+    __syncthreads();
+    float* const yp = reinterpret_cast<float*>(smem);   // [64 rows][NTOK]
+    const int rl0 = warp * 16 + gq;
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++) {
+        if (warp >= kWarps) break;   // a producer warp holds no partial sums
+        const int c = nt * 8 + 2 * t;
+        yp[rl0 * C::NTOK + c] = yacc[nt][0];
+        yp[rl0 * C::NTOK + c + 1] = yacc[nt][1];
+        yp[(rl0 + 8) * C::NTOK + c] = yacc[nt][2];
+        yp[(rl0 + 8) * C::NTOK + c + 1] = yacc[nt][3];
+    }
+    __syncthreads();
+    for (int p = oc.p;;) {
+        if (oc.col[0] < 0) break;   // entries fill the slots in order
+        // tokens four at a time, so that all the x loads of a round are in flight together
+        constexpr int OM = MP < 4 ? MP : 4;
+        for (int mb = 0; mb < Mv; mb += OM) {
+            float xv[OM][OutCursor::OU];
+#pragma unroll
+            for (int i = 0; i < OM; i++) {
+                const int m = mb + i;
+                const __nv_bfloat16* xm = a.x + (size_t)x_row(a, min(m, Mv - 1)) * a.ldx;
+#pragma unroll
+                for (int u = 0; u < OutCursor::OU; u++) xv[i][u] = (m < Mv && oc.col[u] >= 0) ? __bfloat162float(xm[oc.col[u]]) : 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < OM; i++) {
+                float sum = 0.0f;
+#pragma unroll
+                for (int u = 0; u < OutCursor::OU; u++) sum = fmaf(xv[i][u], h2f((uint16_t)oc.val[u]), sum);
+                if (mb + i < Mv) atomicAdd(&yp[oc.row * C::NTOK + mb + i], sum);
+            }
+        }
+        p += OutCursor::OU * oc.stride;
+        if (p >= oc.end) break;
+#pragma unroll
+        for (int u = 0; u < OutCursor::OU; u++) {
+            const int q = p + u * oc.stride;
+            oc.col[u] = q < oc.end ? __ldg(a.col + q) : -1;
+            oc.val[u] = q < oc.end ? __ldg(a.val + q) : 0u;
+        }
+    }
+    __syncthreads();
+    const int rows_cap = (kRowsPerCta + S - 1) / S;
+    const float* slots = reinterpret_cast<const float*>(smem + slot_off);   // [S][rows_cap][NTOK]
+    if (S > 1) {
+        const int me = (int)cluster_rank();
+        constexpr int Q = C::NTOK / 4;   // float4 per row
+        for (int j = threadIdx.x; j < kRowsPerCta * Q; j += blockDim.x) {
+            const int rl = j / Q, c4 = j % Q;
+            const int owner = (S * (rl + 1) - 1) / kRowsPerCta;
+            const int lr = rl - owner * kRowsPerCta / S;
+            const float4 v = *reinterpret_cast<const float4*>(yp + rl * C::NTOK + 4 * c4);
+            st_cluster_v4(slots + ((size_t)(me * rows_cap + lr) * C::NTOK + 4 * c4), owner, v);
+        }
+        cluster_arrive();
+        cluster_wait();
+    }
+    const int rank = S > 1 ? (int)cluster_rank() : 0;
+    const int row_lo = rank * kRowsPerCta / S, rows_per = (rank + 1) * kRowsPerCta / S - row_lo;
+    for (int it = threadIdx.x; it < rows_per * Mv; it += blockDim.x) {
+        const int m = it / rows_per, lr = it % rows_per, rl = row_lo + lr;
+        const int n = blockIdx.x * kRowsPerCta + rl;
+        if (n < a.N) {
+            float v;
+            if (S > 1) {
+                v = 0.0f;
+                for (int r = 0; r < S; r++) v += slots[(size_t)(r * rows_cap + lr) * C::NTOK + m];
+            } else {
+                v = yp[rl * C::NTOK + m];
+            }
+            const size_t yo = (size_t)y_row(a, m) * a.ldy + n;
+            if (a.y_bf16)
+                reinterpret_cast<__nv_bfloat16*>(a.y)[yo] = __float2bfloat16_rn(v);
+            else
+                reinterpret_cast<float*>(a.y)[yo] = v;
+        }
+    }
 }
 
 template <int BITS, int G, int MP>
@@ -445,40 +656,20 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
         if (d < ngrp) issue(dc, dc);
     });
 
-    // FP16 outliers of the tile's rows: two threads per row, and the S CTAs of
-    // a cluster take every S-th pair of the row's entries, so the add-back is
-    // spread over every thread of the cluster.  The CSR bounds are read now
-    // and the first OU entries of each thread right after x is staged; only
-    // the x values they multiply are read after the main loop.
-    static_assert(kWarps * 32 == 2 * kRowsPerCta, "two threads per tile row");
-    constexpr int OU = 4;
-    const int o_row = threadIdx.x >> 1;
-    const int o_n = blockIdx.x * kRowsPerCta + o_row;
-    const int o_stride = 2 * splits;
-    int o_p = 0, o_end = 0;
-    if (a.nnz > 0 && o_n < a.N) {
-        o_p = __ldg(a.row_ptr + o_n) + 2 * (int)blockIdx.y + (int)(threadIdx.x & 1);
-        o_end = __ldg(a.row_ptr + o_n + 1);
-    }
-    int o_col[OU];
-    uint32_t o_val[OU];
+    OutCursor oc;
+    oc.init(a, splits);
 
     const int S = splits;
-    if (ngrp > 0) stage_x<BITS, G, MP>(a, g_begin * G, min(C::XG, ngrp), smem);
+    if (ngrp > 0) stage_x<BITS, G, MP>(a, g_begin * G, min(C::XG, ngrp), smem, blockDim.x);
     __syncthreads();
-#pragma unroll
-    for (int u = 0; u < OU; u++) {
-        const int p = o_p + u * o_stride;
-        o_col[u] = p < o_end ? __ldg(a.col + p) : -1;
-        o_val[u] = p < o_end ? __ldg(a.val + p) : 0u;
-    }
+    oc.fetch(a);
 
     int xnext = C::XG;      // group index (relative) at which x is staged next
     uint32_t xoff = 0;      // byte offset of group jj inside the x block
     for (int jj = 0; jj < ngrp; jj += D) {
         if (jj == xnext) {
             __syncthreads();
-            stage_x<BITS, G, MP>(a, (g_begin + jj) * G, min(C::XG, ngrp - jj), smem);
+            stage_x<BITS, G, MP>(a, (g_begin + jj) * G, min(C::XG, ngrp - jj), smem, blockDim.x);
             __syncthreads();
             xnext += C::XG;
             xoff = 0;
@@ -490,55 +681,11 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
         static_for<0, D>([&](auto dc) {
             constexpr int d = decltype(dc)::value;
             if (jj + d < ngrp) {
-                if constexpr (BITS == 2) {
-                    // per-row lookup tables: low bytes and high bytes of the 4 entries
-                    const uint32_t L0 = __byte_perm(prm[d][0][0], prm[d][0][1], 0x6420);
-                    const uint32_t H0 = __byte_perm(prm[d][0][0], prm[d][0][1], 0x7531);
-                    const uint32_t L1 = __byte_perm(prm[d][1][0], prm[d][1][1], 0x6420);
-                    const uint32_t H1 = __byte_perm(prm[d][1][0], prm[d][1][1], 0x7531);
-                    static_for<0, NW>([&](auto wc) {
-                        constexpr int wi = decltype(wc)::value;
-                        static_for<0, 4>([&](auto jc) {
-                            constexpr int jf = decltype(jc)::value;
-                            const uint32_t f0 = (wr[d][0][wi] >> (2 * jf)) & 0x03030303u;
-                            const uint32_t f1 = (wr[d][1][wi] >> (2 * jf)) & 0x03030303u;
-                            const uint32_t s0l = f0 * 0x11u + 0x4040u, s0h = __umulhi(f0, 0x00110000u) + 0x4040u;
-                            const uint32_t s1l = f1 * 0x11u + 0x4040u, s1h = __umulhi(f1, 0x00110000u) + 0x4040u;
-                            const uint32_t a0 = __byte_perm(L0, H0, s0l), a2 = __byte_perm(L0, H0, s0h);
-                            const uint32_t a1 = __byte_perm(L1, H1, s1l), a3 = __byte_perm(L1, H1, s1h);
-                            constexpr int s = 4 * wi + jf;   // entries 2s (lo) and 2s+1 (hi)
+                {
+                    const unsigned char* xg[NT];
 #pragma unroll
-                            for (int nt = 0; nt < NT; nt++) {
-                                const uint2 b = *reinterpret_cast<const uint2*>(xb[nt] + d * C::GSTRIDE + s * C::SSTRIDE);
-                                mma16816(yacc[nt], a0, a1, a2, a3, b.x, b.y);
-                            }
-                        });
-                    });
-                } else {
-                    float acc[NT][4];
-#pragma unroll
-                    for (int i = 0; i < NT; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
-                    const uint32_t z0 = prm[d][0][1], z1 = prm[d][1][1];
-                    static_for<0, C::STEPS>([&](auto sc) {
-                        constexpr int s = decltype(sc)::value;
-                        const uint32_t a0 = deq_affine<BITS, C::NC, 2 * s>(wr[d][0], z0, magic);
-                        const uint32_t a1 = deq_affine<BITS, C::NC, 2 * s>(wr[d][1], z1, magic);
-                        const uint32_t a2 = deq_affine<BITS, C::NC, 2 * s + 1>(wr[d][0], z0, magic);
-                        const uint32_t a3 = deq_affine<BITS, C::NC, 2 * s + 1>(wr[d][1], z1, magic);
-#pragma unroll
-                        for (int nt = 0; nt < NT; nt++) {
-                            const uint2 b = *reinterpret_cast<const uint2*>(xb[nt] + d * C::GSTRIDE + s * C::SSTRIDE);
-                            mma16816(acc[nt], a0, a1, a2, a3, b.x, b.y);
-                        }
-                    });
-                    const float s0 = h2f((uint16_t)prm[d][0][0]), s1 = h2f((uint16_t)prm[d][1][0]);
-#pragma unroll
-                    for (int nt = 0; nt < NT; nt++) {
-                        yacc[nt][0] = fmaf(s0, acc[nt][0], yacc[nt][0]);
-                        yacc[nt][1] = fmaf(s0, acc[nt][1], yacc[nt][1]);
-                        yacc[nt][2] = fmaf(s1, acc[nt][2], yacc[nt][2]);
-                        yacc[nt][3] = fmaf(s1, acc[nt][3], yacc[nt][3]);
-                    }
+                    for (int nt = 0; nt < NT; nt++) xg[nt] = xb[nt] + d * C::GSTRIDE;
+                    mma_group<BITS, G, MP>(wr[d][0], wr[d][1], prm[d], xg, yacc, magic);
                 }
                 if (jj + d + D < ngrp) issue(dc, std::integral_constant<int, D + d>{});
             }
@@ -547,92 +694,7 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
         xoff += D * C::GSTRIDE;
     }
 
-    // ------------------------------------------------ split-K reduction + epilogue
-    // Partial sums of the tile go to shared memory (the x block is dead now)
-    // and the CTA's share of the outliers is added to them.  With a K split,
-    // rank r owns rows [r*64/S, (r+1)*64/S): every rank writes its partials of
-    // those rows into its own slot in rank r's shared memory (plain 16-byte
-    // remote stores), and after one cluster barrier the owner adds the S
-    // slots and stores its rows.
-    const int Mv = min(a.M, MP);
-    __syncthreads();
-    float* const yp = reinterpret_cast<float*>(smem);   // [64 rows][NTOK]
-    const int rl0 = warp * 16 + gq;
-#pragma unroll
-    for (int nt = 0; nt < NT; nt++) {
-        const int c = nt * 8 + 2 * t;
-        yp[rl0 * C::NTOK + c] = yacc[nt][0];
-        yp[rl0 * C::NTOK + c + 1] = yacc[nt][1];
-        yp[(rl0 + 8) * C::NTOK + c] = yacc[nt][2];
-        yp[(rl0 + 8) * C::NTOK + c + 1] = yacc[nt][3];
-    }
-    __syncthreads();
-    for (int p = o_p;;) {
-        if (o_col[0] < 0) break;   // entries fill the slots in order
-        // tokens four at a time, so that all the x loads of a round are in flight together
-        constexpr int OM = MP < 4 ? MP : 4;
-        for (int mb = 0; mb < Mv; mb += OM) {
-            float xv[OM][OU];
-#pragma unroll
-            for (int i = 0; i < OM; i++) {
-                const int m = mb + i;
-                const __nv_bfloat16* xm = a.x + (size_t)x_row(a, min(m, Mv - 1)) * a.ldx;
-#pragma unroll
-                for (int u = 0; u < OU; u++) xv[i][u] = (m < Mv && o_col[u] >= 0) ? __bfloat162float(xm[o_col[u]]) : 0.0f;
-            }
-#pragma unroll
-            for (int i = 0; i < OM; i++) {
-                float sum = 0.0f;
-#pragma unroll
-                for (int u = 0; u < OU; u++) sum = fmaf(xv[i][u], h2f((uint16_t)o_val[u]), sum);
-                if (mb + i < Mv) atomicAdd(&yp[o_row * C::NTOK + mb + i], sum);
-            }
-        }
-        p += OU * o_stride;
-        if (p >= o_end) break;
-#pragma unroll
-        for (int u = 0; u < OU; u++) {
-            const int q = p + u * o_stride;
-            o_col[u] = q < o_end ? __ldg(a.col + q) : -1;
-            o_val[u] = q < o_end ? __ldg(a.val + q) : 0u;
-        }
-    }
-    __syncthreads();
-    const int rows_cap = (kRowsPerCta + S - 1) / S;
-    const float* slots = reinterpret_cast<const float*>(smem + C::slot_offset(gpsplit));   // [S][rows_cap][NTOK]
-    if (S > 1) {
-        const int me = (int)cluster_rank();
-        constexpr int Q = C::NTOK / 4;   // float4 per row
-        for (int j = threadIdx.x; j < kRowsPerCta * Q; j += blockDim.x) {
-            const int rl = j / Q, c4 = j % Q;
-            const int owner = (S * (rl + 1) - 1) / kRowsPerCta;
-            const int lr = rl - owner * kRowsPerCta / S;
-            const float4 v = *reinterpret_cast<const float4*>(yp + rl * C::NTOK + 4 * c4);
-            st_cluster_v4(slots + ((size_t)(me * rows_cap + lr) * C::NTOK + 4 * c4), owner, v);
-        }
-        cluster_arrive();
-        cluster_wait();
-    }
-    const int rank = S > 1 ? (int)cluster_rank() : 0;
-    const int row_lo = rank * kRowsPerCta / S, rows_per = (rank + 1) * kRowsPerCta / S - row_lo;
-    for (int it = threadIdx.x; it < rows_per * Mv; it += blockDim.x) {
-        const int m = it / rows_per, lr = it % rows_per, rl = row_lo + lr;
-        const int n = blockIdx.x * kRowsPerCta + rl;
-        if (n < a.N) {
-            float v;
-            if (S > 1) {
-                v = 0.0f;
-                for (int r = 0; r < S; r++) v += slots[(size_t)(r * rows_cap + lr) * C::NTOK + m];
-            } else {
-                v = yp[rl * C::NTOK + m];
-            }
-            const size_t yo = (size_t)y_row(a, m) * a.ldy + n;
-            if (a.y_bf16)
-                reinterpret_cast<__nv_bfloat16*>(a.y)[yo] = __float2bfloat16_rn(v);
-            else
-                reinterpret_cast<float*>(a.y)[yo] = v;
-        }
-    }
+    tile_epilogue<BITS, G, MP>(a, splits, C::slot_offset(gpsplit), yacc, oc);
 }
 
 template <int BITS, int G, int MP>
@@ -701,13 +763,42 @@ inline int choose_splits(long long ctas_per_split, int ng)
 // Padded token count of a launch.
 inline int mp_for(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : 64; }
 
-template <int BITS, int G, int MP, typename K, typename A>
-qg_status launch_cluster(K kernel, const A& args, dim3 grid, int S, int gpsplit, cudaStream_t s)
+// Opt a kernel in to `bytes` of dynamic shared memory on the current device
+// (once per kernel and device).
+template <typename K>
+qg_status allow_smem(K kernel, int bytes)
 {
+    static std::mutex mu;
+    static const void* done[64][8] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    const void* key = reinterpret_cast<const void*>(kernel);
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < 8; i++) {
+        if (done[dev][i] == key) return QG_OK;
+        if (!done[dev][i]) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+            if (e != cudaSuccess) return cuda_fail(e, "kernel shared memory attribute");
+            done[dev][i] = key;
+            return QG_OK;
+        }
+    }
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return e == cudaSuccess ? QG_OK : cuda_fail(e, "kernel shared memory attribute");
+}
+
+template <typename K, typename... A>
+qg_status launch_cluster(K kernel, dim3 grid, int S, unsigned threads, size_t smem_bytes, cudaStream_t s,
+                         A... args)
+{
+    if (smem_bytes > 48 * 1024) {
+        qg_status st = allow_smem(kernel, 227 * 1024);
+        if (st != QG_OK) return st;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(kWarps * 32, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)Cfg<BITS, G, MP>::smem(gpsplit, S);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -716,7 +807,7 @@ qg_status launch_cluster(K kernel, const A& args, dim3 grid, int S, int gpsplit,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args, S, gpsplit);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     return QG_OK;
 }
@@ -727,8 +818,9 @@ qg_status dense_mp(const Problem& p, cudaStream_t s)
     const int ng = p.K / G;
     const int tiles = (int)ceil_div(p.N, kRowsPerCta);
     const int S = choose_splits(tiles, ng);
-    return launch_cluster<BITS, G, MP>(k_gemv<BITS, G, MP>, p, dim3((unsigned)tiles, (unsigned)S, 1), S,
-                                       (int)ceil_div(ng, S), s);
+    const dim3 grid((unsigned)tiles, (unsigned)S, 1);
+    const int gps = (int)ceil_div(ng, S);
+    return launch_cluster(k_gemv<BITS, G, MP>, grid, S, kWarps * 32, (size_t)Cfg<BITS, G, MP>::smem(gps, S), s, p, S, gps);
 }
 
 template <int BITS, int G, int MP>
@@ -737,9 +829,9 @@ qg_status grouped_mp(const MoeTable& t, int max_items, int expect_items, cudaStr
     const int ng = t.K / G;
     const int tiles = (int)ceil_div(t.N, kRowsPerCta);
     const int S = choose_splits((long long)tiles * std::max(1, expect_items), ng);
-    return launch_cluster<BITS, G, MP>(k_gemv_moe<BITS, G, MP>, t,
-                                       dim3((unsigned)tiles, (unsigned)S, (unsigned)max_items), S,
-                                       (int)ceil_div(ng, S), s);
+    const int gps = (int)ceil_div(ng, S);
+    return launch_cluster(k_gemv_moe<BITS, G, MP>, dim3((unsigned)tiles, (unsigned)S, (unsigned)max_items), S,
+                          kWarps * 32, (size_t)Cfg<BITS, G, MP>::smem(gps, S), s, t, S, gps);
 }
 
 template <int BITS, int G, template <int, int, int> class F, typename... Args>

@@ -31,6 +31,12 @@ constexpr int kGemvMaxM = 64;
 qg_status launch_gemv(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,
                       qg_ydtype yt, cudaStream_t s);
 
+// Device status word of the library's kernels with bounded waits (nullptr if
+// it has no address on the current device) and its synchronous read
+// (optionally cleared).
+int* device_status_ptr();
+qg_status read_device_status(int* out, int reset);
+
 // ---------------------------------------------------------------- tensor-core GEMM
 size_t gemm_workspace_bytes(int M, const qg_qweight& w);
 qg_status launch_gemm(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,

@@ -205,6 +205,18 @@ QG_API qg_status qgemm_moe_grouped(const uint16_t* x, int32_t T, const int32_t* 
                             const qg_qweight* experts, int32_t E, void* y, qg_ydtype yt, void* ws,
                             size_t ws_bytes, void* stream);
 
+/* Status word of the library's kernels on the current device: QG_OK, or
+ * QG_ERR_TIMEOUT once a bounded wait of the tensor-core product (M above the
+ * decode range) on its shared-memory rings gave up (the kernel then finished
+ * without hanging, and the outputs of that call are not valid).  The pages define no such call; it exists because
+ * the kernels never trap or spin without a limit.
+ *   status  host int32: receives the word.
+ *   reset   non-zero: clear the word after reading it.
+ * Synchronous: waits for the device (cudaMemcpy), so it is a check between
+ * steps, not a call for the hot path.  Returns QG_ERR_INVALID_ARG if status
+ * is NULL and QG_ERR_CUDA if the device cannot be read. */
+QG_API qg_status qgemm_device_status(int32_t* status, int32_t reset);
+
 /* Message describing the calling thread's most recent failure ("" if none). */
 QG_API const char* qgemm_last_error(void);
 

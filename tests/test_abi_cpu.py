@@ -129,6 +129,19 @@ def test_valid_call_without_a_device_reports_cuda_error(qg):
     assert qg.last_error()
 
 
+def test_device_status_query_without_gpu(qg):
+    # a NULL output is rejected on the host; without a device the read fails
+    # with a CUDA status instead of crashing
+    import torch
+    L = qg.lib()
+    assert L.qgemm_device_status(None, 0) == -1
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    v = ctypes.c_int32(123)
+    assert L.qgemm_device_status(ctypes.byref(v), 0) == -5
+    assert v.value == 123
+
+
 def test_moe_validation_without_gpu(qg):
     L = qg.lib()
     arr = (qg.QgQWeight * 2)(_fake_desc(qg), _fake_desc(qg, N=128))

@@ -120,6 +120,19 @@ def test_tensor_core_path_against_oracle(qg, group, M, N, K):
     assert torch.equal(yb, y.to(torch.bfloat16))
 
 
+def test_device_status_stays_clear(qg):
+    # the tensor-core kernel's bounded waits never give up on valid inputs:
+    # after products of both groups the status word is still QG_OK
+    qg.qgemm_device_status(reset=True)
+    for group in (64, 128):
+        q, wmax = _weights(512, 1024, 4, group, 0.001, seed=group)
+        x = wl.gen_x(300, 1024)
+        y = qg.qgemm_forward(x.cuda(), to_device(q))
+        torch.cuda.synchronize()
+        check_product(y, oracle.linear(x, q), x, wmax)
+    assert qg.qgemm_device_status() == 0
+
+
 @pytest.mark.parametrize("group", [64, 128])
 def test_tensor_core_path_repeatable(qg, group):
     # the accumulation order of the tensor-core kernel is fixed, so repeated
