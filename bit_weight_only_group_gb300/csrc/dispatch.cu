@@ -160,26 +160,30 @@ struct MoeWs {
     int* perm;
     int2* items;
     int* n_items;
+    void* x16;   // x in routed order, fp16 (tensor-core path only)
 };
 
 // Upper bound on work items: sum over experts of ceil(count / chunk) with the
 // smallest chunk (1 pair).
 inline int max_items_for(int P, int E, int chunk) { return (int)ceil_div(P, chunk) + E; }
 
-size_t moe_ws_layout(int T, int k, int E, MoeWs* p, void* base)
+size_t moe_ws_layout(int T, int k, int E, const qg_qweight* experts, MoeWs* p, void* base)
 {
     const size_t P = (size_t)T * k;
     const size_t o_off = 0;
     const size_t o_n = align_up(sizeof(int) * ((size_t)E + 1), 256);
     const size_t o_perm = o_n + 256;
     const size_t o_items = align_up(o_perm + sizeof(int) * P, 256);
-    const size_t total = align_up(o_items + sizeof(int2) * (size_t)max_items_for((int)P, E, 1), 256);
+    const size_t o_x16 = align_up(o_items + sizeof(int2) * (size_t)max_items_for((int)P, E, 1), 256);
+    const size_t x16 = moe_tc_eligible(experts, E) ? moe_tc_x16_bytes((int)P, experts[0].K) : 0;
+    const size_t total = o_x16 + x16;
     if (p && base) {
         char* b = static_cast<char*>(base);
         p->offsets = reinterpret_cast<int*>(b + o_off);
         p->n_items = reinterpret_cast<int*>(b + o_n);
         p->perm = reinterpret_cast<int*>(b + o_perm);
         p->items = reinterpret_cast<int2*>(b + o_items);
+        p->x16 = x16 ? static_cast<void*>(b + o_x16) : nullptr;
     }
     return total;
 }
@@ -207,15 +211,26 @@ qg_status launch_gemv_chunked(const uint16_t* x, int M, int ldx, const qg_qweigh
     return QG_OK;
 }
 
-size_t moe_workspace_bytes(int T, int k, int E, const qg_qweight*) { return moe_ws_layout(T, k, E, nullptr, nullptr); }
+size_t moe_workspace_bytes(int T, int k, int E, const qg_qweight* experts)
+{
+    return moe_ws_layout(T, k, E, experts, nullptr, nullptr);
+}
 
 qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const qg_qweight* experts, int E,
                      void* y, qg_ydtype yt, void* ws, size_t, cudaStream_t s)
 {
     MoeWs p;
-    moe_ws_layout(T, k, E, &p, ws);
+    moe_ws_layout(T, k, E, experts, &p, ws);
     const int P = T * k;
     const qg_qweight& w0 = experts[0];
+    if (p.x16) {
+        // tensor cores: every expert's tokens in chunks of up to 256, weights as the MMA's M side
+        k_route<<<1, kRouteThreads, 0, s>>>(topk, P, E, kMoeTcChunk, p.offsets, p.perm, p.items, p.n_items);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
+        return launch_moe_tc(x, T, k, experts, E, y, yt, p.offsets, p.perm, p.items, p.n_items,
+                             max_items_for(P, E, kMoeTcChunk), p.x16, s);
+    }
     // tokens per CTA chunk from the mean load per expert
     const int mean = (P + E - 1) / E;
     const int mp = gemv::mp_for(std::max(1, mean));

@@ -48,4 +48,14 @@ size_t moe_workspace_bytes(int T, int k, int E, const qg_qweight* experts);
 qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const qg_qweight* experts,
                      int E, void* y, qg_ydtype yt, void* ws, size_t ws_bytes, cudaStream_t s);
 
+// Grouped product on the tensor cores (4-bit, K a multiple of 64, at most 32
+// experts): tokens of an expert in chunks of kMoeTcChunk; x16p is workspace
+// for x gathered in routed order (moe_tc_x16_bytes).
+constexpr int kMoeTcChunk = 256;
+bool moe_tc_eligible(const qg_qweight* experts, int E);
+size_t moe_tc_x16_bytes(int P, int K);
+qg_status launch_moe_tc(const uint16_t* x, int T, int k, const qg_qweight* experts, int E, void* y, qg_ydtype yt,
+                        const int* offsets, const int* perm, const int2* items, const int* n_items, int max_items,
+                        void* x16p, cudaStream_t s);
+
 }  // namespace qg

@@ -73,3 +73,24 @@ def test_moe_layer_4096_experts(qg):
     got = y[torch.from_numpy(sample).cuda()]
     k = cfg.top_k
     check_product(got.reshape(-1, cfg.ffn), ref.reshape(-1, cfg.ffn), x[sample].repeat_interleave(k, 0), wmax)
+
+
+@pytest.mark.parametrize("group,T,k,E,hot", [(64, 300, 2, 3, True), (128, 300, 2, 3, True), (128, 40, 2, 40, False)])
+def test_moe_tensor_core_chunks_and_fallback(qg, group, T, k, E, hot):
+    # 4-bit experts run on the tensor cores in chunks of up to 256 routed
+    # pairs per expert: with `hot` routing, expert 0 receives every token's
+    # first slot (300 pairs, two chunks); more than 32 experts take the
+    # decode kernel instead
+    N, K = 200, 640
+    qs, wmax = _experts(E, N, K, 4, group, 0.002, seed=90)
+    x = wl.gen_x(T, K, seed=T + 3)
+    topk = wl.gen_topk(T, k, E, seed=T + 4)
+    if hot:
+        g = torch.Generator().manual_seed(T + 5)
+        topk[:, 0] = 0
+        topk[:, 1] = torch.randint(1, E, (T,), generator=g).to(topk.dtype)
+    y = qg.qgemm_moe_grouped(x.cuda(), topk.cuda(), [to_device(q) for q in qs])
+    torch.cuda.synchronize()
+    ref = oracle.moe(x, topk.numpy(), qs)
+    check_product(y.reshape(T * k, N), ref.reshape(T * k, N), x.repeat_interleave(k, 0), wmax)
+    assert qg.qgemm_device_status() == 0
