@@ -1,26 +1,28 @@
 // Grouped (MoE) fused dequantization product on the 5th-generation tensor
 // cores with the roles of the operands swapped: the dequantized weights are
 // the MMA's M side (128 weight rows per CTA) and an expert's tokens are the N
-// side (N = 16 * ceil(tokens / 16), at most 256), so an expert that receives
+// side (N = 16 * ceil(tokens / 16), at most 128), so an expert that receives
 // a few dozen tokens costs no padding on the tensor core and its weights are
-// read from HBM once (per 256 of its tokens).
+// read from HBM once per 128 of its tokens.
 //     y[pair, n] = sum_k x[token(pair), k] * (w_hat_e[n, k] + S_e[n, k])
 //
 // Routing (a stable counting sort of the (token, slot) pairs by expert,
 // bjdmk.com.cn 5648983 page, sections 1-2) is done by the routing kernel;
 // k_gather_x16 then writes x in that order as fp16 with the K positions of
 // every block of 8 permuted (0,4,1,5,2,6,3,7) like the weight operand, and
-// one CTA of k_gemm_swap_u4 computes a 128-row x (up to 256)-token tile:
-//  * warp 8 (one lane) streams the token tile (TMA, 16-row boxes, 128-byte
-//    swizzle) into a 3-deep ring, warp 9 the packed 4-bit weight tile of the
-//    expert (TMA, 128 rows x 128 bytes = 4 K blocks) into a 4-deep ring;
-//  * warps 0-7 (two threads per weight row) dequantize exactly as the prefill
-//    kernel does (masks -> fp16 1024 + 2^p q, one packed FMA -> q - zp, one
-//    packed multiply by the fp16 scale, FP16 outliers patched in) into a
-//    3-deep ring of 128 x 64 fp16 tiles;
-//  * warp 10 (one lane) issues four tcgen05.mma (M=128, N=tokens, K=16) per K
-//    block into a TMEM accumulator of 128 lanes x 256 columns;
-//  * warps 0-7 read the accumulator (lane = weight row, column = token) and
+// one CTA of k_gemm_swap_u4 computes a 128-row x (up to 128)-token tile:
+//  * warp 16 (one lane) streams the token tile (TMA, 16-row boxes, 128-byte
+//    swizzle) into a ring of up to 16 stages (as many as the token count
+//    allows), warp 17 the packed 4-bit weight tile of the expert (TMA, 128
+//    rows x 128 bytes = 4 K blocks) into a 3-deep ring;
+//  * warps 0-15, in two groups taking alternate K blocks (two threads per
+//    weight row), dequantize as the prefill kernel does (masks -> fp16
+//    1024 + 2^p q, one packed FMA -> q - zp, one packed multiply by the fp16
+//    scale, FP16 outliers patched in) into an 8-deep ring of 128 x 64 fp16
+//    tiles;
+//  * warp 18 issues four tcgen05.mma (M=128, N=tokens, K=16) per K block from
+//    one elected lane into a TMEM accumulator of 128 lanes x 128 columns;
+//  * warps 0-15 read the accumulator (lane = weight row, column = token) and
 //    store y rows in pair order.
 // Every mbarrier wait is bounded; a wait that gives up writes QG_ERR_TIMEOUT
 // into the device status word.
@@ -44,21 +46,29 @@ qg_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, 
 namespace swap {
 
 constexpr int BW = 128;        // weight rows per CTA (MMA M)
-constexpr int NBMAX = 256;     // tokens per CTA (MMA N, a multiple of 16)
+constexpr int NBMAX = 128;     // tokens per CTA (MMA N, a multiple of 16)
 constexpr int BK = 64;         // K block (one 128-byte fp16 row of an operand tile)
 constexpr int PK = 4;          // K blocks per packed tile (128-byte rows at 4 bits)
-constexpr int SX = 3, SP = 4, SA = 3;
-constexpr int kDeqWarps = 8;
+constexpr int SXMAX = 16, SP = 3, SA = 8;   // token ring: up to 16 stages in X_RING bytes
+// Two groups of 8 dequantization warps take alternate K blocks (group g the
+// blocks 4p + g and 4p + g + 2 of packed tile p, both at once: eight
+// independent unpack chains per thread and one proxy fence per tile), so the
+// per-block latencies overlap; group g writes the fp16 slots of parity g and
+// holds up to four of them (two tiles) ahead of the MMA.
+constexpr int kGroups = 2, kGroupWarps = 8;
+constexpr int kDeqWarps = kGroups * kGroupWarps;
+static_assert(SA % kGroups == 0, "a group's K blocks map to its own fp16 slots");
+// one MMA issuer warp per group (K blocks of parity g into accumulator g)
 constexpr int kWarpX = kDeqWarps, kWarpP = kDeqWarps + 1, kWarpMma = kDeqWarps + 2;
-constexpr int kThreads = (kDeqWarps + 3) * 32;
-constexpr int X_BYTES = NBMAX * BK * 2;      // 32 KB
+constexpr int kThreads = (kDeqWarps + 2 + kGroups) * 32;
+constexpr int X_RING = 3 * NBMAX * BK * 2;   // 48 KB, split into stages of NB x 64 fp16
 constexpr int P_BYTES = BW * PK * BK / 2;    // 16 KB
 constexpr int A_BYTES = BW * BK * 2;         // 16 KB
-constexpr int OFF_P = SX * X_BYTES;
+constexpr int OFF_P = X_RING;
 constexpr int OFF_A = OFF_P + SP * P_BYTES;
 constexpr int OFF_BAR = OFF_A + SA * A_BYTES;
 constexpr int SMEM = OFF_BAR + 1024 /* barriers */ + 1024 /* alignment */;
-constexpr int TMEM_COLS = NBMAX;
+constexpr int TMEM_COLS = kGroups * NBMAX;   // one accumulator per group
 constexpr int kMaxExperts = 32;              // tensor maps travel as kernel parameters
 
 struct Maps {
@@ -128,15 +138,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_u32(smem);
     const uint32_t bars = sbase + OFF_BAR;
+    // token ring: stages of NB rows x 128 bytes (a multiple of 2 KB, so every
+    // stage starts on a 1024-byte boundary), as many as fit X_RING (at most
+    // SXMAX): small experts get a deep ring that covers the L2 latency
+    const int x_stage = NB * BK * 2;
+    const int SX = min(SXMAX, X_RING / x_stage) & ~(kGroups - 1);   // even: slot parity = block parity
     auto full_x = [&](int s) { return bars + 8 * s; };
-    auto empty_x = [&](int s) { return bars + 8 * (SX + s); };
-    auto full_p = [&](int s) { return bars + 8 * (2 * SX + s); };
-    auto empty_p = [&](int s) { return bars + 8 * (2 * SX + SP + s); };
-    auto full_a = [&](int s) { return bars + 8 * (2 * SX + 2 * SP + s); };
-    auto empty_a = [&](int s) { return bars + 8 * (2 * SX + 2 * SP + SA + s); };
-    const uint32_t acc_full = bars + 8 * (2 * SX + 2 * SP + 2 * SA);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 8 * (2 * SX + 2 * SP + 2 * SA + 1));
-    auto x_tile = [&](int s) { return sbase + s * X_BYTES; };
+    auto empty_x = [&](int s) { return bars + 8 * (SXMAX + s); };
+    auto full_p = [&](int s) { return bars + 8 * (2 * SXMAX + s); };
+    auto empty_p = [&](int s) { return bars + 8 * (2 * SXMAX + SP + s); };
+    auto full_a = [&](int s) { return bars + 8 * (2 * SXMAX + 2 * SP + s); };
+    auto empty_a = [&](int s) { return bars + 8 * (2 * SXMAX + 2 * SP + SA + s); };
+    const uint32_t acc_full = bars + 8 * (2 * SXMAX + 2 * SP + 2 * SA);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 8 * (2 * SXMAX + 2 * SP + 2 * SA + 1));
+    auto x_tile = [&](int s) { return sbase + s * x_stage; };
     auto p_tile = [&](int s) { return smem + OFF_P + s * P_BYTES; };
     auto a_tile = [&](int s) { return sbase + OFF_A + s * A_BYTES; };
 
@@ -144,8 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < SX; s++) { ptx::mbar_init(full_x(s), 1); ptx::mbar_init(empty_x(s), 1); }
         for (int s = 0; s < SP; s++) { ptx::mbar_init(full_p(s), 1); ptx::mbar_init(empty_p(s), kDeqWarps); }
-        for (int s = 0; s < SA; s++) { ptx::mbar_init(full_a(s), kDeqWarps); ptx::mbar_init(empty_a(s), 1); }
-        ptx::mbar_init(acc_full, 1);
+        for (int s = 0; s < SA; s++) { ptx::mbar_init(full_a(s), kGroupWarps); ptx::mbar_init(empty_a(s), 1); }
+        ptx::mbar_init(acc_full, kGroups);
         ptx::fence_mbar_init();
     }
     if (warp == kWarpMma) {
@@ -188,41 +203,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++s == SP) { s = 0; ph ^= 1u; }
             }
         }
-    } else if (warp == kWarpMma) {
-        // ------------------------------------------------ MMA issuer: D[w rows, tokens] += W * X^T
-        if (lane == 0) {
-            const uint32_t idesc = ptx::idesc_f16_f32(BW, NB);
-            int sx = 0, sa = 0;
-            uint32_t px = 0, pa = 0;
-            for (int kb = 0; kb < KB; kb++) {
-                if (!ptx::mbar_wait(full_x(sx), px) || !ptx::mbar_wait(full_a(sa), pa)) { ok = false; break; }
-                ptx::tc_fence_after();
+    } else if (warp >= kWarpMma) {
+        // ------------------------------------------------ MMA issuers: D_g[w rows, tokens] += W * X^T over
+        // the K blocks of parity g (the whole warp runs the loop; one elected lane issues)
+        const int g = warp - kWarpMma;
+        const uint32_t acc = tmem + (uint32_t)(g * NBMAX);
+        const uint32_t idesc = ptx::idesc_f16_f32(BW, NB);
+        const uint64_t adesc0 = ptx::sw128_desc(a_tile(0)), xdesc0 = ptx::sw128_desc(x_tile(0));
+        for (int kb = g; kb < KB; kb += kGroups) {
+            const int sx = kb % SX, sa = kb % SA;
+            const uint32_t px = (uint32_t)(kb / SX) & 1u, pa = (uint32_t)(kb / SA) & 1u;
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait(full_x(sx), px) && ptx::mbar_wait(full_a(sa), pa));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            // descriptors advance by (byte offset >> 4) in their address field
+            const uint64_t ad = adesc0 + (uint64_t)((sa * A_BYTES) >> 4);
+            const uint64_t xd = xdesc0 + (uint64_t)((sx * x_stage) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; kk++)
-                    ptx::mma_f16(tmem, ptx::sw128_desc(a_tile(sa) + 32 * kk), ptx::sw128_desc(x_tile(sx) + 32 * kk),
-                                 idesc, (kb | kk) != 0);
-                ptx::tc_commit(empty_x(sx));
-                ptx::tc_commit(empty_a(sa));
-                if (++sx == SX) { sx = 0; px ^= 1u; }
-                if (++sa == SA) { sa = 0; pa ^= 1u; }
-            }
-            ptx::tc_commit(acc_full);
+            for (int kk = 0; kk < BK / 16; kk++)
+                ptx::mma_f16_elect(acc, ad + 2 * kk, xd + 2 * kk, idesc, (kb >= kGroups || kk > 0) ? 1u : 0u);
+            ptx::tc_commit_elect(empty_x(sx));
+            ptx::tc_commit_elect(empty_a(sa));
         }
+        ptx::tc_commit_elect(acc_full);
     } else {
         // ------------------------------------------------ dequantization (two threads per weight row)
         const uint32_t magic = a.magic;
-        const int r = threadIdx.x >> 1;                 // 0..127
-        const int hk = threadIdx.x & 1;                 // which 32 k of the block
+        const int grp = threadIdx.x / (kGroupWarps * 32);   // K blocks kb with kb % kGroups == grp
+        const int tg = threadIdx.x % (kGroupWarps * 32);
+        const int r = tg >> 1;                          // 0..127
+        const int hk = tg & 1;                          // which 32 k of the block
         const int nr = n0 + r;
         const int n = min(nr, a.N - 1);
         const uint16_t* sp_row = a.scale[e] + (size_t)n * a.ng;
         const uint8_t* zp_row = a.zp[e] + (size_t)n * a.ng;
         constexpr int KB_PER_G = G / BK;                // 1 or 2
         const int ng = a.ng;
-        // parameters of the current group and of the next two (loads in flight)
-        uint32_t sc_cur = __ldg(sp_row), zq_cur = __ldg(zp_row);
-        uint32_t sc_n1 = ng > 1 ? __ldg(sp_row + 1) : 0u, zq_n1 = ng > 1 ? __ldg(zp_row + 1) : 0u;
-        uint32_t sc_n2 = ng > 2 ? __ldg(sp_row + 2) : 0u, zq_n2 = ng > 2 ? __ldg(zp_row + 2) : 0u;
+        // the row's group parameters are read per K block through L1; warm
+        // their lines now
+        for (int off = 0; off < ng * 2; off += 128) asm volatile("prefetch.global.L1 [%0];" ::"l"(sp_row + off / 2));
+        for (int off = 0; off < ng; off += 128) asm volatile("prefetch.global.L1 [%0];" ::"l"(zp_row + off));
         // outlier cursor of this row: the next entry and the one after it
         const int* ocolp = a.col[e];
         const uint16_t* ovalp = a.val[e];
@@ -240,74 +260,76 @@ __global__ void __launch_bounds__(kThreads, 1)
                 nval = ovalp[op + 1];
             }
         }
-        // swizzled offsets, fixed per thread: source chunk (2*sub + hk) of the
-        // packed row, destination chunks (4*hk + j) of the fp16 row
+        // swizzled offsets, fixed per thread: source chunks (2*sub + hk) of the
+        // packed row for this group's two blocks, destination chunks (4*hk + j)
         const uint32_t rsw = r & 7;
-        uint32_t src_off[PK], dst_off[4];
-#pragma unroll
-        for (int sub = 0; sub < PK; sub++) src_off[sub] = r * 128 + (((2 * sub + hk) ^ rsw) << 4);
+        const uint32_t src0 = r * 128 + (((2 * grp + hk) ^ rsw) << 4);
+        const uint32_t src1 = r * 128 + (((2 * (grp + 2) + hk) ^ rsw) << 4);
+        uint32_t dst_off[4];
 #pragma unroll
         for (int j = 0; j < 4; j++) dst_off[j] = r * 128 + (((4 * hk + j) ^ rsw) << 4);
         unsigned char* const atile0 = smem + OFF_A;
+        auto deq_block = [&](const uint4& w, int kb, unsigned char* at) {
+            const int gi = kb / KB_PER_G;
+            const uint32_t sc = __ldg(sp_row + gi), zq = __ldg(zp_row + gi);
+            const uint32_t add_lo = zq * 0x00010001u + 0xE400E400u;   // -(1024 + zp)
+            const uint32_t add_hi = zq * 0x00100010u + 0xD400D400u;   // -(64 + zp)
+            const uint32_t s2 = __byte_perm(sc, 0u, 0x1010u);
+            *reinterpret_cast<uint4*>(at + dst_off[0]) = tc::deq8_u4(w.x, add_lo, add_hi, s2, magic);
+            *reinterpret_cast<uint4*>(at + dst_off[1]) = tc::deq8_u4(w.y, add_lo, add_hi, s2, magic);
+            *reinterpret_cast<uint4*>(at + dst_off[2]) = tc::deq8_u4(w.z, add_lo, add_hi, s2, magic);
+            *reinterpret_cast<uint4*>(at + dst_off[3]) = tc::deq8_u4(w.w, add_lo, add_hi, s2, magic);
+        };
+        auto patch = [&](int kb, unsigned char* at) {
+            // FP16 outliers in this thread's 32 k of block kb: the dense value there is exactly 0
+            const int k0 = kb * BK + 32 * hk;
+            while (ocol < k0 + 32) {
+                if (ocol >= k0) {
+                    const int kk = ocol - kb * BK;
+                    *reinterpret_cast<uint16_t*>(at + r * 128 + (((kk >> 3) ^ rsw) << 4) + (tc::perm8_pos(kk) << 1)) = oval;
+                }
+                ocol = ncol;
+                oval = nval;
+                if (++op + 1 < oe) {
+                    ncol = ocolp[op + 1];
+                    nval = ovalp[op + 1];
+                } else {
+                    ncol = 0x7FFFFFFF;
+                }
+            }
+        };
         const int KP = (KB + PK - 1) / PK;
-        int sp = 0, sa = 0;
-        uint32_t pp = 0, pa = 1;   // parities: full_p to wait for, empty_a to wait for
+        int sp = 0;
+        uint32_t pp = 0;   // parity of full_p to wait for
         for (int kp = 0; kp < KP && ok; kp++) {
             const unsigned char* pt = p_tile(sp);
             ok = __all_sync(0xffffffffu, ptx::mbar_wait(full_p(sp), pp));
             if (!ok) break;
-#pragma unroll
-            for (int sub = 0; sub < PK; sub++) {
-                const int kb = kp * PK + sub;
-                if (kb >= KB) break;
-                if (kb > 0 && kb % KB_PER_G == 0) {      // next group
-                    const int gi = kb / KB_PER_G;
-                    sc_cur = sc_n1;
-                    zq_cur = zq_n1;
-                    sc_n1 = sc_n2;
-                    zq_n1 = zq_n2;
-                    if (gi + 2 < ng) {
-                        sc_n2 = __ldg(sp_row + gi + 2);
-                        zq_n2 = __ldg(zp_row + gi + 2);
-                    }
-                }
-                const uint32_t add_lo = zq_cur * 0x00010001u + 0xE400E400u;   // -(1024 + zp)
-                const uint32_t add_hi = zq_cur * 0x00100010u + 0xD400D400u;   // -(64 + zp)
-                const uint32_t s2 = __byte_perm(sc_cur, 0u, 0x1010u);
-                const uint4 w = *reinterpret_cast<const uint4*>(pt + src_off[sub]);
-                ok = __all_sync(0xffffffffu, ptx::mbar_wait(empty_a(sa), pa));
-                if (!ok) break;
-                unsigned char* at = atile0 + sa * A_BYTES;
-                *reinterpret_cast<uint4*>(at + dst_off[0]) = tc::deq8_u4(w.x, add_lo, add_hi, s2, magic);
-                *reinterpret_cast<uint4*>(at + dst_off[1]) = tc::deq8_u4(w.y, add_lo, add_hi, s2, magic);
-                *reinterpret_cast<uint4*>(at + dst_off[2]) = tc::deq8_u4(w.z, add_lo, add_hi, s2, magic);
-                *reinterpret_cast<uint4*>(at + dst_off[3]) = tc::deq8_u4(w.w, add_lo, add_hi, s2, magic);
-                // FP16 outliers in this thread's 32 k: the dense value there is exactly 0
-                const int k0 = kb * BK + 32 * hk;
-                while (ocol < k0 + 32) {
-                    if (ocol >= k0) {
-                        const int kk = ocol - kb * BK;
-                        *reinterpret_cast<uint16_t*>(at + r * 128 + (((kk >> 3) ^ rsw) << 4) + (tc::perm8_pos(kk) << 1)) =
-                            oval;
-                    }
-                    ocol = ncol;
-                    oval = nval;
-                    if (++op + 1 < oe) {
-                        ncol = ocolp[op + 1];
-                        nval = ovalp[op + 1];
-                    } else {
-                        ncol = 0x7FFFFFFF;
-                    }
-                }
-                ptx::fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) {
-                    ptx::mbar_arrive(full_a(sa));
-                    // the packed slot goes back to its producer only after the
-                    // stores that consumed its codes
-                    if (sub == PK - 1 || kb == KB - 1) ptx::mbar_arrive(empty_p(sp));
-                }
-                if (++sa == SA) { sa = 0; pa ^= 1u; }
+            const int kb0 = kp * PK + grp, kb1 = kb0 + kGroups;
+            const bool v0 = kb0 < KB, v1 = kb1 < KB;   // uniform over the CTA
+            uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
+            if (v0) w0 = *reinterpret_cast<const uint4*>(pt + src0);
+            if (v1) w1 = *reinterpret_cast<const uint4*>(pt + src1);
+            const int sa0 = kb0 % SA, sa1 = kb1 % SA;   // slots of parity grp
+            bool free_ok = true;
+            if (v0) free_ok = ptx::mbar_wait(empty_a(sa0), ((uint32_t)(kb0 / SA) & 1u) ^ 1u);
+            if (v1 && free_ok) free_ok = ptx::mbar_wait(empty_a(sa1), ((uint32_t)(kb1 / SA) & 1u) ^ 1u);
+            ok = __all_sync(0xffffffffu, free_ok);
+            if (!ok) break;
+            unsigned char* at0 = atile0 + sa0 * A_BYTES;
+            unsigned char* at1 = atile0 + sa1 * A_BYTES;
+            if (v0) deq_block(w0, kb0, at0);
+            if (v1) deq_block(w1, kb1, at1);
+            if (v0) patch(kb0, at0);
+            if (v1) patch(kb1, at1);
+            ptx::fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+                if (v0) ptx::mbar_arrive(full_a(sa0));
+                if (v1) ptx::mbar_arrive(full_a(sa1));
+                // the packed slot goes back to its producer once per warp, after
+                // the stores that consumed its codes
+                ptx::mbar_arrive(empty_p(sp));
             }
             if (++sp == SP) { sp = 0; pp ^= 1u; }
         }
@@ -315,12 +337,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(acc_full, 0));
         if (ok) {
             ptx::tc_fence_after();
-            const int q = warp & 3, half = warp >> 2;   // TMEM lanes 32q.., column chunks of parity `half`
+            // warp w reads TMEM lanes 32 (w % 4).. and every 4th 16-column chunk from w / 4
+            const int q = warp & 3, c0 = warp >> 2;
             const int nrow = n0 + 32 * q + lane;
-            for (int c = half; 16 * c < NB; c += 2) {
-                uint32_t v[16];
+            for (int c = c0; 16 * c < NB; c += kDeqWarps / 4) {
+                uint32_t v[16], v1[16];
                 ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(16 * c), v);
+                ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(NBMAX + 16 * c), v1);
                 ptx::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; j++)   // accumulator 1 holds blocks 1, 3, ... (none when K = 64)
+                    if (KB > 1) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v1[j]));
                 if (nrow < a.N) {
 #pragma unroll
                     for (int j = 0; j < 16; j++) {

@@ -180,29 +180,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == kWarpMma) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = ptx::idesc_f16_f32(MH, BN);
-            int sa = 0, sb = 0;
-            uint32_t pa = 0, pb = 0;
-            for (int kb = 0; kb < KB; kb++) {
-                if (!ptx::mbar_wait(full_a(sa), pa) || !ptx::mbar_wait(full_b(sb), pb)) { ok = false; break; }
-                ptx::tc_fence_after();
-                // tokens [0, 128) into columns [0, 256), tokens [128, 256) into [256, 512):
-                // the fp16 weight tile is read by both
+        // ------------------------------------------------ MMA issuer (the whole warp runs the loop; one elected lane issues)
+        constexpr uint32_t idesc = ptx::idesc_f16_f32(MH, BN);
+        const uint64_t adesc0 = ptx::sw128_desc(a_tile(0)), bdesc0 = ptx::sw128_desc(b_tile(0));
+        int sa = 0, sb = 0;
+        uint32_t pa = 0, pb = 0;
+        for (int kb = 0; kb < KB; kb++) {
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait(full_a(sa), pa) && ptx::mbar_wait(full_b(sb), pb));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            // descriptors advance by (byte offset >> 4) in their address field; tokens
+            // [0, 128) into columns [0, 256), tokens [128, 256) into [256, 512): the fp16
+            // weight tile is read by both
+            const uint64_t ad = adesc0 + (uint64_t)((sa * A_BYTES) >> 4);
+            const uint64_t bd = bdesc0 + (uint64_t)((sb * B_BYTES) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; kk++) {
-                    const uint64_t bd = ptx::sw128_desc(b_tile(sb) + 32 * kk);
-                    ptx::mma_f16(tmem, ptx::sw128_desc(a_tile(sa) + 32 * kk), bd, idesc, (kb | kk) != 0);
-                    ptx::mma_f16(tmem + BN, ptx::sw128_desc(a_tile(sa) + MH * 128 + 32 * kk), bd, idesc, (kb | kk) != 0);
-                }
-                ptx::tc_commit(empty_a(sa));
-                ptx::tc_commit(empty_b(sb));
-                if (++sa == SA) { sa = 0; pa ^= 1u; }
-                if (++sb == SB) { sb = 0; pb ^= 1u; }
+            for (int kk = 0; kk < BK / 16; kk++) {
+                ptx::mma_f16_elect(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                ptx::mma_f16_elect(tmem + BN, ad + ((MH * 128) >> 4) + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
             }
-            ptx::tc_commit(acc_full);
+            ptx::tc_commit_elect(empty_a(sa));
+            ptx::tc_commit_elect(empty_b(sb));
+            if (++sa == SA) { sa = 0; pa ^= 1u; }
+            if (++sb == SB) { sb = 0; pb ^= 1u; }
         }
+        ptx::tc_commit_elect(acc_full);
     } else {
         // ------------------------------------------------ dequantization (two threads per row)
         const uint32_t magic = a.magic;

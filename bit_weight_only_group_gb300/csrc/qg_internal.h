@@ -51,7 +51,7 @@ qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const
 // Grouped product on the tensor cores (4-bit, K a multiple of 64, at most 32
 // experts): tokens of an expert in chunks of kMoeTcChunk; x16p is workspace
 // for x gathered in routed order (moe_tc_x16_bytes).
-constexpr int kMoeTcChunk = 256;
+constexpr int kMoeTcChunk = 128;
 bool moe_tc_eligible(const qg_qweight* experts, int E);
 size_t moe_tc_x16_bytes(int P, int K);
 qg_status launch_moe_tc(const uint16_t* x, int T, int k, const qg_qweight* experts, int E, void* y, qg_ydtype yt,
