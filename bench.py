@@ -60,8 +60,8 @@ def parse():
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum over the 7
 # launches of a layer, profiles/k_gemv_decode_70b_stack_m1.md), valid only
 # for the kernel source it was taken on.
-DECODE_TRAFFIC = {"kernel_sha256": "9e7abb4bbec6f55570aacc0650cc7e5292300641869cfbf4e1f17552675fa5ca",
-                  "bytes_per_layer": 454.208e6}
+DECODE_TRAFFIC = {"kernel_sha256": "33a2ce3634579b9750ec531ed8626f8458f7f9ee4ba651ed1d3132184d7b8167",
+                  "bytes_per_layer": 454.200e6}
 
 
 def decode_traffic(n_layers):
@@ -203,6 +203,18 @@ def layer_bytes(qg, L, M):
     return packed, packed + rest + io
 
 
+def check_graph_covers(g, ys, what):
+    """Replay the captured step once over outputs filled with NaN: every
+    product must have written its output, or work escaped the capture."""
+    for y in ys:
+        y.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    missing = [i for i, y in enumerate(ys) if not torch.isfinite(y).all()]
+    if missing:
+        raise RuntimeError(f"{what}: the captured step did not compute products {missing[:10]}")
+
+
 def time_graph(g, steps, warmup, world, clocks=False):
     clk = Clocks() if clocks else None
     if clk:
@@ -238,12 +250,16 @@ def run_decode(qg, args, world, rank, P):
     xs = [x_ffn if L.K == 28672 else x_hid for L in layers]
     ys = [torch.empty((M, L.N), dtype=torch.float32, device=dev) for L in layers]
 
-    main = torch.cuda.current_stream()
     side = [torch.cuda.Stream(), torch.cuda.Stream()]
 
     def step():
         # one token through the stack; projections that share an input run as
-        # parallel graph branches: {q, k, v} -> o -> {gate, up} -> down
+        # parallel graph branches: {q, k, v} -> o -> {gate, up} -> down.  The
+        # fork and join events are taken on the stream current at call time:
+        # under graph capture that is the capture stream, so the side streams
+        # join the capture (an event from any other stream would leave their
+        # work outside the graph)
+        main = torch.cuda.current_stream()
         for li in range(0, len(layers), 7):
             run = lambda j, s=None: qg.qgemm_forward(xs[li + j], qws[li + j], out=ys[li + j], stream=s)
             fork = torch.cuda.Event()
@@ -277,6 +293,7 @@ def run_decode(qg, args, world, rank, P):
     with torch.cuda.graph(g):
         step()
     torch.cuda.synchronize()
+    check_graph_covers(g, ys, "decode step")
 
     ms, clocks = time_graph(g, args.steps, args.warmup, world, clocks=True)
     ms_max = max_over_ranks(ms, world)
@@ -340,17 +357,48 @@ def run_prefill(qg, args, P):
     xs = [x_ffn if L.K == 28672 else x_hid for L in layers]
     ys = [torch.empty((M, L.N), dtype=torch.float32, device=dev) for L in layers]
     wsb = max(qg.qgemm_workspace_size(M, q) for q in qws)
-    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    # one workspace per concurrent product (each holds its fp16 copy of x)
+    wss = [torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev) for _ in range(3)]
+    side = [torch.cuda.Stream(), torch.cuda.Stream()]
 
     def step():
-        for x, q, y in zip(xs, qws, ys):
-            qg.qgemm_forward(x, q, out=y, workspace=ws)
+        # the layer's dependency structure, as in the decode step: {q, k, v} -> o -> {gate, up} -> down,
+        # products that share an input as parallel graph branches (fork and join on the stream current
+        # at call time, the capture stream under graph capture)
+        main = torch.cuda.current_stream()
+        run = lambda j, w, s=None: qg.qgemm_forward(xs[j], qws[j], out=ys[j], workspace=w, stream=s)
+        fork = torch.cuda.Event()
+        fork.record(main)
+        done = []
+        for sj, j, w in zip(side, (1, 2), wss[1:]):
+            sj.wait_event(fork)
+            with torch.cuda.stream(sj):
+                run(j, w, sj)
+                e = torch.cuda.Event()
+                e.record(sj)
+                done.append(e)
+        run(0, wss[0])
+        for e in done:
+            main.wait_event(e)
+        run(3, wss[0])
+        fork = torch.cuda.Event()
+        fork.record(main)
+        side[0].wait_event(fork)
+        with torch.cuda.stream(side[0]):
+            run(5, wss[1], side[0])
+            e = torch.cuda.Event()
+            e.record(side[0])
+        run(4, wss[0])
+        main.wait_event(e)
+        run(6, wss[0])
 
     step()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         step()
+    torch.cuda.synchronize()
+    check_graph_covers(g, ys, "prefill step")
     steps = max(3, min(20, args.steps // 10))
     ms, _ = time_graph(g, steps, 3, 1)
     flops = sum(2.0 * M * L.N * L.K for L in layers)
@@ -358,7 +406,7 @@ def run_prefill(qg, args, P):
     del qws, g
     torch.cuda.empty_cache()
     return {"metric": "qGEMM TFLOP/s at M=2048", "value": round(tflops, 1), "unit": "TFLOP/s",
-            "ms_per_step": ms / steps, "config": "one 70B-shaped layer (7 products), INT4 g128, 0.1% outliers",
+            "ms_per_step": ms / steps, "config": "one 70B-shaped layer (7 products; q/k/v and gate/up as parallel graph branches), INT4 g128, 0.1% outliers",
             "frac_of_bf16_peak": round(tflops / P["bf16"], 4)}
 
 
@@ -390,6 +438,8 @@ def run_moe(qg, args):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         step()
+    torch.cuda.synchronize()
+    check_graph_covers(g, list(ys.values()), "MoE step")
     steps = max(5, min(50, args.steps))
     # the layer's weights fit in L2; write a buffer larger than L2 between steps
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
