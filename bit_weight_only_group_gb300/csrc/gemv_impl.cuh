@@ -425,6 +425,18 @@ __device__ __forceinline__ void mma_group(const uint32_t (&w0)[Chunk<BITS, G>::N
     }
 }
 
+// Programmatic dependent launch.  The dense decode kernels are launched with
+// programmatic stream serialization, so that the next one can be resident and
+// have its first weight groups in registers while this one drains: a kernel
+// reads only weight data (codes, group parameters, outlier CSR) before
+// griddepcontrol.wait, which returns once the grids it depends on have
+// completed and their writes are visible; x and y are touched only after it.
+// The kernel immediately preceding a decode product on its stream therefore
+// must not write that product's weights (the quantizer ends with an empty
+// kernel for this reason).  Dependents are released after the main loop.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Cluster barrier in two halves, and an fp32 add into another CTA's shared
 // memory (distributed shared memory of the thread-block cluster).
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
@@ -659,6 +671,7 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     OutCursor oc;
     oc.init(a, splits);
 
+    pdl_wait();   // weight loads are in flight; x may come from the preceding kernel
     const int S = splits;
     if (ngrp > 0) stage_x<BITS, G, MP>(a, g_begin * G, min(C::XG, ngrp), smem, blockDim.x);
     __syncthreads();
@@ -694,6 +707,7 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
         xoff += D * C::GSTRIDE;
     }
 
+    pdl_release();
     tile_epilogue<BITS, G, MP>(a, splits, C::slot_offset(gpsplit), yacc, oc);
 }
 
@@ -788,7 +802,7 @@ qg_status allow_smem(K kernel, int bytes)
 }
 
 template <typename K, typename... A>
-qg_status launch_cluster(K kernel, dim3 grid, int S, unsigned threads, size_t smem_bytes, cudaStream_t s,
+qg_status launch_cluster(K kernel, dim3 grid, int S, unsigned threads, size_t smem_bytes, bool pdl, cudaStream_t s,
                          A... args)
 {
     if (smem_bytes > 48 * 1024) {
@@ -800,13 +814,15 @@ qg_status launch_cluster(K kernel, dim3 grid, int S, unsigned threads, size_t sm
     cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = (unsigned)S;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     return QG_OK;
@@ -820,7 +836,11 @@ qg_status dense_mp(const Problem& p, cudaStream_t s)
     const int S = choose_splits(tiles, ng);
     const dim3 grid((unsigned)tiles, (unsigned)S, 1);
     const int gps = (int)ceil_div(ng, S);
-    return launch_cluster(k_gemv<BITS, G, MP>, grid, S, kWarps * 32, (size_t)Cfg<BITS, G, MP>::smem(gps, S), s, p, S, gps);
+    // programmatic dependent launch where K is split across a cluster: the
+    // cluster reduction leaves a tail the next product's start can overlap;
+    // measured slower for unsplit grids (their early dependents crowd the SMs)
+    return launch_cluster(k_gemv<BITS, G, MP>, grid, S, kWarps * 32, (size_t)Cfg<BITS, G, MP>::smem(gps, S), S > 1, s, p,
+                          S, gps);
 }
 
 template <int BITS, int G, int MP>
@@ -831,7 +851,7 @@ qg_status grouped_mp(const MoeTable& t, int max_items, int expect_items, cudaStr
     const int S = choose_splits((long long)tiles * std::max(1, expect_items), ng);
     const int gps = (int)ceil_div(ng, S);
     return launch_cluster(k_gemv_moe<BITS, G, MP>, dim3((unsigned)tiles, (unsigned)S, (unsigned)max_items), S,
-                          kWarps * 32, (size_t)Cfg<BITS, G, MP>::smem(gps, S), s, t, S, gps);
+                          kWarps * 32, (size_t)Cfg<BITS, G, MP>::smem(gps, S), false, s, t, S, gps);
 }
 
 template <int BITS, int G, template <int, int, int> class F, typename... Args>

@@ -482,6 +482,12 @@ __global__ void k_quant_codebook(const unsigned short* __restrict__ W, int N, in
 
 size_t quantize_workspace_bytes(int N, int /*K*/) { return ws_layout(N, nullptr, nullptr); }
 
+// Launched after the quantizer's kernels: a decode product that reads these
+// weights next on the stream may start its weight loads before the kernel
+// preceding it has finished (programmatic dependent launch), so that kernel
+// must not be one that wrote the weights.
+__global__ void k_quant_done() {}
+
 qg_status launch_quantize(const uint16_t* W, float /*frac*/, const qg_qweight& w, void* ws,
                           cudaStream_t s)
 {
@@ -540,6 +546,7 @@ qg_status launch_quantize(const uint16_t* W, float /*frac*/, const qg_qweight& w
             k_quant_affine<128><<<blocks, threads, 0, s>>>(Wh, w.N, w.K, w.bits, rp, w.out_col, w.packed,
                                                            w.scale, w.zp);
     }
+    k_quant_done<<<1, 32, 0, s>>>();
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
     return QG_OK;

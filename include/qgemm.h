@@ -178,6 +178,14 @@ QG_API qg_status qgemm_workspace_size(int32_t M, const qg_qweight* w, size_t* by
  * K across a thread-block cluster); larger M runs the tensor-core kernel
  * (tcgen05 with TMEM accumulators), which converts x to fp16 in the workspace.
  * `ws` may be NULL when qgemm_workspace_size reports 0.
+ * Ordering: the decode kernel is launched with programmatic dependent launch,
+ * so it may start, and read the weight buffers (packed, scale, zp, codebook,
+ * outlier CSR), before the kernel launched just before it on the same stream
+ * has finished; it reads x and writes y only after that kernel has completed.
+ * The kernel launched immediately before qgemm_forward on the stream must
+ * therefore not write w's buffers (qpack_quantize ends with an empty kernel,
+ * and copies are not kernels, so quantizing or uploading on the same stream
+ * just before is safe).
  * Errors: QG_ERR_INVALID_ARG, QG_ERR_ALIGNMENT, QG_ERR_WORKSPACE, QG_ERR_CUDA.
  */
 QG_API qg_status qgemm_forward(const uint16_t* x, int32_t M, int32_t ldx, const qg_qweight* w, void* y,
