@@ -31,7 +31,8 @@ Y_F32, Y_BF16 = 0, 1
 
 ABI_FUNCTIONS = ("qpack_query_sizes", "qpack_workspace_size", "qpack_quantize", "qpack_quantize_noalloc",
                  "qgemm_workspace_size",
-                 "qgemm_forward", "qgemm_moe_workspace_size", "qgemm_moe_grouped", "qgemm_device_status",
+                 "qgemm_forward", "qgemm_forward_multi", "qgemm_moe_workspace_size", "qgemm_moe_grouped",
+                 "qgemm_device_status",
                  "qgemm_last_error")
 
 
@@ -72,6 +73,7 @@ def lib() -> ctypes.CDLL:
         L.qgemm_moe_workspace_size.argtypes = [i32, i32, i32, pq, psz]
         L.qgemm_moe_grouped.argtypes = [vp, i32, vp, i32, pq, i32, vp, ctypes.c_int, vp, sz, vp]
         L.qgemm_device_status.argtypes = [pi32, i32]
+        L.qgemm_forward_multi.argtypes = [vp, i32, i32, pq, i32, ctypes.POINTER(vp), pi32, ctypes.c_int, vp, sz, vp]
         for name in ABI_FUNCTIONS[:-1]:
             getattr(L, name).restype = ctypes.c_int
         L.qgemm_last_error.argtypes = []
@@ -219,6 +221,33 @@ def qgemm_forward(x: torch.Tensor, qw: QWeight, out: torch.Tensor | None = None,
                                _ptr(workspace) if need else None, workspace.numel() if need else 0,
                                _stream(stream)), "qgemm_forward")
     return out
+
+
+def qgemm_forward_multi(x: torch.Tensor, qws, outs=None, out_dtype: torch.dtype = torch.float32,
+                        workspace: torch.Tensor | None = None, stream=None):
+    """[y_q [M, N_q] for each weight]: the products of x with up to four
+    weights that share K, bits and group, in one call."""
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D bfloat16 CUDA tensor with unit inner stride")
+    M = x.shape[0]
+    if outs is None:
+        outs = [torch.empty((M, q.N), dtype=out_dtype, device=x.device) for q in qws]
+    if len(outs) != len(qws):
+        raise ValueError("one output per weight")
+    yt = Y_BF16 if outs[0].dtype == torch.bfloat16 else Y_F32
+    for o in outs:
+        if o.dtype != outs[0].dtype or o.dtype not in (torch.float32, torch.bfloat16) or o.stride(1) != 1:
+            raise ValueError("outputs must share one dtype (float32 or bfloat16) with unit inner stride")
+    need = max(qgemm_workspace_size(M, q) for q in qws)
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    descs = _desc_array(qws)
+    ys = (ctypes.c_void_p * len(outs))(*[o.data_ptr() for o in outs])
+    ld = (ctypes.c_int32 * len(outs))(*[o.stride(0) for o in outs])
+    _check(lib().qgemm_forward_multi(_ptr(x), M, x.stride(0), descs, len(qws), ys, ld, yt,
+                                     _ptr(workspace) if need else None, workspace.numel() if need else 0,
+                                     _stream(stream)), "qgemm_forward_multi")
+    return outs
 
 
 def _desc_array(experts):

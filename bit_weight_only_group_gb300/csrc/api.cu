@@ -160,6 +160,43 @@ qg_status qpack_quantize(const uint16_t* W, float outlier_frac, const qg_qweight
     return launch_quantize(W, outlier_frac, *out, ws, static_cast<cudaStream_t>(stream));
 }
 
+qg_status qgemm_forward_multi(const uint16_t* x, int32_t M, int32_t ldx, const qg_qweight* ws, int32_t n,
+                              void* const* ys, const int32_t* ldys, qg_ydtype yt, void* work, size_t work_bytes,
+                              void* stream)
+{
+    if (n < 1 || n > kMultiMax) return fail(QG_ERR_INVALID_ARG, "qgemm_forward_multi: n=%d not in 1..%d", n, kMultiMax);
+    if (!ws || !ys || !ldys) return fail(QG_ERR_INVALID_ARG, "qgemm_forward_multi: null ws/ys/ldys");
+    for (int q = 0; q < n; q++) {
+        qg_status st = check_qweight(&ws[q], "qgemm_forward_multi");
+        if (st != QG_OK) return st;
+        if (ws[q].K != ws[0].K || ws[q].bits != ws[0].bits || ws[q].group != ws[0].group)
+            return fail(QG_ERR_INVALID_ARG, "qgemm_forward_multi: weights differ in K/bits/group");
+    }
+    if (M < 0) return fail(QG_ERR_INVALID_ARG, "qgemm_forward_multi: M < 0");
+    if (M == 0) return QG_OK;
+    if (!x) return fail(QG_ERR_INVALID_ARG, "qgemm_forward_multi: x is null");
+    if (ldx < ws[0].K) return fail(QG_ERR_INVALID_ARG, "qgemm_forward_multi: ldx=%d < K=%d", ldx, ws[0].K);
+    if (yt != QG_Y_F32 && yt != QG_Y_BF16) return fail(QG_ERR_INVALID_ARG, "qgemm_forward_multi: bad y dtype");
+    if (!aligned(x, 2)) return fail(QG_ERR_ALIGNMENT, "qgemm_forward_multi: x misaligned");
+    for (int q = 0; q < n; q++) {
+        if (!ys[q]) return fail(QG_ERR_INVALID_ARG, "qgemm_forward_multi: ys[%d] is null", q);
+        if (ldys[q] < ws[q].N) return fail(QG_ERR_INVALID_ARG, "qgemm_forward_multi: ldys[%d] < N", q);
+        if (!aligned(ys[q], yt == QG_Y_F32 ? 4 : 2)) return fail(QG_ERR_ALIGNMENT, "qgemm_forward_multi: ys[%d] misaligned", q);
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (M <= kGemvMaxM) return launch_gemv_multi(x, M, ldx, ws, n, ys, ldys, yt, s);
+    // above the decode range: one tensor-core product after the other in the caller's workspace
+    for (int q = 0; q < n; q++) {
+        const size_t need = gemm_workspace_bytes(M, ws[q]);
+        if (need && (!work || work_bytes < need))
+            return fail(QG_ERR_WORKSPACE, "qgemm_forward_multi: workspace %zu bytes < %zu", work ? work_bytes : (size_t)0, need);
+        if (need && !aligned(work, 256)) return fail(QG_ERR_ALIGNMENT, "qgemm_forward_multi: workspace must be 256-byte aligned");
+        qg_status st = launch_gemm(x, M, ldx, ws[q], ys[q], ldys[q], yt, work, work_bytes, s);
+        if (st != QG_OK) return st;
+    }
+    return QG_OK;
+}
+
 qg_status qgemm_workspace_size(int32_t M, const qg_qweight* w, size_t* bytes)
 {
     if (!bytes) return fail(QG_ERR_INVALID_ARG, "bytes is null");

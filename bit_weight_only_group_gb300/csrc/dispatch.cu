@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "gemv_impl.cuh"
@@ -12,10 +13,15 @@
 namespace qg {
 namespace gemv {
 extern template qg_status launch_dense<2>(const Problem&, int, cudaStream_t);
+extern template qg_status launch_multi<2>(const MultiTable&, int, cudaStream_t);
 extern template qg_status launch_dense<3>(const Problem&, int, cudaStream_t);
+extern template qg_status launch_multi<3>(const MultiTable&, int, cudaStream_t);
 extern template qg_status launch_dense<4>(const Problem&, int, cudaStream_t);
+extern template qg_status launch_multi<4>(const MultiTable&, int, cudaStream_t);
 extern template qg_status launch_dense<5>(const Problem&, int, cudaStream_t);
+extern template qg_status launch_multi<5>(const MultiTable&, int, cudaStream_t);
 extern template qg_status launch_dense<6>(const Problem&, int, cudaStream_t);
+extern template qg_status launch_multi<6>(const MultiTable&, int, cudaStream_t);
 extern template qg_status launch_grouped<2>(const MoeTable&, int, int, int, int, cudaStream_t);
 extern template qg_status launch_grouped<3>(const MoeTable&, int, int, int, int, cudaStream_t);
 extern template qg_status launch_grouped<4>(const MoeTable&, int, int, int, int, cudaStream_t);
@@ -194,6 +200,28 @@ qg_status launch_gemv(const uint16_t* x, int M, int ldx, const qg_qweight& w, vo
                       qg_ydtype yt, cudaStream_t s)
 {
     return dense_by_bits(make_problem(x, M, ldx, w, y, ldy, yt), w.bits, w.group, s);
+}
+
+qg_status launch_gemv_multi(const uint16_t* x, int M, int ldx, const qg_qweight* ws, int n, void* const* ys,
+                            const int32_t* ldys, qg_ydtype yt, cudaStream_t s)
+{
+    static_assert(kMultiMax == gemv::kMultiMax, "one limit on products per launch");
+    gemv::MultiTable t;
+    memset(&t, 0, sizeof(t));
+    t.n = n;
+    t.tile_start[0] = 0;
+    for (int q = 0; q < n; q++) {
+        t.p[q] = make_problem(x, M, ldx, ws[q], ys[q], ldys[q], yt);
+        t.tile_start[q + 1] = t.tile_start[q] + (int)ceil_div(ws[q].N, gemv::kRowsPerCta);
+    }
+    for (int q = n; q < gemv::kMultiMax; q++) t.tile_start[q + 1] = t.tile_start[n];
+    switch (ws[0].bits) {
+        case 2: return gemv::launch_multi<2>(t, ws[0].group, s);
+        case 3: return gemv::launch_multi<3>(t, ws[0].group, s);
+        case 4: return gemv::launch_multi<4>(t, ws[0].group, s);
+        case 5: return gemv::launch_multi<5>(t, ws[0].group, s);
+        default: return gemv::launch_multi<6>(t, ws[0].group, s);
+    }
 }
 
 // Products with M above the decode kernel's range, in 64-row passes of the

@@ -467,7 +467,7 @@ struct OutCursor {
     int p, end, row, stride;
     int col[OU];
     uint32_t val[OU];
-    __device__ __forceinline__ void init(const Problem& a, int splits)
+    __device__ __forceinline__ void init(const Problem& a, int splits, int tile)
     {
         row = (int)(threadIdx.x >> 1);
         stride = 2 * splits;
@@ -478,7 +478,7 @@ struct OutCursor {
             col[u] = -1;
             val[u] = 0u;
         }
-        const int n = blockIdx.x * kRowsPerCta + row;
+        const int n = tile * kRowsPerCta + row;
         if (a.nnz > 0 && threadIdx.x < 2 * kRowsPerCta && n < a.N) {
             p = __ldg(a.row_ptr + n) + 2 * (int)blockIdx.y + (int)(threadIdx.x & 1);
             end = __ldg(a.row_ptr + n + 1);
@@ -501,7 +501,7 @@ struct OutCursor {
 // x block at the start of shared memory is reused for the partial sums, and
 // the split-K slots start at byte slot_off.
 template <int BITS, int G, int MP>
-__device__ __forceinline__ void tile_epilogue(const Problem& a, int splits, int slot_off,
+__device__ __forceinline__ void tile_epilogue(const Problem& a, int splits, int slot_off, int tile,
                                               const float (&yacc)[Cfg<BITS, G, MP>::NT][4], OutCursor& oc)
 {
     using C = Cfg<BITS, G, MP>;
@@ -581,7 +581,7 @@ __device__ __forceinline__ void tile_epilogue(const Problem& a, int splits, int 
     const int row_lo = rank * kRowsPerCta / S, rows_per = (rank + 1) * kRowsPerCta / S - row_lo;
     for (int it = threadIdx.x; it < rows_per * Mv; it += blockDim.x) {
         const int m = it / rows_per, lr = it % rows_per, rl = row_lo + lr;
-        const int n = blockIdx.x * kRowsPerCta + rl;
+        const int n = tile * kRowsPerCta + rl;
         if (n < a.N) {
             float v;
             if (S > 1) {
@@ -600,7 +600,7 @@ __device__ __forceinline__ void tile_epilogue(const Problem& a, int splits, int 
 }
 
 template <int BITS, int G, int MP>
-__device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsplit)
+__device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsplit, int tile)
 {
     using C = Cfg<BITS, G, MP>;
     constexpr int NW = C::NW, D = C::D, NT = C::NT;
@@ -611,7 +611,7 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = lane & 3, gq = lane >> 2;
     const uint32_t magic = a.magic;
-    const int row_base = blockIdx.x * kRowsPerCta + warp * 16 + gq;
+    const int row_base = tile * kRowsPerCta + warp * 16 + gq;
     const int r0 = min(row_base, a.N - 1), r1 = min(row_base + 8, a.N - 1);
     const int ng = a.K / G;
     const int g_begin = blockIdx.y * gpsplit;
@@ -669,7 +669,7 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     });
 
     OutCursor oc;
-    oc.init(a, splits);
+    oc.init(a, splits, tile);
 
     pdl_wait();   // weight loads are in flight; x may come from the preceding kernel
     const int S = splits;
@@ -708,13 +708,32 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     }
 
     pdl_release();
-    tile_epilogue<BITS, G, MP>(a, splits, C::slot_offset(gpsplit), yacc, oc);
+    tile_epilogue<BITS, G, MP>(a, splits, C::slot_offset(gpsplit), tile, yacc, oc);
 }
 
 template <int BITS, int G, int MP>
 __global__ void __launch_bounds__(kWarps * 32) k_gemv(const Problem p, int splits, int gpsplit)
 {
-    gemv_body<BITS, G, MP>(p, splits, gpsplit);
+    gemv_body<BITS, G, MP>(p, splits, gpsplit, blockIdx.x);
+}
+
+// Several products that share x, M and K (and bits and group) in one launch:
+// the row tiles of product q are blocks [tile_start[q], tile_start[q + 1])
+// of the grid's x dimension; every tile runs the decode body on its product.
+constexpr int kMultiMax = 4;
+struct MultiTable {
+    Problem p[kMultiMax];
+    int tile_start[kMultiMax + 1];
+    int n;
+};
+
+template <int BITS, int G, int MP>
+__global__ void __launch_bounds__(kWarps * 32) k_gemv_multi(const __grid_constant__ MultiTable t, int splits,
+                                                            int gpsplit)
+{
+    int q = 0;
+    while (q + 1 < t.n && (int)blockIdx.x >= t.tile_start[q + 1]) q++;
+    gemv_body<BITS, G, MP>(t.p[q], splits, gpsplit, (int)blockIdx.x - t.tile_start[q]);
 }
 
 // Grouped product over routed experts.  Pairs (token, slot) are sorted by
@@ -758,7 +777,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_gemv_moe(const __grid_constant_
     p.row_ptr = t.row_ptr[e]; p.col = t.col[e]; p.val = t.val[e]; p.nnz = t.nnz[e];
     p.y = t.y; p.ldy = t.N; p.y_bf16 = t.y_bf16;
     p.magic = t.magic;
-    gemv_body<BITS, G, MP>(p, splits, gpsplit);
+    gemv_body<BITS, G, MP>(p, splits, gpsplit, blockIdx.x);
 }
 
 // K split: the cluster size S (1..8) that brings the grid closest to three
@@ -844,6 +863,18 @@ qg_status dense_mp(const Problem& p, cudaStream_t s)
 }
 
 template <int BITS, int G, int MP>
+qg_status multi_mp(const MultiTable& t, cudaStream_t s)
+{
+    const int ng = t.p[0].K / G;
+    const int tiles = t.tile_start[t.n];
+    const int S = choose_splits(tiles, ng);
+    const dim3 grid((unsigned)tiles, (unsigned)S, 1);
+    const int gps = (int)ceil_div(ng, S);
+    return launch_cluster(k_gemv_multi<BITS, G, MP>, grid, S, kWarps * 32, (size_t)Cfg<BITS, G, MP>::smem(gps, S), S > 1,
+                          s, t, S, gps);
+}
+
+template <int BITS, int G, int MP>
 qg_status grouped_mp(const MoeTable& t, int max_items, int expect_items, cudaStream_t s)
 {
     const int ng = t.K / G;
@@ -873,6 +904,10 @@ struct DenseF {
     static qg_status run(const Problem& p, cudaStream_t s) { return dense_mp<BITS, G, MP>(p, s); }
 };
 template <int BITS, int G, int MP>
+struct MultiF {
+    static qg_status run(const MultiTable& t, cudaStream_t s) { return multi_mp<BITS, G, MP>(t, s); }
+};
+template <int BITS, int G, int MP>
 struct GroupedF {
     static qg_status run(const MoeTable& t, int mi, int ei, cudaStream_t s) { return grouped_mp<BITS, G, MP>(t, mi, ei, s); }
 };
@@ -882,6 +917,13 @@ qg_status launch_dense(const Problem& p, int G, cudaStream_t s)
 {
     const int mp = mp_for(p.M);
     return G == 64 ? by_mp<BITS, 64, DenseF>(mp, p, s) : by_mp<BITS, 128, DenseF>(mp, p, s);
+}
+
+template <int BITS>
+qg_status launch_multi(const MultiTable& t, int G, cudaStream_t s)
+{
+    const int mp = mp_for(t.p[0].M);
+    return G == 64 ? by_mp<BITS, 64, MultiF>(mp, t, s) : by_mp<BITS, 128, MultiF>(mp, t, s);
 }
 
 // t.chunk must equal the padded token count mp.  max_items bounds the

@@ -4,6 +4,7 @@
 namespace qg {
 namespace gemv {
 template qg_status launch_dense<2>(const Problem&, int, cudaStream_t);
+template qg_status launch_multi<2>(const MultiTable&, int, cudaStream_t);
 template qg_status launch_grouped<2>(const MoeTable&, int, int, int, int, cudaStream_t);
 }  // namespace gemv
 }  // namespace qg

@@ -4,6 +4,7 @@
 namespace qg {
 namespace gemv {
 template qg_status launch_dense<3>(const Problem&, int, cudaStream_t);
+template qg_status launch_multi<3>(const MultiTable&, int, cudaStream_t);
 template qg_status launch_grouped<3>(const MoeTable&, int, int, int, int, cudaStream_t);
 }  // namespace gemv
 }  // namespace qg

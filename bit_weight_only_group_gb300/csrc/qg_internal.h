@@ -37,6 +37,11 @@ qg_status launch_gemv(const uint16_t* x, int M, int ldx, const qg_qweight& w, vo
 int* device_status_ptr();
 qg_status read_device_status(int* out, int reset);
 
+// Up to kMultiMax products sharing x (same M, K, bits, group) in one decode launch.
+constexpr int kMultiMax = 4;
+qg_status launch_gemv_multi(const uint16_t* x, int M, int ldx, const qg_qweight* ws, int n, void* const* ys,
+                            const int32_t* ldys, qg_ydtype yt, cudaStream_t s);
+
 // ---------------------------------------------------------------- tensor-core GEMM
 size_t gemm_workspace_bytes(int M, const qg_qweight& w);
 qg_status launch_gemm(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,

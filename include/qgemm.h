@@ -191,6 +191,27 @@ QG_API qg_status qgemm_workspace_size(int32_t M, const qg_qweight* w, size_t* by
 QG_API qg_status qgemm_forward(const uint16_t* x, int32_t M, int32_t ldx, const qg_qweight* w, void* y,
                         int32_t ldy, qg_ydtype yt, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * Several products that share one input in one call (a fused projection,
+ * e.g. the q, k and v, or the gate and up, matrices of a transformer layer):
+ *     ys[q][m, n] = sum_k x[m, k] * (w_hat_q[n, k] + S_q[n, k])   for q < n.
+ * The pages define the single product (bjdmk.com.cn 5414039 page, sections
+ * 2-3); this call computes exactly that product for each weight, so each
+ * ys[q] equals what qgemm_forward would write for ws[q].  In the decode range
+ * (M <= 64) all n products run as one kernel launch over their concatenated
+ * row tiles; above it they run one after the other on the tensor cores in
+ * the caller's workspace (size: the largest qgemm_workspace_size of the ws).
+ *   x     bf16 [M, K], row stride ldx >= K (DEVICE), shared by all products.
+ *   ws    host array of n descriptors, 1 <= n <= 4, same K, bits and group.
+ *   ys    host array of n DEVICE pointers, ys[q] [M, ws[q].N] with row stride
+ *         ldys[q] >= ws[q].N (host array), fp32 or bf16 per `yt`.
+ * Ordering as for qgemm_forward.
+ * Errors: QG_ERR_INVALID_ARG, QG_ERR_ALIGNMENT, QG_ERR_WORKSPACE, QG_ERR_CUDA.
+ */
+QG_API qg_status qgemm_forward_multi(const uint16_t* x, int32_t M, int32_t ldx, const qg_qweight* ws, int32_t n,
+                                     void* const* ys, const int32_t* ldys, qg_ydtype yt, void* work,
+                                     size_t work_bytes, void* stream);
+
 /* Workspace bytes qgemm_moe_grouped needs.  Host-only. */
 QG_API qg_status qgemm_moe_workspace_size(int32_t T, int32_t k, int32_t E, const qg_qweight* experts,
                                    size_t* bytes);

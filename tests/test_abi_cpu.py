@@ -129,6 +129,26 @@ def test_valid_call_without_a_device_reports_cuda_error(qg):
     assert qg.last_error()
 
 
+def test_forward_multi_validation_without_gpu(qg):
+    # bad counts, mismatched weights and null outputs are rejected on the host
+    L = qg.lib()
+    d = _fake_desc(qg)
+    arr = (qg.QgQWeight * 2)(d, d)
+    ys = (ctypes.c_void_p * 2)(0x200000, 0x300000)
+    ld = (ctypes.c_int32 * 2)(d.N, d.N)
+    x = ctypes.c_void_p(0x100000)
+    assert L.qgemm_forward_multi(x, 1, d.K, arr, 0, ys, ld, 0, None, 0, None) == -1
+    assert L.qgemm_forward_multi(x, 1, d.K, arr, 5, ys, ld, 0, None, 0, None) == -1
+    bad = (qg.QgQWeight * 2)(d, d)
+    bad[1].K = d.K * 2
+    assert L.qgemm_forward_multi(x, 1, d.K, bad, 2, ys, ld, 0, None, 0, None) == -1
+    ys0 = (ctypes.c_void_p * 2)(0x200000, None)
+    assert L.qgemm_forward_multi(x, 1, d.K, arr, 2, ys0, ld, 0, None, 0, None) == -1
+    short = (ctypes.c_int32 * 2)(d.N, d.N - 1)
+    assert L.qgemm_forward_multi(x, 1, d.K, arr, 2, ys, short, 0, None, 0, None) == -1
+    assert L.qgemm_forward_multi(x, 0, d.K, arr, 2, ys, ld, 0, None, 0, None) == 0   # M = 0: nothing to do
+
+
 def test_device_status_query_without_gpu(qg):
     # a NULL output is rejected on the host; without a device the read fails
     # with a CUDA status instead of crashing

@@ -161,3 +161,17 @@ def test_tensor_core_path_full_size_sampled(qg):
         n1 = n0 + 64
         wmax = float(np.abs(oracle.dequant(q, n0, n1)).max())
         check_product(y[toks.cuda(), n0:n1], oracle.linear(x[toks], q, n0, n1), x[toks], wmax)
+
+
+@pytest.mark.parametrize("bits,group,M", [(4, 128, 1), (4, 128, 8), (3, 64, 16), (4, 128, 130)])
+def test_forward_multi_against_oracle(qg, bits, group, M):
+    # a fused projection: three weights sharing x (different N, one ragged
+    # tile) in one call; each output is the single product of its weight
+    K = 1024
+    shapes = [(512, 11), (128, 12), (200, 13)]
+    qs = [_weights(N, K, bits, group, 0.002, seed=sd) for N, sd in shapes]
+    x = wl.gen_x(M, K, seed=M + 5)
+    ys = qg.qgemm_forward_multi(x.cuda(), [to_device(q) for q, _ in qs])
+    torch.cuda.synchronize()
+    for (q, wmax), y in zip(qs, ys):
+        check_product(y, oracle.linear(x, q), x, wmax)
