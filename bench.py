@@ -57,11 +57,11 @@ def parse():
 
 
 # DRAM bytes (read + written) per 70B-shaped layer of the decode step, from one
-# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum over the 7
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum over the 5
 # launches of a layer, profiles/k_gemv_decode_70b_stack_m1.md), valid only
 # for the kernel source it was taken on.
-DECODE_TRAFFIC = {"kernel_sha256": "33a2ce3634579b9750ec531ed8626f8458f7f9ee4ba651ed1d3132184d7b8167",
-                  "bytes_per_layer": 454.200e6}
+DECODE_TRAFFIC = {"kernel_sha256": "6f0a8f15b4da0d037a41a61cc85e4430f3a5cf490983b533d151bed85a3b6248",
+                  "bytes_per_layer": 453.956e6}
 
 
 def decode_traffic(n_layers):
@@ -308,8 +308,8 @@ def run_decode(qg, args, world, rank, P):
     achieved = allb / per_step_s / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": P["hbm"], "unit": "GB/s",
             "frac": round(achieved / P["hbm"], 4), "traffic": decode_traffic(len(layers) // 7),
-            "traffic_unit": "bytes per step (the achieved figure is per step: the step is 560 launches of this kernel)",
-            "kernel": "k_gemv<4,128,1> (decode qGEMV, the only kernel of the step)",
+            "traffic_unit": "bytes per step (the achieved figure is per step: the step is 400 launches of this kernel)",
+            "kernel": "k_gemv<4,128,1> / k_gemv_multi<4,128,1> (decode qGEMV, the only kernel of the step)",
             "peak_source": P["src"] + " hbm_gbs"}
     out = dict(value=value, ms_per_step=ms_max / args.steps, roofline=roof, e2e=e2e, clocks=clocks,
                gpu_launches=(len(layers) // 7) * 5 * args.steps, setup_s=round(setup_s, 1),
