@@ -36,6 +36,26 @@ qg_status cuda_fail(cudaError_t e, const char* what)
     return QG_ERR_CUDA;
 }
 
+// Dynamic shared memory per CTA that lets at most `cap` CTAs share an SM.
+int smem_for_cap(int cap)
+{
+    static int cache[64][2] = {};   // per device: shared memory per SM, reserved per CTA
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    if (!cache[dev][0]) {
+        int per_sm = 0, reserved = 0;
+        if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+            per_sm <= 0)
+            per_sm = 233472;
+        if (cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+            reserved < 0)
+            reserved = 1024;
+        cache[dev][1] = reserved;
+        cache[dev][0] = per_sm;
+    }
+    return cache[dev][0] / (cap + 1) - cache[dev][1] + 16;   // (cap + 1) CTAs no longer fit, cap still do
+}
+
 int num_sms()
 {
     static int cache[64] = {0};

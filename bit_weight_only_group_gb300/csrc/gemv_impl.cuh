@@ -295,15 +295,21 @@ struct Cfg {
     // split-K slots: rank r receives [S][ceil(64/S)][NTOK] partials of its rows (S <= 8)
     static constexpr int SLOT_BYTES = (kRowsPerCta + 8) * NTOK * 4;
     static constexpr int XS_BUDGET = 49152 - SLOT_BYTES;
-    static constexpr int D = D_CLAMP < XS_BUDGET / GSTRIDE ? D_CLAMP : XS_BUDGET / GSTRIDE;
-    static constexpr int XG = (XS_BUDGET / GSTRIDE) / D * D;      // groups per x block
+    // affine widths stage the tile's group parameters beside x: one 32-bit
+    // word (fp16 scale | zero-point << 16) per row and group
+    static constexpr int PSTRIDE = BITS == 2 ? 0 : kRowsPerCta * 4;
+    static constexpr int BSTRIDE = GSTRIDE + PSTRIDE;             // block bytes per group
+    static constexpr int D = D_CLAMP < XS_BUDGET / BSTRIDE ? D_CLAMP : XS_BUDGET / BSTRIDE;
+    static constexpr int XG = (XS_BUDGET / BSTRIDE) / D * D;      // groups per x block
     static_assert(XG >= D, "x block smaller than the prefetch ring");
-    // dynamic shared memory for a split of gpsplit groups: the x block (reused
-    // for the partial sums after the main loop), then the split-K slots,
-    // which other ranks may write while this CTA still reads x
+    // dynamic shared memory for a split of gpsplit groups: the x block, the
+    // parameter block (both reused for the partial sums after the main loop),
+    // then the split-K slots, which other ranks may write while this CTA
+    // still reads x
+    __host__ __device__ static int prm_offset(int gpsplit) { return (gpsplit < XG ? gpsplit : XG) * GSTRIDE; }
     __host__ __device__ static int slot_offset(int gpsplit)
     {
-        const int xs = (gpsplit < XG ? gpsplit : XG) * GSTRIDE;
+        const int xs = (gpsplit < XG ? gpsplit : XG) * BSTRIDE;
         return ((xs > RED_BYTES ? xs : RED_BYTES) + 15) / 16 * 16;
     }
     static int smem(int gpsplit, int S) { return slot_offset(gpsplit) + (S > 1 ? SLOT_BYTES : 0); }
@@ -357,6 +363,49 @@ __device__ void stage_x(const Problem& a, int kbase, int ngr, unsigned char* xs,
         uint32_t v[NV];
         load(it, v);
         store(it, v);
+    }
+}
+
+// Stage the scale and zero-point of the tile's 64 rows for the ngr groups
+// starting at matrix group g0, one 32-bit word per (group, row): fp16 scale
+// bits | zero-point << 16, at word (gi * kWarps + row / 16) * 16 + (row % 8) * 2
+// + (row / 8) % 2.  The rows r and r + 8 of a thread are adjacent (one 8-byte
+// shared load per group), and a warp reads 32 contiguous bytes.  Read from
+// global memory as 16-byte runs of 8 groups of a row where the layout allows,
+// else one group at a time.  (Loading the parameters per group inside the
+// streaming loop touched 8 rows' sectors per load and kept the L1 data path
+// busy; staged, they cost a few wavefronts per CTA and group.)
+template <int BITS, int G>
+__device__ void stage_prm(const Problem& a, int tile, int g0, int ngr, uint32_t* ps, int nthr)
+{
+    const int ng = a.K / G;
+    auto word = [](int gi, int rl) { return (gi * kWarps + rl / 16) * 16 + (rl % 8) * 2 + (rl / 8) % 2; };
+    const bool vec = ng % 8 == 0 && g0 % 8 == 0 && (reinterpret_cast<uintptr_t>(a.scale) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(a.zp) & 7u) == 0;
+    if (vec) {
+        const int nch = (ngr + 7) / 8;
+        for (int it = threadIdx.x; it < kRowsPerCta * nch; it += nthr) {
+            const int rl = it % kRowsPerCta, c = it / kRowsPerCta;
+            const int n = min(tile * kRowsPerCta + rl, a.N - 1);
+            const size_t base = (size_t)n * ng + g0 + 8 * c;   // a multiple of 8, and base + 8 <= (n + 1) * ng
+            const uint4 sv = __ldg(reinterpret_cast<const uint4*>(a.scale + base));
+            const uint2 zv = __ldg(reinterpret_cast<const uint2*>(a.zp + base));
+            const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+            const uint32_t zw[2] = {zv.x, zv.y};
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                if (8 * c + j < ngr)
+                    ps[word(8 * c + j, rl)] = ((sw[j / 2] >> (16 * (j & 1))) & 0xFFFFu) |
+                                              (((zw[j / 4] >> (8 * (j & 3))) & 0xFFu) << 16);
+            }
+        }
+    } else {
+        for (int it = threadIdx.x; it < kRowsPerCta * ngr; it += nthr) {
+            const int rl = it % kRowsPerCta, gi = it / kRowsPerCta;
+            const int n = min(tile * kRowsPerCta + rl, a.N - 1);
+            const size_t idx = (size_t)n * ng + g0 + gi;
+            ps[word(gi, rl)] = (uint32_t)__ldg(a.scale + idx) | ((uint32_t)__ldg(a.zp + idx) << 16);
+        }
     }
 }
 
@@ -622,12 +671,10 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     const uint8_t* p0 = a.packed + (size_t)r0 * rowbytes + (size_t)g_begin * GB + t * CB;
     const uint8_t* p1 = a.packed + (size_t)r1 * rowbytes + (size_t)g_begin * GB + t * CB;
     const size_t pidx0 = (size_t)r0 * ng + g_begin, pidx1 = (size_t)r1 * ng + g_begin;
-    const uint16_t* sp0 = a.scale + pidx0;
-    const uint16_t* sp1 = a.scale + pidx1;
-    const uint8_t* zq0 = a.zp + pidx0;
-    const uint8_t* zq1 = a.zp + pidx1;
     const uint2* cq0 = a.cb + pidx0;
     const uint2* cq1 = a.cb + pidx1;
+    // affine: the staged group parameters, this thread's words of block group 0
+    const uint32_t* const ps = reinterpret_cast<const uint32_t*>(smem + C::prm_offset(gpsplit)) + warp * 16 + gq * 2;
 
     // this lane's B-fragment slot (token clamped to MP-1; its column is discarded)
     uint32_t xlo[NT];
@@ -639,9 +686,10 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     for (int i = 0; i < NT; i++) yacc[i][0] = yacc[i][1] = yacc[i][2] = yacc[i][3] = 0.0f;
 
     uint32_t wr[D][2][NW];
-    uint32_t prm[D][2][2];   // affine: scale bits, zp; codebook: two words of 4 fp16
+    uint32_t prm[D][2][2];   // group parameters: affine scale bits, zp; codebook two words of 4 fp16
 
-    // load group (current base + REL) into ring slot SLOT
+    // load group (current base + REL) into ring slot SLOT (codebooks ride the
+    // ring with the codes; affine parameters are staged per x block)
     auto issue = [&](auto slot_c, auto rel_c) {
         constexpr int SLOT = decltype(slot_c)::value, REL = decltype(rel_c)::value;
         Chunk<BITS, G>::load(p0 + REL * GB, wr[SLOT][0]);
@@ -650,17 +698,11 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
             const uint2 c0 = __ldg(cq0 + REL), c1 = __ldg(cq1 + REL);
             prm[SLOT][0][0] = c0.x; prm[SLOT][0][1] = c0.y;
             prm[SLOT][1][0] = c1.x; prm[SLOT][1][1] = c1.y;
-        } else {
-            prm[SLOT][0][0] = __ldg(sp0 + REL);
-            prm[SLOT][1][0] = __ldg(sp1 + REL);
-            prm[SLOT][0][1] = __ldg(zq0 + REL);
-            prm[SLOT][1][1] = __ldg(zq1 + REL);
         }
     };
     auto advance = [&]() {
         p0 += D * GB; p1 += D * GB;
         if constexpr (BITS == 2) { cq0 += D; cq1 += D; }
-        else { sp0 += D; sp1 += D; zq0 += D; zq1 += D; }
     };
 
     static_for<0, D>([&](auto dc) {
@@ -671,25 +713,41 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     OutCursor oc;
     oc.init(a, splits, tile);
 
+    uint32_t* const pblock = reinterpret_cast<uint32_t*>(smem + C::prm_offset(gpsplit));
+    if constexpr (BITS != 2)   // weight data: staged before the dependency wait
+        if (ngrp > 0) stage_prm<BITS, G>(a, tile, g_begin, min(C::XG, ngrp), pblock, blockDim.x);
+
     pdl_wait();   // weight loads are in flight; x may come from the preceding kernel
-    const int S = splits;
     if (ngrp > 0) stage_x<BITS, G, MP>(a, g_begin * G, min(C::XG, ngrp), smem, blockDim.x);
     __syncthreads();
     oc.fetch(a);
 
     int xnext = C::XG;      // group index (relative) at which x is staged next
     uint32_t xoff = 0;      // byte offset of group jj inside the x block
+    int pw = 0;             // word offset of group jj inside the parameter block
     for (int jj = 0; jj < ngrp; jj += D) {
         if (jj == xnext) {
             __syncthreads();
             stage_x<BITS, G, MP>(a, (g_begin + jj) * G, min(C::XG, ngrp - jj), smem, blockDim.x);
+            if constexpr (BITS != 2) stage_prm<BITS, G>(a, tile, g_begin + jj, min(C::XG, ngrp - jj), pblock, blockDim.x);
             __syncthreads();
             xnext += C::XG;
             xoff = 0;
+            pw = 0;
         }
         const unsigned char* xb[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; nt++) xb[nt] = smem + xoff + xlo[nt];
+        if constexpr (BITS != 2) {
+            static_for<0, D>([&](auto dc) {
+                constexpr int d = decltype(dc)::value;
+                if (jj + d < ngrp) {   // only staged groups lie inside the block
+                    const uint2 v = *reinterpret_cast<const uint2*>(ps + pw + d * kWarps * 16);
+                    prm[d][0][0] = v.x; prm[d][0][1] = v.x >> 16;
+                    prm[d][1][0] = v.y; prm[d][1][1] = v.y >> 16;
+                }
+            });
+        }
 
         static_for<0, D>([&](auto dc) {
             constexpr int d = decltype(dc)::value;
@@ -705,6 +763,7 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
         });
         advance();
         xoff += D * C::GSTRIDE;
+        pw += D * kWarps * 16;
     }
 
     pdl_release();
@@ -847,6 +906,17 @@ qg_status launch_cluster(K kernel, dim3 grid, int S, unsigned threads, size_t sm
     return QG_OK;
 }
 
+// Dynamic shared memory of a decode launch.  Clustered (K-split) launches are
+// held to at most four CTAs per SM: cluster placement otherwise packed five
+// CTAs onto some SMs while others ran two or three, and the crowded SMs set
+// the launch's time.
+template <int BITS, int G, int MP>
+size_t decode_smem(int gps, int S)
+{
+    const int need = Cfg<BITS, G, MP>::smem(gps, S);
+    return (size_t)(S > 1 ? std::max(need, smem_for_cap(4)) : need);
+}
+
 template <int BITS, int G, int MP>
 qg_status dense_mp(const Problem& p, cudaStream_t s)
 {
@@ -858,7 +928,7 @@ qg_status dense_mp(const Problem& p, cudaStream_t s)
     // programmatic dependent launch where K is split across a cluster: the
     // cluster reduction leaves a tail the next product's start can overlap;
     // measured slower for unsplit grids (their early dependents crowd the SMs)
-    return launch_cluster(k_gemv<BITS, G, MP>, grid, S, kWarps * 32, (size_t)Cfg<BITS, G, MP>::smem(gps, S), S > 1, s, p,
+    return launch_cluster(k_gemv<BITS, G, MP>, grid, S, kWarps * 32, decode_smem<BITS, G, MP>(gps, S), S > 1, s, p,
                           S, gps);
 }
 
@@ -870,7 +940,7 @@ qg_status multi_mp(const MultiTable& t, cudaStream_t s)
     const int S = choose_splits(tiles, ng);
     const dim3 grid((unsigned)tiles, (unsigned)S, 1);
     const int gps = (int)ceil_div(ng, S);
-    return launch_cluster(k_gemv_multi<BITS, G, MP>, grid, S, kWarps * 32, (size_t)Cfg<BITS, G, MP>::smem(gps, S), S > 1,
+    return launch_cluster(k_gemv_multi<BITS, G, MP>, grid, S, kWarps * 32, decode_smem<BITS, G, MP>(gps, S), S > 1,
                           s, t, S, gps);
 }
 
@@ -882,7 +952,7 @@ qg_status grouped_mp(const MoeTable& t, int max_items, int expect_items, cudaStr
     const int S = choose_splits((long long)tiles * std::max(1, expect_items), ng);
     const int gps = (int)ceil_div(ng, S);
     return launch_cluster(k_gemv_moe<BITS, G, MP>, dim3((unsigned)tiles, (unsigned)S, (unsigned)max_items), S,
-                          kWarps * 32, (size_t)Cfg<BITS, G, MP>::smem(gps, S), false, s, t, S, gps);
+                          kWarps * 32, decode_smem<BITS, G, MP>(gps, S), false, s, t, S, gps);
 }
 
 template <int BITS, int G, template <int, int, int> class F, typename... Args>

@@ -16,6 +16,9 @@ qg_status cuda_fail(cudaError_t e, const char* what);
 
 // Number of SMs of the current device (cached per device).
 int num_sms();
+// Dynamic shared memory per CTA that lets at most `cap` CTAs share an SM of
+// the current device (1 <= cap <= 8).
+int smem_for_cap(int cap);
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
