@@ -252,7 +252,7 @@ qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const
     const int P = T * k;
     const qg_qweight& w0 = experts[0];
     if (p.x16) {
-        // tensor cores: every expert's tokens in chunks of up to 256, weights as the MMA's M side
+        // tensor cores: every expert's tokens in chunks of up to kMoeTcChunk, weights as the MMA's M side
         k_route<<<1, kRouteThreads, 0, s>>>(topk, P, E, kMoeTcChunk, p.offsets, p.perm, p.items, p.n_items);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");

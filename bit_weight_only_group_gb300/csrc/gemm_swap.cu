@@ -1,16 +1,17 @@
 // Grouped (MoE) fused dequantization product on the 5th-generation tensor
 // cores with the roles of the operands swapped: the dequantized weights are
 // the MMA's M side (128 weight rows per CTA) and an expert's tokens are the N
-// side (N = 16 * ceil(tokens / 16), at most 128), so an expert that receives
-// a few dozen tokens costs no padding on the tensor core and its weights are
-// read from HBM once per 128 of its tokens.
+// side (N = 16 * ceil(tokens / 16), at most one routing chunk of 64), so an
+// expert that receives a few dozen tokens costs no padding on the tensor
+// core; an expert with more tokens has several chunks, whose CTAs read the
+// same weight tiles at about the same time (HBM once, L2 after).
 //     y[pair, n] = sum_k x[token(pair), k] * (w_hat_e[n, k] + S_e[n, k])
 //
 // Routing (a stable counting sort of the (token, slot) pairs by expert,
 // bjdmk.com.cn 5648983 page, sections 1-2) is done by the routing kernel;
 // k_gather_x16 then writes x in that order as fp16 with the K positions of
 // every block of 8 permuted (0,4,1,5,2,6,3,7) like the weight operand, and
-// one CTA of k_gemm_swap_u4 computes a 128-row x (up to 128)-token tile:
+// one CTA of k_gemm_swap_u4 computes a 128-row x (up to 64)-token tile:
 //  * warp 16 (one lane) streams the token tile (TMA, 16-row boxes, 128-byte
 //    swizzle) into a ring of up to 16 stages (as many as the token count
 //    allows), warp 17 the packed 4-bit weight tile of the expert (TMA, 128
@@ -18,7 +19,7 @@
 //  * warps 0-15, in two groups taking alternate K blocks (two threads per
 //    weight row), dequantize as the prefill kernel does (masks -> fp16
 //    1024 + 2^p q, one packed FMA -> q - zp, one packed multiply by the fp16
-//    scale, FP16 outliers patched in) into an 8-deep ring of 128 x 64 fp16
+//    scale, FP16 outliers patched in) into a 6-deep ring of 128 x 64 fp16
 //    tiles;
 //  * warp 18 issues four tcgen05.mma (M=128, N=tokens, K=16) per K block from
 //    one elected lane into a TMEM accumulator of 128 lanes x 128 columns;
@@ -49,19 +50,19 @@ constexpr int BW = 128;        // weight rows per CTA (MMA M)
 constexpr int NBMAX = 128;     // tokens per CTA (MMA N, a multiple of 16)
 constexpr int BK = 64;         // K block (one 128-byte fp16 row of an operand tile)
 constexpr int PK = 4;          // K blocks per packed tile (128-byte rows at 4 bits)
-constexpr int SXMAX = 16, SP = 3, SA = 8;   // token ring: up to 16 stages in X_RING bytes
+constexpr int SXMAX = 16, SP = 3, SA = 6;   // token ring: up to 16 stages in X_RING bytes
 // Two groups of 8 dequantization warps take alternate K blocks (group g the
 // blocks 4p + g and 4p + g + 2 of packed tile p, both at once: eight
 // independent unpack chains per thread and one proxy fence per tile), so the
 // per-block latencies overlap; group g writes the fp16 slots of parity g and
-// holds up to four of them (two tiles) ahead of the MMA.
+// holds up to three of them ahead of the MMA.
 constexpr int kGroups = 2, kGroupWarps = 8;
 constexpr int kDeqWarps = kGroups * kGroupWarps;
 static_assert(SA % kGroups == 0, "a group's K blocks map to its own fp16 slots");
 // one MMA issuer warp per group (K blocks of parity g into accumulator g)
 constexpr int kWarpX = kDeqWarps, kWarpP = kDeqWarps + 1, kWarpMma = kDeqWarps + 2;
 constexpr int kThreads = (kDeqWarps + 2 + kGroups) * 32;
-constexpr int X_RING = 3 * NBMAX * BK * 2;   // 48 KB, split into stages of NB x 64 fp16
+constexpr int X_RING = 80 * 1024;           // split into stages of NB x 64 fp16
 constexpr int P_BYTES = BW * PK * BK / 2;    // 16 KB
 constexpr int A_BYTES = BW * BK * 2;         // 16 KB
 constexpr int OFF_P = X_RING;
@@ -269,9 +270,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 4; j++) dst_off[j] = r * 128 + (((4 * hk + j) ^ rsw) << 4);
         unsigned char* const atile0 = smem + OFF_A;
-        auto deq_block = [&](const uint4& w, int kb, unsigned char* at) {
-            const int gi = kb / KB_PER_G;
-            const uint32_t sc = __ldg(sp_row + gi), zq = __ldg(zp_row + gi);
+        // group parameters of this thread's two K blocks of packed tile kp
+        // (scale | zp << 16 each), loaded one packed tile ahead of their use
+        auto load_prm = [&](int kp, uint32_t (&pq)[2]) {
+#pragma unroll
+            for (int b = 0; b < 2; b++) {
+                const int kb = kp * PK + grp + b * kGroups;
+                const int gi = min(kb, KB - 1) / KB_PER_G;
+                pq[b] = (uint32_t)__ldg(sp_row + gi) | ((uint32_t)__ldg(zp_row + gi) << 16);
+            }
+        };
+        auto deq_block = [&](const uint4& w, uint32_t pq, unsigned char* at) {
+            const uint32_t sc = pq & 0xFFFFu, zq = pq >> 16;
             const uint32_t add_lo = zq * 0x00010001u + 0xE400E400u;   // -(1024 + zp)
             const uint32_t add_hi = zq * 0x00100010u + 0xD400D400u;   // -(64 + zp)
             const uint32_t s2 = __byte_perm(sc, 0u, 0x1010u);
@@ -301,7 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int KP = (KB + PK - 1) / PK;
         int sp = 0;
         uint32_t pp = 0;   // parity of full_p to wait for
+        uint32_t pcur[2], pnext[2];
+        load_prm(0, pcur);
         for (int kp = 0; kp < KP && ok; kp++) {
+            if (kp + 1 < KP) load_prm(kp + 1, pnext);
             const unsigned char* pt = p_tile(sp);
             ok = __all_sync(0xffffffffu, ptx::mbar_wait(full_p(sp), pp));
             if (!ok) break;
@@ -318,8 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             unsigned char* at0 = atile0 + sa0 * A_BYTES;
             unsigned char* at1 = atile0 + sa1 * A_BYTES;
-            if (v0) deq_block(w0, kb0, at0);
-            if (v1) deq_block(w1, kb1, at1);
+            if (v0) deq_block(w0, pcur[0], at0);
+            if (v1) deq_block(w1, pcur[1], at1);
             if (v0) patch(kb0, at0);
             if (v1) patch(kb1, at1);
             ptx::fence_proxy_async();
@@ -332,6 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mbar_arrive(empty_p(sp));
             }
             if (++sp == SP) { sp = 0; pp ^= 1u; }
+            pcur[0] = pnext[0];
+            pcur[1] = pnext[1];
         }
         // ------------------------------------------------ epilogue: TMEM (lane = weight row, column = token) -> y
         if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(acc_full, 0));
@@ -412,7 +427,8 @@ static qg_status moe_tc_run(const uint16_t* x, int T, int k, const qg_qweight* e
         a.val[e] = experts[e].out_val;
         a.nnz[e] = experts[e].nnz;
     }
-    a.N = N; a.K = K; a.ng = K / G; a.chunk = NBMAX;
+    static_assert(kMoeTcChunk <= NBMAX && kMoeTcChunk % 16 == 0, "routing chunk fits one CTA's token tile");
+    a.N = N; a.K = K; a.ng = K / G; a.chunk = kMoeTcChunk;
     a.offsets = offsets; a.perm = perm; a.items = items; a.n_items = n_items;
     a.y = y; a.y_bf16 = yt == QG_Y_BF16;
     a.status = device_status_ptr();

@@ -58,8 +58,11 @@ qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const
 
 // Grouped product on the tensor cores (4-bit, K a multiple of 64, at most 32
 // experts): tokens of an expert in chunks of kMoeTcChunk; x16p is workspace
-// for x gathered in routed order (moe_tc_x16_bytes).
-constexpr int kMoeTcChunk = 128;
+// for x gathered in routed order (moe_tc_x16_bytes).  Chunks of 64 tokens
+// keep a token tile's K block at 8 KB, so the token ring holds ten of them;
+// an expert with more tokens reads its weights once per chunk, mostly from
+// L2 (the chunks' CTAs run together).
+constexpr int kMoeTcChunk = 64;
 bool moe_tc_eligible(const qg_qweight* experts, int E);
 size_t moe_tc_x16_bytes(int P, int K);
 qg_status launch_moe_tc(const uint16_t* x, int T, int k, const qg_qweight* experts, int E, void* y, qg_ydtype yt,
