@@ -50,8 +50,9 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--layers", type=int, default=80, help="layers of the 70B-shaped stack")
     ap.add_argument("--no-secondary", action="store_true", help="skip the prefill and MoE lines")
-    ap.add_argument("--mode", choices=("all", "prefill", "moe"), default="all",
-                    help="'prefill' / 'moe': run only that measurement and print its object (profiling runs)")
+    ap.add_argument("--mode", choices=("all", "prefill", "moe", "widths"), default="all",
+                    help="'prefill' / 'moe' / 'widths': run only that measurement and print its object "
+                         "(profiling runs; 'widths' = the mixed-width sweep and the 7B-shaped stack, M=1)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
     return ap.parse_args()
 
@@ -441,6 +442,89 @@ def run_moe(qg, args):
             "l2": "L2 flushed (512 MB write) before each step"}
 
 
+def time_graph_once(step, reps):
+    """Capture step in a CUDA graph and return its mean replay time in ms."""
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_widths(qg, args, P):
+    """Decode (M=1) over the mixed-width sweep -- each layer timed as a graph of
+    copies whose weights exceed L2 -- and one step of the 32-layer 7B-shaped
+    stack with per-layer widths (224 products, one launch each)."""
+    dev = torch.device("cuda")
+    clone = lambda t: None if t is None else t.clone()
+    sweep = []
+    for L in wl.mixed_sweep():
+        W = wl.gen_weight(L.N, L.K, outlier_frac=L.frac, device=dev, distinct_positions=False)
+        q = qg.qpack_quantize(W, L.bits, L.group, L.frac)
+        del W
+        copies = max(4, int(600e6 // q.nbytes()))
+        cs = [q] + [qg.QWeight(q.N, q.K, q.bits, q.group, q.packed.clone(), clone(q.scale), clone(q.zp),
+                               clone(q.codebook), q.row_ptr.clone(), q.col.clone(), q.val.clone(), q.nnz)
+                    for _ in range(copies - 1)]
+        x = wl.gen_x(1, L.K, device=dev)
+        y = torch.empty((1, L.N), device=dev)
+
+        def step():
+            for c in cs:
+                qg.qgemm_forward(x, c, out=y)
+        us = time_graph_once(step, 5) * 1e3 / len(cs)
+        packed = L.N * L.K * L.bits // 8
+        sweep.append({"layer": L.name, "us": round(us, 2), "packed_GBps": round(packed / us / 1e3, 1),
+                      "all_GBps": round(q.nbytes() / us / 1e3, 1)})
+        del cs, q
+        torch.cuda.empty_cache()
+    return {"metric": "decode GB/s at M=1 over widths 2/3/5/6", "sweep": sweep, "stack_7b": run_stack7b(qg, P),
+            "config": "mixed-width sweep 4096x4096 and 11008x4096 x widths {2,3,5,6} x groups {64,128}, 0.1% "
+                      "outliers; 7B-shaped stack 32 layers with per-layer widths, group 128",
+            "l2": "graphs of copies larger than L2 (sweep); 3.2 GB per step (stack)"}
+
+
+def run_stack7b(qg, P):
+    """One decode step (M=1) of the 32-layer 7B-shaped stack with per-layer
+    widths 2 (codebook) / 3 / 5 / 6, group 128, 0.1 % outliers: 224 products,
+    one launch each, in a CUDA graph."""
+    dev = torch.device("cuda")
+    layers = wl.stack_7b()
+    qs = []
+    for i, L in enumerate(layers):
+        W = wl.gen_weight(L.N, L.K, seed=wl.SEED_W + i, outlier_frac=L.frac, device=dev, distinct_positions=False)
+        qs.append(qg.qpack_quantize(W, L.bits, L.group, L.frac))
+        del W
+    xh, xf = wl.gen_x(1, 4096, device=dev), wl.gen_x(1, 11008, device=dev)
+    ys = [torch.empty((1, L.N), device=dev) for L in layers]
+
+    def step7():
+        for L, q, y in zip(layers, qs, ys):
+            qg.qgemm_forward(xf if L.K == 11008 else xh, q, out=y)
+    ms = time_graph_once(step7, 20)
+    packed = sum(L.N * L.K * L.bits // 8 for L in layers)
+    allb = sum(q.nbytes() for q in qs)
+    del qs
+    torch.cuda.empty_cache()
+    return {"metric": "7B-shaped mixed-width stack decode", "value": round(packed / ms / 1e6, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "all_GBps": round(allb / ms / 1e6, 1),
+            "frac_of_hbm_peak": round(allb / ms / 1e6 / P["hbm"], 4), "weights_GB": round(allb / 1e9, 3),
+            "launches": len(layers),
+            "config": "32 layers q/k/v/o 4096x4096, gate/up 11008x4096, down 4096x11008; widths 6 (layers 0, 1, "
+                      "30, 31), else q/k/o 5, v 6, gate/up 2 (codebook), down 2/3/5; group 128, 0.1% outliers, "
+                      "M=1, one launch per product"}
+
+
 # ---------------------------------------------------------------- CPU oracle
 def oracle_sample():
     """A bounded sample of the 70B decode workload for the CPU oracle: 128
@@ -514,7 +598,8 @@ def main():
     qg.lib()
     P = peaks()
     if args.mode != "all":
-        out = run_prefill(qg, args, P) if args.mode == "prefill" else run_moe(qg, args)
+        out = (run_prefill(qg, args, P) if args.mode == "prefill" else
+               run_moe(qg, args) if args.mode == "moe" else run_widths(qg, args, P))
         if rank == 0:
             print(json.dumps(out))
         return 0
@@ -541,6 +626,10 @@ def main():
             line["moe"] = run_moe(qg, args)
         except Exception as e:
             line["moe"] = {"error": repr(e)}
+        try:
+            line["decode_7b_mixed"] = run_stack7b(qg, P)
+        except Exception as e:
+            line["decode_7b_mixed"] = {"error": repr(e)}
     if rank == 0:
         v, cores, txt = oracle_rate(args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",

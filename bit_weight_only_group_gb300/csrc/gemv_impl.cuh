@@ -906,15 +906,18 @@ qg_status launch_cluster(K kernel, dim3 grid, int S, unsigned threads, size_t sm
     return QG_OK;
 }
 
-// Dynamic shared memory of a decode launch.  Clustered (K-split) launches are
-// held to at most four CTAs per SM: cluster placement otherwise packed five
-// CTAs onto some SMs while others ran two or three, and the crowded SMs set
-// the launch's time.
+// Dynamic shared memory of a decode launch, which also caps the CTAs an SM
+// runs.  Clustered (K-split) launches are held to at most four CTAs per SM:
+// cluster placement otherwise packed five CTAs onto some SMs while others ran
+// two or three, and the crowded SMs set the launch's time.  Unsplit launches
+// (about three CTAs per SM of their own) are held to three, so that the
+// CTAs of a dependent launch, started early by programmatic dependent launch,
+// take only the SMs this launch is leaving.
 template <int BITS, int G, int MP>
 size_t decode_smem(int gps, int S)
 {
     const int need = Cfg<BITS, G, MP>::smem(gps, S);
-    return (size_t)(S > 1 ? std::max(need, smem_for_cap(4)) : need);
+    return (size_t)std::max(need, smem_for_cap(S > 1 ? 4 : 3));
 }
 
 template <int BITS, int G, int MP>
@@ -925,10 +928,10 @@ qg_status dense_mp(const Problem& p, cudaStream_t s)
     const int S = choose_splits(tiles, ng);
     const dim3 grid((unsigned)tiles, (unsigned)S, 1);
     const int gps = (int)ceil_div(ng, S);
-    // programmatic dependent launch where K is split across a cluster: the
-    // cluster reduction leaves a tail the next product's start can overlap;
-    // measured slower for unsplit grids (their early dependents crowd the SMs)
-    return launch_cluster(k_gemv<BITS, G, MP>, grid, S, kWarps * 32, decode_smem<BITS, G, MP>(gps, S), S > 1, s, p,
+    // programmatic dependent launch: the next product's CTAs start their weight
+    // loads while this one drains (the per-SM caps of decode_smem keep them
+    // from crowding the SMs this launch still uses)
+    return launch_cluster(k_gemv<BITS, G, MP>, grid, S, kWarps * 32, decode_smem<BITS, G, MP>(gps, S), true, s, p,
                           S, gps);
 }
 
@@ -940,7 +943,7 @@ qg_status multi_mp(const MultiTable& t, cudaStream_t s)
     const int S = choose_splits(tiles, ng);
     const dim3 grid((unsigned)tiles, (unsigned)S, 1);
     const int gps = (int)ceil_div(ng, S);
-    return launch_cluster(k_gemv_multi<BITS, G, MP>, grid, S, kWarps * 32, decode_smem<BITS, G, MP>(gps, S), S > 1,
+    return launch_cluster(k_gemv_multi<BITS, G, MP>, grid, S, kWarps * 32, decode_smem<BITS, G, MP>(gps, S), true,
                           s, t, S, gps);
 }
 
