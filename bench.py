@@ -61,8 +61,8 @@ def parse():
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum over the 5
 # launches of a layer, profiles/k_gemv_decode_70b_stack_m1.md), valid only
 # for the kernel source it was taken on.
-DECODE_TRAFFIC = {"kernel_sha256": "a12b91c95fafd38a0dfddce49626b4c719bcae6592c6a5be17a65549255e1b83",
-                  "bytes_per_layer": 454.050e6}
+DECODE_TRAFFIC = {"kernel_sha256": "4d76dd81e7126a9ec22dcc9fd6b145379a26aee92cacbfebeeefe1d79f5e6744",
+                  "bytes_per_layer": 454.179e6}
 
 
 def decode_traffic(n_layers):
