@@ -496,8 +496,9 @@ def run_widths(qg, args, P):
 
 def run_stack7b(qg, P):
     """One decode step (M=1) of the 32-layer 7B-shaped stack with per-layer
-    widths 2 (codebook) / 3 / 5 / 6, group 128, 0.1 % outliers: 224 products,
-    one launch each, in a CUDA graph."""
+    widths 2 (codebook) / 3 / 5 / 6, group 128, 0.1 % outliers: 224 products
+    in a CUDA graph, those that share x, width and group (q/k, gate/up) fused
+    into one call."""
     dev = torch.device("cuda")
     layers = wl.stack_7b()
     qs = []
@@ -507,10 +508,29 @@ def run_stack7b(qg, P):
         del W
     xh, xf = wl.gen_x(1, 4096, device=dev), wl.gen_x(1, 11008, device=dev)
     ys = [torch.empty((1, L.N), device=dev) for L in layers]
+    # products that read the same x with the same width and group run as one
+    # fused call: q/k(/v) and gate/up of a layer
+    calls = []
+    for li in range(0, len(layers), 7):
+        for grp in ((0, 1, 2), (3,), (4, 5), (6,)):
+            idx = [li + j for j in grp]
+            run = [idx[0]]
+            for i in idx[1:]:
+                if layers[i].bits == layers[run[0]].bits:
+                    run.append(i)
+                else:
+                    calls.append(run)
+                    run = [i]
+            calls.append(run)
+    launches = len(calls)
 
     def step7():
-        for L, q, y in zip(layers, qs, ys):
-            qg.qgemm_forward(xf if L.K == 11008 else xh, q, out=y)
+        for run in calls:
+            x = xf if layers[run[0]].K == 11008 else xh
+            if len(run) == 1:
+                qg.qgemm_forward(x, qs[run[0]], out=ys[run[0]])
+            else:
+                qg.qgemm_forward_multi(x, [qs[i] for i in run], outs=[ys[i] for i in run])
     ms = time_graph_once(step7, 20)
     packed = sum(L.N * L.K * L.bits // 8 for L in layers)
     allb = sum(q.nbytes() for q in qs)
@@ -519,10 +539,10 @@ def run_stack7b(qg, P):
     return {"metric": "7B-shaped mixed-width stack decode", "value": round(packed / ms / 1e6, 1), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "all_GBps": round(allb / ms / 1e6, 1),
             "frac_of_hbm_peak": round(allb / ms / 1e6 / P["hbm"], 4), "weights_GB": round(allb / 1e9, 3),
-            "launches": len(layers),
+            "launches": launches,
             "config": "32 layers q/k/v/o 4096x4096, gate/up 11008x4096, down 4096x11008; widths 6 (layers 0, 1, "
                       "30, 31), else q/k/o 5, v 6, gate/up 2 (codebook), down 2/3/5; group 128, 0.1% outliers, "
-                      "M=1, one launch per product"}
+                      "M=1; products sharing x and width fused per call (q/k, gate/up; q/k/v where all 6-bit)"}
 
 
 # ---------------------------------------------------------------- CPU oracle
