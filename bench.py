@@ -5,14 +5,16 @@ replicas under torchrun).
 Headline (``value``): decode qGEMV weight throughput at M = 1 over the
 70B-shaped stack -- 80 layers x (q, k, v, o, gate, up, down), INT4 group 128
 with 0.1 % FP16 outliers, 36 GB of quantized weights resident in HBM.  One
-step = the 560 products of one token (q/k/v as one fused call: 400 launches),
+step = the 560 products of one token (q/k/v and gate/up as fused calls: 320
+launches),
 captured once in a CUDA graph and replayed.  The unit is GB/s of packed-weight bytes (codes only); the
 all-bytes figure (codes + scales + zero-points + outlier CSR + x + y) is the
 roofline's ``achieved``.
 
 Secondary lines in the same JSON object: prefill qGEMM TFLOP/s at M = 2048 on
-one layer of the same stack, and the MoE layer (16 experts, 256 tokens, top-2
-Zipf routing) through the grouped entry point.
+one layer of the same stack, the MoE layer (16 experts, 256 tokens, top-2
+Zipf routing) through the grouped entry point, and one decode step of the
+7B-shaped stack with per-layer widths 2/3/5/6.
 
 ``--impl reference`` times the CPU oracle (plain C, fp64) on the host cores
 on a bounded sample of the same workload.
@@ -58,11 +60,11 @@ def parse():
 
 
 # DRAM bytes (read + written) per 70B-shaped layer of the decode step, from one
-# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum over the 5
-# launches of a layer, profiles/k_gemv_decode_70b_stack_m1.md), valid only
-# for the kernel source it was taken on.
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum over the launches
+# of a layer, profiles/k_gemv_decode_70b_stack_m1.md), valid only for the
+# kernel source it was taken on.
 DECODE_TRAFFIC = {"kernel_sha256": "4d76dd81e7126a9ec22dcc9fd6b145379a26aee92cacbfebeeefe1d79f5e6744",
-                  "bytes_per_layer": 454.179e6}
+                  "bytes_per_layer": 453.861e6}
 
 
 def decode_traffic(n_layers):
@@ -253,14 +255,15 @@ def run_decode(qg, args, world, rank, P):
 
     def step():
         # one token through the stack, on one stream: the fused q/k/v
-        # projection (one call, one launch), then o, gate, up, down -- five
+        # projection (one call, one launch), o, the fused gate/up projection
+        # (896 row tiles: two waves at three CTAs per SM), down -- four
         # decode launches per layer; consecutive launches overlap through
-        # programmatic dependent launch.  (Fusing gate and up as well measured
-        # slower: 896 row tiles make one and a half waves.)
+        # programmatic dependent launch
         for li in range(0, len(layers), 7):
             qg.qgemm_forward_multi(xs[li], qws[li:li + 3], outs=ys[li:li + 3])
-            for j in (3, 4, 5, 6):
-                qg.qgemm_forward(xs[li + j], qws[li + j], out=ys[li + j])
+            qg.qgemm_forward(xs[li + 3], qws[li + 3], out=ys[li + 3])
+            qg.qgemm_forward_multi(xs[li + 4], qws[li + 4:li + 6], outs=ys[li + 4:li + 6])
+            qg.qgemm_forward(xs[li + 6], qws[li + 6], out=ys[li + 6])
 
     step()                      # eager once (lazy module/function loading outside capture)
     torch.cuda.synchronize()
@@ -303,17 +306,17 @@ def run_decode(qg, args, world, rank, P):
     e2e = {"value": sum_over_ranks(packed, world) / (e2e_ms / 1e3 / args.steps) / 1e9, "unit": "GB/s",
            "h2d_bytes_per_step": xh_pin.numel() * 2 + xf_pin.numel() * 2,
            "d2h_bytes_per_step": y_pin.numel() * 4,
-           "note": "the step's 400 C-ABI calls (fused q/k/v, o, gate, up, down per layer) captured once "
+           "note": "the step's 320 C-ABI calls (fused q/k/v, o, fused gate/up, down per layer) captured once "
                    "in a CUDA graph on one stream, replayed per step"}
 
     achieved = allb / per_step_s / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": P["hbm"], "unit": "GB/s",
             "frac": round(achieved / P["hbm"], 4), "traffic": decode_traffic(len(layers) // 7),
-            "traffic_unit": "bytes per step (the achieved figure is per step: the step is 400 launches of this kernel)",
+            "traffic_unit": "bytes per step (the achieved figure is per step: the step is 320 launches of this kernel)",
             "kernel": "k_gemv<4,128,1> / k_gemv_multi<4,128,1> (decode qGEMV, the only kernel of the step)",
             "peak_source": P["src"] + " hbm_gbs"}
     out = dict(value=value, ms_per_step=ms_max / args.steps, roofline=roof, e2e=e2e, clocks=clocks,
-               gpu_launches=(len(layers) // 7) * 5 * args.steps, setup_s=round(setup_s, 1),
+               gpu_launches=(len(layers) // 7) * 4 * args.steps, setup_s=round(setup_s, 1),
                weights_GB=round(sum(q.nbytes() for q in qws) / 1e9, 3), all_bytes_GBps=round(achieved, 1),
                frac_of_nominal_8TBs=round(value / 8000.0, 4))
     del qws, g
