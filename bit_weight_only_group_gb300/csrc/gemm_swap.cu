@@ -211,9 +211,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t acc = tmem + (uint32_t)(g * NBMAX);
         const uint32_t idesc = ptx::idesc_f16_f32(BW, NB);
         const uint64_t adesc0 = ptx::sw128_desc(a_tile(0)), xdesc0 = ptx::sw128_desc(x_tile(0));
+        // ring slots and phases of block kb, advanced by kGroups blocks per
+        // iteration (SX and SA are even, so a slot keeps its block parity)
+        int sx = g, sa = g;
+        uint32_t px = 0, pa = 0;
         for (int kb = g; kb < KB; kb += kGroups) {
-            const int sx = kb % SX, sa = kb % SA;
-            const uint32_t px = (uint32_t)(kb / SX) & 1u, pa = (uint32_t)(kb / SA) & 1u;
             ok = __all_sync(0xffffffffu, ptx::mbar_wait(full_x(sx), px) && ptx::mbar_wait(full_a(sa), pa));
             if (!ok) break;
             ptx::tc_fence_after();
@@ -225,6 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mma_f16_elect(acc, ad + 2 * kk, xd + 2 * kk, idesc, (kb >= kGroups || kk > 0) ? 1u : 0u);
             ptx::tc_commit_elect(empty_x(sx));
             ptx::tc_commit_elect(empty_a(sa));
+            if ((sx += kGroups) >= SX) { sx -= SX; px ^= 1u; }
+            if ((sa += kGroups) >= SA) { sa -= SA; pa ^= 1u; }
         }
         ptx::tc_commit_elect(acc_full);
     } else {
@@ -313,6 +317,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pp = 0;   // parity of full_p to wait for
         uint32_t pcur[2], pnext[2];
         load_prm(0, pcur);
+        // fp16 slots and phases of this group's blocks kb0 = 4 kp + grp and
+        // kb1 = kb0 + 2, advanced by PK blocks per packed tile
+        int sa0 = grp, sa1 = grp + kGroups;
+        uint32_t pa0 = 0, pa1 = 0;
+        static_assert(SA > PK && SA > 2 * kGroups, "one wrap per advance");
         for (int kp = 0; kp < KP && ok; kp++) {
             if (kp + 1 < KP) load_prm(kp + 1, pnext);
             const unsigned char* pt = p_tile(sp);
@@ -323,10 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
             if (v0) w0 = *reinterpret_cast<const uint4*>(pt + src0);
             if (v1) w1 = *reinterpret_cast<const uint4*>(pt + src1);
-            const int sa0 = kb0 % SA, sa1 = kb1 % SA;   // slots of parity grp
             bool free_ok = true;
-            if (v0) free_ok = ptx::mbar_wait(empty_a(sa0), ((uint32_t)(kb0 / SA) & 1u) ^ 1u);
-            if (v1 && free_ok) free_ok = ptx::mbar_wait(empty_a(sa1), ((uint32_t)(kb1 / SA) & 1u) ^ 1u);
+            if (v0) free_ok = ptx::mbar_wait(empty_a(sa0), pa0 ^ 1u);
+            if (v1 && free_ok) free_ok = ptx::mbar_wait(empty_a(sa1), pa1 ^ 1u);
             ok = __all_sync(0xffffffffu, free_ok);
             if (!ok) break;
             unsigned char* at0 = atile0 + sa0 * A_BYTES;
@@ -345,6 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mbar_arrive(empty_p(sp));
             }
             if (++sp == SP) { sp = 0; pp ^= 1u; }
+            if ((sa0 += PK) >= SA) { sa0 -= SA; pa0 ^= 1u; }
+            if ((sa1 += PK) >= SA) { sa1 -= SA; pa1 ^= 1u; }
             pcur[0] = pnext[0];
             pcur[1] = pnext[1];
         }
