@@ -465,13 +465,13 @@ def time_graph_once(step, reps):
 
 
 def run_widths(qg, args, P):
-    """Decode (M=1) over the mixed-width sweep -- each layer timed as a graph of
-    copies whose weights exceed L2 -- and one step of the 32-layer 7B-shaped
-    stack with per-layer widths (224 products, one launch each)."""
+    """Decode (M=1) over the single 4096x4096 INT4 layer and the mixed-width
+    sweep -- each layer timed as a graph of copies whose weights exceed L2 --
+    and one step of the 32-layer 7B-shaped stack with per-layer widths."""
     dev = torch.device("cuda")
     clone = lambda t: None if t is None else t.clone()
     sweep = []
-    for L in wl.mixed_sweep():
+    for L in [wl.single_layer()] + wl.mixed_sweep():
         W = wl.gen_weight(L.N, L.K, outlier_frac=L.frac, device=dev, distinct_positions=False)
         q = qg.qpack_quantize(W, L.bits, L.group, L.frac)
         del W
