@@ -12,6 +12,8 @@ Entry points (same names as the C ABI):
 * ``qpack_quantize(W, bits, group, outlier_frac)`` -> :class:`QWeight`
 * ``qgemm_forward(x, qw)`` -> y = x . (dequant(W) + outliers)^T
 * ``qgemm_moe_grouped(x, topk_ids, experts)`` -> y [T, k, N]
+* ``qgemm_moe_grouped_multi(x, topk_ids, [experts_0, experts_1])`` -> [y_0, y_1]
+  (products sharing one routing, e.g. an MoE layer's gate and up)
 """
 from __future__ import annotations
 
@@ -32,6 +34,7 @@ Y_F32, Y_BF16 = 0, 1
 ABI_FUNCTIONS = ("qpack_query_sizes", "qpack_workspace_size", "qpack_quantize", "qpack_quantize_noalloc",
                  "qgemm_workspace_size",
                  "qgemm_forward", "qgemm_forward_multi", "qgemm_moe_workspace_size", "qgemm_moe_grouped",
+                 "qgemm_moe_grouped_multi",
                  "qgemm_device_status",
                  "qgemm_last_error")
 
@@ -72,6 +75,8 @@ def lib() -> ctypes.CDLL:
         L.qgemm_forward.argtypes = [vp, i32, i32, pq, vp, i32, ctypes.c_int, vp, sz, vp]
         L.qgemm_moe_workspace_size.argtypes = [i32, i32, i32, pq, psz]
         L.qgemm_moe_grouped.argtypes = [vp, i32, vp, i32, pq, i32, vp, ctypes.c_int, vp, sz, vp]
+        L.qgemm_moe_grouped_multi.argtypes = [vp, i32, vp, i32, pq, i32, i32, ctypes.POINTER(vp), ctypes.c_int, vp,
+                                              sz, vp]
         L.qgemm_device_status.argtypes = [pi32, i32]
         L.qgemm_forward_multi.argtypes = [vp, i32, i32, pq, i32, ctypes.POINTER(vp), pi32, ctypes.c_int, vp, sz, vp]
         for name in ABI_FUNCTIONS[:-1]:
@@ -284,6 +289,39 @@ def qgemm_moe_grouped(x: torch.Tensor, topk_ids: torch.Tensor, experts, out: tor
     _check(lib().qgemm_moe_grouped(_ptr(x), T, _ptr(topk_ids), k, arr, len(experts), _ptr(out), yt,
                                    _ptr(workspace), workspace.numel(), _stream(stream)), "qgemm_moe_grouped")
     return out
+
+
+def qgemm_moe_grouped_multi(x: torch.Tensor, topk_ids: torch.Tensor, experts_per_product, outs=None,
+                            out_dtype: torch.dtype = torch.float32, workspace: torch.Tensor | None = None,
+                            stream=None) -> list:
+    """[y_p]: the grouped product of each expert list in experts_per_product
+    (at most 2 lists of equal length, all matrices of one shape, width and
+    group) over one routing of topk_ids."""
+    if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bfloat16 CUDA tensor [T, K]")
+    if topk_ids.dtype != torch.int32 or not topk_ids.is_contiguous():
+        raise ValueError("topk_ids must be a contiguous int32 tensor [T, k]")
+    n = len(experts_per_product)
+    E = len(experts_per_product[0])
+    if any(len(ex) != E for ex in experts_per_product):
+        raise ValueError("every product needs the same number of experts")
+    T, k = topk_ids.shape
+    N = experts_per_product[0][0].N
+    if outs is None:
+        outs = [torch.empty((T, k, N), dtype=out_dtype, device=x.device) for _ in range(n)]
+    if len(outs) != n:
+        raise ValueError("one output per product")
+    yt = Y_BF16 if outs[0].dtype == torch.bfloat16 else Y_F32
+    if any(o.dtype != outs[0].dtype for o in outs):
+        raise ValueError("outputs must share one dtype")
+    arr = _desc_array([w for ex in experts_per_product for w in ex])
+    ys = (ctypes.c_void_p * n)(*[o.data_ptr() for o in outs])
+    need = qgemm_moe_workspace_size(T, k, experts_per_product[0])
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    _check(lib().qgemm_moe_grouped_multi(_ptr(x), T, _ptr(topk_ids), k, arr, E, n, ys, yt, _ptr(workspace),
+                                         workspace.numel(), _stream(stream)), "qgemm_moe_grouped_multi")
+    return outs
 
 
 def qgemm_device_status(reset: bool = False) -> int:

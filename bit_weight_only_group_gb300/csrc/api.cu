@@ -255,35 +255,55 @@ qg_status qgemm_moe_workspace_size(int32_t T, int32_t k, int32_t E, const qg_qwe
     if (!bytes) return fail(QG_ERR_INVALID_ARG, "bytes is null");
     if (T < 0 || k <= 0 || E <= 0 || E > kMoeMaxExperts || !experts)
         return fail(QG_ERR_INVALID_ARG, "qgemm_moe_workspace_size: bad T/k/E");
-    *bytes = moe_workspace_bytes(T, k, E, experts);
+    *bytes = moe_workspace_bytes(T, k, E, 1, experts);   // enough for any number of products per call
     return QG_OK;
+}
+
+static qg_status moe_checked(const char* fn, const uint16_t* x, int32_t T, const int32_t* topk_ids, int32_t k,
+                             const qg_qweight* experts, int32_t E, int32_t n, void* const* ys, qg_ydtype yt,
+                             void* ws, size_t ws_bytes, void* stream)
+{
+    if (T < 0 || k <= 0) return fail(QG_ERR_INVALID_ARG, "%s: T < 0 or k <= 0", fn);
+    if (E <= 0 || E > kMoeMaxExperts) return fail(QG_ERR_INVALID_ARG, "%s: E must be in 1..%d", fn, kMoeMaxExperts);
+    if (n < 1 || n > kMoeMaxProducts)
+        return fail(QG_ERR_INVALID_ARG, "%s: n must be in 1..%d", fn, kMoeMaxProducts);
+    if (!experts) return fail(QG_ERR_INVALID_ARG, "%s: experts is null", fn);
+    for (int e = 0; e < E * n; e++) {
+        qg_status st = check_qweight(&experts[e], fn);
+        if (st != QG_OK) return st;
+        if (experts[e].N != experts[0].N || experts[e].K != experts[0].K || experts[e].bits != experts[0].bits ||
+            experts[e].group != experts[0].group)
+            return fail(QG_ERR_INVALID_ARG, "%s: experts differ in N/K/bits/group", fn);
+    }
+    if (T == 0) return QG_OK;
+    if (!x || !topk_ids || !ys) return fail(QG_ERR_INVALID_ARG, "%s: null x/topk_ids/y", fn);
+    for (int q = 0; q < n; q++)
+        if (!ys[q]) return fail(QG_ERR_INVALID_ARG, "%s: null y", fn);
+    if (yt != QG_Y_F32 && yt != QG_Y_BF16) return fail(QG_ERR_INVALID_ARG, "%s: bad y dtype", fn);
+    if (!aligned(x, 2) || !aligned(topk_ids, 4)) return fail(QG_ERR_ALIGNMENT, "%s: misaligned x/topk_ids/y", fn);
+    for (int q = 0; q < n; q++)
+        if (!aligned(ys[q], yt == QG_Y_F32 ? 4 : 2)) return fail(QG_ERR_ALIGNMENT, "%s: misaligned x/topk_ids/y", fn);
+    const size_t need = moe_workspace_bytes(T, k, E, n, experts);
+    if (need && (!ws || ws_bytes < need))
+        return fail(QG_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu", fn, ws ? ws_bytes : (size_t)0, need);
+    if (need && !aligned(ws, 256)) return fail(QG_ERR_ALIGNMENT, "%s: workspace must be 256-byte aligned", fn);
+    return launch_moe(x, T, topk_ids, k, experts, E, n, ys, yt, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 qg_status qgemm_moe_grouped(const uint16_t* x, int32_t T, const int32_t* topk_ids, int32_t k,
                             const qg_qweight* experts, int32_t E, void* y, qg_ydtype yt, void* ws,
                             size_t ws_bytes, void* stream)
 {
-    if (T < 0 || k <= 0) return fail(QG_ERR_INVALID_ARG, "qgemm_moe_grouped: T < 0 or k <= 0");
-    if (E <= 0 || E > kMoeMaxExperts)
-        return fail(QG_ERR_INVALID_ARG, "qgemm_moe_grouped: E must be in 1..%d", kMoeMaxExperts);
-    if (!experts) return fail(QG_ERR_INVALID_ARG, "qgemm_moe_grouped: experts is null");
-    for (int e = 0; e < E; e++) {
-        qg_status st = check_qweight(&experts[e], "qgemm_moe_grouped");
-        if (st != QG_OK) return st;
-        if (experts[e].N != experts[0].N || experts[e].K != experts[0].K || experts[e].bits != experts[0].bits ||
-            experts[e].group != experts[0].group)
-            return fail(QG_ERR_INVALID_ARG, "qgemm_moe_grouped: experts differ in N/K/bits/group");
-    }
-    if (T == 0) return QG_OK;
-    if (!x || !topk_ids || !y) return fail(QG_ERR_INVALID_ARG, "qgemm_moe_grouped: null x/topk_ids/y");
-    if (yt != QG_Y_F32 && yt != QG_Y_BF16) return fail(QG_ERR_INVALID_ARG, "qgemm_moe_grouped: bad y dtype");
-    if (!aligned(x, 2) || !aligned(topk_ids, 4) || !aligned(y, yt == QG_Y_F32 ? 4 : 2))
-        return fail(QG_ERR_ALIGNMENT, "qgemm_moe_grouped: misaligned x/topk_ids/y");
-    const size_t need = moe_workspace_bytes(T, k, E, experts);
-    if (need && (!ws || ws_bytes < need))
-        return fail(QG_ERR_WORKSPACE, "qgemm_moe_grouped: workspace %zu bytes < %zu", ws ? ws_bytes : (size_t)0, need);
-    if (need && !aligned(ws, 256)) return fail(QG_ERR_ALIGNMENT, "qgemm_moe_grouped: workspace must be 256-byte aligned");
-    return launch_moe(x, T, topk_ids, k, experts, E, y, yt, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+    void* ys[1] = {y};
+    return moe_checked("qgemm_moe_grouped", x, T, topk_ids, k, experts, E, 1, y ? ys : nullptr, yt, ws, ws_bytes,
+                       stream);
+}
+
+qg_status qgemm_moe_grouped_multi(const uint16_t* x, int32_t T, const int32_t* topk_ids, int32_t k,
+                                  const qg_qweight* experts, int32_t E, int32_t n, void* const* ys, qg_ydtype yt,
+                                  void* ws, size_t ws_bytes, void* stream)
+{
+    return moe_checked("qgemm_moe_grouped_multi", x, T, topk_ids, k, experts, E, n, ys, yt, ws, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -173,7 +173,7 @@ struct MoeWs {
 // smallest chunk (1 pair).
 inline int max_items_for(int P, int E, int chunk) { return (int)ceil_div(P, chunk) + E; }
 
-size_t moe_ws_layout(int T, int k, int E, const qg_qweight* experts, MoeWs* p, void* base)
+size_t moe_ws_layout(int T, int k, int E, int n, const qg_qweight* experts, MoeWs* p, void* base)
 {
     const size_t P = (size_t)T * k;
     const size_t o_off = 0;
@@ -181,7 +181,7 @@ size_t moe_ws_layout(int T, int k, int E, const qg_qweight* experts, MoeWs* p, v
     const size_t o_perm = o_n + 256;
     const size_t o_items = align_up(o_perm + sizeof(int) * P, 256);
     const size_t o_x16 = align_up(o_items + sizeof(int2) * (size_t)max_items_for((int)P, E, 1), 256);
-    const size_t x16 = moe_tc_eligible(experts, E) ? moe_tc_x16_bytes((int)P, experts[0].K) : 0;
+    const size_t x16 = moe_tc_eligible(experts, E, n) ? moe_tc_x16_bytes((int)P, experts[0].K) : 0;
     const size_t total = o_x16 + x16;
     if (p && base) {
         char* b = static_cast<char*>(base);
@@ -239,16 +239,16 @@ qg_status launch_gemv_chunked(const uint16_t* x, int M, int ldx, const qg_qweigh
     return QG_OK;
 }
 
-size_t moe_workspace_bytes(int T, int k, int E, const qg_qweight* experts)
+size_t moe_workspace_bytes(int T, int k, int E, int n, const qg_qweight* experts)
 {
-    return moe_ws_layout(T, k, E, experts, nullptr, nullptr);
+    return moe_ws_layout(T, k, E, n, experts, nullptr, nullptr);
 }
 
 qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const qg_qweight* experts, int E,
-                     void* y, qg_ydtype yt, void* ws, size_t, cudaStream_t s)
+                     int n, void* const* ys, qg_ydtype yt, void* ws, size_t, cudaStream_t s)
 {
     MoeWs p;
-    moe_ws_layout(T, k, E, experts, &p, ws);
+    moe_ws_layout(T, k, E, n, experts, &p, ws);
     const int P = T * k;
     const qg_qweight& w0 = experts[0];
     if (p.x16) {
@@ -256,7 +256,7 @@ qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const
         k_route<<<1, kRouteThreads, 0, s>>>(topk, P, E, kMoeTcChunk, p.offsets, p.perm, p.items, p.n_items);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
-        return launch_moe_tc(x, T, k, experts, E, y, yt, p.offsets, p.perm, p.items, p.n_items,
+        return launch_moe_tc(x, T, k, experts, E, n, ys, yt, p.offsets, p.perm, p.items, p.n_items,
                              max_items_for(P, E, kMoeTcChunk), p.x16, s);
     }
     // tokens per CTA chunk from the mean load per expert
@@ -266,37 +266,44 @@ qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
 
-    gemv::MoeTable t;
-    memset(&t, 0, sizeof(t));
-    t.x = reinterpret_cast<const __nv_bfloat16*>(x);
-    t.ldx = w0.K; t.N = w0.N; t.K = w0.K; t.topk = k;
-    t.chunk = mp;
-    t.offsets = p.offsets;
-    t.perm = p.perm;
-    t.items = p.items;
-    t.n_items = p.n_items;
-    t.y = y;
-    t.y_bf16 = yt == QG_Y_BF16;
-    t.magic = gemv::kF16Magic;
-    for (int i = 0; i < E; i++) {
-        t.packed[i] = experts[i].packed;
-        t.scale[i] = experts[i].scale;
-        t.zp[i] = experts[i].zp;
-        t.cb[i] = reinterpret_cast<const uint2*>(experts[i].codebook);
-        t.row_ptr[i] = experts[i].out_row_ptr;
-        t.col[i] = experts[i].out_col;
-        t.val[i] = experts[i].out_val;
-        t.nnz[i] = experts[i].nnz;
+    // one grouped decode launch per product over the shared routing
+    for (int q = 0; q < n; q++) {
+        const qg_qweight* ex = experts + (size_t)q * E;
+        gemv::MoeTable t;
+        memset(&t, 0, sizeof(t));
+        t.x = reinterpret_cast<const __nv_bfloat16*>(x);
+        t.ldx = w0.K; t.N = w0.N; t.K = w0.K; t.topk = k;
+        t.chunk = mp;
+        t.offsets = p.offsets;
+        t.perm = p.perm;
+        t.items = p.items;
+        t.n_items = p.n_items;
+        t.y = ys[q];
+        t.y_bf16 = yt == QG_Y_BF16;
+        t.magic = gemv::kF16Magic;
+        for (int i = 0; i < E; i++) {
+            t.packed[i] = ex[i].packed;
+            t.scale[i] = ex[i].scale;
+            t.zp[i] = ex[i].zp;
+            t.cb[i] = reinterpret_cast<const uint2*>(ex[i].codebook);
+            t.row_ptr[i] = ex[i].out_row_ptr;
+            t.col[i] = ex[i].out_col;
+            t.val[i] = ex[i].out_val;
+            t.nnz[i] = ex[i].nnz;
+        }
+        const int maxi = max_items_for(P, E, t.chunk);
+        const int expect = std::min(maxi, (int)ceil_div(P, t.chunk) + E / 2);
+        qg_status st;
+        switch (w0.bits) {
+            case 2: st = gemv::launch_grouped<2>(t, maxi, expect, w0.group, mp, s); break;
+            case 3: st = gemv::launch_grouped<3>(t, maxi, expect, w0.group, mp, s); break;
+            case 4: st = gemv::launch_grouped<4>(t, maxi, expect, w0.group, mp, s); break;
+            case 5: st = gemv::launch_grouped<5>(t, maxi, expect, w0.group, mp, s); break;
+            default: st = gemv::launch_grouped<6>(t, maxi, expect, w0.group, mp, s); break;
+        }
+        if (st != QG_OK) return st;
     }
-    const int maxi = max_items_for(P, E, t.chunk);
-    const int expect = std::min(maxi, (int)ceil_div(P, t.chunk) + E / 2);
-    switch (w0.bits) {
-        case 2: return gemv::launch_grouped<2>(t, maxi, expect, w0.group, mp, s);
-        case 3: return gemv::launch_grouped<3>(t, maxi, expect, w0.group, mp, s);
-        case 4: return gemv::launch_grouped<4>(t, maxi, expect, w0.group, mp, s);
-        case 5: return gemv::launch_grouped<5>(t, maxi, expect, w0.group, mp, s);
-        default: return gemv::launch_grouped<6>(t, maxi, expect, w0.group, mp, s);
-    }
+    return QG_OK;
 }
 
 }  // namespace qg

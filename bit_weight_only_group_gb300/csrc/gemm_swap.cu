@@ -70,7 +70,8 @@ constexpr int OFF_A = OFF_P + SP * P_BYTES;
 constexpr int OFF_BAR = OFF_A + SA * A_BYTES;
 constexpr int SMEM = OFF_BAR + 1024 /* barriers */ + 1024 /* alignment */;
 constexpr int TMEM_COLS = kGroups * NBMAX;   // one accumulator per group
-constexpr int kMaxExperts = 32;              // tensor maps travel as kernel parameters
+constexpr int kMaxExperts = 32;              // tensor maps travel as kernel parameters (all products' experts)
+constexpr int kMaxProducts = 2;              // products sharing the routing in one launch (gate and up)
 
 struct Maps {
     CUtensorMap w[kMaxExperts];   // packed codes of each expert, box 128 bytes x 128 rows
@@ -78,6 +79,7 @@ struct Maps {
 
 struct Args {
     int N, K, ng, chunk;
+    int E, tiles;         // experts per product, row tiles per product
     const int* offsets;   // [E + 1] pair offsets of each expert in routed order
     const int* perm;      // routed order -> pair id (token * topk + slot)
     const int2* items;    // (expert, chunk)
@@ -88,7 +90,7 @@ struct Args {
     const int* col[kMaxExperts];
     const uint16_t* val[kMaxExperts];
     int nnz[kMaxExperts];
-    void* y;              // [pairs, N]
+    void* y[kMaxProducts];   // per product: [pairs, N]
     int y_bf16;
     int* status;
     uint32_t magic;       // gemv::kF16Magic, a run-time value (one logic op per code pair)
@@ -129,10 +131,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((int)blockIdx.y >= *a.n_items) return;
     const int2 item = a.items[blockIdx.y];
     const int e = item.x;
+    // blockIdx.x: row tile of product blockIdx.x / tiles; ep indexes that product's expert e
+    const int prod = (int)blockIdx.x / a.tiles;
+    const int ep = prod * a.E + e;
     const int m0 = a.offsets[e] + item.y * a.chunk;
     const int ntok = min(a.chunk, a.offsets[e + 1] - m0);
     const int NB = (ntok + 15) & ~15;   // MMA N: tokens rounded up to 16
-    const int n0 = blockIdx.x * BW;
+    const int n0 = ((int)blockIdx.x % a.tiles) * BW;
     const int KB = a.K / BK;
 
     extern __shared__ unsigned char smem_raw[];
@@ -170,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == kWarpX && lane == 0) {
         ptx::prefetch_tensormap(&xmap);
-        ptx::prefetch_tensormap(&maps.w[e]);
+        ptx::prefetch_tensormap(&maps.w[ep]);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -200,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kp = 0; kp < KP; kp++) {
                 if (!ptx::mbar_wait(empty_p(s), ph ^ 1u)) { ok = false; break; }
                 ptx::mbar_expect_tx(full_p(s), P_BYTES);
-                ptx::tma_load_2d(ptx::smem_u32(p_tile(s)), &maps.w[e], kp * (PK * BK / 2), n0, full_p(s));
+                ptx::tma_load_2d(ptx::smem_u32(p_tile(s)), &maps.w[ep], kp * (PK * BK / 2), n0, full_p(s));
                 if (++s == SP) { s = 0; ph ^= 1u; }
             }
         }
@@ -240,8 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hk = tg & 1;                          // which 32 k of the block
         const int nr = n0 + r;
         const int n = min(nr, a.N - 1);
-        const uint16_t* sp_row = a.scale[e] + (size_t)n * a.ng;
-        const uint8_t* zp_row = a.zp[e] + (size_t)n * a.ng;
+        const uint16_t* sp_row = a.scale[ep] + (size_t)n * a.ng;
+        const uint8_t* zp_row = a.zp[ep] + (size_t)n * a.ng;
         constexpr int KB_PER_G = G / BK;                // 1 or 2
         const int ng = a.ng;
         // the row's group parameters are read per K block through L1; warm
@@ -249,13 +254,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int off = 0; off < ng * 2; off += 128) asm volatile("prefetch.global.L1 [%0];" ::"l"(sp_row + off / 2));
         for (int off = 0; off < ng; off += 128) asm volatile("prefetch.global.L1 [%0];" ::"l"(zp_row + off));
         // outlier cursor of this row: the next entry and the one after it
-        const int* ocolp = a.col[e];
-        const uint16_t* ovalp = a.val[e];
+        const int* ocolp = a.col[ep];
+        const uint16_t* ovalp = a.val[ep];
         int op = 0, oe = 0, ocol = 0x7FFFFFFF, ncol = 0x7FFFFFFF;
         uint16_t oval = 0, nval = 0;
-        if (a.nnz[e] > 0 && nr < a.N) {
-            op = a.row_ptr[e][n];
-            oe = a.row_ptr[e][n + 1];
+        if (a.nnz[ep] > 0 && nr < a.N) {
+            op = a.row_ptr[ep][n];
+            oe = a.row_ptr[ep][n + 1];
             if (op < oe) {
                 ocol = ocolp[op];
                 oval = ovalp[op];
@@ -380,9 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (col < ntok) {
                             const size_t yo = (size_t)a.perm[m0 + col] * a.N + nrow;
                             if (a.y_bf16)
-                                reinterpret_cast<__nv_bfloat16*>(a.y)[yo] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                                reinterpret_cast<__nv_bfloat16*>(a.y[prod])[yo] = __float2bfloat16_rn(__uint_as_float(v[j]));
                             else
-                                reinterpret_cast<float*>(a.y)[yo] = __uint_as_float(v[j]);
+                                reinterpret_cast<float*>(a.y[prod])[yo] = __uint_as_float(v[j]);
                         }
                     }
                 }
@@ -398,17 +403,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace swap
 
-bool moe_tc_eligible(const qg_qweight* experts, int E)
+bool moe_tc_eligible(const qg_qweight* experts, int E, int n)
 {
-    return E <= swap::kMaxExperts && experts[0].bits == 4 && experts[0].K % swap::BK == 0;
+    return n >= 1 && n <= swap::kMaxProducts && E * n <= swap::kMaxExperts && experts[0].bits == 4 &&
+           experts[0].K % swap::BK == 0;
 }
 
 size_t moe_tc_x16_bytes(int P, int K) { return align_up((size_t)P * K * 2, 256); }
 
+// n products (experts[p * E + e] is expert e of product p) over one routing:
+// x is gathered once, and one launch covers every product's row tiles.
 template <int G>
-static qg_status moe_tc_run(const uint16_t* x, int T, int k, const qg_qweight* experts, int E, void* y, qg_ydtype yt,
-                            const int* offsets, const int* perm, const int2* items, const int* n_items, int max_items,
-                            void* x16p, cudaStream_t s)
+static qg_status moe_tc_run(const uint16_t* x, int T, int k, const qg_qweight* experts, int E, int n,
+                            void* const* ys, qg_ydtype yt, const int* offsets, const int* perm, const int2* items,
+                            const int* n_items, int max_items, void* x16p, cudaStream_t s)
 {
     using namespace swap;
     const int P = T * k, N = experts[0].N, K = experts[0].K;
@@ -426,39 +434,41 @@ static qg_status moe_tc_run(const uint16_t* x, int T, int k, const qg_qweight* e
     memset(&maps, 0, sizeof(maps));
     Args a;
     memset(&a, 0, sizeof(a));
-    for (int e = 0; e < E; e++) {
-        st = encode_2d(&maps.w[e], CU_TENSOR_MAP_DATA_TYPE_UINT8, experts[e].packed, (uint64_t)K / 2, (uint64_t)N,
+    for (int i = 0; i < n * E; i++) {
+        st = encode_2d(&maps.w[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, experts[i].packed, (uint64_t)K / 2, (uint64_t)N,
                        (uint64_t)K / 2, PK * BK / 2, BW, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st != QG_OK) return st;
-        a.scale[e] = experts[e].scale;
-        a.zp[e] = experts[e].zp;
-        a.row_ptr[e] = experts[e].out_row_ptr;
-        a.col[e] = experts[e].out_col;
-        a.val[e] = experts[e].out_val;
-        a.nnz[e] = experts[e].nnz;
+        a.scale[i] = experts[i].scale;
+        a.zp[i] = experts[i].zp;
+        a.row_ptr[i] = experts[i].out_row_ptr;
+        a.col[i] = experts[i].out_col;
+        a.val[i] = experts[i].out_val;
+        a.nnz[i] = experts[i].nnz;
     }
     static_assert(kMoeTcChunk <= NBMAX && kMoeTcChunk % 16 == 0, "routing chunk fits one CTA's token tile");
     a.N = N; a.K = K; a.ng = K / G; a.chunk = kMoeTcChunk;
+    a.E = E; a.tiles = (int)ceil_div(N, BW);
     a.offsets = offsets; a.perm = perm; a.items = items; a.n_items = n_items;
-    a.y = y; a.y_bf16 = yt == QG_Y_BF16;
+    for (int p = 0; p < n; p++) a.y[p] = ys[p];
+    a.y_bf16 = yt == QG_Y_BF16;
     a.status = device_status_ptr();
     a.magic = gemv::kF16Magic;
     st = gemv::allow_smem(k_gemm_swap_u4<G>, SMEM);
     if (st != QG_OK) return st;
-    dim3 grid((unsigned)ceil_div(N, BW), (unsigned)max_items, 1);
+    dim3 grid((unsigned)(a.tiles * n), (unsigned)max_items, 1);
     k_gemm_swap_u4<G><<<grid, kThreads, SMEM, s>>>(xmap, maps, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "grouped tensor-core kernel launch");
     return QG_OK;
 }
 
-qg_status launch_moe_tc(const uint16_t* x, int T, int k, const qg_qweight* experts, int E, void* y, qg_ydtype yt,
-                        const int* offsets, const int* perm, const int2* items, const int* n_items, int max_items,
-                        void* x16p, cudaStream_t s)
+qg_status launch_moe_tc(const uint16_t* x, int T, int k, const qg_qweight* experts, int E, int n, void* const* ys,
+                        qg_ydtype yt, const int* offsets, const int* perm, const int2* items, const int* n_items,
+                        int max_items, void* x16p, cudaStream_t s)
 {
     return experts[0].group == 64
-               ? moe_tc_run<64>(x, T, k, experts, E, y, yt, offsets, perm, items, n_items, max_items, x16p, s)
-               : moe_tc_run<128>(x, T, k, experts, E, y, yt, offsets, perm, items, n_items, max_items, x16p, s);
+               ? moe_tc_run<64>(x, T, k, experts, E, n, ys, yt, offsets, perm, items, n_items, max_items, x16p, s)
+               : moe_tc_run<128>(x, T, k, experts, E, n, ys, yt, offsets, perm, items, n_items, max_items, x16p, s);
 }
 
 }  // namespace qg

@@ -52,21 +52,24 @@ qg_status launch_gemm(const uint16_t* x, int M, int ldx, const qg_qweight& w, vo
 
 // ---------------------------------------------------------------- grouped MoE
 constexpr int kMoeMaxExperts = 256;
-size_t moe_workspace_bytes(int T, int k, int E, const qg_qweight* experts);
+constexpr int kMoeMaxProducts = 2;   // products sharing one routing per call (gate and up)
+// n products over the same routing: experts[p * E + e] is expert e of
+// product p, ys[p] its output.
+size_t moe_workspace_bytes(int T, int k, int E, int n, const qg_qweight* experts);
 qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const qg_qweight* experts,
-                     int E, void* y, qg_ydtype yt, void* ws, size_t ws_bytes, cudaStream_t s);
+                     int E, int n, void* const* ys, qg_ydtype yt, void* ws, size_t ws_bytes, cudaStream_t s);
 
 // Grouped product on the tensor cores (4-bit, K a multiple of 64, at most 32
-// experts): tokens of an expert in chunks of kMoeTcChunk; x16p is workspace
+// experts over all n products): tokens of an expert in chunks of kMoeTcChunk; x16p is workspace
 // for x gathered in routed order (moe_tc_x16_bytes).  Chunks of 64 tokens
 // keep a token tile's K block at 8 KB, so the token ring holds ten of them;
 // an expert with more tokens reads its weights once per chunk, mostly from
 // L2 (the chunks' CTAs run together).
 constexpr int kMoeTcChunk = 64;
-bool moe_tc_eligible(const qg_qweight* experts, int E);
+bool moe_tc_eligible(const qg_qweight* experts, int E, int n);
 size_t moe_tc_x16_bytes(int P, int K);
-qg_status launch_moe_tc(const uint16_t* x, int T, int k, const qg_qweight* experts, int E, void* y, qg_ydtype yt,
-                        const int* offsets, const int* perm, const int2* items, const int* n_items, int max_items,
-                        void* x16p, cudaStream_t s);
+qg_status launch_moe_tc(const uint16_t* x, int T, int k, const qg_qweight* experts, int E, int n, void* const* ys,
+                        qg_ydtype yt, const int* offsets, const int* perm, const int2* items, const int* n_items,
+                        int max_items, void* x16p, cudaStream_t s);
 
 }  // namespace qg

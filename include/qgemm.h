@@ -212,7 +212,8 @@ QG_API qg_status qgemm_forward_multi(const uint16_t* x, int32_t M, int32_t ldx, 
                                      void* const* ys, const int32_t* ldys, qg_ydtype yt, void* work,
                                      size_t work_bytes, void* stream);
 
-/* Workspace bytes qgemm_moe_grouped needs.  Host-only. */
+/* Workspace bytes qgemm_moe_grouped (and qgemm_moe_grouped_multi with the
+ * same T, k, E and experts[0 .. E-1]) needs.  Host-only. */
 QG_API qg_status qgemm_moe_workspace_size(int32_t T, int32_t k, int32_t E, const qg_qweight* experts,
                                    size_t* bytes);
 
@@ -233,6 +234,24 @@ QG_API qg_status qgemm_moe_workspace_size(int32_t T, int32_t k, int32_t E, const
 QG_API qg_status qgemm_moe_grouped(const uint16_t* x, int32_t T, const int32_t* topk_ids, int32_t k,
                             const qg_qweight* experts, int32_t E, void* y, qg_ydtype yt, void* ws,
                             size_t ws_bytes, void* stream);
+
+/*
+ * n grouped products over one routing: products that read the same routed x
+ * (an MoE layer's gate and up projections) share the routing, the gathered
+ * x and one launch.  For each product p < n:
+ *   y_p[t, j, :] = x[t, :] . (w_hat + S)_{p, e}^T   with e = topk_ids[t, j],
+ * exactly as qgemm_moe_grouped computes it for experts[p * E .. p * E + E - 1].
+ *   experts   HOST array of n * E descriptors (product p's experts at
+ *             p * E .. p * E + E - 1); all share N, K, bits and group.
+ *   n         1 <= n <= 2.
+ *   ys        HOST array of n DEVICE pointers, each [T, k, N] contiguous, fp32
+ *             or bf16 per `yt`.
+ *   ws        at least qgemm_moe_workspace_size(T, k, E, experts) bytes.
+ * Other arguments, ordering and errors as for qgemm_moe_grouped.
+ */
+QG_API qg_status qgemm_moe_grouped_multi(const uint16_t* x, int32_t T, const int32_t* topk_ids, int32_t k,
+                                         const qg_qweight* experts, int32_t E, int32_t n, void* const* ys,
+                                         qg_ydtype yt, void* ws, size_t ws_bytes, void* stream);
 
 /* Status word of the library's kernels on the current device: QG_OK, or
  * QG_ERR_TIMEOUT once a bounded wait of the tensor-core product (M above the

@@ -173,3 +173,22 @@ def test_moe_validation_without_gpu(qg):
     b = ctypes.c_size_t()
     assert L.qgemm_moe_workspace_size(256, 2, 1, arr2, ctypes.byref(b)) == 0 and b.value > 0
     assert L.qgemm_moe_grouped(x, 4, ids, 2, arr2, 1, y, 0, None, 0, None) == -4    # no workspace
+
+
+def test_moe_multi_validation_without_gpu(qg):
+    # product counts outside 1..2, mismatched experts and null outputs are
+    # rejected on the host; T = 0 is a no-op
+    L = qg.lib()
+    d = _fake_desc(qg)
+    arr = (qg.QgQWeight * 4)(d, d, d, d)
+    x, ids = ctypes.c_void_p(0x300000), ctypes.c_void_p(0x310000)
+    ys = (ctypes.c_void_p * 2)(0x320000, 0x330000)
+    assert L.qgemm_moe_grouped_multi(x, 4, ids, 2, arr, 2, 0, ys, 0, None, 0, None) == -1
+    assert L.qgemm_moe_grouped_multi(x, 4, ids, 2, arr, 1, 3, ys, 0, None, 0, None) == -1
+    bad = (qg.QgQWeight * 4)(d, d, d, d)
+    bad[3].N = d.N * 2
+    assert L.qgemm_moe_grouped_multi(x, 4, ids, 2, bad, 2, 2, ys, 0, None, 0, None) == -1
+    ys0 = (ctypes.c_void_p * 2)(0x320000, None)
+    assert L.qgemm_moe_grouped_multi(x, 4, ids, 2, arr, 2, 2, ys0, 0, None, 0, None) == -1
+    assert L.qgemm_moe_grouped_multi(x, 0, ids, 2, arr, 2, 2, ys, 0, None, 0, None) == 0
+    assert L.qgemm_moe_grouped_multi(x, 4, ids, 2, arr, 2, 2, ys, 0, None, 0, None) == -4   # no workspace

@@ -94,3 +94,30 @@ def test_moe_tensor_core_chunks_and_fallback(qg, group, T, k, E, hot):
     ref = oracle.moe(x, topk.numpy(), qs)
     check_product(y.reshape(T * k, N), ref.reshape(T * k, N), x.repeat_interleave(k, 0), wmax)
     assert qg.qgemm_device_status() == 0
+
+
+@pytest.mark.parametrize("bits,group,E,T", [(4, 128, 16, 300), (4, 64, 3, 90), (4, 128, 20, 60), (3, 128, 5, 40)])
+def test_moe_multi_against_oracle(qg, bits, group, E, T):
+    # two products over one routing (gate and up): 4-bit with 2 * E <= 32
+    # experts takes the tensor cores (the 300-token case puts some experts
+    # above one 64-token chunk), 2 * 20 experts and 3-bit take the decode
+    # kernel, launched per product over the shared routing
+    N, K, k = 200, 640, 2
+    qa, wa = _experts(E, N, K, bits, group, 0.002, seed=110)
+    qb, wb = _experts(E, N, K, bits, group, 0.002, seed=310)
+    x = wl.gen_x(T, K, seed=T + 7)
+    topk = wl.gen_topk(T, k, E, seed=T + 8)
+    ya, yb = qg.qgemm_moe_grouped_multi(x.cuda(), topk.cuda(), [[to_device(q) for q in qa], [to_device(q) for q in qb]])
+    torch.cuda.synchronize()
+    for y, qs, wmax in ((ya, qa, wa), (yb, qb, wb)):
+        ref = oracle.moe(x, topk.numpy(), qs)
+        check_product(y.reshape(T * k, N), ref.reshape(T * k, N), x.repeat_interleave(k, 0), wmax)
+    # where the single calls take the same kernel (not 4-bit with 16 < E <= 32,
+    # which one product alone runs on the tensor cores), the fused call equals
+    # two single calls bit for bit
+    if not (bits == 4 and 16 < E <= 32):
+        sa = qg.qgemm_moe_grouped(x.cuda(), topk.cuda(), [to_device(q) for q in qa])
+        sb = qg.qgemm_moe_grouped(x.cuda(), topk.cuda(), [to_device(q) for q in qb])
+        torch.cuda.synchronize()
+        assert torch.equal(sa, ya) and torch.equal(sb, yb)
+    assert qg.qgemm_device_status() == 0
