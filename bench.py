@@ -206,6 +206,20 @@ def layer_bytes(qg, L, M):
     return packed, packed + rest + io
 
 
+def decode_config(n_layers, world):
+    """The headline workload's config object (both arms report this one)."""
+    weights = 0
+    for L in wl.stack_70b(n_layers):
+        ng = L.K // L.group
+        nnz = int(L.frac * L.N * L.K)
+        weights += L.N * L.K * L.bits // 8 + L.N * ng * 3 + (L.N + 1) * 4 + nnz * 6
+    return {"workload": f"70B-shaped stack decode: {n_layers} layers x q/k/v/o/gate/up/down, INT4 group 128, "
+                        "0.1% FP16 outliers, M=1, y fp32",
+            "layers": n_layers, "M": 1, "weights_GB_per_gpu": round(weights / 1e9, 3),
+            "l2": "inputs larger than L2 (weights per step far above 129 MB)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def check_graph_covers(g, ys, what):
     """Replay the captured step once over outputs filled with NaN: every
     product must have written its output, or work escaped the capture."""
@@ -608,7 +622,7 @@ def run_reference(args, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": "70B-shaped stack decode M=1, INT4 g128, 0.1% outliers (bounded row sample)"},
+            "config": decode_config(args.layers, world),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": txt},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -634,11 +648,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dec["ms_per_step"], 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "int4 weights, fp16 x fp16 MMA, fp32 accumulate", "data": "synthetic",
-            "config": {"workload": "70B-shaped stack decode: 80 layers x q/k/v/o/gate/up/down, INT4 group 128, "
-                                   "0.1% FP16 outliers, M=1, y fp32",
-                       "layers": args.layers, "M": 1, "weights_GB_per_gpu": dec["weights_GB"],
-                       "l2": "inputs larger than L2 (weights per step far above 129 MB)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "config": decode_config(args.layers, world),
             "frac_of_hbm_peak": round(dec["value"] / P["hbm"], 4),
             "frac_of_nominal_8TBs": dec["frac_of_nominal_8TBs"],
             "roofline": dec["roofline"], "e2e": dec["e2e"], "clocks": dec["clocks"],
