@@ -201,9 +201,33 @@ struct Chunk {
     static constexpr int NC = G / 4;
     static constexpr int CB = NC * BITS / 8;
     static constexpr int NW = (NC * BITS + 31) / 32;
+    // CB = 12 or 20 (3-bit and 5-bit g128, 6-bit g64): rows and groups are
+    // 8-byte aligned and CB = 4 (mod 8), so a chunk starts 8-byte aligned on
+    // even lanes t and 4 bytes past that on odd ones.  It is read as one
+    // 4-byte and (CB - 4) / 8 8-byte loads -- the 4-byte one at the end of
+    // the chunk on even lanes, at its start on odd ones -- instead of CB / 4
+    // 4-byte loads, which filled the load queue.  The words stay in load
+    // order R = (8-byte words..., 4-byte word) in the ring; order() puts them
+    // in stream order when the group is used (odd lanes: the 4-byte word
+    // first).
+    static constexpr bool SPLIT = CB % 8 == 4 && CB > 4;
+    __device__ __forceinline__ static void order(const uint32_t (&r)[NW], uint32_t (&w)[NW], bool odd)
+    {
+#pragma unroll
+        for (int i = 0; i < NW; i++) w[i] = odd ? r[(i + NW - 1) % NW] : r[i];
+    }
     __device__ __forceinline__ static void load(const uint8_t* p, uint32_t (&w)[NW])
     {
-        if constexpr (CB % 16 == 0) {
+        if constexpr (SPLIT) {
+            const bool odd = (reinterpret_cast<uintptr_t>(p) & 4u) != 0;
+            const uint8_t* p8 = p + (odd ? 4 : 0);
+#pragma unroll
+            for (int i = 0; i < (CB - 4) / 8; i++) {
+                const uint2 v = ldg_stream64(p8 + 8 * i);
+                w[2 * i] = v.x; w[2 * i + 1] = v.y;
+            }
+            w[NW - 1] = ldg_stream32(p + (odd ? 0 : CB - 4));
+        } else if constexpr (CB % 16 == 0) {
 #pragma unroll
             for (int i = 0; i < CB / 16; i++) {
                 const uint4 v = ldg_stream128(p + 16 * i);
@@ -676,6 +700,7 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     // affine: the staged group parameters, this thread's words of block group 0
     const uint32_t* const ps = reinterpret_cast<const uint32_t*>(smem + C::prm_offset(gpsplit)) + warp * 16 + gq * 2;
 
+    const bool odd_chunk = ((t * CB) & 4) != 0;   // the chunk starts 4 bytes past an 8-byte boundary
     // this lane's B-fragment slot (token clamped to MP-1; its column is discarded)
     uint32_t xlo[NT];
 #pragma unroll
@@ -756,7 +781,14 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
                     const unsigned char* xg[NT];
 #pragma unroll
                     for (int nt = 0; nt < NT; nt++) xg[nt] = xb[nt] + d * C::GSTRIDE;
-                    mma_group<BITS, G, MP>(wr[d][0], wr[d][1], prm[d], xg, yacc, magic);
+                    if constexpr (Chunk<BITS, G>::SPLIT) {
+                        uint32_t s0[NW], s1[NW];
+                        Chunk<BITS, G>::order(wr[d][0], s0, odd_chunk);
+                        Chunk<BITS, G>::order(wr[d][1], s1, odd_chunk);
+                        mma_group<BITS, G, MP>(s0, s1, prm[d], xg, yacc, magic);
+                    } else {
+                        mma_group<BITS, G, MP>(wr[d][0], wr[d][1], prm[d], xg, yacc, magic);
+                    }
                 }
                 if (jj + d + D < ngrp) issue(dc, std::integral_constant<int, D + d>{});
             }
