@@ -63,8 +63,8 @@ def parse():
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum over the launches
 # of a layer, profiles/k_gemv_decode_70b_stack_m1.md), valid only for the
 # kernel source it was taken on.
-DECODE_TRAFFIC = {"kernel_sha256": "4d76dd81e7126a9ec22dcc9fd6b145379a26aee92cacbfebeeefe1d79f5e6744",
-                  "bytes_per_layer": 453.861e6}
+DECODE_TRAFFIC = {"kernel_sha256": "81d0b63f634cec6ff1293db11d0c73c32a4f2d0e1db0015e1f9451b94cd4397c",
+                  "bytes_per_layer": 454.066e6}
 
 
 def decode_traffic(n_layers):
