@@ -21,10 +21,13 @@
 //    1024 + 2^p q, one packed FMA -> q - zp, one packed multiply by the fp16
 //    scale, FP16 outliers patched in) into a 6-deep ring of 128 x 64 fp16
 //    tiles;
-//  * warp 18 issues four tcgen05.mma (M=128, N=tokens, K=16) per K block from
-//    one elected lane into a TMEM accumulator of 128 lanes x 128 columns;
-//  * warps 0-15 read the accumulator (lane = weight row, column = token) and
-//    store y rows in pair order.
+//  * warps 18 and 19, one per dequantization group, each issue four
+//    tcgen05.mma (M=128, N=tokens, K=16) per K block of their parity from one
+//    elected lane into their own TMEM accumulator of 128 lanes x 128 columns;
+//  * warps 0-15 add the two accumulators (lane = weight row, column = token)
+//    and store y rows in pair order.
+// One launch may cover several products over the same routing (an MoE
+// layer's gate and up): blockIdx.x runs over every product's row tiles.
 // Every mbarrier wait is bounded; a wait that gives up writes QG_ERR_TIMEOUT
 // into the device status word.
 #include <cuda_bf16.h>
