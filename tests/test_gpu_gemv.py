@@ -175,3 +175,29 @@ def test_forward_multi_against_oracle(qg, bits, group, M):
     torch.cuda.synchronize()
     for (q, wmax), y in zip(qs, ys):
         check_product(y, oracle.linear(x, q), x, wmax)
+
+
+def test_decode_full_size_sampled(qg):
+    # the decode launches of the 70B-shaped stack at full size, M = 1, as the
+    # bench step issues them: fused q/k/v, o alone, fused gate/up, down alone.
+    # No outliers (a row's quantization then depends on that row only), so
+    # the oracle quantizes just the sampled rows of each seeded W while the
+    # device quantizes all of it.
+    hid, ffn, kv = 8192, 28672, 1024
+    shapes = {"q": (hid, hid), "k": (kv, hid), "v": (kv, hid), "o": (hid, hid),
+              "gate": (ffn, hid), "up": (ffn, hid), "down": (hid, ffn)}
+    Ws = {p: wl.gen_weight(N, K, seed=2000 + i) for i, (p, (N, K)) in enumerate(shapes.items())}
+    qws = {p: qg.qpack_quantize(W.cuda(), 4, 128, 0.0) for p, W in Ws.items()}
+    x_hid, x_ffn = wl.gen_x(1, hid, seed=41), wl.gen_x(1, ffn, seed=42)
+    ys = {}
+    ys.update(zip(("q", "k", "v"), qg.qgemm_forward_multi(x_hid.cuda(), [qws["q"], qws["k"], qws["v"]])))
+    ys["o"] = qg.qgemm_forward(x_hid.cuda(), qws["o"])
+    ys.update(zip(("gate", "up"), qg.qgemm_forward_multi(x_hid.cuda(), [qws["gate"], qws["up"]])))
+    ys["down"] = qg.qgemm_forward(x_ffn.cuda(), qws["down"])
+    torch.cuda.synchronize()
+    for p, (N, K) in shapes.items():
+        x = x_ffn if K == ffn else x_hid
+        for n0 in sorted({0, (N // 2) // 64 * 64 - 32, N - 64}):
+            q = oracle.quantize(Ws[p][n0:n0 + 64], 4, 128, 0.0)
+            wmax = float(np.abs(oracle.dequant(q)).max())
+            check_product(ys[p][:, n0:n0 + 64], oracle.linear(x, q), x, wmax)
