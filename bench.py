@@ -63,8 +63,8 @@ def parse():
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum over the launches
 # of a layer, profiles/k_gemv_decode_70b_stack_m1.md), valid only for the
 # kernel source it was taken on.
-DECODE_TRAFFIC = {"kernel_sha256": "81d0b63f634cec6ff1293db11d0c73c32a4f2d0e1db0015e1f9451b94cd4397c",
-                  "bytes_per_layer": 454.066e6}
+DECODE_TRAFFIC = {"kernel_sha256": "a0a55612a8bb9fef472524400d7228b514bb7911791c9362a1a5b9b73b45cf34",
+                  "bytes_per_layer": 453.862e6}
 
 
 def decode_traffic(n_layers):
