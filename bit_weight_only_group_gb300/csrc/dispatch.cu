@@ -247,7 +247,7 @@ size_t moe_workspace_bytes(int T, int k, int E, int n, const qg_qweight* experts
 qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const qg_qweight* experts, int E,
                      int n, void* const* ys, qg_ydtype yt, void* ws, size_t, cudaStream_t s)
 {
-    MoeWs p;
+    MoeWs p{};
     moe_ws_layout(T, k, E, n, experts, &p, ws);
     const int P = T * k;
     const qg_qweight& w0 = experts[0];

@@ -393,7 +393,7 @@ qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, i
               cudaStream_t s)
 {
     using C = Cfg<4>;
-    Ws p;
+    Ws p{};
     ws_layout(M, w.K, &p, ws);
     {
         const long long total8 = (long long)M * w.K / 8;

@@ -491,7 +491,7 @@ __global__ void k_quant_done() {}
 qg_status launch_quantize(const uint16_t* W, float /*frac*/, const qg_qweight& w, void* ws,
                           cudaStream_t s)
 {
-    QuantWs p;
+    QuantWs p{};
     ws_layout(w.N, &p, ws);
     const long long total = (long long)w.N * w.K;
     const int sms = num_sms();
