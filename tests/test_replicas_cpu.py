@@ -2,7 +2,8 @@
 torchrun launches them.  The product path does not shard across GPUs (each
 rank is an independent replica), so what runs on more than one rank is the
 host logic: rendezvous, barrier, the max of the ranks' times and the sum of
-their work, and the reference arm printing on rank 0 alone."""
+their work, and the reference arm printing on rank 0 alone.  One more test
+runs the reference arm on one rank and checks its line's contract keys."""
 import json
 import os
 import socket
@@ -69,3 +70,25 @@ def test_reference_arm_prints_on_rank_zero_only():
     d = json.loads(lines[0][0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["config"]["parallelism"] == "replicas x2"
+
+
+def test_reference_arm_line_has_the_contract_keys():
+    # one rank: the reference arm's JSON line carries the keys the bench
+    # contract asks for, with the headline's metric and config
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        env.pop(k, None)
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "1"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=240)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    sys.path.insert(0, ROOT)
+    import bench
+    assert d["metric"] == bench.METRIC and d["config"] == bench.decode_config(80, 1)
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
