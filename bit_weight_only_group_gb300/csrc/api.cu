@@ -1,5 +1,6 @@
 // C-ABI entry points of libqgemm: argument validation (host, before any
 // launch), dispatch to the kernels, and per-thread error messages.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -36,35 +37,47 @@ qg_status cuda_fail(cudaError_t e, const char* what)
     return QG_ERR_CUDA;
 }
 
+// Per-device attribute caches (any thread may call; the values written are
+// the same whoever writes them, and the atomics make the reads well defined).
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_smem_per_sm[kMaxDevices];
+std::atomic<int> g_smem_reserved[kMaxDevices];
+std::atomic<int> g_sm_count[kMaxDevices];
+}  // namespace
+
 // Dynamic shared memory per CTA that lets at most `cap` CTAs share an SM.
 int smem_for_cap(int cap)
 {
-    static int cache[64][2] = {};   // per device: shared memory per SM, reserved per CTA
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-    if (!cache[dev][0]) {
-        int per_sm = 0, reserved = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+    int per_sm = g_smem_per_sm[dev].load(std::memory_order_acquire);
+    int reserved = g_smem_reserved[dev].load(std::memory_order_relaxed);
+    if (!per_sm) {
         if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
             per_sm <= 0)
             per_sm = 233472;
         if (cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
             reserved < 0)
             reserved = 1024;
-        cache[dev][1] = reserved;
-        cache[dev][0] = per_sm;
+        g_smem_reserved[dev].store(reserved, std::memory_order_relaxed);
+        g_smem_per_sm[dev].store(per_sm, std::memory_order_release);
     }
-    return cache[dev][0] / (cap + 1) - cache[dev][1] + 16;   // (cap + 1) CTAs no longer fit, cap still do
+    return per_sm / (cap + 1) - reserved + 16;   // (cap + 1) CTAs no longer fit, cap still do
 }
 
 int num_sms()
 {
-    static int cache[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-    if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    if (cached) {
+        const int v = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (v) return v;
+    }
     int v = 0;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
-    if (dev >= 0 && dev < 64) cache[dev] = v;
+    if (cached) g_sm_count[dev].store(v, std::memory_order_relaxed);
     return v;
 }
 
