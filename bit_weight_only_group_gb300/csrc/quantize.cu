@@ -21,6 +21,7 @@
 //   5. k_compact     one warp per row writes CSR columns/values in k order;
 //   6. k_quant_*     one thread per (row, group): group statistics, scale /
 //                    zero-point or codebook, codes, packing.
+#include <atomic>
 #include <cuda_fp16.h>
 
 #include "qg_internal.h"
@@ -500,14 +501,14 @@ qg_status launch_quantize(const uint16_t* W, float /*frac*/, const qg_qweight& w
     if (has_out) {
         e = cudaMemsetAsync(p.hist, 0, sizeof(unsigned) * kBins, s);
         if (e != cudaSuccess) return cuda_fail(e, "memset histogram");
-        static bool attr_set[64] = {false};
+        static std::atomic<bool> attr_set[64];   // per device (setting it twice is harmless)
         int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev < 64 && !attr_set[dev]) {
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
+        if (dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
             e = cudaFuncSetAttribute(k_hist, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)(sizeof(unsigned) * kBins));
             if (e != cudaSuccess) return cuda_fail(e, "k_hist smem attribute");
-            attr_set[dev] = true;
+            if (dev < 64) attr_set[dev].store(true, std::memory_order_release);
         }
         long long blocks = ceil_div(total / 8 + 1, 1024);
         if (blocks > sms) blocks = sms;
