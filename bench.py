@@ -13,8 +13,9 @@ roofline's ``achieved``.
 
 Secondary lines in the same JSON object: prefill qGEMM TFLOP/s at M = 2048 on
 one layer of the same stack, the MoE layer (16 experts, 256 tokens, top-2
-Zipf routing) through the grouped entry point, and one decode step of the
-7B-shaped stack with per-layer widths 2/3/5/6.
+Zipf routing) through the grouped entry point, one decode step of the
+7B-shaped stack with per-layer widths 2/3/5/6, and the device quantizer
+(offline) on one 28672 x 8192 matrix.
 
 ``--impl reference`` times the CPU oracle (plain C, fp64) on the host cores
 on a bounded sample of the same workload.
@@ -514,6 +515,35 @@ def run_widths(qg, args, P):
             "l2": "graphs of copies larger than L2 (sweep); 3.2 GB per step (stack)"}
 
 
+def run_quantize(qg, P):
+    """The device quantizer (outlier selection, group statistics, codes,
+    packing: offline, not on the decode path) on one 28672 x 8192 fp16
+    matrix of the 70B stack, INT4 group 128, 0.1 % outliers, into preallocated
+    buffers; GB/s of fp16 W read (each call makes five passes over W)."""
+    dev = torch.device("cuda")
+    N, K, bits, group, frac = 28672, 8192, 4, 128, 0.001
+    W = wl.gen_weight(N, K, outlier_frac=frac, device=dev, distinct_positions=False)
+    out = qg.QWeight.empty(N, K, bits, group, frac, dev)
+    ws = torch.empty(qg.qpack_workspace_size(N, K), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        qg.qpack_quantize(W, bits, group, frac, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    reps = 10
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        qg.qpack_quantize(W, bits, group, frac, out=out, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    wbytes = N * K * 2
+    del W, out, ws
+    torch.cuda.empty_cache()
+    return {"metric": "device quantizer (offline)", "value": round(wbytes / ms / 1e6, 1), "unit": "GB/s of fp16 W",
+            "ms_per_matrix": round(ms, 4), "passes_over_W": 5,
+            "config": "28672x8192 fp16 W, INT4 group 128, 0.1% outliers, outputs and workspace preallocated"}
+
+
 def run_stack7b(qg, P):
     """One decode step (M=1) of the 32-layer 7B-shaped stack with per-layer
     widths 2 (codebook) / 3 / 5 / 6, group 128, 0.1 % outliers: 224 products
@@ -666,6 +696,10 @@ def main():
             line["decode_7b_mixed"] = run_stack7b(qg, P)
         except Exception as e:
             line["decode_7b_mixed"] = {"error": repr(e)}
+        try:
+            line["quantize"] = run_quantize(qg, P)
+        except Exception as e:
+            line["quantize"] = {"error": repr(e)}
     if rank == 0:
         v, cores, txt = oracle_rate(args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
