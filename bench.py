@@ -62,8 +62,8 @@ def parse():
 
 # DRAM bytes (read + written) per 70B-shaped layer of the decode step, from one
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum over the launches
-# of a layer, profiles/k_gemv_decode_70b_stack_m1.md), valid only for the
-# kernel source it was taken on.
+# of a layer, captured on a 2-layer stack), valid only for the kernel source
+# it was taken on.
 DECODE_TRAFFIC = {"kernel_sha256": "a0a55612a8bb9fef472524400d7228b514bb7911791c9362a1a5b9b73b45cf34",
                   "bytes_per_layer": 453.862e6}
 

@@ -1,5 +1,7 @@
 // C-ABI entry points of libqgemm: argument validation (host, before any
 // launch), dispatch to the kernels, and per-thread error messages.
+#include <cuda.h>
+
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -81,8 +83,6 @@ int num_sms()
     return v;
 }
 
-namespace {
-
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int64_t nnz_of(int64_t N, int64_t K, float frac)
@@ -101,7 +101,8 @@ qg_status check_shape(int64_t N, int64_t K, int bits, int group)
     return QG_OK;
 }
 
-// Validate a weight descriptor for use by a product kernel.
+// Validate a weight descriptor for use by a product kernel or as the output
+// of a quantizer.
 qg_status check_qweight(const qg_qweight* w, const char* who)
 {
     if (!w) return fail(QG_ERR_INVALID_ARG, "%s: null weight descriptor", who);
@@ -126,7 +127,56 @@ qg_status check_qweight(const qg_qweight* w, const char* who)
     return QG_OK;
 }
 
-}  // namespace
+// Checks shared by both quantizer entry points (everything but the scratch).
+qg_status check_quantize_args(const uint16_t* W, float outlier_frac, const qg_qweight* out, const char* who)
+{
+    if (!W) return fail(QG_ERR_INVALID_ARG, "%s: W is null", who);
+    if (!aligned(W, 16)) return fail(QG_ERR_ALIGNMENT, "%s: W must be 16-byte aligned", who);
+    qg_status st = check_qweight(out, who);
+    if (st != QG_OK) return st;
+    if (!(outlier_frac >= 0.0f && outlier_frac < 1.0f))
+        return fail(QG_ERR_INVALID_ARG, "%s: outlier_frac must be in [0, 1)", who);
+    const int64_t n = nnz_of(out->N, out->K, outlier_frac);
+    if (n != out->nnz)
+        return fail(QG_ERR_INVALID_ARG, "%s: nnz=%d but floor(frac*N*K)=%lld", who, out->nnz, (long long)n);
+    if (out->nnz > 0 && (int64_t)out->N * out->K > 0xFFFFFFFFll)
+        return fail(QG_ERR_INVALID_ARG, "%s: N*K above 2^32 with outliers", who);
+    return QG_OK;
+}
+
+// Identity of the CUDA context current on this thread (0 if none): caches of
+// device addresses are keyed on it, so that a context destroyed and created
+// again (cudaDeviceReset) gets its addresses looked up again.
+unsigned long long current_context_id()
+{
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static std::atomic<GetCurrent> get_current{nullptr};
+    static std::atomic<GetId> get_id{nullptr};
+    GetCurrent gc = get_current.load(std::memory_order_acquire);
+    GetId gi = get_id.load(std::memory_order_acquire);
+    if (!gc || !gi) {
+        void* f1 = nullptr;
+        void* f2 = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+            q1 != cudaDriverEntryPointSuccess || !f1)
+            return 0;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+            q2 != cudaDriverEntryPointSuccess || !f2)
+            return 0;
+        gc = reinterpret_cast<GetCurrent>(f1);
+        gi = reinterpret_cast<GetId>(f2);
+        get_current.store(gc, std::memory_order_release);
+        get_id.store(gi, std::memory_order_release);
+    }
+    CUcontext ctx = nullptr;
+    if (gc(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    if (gi(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id + 1;   // never 0 for a live context
+}
+
 }  // namespace qg
 
 using namespace qg;
@@ -175,17 +225,8 @@ qg_status qpack_workspace_size(int32_t N, int32_t K, size_t* bytes)
 qg_status qpack_quantize(const uint16_t* W, float outlier_frac, const qg_qweight* out, void* ws,
                          size_t ws_bytes, void* stream)
 {
-    if (!W) return fail(QG_ERR_INVALID_ARG, "qpack_quantize: W is null");
-    if (!aligned(W, 16)) return fail(QG_ERR_ALIGNMENT, "qpack_quantize: W must be 16-byte aligned");
-    qg_status st = check_qweight(out, "qpack_quantize");
+    qg_status st = check_quantize_args(W, outlier_frac, out, "qpack_quantize");
     if (st != QG_OK) return st;
-    if (!(outlier_frac >= 0.0f && outlier_frac < 1.0f))
-        return fail(QG_ERR_INVALID_ARG, "qpack_quantize: outlier_frac must be in [0, 1)");
-    const int64_t n = nnz_of(out->N, out->K, outlier_frac);
-    if (n != out->nnz)
-        return fail(QG_ERR_INVALID_ARG, "qpack_quantize: nnz=%d but floor(frac*N*K)=%lld", out->nnz, (long long)n);
-    if (out->nnz > 0 && (int64_t)out->N * out->K > 0xFFFFFFFFll)
-        return fail(QG_ERR_INVALID_ARG, "qpack_quantize: N*K above 2^32 with outliers");
     const size_t need = quantize_workspace_bytes(out->N, out->K);
     if (!ws || ws_bytes < need)
         return fail(QG_ERR_WORKSPACE, "qpack_quantize: workspace %zu bytes < %zu", ws ? ws_bytes : (size_t)0, need);

@@ -38,17 +38,22 @@ namespace {
 constexpr int kMaxStatusDevices = 64;
 std::mutex g_status_mu;
 int* g_status_addr[kMaxStatusDevices];
+unsigned long long g_status_ctx[kMaxStatusDevices];
 }  // namespace
 
+// Address of g_device_status in the current context, looked up once per
+// device and context (a context created anew gets a new lookup).
 int* device_status_ptr()
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxStatusDevices) return nullptr;
     std::lock_guard<std::mutex> lock(g_status_mu);
-    if (!g_status_addr[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!g_status_addr[dev] || !ctx || ctx != g_status_ctx[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
         g_status_addr[dev] = static_cast<int*>(p);
+        g_status_ctx[dev] = current_context_id();
     }
     return g_status_addr[dev];
 }

@@ -8,7 +8,7 @@
 //     y[pair, n] = sum_k x[token(pair), k] * (w_hat_e[n, k] + S_e[n, k])
 //
 // Routing (a stable counting sort of the (token, slot) pairs by expert,
-// bjdmk.com.cn 5648983 page, sections 1-2) is done by the routing kernel;
+// "On-device MoE" page, sections 1-2) is done by the routing kernel;
 // k_gather_x16 then writes x in that order as fp16 with the K positions of
 // every block of 8 permuted (0,4,1,5,2,6,3,7) like the weight operand, and
 // one CTA of k_gemm_swap_u4 computes a 128-row x (up to 64)-token tile:

@@ -3,7 +3,7 @@
 //     y[m, n] = sum_k x[m, k] * (w_hat[n, k] + S[n, k])
 //
 // The pages' fused kernel dequantizes INT4 tiles into shared memory and runs
-// the tensor cores on them (bjdmk.com.cn 5414039 page, section 3); this is
+// the tensor cores on them ("70B on one GPU" page, section 3); this is
 // that structure written for sm_103a:
 //  * one CTA computes a 256 x 256 tile of y (256 tokens x 256 weight rows)
 //    as two fp32 accumulators of 128 tokens in tensor memory (all 512 TMEM

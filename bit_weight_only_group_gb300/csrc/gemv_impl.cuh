@@ -1,7 +1,7 @@
 // Decode-side fused dequantization product for small M (M <= 64):
 //     y[m, n] = sum_k x[m, k] * (w_hat[n, k] + S[n, k])
 // Memory-bound: every packed weight byte is read from HBM once, unpacked in
-// registers (never written back as fp16 -- pwwt.cn page, section 4.1: unpack
+// registers (never written back as fp16 -- "Mixed-width quantization" page, section 4.1: unpack
 // and multiply-accumulate in one loop, the value lives only in registers),
 // and consumed by warp-level tensor-core MMAs with fp32 accumulation
 // (section 4.2 requires fp32 accumulation).
@@ -25,7 +25,7 @@
 //    Elephants Can't Run"; the per-width pair plans are this library's own.)
 //  * 2-bit groups hold 4 fp16 codebook entries; two byte-permutes (PRMT)
 //    look up a pair of entries at once from a 2-register table.
-//  * the FP16 outliers (bjdmk.com.cn 5414039 page, section 2, step 3: added
+//  * the FP16 outliers ("70B on one GPU" page, section 2, step 3: added
 //    back after the product) are applied in the cluster epilogue from CSR.
 #pragma once
 

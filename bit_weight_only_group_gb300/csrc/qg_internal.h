@@ -20,6 +20,15 @@ int num_sms();
 // the current device (1 <= cap <= 8).
 int smem_for_cap(int cap);
 
+// Argument checks shared by the entry points (each sets the error message).
+bool aligned(const void* p, size_t a);
+int64_t nnz_of(int64_t N, int64_t K, float frac);
+qg_status check_shape(int64_t N, int64_t K, int bits, int group);
+qg_status check_qweight(const qg_qweight* w, const char* who);
+qg_status check_quantize_args(const uint16_t* W, float outlier_frac, const qg_qweight* out, const char* who);
+// Identity of the thread's current CUDA context (0 if none).
+unsigned long long current_context_id();
+
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

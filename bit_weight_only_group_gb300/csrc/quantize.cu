@@ -3,12 +3,12 @@
 // explicit IEEE round-to-nearest-even intrinsic (this file is also built with
 // -fmad=false), evaluated in the same order as the method's definition.
 //
-// Method (bjdmk.com.cn 5414039 page, section 2, "group-wise outlier-aware
+// Method ("70B on one GPU" page, section 2, "group-wise outlier-aware
 // quantization"): the largest-magnitude fraction of weights is kept apart in
 // FP16; each group of consecutive weights gets its own scale/zero-point from
-// the min/max of its remaining weights (m.mzlw.cn 206779 page, section 1.1
-// formula); 2-bit groups use a 4-entry k-means codebook (pwwt.cn page,
-// sections 2.1 and 4.1); codes are packed LSB-first (pwwt.cn, section 3).
+// the min/max of its remaining weights ("Inference acceleration guide" page, section 1.1
+// formula); 2-bit groups use a 4-entry k-means codebook ("Mixed-width quantization" page,
+// sections 2.1 and 4.1); codes are packed LSB-first ("Mixed-width quantization" page, section 3).
 //
 // Launch sequence (all on the caller's stream, no host sync):
 //   1. k_hist        per-block shared-memory histogram of the 15-bit |w|

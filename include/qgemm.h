@@ -7,21 +7,21 @@
  * The method (from the pages this library follows):
  *  - affine asymmetric quantizer: scale = (max - min) / (qmax - qmin),
  *    zero_point = qmin - round(min / scale), q = round(w / scale) +
- *    zero_point, w_hat = (q - zero_point) * scale  (m.mzlw.cn 206779 page,
+ *    zero_point, w_hat = (q - zero_point) * scale  ("Inference acceleration guide" page,
  *    section 1.1 "quantization is a lossy mapping");
  *  - statistics per group of consecutive weights along K (64 or 128), after
  *    excluding the largest-magnitude 0.1 % of weights, which are kept in FP16
- *    and added back after the product  (bjdmk.com.cn 5414039 page, section 2,
+ *    and added back after the product  ("70B on one GPU" page, section 2,
  *    "group-wise outlier-aware quantization", steps 1-3);
  *  - widths 2, 3, 4, 5, 6 bits; 2-bit groups use a 4-entry non-uniform
- *    codebook found by k-means  (pwwt.cn page, section 2.1 table and 4.1);
+ *    codebook found by k-means  ("Mixed-width quantization" page, section 2.1 table and 4.1);
  *  - codes packed LSB-first in a little-endian bit stream: 3-bit 8 values
  *    in 3 bytes, 5-bit 8 values in 5 bytes, 6-bit 4 values in 3 bytes,
  *    2-bit 4 values per byte, 4-bit two per byte with the even index in the
- *    low half  (pwwt.cn page, sections 3.1-3.2 and the 2.1 table);
+ *    low half  ("Mixed-width quantization" page, sections 3.1-3.2 and the 2.1 table);
  *  - unpacking happens on the computing device, fused into the product,
- *    with fp32 accumulation  (pwwt.cn page, sections 1.2 and 4.1-4.2;
- *    bjdmk.com.cn 5414039 page, section 3 "kernel fusion").
+ *    with fp32 accumulation  ("Mixed-width quantization" page, sections 1.2 and 4.1-4.2;
+ *    "70B on one GPU" page, section 3 "kernel fusion").
  *
  * Conventions shared by every entry point:
  *  - Every pointer in a qg_qweight, every x / y / topk_ids / W argument and
@@ -66,7 +66,7 @@ typedef enum { QG_Y_F32 = 0, QG_Y_BF16 = 1 } qg_ydtype;
 
 /*
  * A quantized weight matrix W [N, K] in the planar layout (codes in one
- * array, per-group parameters in others; pwwt.cn page, section 3.3).
+ * array, per-group parameters in others; "Mixed-width quantization" page, section 3.3).
  *
  *  N, K        output and input features.  K % group == 0.
  *  bits        2, 3, 4, 5 or 6.
@@ -101,7 +101,7 @@ typedef struct {
  * nnz = floor(outlier_frac * N * K) evaluated in double; the outlier arrays
  * take (N+1)*4 + nnz*4 + nnz*2 bytes.  Any output pointer may be NULL.
  * Effective bits per weight = bits + 24/group (fp16 scale + u8 zp) or
- * 2 + 64/group (2-bit codebook of 4 fp16 entries); pwwt.cn page, section 2.3
+ * 2 + 64/group (2-bit codebook of 4 fp16 entries); "Mixed-width quantization" page, section 2.3
  * gives the same accounting for the scale overhead.
  * Errors: QG_ERR_INVALID_ARG for N, K <= 0, K % group, outlier_frac outside
  * [0, 1); QG_ERR_UNSUPPORTED for bits outside 2..6 or group not 64/128.
@@ -117,8 +117,8 @@ QG_API qg_status qpack_workspace_size(int32_t N, int32_t K, size_t* bytes);
  * Quantize and pack W [N, K] (fp16, row-major, DEVICE, 16-byte aligned, all
  * values finite) into the buffers of `out`, whose N, K, bits, group and nnz
  * the caller fills (nnz from qpack_query_sizes) and whose pointers the
- * caller allocates.  Steps (bjdmk.com.cn 5414039 page, section 2; m.mzlw.cn
- * 206779 page, section 1.1; pwwt.cn page, sections 3-4):
+ * caller allocates.  Steps ("70B on one GPU" page, section 2; "Inference acceleration guide"
+ * page, section 1.1; "Mixed-width quantization" page, sections 3-4):
  *   1. outliers: the nnz largest |w| of the whole matrix (ties: lower
  *      linear index n*K + k), stored as CSR, columns ascending;
  *   2. per (row, group): min/max over the non-outliers with 0 included;
@@ -149,12 +149,17 @@ QG_API qg_status qpack_quantize(const uint16_t* W, float outlier_frac, const qg_
  * callers only.  Same operation, arguments and results as qpack_quantize
  * (bit-identical output).
  *  - Scratch: a fixed 1 MiB array in the library's own device memory, held
- *    by every GPU that loads the library until the process exits.  Matrices
- *    whose scratch need (qpack_workspace_size) exceeds it -- more than about
- *    76,000 rows -- are rejected with QG_ERR_WORKSPACE before anything runs.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current) and caches it; make
- *    that first call before any stream capture.
+ *    by every GPU that loads the library until the process exits.  Only the
+ *    outlier selection uses it: without outliers (outlier_frac = 0) any size
+ *    is accepted; with outliers, matrices whose scratch need
+ *    (qpack_workspace_size) exceeds it -- more than about 76,000 rows -- are
+ *    rejected with QG_ERR_WORKSPACE before anything runs.
+ *  - Argument checks and their status codes are exactly qpack_quantize's.
+ *  - The first call with outliers on each device looks up the array's
+ *    device address (cudaGetSymbolAddress, with that device current) and
+ *    caches it for that device's current context; make that first call
+ *    before any stream capture.  A context created anew (after
+ *    cudaDeviceReset) gets a new lookup on its first such call.
  *  - Every call shares the array and it keeps the last call's contents; each
  *    call clears what must start at zero.  Calls that overlap on the GPU
  *    (e.g. on two unordered streams) race on the array: order them.
@@ -168,8 +173,8 @@ QG_API qg_status qgemm_workspace_size(int32_t M, const qg_qweight* w, size_t* by
 
 /*
  * y[m, n] = sum_k x[m, k] * (w_hat[n, k] + S[n, k])   for m < M, n < N,
- * with w_hat the dequantized weight and S the FP16 outliers (bjdmk.com.cn
- * 5414039 page, sections 2-3).  Dequantization happens in registers / on-chip
+ * with w_hat the dequantized weight and S the FP16 outliers ("70B on one GPU"
+ * page, sections 2-3).  Dequantization happens in registers / on-chip
  * memory inside the product; accumulation is fp32.
  *   x   bf16 [M, K] row-major with row stride ldx >= K elements (DEVICE).
  *   y   [M, N] row-major with row stride ldy >= N elements, fp32 or bf16
@@ -195,7 +200,7 @@ QG_API qg_status qgemm_forward(const uint16_t* x, int32_t M, int32_t ldx, const 
  * Several products that share one input in one call (a fused projection,
  * e.g. the q, k and v, or the gate and up, matrices of a transformer layer):
  *     ys[q][m, n] = sum_k x[m, k] * (w_hat_q[n, k] + S_q[n, k])   for q < n.
- * The pages define the single product (bjdmk.com.cn 5414039 page, sections
+ * The pages define the single product ("70B on one GPU" page, sections
  * 2-3); this call computes exactly that product for each weight, so each
  * ys[q] equals what qgemm_forward would write for ws[q].  In the decode range
  * (M <= 64) all n products run as one kernel launch over their concatenated
@@ -218,7 +223,7 @@ QG_API qg_status qgemm_moe_workspace_size(int32_t T, int32_t k, int32_t E, const
                                    size_t* bytes);
 
 /*
- * Grouped product over top-k routed experts (bjdmk.com.cn 5648983 page,
+ * Grouped product over top-k routed experts ("On-device MoE" page,
  * sections 1-2: each token activates its top-k of the experts):
  *   y[t, j, :] = x[t, :] . (w_hat + S)_{e}^T   with e = topk_ids[t, j],
  * for t < T, j < k.  No gate weights are applied.

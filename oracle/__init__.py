@@ -8,11 +8,11 @@ Every function takes and returns numpy arrays (torch CPU tensors are accepted
 as inputs).  fp16/bf16 data travel as their uint16 bit patterns.
 
 What each function follows is cited in ``qoracle.c``; in short:
-``quantize`` is the affine asymmetric quantizer (m.mzlw.cn 206779 page,
+``quantize`` is the affine asymmetric quantizer ("Inference acceleration guide" page,
 section 1.1) with per-group statistics after excluding the largest-magnitude
-outliers, which are kept in FP16 (bjdmk.com.cn 5414039 page, section 2), a
-4-entry k-means codebook at 2 bits (pwwt.cn page, sections 2.1 and 4.1) and
-LSB-first packing (pwwt.cn page, sections 3.1-3.2); ``linear`` is
+outliers, which are kept in FP16 ("70B on one GPU" page, section 2), a
+4-entry k-means codebook at 2 bits ("Mixed-width quantization" page, sections 2.1 and 4.1) and
+LSB-first packing ("Mixed-width quantization" page, sections 3.1-3.2); ``linear`` is
 y = x . (x_hat + S)^T in fp64.
 """
 from __future__ import annotations

@@ -11,21 +11,21 @@
  *
  *  - Affine asymmetric quantizer: scale = (max - min) / (qmax - qmin),
  *    zero_point = qmin - round(min / scale), q = round(x / scale) + zero_point,
- *    x_hat = (q - zero_point) * scale  (m.mzlw.cn 206779 page, section 1.1).
+ *    x_hat = (q - zero_point) * scale  ("Inference acceleration guide" page, section 1.1).
  *  - Per-group statistics over groups of consecutive weights along K, with the
  *    top 0.1 % of weights by magnitude excluded and kept as FP16 outliers that
- *    are added back after the matrix product (bjdmk.com.cn 5414039 page,
+ *    are added back after the matrix product ("70B on one GPU" page,
  *    section 2, steps 1-3; group size 128).
  *  - 2-bit layers use a 4-entry non-uniform codebook found by k-means
- *    (pwwt.cn page, sections 2.1 table and 4.1).
+ *    ("Mixed-width quantization" page, sections 2.1 table and 4.1).
  *  - Packing: b-bit codes stored LSB-first in a little-endian bit stream;
  *    the pages' unpack routines read 3-bit units of 8 values in 3 bytes with
  *    shifts 0,3,...,21, 6-bit units of 4 values in 3 bytes with shifts
- *    0,6,12,18, 5-bit units of 8 values in 5 bytes with shifts 5i (pwwt.cn
+ *    0,6,12,18, 5-bit units of 8 values in 5 bytes with shifts 5i ("Mixed-width quantization"
  *    page, sections 3.1-3.2), the 4-bit value pair as the low/high half of a
  *    byte (section 2.1 table).
  *  - The product accumulates in fp64 here (the pages require at least fp32
- *    accumulation, pwwt.cn page, section 4.2).
+ *    accumulation, "Mixed-width quantization" page, section 4.2).
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *  round = round-half-to-even; q clamped to [0, 2^b - 1]; the group range is

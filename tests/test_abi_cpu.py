@@ -115,6 +115,43 @@ def test_quantize_validation_without_gpu(qg):
     assert L.qpack_quantize(W, 0.001, ctypes.byref(d), ctypes.c_void_p(0x600010), ws_need, None) == -3
 
 
+def test_both_quantizers_refuse_the_same_bad_descriptors(qg):
+    # qpack_quantize and qpack_quantize_noalloc share their argument checks:
+    # each bad descriptor gets the same status from both, before any launch
+    L = qg.lib()
+    f = L.qpack_quantize_noalloc
+    f.argtypes = [ctypes.c_void_p, ctypes.c_float, ctypes.POINTER(qg.QgQWeight), ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    W = ctypes.c_void_p(0x400000)
+    ws = ctypes.c_void_p(0x600000)
+
+    def good():
+        d = _fake_desc(qg, N=64, K=1024, nnz=oracle.nnz(64, 1024, 0.001))
+        d.out_row_ptr, d.out_col, d.out_val = 0x500000, 0x510000, 0x520000
+        return d
+
+    cases = []
+    d = good(); d.out_col = 0x510002; cases.append(("misaligned out_col", d, 0.001, -3))
+    d = good(); d.out_val = 0x520001; cases.append(("misaligned out_val", d, 0.001, -3))
+    d = good(); d.out_row_ptr = 0x500002; cases.append(("misaligned row_ptr", d, 0.001, -3))
+    d = good(); d.scale = 0x110001; cases.append(("misaligned scale", d, 0.001, -3))
+    d = good(); d.bits, d.scale, d.zp, d.codebook = 2, None, None, 0x130004
+    cases.append(("misaligned codebook", d, 0.001, -3))
+    d = good(); d.packed = 0x100008; cases.append(("misaligned packed", d, 0.001, -3))
+    d = good(); cases.append(("wrong nnz", d, 0.002, -1))
+    d = good(); d.out_col = None; cases.append(("null outlier array", d, 0.001, -1))
+    d = good(); d.N, d.K, d.nnz = 1 << 20, 1 << 15, 0; cases.append(("N*K above the product limit", d, 0.0, -1))
+    d = good(); d.bits = 7; cases.append(("unsupported width", d, 0.001, -2))
+    d = good(); d.group = 32; cases.append(("unsupported group", d, 0.001, -2))
+    d = good(); cases.append(("outlier_frac out of range", d, 1.5, -1))
+    for what, d, frac, expect in cases:
+        a = L.qpack_quantize(W, frac, ctypes.byref(d), ws, 1 << 30, None)
+        b = f(W, frac, ctypes.byref(d), None)
+        assert a == b == expect, (what, a, b)
+    assert f(ctypes.c_void_p(0x400002), 0.001, ctypes.byref(good()), None) == -3   # misaligned W
+    assert f(None, 0.001, ctypes.byref(good()), None) == -1
+
+
 def test_valid_call_without_a_device_reports_cuda_error(qg):
     # every argument passes host validation; the first CUDA call then fails
     # (no device here) and the status says so instead of crashing

@@ -77,9 +77,9 @@ def test_moe_layer_4096_experts(qg):
 
 @pytest.mark.parametrize("group,T,k,E,hot", [(64, 300, 2, 3, True), (128, 300, 2, 3, True), (128, 40, 2, 40, False)])
 def test_moe_tensor_core_chunks_and_fallback(qg, group, T, k, E, hot):
-    # 4-bit experts run on the tensor cores in chunks of up to 256 routed
+    # 4-bit experts run on the tensor cores in chunks of up to 64 routed
     # pairs per expert: with `hot` routing, expert 0 receives every token's
-    # first slot (300 pairs, two chunks); more than 32 experts take the
+    # first slot (300 pairs, five chunks); more than 32 experts take the
     # decode kernel instead
     N, K = 200, 640
     qs, wmax = _experts(E, N, K, 4, group, 0.002, seed=90)

@@ -37,7 +37,7 @@ def test_pack_matches_hand_worked_units(bits, codes, expect):
     assert got.tolist() == codes
 
 
-UNIT = {2: 4, 3: 8, 4: 2, 5: 8, 6: 4}   # values per packing unit (pwwt.cn section 3.1)
+UNIT = {2: 4, 3: 8, 4: 2, 5: 8, 6: 4}   # values per packing unit ("Mixed-width quantization" page, section 3.1)
 UNIT_BYTES = {2: 1, 3: 3, 4: 1, 5: 5, 6: 3}
 
 
@@ -133,7 +133,7 @@ def test_sizing_7b_mixed_stack_is_a_bit_over_3GB():
     g = _sizing()
     total = sum(_bytes(L) for L in wl.stack_7b()) / 1e9
     assert g["stack7b_mixed_GB_min"][0] < total < g["stack7b_mixed_GB_max"][0], total
-    # average payload width of the stack is about 3.5 bits (pwwt.cn section 2.2: 3.4-3.6)
+    # average payload width of the stack is about 3.5 bits ("Mixed-width quantization" page, section 2.2: 3.4-3.6)
     w = sum(L.N * L.K * L.bits for L in wl.stack_7b()) / sum(L.N * L.K for L in wl.stack_7b())
     assert 3.4 <= w <= 3.7, w
 
@@ -245,6 +245,32 @@ def test_affine_grid_aligned_ramp_is_exact():
     assert (oracle.dequant(q) == W.astype(np.float64)).all()
     assert (q.scale.view(np.float16) == np.float16(0.25)).all()
     assert (q.zp == 5).all()
+
+
+def test_affine_exact_ties_round_half_to_even():
+    # "round" in the quantizer formula (inference-acceleration guide page,
+    # section 1.1) read as round half to even.  Two 4-bit groups whose range
+    # is exactly 3.75 force scale = 3.75 / 15 = 0.25 (exact in fp32 and fp16),
+    # and weights at odd multiples of 0.125 land exactly on k + 1/2.  The
+    # codes below are worked out by hand; rounding half away from zero, or
+    # half up, gives a different code for every tie.
+    g = 64
+    a = np.zeros(g, np.float16)             # min -1.25, max 2.5: zp = -round(-5) = 5 (no tie)
+    a[:9] = [-1.25, 2.5, 0.125, 0.625, -0.125, -0.625, 1.125, 0.375, -0.375]
+    b = np.zeros(g, np.float16)             # min -1.125, max 2.625: min/scale = -4.5 is a tie
+    b[:3] = [-1.125, 2.625, 0.875]
+    q = oracle.quantize(np.concatenate([a, b])[None, :], 4, g, 0.0)
+    assert (q.scale.view(np.float16) == np.float16(0.25)).all()
+    # zp = 0 - round(min / scale): round(-5) = -5 and round(-4.5) = -4 (even)
+    assert q.zp.tolist() == [[5, 4]]
+    codes = oracle.unpack(q.packed[0], 2 * g, 4)
+    # group a, q = round(w / 0.25) + 5: -5 -> 0, 10 -> 15, 0.5 -> 0, 2.5 -> 2,
+    # -0.5 -> 0, -2.5 -> -2, 4.5 -> 4, 1.5 -> 2, -1.5 -> -2; zeros -> 5
+    assert codes[:9].tolist() == [0, 15, 5, 7, 5, 3, 9, 7, 3]
+    assert (codes[9:g] == 5).all()
+    # group b, q = round(w / 0.25) + 4: -4.5 -> -4, 10.5 -> 10, 3.5 -> 4; zeros -> 4
+    assert codes[g:g + 3].tolist() == [0, 14, 8]
+    assert (codes[g + 3:] == 4).all()
 
 
 def test_affine_zero_and_one_signed_groups():

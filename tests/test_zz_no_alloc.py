@@ -14,7 +14,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as wl
+from _parity import assert_quantized_equal
 
 pytestmark = pytest.mark.gpu
 
@@ -60,15 +62,32 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row():
         got = _quantize_noalloc(qg, W, bits, group, frac)
         torch.cuda.synchronize()
         _same(got, ref)
+        # and the bytes are the oracle's
+        assert_quantized_equal(got, oracle.quantize(W.cpu(), bits, group, frac))
 
 
-def test_noalloc_rejects_matrices_beyond_its_scratch():
+def test_noalloc_rejects_matrices_with_outliers_beyond_its_scratch():
+    # with outliers the selection needs 12 bytes of scratch per row: 100,000
+    # rows do not fit the fixed array and the call is refused before any launch
     import bit_weight_only_group_gb300 as qg
     N, K = 100_000, 64
-    d = qg.QgQWeight(N, K, 4, 64, 0x100000, 0x200000, 0x300000, None, 0, None, None, None)
+    nnz = oracle.nnz(N, K, 0.001)
+    d = qg.QgQWeight(N, K, 4, 64, 0x100000, 0x200000, 0x300000, None, nnz, 0x500000, 0x600000, 0x700000)
     f = qg.lib().qpack_quantize_noalloc
     f.argtypes = [ctypes.c_void_p, ctypes.c_float, ctypes.POINTER(qg.QgQWeight), ctypes.c_void_p]
     f.restype = ctypes.c_int
-    st = f(ctypes.c_void_p(0x400000), 0.0, ctypes.byref(d), None)
+    st = f(ctypes.c_void_p(0x400000), 0.001, ctypes.byref(d), None)
     assert st == -4
     assert "scratch" in qg.last_error()
+
+
+def test_noalloc_without_outliers_takes_any_row_count():
+    # no outliers: no scratch is used, so a matrix far above the scratch's
+    # row limit quantizes, with the same bytes as the workspace entry point
+    import bit_weight_only_group_gb300 as qg
+    N, K = 100_000, 128
+    W = wl.gen_weight(N, K, seed=21).cuda()
+    ref = _quantize_with_workspace(qg, W, 4, 128, 0.0)
+    got = _quantize_noalloc(qg, W, 4, 128, 0.0)
+    torch.cuda.synchronize()
+    _same(got, ref)

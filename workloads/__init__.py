@@ -7,14 +7,14 @@ per-layer bit-width tables and seeded random draws.
 Shapes and widths come from the pages this project follows:
 
 * single 4096x4096 layer, 4-bit, group 128 ("a 4096x4096 weight tensor",
-  pwwt.cn page, section 1.2);
+  "Mixed-width quantization" page, section 1.2);
 * mixed 2/3/5/6-bit widths with a 2-bit share of about half the layers,
   3-bit at most 8 %, 5-bit in attention/middle layers, 6-bit at the ends
-  (pwwt.cn page, section 2.2, width-allocation table);
+  ("Mixed-width quantization" page, section 2.2, width-allocation table);
 * a 70B-shaped stack kept at INT4 group 128 with FP16 outliers
-  (bjdmk.com.cn 5414039 page, section 2);
+  ("70B on one GPU" page, section 2);
 * an MoE layer with 16 experts and top-2 routing over a skewed expert
-  popularity (bjdmk.com.cn 5648983 page, sections 1-2).
+  popularity ("On-device MoE" page, sections 1-2).
 
 Value distributions: weights ~ N(0, 0.02) drawn in fp32 and cast to fp16;
 planted outliers of magnitude U(3, 6) with a random sign (the 5414039 page,
