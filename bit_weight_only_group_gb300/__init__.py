@@ -35,7 +35,7 @@ ABI_FUNCTIONS = ("qpack_query_sizes", "qpack_workspace_size", "qpack_quantize", 
                  "qgemm_workspace_size",
                  "qgemm_forward", "qgemm_forward_multi", "qgemm_moe_workspace_size", "qgemm_moe_grouped",
                  "qgemm_moe_grouped_multi",
-                 "qgemm_device_status",
+                 "qgemm_device_status", "qgemm_selftest_bounded_wait",
                  "qgemm_last_error")
 
 
@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
         L.qgemm_moe_grouped_multi.argtypes = [vp, i32, vp, i32, pq, i32, i32, ctypes.POINTER(vp), ctypes.c_int, vp,
                                               sz, vp]
         L.qgemm_device_status.argtypes = [pi32, i32]
+        L.qgemm_selftest_bounded_wait.argtypes = [i32, vp]
         L.qgemm_forward_multi.argtypes = [vp, i32, i32, pq, i32, ctypes.POINTER(vp), pi32, ctypes.c_int, vp, sz, vp]
         for name in ABI_FUNCTIONS[:-1]:
             getattr(L, name).restype = ctypes.c_int
@@ -330,3 +331,9 @@ def qgemm_device_status(reset: bool = False) -> int:
     v = ctypes.c_int32(0)
     _check(lib().qgemm_device_status(ctypes.byref(v), 1 if reset else 0), "qgemm_device_status")
     return v.value
+
+
+def qgemm_selftest_bounded_wait(poll_limit: int = 2, stream=None) -> None:
+    """Launch the kernel whose bounded mbarrier wait must give up; afterwards
+    qgemm_device_status() reads QG_ERR_TIMEOUT (-6)."""
+    _check(lib().qgemm_selftest_bounded_wait(poll_limit, _stream(stream)), "qgemm_selftest_bounded_wait")

@@ -195,6 +195,13 @@ qg_status qgemm_device_status(int32_t* status, int32_t reset)
     return QG_OK;
 }
 
+qg_status qgemm_selftest_bounded_wait(int32_t poll_limit, void* stream)
+{
+    if (poll_limit < 1 || poll_limit > 64)
+        return fail(QG_ERR_INVALID_ARG, "qgemm_selftest_bounded_wait: poll_limit=%d not in 1..64", poll_limit);
+    return launch_wait_selftest((uint32_t)poll_limit, static_cast<cudaStream_t>(stream));
+}
+
 qg_status qpack_query_sizes(int32_t N, int32_t K, int32_t bits, int32_t group, float outlier_frac,
                             size_t* packed_bytes, size_t* scale_bytes, size_t* zp_bytes,
                             size_t* codebook_bytes, int32_t* nnz)

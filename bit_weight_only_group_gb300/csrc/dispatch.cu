@@ -74,6 +74,33 @@ qg_status read_device_status(int* out, int reset)
     return QG_OK;
 }
 
+// Self-check of the bounded waits: one mbarrier that nothing ever arrives on,
+// waited on with a poll limit; the wait gives up and the kernel reports
+// QG_ERR_TIMEOUT through the status word, as a tensor-core kernel does when
+// one of its waits runs out.  It issues no TMA and no MMA, and holds nothing
+// when it exits.
+__global__ void k_wait_selftest(int* status, uint32_t limit)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = ptx::smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(b, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !ptx::mbar_wait_bounded(b, 0, limit) && status) atomicExch(status, (int)QG_ERR_TIMEOUT);
+}
+
+qg_status launch_wait_selftest(uint32_t limit, cudaStream_t s)
+{
+    int* st = device_status_ptr();
+    if (!st) return fail(QG_ERR_CUDA, "qgemm_selftest_bounded_wait: no device status word on the current device");
+    k_wait_selftest<<<1, 32, 0, s>>>(st, limit);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "qgemm_selftest_bounded_wait: launch");
+    return QG_OK;
+}
+
 namespace {
 
 gemv::Problem make_problem(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,
@@ -227,21 +254,6 @@ qg_status launch_gemv_multi(const uint16_t* x, int M, int ldx, const qg_qweight*
         case 5: return gemv::launch_multi<5>(t, ws[0].group, s);
         default: return gemv::launch_multi<6>(t, ws[0].group, s);
     }
-}
-
-// Products with M above the decode kernel's range, in 64-row passes of the
-// decode kernel.  (The tensor-core kernel takes these over where built.)
-qg_status launch_gemv_chunked(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,
-                              qg_ydtype yt, cudaStream_t s)
-{
-    const size_t esz = yt == QG_Y_BF16 ? 2 : 4;
-    for (int m0 = 0; m0 < M; m0 += kGemvMaxM) {
-        const int mc = std::min(kGemvMaxM, M - m0);
-        qg_status st = launch_gemv(x + (size_t)m0 * ldx, mc, ldx, w, static_cast<char*>(y) + (size_t)m0 * ldy * esz,
-                                   ldy, yt, s);
-        if (st != QG_OK) return st;
-    }
-    return QG_OK;
 }
 
 size_t moe_workspace_bytes(int T, int k, int E, int n, const qg_qweight* experts)

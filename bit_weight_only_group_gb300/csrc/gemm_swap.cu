@@ -28,8 +28,11 @@
 //    and store y rows in pair order.
 // One launch may cover several products over the same routing (an MoE
 // layer's gate and up): blockIdx.x runs over every product's row tiles.
+// Rows whose largest scale times 15 exceeds fp16's range are built at
+// scale * 2^-e and their outputs multiplied by 2^e (see row_exponent).
 // Every mbarrier wait is bounded; a wait that gives up writes QG_ERR_TIMEOUT
-// into the device status word.
+// into the device status word (TMA loads or MMAs the CTA issued may then
+// still be in flight when it exits, and that call's output is not valid).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
@@ -71,7 +74,8 @@ constexpr int A_BYTES = BW * BK * 2;         // 16 KB
 constexpr int OFF_P = X_RING;
 constexpr int OFF_A = OFF_P + SP * P_BYTES;
 constexpr int OFF_BAR = OFF_A + SA * A_BYTES;
-constexpr int SMEM = OFF_BAR + 1024 /* barriers */ + 1024 /* alignment */;
+constexpr int OFF_EROW = OFF_BAR + 512;     // per-row exponents (128 bytes)
+constexpr int SMEM = OFF_BAR + 1024 /* barriers, exponents */ + 1024 /* alignment */;
 constexpr int TMEM_COLS = kGroups * NBMAX;   // one accumulator per group
 constexpr int kMaxExperts = 32;              // tensor maps travel as kernel parameters (all products' experts)
 constexpr int kMaxProducts = 2;              // products sharing the routing in one launch (gate and up)
@@ -160,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto empty_a = [&](int s) { return bars + 8 * (2 * SXMAX + 2 * SP + SA + s); };
     const uint32_t acc_full = bars + 8 * (2 * SXMAX + 2 * SP + 2 * SA);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 8 * (2 * SXMAX + 2 * SP + 2 * SA + 1));
+    uint8_t* e_row = smem + OFF_EROW;
     auto x_tile = [&](int s) { return sbase + s * x_stage; };
     auto p_tile = [&](int s) { return smem + OFF_P + s * P_BYTES; };
     auto a_tile = [&](int s) { return sbase + OFF_A + s * A_BYTES; };
@@ -256,6 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // their lines now
         for (int off = 0; off < ng * 2; off += 128) asm volatile("prefetch.global.L1 [%0];" ::"l"(sp_row + off / 2));
         for (int off = 0; off < ng; off += 128) asm volatile("prefetch.global.L1 [%0];" ::"l"(zp_row + off));
+        // power-of-two headroom of this row, published for the epilogue
+        const int ex = tc::row_exponent<4>(sp_row, ng, hk);
+        if (grp == 0 && hk == 0) e_row[r] = (uint8_t)ex;
         // outlier cursor of this row: the next entry and the one after it
         const int* ocolp = a.col[ep];
         const uint16_t* ovalp = a.val[ep];
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int b = 0; b < 2; b++) {
                 const int kb = kp * PK + grp + b * kGroups;
                 const int gi = min(kb, KB - 1) / KB_PER_G;
-                pq[b] = (uint32_t)__ldg(sp_row + gi) | ((uint32_t)__ldg(zp_row + gi) << 16);
+                pq[b] = tc::f16_times_pow2(__ldg(sp_row + gi), ex) | ((uint32_t)__ldg(zp_row + gi) << 16);
             }
         };
         auto deq_block = [&](const uint4& w, uint32_t pq, unsigned char* at) {
@@ -308,7 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (ocol < k0 + 32) {
                 if (ocol >= k0) {
                     const int kk = ocol - kb * BK;
-                    *reinterpret_cast<uint16_t*>(at + r * 128 + (((kk >> 3) ^ rsw) << 4) + (tc::perm8_pos(kk) << 1)) = oval;
+                    const int pos = tc::chunk_pos<4>(kk & 31);
+                    *reinterpret_cast<uint16_t*>(at + r * 128 + (((4 * (kk >> 5) + (pos >> 3)) ^ rsw) << 4) + ((pos & 7) << 1)) =
+                        (uint16_t)tc::f16_times_pow2(oval, ex);
                 }
                 ocol = ncol;
                 oval = nval;
@@ -367,20 +377,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             pcur[1] = pnext[1];
         }
         // ------------------------------------------------ epilogue: TMEM (lane = weight row, column = token) -> y
+        tc::deq_sync();   // every row's exponent is in shared memory
         if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(acc_full, 0));
         if (ok) {
             ptx::tc_fence_after();
             // warp w reads TMEM lanes 32 (w % 4).. and every 4th 16-column chunk from w / 4
             const int q = warp & 3, c0 = warp >> 2;
             const int nrow = n0 + 32 * q + lane;
+            const float rescale = __int_as_float((127 + e_row[32 * q + lane]) << 23);   // 2^e of the row
             for (int c = c0; 16 * c < NB; c += kDeqWarps / 4) {
                 uint32_t v[16], v1[16];
                 ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(16 * c), v);
                 ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(NBMAX + 16 * c), v1);
                 ptx::tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; j++)   // accumulator 1 holds blocks 1, 3, ... (none when K = 64)
+                for (int j = 0; j < 16; j++) {   // accumulator 1 holds blocks 1, 3, ... (none when K = 64)
                     if (KB > 1) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v1[j]));
+                    v[j] = __float_as_uint(__uint_as_float(v[j]) * rescale);
+                }
                 if (nrow < a.N) {
 #pragma unroll
                     for (int j = 0; j < 16; j++) {

@@ -1,33 +1,40 @@
 // Prefill-side fused dequantization product on the 5th-generation tensor
-// cores (tcgen05 + TMEM), for M above the decode range:
+// cores (tcgen05 + TMEM), for M above the decode range, at every width:
 //     y[m, n] = sum_k x[m, k] * (w_hat[n, k] + S[n, k])
 //
 // The pages' fused kernel dequantizes INT4 tiles into shared memory and runs
 // the tensor cores on them ("70B on one GPU" page, section 3); this is
-// that structure written for sm_103a:
+// that structure written for sm_103a and extended to the 2/3/5/6-bit widths
+// of the "Mixed-width quantization" page (sections 2-3):
 //  * one CTA computes a 256 x 256 tile of y (256 tokens x 256 weight rows)
 //    as two fp32 accumulators of 128 tokens in tensor memory (all 512 TMEM
 //    columns), so every dequantized weight tile feeds 256 tokens;
 //  * warp 16 (one lane) streams the fp16 x tiles (TMA, 128-byte swizzle,
-//    256 x 64) into a 2-deep ring and warp 17 the packed 4-bit weight tiles
-//    (TMA, 256 rows x 128 bytes = 4 K blocks, 128-byte swizzle) into a 2-deep
-//    ring; each ring has its own full/empty mbarriers, so loads run ahead of
-//    the consumers;
-//  * warps 0-15 (two threads per weight row, 32 k each) unpack the codes with
-//    masks into fp16 1024 + 2^p q, turn them into the exact integers q - zp
-//    with one packed FMA and multiply by the fp16 group scale (one
-//    rounding), patch the FP16 outliers of the block in place, and store the
-//    256 x 64 fp16 tile in the K-major 128-byte-swizzled layout the tensor
-//    core reads (K order permuted inside blocks of 8, matching x);
-//    the fp16 tiles go to a 3-deep ring (the packed slot is released once
-//    the stores that consumed its codes are issued);
+//    256 x 64) into a 2-deep ring; at 4 bits warp 17 streams the packed
+//    weight tiles (TMA, 256 rows x 128 bytes = 4 K blocks, 128-byte swizzle)
+//    into a 2-deep ring; at the other widths, whose K blocks are not 128-byte
+//    multiples, each dequantization thread loads its own codes from global
+//    memory (a register ring four K blocks deep);
+//  * warps 0-15 (two threads per weight row, 32 k each) unpack the codes
+//    into fp16 pairs -- masks into fp16 1024 + 2^p q and one packed FMA give
+//    the exact integers q - zp (per-width pair plans, the decode kernel's),
+//    one packed multiply applies the fp16 group scale (one rounding); 2-bit
+//    codes look their fp16 codebook entries up with byte permutes -- patch
+//    the FP16 outliers of the block in, and store the 256 x 64 fp16 tile in
+//    the K-major 128-byte-swizzled layout the tensor core reads (K order
+//    permuted inside every 32 as the pair plan orders the codes, matching
+//    x) into a ring of 3 (4 bits) or 4 stages;
 //  * warp 18 (one lane) issues eight tcgen05.mma (M=128, N=256, K=16) per K
 //    block, four per accumulator, and commits them to the x and fp16
 //    rings' "empty" barriers;
 //  * warps 0-15 then read the accumulator with tcgen05.ld and store y.
-// Every mbarrier wait is bounded (a wait that gives up writes QG_ERR_TIMEOUT
-// into the device status word read by qgemm_device_status).  x is first
-// converted bf16 -> fp16 into the workspace (exact in fp16's normal range).
+// Rows whose largest scale times 2^bits - 1 exceeds fp16's range (groups
+// near +-65504) are built at scale * 2^-e and their outputs multiplied by
+// 2^e, so the operand never overflows.  Every mbarrier wait is bounded (a
+// wait that gives up writes QG_ERR_TIMEOUT into the device status word read
+// by qgemm_device_status; TMA loads or MMAs the CTA issued may then still be
+// in flight when it exits, and that call's output is not valid).  x is first
+// converted bf16 -> fp16 into the workspace (exact in fp16's range).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
@@ -40,9 +47,6 @@
 #include "qg_internal.h"
 
 namespace qg {
-
-qg_status launch_gemv_chunked(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,
-                              qg_ydtype yt, cudaStream_t s);
 
 qg_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw)
@@ -71,9 +75,10 @@ namespace tc {
 
 constexpr int BM = 256, BN = 256, BK = 64;
 constexpr int MH = 128;                 // tokens per accumulator (one tcgen05.mma covers M = 128)
-constexpr int SA = 2, SP = 2, SB = 3;   // ring depths: x tiles, packed tiles, fp16 weight tiles
+constexpr int SA = 2, SP = 2;           // ring depths: x tiles, packed tiles (4 bits)
 constexpr int TMEM_COLS = 2 * BN;       // two fp32 accumulators of 128 x 256
 constexpr int PK = 4;                   // K blocks per packed tile (128-byte rows at 4 bits)
+constexpr int DG = 4;                   // K blocks of codes in flight per thread (other widths)
 constexpr int kDeqWarps = 16;
 constexpr int kWarpA = kDeqWarps, kWarpP = kDeqWarps + 1, kWarpMma = kDeqWarps + 2;
 constexpr int kThreads = (kDeqWarps + 3) * 32;
@@ -82,18 +87,23 @@ constexpr int B_BYTES = BN * BK * 2;   // 32 KB fp16
 
 template <int BITS>
 struct Cfg {
-    static constexpr int P_BYTES = BN * PK * BK * BITS / 8;   // packed tile: 256 rows x 128 bytes
+    static constexpr bool TMA_CODES = BITS == 4;
+    static constexpr int SB = TMA_CODES ? 3 : 4;                        // fp16 weight tiles
+    static constexpr int P_BYTES = TMA_CODES ? BN * PK * BK * BITS / 8 : 0;   // 256 rows x 128 bytes
     static constexpr int P_ALIGNED = (P_BYTES + 1023) / 1024 * 1024;
     static constexpr int OFF_B = SA * A_BYTES;
     static constexpr int OFF_P = OFF_B + SB * B_BYTES;
     static constexpr int OFF_BAR = OFF_P + SP * P_ALIGNED;
-    static constexpr int SMEM = OFF_BAR + 1024 /* barriers */ + 1024 /* alignment */;
+    static constexpr int OFF_EROW = OFF_BAR + 512;                      // per-row exponents (256 bytes)
+    static constexpr int SMEM = OFF_BAR + 1024 /* barriers, exponents */ + 1024 /* alignment */;
 };
 
 struct Args {
     int M, N, K, ng;
+    const uint8_t* packed;   // codes (read directly at widths other than 4)
     const uint16_t* scale;
     const uint8_t* zp;
+    const uint2* cb;         // 2-bit codebooks: 4 fp16 entries per group
     const int* row_ptr;
     const int* col;
     const uint16_t* val;
@@ -105,13 +115,15 @@ struct Args {
     uint32_t magic;   // gemv::kF16Magic, a run-time value (one logic op per code pair)
 };
 
-template <int G>
+static_assert(kDeqWarps * 32 == 512, "deq_sync counts 512 dequantization threads");
+
+template <int BITS, int G>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_tc_u4(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
-                 const __grid_constant__ Args a)
+    k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+              const __grid_constant__ Args a)
 {
-    constexpr int BITS = 4;
     using C = Cfg<BITS>;
+    constexpr int SB = C::SB;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_u32(smem);
@@ -125,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto empty_b = [&](int s) { return bars + 8 * (2 * SA + 2 * SP + SB + s); };
     const uint32_t acc_full = bars + 8 * (2 * SA + 2 * SP + 2 * SB);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * (2 * SA + 2 * SP + 2 * SB + 1));
+    uint8_t* e_row = smem + C::OFF_EROW;
     auto a_tile = [&](int s) { return sbase + s * A_BYTES; };
     auto b_tile = [&](int s) { return sbase + C::OFF_B + s * B_BYTES; };
     auto p_tile = [&](int s) { return smem + C::OFF_P + s * C::P_ALIGNED; };
@@ -135,7 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SA; s++) { ptx::mbar_init(full_a(s), 1); ptx::mbar_init(empty_a(s), 1); }
-        for (int s = 0; s < SP; s++) { ptx::mbar_init(full_p(s), 1); ptx::mbar_init(empty_p(s), kDeqWarps); }
+        if constexpr (C::TMA_CODES)
+            for (int s = 0; s < SP; s++) { ptx::mbar_init(full_p(s), 1); ptx::mbar_init(empty_p(s), kDeqWarps); }
         for (int s = 0; s < SB; s++) { ptx::mbar_init(full_b(s), kDeqWarps); ptx::mbar_init(empty_b(s), 1); }
         ptx::mbar_init(acc_full, 1);
         ptx::fence_mbar_init();
@@ -146,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == kWarpA && lane == 0) {
         ptx::prefetch_tensormap(&xmap);
-        ptx::prefetch_tensormap(&wmap);
+        if constexpr (C::TMA_CODES) ptx::prefetch_tensormap(&wmap);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -167,16 +181,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == kWarpP) {
-        // ------------------------------------------------ packed weight tiles (TMA, PK K blocks each)
-        if (lane == 0) {
-            const int KP = (KB + PK - 1) / PK;
-            int s = 0;
-            uint32_t ph = 0;
-            for (int kp = 0; kp < KP; kp++) {
-                if (!ptx::mbar_wait(empty_p(s), ph ^ 1u)) { ok = false; break; }
-                ptx::mbar_expect_tx(full_p(s), C::P_BYTES);
-                ptx::tma_load_2d(ptx::smem_u32(p_tile(s)), &wmap, kp * (PK * BK * BITS / 8), n0, full_p(s));
-                if (++s == SP) { s = 0; ph ^= 1u; }
+        // ------------------------------------------------ packed weight tiles (TMA, PK K blocks each; 4 bits)
+        if constexpr (C::TMA_CODES) {
+            if (lane == 0) {
+                const int KP = (KB + PK - 1) / PK;
+                int s = 0;
+                uint32_t ph = 0;
+                for (int kp = 0; kp < KP; kp++) {
+                    if (!ptx::mbar_wait(empty_p(s), ph ^ 1u)) { ok = false; break; }
+                    ptx::mbar_expect_tx(full_p(s), C::P_BYTES);
+                    ptx::tma_load_2d(ptx::smem_u32(p_tile(s)), &wmap, kp * (PK * BK * BITS / 8), n0, full_p(s));
+                    if (++s == SP) { s = 0; ph ^= 1u; }
+                }
             }
         }
     } else if (warp == kWarpMma) {
@@ -212,14 +228,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hk = threadIdx.x & 1;                 // which 32 k of the block
         const int nr = n0 + r;
         const int n = min(nr, a.N - 1);
-        const uint16_t* sp_row = a.scale + (size_t)n * a.ng;
-        const uint8_t* zp_row = a.zp + (size_t)n * a.ng;
-        constexpr int KB_PER_G = G / BK;                // 1 or 2
         const int ng = a.ng;
-        // parameters of the current group and of the next two (loads in flight)
-        uint32_t sc_cur = __ldg(sp_row), zq_cur = __ldg(zp_row);
-        uint32_t sc_n1 = ng > 1 ? __ldg(sp_row + 1) : 0u, zq_n1 = ng > 1 ? __ldg(zp_row + 1) : 0u;
-        uint32_t sc_n2 = ng > 2 ? __ldg(sp_row + 2) : 0u, zq_n2 = ng > 2 ? __ldg(zp_row + 2) : 0u;
+        constexpr int KB_PER_G = G / BK;                // 1 or 2
+        // power-of-two headroom of this row (affine widths; codebook entries are fp16 already)
+        int ex = 0;
+        if constexpr (BITS != 2) ex = row_exponent<BITS>(a.scale + (size_t)n * ng, ng, hk);
+        if (hk == 0) e_row[r] = (uint8_t)ex;
+        // group parameters of the current group and of the next two (loads in
+        // flight): affine (scale bits, zero-point); codebook (two words of 4 fp16)
+        const uint16_t* sp_row = a.scale + (size_t)n * ng;
+        const uint8_t* zp_row = a.zp + (size_t)n * ng;
+        const uint2* cb_row = a.cb + (size_t)n * ng;
+        uint2 prm[3];
+        auto load_prm = [&](int gi) -> uint2 {
+            if constexpr (BITS == 2) return __ldg(cb_row + gi);
+            else return make_uint2(f16_times_pow2(__ldg(sp_row + gi), ex), (uint32_t)__ldg(zp_row + gi));
+        };
+        prm[0] = load_prm(0);
+        prm[1] = ng > 1 ? load_prm(1) : make_uint2(0u, 0u);
+        prm[2] = ng > 2 ? load_prm(2) : make_uint2(0u, 0u);
         // outlier cursor of this row: the next entry (ocol, oval) and the one
         // after it (ncol, nval), so that consuming an entry never waits for a load
         int op = 0, oe = 0, ocol = 0x7FFFFFFF, ncol = 0x7FFFFFFF;
@@ -236,78 +263,150 @@ __global__ void __launch_bounds__(kThreads, 1)
                 nval = a.val[op + 1];
             }
         }
-        // swizzled offsets, fixed per thread: source chunk (2*sub + hk) of the
-        // packed row, destination chunks (4*hk + j) of the fp16 row
+        // swizzled destination chunks (4*hk + j) of the fp16 row, fixed per thread
         const uint32_t rsw = r & 7;
-        uint32_t src_off[PK], dst_off[4];
-#pragma unroll
-        for (int sub = 0; sub < PK; sub++) src_off[sub] = r * 128 + (((2 * sub + hk) ^ rsw) << 4);
+        uint32_t dst_off[4];
 #pragma unroll
         for (int j = 0; j < 4; j++) dst_off[j] = r * 128 + (((4 * hk + j) ^ rsw) << 4);
         unsigned char* const btile0 = smem + C::OFF_B;
-        const int KP = (KB + PK - 1) / PK;
-        int sp = 0, sb = 0;
-        uint32_t pp = 0, pb = 1;   // parities: full_p to wait for, empty_b to wait for
-        for (int kp = 0; kp < KP && ok; kp++) {
-            const unsigned char* pt = p_tile(sp);
-            if (!ptx::mbar_wait(full_p(sp), pp)) { ok = false; break; }
+
+        // the operand of block kb in registers (16 fp16 pairs) -> the fp16 ring,
+        // outliers patched in; returns false if a wait gave up
+        int sb = 0;
+        uint32_t pb = 1;   // parity of empty_b to wait for
+        auto emit = [&](int kb, const uint32_t (&pr)[16]) -> bool {
+            if (!ptx::mbar_wait(empty_b(sb), pb)) return false;
+            unsigned char* bt = btile0 + sb * B_BYTES;
 #pragma unroll
-            for (int sub = 0; sub < PK; sub++) {
-                const int kb = kp * PK + sub;
-                if (kb >= KB) break;
-                if (kb > 0 && kb % KB_PER_G == 0) {      // next group
-                    const int gi = kb / KB_PER_G;
-                    sc_cur = sc_n1;
-                    zq_cur = zq_n1;
-                    sc_n1 = sc_n2;
-                    zq_n1 = zq_n2;
-                    if (gi + 2 < ng) {
-                        sc_n2 = __ldg(sp_row + gi + 2);
-                        zq_n2 = __ldg(zp_row + gi + 2);
-                    }
+            for (int j = 0; j < 4; j++)
+                *reinterpret_cast<uint4*>(bt + dst_off[j]) = make_uint4(pr[4 * j], pr[4 * j + 1], pr[4 * j + 2], pr[4 * j + 3]);
+            // FP16 outliers in this thread's 32 k; the dense value there is
+            // exactly 0 (affine), or the codebook entry nearest 0 (2 bits,
+            // whose stored value is the residual)
+            const int k0 = kb * BK + 32 * hk;
+            while (ocol < k0 + 32) {
+                if (ocol >= k0) {
+                    const int pos = chunk_pos<BITS>(ocol - k0);
+                    uint16_t* dst = reinterpret_cast<uint16_t*>(bt + r * 128 + (((4 * hk + (pos >> 3)) ^ rsw) << 4) + ((pos & 7) << 1));
+                    if constexpr (BITS == 2) *dst = f16_add_sat(*dst, oval, 0);
+                    else *dst = (uint16_t)f16_times_pow2(oval, ex);
                 }
-                const uint32_t add_lo = zq_cur * 0x00010001u + 0xE400E400u;   // -(1024 + zp)
-                const uint32_t add_hi = zq_cur * 0x00100010u + 0xD400D400u;   // -(64 + zp)
-                const uint32_t s2 = __byte_perm(sc_cur, 0u, 0x1010u);
-                const uint4 w = *reinterpret_cast<const uint4*>(pt + src_off[sub]);
-                if (!ptx::mbar_wait(empty_b(sb), pb)) { ok = false; break; }
-                unsigned char* bt = btile0 + sb * B_BYTES;
-                *reinterpret_cast<uint4*>(bt + dst_off[0]) = deq8_u4(w.x, add_lo, add_hi, s2, magic);
-                *reinterpret_cast<uint4*>(bt + dst_off[1]) = deq8_u4(w.y, add_lo, add_hi, s2, magic);
-                *reinterpret_cast<uint4*>(bt + dst_off[2]) = deq8_u4(w.z, add_lo, add_hi, s2, magic);
-                *reinterpret_cast<uint4*>(bt + dst_off[3]) = deq8_u4(w.w, add_lo, add_hi, s2, magic);
-                // FP16 outliers in this thread's 32 k: the dense value there is exactly 0
-                const int k0 = kb * BK + 32 * hk;
-                while (ocol < k0 + 32) {
-                    if (ocol >= k0) {
-                        const int kk = ocol - kb * BK;
-                        *reinterpret_cast<uint16_t*>(bt + r * 128 + (((kk >> 3) ^ rsw) << 4) + (perm8_pos(kk) << 1)) = oval;
-                    }
-                    ocol = ncol;
-                    oval = nval;
-                    if (++op + 1 < oe) {
-                        ncol = a.col[op + 1];
-                        nval = a.val[op + 1];
-                    } else {
-                        ncol = 0x7FFFFFFF;
-                    }
+                ocol = ncol;
+                oval = nval;
+                if (++op + 1 < oe) {
+                    ncol = a.col[op + 1];
+                    nval = a.val[op + 1];
+                } else {
+                    ncol = 0x7FFFFFFF;
                 }
-                ptx::fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) {
-                    ptx::mbar_arrive(full_b(sb));
-                    // the packed slot goes back to its producer only after the
-                    // stores that consumed its codes: a shared load of the
-                    // whole warp completes in several wavefronts, and a
-                    // release right after issuing it let the next TMA tile
-                    // overwrite rows that the later lanes had not read yet
-                    if (sub == PK - 1 || kb == KB - 1) ptx::mbar_arrive(empty_p(sp));
-                }
-                if (++sb == SB) { sb = 0; pb ^= 1u; }
             }
-            if (++sp == SP) { sp = 0; pp ^= 1u; }
+            ptx::fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(full_b(sb));
+            if (++sb == SB) { sb = 0; pb ^= 1u; }
+            return true;
+        };
+        // next group: shift the parameter window
+        auto next_group = [&](int kb) {
+            if (kb > 0 && kb % KB_PER_G == 0) {
+                const int gi = kb / KB_PER_G;
+                prm[0] = prm[1];
+                prm[1] = prm[2];
+                if (gi + 2 < ng) prm[2] = load_prm(gi + 2);
+            }
+        };
+
+        if constexpr (C::TMA_CODES) {
+            // 4 bits: codes come from the TMA ring (source chunk 2*sub + hk of the packed row)
+            uint32_t src_off[PK];
+#pragma unroll
+            for (int sub = 0; sub < PK; sub++) src_off[sub] = r * 128 + (((2 * sub + hk) ^ rsw) << 4);
+            const int KP = (KB + PK - 1) / PK;
+            int sp = 0;
+            uint32_t pp = 0;   // parity of full_p to wait for
+            for (int kp = 0; kp < KP && ok; kp++) {
+                const unsigned char* pt = p_tile(sp);
+                if (!ptx::mbar_wait(full_p(sp), pp)) { ok = false; break; }
+#pragma unroll
+                for (int sub = 0; sub < PK; sub++) {
+                    const int kb = kp * PK + sub;
+                    if (kb >= KB) break;
+                    next_group(kb);
+                    const uint32_t zq = prm[0].y;
+                    const uint32_t add_lo = zq * 0x00010001u + 0xE400E400u;   // -(1024 + zp)
+                    const uint32_t add_hi = zq * 0x00100010u + 0xD400D400u;   // -(64 + zp)
+                    const uint32_t s2 = __byte_perm(prm[0].x, 0u, 0x1010u);
+                    const uint4 w = *reinterpret_cast<const uint4*>(pt + src_off[sub]);
+                    uint32_t pr[16];
+                    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const uint4 d = deq8_u4(wv[j], add_lo, add_hi, s2, magic);
+                        pr[4 * j] = d.x; pr[4 * j + 1] = d.y; pr[4 * j + 2] = d.z; pr[4 * j + 3] = d.w;
+                    }
+                    if (!emit(kb, pr)) { ok = false; break; }
+                    // the packed slot goes back to its producer only after the
+                    // stores that consumed its codes (emit synchronized the warp):
+                    // a shared load of the whole warp completes in several
+                    // wavefronts, and a release right after issuing it let the
+                    // next TMA tile overwrite rows that later lanes had not read
+                    if (lane == 0 && (sub == PK - 1 || kb == KB - 1)) ptx::mbar_arrive(empty_p(sp));
+                }
+                if (++sp == SP) { sp = 0; pp ^= 1u; }
+            }
+        } else {
+            // other widths: each thread's 32-code chunk of block kb is 4*BITS
+            // bytes at byte (2*kb + hk) * 4*BITS of the row, loaded DG blocks ahead
+            using Ch = gemv::Chunk<BITS, 128>;
+            constexpr int NW = Ch::NW;
+            const uint8_t* prow = a.packed + (size_t)n * ((size_t)a.K * BITS / 8) + hk * 4 * BITS;
+            const bool odd = Ch::SPLIT && hk;   // the chunk starts 4 bytes past an 8-byte boundary
+            uint32_t wr[DG][NW];
+            gemv::static_for<0, DG>([&](auto dc) {
+                constexpr int d = decltype(dc)::value;
+                if (d < KB) Ch::load(prow + d * 8 * BITS, wr[d]);
+            });
+            for (int kb0 = 0; kb0 < KB && ok; kb0 += DG) {
+                gemv::static_for<0, DG>([&](auto dc) {
+                    constexpr int d = decltype(dc)::value;
+                    const int kb = kb0 + d;
+                    if (ok && kb < KB) {
+                        next_group(kb);
+                        uint32_t w[NW];
+                        if constexpr (Ch::SPLIT) Ch::order(wr[d], w, odd);
+                        else {
+#pragma unroll
+                            for (int i = 0; i < NW; i++) w[i] = wr[d][i];
+                        }
+                        uint32_t pr[16];
+                        if constexpr (BITS == 2) {
+                            const uint32_t lo = __byte_perm(prm[0].x, prm[0].y, 0x6420);
+                            const uint32_t hi = __byte_perm(prm[0].x, prm[0].y, 0x7531);
+                            gemv::static_for<0, NW>([&](auto wc) {
+                                constexpr int wi = decltype(wc)::value;
+#pragma unroll
+                                for (int jf = 0; jf < 4; jf++) {
+                                    const uint32_t f = (w[wi] >> (2 * jf)) & 0x03030303u;
+                                    pr[2 * (4 * wi + jf)] = cb_pair<0>(f, lo, hi);
+                                    pr[2 * (4 * wi + jf) + 1] = cb_pair<1>(f, lo, hi);
+                                }
+                            });
+                        } else {
+                            const uint32_t s2 = __byte_perm(prm[0].x, 0u, 0x1010u);
+                            const uint32_t zq = prm[0].y;
+                            gemv::static_for<0, 16>([&](auto ec) {
+                                constexpr int e = decltype(ec)::value;
+                                pr[e] = hmul2_u32(gemv::deq_affine<BITS, 32, e>(w, zq, magic), s2);
+                            });
+                        }
+                        if (kb + DG < KB) Ch::load(prow + (kb + DG) * 8 * BITS, wr[d]);
+                        if (!emit(kb, pr)) ok = false;
+                    }
+                });
+            }
         }
         // ------------------------------------------------ epilogue: TMEM -> y
+        deq_sync();   // every row's exponent is in shared memory
         if (ok && ptx::mbar_wait(acc_full, 0)) {
             ptx::tc_fence_after();
             // warp w reads TMEM lanes 32 (w % 4) .. (the lanes a warp may
@@ -321,6 +420,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t v[16];
                 ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, v);
                 ptx::tmem_ld_wait();
+                // rows built at scale * 2^-e: multiply back by 2^e (exact)
+                const uint4 ew = *reinterpret_cast<const uint4*>(e_row + cb);
+                if (ew.x | ew.y | ew.z | ew.w) {
+                    const uint32_t ewa[4] = {ew.x, ew.y, ew.z, ew.w};
+#pragma unroll
+                    for (int j = 0; j < 16; j++) {
+                        const int ej = (ewa[j >> 2] >> (8 * (j & 3))) & 0xFF;
+                        v[j] = __float_as_uint(__uint_as_float(v[j]) * __int_as_float((127 + ej) << 23));
+                    }
+                }
                 if (m < a.M) {
                     const int nb = n0 + cb;
                     if (a.y_bf16) {
@@ -355,22 +464,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpMma) ptx::tmem_dealloc(tmem, TMEM_COLS);
 }
 
-// bf16 [M, ldx] -> fp16 [M, K] (exact for |x| in fp16's normal range), with
-// the K positions of every block of 8 in the order (0,4,1,5,2,6,3,7) the
-// weight operand uses.
+// bf16 [M, ldx] -> fp16 [M, K] (exact for |x| in fp16's range), with the K
+// positions of every block of 32 in the order the weight operand uses: the
+// pair plan of the width puts codes lo and hi of entry e at 2e and 2e + 1.
+// One thread converts one block of 32 (64 bytes in, 64 bytes out).
+template <int BITS>
 __global__ void k_x_to_f16(const __nv_bfloat16* __restrict__ x, int M, int K, int ldx, __half* __restrict__ out)
 {
-    const long long total8 = (long long)M * K / 8;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total8;
+    const long long total32 = (long long)M * K / 32;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total32;
          i += (long long)gridDim.x * blockDim.x) {
-        const long long e = i * 8;
+        const long long e = i * 32;
         const int m = (int)(e / K), k = (int)(e % K);
         const __nv_bfloat16* src = x + (size_t)m * ldx + k;
-        constexpr int perm[8] = {0, 4, 1, 5, 2, 6, 3, 7};
-        __half h[8];
+        uint32_t v[16];   // the 32 bf16 values, two per word
+        if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
 #pragma unroll
-        for (int j = 0; j < 8; j++) h[j] = __float2half_rn(__bfloat162float(src[perm[j]]));
-        *reinterpret_cast<uint4*>(out + e) = *reinterpret_cast<const uint4*>(h);
+            for (int j = 0; j < 4; j++) {
+                const uint4 q = __ldg(reinterpret_cast<const uint4*>(src) + j);
+                v[4 * j] = q.x; v[4 * j + 1] = q.y; v[4 * j + 2] = q.z; v[4 * j + 3] = q.w;
+            }
+        } else {
+            const unsigned short* s16 = reinterpret_cast<const unsigned short*>(src);
+#pragma unroll
+            for (int j = 0; j < 16; j++) v[j] = (uint32_t)__ldg(s16 + 2 * j) | ((uint32_t)__ldg(s16 + 2 * j + 1) << 16);
+        }
+        auto f16 = [&](int c) -> uint32_t {   // bf16 -> fp32 (exact) -> fp16
+            const uint32_t b = (c & 1) ? (v[c >> 1] & 0xFFFF0000u) : (v[c >> 1] << 16);
+            return __half_as_ushort(__float2half_rn(__uint_as_float(b)));
+        };
+        uint32_t o[16];
+        gemv::static_for<0, 16>([&](auto ec) {
+            constexpr gemv::PairE q = gemv::plan_entry(BITS, 32, decltype(ec)::value);
+            o[decltype(ec)::value] = f16(q.lo) | (f16(q.hi) << 16);
+        });
+        uint4* dst = reinterpret_cast<uint4*>(out + e);
+#pragma unroll
+        for (int j = 0; j < 4; j++) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
     }
 }
 
@@ -386,58 +516,69 @@ size_t ws_layout(int M, int K, Ws* w, void* base)
     return total;
 }
 
-bool eligible(const qg_qweight& w) { return w.bits == 4 && (w.K % BK) == 0; }
-
-template <int G>
+template <int BITS, int G>
 qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy, qg_ydtype yt, void* ws,
               cudaStream_t s)
 {
-    using C = Cfg<4>;
+    using C = Cfg<BITS>;
     Ws p{};
     ws_layout(M, w.K, &p, ws);
     {
-        const long long total8 = (long long)M * w.K / 8;
-        const int blocks = (int)std::min<long long>(ceil_div(total8, 256), (long long)num_sms() * 8);
-        k_x_to_f16<<<blocks, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), M, w.K, ldx, p.x16);
+        const long long total32 = (long long)M * w.K / 32;
+        const int blocks = (int)std::min<long long>(ceil_div(total32, 256), (long long)num_sms() * 8);
+        k_x_to_f16<BITS><<<blocks, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), M, w.K, ldx, p.x16);
     }
     CUtensorMap xmap, wmap;
     qg_status st = encode_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.x16, (uint64_t)w.K, (uint64_t)M,
                              (uint64_t)w.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != QG_OK) return st;
-    st = encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.packed, (uint64_t)w.K / 2, (uint64_t)w.N,
-                   (uint64_t)w.K / 2, PK * BK / 2, BN, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st != QG_OK) return st;
+    if constexpr (C::TMA_CODES) {
+        st = encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.packed, (uint64_t)w.K * BITS / 8, (uint64_t)w.N,
+                       (uint64_t)w.K * BITS / 8, PK * BK * BITS / 8, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != QG_OK) return st;
+    } else {
+        wmap = xmap;   // unused: the codes are read directly
+    }
     Args a;
     a.M = M; a.N = w.N; a.K = w.K; a.ng = w.K / G;
-    a.scale = w.scale; a.zp = w.zp;
+    a.packed = w.packed;
+    a.scale = w.scale; a.zp = w.zp; a.cb = reinterpret_cast<const uint2*>(w.codebook);
     a.row_ptr = w.out_row_ptr; a.col = w.out_col; a.val = w.out_val; a.nnz = w.nnz;
     a.y = y; a.ldy = ldy; a.y_bf16 = yt == QG_Y_BF16;
     a.status = device_status_ptr();
     a.magic = gemv::kF16Magic;
     {
-        qg_status st2 = gemv::allow_smem(k_gemm_tc_u4<G>, C::SMEM);
+        qg_status st2 = gemv::allow_smem(k_gemm_tc<BITS, G>, C::SMEM);
         if (st2 != QG_OK) return st2;
     }
     dim3 grid((unsigned)ceil_div(M, BM), (unsigned)ceil_div(w.N, BN), 1);
-    k_gemm_tc_u4<G><<<grid, kThreads, C::SMEM, s>>>(xmap, wmap, a);
+    k_gemm_tc<BITS, G><<<grid, kThreads, C::SMEM, s>>>(xmap, wmap, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
     return QG_OK;
 }
 
+template <int BITS>
+qg_status run_bits(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy, qg_ydtype yt, void* ws,
+                   cudaStream_t s)
+{
+    return w.group == 64 ? run<BITS, 64>(x, M, ldx, w, y, ldy, yt, ws, s) : run<BITS, 128>(x, M, ldx, w, y, ldy, yt, ws, s);
+}
+
 }  // namespace tc
 
-size_t gemm_workspace_bytes(int M, const qg_qweight& w)
-{
-    return tc::eligible(w) ? tc::ws_layout(M, w.K, nullptr, nullptr) : 0;
-}
+size_t gemm_workspace_bytes(int M, const qg_qweight& w) { return tc::ws_layout(M, w.K, nullptr, nullptr); }
 
 qg_status launch_gemm(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy, qg_ydtype yt,
                       void* ws, size_t, cudaStream_t s)
 {
-    if (tc::eligible(w))
-        return w.group == 64 ? tc::run<64>(x, M, ldx, w, y, ldy, yt, ws, s) : tc::run<128>(x, M, ldx, w, y, ldy, yt, ws, s);
-    return launch_gemv_chunked(x, M, ldx, w, y, ldy, yt, s);
+    switch (w.bits) {
+        case 2: return tc::run_bits<2>(x, M, ldx, w, y, ldy, yt, ws, s);
+        case 3: return tc::run_bits<3>(x, M, ldx, w, y, ldy, yt, ws, s);
+        case 4: return tc::run_bits<4>(x, M, ldx, w, y, ldy, yt, ws, s);
+        case 5: return tc::run_bits<5>(x, M, ldx, w, y, ldy, yt, ws, s);
+        default: return tc::run_bits<6>(x, M, ldx, w, y, ldy, yt, ws, s);
+    }
 }
 
 }  // namespace qg

@@ -40,10 +40,11 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Bounded wait for the phase with parity `parity`; false if it gave up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+// Wait of at most `limit` polls for the phase with parity `parity`; false if
+// it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t limit)
 {
-    for (uint32_t it = 0; it < kSpinLimit; it++) {
+    for (uint32_t it = 0; it < limit; it++) {
         uint32_t ok;
         asm volatile(
             "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
@@ -54,6 +55,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     }
     return false;
 }
+
+// Bounded wait (kSpinLimit polls: seconds); false if it gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) { return mbar_wait_bounded(bar, parity, kSpinLimit); }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar)
 {

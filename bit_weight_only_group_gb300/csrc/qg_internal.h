@@ -48,6 +48,8 @@ qg_status launch_gemv(const uint16_t* x, int M, int ldx, const qg_qweight& w, vo
 // (optionally cleared).
 int* device_status_ptr();
 qg_status read_device_status(int* out, int reset);
+// A kernel whose one mbarrier wait (limit polls) must give up (QG_ERR_TIMEOUT).
+qg_status launch_wait_selftest(uint32_t limit, cudaStream_t s);
 
 // Up to kMultiMax products sharing x (same M, K, bits, group) in one decode launch.
 constexpr int kMultiMax = 4;

@@ -1,5 +1,6 @@
-// Dequantization helpers shared by the tensor-core kernels (4-bit codes to
-// the fp16 operand they stage in shared memory).
+// Dequantization helpers shared by the tensor-core kernels: packed codes to
+// the fp16 operand they stage in shared memory, and the per-row power-of-two
+// exponent that keeps that operand finite.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -36,8 +37,88 @@ __device__ __forceinline__ uint4 deq8_u4(uint32_t v, uint32_t add_lo, uint32_t a
                       hmul2_u32(gemv::hfma2_u32(r2, one, add_lo), s2), hmul2_u32(gemv::hfma2_u32(r3, sixteenth, add_hi), s2));
 }
 
-// position of k (mod 8) inside a permuted block of 8: inverse of (0,4,1,5,2,6,3,7)
-__device__ __forceinline__ int perm8_pos(int k) { return ((k & 3) << 1) | ((k >> 2) & 1); }
+// Named barrier over the 512 threads of the dequantization warps (warps
+// 0 .. 15) of the tensor-core kernels; the producer and MMA warps do not take
+// part.
+__device__ __forceinline__ void deq_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+
+// Position of code c (0..31) of a thread's 32-code chunk in the fp16 operand
+// the tensor-core kernels write: pair plan entry e puts its codes lo and hi at
+// positions 2e and 2e + 1 (the x operand is permuted the same way).
+template <int BITS>
+__device__ __forceinline__ int chunk_pos(int c)
+{
+    int p = 0;
+#pragma unroll
+    for (int e = 0; e < 16; e++) {
+        constexpr int NC = 32;
+        const gemv::PairE q = gemv::plan_entry(BITS, NC, e);
+        p = q.lo == c ? 2 * e : q.hi == c ? 2 * e + 1 : p;
+    }
+    return p;
+}
+
+// Exponent e >= 0 of one weight row such that every operand value of the
+// row, (q - zp) * scale * 2^-e, stays inside fp16's finite range: |q - zp|
+// is at most 2^bits - 1, so the bound is the row's largest scale times that.
+// (A 4-bit group over [0, 65504] has scale 4368, and 15 * 4368 = 65520
+// rounds to infinity in fp16.)  The operand is built with the scale times
+// 2^-e (exact) and the row's accumulator is multiplied by 2^e (exact) when
+// it is stored.  The two threads of a row (lanes 2i and 2i + 1 of a warp
+// whose lanes all call this) each scan half of the row's groups.
+template <int BITS>
+__device__ __forceinline__ int row_exponent(const uint16_t* srow, int ng, int hk)
+{
+    uint32_t m = 0;
+    if (ng % 8 == 0 && (reinterpret_cast<uintptr_t>(srow) & 15u) == 0) {
+        for (int c = hk; c < ng / 8; c += 2) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(srow) + c);
+            m = __vmaxu2(m, v.x & 0x7FFF7FFFu);
+            m = __vmaxu2(m, v.y & 0x7FFF7FFFu);
+            m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
+            m = __vmaxu2(m, v.w & 0x7FFF7FFFu);
+        }
+    } else {
+        for (int g = hk; g < ng; g += 2) m = max(m, (uint32_t)(__ldg(srow + g) & 0x7FFFu));
+    }
+    m = max(m & 0xFFFFu, m >> 16);
+    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    float b = __half2float(__ushort_as_half((uint16_t)m)) * (float)((1 << BITS) - 1);
+    int e = 0;
+    while (b > 65504.0f && e < 30) {
+        b *= 0.5f;
+        ++e;
+    }
+    return e;
+}
+
+// fp16 value h times 2^-e (exact while the result stays a normal number).
+__device__ __forceinline__ uint32_t f16_times_pow2(uint32_t h, int e)
+{
+    if (!e) return h & 0xFFFFu;
+    const float v = __half2float(__ushort_as_half((uint16_t)h)) * __int_as_float((127 - e) << 23);
+    return __half_as_ushort(__float2half_rn(v));
+}
+
+// fp16 value of a + b, with a result beyond fp16's range held at +-65504
+// (the 2-bit operand at an outlier: codebook entry plus stored residual,
+// whose exact sum is the weight, at most half an fp16 step past 65504).
+__device__ __forceinline__ uint16_t f16_add_sat(uint16_t a, uint16_t b, int e)
+{
+    float v = (__half2float(__ushort_as_half(a)) + __half2float(__ushort_as_half(b))) * __int_as_float((127 - e) << 23);
+    v = fminf(fmaxf(v, -65504.0f), 65504.0f);
+    return __half_as_ushort(__float2half_rn(v));
+}
+
+// 2-bit codebook lookup of the operand pair of plan entry 2s + H (H = 0: the
+// codes in bytes 0 and 1 of f, H = 1: bytes 2 and 3), f = four 2-bit codes,
+// one per byte; L / H hold the low / high bytes of the group's 4 entries.
+template <int HALF>
+__device__ __forceinline__ uint32_t cb_pair(uint32_t f, uint32_t lo, uint32_t hi)
+{
+    const uint32_t sel = HALF ? __umulhi(f, 0x00110000u) + 0x4040u : f * 0x11u + 0x4040u;
+    return __byte_perm(lo, hi, sel);
+}
 
 }  // namespace tc
 }  // namespace qg

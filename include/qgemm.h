@@ -270,6 +270,18 @@ QG_API qg_status qgemm_moe_grouped_multi(const uint16_t* x, int32_t T, const int
  * is NULL and QG_ERR_CUDA if the device cannot be read. */
 QG_API qg_status qgemm_device_status(int32_t* status, int32_t reset);
 
+/* Self-check of the failure path of the bounded waits: launches one small
+ * kernel on `stream` whose single mbarrier wait (at most poll_limit polls,
+ * each suspending up to 0.1 ms) has nothing to wait for and gives up, so the
+ * kernel sets the status word to QG_ERR_TIMEOUT and returns, exactly as a
+ * tensor-core kernel does when one of its waits runs out.  It issues no TMA
+ * and no MMA.  Read the result with qgemm_device_status (which also clears
+ * it).  The pages define no such call; it exists so that this path can be
+ * exercised without breaking a product kernel.
+ *   poll_limit  1 .. 64.
+ * Errors: QG_ERR_INVALID_ARG, QG_ERR_CUDA. */
+QG_API qg_status qgemm_selftest_bounded_wait(int32_t poll_limit, void* stream);
+
 /* Message describing the calling thread's most recent failure ("" if none). */
 QG_API const char* qgemm_last_error(void);
 

@@ -120,6 +120,41 @@ def test_tensor_core_path_against_oracle(qg, group, M, N, K):
     assert torch.equal(yb, y.to(torch.bfloat16))
 
 
+@pytest.mark.parametrize("bits", [2, 3, 5, 6])
+@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("M,N,K", [(300, 600, 1024), (129, 200, 384)])
+def test_tensor_core_path_every_width(qg, bits, group, M, N, K):
+    # 2/3/5/6-bit weights above the decode range: the tcgen05 kernel with the
+    # codes read by the dequantization threads and unpacked by the width's
+    # pair plan (x permuted to match), FP16 outliers patched into the operand
+    q, wmax = _weights(N, K, bits, group, 0.003, seed=M + N + bits)
+    x = wl.gen_x(M, K, seed=M + bits)
+    qd = to_device(q)
+    y = qg.qgemm_forward(x.cuda(), qd)
+    torch.cuda.synchronize()
+    check_product(y, oracle.linear(x, q), x, wmax)
+    for _ in range(3):   # fixed accumulation order: repeated calls agree bit for bit
+        assert torch.equal(qg.qgemm_forward(x.cuda(), qd), y)
+
+
+@pytest.mark.parametrize("bits", [2, 5])
+def test_tensor_core_path_every_width_full_size_sampled(qg, bits):
+    # 11008 x 4096 at M = 2048 (the mixed-width sweep's larger shape at the
+    # prefill length); no outliers, so the oracle quantizes only the sampled
+    # rows of the seeded W while the device quantizes all of it
+    M, N, K = 2048, 11008, 4096
+    W = wl.gen_weight(N, K, seed=77 + bits)
+    qw = qg.qpack_quantize(W.cuda(), bits, 128, 0.0)
+    x = wl.gen_x(M, K, seed=78)
+    y = qg.qgemm_forward(x.cuda(), qw)
+    torch.cuda.synchronize()
+    toks = torch.arange(0, M, 89)
+    for n0 in (0, 5504 - 32, N - 64):
+        q = oracle.quantize(W[n0:n0 + 64], bits, 128, 0.0)
+        wmax = float(np.abs(oracle.dequant(q)).max())
+        check_product(y[toks.cuda(), n0:n0 + 64], oracle.linear(x[toks], q), x[toks], wmax)
+
+
 def test_device_status_stays_clear(qg):
     # the tensor-core kernel's bounded waits never give up on valid inputs:
     # after products of both groups the status word is still QG_OK
@@ -130,6 +165,23 @@ def test_device_status_stays_clear(qg):
         y = qg.qgemm_forward(x.cuda(), to_device(q))
         torch.cuda.synchronize()
         check_product(y, oracle.linear(x, q), x, wmax)
+    assert qg.qgemm_device_status() == 0
+
+
+def test_bounded_wait_gives_up_and_reports_timeout(qg):
+    # a kernel waits on an mbarrier that nothing arrives on, with a poll
+    # limit of 2: the wait runs out, the status word reads QG_ERR_TIMEOUT,
+    # reading it with reset clears it, and the context stays usable
+    assert qg.qgemm_device_status(reset=True) in (0, -6)
+    qg.qgemm_selftest_bounded_wait(2)
+    torch.cuda.synchronize()
+    assert qg.qgemm_device_status(reset=True) == -6
+    assert qg.qgemm_device_status() == 0
+    q, wmax = _weights(256, 512, 4, 128, 0.0, seed=3)
+    x = wl.gen_x(300, 512)
+    y = qg.qgemm_forward(x.cuda(), to_device(q))
+    torch.cuda.synchronize()
+    check_product(y, oracle.linear(x, q), x, wmax)
     assert qg.qgemm_device_status() == 0
 
 
@@ -201,3 +253,18 @@ def test_decode_full_size_sampled(qg):
             q = oracle.quantize(Ws[p][n0:n0 + 64], 4, 128, 0.0)
             wmax = float(np.abs(oracle.dequant(q)).max())
             check_product(ys[p][:, n0:n0 + 64], oracle.linear(x, q), x, wmax)
+
+
+@pytest.mark.parametrize("M", [1, 16, 64])
+def test_decode_long_k_with_outliers(qg, M):
+    # the down projection's K = 28672 with 0.1 % outliers, quantized whole by
+    # the oracle: about 29 outliers per row, so the decode kernel's outlier
+    # cursor refills many times across the cluster's ranks
+    N, K, frac = 256, 28672, 0.001
+    q, wmax = _weights(N, K, 4, 128, frac, seed=901)
+    per_row = np.diff(q.row_ptr)
+    assert per_row.mean() > 20 and per_row.max() > 40
+    x = wl.gen_x(M, K, seed=902)
+    y = qg.qgemm_forward(x.cuda(), to_device(q))
+    torch.cuda.synchronize()
+    check_product(y, oracle.linear(x, q), x, wmax)

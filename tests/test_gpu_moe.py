@@ -121,3 +121,19 @@ def test_moe_multi_against_oracle(qg, bits, group, E, T):
         torch.cuda.synchronize()
         assert torch.equal(sa, ya) and torch.equal(sb, yb)
     assert qg.qgemm_device_status() == 0
+
+
+def test_moe_layer_4096_experts_with_outliers(qg):
+    # the MoE workload's gate projection (16 experts of 3072 x 4096, INT4
+    # group 128) with 0.1 % FP16 outliers per expert, 256 tokens top-2 Zipf
+    cfg = wl.MoE()
+    qs, wmax = _experts(cfg.n_experts, cfg.ffn, cfg.hidden, 4, 128, 0.001, seed=600)
+    x = wl.gen_x(cfg.tokens, cfg.hidden, seed=601)
+    topk = wl.gen_topk(cfg.tokens, cfg.top_k, cfg.n_experts)
+    y = qg.qgemm_moe_grouped(x.cuda(), topk.cuda(), [to_device(q) for q in qs])
+    torch.cuda.synchronize()
+    pairs = torch.arange(0, cfg.tokens * cfg.top_k, 7)
+    tok, slot = pairs // cfg.top_k, pairs % cfg.top_k
+    ref = oracle.moe(x[tok], topk[tok].numpy(), qs)          # [n, k, N]
+    got = y[tok.cuda(), slot.cuda()]
+    check_product(got, ref[np.arange(len(pairs)), slot.numpy()], x[tok], wmax)

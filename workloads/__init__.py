@@ -17,7 +17,7 @@ Shapes and widths come from the pages this project follows:
   popularity ("On-device MoE" page, sections 1-2).
 
 Value distributions: weights ~ N(0, 0.02) drawn in fp32 and cast to fp16;
-planted outliers of magnitude U(3, 6) with a random sign (the 5414039 page,
+planted outliers of magnitude U(3, 6) with a random sign (the "70B on one GPU" page,
 section 2, reports outliers above 3.0 on a distribution concentrated near 0);
 activations ~ N(0, 1) drawn in fp32 and cast to bf16.
 """
@@ -170,6 +170,31 @@ def gen_weight(N: int, K: int, seed: int = SEED_W, std: float = 0.02,
         mag = torch.rand((n_out,), generator=go, device=device).mul_(3.0).add_(3.0)
         sgn = torch.randint(0, 2, (n_out,), generator=go, device=device).float().mul_(2.0).sub_(1.0)
         w.view(-1)[pos] = mag * sgn
+    return w.to(torch.float16)
+
+
+def gen_extreme_weight(N: int, K: int, group: int, seed: int = SEED_W) -> torch.Tensor:
+    """W [N, K] fp16 ~ N(0, 0.02) whose first rows hold groups at the edges of
+    fp16's range, in group 0 of each row:
+
+    row 0: a ramp over [0, 65504]; row 1: alternating +-65504;
+    row 2: a ramp over [-2256, 65504] (a range whose 4-bit scale puts the top
+    grid point past 65504); row 3: one value 65504 among zeros;
+    row 4: all zero; row 5: all -1.0 (one-signed); row 6: a ramp over
+    [-65504, 0]; row 7: 6.0e4 and -6.0e4 at both ends of a small group.
+    The other groups and rows stay ~ N(0, 0.02).  N >= 8, K >= group.
+    """
+    w = gen_weight(N, K, seed=seed).float()
+    g = group
+    w[0, :g] = torch.linspace(0.0, 65504.0, g)
+    w[1, :g] = torch.tensor([65504.0, -65504.0]).repeat(g // 2)
+    w[2, :g] = torch.linspace(-2256.0, 65504.0, g)
+    w[3, :g] = 0.0
+    w[3, g // 3] = 65504.0
+    w[4, :] = 0.0
+    w[5, :] = -1.0
+    w[6, :g] = torch.linspace(-65504.0, 0.0, g)
+    w[7, 0], w[7, g - 1] = 6.0e4, -6.0e4
     return w.to(torch.float16)
 
 
