@@ -5,17 +5,21 @@ replicas under torchrun).
 Headline (``value``): decode qGEMV weight throughput at M = 1 over the
 70B-shaped stack -- 80 layers x (q, k, v, o, gate, up, down), INT4 group 128
 with 0.1 % FP16 outliers, 36 GB of quantized weights resident in HBM.  One
-step = the 560 products of one token (q/k/v and gate/up as fused calls: 320
-launches),
-captured once in a CUDA graph and replayed.  The unit is GB/s of packed-weight bytes (codes only); the
+token = the 560 products of the stack (q/k/v and gate/up as fused calls: 320
+launches), captured once in a CUDA graph; a step is ``tokens_per_step``
+consecutive tokens (graph replays), chosen so that the timed region lasts at
+least two seconds.  The unit is GB/s of packed-weight bytes (codes only); the
 all-bytes figure (codes + scales + zero-points + outlier CSR + x + y) is the
 roofline's ``achieved``.
 
-Secondary lines in the same JSON object: prefill qGEMM TFLOP/s at M = 2048 on
-one layer of the same stack, the MoE layer (16 experts, 256 tokens, top-2
-Zipf routing) through the grouped entry point, one decode step of the
-7B-shaped stack with per-layer widths 2/3/5/6, and the device quantizer
-(offline) on one 28672 x 8192 matrix.
+Secondary objects in the same JSON line, each with the clock record of its
+own timed region: the same stack at M = 16 and 64; prefill qGEMM TFLOP/s at
+M = 2048 on one layer of the stack and on 11008 x 4096 products at widths
+2/3/4/5/6; the MoE layer (16 experts, 256 tokens, top-2 Zipf routing); the
+single 4096 x 4096 INT4 layer and the mixed-width sweep (2/3/5/6 bits,
+groups 64/128) at M = 1, 8, 32; the 7B-shaped mixed-width stack at M = 1, 8,
+32; the device quantizer; and two CPU figures: the oracle (``cpu_baseline``)
+and the fused multi-threaded CPU qGEMV (``cpu_fused_baseline``).
 
 ``--impl reference`` times the CPU oracle (plain C, fp64) on the host cores
 on a bounded sample of the same workload.
@@ -27,6 +31,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -53,9 +58,10 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--layers", type=int, default=80, help="layers of the 70B-shaped stack")
     ap.add_argument("--no-secondary", action="store_true", help="skip the prefill and MoE lines")
-    ap.add_argument("--mode", choices=("all", "prefill", "moe", "widths"), default="all",
-                    help="'prefill' / 'moe' / 'widths': run only that measurement and print its object "
-                         "(profiling runs; 'widths' = the mixed-width sweep and the 7B-shaped stack, M=1)")
+    ap.add_argument("--mode", choices=("all", "decode", "prefill", "moe", "widths"), default="all",
+                    help="run only that measurement and print its object (profiling runs): 'decode' = the "
+                         "headline alone; 'prefill' = the 70B layer and the width sweep at M=2048; 'widths' = "
+                         "the single layer, the mixed-width sweep and the 7B-shaped stack at M=1, 8, 32")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
     return ap.parse_args()
 
@@ -126,14 +132,15 @@ def sum_over_ranks(v: float, world: int) -> float:
 
 # ---------------------------------------------------------------- clocks
 class Clocks:
-    """nvidia-smi sampled every 200 ms; only samples whose timestamp falls in
-    the timed region are kept."""
+    """nvidia-smi sampled every 200 ms for the whole run; each timed region
+    reads the samples whose timestamp falls inside it (window)."""
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self):
         self.proc = None
+        self.rows = None
         try:
             self.dev = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
         except Exception:
@@ -148,18 +155,12 @@ class Clocks:
                                           "-lms", "200", "-i", self.dev], stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+        return self
 
-    def stop(self, t0: float, t1: float):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.fh.close()
-        rows = []
+    def _read(self):
         import datetime
+        rows = []
+        self.fh.flush()
         for line in open(self.path):
             f = [c.strip() for c in line.split(",")]
             if len(f) < 9:
@@ -169,9 +170,15 @@ class Clocks:
                 sm = float(f[1])
             except ValueError:
                 continue
-            if t0 <= ts <= t1:
-                rows.append((sm, f))
-        os.unlink(self.path)
+            rows.append((ts, sm, f))
+        return rows
+
+    def window(self, t0: float, t1: float):
+        """Clock record of the timed region [t0, t1] (wall-clock seconds)."""
+        if self.proc is None:
+            return None
+        time.sleep(0.25)   # the sample that closes the region
+        rows = [(sm, f) for ts, sm, f in self._read() if t0 <= ts <= t1]
         if not rows:
             return {"sm_mhz": None, "samples": 0, "reasons": [], "note": "no nvidia-smi sample inside the timed region"}
         reasons = set()
@@ -182,6 +189,25 @@ class Clocks:
         pw = [float(f[3]) for _, f in rows if f[3].replace(".", "").isdigit()]
         return {"sm_mhz": statistics.median(sm for sm, _ in rows), "sm_max_mhz": float(rows[0][1][2]),
                 "samples": len(rows), "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons)}
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        os.unlink(self.path)
+        self.proc = None
+
+
+CLK = None   # the run's sampler (rank 0 of each process: every process samples its own GPU)
+
+
+def region_clocks(t0, t1):
+    return CLK.window(t0, t1) if CLK is not None else None
 
 
 # ---------------------------------------------------------------- our arm
@@ -233,27 +259,77 @@ def check_graph_covers(g, ys, what):
         raise RuntimeError(f"{what}: the captured step did not compute products {missing[:10]}")
 
 
-def time_graph(g, steps, warmup, world, clocks=False):
-    clk = Clocks() if clocks else None
-    if clk:
-        clk.start()
+def capture(step):
+    """Run step once eagerly (lazy loading outside capture), then capture it."""
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_replays(g, n, warmup=3, world=1, flush=None):
+    """Device time (ms) of n replays of g on the current stream, bracketed by
+    a barrier and a synchronize on both sides, and the wall-clock window of
+    the timed region.  flush: a buffer larger than L2, rewritten before each
+    replay (inside the timed region: its time is measured separately and
+    subtracted by the caller)."""
+    s = torch.cuda.current_stream()
     for _ in range(warmup):
         g.replay()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    s = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.time()
     e0.record(s)
-    for _ in range(steps):
+    for _ in range(n):
+        if flush is not None:
+            flush.fill_(1.0)
         g.replay()
     e1.record(s)
     torch.cuda.synchronize()
     t1 = time.time()
     barrier(world)
-    ms = e0.elapsed_time(e1)
-    return ms, (clk.stop(t0, t1) if clk else None)
+    return e0.elapsed_time(e1), (t0, t1)
+
+
+def reps_for(g, seconds, cap=100000):
+    """Replays of g that take about `seconds` (one timed probe of 3 replays)."""
+    ms, _ = time_replays(g, 3, warmup=1)
+    return int(max(3, min(cap, math.ceil(seconds * 1e3 / max(ms / 3, 1e-3)))))
+
+
+def timed_object(g, seconds=0.5, flush=None):
+    """(ms per replay, replays, clock record) of a secondary measurement whose
+    timed region lasts about `seconds`."""
+    n = reps_for(g, seconds)
+    ms, (t0, t1) = time_replays(g, n, flush=flush)
+    return ms / n, n, region_clocks(t0, t1)
+
+
+def decode_stack_step(qg, layers, qws, xs, ys):
+    """One token (or M tokens) through the stack on one stream: the fused
+    q/k/v projection (one call, one launch), o, the fused gate/up projection,
+    down -- four decode launches per layer; consecutive launches overlap
+    through programmatic dependent launch."""
+    def step():
+        for li in range(0, len(layers), 7):
+            qg.qgemm_forward_multi(xs[li], qws[li:li + 3], outs=ys[li:li + 3])
+            qg.qgemm_forward(xs[li + 3], qws[li + 3], out=ys[li + 3])
+            qg.qgemm_forward_multi(xs[li + 4], qws[li + 4:li + 6], outs=ys[li + 4:li + 6])
+            qg.qgemm_forward(xs[li + 6], qws[li + 6], out=ys[li + 6])
+    return step
+
+
+def stack_inputs(layers, M, dev, seed_off=0):
+    x_hid = wl.gen_x(M, 8192, seed=wl.SEED_X + seed_off, device=dev)
+    x_ffn = wl.gen_x(M, 28672, seed=wl.SEED_X + 1 + seed_off, device=dev)
+    xs = [x_ffn if L.K == 28672 else x_hid for L in layers]
+    ys = [torch.empty((M, L.N), dtype=torch.float32, device=dev) for L in layers]
+    return x_hid, x_ffn, xs, ys
 
 
 def run_decode(qg, args, world, rank, P):
@@ -263,80 +339,85 @@ def run_decode(qg, args, world, rank, P):
     qws = build_stack(qg, layers, dev)
     setup_s = time.time() - t0
     M = 1
-    x_hid = wl.gen_x(M, 8192, device=dev)
-    x_ffn = wl.gen_x(M, 28672, seed=wl.SEED_X + 1, device=dev)
-    xs = [x_ffn if L.K == 28672 else x_hid for L in layers]
-    ys = [torch.empty((M, L.N), dtype=torch.float32, device=dev) for L in layers]
-
-    def step():
-        # one token through the stack, on one stream: the fused q/k/v
-        # projection (one call, one launch), o, the fused gate/up projection
-        # (896 row tiles: two waves at three CTAs per SM), down -- four
-        # decode launches per layer; consecutive launches overlap through
-        # programmatic dependent launch
-        for li in range(0, len(layers), 7):
-            qg.qgemm_forward_multi(xs[li], qws[li:li + 3], outs=ys[li:li + 3])
-            qg.qgemm_forward(xs[li + 3], qws[li + 3], out=ys[li + 3])
-            qg.qgemm_forward_multi(xs[li + 4], qws[li + 4:li + 6], outs=ys[li + 4:li + 6])
-            qg.qgemm_forward(xs[li + 6], qws[li + 6], out=ys[li + 6])
-
-    step()                      # eager once (lazy module/function loading outside capture)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        step()
-    torch.cuda.synchronize()
+    x_hid, x_ffn, xs, ys = stack_inputs(layers, M, dev)
+    g = capture(decode_stack_step(qg, layers, qws, xs, ys))
     check_graph_covers(g, ys, "decode step")
 
-    ms, clocks = time_graph(g, args.steps, args.warmup, world, clocks=True)
+    # tokens per step: enough that the timed region (steps x tokens) lasts >= 2 s
+    tok_ms, _ = time_replays(g, 3, warmup=2)
+    tok_ms /= 3
+    R = max(1, math.ceil(2000.0 / (args.steps * tok_ms)))
+    R = int(max_over_ranks(float(R), world))
+    ms, (c0, c1) = time_replays(g, args.steps * R, warmup=args.warmup * R, world=world)
+    clocks = region_clocks(c0, c1)
     ms_max = max_over_ranks(ms, world)
     packed = sum(layer_bytes(qg, L, M)[0] for L in layers)
     allb = sum(layer_bytes(qg, L, M)[1] for L in layers)
-    per_step_s = ms_max / 1e3 / args.steps
-    value = sum_over_ranks(packed, world) / per_step_s / 1e9
+    per_token_s = ms_max / 1e3 / (args.steps * R)
+    value = sum_over_ranks(packed, world) / per_token_s / 1e9
 
-    # end to end: pinned host x -> device, the captured step, final y -> host
+    # end to end: per token, pinned host x -> device, the captured token, y -> host
     xh_pin = x_hid.cpu().pin_memory()
     xf_pin = x_ffn.cpu().pin_memory()
     y_pin = torch.empty_like(ys[-1], device="cpu").pin_memory()
     s = torch.cuda.current_stream()
-    for _ in range(args.warmup):
+
+    def e2e_token():
         x_hid.copy_(xh_pin, non_blocking=True)
         x_ffn.copy_(xf_pin, non_blocking=True)
         g.replay()
         y_pin.copy_(ys[-1], non_blocking=True)
+    for _ in range(args.warmup * R):
+        e2e_token()
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s)
-    for _ in range(args.steps):
-        x_hid.copy_(xh_pin, non_blocking=True)
-        x_ffn.copy_(xf_pin, non_blocking=True)
-        g.replay()
-        y_pin.copy_(ys[-1], non_blocking=True)
+    for _ in range(args.steps * R):
+        e2e_token()
     e1.record(s)
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    e2e = {"value": sum_over_ranks(packed, world) / (e2e_ms / 1e3 / args.steps) / 1e9, "unit": "GB/s",
-           "h2d_bytes_per_step": xh_pin.numel() * 2 + xf_pin.numel() * 2,
-           "d2h_bytes_per_step": y_pin.numel() * 4,
-           "note": "the step's 320 C-ABI calls (fused q/k/v, o, fused gate/up, down per layer) captured once "
-                   "in a CUDA graph on one stream, replayed per step"}
+    e2e = {"value": sum_over_ranks(packed, world) / (e2e_ms / 1e3 / (args.steps * R)) / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": R * (xh_pin.numel() * 2 + xf_pin.numel() * 2),
+           "d2h_bytes_per_step": R * y_pin.numel() * 4,
+           "note": f"per token: x copied from pinned host memory, the token's 320 C-ABI calls (captured once in "
+                   f"a CUDA graph on one stream), y read back; {R} tokens per step"}
 
-    achieved = allb / per_step_s / 1e9
+    achieved = allb / per_token_s / 1e9
+    traffic = decode_traffic(len(layers) // 7)
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": P["hbm"], "unit": "GB/s",
-            "frac": round(achieved / P["hbm"], 4), "traffic": decode_traffic(len(layers) // 7),
-            "traffic_unit": "bytes per step (the achieved figure is per step: the step is 320 launches of this kernel)",
+            "frac": round(achieved / P["hbm"], 4), "traffic": None if traffic is None else traffic * R,
+            "traffic_unit": "bytes per step (R tokens; the achieved figure is per step as well: every launch "
+                            "of the step is this kernel)",
             "kernel": "k_gemv<4,128,1> / k_gemv_multi<4,128,1> (decode qGEMV, the only kernel of the step)",
             "peak_source": P["src"] + " hbm_gbs"}
-    out = dict(value=value, ms_per_step=ms_max / args.steps, roofline=roof, e2e=e2e, clocks=clocks,
-               gpu_launches=(len(layers) // 7) * 4 * args.steps, setup_s=round(setup_s, 1),
-               weights_GB=round(sum(q.nbytes() for q in qws) / 1e9, 3), all_bytes_GBps=round(achieved, 1),
-               frac_of_nominal_8TBs=round(value / 8000.0, 4))
-    del qws, g
-    torch.cuda.empty_cache()
-    return out
+    out = dict(value=value, ms_per_step=ms_max / args.steps, tokens_per_step=R, ms_per_token=ms_max / (args.steps * R),
+               roofline=roof, e2e=e2e, clocks=clocks, gpu_launches=(len(layers) // 7) * 4 * args.steps * R,
+               setup_s=round(setup_s, 1), weights_GB=round(sum(q.nbytes() for q in qws) / 1e9, 3),
+               all_bytes_GBps=round(achieved, 1), frac_of_nominal_8TBs=round(value / 8000.0, 4),
+               bytes_per_token=allb, packed_bytes_per_token=packed)
+    del g
+    return out, qws
+
+
+def run_decode_m(qg, qws, layers, M, P):
+    """The 70B-shaped stack at M tokens per product (the decode configs at
+    M = 16 and 64): weights already resident, one graph of the 320 launches."""
+    dev = torch.device("cuda")
+    _, _, xs, ys = stack_inputs(layers, M, dev, seed_off=10 + M)
+    g = capture(decode_stack_step(qg, layers, qws, xs, ys))
+    check_graph_covers(g, ys, f"decode step M={M}")
+    ms, n, clocks = timed_object(g, 0.6)
+    packed = sum(layer_bytes(qg, L, M)[0] for L in layers)
+    allb = sum(layer_bytes(qg, L, M)[1] for L in layers)
+    del g
+    return {"metric": f"decode qGEMV weight GB/s at M={M}", "value": round(packed / ms / 1e6, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "all_GBps": round(allb / ms / 1e6, 1),
+            "frac_of_hbm_peak": round(allb / ms / 1e6 / P["hbm"], 4), "replays": n, "clocks": clocks,
+            "config": f"70B-shaped stack, {len(layers) // 7} layers, INT4 g128, 0.1% outliers, M={M}; 320 launches "
+                      "per step (fused q/k/v, o, fused gate/up, down)"}
 
 
 def run_prefill(qg, args, P):
@@ -345,10 +426,7 @@ def run_prefill(qg, args, P):
     dev = torch.device("cuda")
     qws = build_stack(qg, layers, dev)
     M = wl.STACK_70B_PREFILL_M
-    x_hid = wl.gen_x(M, 8192, device=dev)
-    x_ffn = wl.gen_x(M, 28672, seed=wl.SEED_X + 1, device=dev)
-    xs = [x_ffn if L.K == 28672 else x_hid for L in layers]
-    ys = [torch.empty((M, L.N), dtype=torch.float32, device=dev) for L in layers]
+    x_hid, x_ffn, xs, ys = stack_inputs(layers, M, dev)
     wsb = max(qg.qgemm_workspace_size(M, q) for q in qws)
     # one workspace per concurrent product (each holds its fp16 copy of x)
     wss = [torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev) for _ in range(3)]
@@ -385,22 +463,49 @@ def run_prefill(qg, args, P):
         main.wait_event(e)
         run(6, wss[0])
 
-    step()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        step()
-    torch.cuda.synchronize()
+    g = capture(step)
     check_graph_covers(g, ys, "prefill step")
-    steps = max(3, min(20, args.steps // 10))
-    ms, _ = time_graph(g, steps, 3, 1)
+    ms, n, clocks = timed_object(g, 0.6)
     flops = sum(2.0 * M * L.N * L.K for L in layers)
-    tflops = flops / (ms / 1e3 / steps) / 1e12
+    tflops = flops / (ms / 1e3) / 1e12
     del qws, g
     torch.cuda.empty_cache()
     return {"metric": "qGEMM TFLOP/s at M=2048", "value": round(tflops, 1), "unit": "TFLOP/s",
-            "ms_per_step": ms / steps, "config": "one 70B-shaped layer (7 products; q/k/v and gate/up as parallel graph branches), INT4 g128, 0.1% outliers",
-            "frac_of_bf16_peak": round(tflops / P["bf16"], 4)}
+            "ms_per_step": round(ms, 4), "replays": n, "clocks": clocks,
+            "config": "one 70B-shaped layer (7 products; q/k/v and gate/up as parallel graph branches), INT4 g128, "
+                      "0.1% outliers, M=2048",
+            "frac_of_bf16_peak": round(tflops / P["bf16"], 4),
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": P["bf16"], "unit": "TFLOP/s",
+                         "frac": round(tflops / P["bf16"], 4), "traffic": None,
+                         "kernel": "k_gemm_tc<4,128> (tcgen05, TMEM accumulators)",
+                         "peak_source": P["src"] + " bf16_tflops (burst: fp16 and bf16 share the tensor rate)"}}
+
+
+def run_prefill_widths(qg, P):
+    """11008 x 4096 products at M = 2048 for every width (group 128, 0.1 %
+    outliers): the tensor-core kernel, TFLOP/s."""
+    dev = torch.device("cuda")
+    M, N, K = wl.STACK_70B_PREFILL_M, 11008, 4096
+    W = wl.gen_weight(N, K, outlier_frac=0.001, device=dev, distinct_positions=False)
+    x = wl.gen_x(M, K, device=dev)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    out = {}
+    t_all0 = time.time()
+    for bits in (2, 3, 4, 5, 6):
+        q = qg.qpack_quantize(W, bits, 128, 0.001)
+        ws = torch.empty(qg.qgemm_workspace_size(M, q), dtype=torch.uint8, device=dev)
+        g = capture(lambda: qg.qgemm_forward(x, q, out=y, workspace=ws))
+        ms, n, clocks = timed_object(g, 0.4)
+        tf = 2.0 * M * N * K / (ms / 1e3) / 1e12
+        out[f"w{bits}"] = {"TFLOP_s": round(tf, 1), "frac_of_bf16_peak": round(tf / P["bf16"], 4),
+                           "us": round(ms * 1e3, 1), "replays": n, "clocks": clocks}
+        del g, q, ws
+    del W
+    torch.cuda.empty_cache()
+    return {"metric": "qGEMM TFLOP/s at M=2048 by width", "unit": "TFLOP/s", "by_width": out,
+            "config": "W 11008x4096 ~N(0,0.02) + 0.1% outliers, group 128, x bf16 [2048, 4096], y fp32; "
+                      "one product per replay (k_x_to_f16 + k_gemm_tc<bits,128>)",
+            "seconds": round(time.time() - t_all0, 1)}
 
 
 def run_moe(qg, args):
@@ -428,91 +533,97 @@ def run_moe(qg, args):
                                    workspace=ws)
         qg.qgemm_moe_grouped(xd, topk, experts["down"], out=ys["down"], workspace=ws)
 
-    step()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        step()
-    torch.cuda.synchronize()
+    g = capture(step)
     check_graph_covers(g, list(ys.values()), "MoE step")
-    steps = max(5, min(50, args.steps))
-    # the layer's weights fit in L2; write a buffer larger than L2 between steps
+    # the layer's weights fit in L2: a buffer larger than L2 is rewritten before
+    # each replay; its own time (measured alone) is subtracted
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    s = torch.cuda.current_stream()
-    for _ in range(3):
-        g.replay()
-    torch.cuda.synchronize()
-    tot = 0.0
-    for _ in range(steps):
-        flush.fill_(1.0)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s)
-        g.replay()
-        e1.record(s)
-        torch.cuda.synchronize()
-        tot += e0.elapsed_time(e1)
-    ms = tot / steps
+    gf = capture(lambda: flush.fill_(1.0))
+    n = reps_for(g, 0.5, cap=2000)
+    ms_both, (t0, t1) = time_replays(g, n, flush=flush)
+    ms_flush, _ = time_replays(gf, n)
+    ms = (ms_both - ms_flush) / n
+    clocks = region_clocks(t0, t1)
     touched = torch.unique(topk).numel()
     used = sorted(set(topk.flatten().tolist()))
-    wbytes = sum(experts[n][e].nbytes() for n, _, _ in projs for e in used)
+    wbytes = sum(experts[n_][e].nbytes() for n_, _, _ in projs for e in used)
     flops = sum(2.0 * cfg.tokens * cfg.top_k * N * K for _, N, K in projs)
     return {"metric": "MoE grouped qGEMM", "value": round(wbytes / (ms / 1e3) / 1e9, 1), "unit": "GB/s",
-            "tflops": round(flops / (ms / 1e3) / 1e12, 2), "ms_per_step": ms, "experts_touched": touched,
+            "tflops": round(flops / (ms / 1e3) / 1e12, 2), "ms_per_step": round(ms, 4), "experts_touched": touched,
+            "replays": n, "clocks": clocks,
             "config": "16 experts gate/up 3072x4096 + down 4096x3072, INT4 g128, 256 tokens top-2 Zipf(1.1); "
                       "gate and up in one call over one routing",
-            "l2": "L2 flushed (512 MB write) before each step"}
+            "l2": "a 512 MB buffer rewritten before each replay (L2 flushed); its time, measured alone, subtracted"}
 
 
-def time_graph_once(step, reps):
-    """Capture step in a CUDA graph and return its mean replay time in ms."""
-    step()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        step()
-    for _ in range(3):
-        g.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / reps
-
-
-def run_widths(qg, args, P):
-    """Decode (M=1) over the single 4096x4096 INT4 layer and the mixed-width
-    sweep -- each layer timed as a graph of copies whose weights exceed L2 --
-    and one step of the 32-layer 7B-shaped stack with per-layer widths."""
-    dev = torch.device("cuda")
+def weight_copies(qg, q, min_bytes=600e6):
+    """q and clones of it, together larger than L2 several times over."""
     clone = lambda t: None if t is None else t.clone()
-    sweep = []
-    for L in [wl.single_layer()] + wl.mixed_sweep():
+    copies = max(4, int(math.ceil(min_bytes / q.nbytes())))
+    return [q] + [qg.QWeight(q.N, q.K, q.bits, q.group, q.packed.clone(), clone(q.scale), clone(q.zp),
+                             clone(q.codebook), q.row_ptr.clone(), q.col.clone(), q.val.clone(), q.nnz)
+                  for _ in range(copies - 1)]
+
+
+def layer_rate(qg, cs, M, P, seconds=0.15):
+    """One decode product per copy in one graph (the copies exceed L2)."""
+    dev = torch.device("cuda")
+    q = cs[0]
+    x = wl.gen_x(M, q.K, seed=wl.SEED_X + M, device=dev)
+    y = torch.empty((M, q.N), device=dev)
+    g = capture(lambda: [qg.qgemm_forward(x, c, out=y) for c in cs])
+    ms, n, clocks = timed_object(g, seconds)
+    us = ms * 1e3 / len(cs)
+    packed = q.N * q.K * q.bits // 8
+    allb = q.nbytes() + M * q.K * 2 + M * q.N * 4
+    del g
+    return {"M": M, "us": round(us, 2), "packed_GBps": round(packed / us / 1e3, 1),
+            "all_GBps": round(allb / us / 1e3, 1), "frac_of_hbm_peak": round(allb / us / 1e3 / P["hbm"], 4),
+            "clocks": clocks}
+
+
+def run_single_layer(qg, P):
+    """The single 4096 x 4096 INT4 group-128 layer at M = 1 (no outliers): one
+    product per weight copy, 64+ copies in one graph."""
+    dev = torch.device("cuda")
+    L = wl.single_layer()
+    W = wl.gen_weight(L.N, L.K, device=dev)
+    q = qg.qpack_quantize(W, L.bits, L.group, L.frac)
+    cs = weight_copies(qg, q, min_bytes=64 * q.nbytes())
+    r = layer_rate(qg, cs, 1, P, seconds=0.5)
+    del cs, q, W
+    torch.cuda.empty_cache()
+    return {"metric": "decode qGEMV weight GB/s at M=1, single layer", "value": r["packed_GBps"], "unit": "GB/s",
+            "us_per_call": r["us"], "all_GBps": r["all_GBps"], "clocks": r["clocks"],
+            "roofline": {"bound": "hbm", "achieved": r["all_GBps"], "peak": P["hbm"], "unit": "GB/s",
+                         "frac": r["frac_of_hbm_peak"], "traffic": None,
+                         "kernel": "k_gemv<4,128,1>", "peak_source": P["src"] + " hbm_gbs"},
+            "config": "W 4096x4096 ~N(0,0.02), INT4 g128, no outliers, x bf16 [1,4096], y fp32; 64 weight copies "
+                      "(563 MB, above L2) in one graph, one product per copy"}
+
+
+def run_sweep(qg, P):
+    """The mixed-width sweep: 4096x4096 and 11008x4096, widths 2/3/5/6, groups
+    64/128, 0.1 % outliers, M = 1, 8, 32; each product over weight copies
+    larger than L2."""
+    dev = torch.device("cuda")
+    rows = []
+    t0 = time.time()
+    for L in wl.mixed_sweep():
         W = wl.gen_weight(L.N, L.K, outlier_frac=L.frac, device=dev, distinct_positions=False)
         q = qg.qpack_quantize(W, L.bits, L.group, L.frac)
         del W
-        copies = max(4, int(600e6 // q.nbytes()))
-        cs = [q] + [qg.QWeight(q.N, q.K, q.bits, q.group, q.packed.clone(), clone(q.scale), clone(q.zp),
-                               clone(q.codebook), q.row_ptr.clone(), q.col.clone(), q.val.clone(), q.nnz)
-                    for _ in range(copies - 1)]
-        x = wl.gen_x(1, L.K, device=dev)
-        y = torch.empty((1, L.N), device=dev)
-
-        def step():
-            for c in cs:
-                qg.qgemm_forward(x, c, out=y)
-        us = time_graph_once(step, 5) * 1e3 / len(cs)
-        packed = L.N * L.K * L.bits // 8
-        sweep.append({"layer": L.name, "us": round(us, 2), "packed_GBps": round(packed / us / 1e3, 1),
-                      "all_GBps": round(q.nbytes() / us / 1e3, 1)})
+        cs = weight_copies(qg, q)
+        for M in (1, 8, 32):
+            r = layer_rate(qg, cs, M, P)
+            r["layer"] = L.name
+            rows.append(r)
         del cs, q
         torch.cuda.empty_cache()
-    return {"metric": "decode GB/s at M=1 over widths 2/3/5/6", "sweep": sweep, "stack_7b": run_stack7b(qg, P),
-            "config": "mixed-width sweep 4096x4096 and 11008x4096 x widths {2,3,5,6} x groups {64,128}, 0.1% "
-                      "outliers; 7B-shaped stack 32 layers with per-layer widths, group 128",
-            "l2": "graphs of copies larger than L2 (sweep); 3.2 GB per step (stack)"}
+    return {"metric": "decode qGEMV GB/s over widths 2/3/5/6 at M = 1, 8, 32", "unit": "GB/s", "rows": rows,
+            "config": "W 4096x4096 and 11008x4096 ~N(0,0.02) + 0.1% outliers, widths {2 (codebook),3,5,6} x groups "
+                      "{64,128}; x bf16 [M, K]; weight copies above 600 MB per graph",
+            "seconds": round(time.time() - t0, 1)}
 
 
 def run_quantize(qg, P):
@@ -525,30 +636,17 @@ def run_quantize(qg, P):
     W = wl.gen_weight(N, K, outlier_frac=frac, device=dev, distinct_positions=False)
     out = qg.QWeight.empty(N, K, bits, group, frac, dev)
     ws = torch.empty(qg.qpack_workspace_size(N, K), dtype=torch.uint8, device=dev)
-    for _ in range(3):
-        qg.qpack_quantize(W, bits, group, frac, out=out, workspace=ws)
-    torch.cuda.synchronize()
-    reps = 10
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        qg.qpack_quantize(W, bits, group, frac, out=out, workspace=ws)
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
+    g = capture(lambda: qg.qpack_quantize(W, bits, group, frac, out=out, workspace=ws))
+    ms, n, clocks = timed_object(g, 0.4)
     wbytes = N * K * 2
-    del W, out, ws
+    del W, out, ws, g
     torch.cuda.empty_cache()
     return {"metric": "device quantizer (offline)", "value": round(wbytes / ms / 1e6, 1), "unit": "GB/s of fp16 W",
-            "ms_per_matrix": round(ms, 4), "passes_over_W": 5,
+            "ms_per_matrix": round(ms, 4), "passes_over_W": 5, "replays": n, "clocks": clocks,
             "config": "28672x8192 fp16 W, INT4 group 128, 0.1% outliers, outputs and workspace preallocated"}
 
 
-def run_stack7b(qg, P):
-    """One decode step (M=1) of the 32-layer 7B-shaped stack with per-layer
-    widths 2 (codebook) / 3 / 5 / 6, group 128, 0.1 % outliers: 224 products
-    in a CUDA graph, those that share x, width and group (q/k, gate/up) fused
-    into one call."""
+def build_stack7b(qg):
     dev = torch.device("cuda")
     layers = wl.stack_7b()
     qs = []
@@ -556,8 +654,17 @@ def run_stack7b(qg, P):
         W = wl.gen_weight(L.N, L.K, seed=wl.SEED_W + i, outlier_frac=L.frac, device=dev, distinct_positions=False)
         qs.append(qg.qpack_quantize(W, L.bits, L.group, L.frac))
         del W
-    xh, xf = wl.gen_x(1, 4096, device=dev), wl.gen_x(1, 11008, device=dev)
-    ys = [torch.empty((1, L.N), device=dev) for L in layers]
+    return layers, qs
+
+
+def run_stack7b(qg, P, layers, qs, M):
+    """One decode step (M tokens) of the 32-layer 7B-shaped stack with
+    per-layer widths 2 (codebook) / 3 / 5 / 6, group 128, 0.1 % outliers: 224
+    products in a CUDA graph, those that share x, width and group (q/k,
+    gate/up) fused into one call."""
+    dev = torch.device("cuda")
+    xh, xf = wl.gen_x(M, 4096, device=dev), wl.gen_x(M, 11008, device=dev)
+    ys = [torch.empty((M, L.N), device=dev) for L in layers]
     # products that read the same x with the same width and group run as one
     # fused call: q/k(/v) and gate/up of a layer
     calls = []
@@ -572,7 +679,6 @@ def run_stack7b(qg, P):
                     calls.append(run)
                     run = [i]
             calls.append(run)
-    launches = len(calls)
 
     def step7():
         for run in calls:
@@ -581,18 +687,73 @@ def run_stack7b(qg, P):
                 qg.qgemm_forward(x, qs[run[0]], out=ys[run[0]])
             else:
                 qg.qgemm_forward_multi(x, [qs[i] for i in run], outs=[ys[i] for i in run])
-    ms = time_graph_once(step7, 20)
+    g = capture(step7)
+    check_graph_covers(g, ys, f"7B step M={M}")
+    ms, n, clocks = timed_object(g, 0.5)
     packed = sum(L.N * L.K * L.bits // 8 for L in layers)
-    allb = sum(q.nbytes() for q in qs)
-    del qs
-    torch.cuda.empty_cache()
-    return {"metric": "7B-shaped mixed-width stack decode", "value": round(packed / ms / 1e6, 1), "unit": "GB/s",
-            "ms_per_step": round(ms, 4), "all_GBps": round(allb / ms / 1e6, 1),
+    allb = sum(q.nbytes() for q in qs) + sum(M * (L.K * 2 + L.N * 4) for L in layers)
+    del g
+    return {"metric": f"7B-shaped mixed-width stack decode, M={M}", "value": round(packed / ms / 1e6, 1),
+            "unit": "GB/s", "ms_per_step": round(ms, 4), "all_GBps": round(allb / ms / 1e6, 1),
             "frac_of_hbm_peak": round(allb / ms / 1e6 / P["hbm"], 4), "weights_GB": round(allb / 1e9, 3),
-            "launches": launches,
+            "launches": len(calls), "replays": n, "clocks": clocks,
             "config": "32 layers q/k/v/o 4096x4096, gate/up 11008x4096, down 4096x11008; widths 6 (layers 0, 1, "
                       "30, 31), else q/k/o 5, v 6, gate/up 2 (codebook), down 2/3/5; group 128, 0.1% outliers, "
-                      "M=1; products sharing x and width fused per call (q/k, gate/up; q/k/v where all 6-bit)"}
+                      f"M={M}; products sharing x and width fused per call (q/k, gate/up; q/k/v where all 6-bit)"}
+
+
+def run_cpu_fused(qg, seconds, qs7=None, layers7=None):
+    """The fused multi-threaded CPU qGEMV (every host core) at M = 1 on the
+    single 4096 x 4096 layer, on one 4096 x 4096 and one 11008 x 4096 layer of
+    each sweep width (group 128), and on the 7B-shaped stack; the quantized
+    weights are the device quantizer's (bit-identical to the oracle's),
+    copied to host memory."""
+    import cpu_baseline as cb
+    cb.build()
+    dev = torch.device("cuda")
+    cores = cb.cores()
+    out = {}
+
+    def rate(hws, budget):
+        xs = {}
+        for hw in hws:
+            if hw.K not in xs:
+                xs[hw.K] = wl.gen_x(1, hw.K, seed=wl.SEED_X + hw.K).float().numpy().ravel()
+        ys = [np.empty(hw.N, np.float32) for hw in hws]
+        for hw, y in zip(hws, ys):
+            cb.gemv(xs[hw.K], hw, y)
+        t0 = time.time()
+        passes = 0
+        while passes == 0 or time.time() - t0 < budget:
+            for hw, y in zip(hws, ys):
+                cb.gemv(xs[hw.K], hw, y)
+            passes += 1
+        dt = time.time() - t0
+        return sum(hw.nbytes_packed() for hw in hws) * passes / dt / 1e9, passes
+
+    per = seconds / 4
+    L = wl.single_layer()
+    q = qg.qpack_quantize(wl.gen_weight(L.N, L.K, device=dev), L.bits, L.group, L.frac)
+    v, p = rate([cb.HostWeight.from_device(q)], per)
+    out["single_4096_int4_g128"] = {"GBps": round(v, 3), "passes": p}
+    for L in wl.mixed_sweep():
+        if L.group != 128:
+            continue
+        W = wl.gen_weight(L.N, L.K, outlier_frac=L.frac, device=dev, distinct_positions=False)
+        q = qg.qpack_quantize(W, L.bits, L.group, L.frac)
+        v, p = rate([cb.HostWeight.from_device(q)], per / 8)
+        out[f"sweep_{L.name}"] = {"GBps": round(v, 3), "passes": p}
+    if qs7 is not None:
+        hws = [cb.HostWeight.from_device(q) for q in qs7]
+        v, p = rate(hws, per)
+        out["stack_7b"] = {"GBps": round(v, 3), "passes": p}
+    head = out["single_4096_int4_g128"]["GBps"]
+    return {"value": head, "unit": "GB/s", "cores": cores,
+            "kind": "fused CPU qGEMV: unpack + fp32 FMA with the group scale factored out, std::thread row blocks "
+                    "over every hardware thread",
+            "sample": f"M=1, packed-weight GB/s; value = the single 4096x4096 INT4 g128 layer; about {seconds:.0f} s "
+                      "in all",
+            "per_config": out}
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -659,7 +820,15 @@ def run_reference(args, world, rank):
     return 0
 
 
+def secondary(line, key, fn, *a):
+    try:
+        line[key] = fn(*a)
+    except Exception as e:  # report, do not hide
+        line[key] = {"error": repr(e)}
+
+
 def main():
+    global CLK
     args = parse()
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -667,44 +836,64 @@ def main():
     import bit_weight_only_group_gb300 as qg
     qg.lib()
     P = peaks()
-    if args.mode != "all":
-        out = (run_prefill(qg, args, P) if args.mode == "prefill" else
-               run_moe(qg, args) if args.mode == "moe" else run_widths(qg, args, P))
+    CLK = Clocks().start()
+    try:
+        if args.mode != "all":
+            out = {}
+            if args.mode == "prefill":
+                out = run_prefill(qg, args, P)
+                out["widths"] = run_prefill_widths(qg, P)
+            elif args.mode == "moe":
+                out = run_moe(qg, args)
+            elif args.mode == "widths":
+                layers7, qs7 = build_stack7b(qg)
+                out = {"single": run_single_layer(qg, P), "sweep": run_sweep(qg, P),
+                       "stack_7b": [run_stack7b(qg, P, layers7, qs7, M) for M in (1, 8, 32)]}
+            elif args.mode == "decode":
+                dec, qws = run_decode(qg, args, world, rank, P)
+                out = {k: v for k, v in dec.items()}
+                for M in (16, 64):
+                    out[f"m{M}"] = run_decode_m(qg, qws, wl.stack_70b(args.layers), M, P)
+            if rank == 0:
+                print(json.dumps(out))
+            return 0
+        dec, qws = run_decode(qg, args, world, rank, P)
+        line = {"metric": METRIC, "value": round(dec["value"], 1), "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dec["ms_per_step"], 4),
+                "tokens_per_step": dec["tokens_per_step"], "ms_per_token": round(dec["ms_per_token"], 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "int4 weights, fp16 x fp16 MMA, fp32 accumulate", "data": "synthetic",
+                "config": dict(decode_config(args.layers, world), tokens_per_step=dec["tokens_per_step"]),
+                "frac_of_hbm_peak": round(dec["value"] / P["hbm"], 4),
+                "frac_of_nominal_8TBs": dec["frac_of_nominal_8TBs"],
+                "roofline": dec["roofline"], "e2e": dec["e2e"], "clocks": dec["clocks"],
+                "gpu_launches": dec["gpu_launches"], "setup_s": dec["setup_s"]}
+        if not args.no_secondary and rank == 0:
+            layers = wl.stack_70b(args.layers)
+            for M in (16, 64):
+                secondary(line, f"decode_70b_m{M}", run_decode_m, qg, qws, layers, M, P)
+            del qws
+            torch.cuda.empty_cache()
+            secondary(line, "prefill", run_prefill, qg, args, P)
+            secondary(line, "prefill_widths", run_prefill_widths, qg, P)
+            secondary(line, "moe", run_moe, qg, args)
+            layers7, qs7 = build_stack7b(qg)
+            for M, key in ((1, "decode_7b_mixed"), (8, "decode_7b_mixed_m8"), (32, "decode_7b_mixed_m32")):
+                secondary(line, key, run_stack7b, qg, P, layers7, qs7, M)
+            secondary(line, "single_layer", run_single_layer, qg, P)
+            secondary(line, "mixed_sweep", run_sweep, qg, P)
+            secondary(line, "quantize", run_quantize, qg, P)
+            secondary(line, "cpu_fused_baseline", run_cpu_fused, qg, args.cpu_seconds, qs7, layers7)
+            del qs7
+        else:
+            del qws
         if rank == 0:
-            print(json.dumps(out))
-        return 0
-    dec = run_decode(qg, args, world, rank, P)
-    line = {"metric": METRIC, "value": round(dec["value"], 1), "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dec["ms_per_step"], 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "int4 weights, fp16 x fp16 MMA, fp32 accumulate", "data": "synthetic",
-            "config": decode_config(args.layers, world),
-            "frac_of_hbm_peak": round(dec["value"] / P["hbm"], 4),
-            "frac_of_nominal_8TBs": dec["frac_of_nominal_8TBs"],
-            "roofline": dec["roofline"], "e2e": dec["e2e"], "clocks": dec["clocks"],
-            "gpu_launches": dec["gpu_launches"], "setup_s": dec["setup_s"]}
-    if not args.no_secondary and rank == 0:
-        try:
-            line["prefill"] = run_prefill(qg, args, P)
-        except Exception as e:  # report, do not hide
-            line["prefill"] = {"error": repr(e)}
-        try:
-            line["moe"] = run_moe(qg, args)
-        except Exception as e:
-            line["moe"] = {"error": repr(e)}
-        try:
-            line["decode_7b_mixed"] = run_stack7b(qg, P)
-        except Exception as e:
-            line["decode_7b_mixed"] = {"error": repr(e)}
-        try:
-            line["quantize"] = run_quantize(qg, P)
-        except Exception as e:
-            line["quantize"] = {"error": repr(e)}
-    if rank == 0:
-        v, cores, txt = oracle_rate(args.cpu_seconds)
-        line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                "sample": txt}
-        print(json.dumps(line))
+            v, cores, txt = oracle_rate(args.cpu_seconds)
+            line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                    "sample": txt}
+            print(json.dumps(line))
+    finally:
+        CLK.stop()
     barrier(world)
     if world > 1:
         import torch.distributed as dist

@@ -31,11 +31,14 @@ STATUS_NAMES = {0: "QG_OK", -1: "QG_ERR_INVALID_ARG", -2: "QG_ERR_UNSUPPORTED", 
                 -4: "QG_ERR_WORKSPACE", -5: "QG_ERR_CUDA", -6: "QG_ERR_TIMEOUT", -7: "QG_ERR_DEVICE_STATUS"}
 Y_F32, Y_BF16 = 0, 1
 
-ABI_FUNCTIONS = ("qpack_query_sizes", "qpack_workspace_size", "qpack_quantize", "qpack_quantize_noalloc",
+QUANT_MODES = {"asymmetric": 0, "symmetric": 1, "linear2": 2}
+
+ABI_FUNCTIONS = ("qpack_query_sizes", "qpack_workspace_size", "qpack_quantize", "qpack_quantize_mode",
+                 "qpack_quantize_noalloc",
                  "qgemm_workspace_size",
                  "qgemm_forward", "qgemm_forward_multi", "qgemm_moe_workspace_size", "qgemm_moe_grouped",
                  "qgemm_moe_grouped_multi",
-                 "qgemm_device_status", "qgemm_selftest_bounded_wait",
+                 "qgemm_device_status", "qgemm_selftest_bounded_wait", "qdiag_workspace_size", "qdiag_layer",
                  "qgemm_last_error")
 
 
@@ -71,6 +74,7 @@ def lib() -> ctypes.CDLL:
         L.qpack_query_sizes.argtypes = [i32, i32, i32, i32, f32, psz, psz, psz, psz, pi32]
         L.qpack_workspace_size.argtypes = [i32, i32, psz]
         L.qpack_quantize.argtypes = [vp, f32, pq, vp, sz, vp]
+        L.qpack_quantize_mode.argtypes = [vp, f32, ctypes.c_int, pq, vp, sz, vp]
         L.qgemm_workspace_size.argtypes = [i32, pq, psz]
         L.qgemm_forward.argtypes = [vp, i32, i32, pq, vp, i32, ctypes.c_int, vp, sz, vp]
         L.qgemm_moe_workspace_size.argtypes = [i32, i32, i32, pq, psz]
@@ -79,6 +83,8 @@ def lib() -> ctypes.CDLL:
                                               sz, vp]
         L.qgemm_device_status.argtypes = [pi32, i32]
         L.qgemm_selftest_bounded_wait.argtypes = [i32, vp]
+        L.qdiag_workspace_size.argtypes = [i32, i32, i32, psz]
+        L.qdiag_layer.argtypes = [vp, pq, f32, vp, vp, vp, sz, vp]
         L.qgemm_forward_multi.argtypes = [vp, i32, i32, pq, i32, ctypes.POINTER(vp), pi32, ctypes.c_int, vp, sz, vp]
         for name in ABI_FUNCTIONS[:-1]:
             getattr(L, name).restype = ctypes.c_int
@@ -168,8 +174,11 @@ class QWeight:
 
 
 def qpack_quantize(W: torch.Tensor, bits: int, group: int, outlier_frac: float = 0.0,
-                   out: QWeight | None = None, workspace: torch.Tensor | None = None, stream=None) -> QWeight:
-    """Quantize and pack W [N, K] (fp16, CUDA) on the device."""
+                   out: QWeight | None = None, workspace: torch.Tensor | None = None, stream=None,
+                   mode: str = "asymmetric") -> QWeight:
+    """Quantize and pack W [N, K] (fp16, CUDA) on the device.  mode:
+    'asymmetric' (qpack_quantize), 'symmetric' or 'linear2'
+    (qpack_quantize_mode)."""
     if W.dtype != torch.float16 or not W.is_cuda or W.dim() != 2:
         raise ValueError("W must be a 2-D float16 CUDA tensor")
     W = W.contiguous()
@@ -178,8 +187,12 @@ def qpack_quantize(W: torch.Tensor, bits: int, group: int, outlier_frac: float =
     ws_bytes = qpack_workspace_size(N, K)
     ws = workspace if workspace is not None else torch.empty(ws_bytes, dtype=torch.uint8, device=W.device)
     d = qw.desc()
-    _check(lib().qpack_quantize(_ptr(W), outlier_frac, ctypes.byref(d), _ptr(ws), ws.numel(), _stream(stream)),
-           "qpack_quantize")
+    if mode == "asymmetric":
+        _check(lib().qpack_quantize(_ptr(W), outlier_frac, ctypes.byref(d), _ptr(ws), ws.numel(), _stream(stream)),
+               "qpack_quantize")
+    else:
+        _check(lib().qpack_quantize_mode(_ptr(W), outlier_frac, QUANT_MODES[mode], ctypes.byref(d), _ptr(ws),
+                                         ws.numel(), _stream(stream)), "qpack_quantize_mode")
     return qw
 
 
@@ -337,3 +350,33 @@ def qgemm_selftest_bounded_wait(poll_limit: int = 2, stream=None) -> None:
     """Launch the kernel whose bounded mbarrier wait must give up; afterwards
     qgemm_device_status() reads QG_ERR_TIMEOUT (-6)."""
     _check(lib().qgemm_selftest_bounded_wait(poll_limit, _stream(stream)), "qgemm_selftest_bounded_wait")
+
+
+class QgDiag(ctypes.Structure):
+    """Mirror of ``qg_diag`` in include/qgemm.h."""
+    _fields_ = [("max_abs_err", ctypes.c_double), ("rmse", ctypes.c_double), ("cosine", ctypes.c_double),
+                ("max_range_ratio", ctypes.c_double), ("groups_over", ctypes.c_int64)]
+
+
+def qdiag_layer(W: torch.Tensor, qw: QWeight, threshold: float = 8.0, ratio: bool = False, stream=None):
+    """Diagnostics of qw against the original fp16 W [N, K] (CUDA), computed
+    on the device: dict of max_abs_err, rmse, cosine, max_range_ratio,
+    groups_over (and the per-group ratio tensor [N, K/group] if asked).
+    Reading the result synchronizes the stream."""
+    if W.dtype != torch.float16 or not W.is_cuda or tuple(W.shape) != (qw.N, qw.K) or not W.is_contiguous():
+        raise ValueError("W must be the contiguous fp16 CUDA [N, K] matrix of qw")
+    b = ctypes.c_size_t()
+    _check(lib().qdiag_workspace_size(qw.N, qw.K, qw.group, ctypes.byref(b)), "qdiag_workspace_size")
+    ws = torch.empty(max(b.value, 1), dtype=torch.uint8, device=W.device)
+    out = torch.zeros(5, dtype=torch.float64, device=W.device)   # one qg_diag (40 bytes)
+    r = torch.empty((qw.N, qw.K // qw.group), dtype=torch.float32, device=W.device) if ratio else None
+    d = qw.desc()
+    _check(lib().qdiag_layer(_ptr(W), ctypes.byref(d), threshold, _ptr(r), _ptr(out), _ptr(ws), ws.numel(),
+                             _stream(stream)), "qdiag_layer")
+    raw = out.cpu().numpy().tobytes()
+    res = QgDiag.from_buffer_copy(raw)
+    o = dict(max_abs_err=res.max_abs_err, rmse=res.rmse, cosine=res.cosine, max_range_ratio=res.max_range_ratio,
+             groups_over=int(res.groups_over))
+    if ratio:
+        o["ratio"] = r
+    return o

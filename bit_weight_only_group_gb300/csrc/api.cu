@@ -195,6 +195,32 @@ qg_status qgemm_device_status(int32_t* status, int32_t reset)
     return QG_OK;
 }
 
+qg_status qdiag_workspace_size(int32_t N, int32_t K, int32_t group, size_t* bytes)
+{
+    if (!bytes) return fail(QG_ERR_INVALID_ARG, "qdiag_workspace_size: bytes is null");
+    qg_status st = check_shape(N, K, 4, group);
+    if (st != QG_OK) return st;
+    *bytes = diag_workspace_bytes(N, K, group);
+    return QG_OK;
+}
+
+qg_status qdiag_layer(const uint16_t* W, const qg_qweight* w, float threshold, float* group_ratio, qg_diag* out,
+                      void* ws, size_t ws_bytes, void* stream)
+{
+    qg_status st = check_qweight(w, "qdiag_layer");
+    if (st != QG_OK) return st;
+    if (!W || !out) return fail(QG_ERR_INVALID_ARG, "qdiag_layer: W or out is null");
+    if (!aligned(W, 16)) return fail(QG_ERR_ALIGNMENT, "qdiag_layer: W must be 16-byte aligned");
+    if (!aligned(out, 8) || (group_ratio && !aligned(group_ratio, 4)))
+        return fail(QG_ERR_ALIGNMENT, "qdiag_layer: out or group_ratio misaligned");
+    if (!(threshold == threshold)) return fail(QG_ERR_INVALID_ARG, "qdiag_layer: threshold is NaN");
+    const size_t need = diag_workspace_bytes(w->N, w->K, w->group);
+    if (!ws || ws_bytes < need)
+        return fail(QG_ERR_WORKSPACE, "qdiag_layer: workspace %zu bytes < %zu", ws ? ws_bytes : (size_t)0, need);
+    if (!aligned(ws, 256)) return fail(QG_ERR_ALIGNMENT, "qdiag_layer: workspace must be 256-byte aligned");
+    return launch_diag(W, *w, threshold, group_ratio, out, ws, static_cast<cudaStream_t>(stream));
+}
+
 qg_status qgemm_selftest_bounded_wait(int32_t poll_limit, void* stream)
 {
     if (poll_limit < 1 || poll_limit > 64)
@@ -227,6 +253,22 @@ qg_status qpack_workspace_size(int32_t N, int32_t K, size_t* bytes)
     if (N <= 0 || K <= 0) return fail(QG_ERR_INVALID_ARG, "N and K must be positive");
     *bytes = quantize_workspace_bytes(N, K);
     return QG_OK;
+}
+
+qg_status qpack_quantize_mode(const uint16_t* W, float outlier_frac, qg_quant_mode mode, const qg_qweight* out,
+                              void* ws, size_t ws_bytes, void* stream)
+{
+    qg_status st = check_quantize_args(W, outlier_frac, out, "qpack_quantize_mode");
+    if (st != QG_OK) return st;
+    if (mode != QG_QUANT_ASYMMETRIC && mode != QG_QUANT_SYMMETRIC && mode != QG_QUANT_LINEAR2)
+        return fail(QG_ERR_INVALID_ARG, "qpack_quantize_mode: unknown mode %d", (int)mode);
+    if (mode == QG_QUANT_LINEAR2 && out->bits != 2)
+        return fail(QG_ERR_UNSUPPORTED, "qpack_quantize_mode: QG_QUANT_LINEAR2 is a 2-bit format (bits=%d)", out->bits);
+    const size_t need = quantize_workspace_bytes(out->N, out->K);
+    if (!ws || ws_bytes < need)
+        return fail(QG_ERR_WORKSPACE, "qpack_quantize_mode: workspace %zu bytes < %zu", ws ? ws_bytes : (size_t)0, need);
+    if (!aligned(ws, 256)) return fail(QG_ERR_ALIGNMENT, "qpack_quantize_mode: workspace must be 256-byte aligned");
+    return launch_quantize(W, outlier_frac, *out, ws, static_cast<cudaStream_t>(stream), (int)mode);
 }
 
 qg_status qpack_quantize(const uint16_t* W, float outlier_frac, const qg_qweight* out, void* ws,

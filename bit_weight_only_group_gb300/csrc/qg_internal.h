@@ -34,8 +34,9 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // ---------------------------------------------------------------- quantizer
 size_t quantize_workspace_bytes(int N, int K);
+// mode: 0 asymmetric (codebook at 2 bits), 1 symmetric, 2 linear 2-bit (qg_quant_mode)
 qg_status launch_quantize(const uint16_t* W, float frac, const qg_qweight& w, void* ws,
-                          cudaStream_t s);
+                          cudaStream_t s, int mode = 0);
 
 // ---------------------------------------------------------------- decode GEMV
 // Largest M the register-dequant kernel handles in one pass.
@@ -82,5 +83,10 @@ size_t moe_tc_x16_bytes(int P, int K);
 qg_status launch_moe_tc(const uint16_t* x, int T, int k, const qg_qweight* experts, int E, int n, void* const* ys,
                         qg_ydtype yt, const int* offsets, const int* perm, const int2* items, const int* n_items,
                         int max_items, void* x16p, cudaStream_t s);
+
+// ---------------------------------------------------------------- diagnostics
+size_t diag_workspace_bytes(int N, int K, int group);
+qg_status launch_diag(const uint16_t* W, const qg_qweight& w, float threshold, float* ratio, qg_diag* out, void* ws,
+                      cudaStream_t s);
 
 }  // namespace qg

@@ -332,22 +332,13 @@ __device__ __forceinline__ bool is_out(const unsigned (&om)[G / 32], int i)
     return (om[i >> 5] >> (i & 31)) & 1u;
 }
 
+// Affine parameters of a group (range widened to contain 0): fp16 scale
+// rounded up from (max - min) / qmax (1.0 when max == min), zero point
+// clamp(-round(min / scale), 0, qmax).
 template <int G>
-__global__ void k_quant_affine(const unsigned short* __restrict__ W, int N, int K, int bits,
-                               const int* __restrict__ row_ptr, const int* __restrict__ col,
-                               unsigned char* __restrict__ packed, unsigned short* __restrict__ scale,
-                               unsigned char* __restrict__ zp_out)
+__device__ __forceinline__ void affine_params(const unsigned short* __restrict__ src, const unsigned (&om)[G / 32],
+                                              int qmax, unsigned short* s16_out, int* zp_out)
 {
-    const int ng = K / G;
-    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (gid >= (long long)N * ng) return;
-    const int n = (int)(gid / ng), j = (int)(gid % ng);
-    const int k0 = j * G;
-    unsigned om[G / 32];
-    int first;
-    group_outliers<G>(row_ptr, col, n, k0, om, &first);
-    const unsigned short* src = W + (size_t)n * K + k0;
-    const int qmax = (1 << bits) - 1;
     float mn = 0.0f, mx = 0.0f;
     for_group<G>(src, [&](int i, unsigned short h) {
         if (is_out<G>(om, i)) return;
@@ -363,11 +354,58 @@ __global__ void k_quant_affine(const unsigned short* __restrict__ W, int N, int 
         const float s32 = __fdiv_rn(range, (float)qmax);
         s16 = __half_as_ushort(__float2half_ru(s32));
     }
-    const float s = h2f(s16);
-    const float r = rintf(__fdiv_rn(mn, s));
+    const float r = rintf(__fdiv_rn(mn, h2f(s16)));
     int zp = -(int)r;
-    zp = zp < 0 ? 0 : (zp > qmax ? qmax : zp);
+    *zp_out = zp < 0 ? 0 : (zp > qmax ? qmax : zp);
+    *s16_out = s16;
+}
 
+// Largest |w| over the group's non-outliers.
+template <int G>
+__device__ __forceinline__ float group_amax(const unsigned short* __restrict__ src, const unsigned (&om)[G / 32])
+{
+    float amax = 0.0f;
+    for_group<G>(src, [&](int i, unsigned short h) {
+        if (!is_out<G>(om, i)) amax = fmaxf(amax, fabsf(h2f(h)));
+    });
+    return amax;
+}
+
+// Widths 3..6.  sym == 0: asymmetric (scale and zero point from the group's
+// range); sym == 1: symmetric, integer range [-qs, qs] with qs = 2^(b-1) - 1,
+// scale rounded up from amax / qs (1.0 if amax is 0), codes q + 2^(b-1) with
+// the zero point fixed at 2^(b-1).  Outliers take the zero point's code.
+template <int G>
+__global__ void k_quant_affine(const unsigned short* __restrict__ W, int N, int K, int bits, int sym,
+                               const int* __restrict__ row_ptr, const int* __restrict__ col,
+                               unsigned char* __restrict__ packed, unsigned short* __restrict__ scale,
+                               unsigned char* __restrict__ zp_out)
+{
+    const int ng = K / G;
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gid >= (long long)N * ng) return;
+    const int n = (int)(gid / ng), j = (int)(gid % ng);
+    const int k0 = j * G;
+    unsigned om[G / 32];
+    int first;
+    group_outliers<G>(row_ptr, col, n, k0, om, &first);
+    const unsigned short* src = W + (size_t)n * K + k0;
+    const int qmax = (1 << bits) - 1;
+    unsigned short s16;
+    int zp, qlo, qhi;
+    if (sym) {
+        const int qs = (1 << (bits - 1)) - 1;
+        const float amax = group_amax<G>(src, om);
+        s16 = amax == 0.0f ? (unsigned short)0x3C00 : __half_as_ushort(__float2half_ru(__fdiv_rn(amax, (float)qs)));
+        zp = 1 << (bits - 1);
+        qlo = zp - qs;
+        qhi = zp + qs;
+    } else {
+        affine_params<G>(src, om, qmax, &s16, &zp);
+        qlo = 0;
+        qhi = qmax;
+    }
+    const float s = h2f(s16);
     BitWriter bw{reinterpret_cast<unsigned*>(packed + ((size_t)n * K + k0) * bits / 8), 0ull, 0};
     for_group<G>(src, [&](int i, unsigned short h) {
         int q;
@@ -375,12 +413,74 @@ __global__ void k_quant_affine(const unsigned short* __restrict__ W, int N, int 
             q = zp;
         } else {
             q = (int)rintf(__fdiv_rn(h2f(h), s)) + zp;
-            q = q < 0 ? 0 : (q > qmax ? qmax : q);
+            q = q < qlo ? qlo : (q > qhi ? qhi : q);
         }
         bw.put((unsigned)q, bits);
     });
     scale[gid] = s16;
     zp_out[gid] = (unsigned char)zp;
+}
+
+// 2-bit groups on a uniform grid, stored as the four constants a code
+// selects.  mode 1 (symmetric): levels -s, 0, s with s = amax rounded up to
+// fp16 (1.0 if 0), codes round(w / s) clamped to [-1, 1], plus 1; constants
+// (-s, 0, s, s).  mode 2 (linear): the affine grid at 2 bits, constants
+// fp16((i - zp) * scale).  The zero code's constant is exactly 0: outliers
+// take it and keep their own value as the stored residual.
+template <int G>
+__global__ void k_quant_uniform2(const unsigned short* __restrict__ W, int N, int K, int mode,
+                                 const int* __restrict__ row_ptr, const int* __restrict__ col,
+                                 unsigned char* __restrict__ packed, unsigned short* __restrict__ cb,
+                                 unsigned short* __restrict__ val)
+{
+    const int ng = K / G;
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gid >= (long long)N * ng) return;
+    const int n = (int)(gid / ng), j = (int)(gid % ng);
+    const int k0 = j * G;
+    unsigned om[G / 32];
+    int first;
+    group_outliers<G>(row_ptr, col, n, k0, om, &first);
+    const unsigned short* src = W + (size_t)n * K + k0;
+    unsigned short s16;
+    int zp, qlo, qhi;
+    unsigned short e[4];
+    if (mode == 1) {
+        const float amax = group_amax<G>(src, om);
+        s16 = amax == 0.0f ? (unsigned short)0x3C00 : __half_as_ushort(__float2half_ru(amax));
+        zp = 1;
+        qlo = 0;
+        qhi = 2;
+        e[0] = (unsigned short)(s16 | 0x8000u);
+        e[1] = 0;
+        e[2] = s16;
+        e[3] = s16;
+    } else {
+        affine_params<G>(src, om, 3, &s16, &zp);
+        qlo = 0;
+        qhi = 3;
+        const float sf = h2f(s16);
+#pragma unroll
+        for (int i = 0; i < 4; i++) e[i] = __half_as_ushort(__float2half_rn(__fmul_rn((float)(i - zp), sf)));
+    }
+    const float s = h2f(s16);
+    BitWriter bw{reinterpret_cast<unsigned*>(packed + ((size_t)n * K + k0) * 2 / 8), 0ull, 0};
+    int p = first;
+    for_group<G>(src, [&](int i, unsigned short h) {
+        int q;
+        if (is_out<G>(om, i)) {
+            q = zp;
+            val[p++] = h;
+        } else {
+            q = (int)rintf(__fdiv_rn(h2f(h), s)) + zp;
+            q = q < qlo ? qlo : (q > qhi ? qhi : q);
+        }
+        bw.put((unsigned)q, 2);
+    });
+    uint2 packed_cb;
+    packed_cb.x = (unsigned)e[0] | ((unsigned)e[1] << 16);
+    packed_cb.y = (unsigned)e[2] | ((unsigned)e[3] << 16);
+    reinterpret_cast<uint2*>(cb)[gid] = packed_cb;
 }
 
 __device__ __forceinline__ int nearest4(float v, float c0, float c1, float c2, float c3)
@@ -490,7 +590,7 @@ size_t quantize_workspace_bytes(int N, int /*K*/) { return ws_layout(N, nullptr,
 __global__ void k_quant_done() {}
 
 qg_status launch_quantize(const uint16_t* W, float /*frac*/, const qg_qweight& w, void* ws,
-                          cudaStream_t s)
+                          cudaStream_t s, int mode)
 {
     QuantWs p{};
     ws_layout(w.N, &p, ws);
@@ -532,7 +632,14 @@ qg_status launch_quantize(const uint16_t* W, float /*frac*/, const qg_qweight& w
     const int threads = 128;
     const int blocks = (int)ceil_div(groups, threads);
     const unsigned short* Wh = reinterpret_cast<const unsigned short*>(W);
-    if (w.bits == 2) {
+    if (w.bits == 2 && mode != 0) {
+        if (w.group == 64)
+            k_quant_uniform2<64><<<blocks, threads, 0, s>>>(Wh, w.N, w.K, mode, rp, w.out_col, w.packed, w.codebook,
+                                                            w.out_val);
+        else
+            k_quant_uniform2<128><<<blocks, threads, 0, s>>>(Wh, w.N, w.K, mode, rp, w.out_col, w.packed, w.codebook,
+                                                             w.out_val);
+    } else if (w.bits == 2) {
         if (w.group == 64)
             k_quant_codebook<64><<<blocks, threads, 0, s>>>(Wh, w.N, w.K, rp, w.out_col, w.packed,
                                                             w.codebook, w.out_val);
@@ -541,10 +648,10 @@ qg_status launch_quantize(const uint16_t* W, float /*frac*/, const qg_qweight& w
                                                              w.codebook, w.out_val);
     } else {
         if (w.group == 64)
-            k_quant_affine<64><<<blocks, threads, 0, s>>>(Wh, w.N, w.K, w.bits, rp, w.out_col, w.packed,
+            k_quant_affine<64><<<blocks, threads, 0, s>>>(Wh, w.N, w.K, w.bits, mode, rp, w.out_col, w.packed,
                                                           w.scale, w.zp);
         else
-            k_quant_affine<128><<<blocks, threads, 0, s>>>(Wh, w.N, w.K, w.bits, rp, w.out_col, w.packed,
+            k_quant_affine<128><<<blocks, threads, 0, s>>>(Wh, w.N, w.K, w.bits, mode, rp, w.out_col, w.packed,
                                                            w.scale, w.zp);
     }
     k_quant_done<<<1, 32, 0, s>>>();

@@ -139,6 +139,36 @@ QG_API qg_status qpack_workspace_size(int32_t N, int32_t K, size_t* bytes);
 QG_API qg_status qpack_quantize(const uint16_t* W, float outlier_frac, const qg_qweight* out, void* ws,
                          size_t ws_bytes, void* stream);
 
+/* Quantizer variants ("Mixed-width quantization" page, sections 2.3 and
+ * 4.1-4.2), all stored in the formats above, so every product entry point
+ * takes them unchanged:
+ *  QG_QUANT_ASYMMETRIC  qpack_quantize's quantizer (affine with a zero point
+ *                       at 3..6 bits, a 4-entry k-means codebook at 2 bits).
+ *  QG_QUANT_SYMMETRIC   no zero point (section 2.3 prefers it for the narrow
+ *                       widths): with qs = 2^(bits-1) - 1 (the symmetric
+ *                       integer range of the inference-acceleration guide
+ *                       page's INT8 example, section 1.1, [-qs, qs]) and amax
+ *                       the group's largest |w| over its non-outliers,
+ *                       scale = fp16 rounded up of amax / qs (1.0 if amax is
+ *                       0), q = clamp(round(w / scale), -qs, qs).  Widths
+ *                       3..6: stored as codes q + 2^(bits-1) with the zero
+ *                       point fixed at 2^(bits-1).  2 bits: levels -s, 0, s
+ *                       stored as the constants (-s, 0, s, s), codes q + 1.
+ *  QG_QUANT_LINEAR2     2 bits only: the affine grid (qpack_quantize's
+ *                       formula at qmax = 3) stored as its four constants
+ *                       fp16((i - zp) * scale), i = 0..3, which the code
+ *                       selects (section 4.2: a linear 2-bit grid maps codes
+ *                       to four constants, no k-means codebook).
+ * In every mode the constant or grid point of the zero code is exactly 0,
+ * outliers take that code, and their stored value is the weight itself. */
+typedef enum { QG_QUANT_ASYMMETRIC = 0, QG_QUANT_SYMMETRIC = 1, QG_QUANT_LINEAR2 = 2 } qg_quant_mode;
+
+/* qpack_quantize with a quantizer variant.  Arguments, workspace, results
+ * and errors as qpack_quantize, plus QG_ERR_INVALID_ARG for an unknown mode
+ * and QG_ERR_UNSUPPORTED for QG_QUANT_LINEAR2 at bits != 2. */
+QG_API qg_status qpack_quantize_mode(const uint16_t* W, float outlier_frac, qg_quant_mode mode,
+                                     const qg_qweight* out, void* ws, size_t ws_bytes, void* stream);
+
 /*
  * qpack_quantize without a workspace argument, for callers that cannot
  * allocate device memory when they quantize: code inside a host application
@@ -269,6 +299,44 @@ QG_API qg_status qgemm_moe_grouped_multi(const uint16_t* x, int32_t T, const int
  * steps, not a call for the hot path.  Returns QG_ERR_INVALID_ARG if status
  * is NULL and QG_ERR_CUDA if the device cannot be read. */
 QG_API qg_status qgemm_device_status(int32_t* status, int32_t reset);
+
+/*
+ * Diagnostics of one quantized layer against its original weights
+ * ("Mixed-width quantization" page, section 6.1: unpack the quantized weights
+ * and compare them element by element with the original fp16 weights --
+ * maximum absolute error, root mean square error, cosine similarity --
+ * section 6.2: a block whose largest value is far above its second largest
+ * holds one extreme value that stretches its scale).  Over all N*K elements,
+ * e = w - (w_hat + S) (the FP16 outliers are part of the layer's weight):
+ */
+typedef struct {
+    double max_abs_err;      /* max |e| */
+    double rmse;             /* sqrt(sum e^2 / (N*K)) */
+    double cosine;           /* sum w*v / (|w| |v|), v = w_hat + S; 1 if both are 0, 0 if one is */
+    double max_range_ratio;  /* largest group ratio (see group_ratio) */
+    int64_t groups_over;     /* groups whose ratio exceeds the threshold */
+} qg_diag;
+
+/* Workspace bytes qdiag_layer needs (one partial per 128 groups).  Host-only.
+ * Errors: QG_ERR_INVALID_ARG / QG_ERR_UNSUPPORTED as qpack_query_sizes. */
+QG_API qg_status qdiag_workspace_size(int32_t N, int32_t K, int32_t group, size_t* bytes);
+
+/*
+ *   W            fp16 [N, K] the original weights (DEVICE, 16-byte aligned).
+ *   w            the quantized layer (any width, group, outliers).
+ *   threshold    groups with ratio > threshold are counted in groups_over.
+ *   group_ratio  DEVICE fp32 [N, K/group] or NULL: per group, its largest
+ *                |w| over its second largest |w| (magnitudes counted with
+ *                multiplicity): 1 for an all-zero group, +inf when exactly
+ *                one element is nonzero.
+ *   out          DEVICE pointer to one qg_diag (8-byte aligned), written by
+ *                the call's last kernel; read it after the stream reaches it.
+ * Sums are fp32 within a group and fp64 across groups, reduced in a fixed
+ * order (deterministic).  Errors: QG_ERR_INVALID_ARG, QG_ERR_ALIGNMENT,
+ * QG_ERR_WORKSPACE, QG_ERR_CUDA.
+ */
+QG_API qg_status qdiag_layer(const uint16_t* W, const qg_qweight* w, float threshold, float* group_ratio,
+                             qg_diag* out, void* ws, size_t ws_bytes, void* stream);
 
 /* Self-check of the failure path of the bounded waits: launches one small
  * kernel on `stream` whose single mbarrier wait (at most poll_limit polls,

@@ -75,10 +75,15 @@ def lib():
         L.orc_quantize.argtypes = [vp, i64, i64, ctypes.c_int, ctypes.c_int, f32,
                                    vp, vp, vp, vp, vp, vp, vp]
         L.orc_quantize.restype = ctypes.c_int
+        L.orc_quantize_mode.argtypes = [vp, i64, i64, ctypes.c_int, ctypes.c_int, f32, ctypes.c_int,
+                                        vp, vp, vp, vp, vp, vp, vp]
+        L.orc_quantize_mode.restype = ctypes.c_int
         L.orc_dequant_rows.argtypes = [ctypes.POINTER(_QW), i64, i64, vp]
         L.orc_dequant_rows.restype = ctypes.c_int
         L.orc_linear_rows.argtypes = [vp, i64, i64, ctypes.POINTER(_QW), i64, i64, vp]
         L.orc_linear_rows.restype = ctypes.c_int
+        L.orc_diagnostics.argtypes = [vp, ctypes.POINTER(_QW), ctypes.c_double, vp, vp]
+        L.orc_diagnostics.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -192,8 +197,15 @@ def select_outliers(W, frac: float):
     return row_ptr, col[:n]
 
 
-def quantize(W, bits: int, group: int, frac: float = 0.0) -> QWeight:
-    """Quantize and pack W [N, K] (fp16)."""
+MODES = {"asymmetric": 0, "symmetric": 1, "linear2": 2}
+
+
+def quantize(W, bits: int, group: int, frac: float = 0.0, mode: str = "asymmetric") -> QWeight:
+    """Quantize and pack W [N, K] (fp16).  mode: 'asymmetric' (affine with a
+    zero point at 3-6 bits, k-means codebook at 2), 'symmetric' (no zero
+    point: the affine format with the zero point fixed at 2^(b-1); at 2
+    bits the constants -s, 0, s, s) or 'linear2' (2 bits only: the affine
+    grid's four constants)."""
     W = as_u16(W)
     N, K = W.shape
     sz = sizes(N, K, bits, group, frac)
@@ -206,7 +218,7 @@ def quantize(W, bits: int, group: int, frac: float = 0.0) -> QWeight:
     row_ptr = np.empty(N + 1, np.int32)
     col = np.empty(max(n, 1), np.int32)
     val = np.empty(max(n, 1), np.uint16)
-    rc = lib().orc_quantize(_p(W), N, K, bits, group, float(np.float32(frac)), _p(packed),
+    rc = lib().orc_quantize_mode(_p(W), N, K, bits, group, float(np.float32(frac)), MODES[mode], _p(packed),
                             _p(scale) if scale is not None else None,
                             _p(zp) if zp is not None else None,
                             _p(cb) if cb is not None else None,
@@ -241,6 +253,22 @@ def linear(x, q: QWeight, n0: int = 0, n1: int | None = None) -> np.ndarray:
     if rc != 0:
         raise ValueError(f"orc_linear_rows failed ({rc})")
     return y
+
+
+def diagnostics(W, q: QWeight, threshold: float = 8.0):
+    """Per-layer diagnostics of q against the original fp16 W: dict with
+    max_abs_err, rmse, cosine, max_range_ratio, groups_over (threshold) and
+    the per-group ratio array [N, K/group] (see ``orc_diagnostics``)."""
+    W = as_u16(W)
+    assert W.shape == (q.N, q.K)
+    out = np.zeros(5, np.float64)
+    ratio = np.empty((q.N, q.K // q.group), np.float64)
+    s = q._struct()
+    rc = lib().orc_diagnostics(_p(np.ascontiguousarray(W)), ctypes.byref(s), float(threshold), _p(out), _p(ratio))
+    if rc != 0:
+        raise ValueError(f"orc_diagnostics failed ({rc})")
+    return dict(max_abs_err=out[0], rmse=out[1], cosine=out[2], max_range_ratio=out[3], groups_over=int(out[4]),
+                ratio=ratio)
 
 
 def moe(x, topk, experts) -> np.ndarray:

@@ -294,6 +294,87 @@ static void quant_group_affine(const uint16_t *w, const uint8_t *is_out, int g, 
     *zp_out = (uint8_t)zp;
 }
 
+/* Symmetric quantizer of one group, stored in the affine format ("Mixed-
+ * width quantization" page, section 2.3: no zero point for the narrow
+ * widths, the scale absorbs the offset; the integer range follows the
+ * symmetric INT8 example of the inference-acceleration guide page, section
+ * 1.1, [-(2^(b-1) - 1), 2^(b-1) - 1]).  With qs = 2^(b-1) - 1 and amax the
+ * largest |w| over the non-outliers: scale = fp16 rounded up of amax / qs
+ * (1.0 if amax is 0), q = clamp(round(w / scale), -qs, qs), stored as
+ * q + 2^(b-1) with the zero point byte fixed at 2^(b-1); q = 0 at outliers. */
+static void quant_group_symmetric(const uint16_t *w, const uint8_t *is_out, int g, int bits,
+                                  uint8_t *codes, uint16_t *scale16, uint8_t *zp_out)
+{
+    const int qs = (1 << (bits - 1)) - 1, zp = 1 << (bits - 1);
+    float amax = 0.0f;
+    for (int i = 0; i < g; i++) {
+        if (is_out[i]) continue;
+        float a = fabsf(orc_f16_to_f32(w[i]));
+        if (a > amax) amax = a;
+    }
+    uint16_t s16 = amax == 0.0f ? 0x3C00 : f32_to_f16(amax / (float)qs, 1);
+    float s = orc_f16_to_f32(s16);
+    for (int i = 0; i < g; i++) {
+        int q = 0;
+        if (!is_out[i]) {
+            q = (int)rintf(orc_f16_to_f32(w[i]) / s);
+            if (q < -qs) q = -qs;
+            if (q > qs) q = qs;
+        }
+        codes[i] = (uint8_t)(q + zp);
+    }
+    *scale16 = s16;
+    *zp_out = (uint8_t)zp;
+}
+
+/* 2-bit groups on a uniform grid, stored as the four constants a code
+ * selects ("Mixed-width quantization" page, section 4.2: a linear 2-bit grid
+ * maps each code to one of four constants picked by a select instruction,
+ * not a k-means codebook).  mode 1 (symmetric): the symmetric rule above at
+ * b = 2 (qs = 1, levels -s, 0, s; the fourth constant repeats s), codes
+ * q + 1.  mode 2 (linear): the affine quantizer at b = 2 (range widened to
+ * contain 0, scale = fp16 rounded up of (max - min) / 3, zp = clamp(-round(
+ * min / scale), 0, 3), q = clamp(round(w / scale) + zp, 0, 3)), constants
+ * fp16((i - zp) * scale) for i = 0..3.  Either way the constant of the zero
+ * code is exactly 0, so an outlier takes that code and keeps fp16(w) as its
+ * stored value. */
+static void quant_group_uniform2(const uint16_t *w, const uint8_t *is_out, int g, int mode,
+                                 uint8_t *codes, uint16_t cb16[4], uint16_t *resid)
+{
+    if (mode == 1) {
+        float amax = 0.0f;
+        for (int i = 0; i < g; i++) {
+            if (is_out[i]) continue;
+            float a = fabsf(orc_f16_to_f32(w[i]));
+            if (a > amax) amax = a;
+        }
+        uint16_t s16 = amax == 0.0f ? 0x3C00 : f32_to_f16(amax, 1);
+        float s = orc_f16_to_f32(s16);
+        for (int i = 0; i < g; i++) {
+            int q = 0;
+            if (!is_out[i]) {
+                q = (int)rintf(orc_f16_to_f32(w[i]) / s);
+                if (q < -1) q = -1;
+                if (q > 1) q = 1;
+            }
+            codes[i] = (uint8_t)(q + 1);
+            if (is_out[i]) resid[i] = w[i];
+        }
+        cb16[0] = (uint16_t)(s16 | 0x8000);
+        cb16[1] = 0;
+        cb16[2] = s16;
+        cb16[3] = s16;
+        return;
+    }
+    uint16_t s16;
+    uint8_t zp;
+    quant_group_affine(w, is_out, g, 2, codes, &s16, &zp);
+    float s = orc_f16_to_f32(s16);
+    for (int i = 0; i < 4; i++) cb16[i] = f32_to_f16((float)(i - (int)zp) * s, 0);
+    for (int i = 0; i < g; i++)
+        if (is_out[i]) resid[i] = w[i];
+}
+
 /* Index of the entry nearest to v; ties go to the lower index. */
 static int nearest4(float v, const float c[4])
 {
@@ -376,11 +457,12 @@ static void quant_group_codebook(const uint16_t *w, const uint8_t *is_out, int g
  * scale fp16 [N, K/group] and zp u8 [N, K/group] for bits != 2,
  * cb fp16 [N, K/group, 4] for bits == 2, outlier CSR row_ptr [N+1],
  * col [nnz], val fp16 [nnz].  Unused outputs may be NULL. */
-int orc_quantize(const uint16_t *W, int64_t N, int64_t K, int bits, int group, float frac,
-                 uint8_t *packed, uint16_t *scale, uint8_t *zp, uint16_t *cb,
-                 int32_t *row_ptr, int32_t *col, uint16_t *val)
+int orc_quantize_mode(const uint16_t *W, int64_t N, int64_t K, int bits, int group, float frac, int mode,
+                      uint8_t *packed, uint16_t *scale, uint8_t *zp, uint16_t *cb,
+                      int32_t *row_ptr, int32_t *col, uint16_t *val)
 {
     if (!valid_shape(N, K, bits, group) || frac < 0.0f || frac >= 1.0f) return ORC_EINVAL;
+    if (mode < 0 || mode > 2 || (mode == 2 && bits != 2)) return ORC_EINVAL;
     for (int64_t i = 0; i < N * K; i++)
         if (!finite16(W[i])) return ORC_ENONFINITE;
     int64_t ng = K / group;
@@ -402,9 +484,15 @@ int orc_quantize(const uint16_t *W, int64_t N, int64_t K, int bits, int group, f
         const uint8_t *mr = mask + n * K;
         for (int64_t j = 0; j < ng; j++) {
             int64_t k0 = j * group;
-            if (bits == 2)
+            if (bits == 2 && mode == 0)
                 quant_group_codebook(wr + k0, mr + k0, group, codes + k0, cb + (n * ng + j) * 4,
                                      resid + k0);
+            else if (bits == 2)
+                quant_group_uniform2(wr + k0, mr + k0, group, mode, codes + k0, cb + (n * ng + j) * 4,
+                                     resid + k0);
+            else if (mode == 1)
+                quant_group_symmetric(wr + k0, mr + k0, group, bits, codes + k0, scale + n * ng + j,
+                                      zp + n * ng + j);
             else
                 quant_group_affine(wr + k0, mr + k0, group, bits, codes + k0, scale + n * ng + j,
                                    zp + n * ng + j);
@@ -421,6 +509,14 @@ int orc_quantize(const uint16_t *W, int64_t N, int64_t K, int bits, int group, f
     row_ptr[N] = (int32_t)p;
     free(mask); free(codes); free(resid);
     return ORC_OK;
+}
+
+/* The default quantizer: asymmetric affine at 3..6 bits, k-means codebook at 2. */
+int orc_quantize(const uint16_t *W, int64_t N, int64_t K, int bits, int group, float frac,
+                 uint8_t *packed, uint16_t *scale, uint8_t *zp, uint16_t *cb,
+                 int32_t *row_ptr, int32_t *col, uint16_t *val)
+{
+    return orc_quantize_mode(W, N, K, bits, group, frac, 0, packed, scale, zp, cb, row_ptr, col, val);
 }
 
 /* ------------------------------------------------------------------ */
@@ -494,5 +590,70 @@ int orc_linear_rows(const uint16_t *x, int64_t M, int64_t ldx, const orc_qweight
         }
     }
     free(row); free(xd); free(codes);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* per-layer quantization diagnostics                                   */
+/* ------------------------------------------------------------------ */
+
+/* Diagnostics of one quantized layer ("Mixed-width quantization" page,
+ * section 6.1: unpack the quantized weights and compare them element by
+ * element with the original fp16 weights -- maximum absolute error, root
+ * mean square error, cosine similarity; section 6.2: the "dynamic range
+ * ratio" of a block, its largest value over its second largest, flags
+ * blocks that hold one extreme value).
+ *   e[n,k] = w[n,k] - (x_hat[n,k] + S[n,k]) over all N*K elements (the
+ *   layer's effective weight includes the FP16 outliers added back);
+ *   out[0] = max |e|, out[1] = sqrt(sum e^2 / (N*K)),
+ *   out[2] = sum w*v / (|w| |v|) with v = x_hat + S (1 if both norms are 0,
+ *   0 if only one is), out[3] = largest group ratio,
+ *   out[4] = number of groups whose ratio exceeds `threshold`.
+ * ratio[n*ng + j] (may be NULL) = max |w| / second largest |w| over the
+ * group's elements (magnitudes, counted with multiplicity): 1 for an
+ * all-zero group, +infinity when exactly one element is nonzero.
+ * Everything in fp64, in ascending element order. */
+int orc_diagnostics(const uint16_t *W, const orc_qweight *q, double threshold, double *out, double *ratio)
+{
+    int64_t N = q->N, K = q->K, g = q->group, ng = K / g;
+    double *v = (double *)malloc(sizeof(double) * (size_t)K);
+    uint8_t *codes = (uint8_t *)malloc((size_t)K);
+    if (!v || !codes) {
+        free(v); free(codes);
+        return ORC_ENOMEM;
+    }
+    double emax = 0.0, se = 0.0, sww = 0.0, svv = 0.0, swv = 0.0, rmax = 0.0, over = 0.0;
+    for (int64_t n = 0; n < N; n++) {
+        dequant_row(q, n, codes, v);
+        for (int64_t j = 0; j < ng; j++) {
+            double m1 = 0.0, m2 = 0.0;
+            for (int64_t i = j * g; i < (j + 1) * g; i++) {
+                double w = orc_f16_to_f64(W[n * K + i]);
+                double e = w - v[i];
+                if (fabs(e) > emax) emax = fabs(e);
+                se += e * e;
+                sww += w * w;
+                svv += v[i] * v[i];
+                swv += w * v[i];
+                double a = fabs(w);
+                if (a > m1) {
+                    m2 = m1;
+                    m1 = a;
+                } else if (a > m2) {
+                    m2 = a;
+                }
+            }
+            double r = m1 == 0.0 ? 1.0 : (m2 == 0.0 ? INFINITY : m1 / m2);
+            if (ratio) ratio[n * ng + j] = r;
+            if (r > rmax) rmax = r;
+            if (r > threshold) over += 1.0;
+        }
+    }
+    out[0] = emax;
+    out[1] = sqrt(se / (double)(N * K));
+    out[2] = (sww == 0.0 && svv == 0.0) ? 1.0 : (sww == 0.0 || svv == 0.0) ? 0.0 : swv / (sqrt(sww) * sqrt(svv));
+    out[3] = rmax;
+    out[4] = over;
+    free(v); free(codes);
     return ORC_OK;
 }

@@ -152,6 +152,30 @@ def test_both_quantizers_refuse_the_same_bad_descriptors(qg):
     assert f(None, 0.001, ctypes.byref(good()), None) == -1
 
 
+def test_quantize_mode_validation_without_gpu(qg):
+    L = qg.lib()
+    W = ctypes.c_void_p(0x400000)
+    ws = ctypes.c_void_p(0x600000)
+    d = _fake_desc(qg, N=64, K=1024)
+    need = qg.qpack_workspace_size(64, 1024)
+    assert L.qpack_quantize_mode(W, 0.0, 7, ctypes.byref(d), ws, need, None) == -1      # unknown mode
+    assert L.qpack_quantize_mode(W, 0.0, 2, ctypes.byref(d), ws, need, None) == -2      # linear2 needs 2 bits
+    assert L.qpack_quantize_mode(W, 0.0, 1, ctypes.byref(d), ws, need - 1, None) == -4  # workspace
+    assert L.qpack_quantize_mode(ctypes.c_void_p(0x400002), 0.0, 1, ctypes.byref(d), ws, need, None) == -3
+
+
+def test_diagnostics_validation_without_gpu(qg):
+    L = qg.lib()
+    d = _fake_desc(qg, N=64, K=1024)
+    need = ctypes.c_size_t()
+    assert L.qdiag_workspace_size(64, 1024, 64, ctypes.byref(need)) == 0 and need.value > 0
+    W, out, ws = ctypes.c_void_p(0x400000), ctypes.c_void_p(0x700000), ctypes.c_void_p(0x600000)
+    assert L.qdiag_layer(None, ctypes.byref(d), 8.0, None, out, ws, need.value, None) == -1
+    assert L.qdiag_layer(W, ctypes.byref(d), 8.0, None, ctypes.c_void_p(0x700004), ws, need.value, None) == -3
+    assert L.qdiag_layer(W, ctypes.byref(d), 8.0, None, out, ws, need.value - 1, None) == -4
+    assert L.qdiag_layer(W, ctypes.byref(d), float("nan"), None, out, ws, need.value, None) == -1
+
+
 def test_valid_call_without_a_device_reports_cuda_error(qg):
     # every argument passes host validation; the first CUDA call then fails
     # (no device here) and the status says so instead of crashing

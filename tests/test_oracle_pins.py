@@ -442,3 +442,150 @@ def test_moe_routes_each_pair_to_its_expert():
         for j in range(k):
             assert (y[t, j] == oracle.linear(xb[t:t + 1], experts[topk[t, j]])[0]).all()
     assert all(len(set(r)) == k for r in topk.tolist())
+
+
+# ---------------------------------------------------------------- layer diagnostics
+def test_diagnostics_hand_worked_group():
+    # "Mixed-width quantization" page, section 6.1 (max |error|, RMSE, cosine
+    # of unpacked vs original weights) and 6.2 (block max over second max).
+    # One 4-bit group of 64: w0 = 1.5, w1 = 0.75, zeros elsewhere.  By hand:
+    # scale = fp16 rounded up of 1.5 / 15 = 0.10003662109375, zp = 0,
+    # q0 = round(14.9945) = 15, q1 = round(7.4973) = 7, so
+    # w_hat0 = 1.50054931640625 and w_hat1 = 0.70025634765625.
+    W = np.zeros((1, 64), np.float16)
+    W[0, 0], W[0, 1] = 1.5, 0.75
+    q = oracle.quantize(W, 4, 64, 0.0)
+    assert q.scale.view(np.float16)[0, 0] == np.float16(0.10003662109375)
+    h0, h1 = 1.50054931640625, 0.70025634765625
+    e0, e1 = 1.5 - h0, 0.75 - h1
+    d = oracle.diagnostics(W, q, threshold=1.5)
+    assert d["max_abs_err"] == abs(e1) == 0.04974365234375
+    assert d["rmse"] == pytest.approx(math.sqrt((e0 ** 2 + e1 ** 2) / 64), rel=1e-15)
+    cos = (1.5 * h0 + 0.75 * h1) / (math.hypot(1.5, 0.75) * math.hypot(h0, h1))
+    assert d["cosine"] == pytest.approx(cos, rel=1e-15)
+    assert d["ratio"].tolist() == [[2.0]] and d["max_range_ratio"] == 2.0 and d["groups_over"] == 1
+    assert oracle.diagnostics(W, q, threshold=2.0)["groups_over"] == 0
+
+
+def test_diagnostics_range_ratio_special_groups():
+    W = np.zeros((1, 5 * 64), np.float16)
+    W[0, 64:128][10] = 0.5                       # one nonzero: ratio +inf
+    W[0, 128:192][[3, 40]] = [-0.25, 0.25]       # equal magnitudes: 1
+    W[0, 192:256][[0, 1, 2]] = [3.0, -4.0, 1.0]  # 4 / 3 (magnitudes, either sign)
+    W[0, 256:320][5] = -2.0                      # one nonzero, negative: +inf
+    d = oracle.diagnostics(W, oracle.quantize(W, 5, 64, 0.0), threshold=1.2)
+    r = d["ratio"][0]
+    assert r[0] == 1.0 and np.isinf(r[1]) and r[2] == 1.0 and r[3] == pytest.approx(4 / 3) and np.isinf(r[4])
+    assert d["groups_over"] == 3 and np.isinf(d["max_range_ratio"])
+
+
+def test_diagnostics_exact_layer_and_outliers_count_as_exact():
+    # weights on the 4-bit grid reproduce exactly: no error, cosine 1; an
+    # outlier is stored in FP16 and added back, so it adds no error either
+    ramp = np.tile((np.arange(16) - 5) * 0.25, 8)
+    W = np.stack([ramp, ramp[::-1]]).astype(np.float16)
+    d = oracle.diagnostics(W, oracle.quantize(W, 4, 128, 0.0))
+    assert d["max_abs_err"] == 0.0 and d["rmse"] == 0.0 and d["cosine"] == 1.0
+    W2 = W.copy()
+    W2[1, 7] = np.float16(1000.0)
+    q2 = oracle.quantize(W2, 4, 128, 1 / 256)    # exactly one outlier: the 1000
+    assert q2.nnz == 1 and q2.col.tolist() == [7]
+    d2 = oracle.diagnostics(W2, q2)
+    assert d2["max_range_ratio"] == 1000.0 / 2.5
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6])
+def test_diagnostics_invariants(bits):
+    N, K, group = 48, 512, 64
+    W = wl.gen_weight(N, K, seed=70 + bits, outlier_frac=0.002, outlier_seed=71)
+    q = oracle.quantize(W, bits, group, 0.002)
+    d = oracle.diagnostics(W, q)
+    e = W.double().numpy() - oracle.dequant(q)
+    assert d["max_abs_err"] == np.abs(e).max()
+    assert d["rmse"] <= d["max_abs_err"]
+    assert -1.0 <= d["cosine"] <= 1.0
+    if bits != 2:   # affine: half a step per element at most
+        s = oracle.f16_to_f32(q.scale).astype(np.float64).max()
+        assert d["max_abs_err"] <= s * (0.5 + 2.0 ** -20)
+    # wider codes fit better
+    if bits >= 3:
+        dq = oracle.diagnostics(W, oracle.quantize(W, bits - 1 if bits > 3 else 3, group, 0.002))
+        assert dq["rmse"] >= d["rmse"] * (1 - 1e-12)
+
+
+# ---------------------------------------------------------------- quantizer variants
+def _codes(q):
+    return oracle.unpack(q.packed[0], q.K, q.bits)
+
+
+def test_symmetric_3bit_hand_worked():
+    # no zero point ("Mixed-width quantization" page, section 2.3), integer
+    # range [-3, 3] at 3 bits (the symmetric convention of the inference-
+    # acceleration guide page, section 1.1): amax 1.5 -> scale 0.5, stored
+    # codes q + 4; ties round to even (-2.5 -> -2, 1.5 -> 2, 0.5 -> 0)
+    W = np.zeros((1, 64), np.float16)
+    W[0, :6] = [1.5, -1.25, 0.75, -0.75, 0.25, 1.0]
+    q = oracle.quantize(W, 3, 64, 0.0, mode="symmetric")
+    assert q.scale.view(np.float16)[0, 0] == np.float16(0.5) and q.zp[0, 0] == 4
+    c = _codes(q)
+    assert c[:6].tolist() == [7, 2, 6, 2, 4, 6] and (c[6:] == 4).all()
+
+
+def test_symmetric_2bit_constants_hand_worked():
+    # 2 bits, symmetric: levels -s, 0, s with s = amax (the fourth constant repeats s)
+    W = np.zeros((1, 64), np.float16)
+    W[0, :5] = [0.75, -0.3, 0.4, -0.75, 0.2]
+    q = oracle.quantize(W, 2, 64, 0.0, mode="symmetric")
+    assert q.cb.view(np.float16)[0, 0].tolist() == [-0.75, 0.0, 0.75, 0.75]
+    c = _codes(q)
+    assert c[:5].tolist() == [2, 1, 2, 0, 1] and (c[5:] == 1).all()
+
+
+def test_linear2_hand_worked():
+    # the affine grid at 2 bits: range [-1.25, 2.5] -> scale 1.25, zp 1;
+    # constants (i - 1) * 1.25; 0.5 -> 0 and 1.5 -> 2 (ties to even)
+    W = np.zeros((1, 64), np.float16)
+    W[0, :4] = [-1.25, 2.5, 0.625, 1.875]
+    q = oracle.quantize(W, 2, 64, 0.0, mode="linear2")
+    assert q.cb.view(np.float16)[0, 0].tolist() == [-1.25, 0.0, 1.25, 2.5]
+    c = _codes(q)
+    assert c[:4].tolist() == [0, 3, 1, 3] and (c[4:] == 1).all()
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6])
+def test_symmetric_is_odd_and_within_half_a_step(bits):
+    # round half to even and a clamp at +-qs are odd functions: quantizing -W
+    # gives exactly -w_hat; every non-outlier is within half a step; the
+    # outliers come back exactly
+    N, K, group, frac = 24, 512, 64, 0.004
+    W = wl.gen_weight(N, K, seed=80 + bits, outlier_frac=frac, outlier_seed=81)
+    q = oracle.quantize(W, bits, group, frac, mode="symmetric")
+    qn = oracle.quantize(-W, bits, group, frac, mode="symmetric")
+    xh, xn = oracle.dequant(q), oracle.dequant(qn)
+    assert np.array_equal(xn, -xh)
+    w = W.double().numpy()
+    out = _outlier_mask(q)
+    assert (xh[out] == w[out]).all()
+    if bits == 2:
+        s = q.cb.view(np.float16)[..., 2].astype(np.float64)
+    else:
+        s = q.scale.view(np.float16).astype(np.float64)
+        assert (q.zp == 1 << (bits - 1)).all() and (_groups(q) != 0).all()
+    sg = np.repeat(s, group, axis=1)
+    if bits > 2:
+        assert (np.abs(w - xh)[~out] <= sg[~out] * (0.5 + 2.0 ** -20)).all()
+    else:   # 3 levels: values beyond s/2 of every level can only be above 1.5 s, impossible by amax = s
+        assert (np.abs(w - xh)[~out] <= sg[~out] * (0.5 + 2.0 ** -20)).all()
+
+
+def test_linear2_constants_are_the_affine_grid():
+    N, K, group, frac = 24, 512, 128, 0.004
+    W = wl.gen_weight(N, K, seed=90, outlier_frac=frac, outlier_seed=91)
+    q = oracle.quantize(W, 2, group, frac, mode="linear2")
+    cb = q.cb.view(np.float16).astype(np.float64)             # [N, ng, 4]
+    step = cb[..., 1:] - cb[..., :-1]
+    # uniform: equal steps (each constant rounded to fp16 once)
+    assert np.allclose(step, step[..., :1], rtol=2e-3)
+    assert ((cb == 0).sum(-1) == 1).all()                       # the zero code's constant is exactly 0
+    out = _outlier_mask(q)
+    assert (oracle.dequant(q)[out] == W.double().numpy()[out]).all()
