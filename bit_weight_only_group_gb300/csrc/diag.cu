@@ -216,7 +216,8 @@ qg_status launch_diag(const uint16_t* W, const qg_qweight& w, float threshold, f
         case 3: return diag::run_bits<3>(W, w, threshold, ratio, out, ws, s);
         case 4: return diag::run_bits<4>(W, w, threshold, ratio, out, ws, s);
         case 5: return diag::run_bits<5>(W, w, threshold, ratio, out, ws, s);
-        default: return diag::run_bits<6>(W, w, threshold, ratio, out, ws, s);
+        case 6: return diag::run_bits<6>(W, w, threshold, ratio, out, ws, s);
+        default: return diag::run_bits<8>(W, w, threshold, ratio, out, ws, s);
     }
 }
 

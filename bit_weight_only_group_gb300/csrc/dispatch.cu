@@ -27,6 +27,9 @@ extern template qg_status launch_grouped<3>(const MoeTable&, int, int, int, int,
 extern template qg_status launch_grouped<4>(const MoeTable&, int, int, int, int, cudaStream_t);
 extern template qg_status launch_grouped<5>(const MoeTable&, int, int, int, int, cudaStream_t);
 extern template qg_status launch_grouped<6>(const MoeTable&, int, int, int, int, cudaStream_t);
+extern template qg_status launch_dense<8>(const Problem&, int, cudaStream_t);
+extern template qg_status launch_multi<8>(const MultiTable&, int, cudaStream_t);
+extern template qg_status launch_grouped<8>(const MoeTable&, int, int, int, int, cudaStream_t);
 }  // namespace gemv
 
 // Device status word of the library's kernels (QG_OK, or QG_ERR_TIMEOUT after
@@ -130,7 +133,8 @@ qg_status dense_by_bits(const gemv::Problem& p, int bits, int group, cudaStream_
         case 3: return gemv::launch_dense<3>(p, group, s);
         case 4: return gemv::launch_dense<4>(p, group, s);
         case 5: return gemv::launch_dense<5>(p, group, s);
-        default: return gemv::launch_dense<6>(p, group, s);
+        case 6: return gemv::launch_dense<6>(p, group, s);
+        default: return gemv::launch_dense<8>(p, group, s);
     }
 }
 
@@ -252,7 +256,8 @@ qg_status launch_gemv_multi(const uint16_t* x, int M, int ldx, const qg_qweight*
         case 3: return gemv::launch_multi<3>(t, ws[0].group, s);
         case 4: return gemv::launch_multi<4>(t, ws[0].group, s);
         case 5: return gemv::launch_multi<5>(t, ws[0].group, s);
-        default: return gemv::launch_multi<6>(t, ws[0].group, s);
+        case 6: return gemv::launch_multi<6>(t, ws[0].group, s);
+        default: return gemv::launch_multi<8>(t, ws[0].group, s);
     }
 }
 
@@ -316,7 +321,8 @@ qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const
             case 3: st = gemv::launch_grouped<3>(t, maxi, expect, w0.group, mp, s); break;
             case 4: st = gemv::launch_grouped<4>(t, maxi, expect, w0.group, mp, s); break;
             case 5: st = gemv::launch_grouped<5>(t, maxi, expect, w0.group, mp, s); break;
-            default: st = gemv::launch_grouped<6>(t, maxi, expect, w0.group, mp, s); break;
+            case 6: st = gemv::launch_grouped<6>(t, maxi, expect, w0.group, mp, s); break;
+            default: st = gemv::launch_grouped<8>(t, maxi, expect, w0.group, mp, s); break;
         }
         if (st != QG_OK) return st;
     }

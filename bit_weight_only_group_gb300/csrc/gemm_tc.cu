@@ -577,7 +577,8 @@ qg_status launch_gemm(const uint16_t* x, int M, int ldx, const qg_qweight& w, vo
         case 3: return tc::run_bits<3>(x, M, ldx, w, y, ldy, yt, ws, s);
         case 4: return tc::run_bits<4>(x, M, ldx, w, y, ldy, yt, ws, s);
         case 5: return tc::run_bits<5>(x, M, ldx, w, y, ldy, yt, ws, s);
-        default: return tc::run_bits<6>(x, M, ldx, w, y, ldy, yt, ws, s);
+        case 6: return tc::run_bits<6>(x, M, ldx, w, y, ldy, yt, ws, s);
+        default: return tc::run_bits<8>(x, M, ldx, w, y, ldy, yt, ws, s);
     }
 }
 

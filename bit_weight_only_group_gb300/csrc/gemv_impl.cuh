@@ -70,6 +70,10 @@ __host__ __device__ constexpr PairE plan_entry(int bits, int nc, int e)
         const int lo = 16 * w + (h ? 8 : 0) + j;
         return PairE{lo, lo + 4, 0, 0, 0};
     }
+    if (bits == 8) {   // bytes (4j + h, 4j + h + 2) of word j: windows at 32j and 32j + 8
+        const int j = e / 2, h = e % 2;
+        return PairE{4 * j + h, 4 * j + h + 2, 0, 0, 32 * j + 8 * h};
+    }
     if (bits == 6) {   // (i, i+2) within each 4-code unit (3 bytes)
         const int m = e / 2, q = e % 2;
         const int lo = 4 * m + q;
@@ -311,7 +315,7 @@ struct Cfg {
     static constexpr int NT = (MP + 7) / 8;                       // n8 token tiles
     static constexpr int NTOK = 8 * NT;
     // prefetch depth (groups) of the register ring
-    static constexpr int D_CLAMP = MP <= 16 ? 4 : 2;
+    static constexpr int D_CLAMP = (MP <= 16 && NW < 8) ? 4 : 2;   // 8-word chunks (8 bits, group 128): 2
     static constexpr int TSTRIDE = 32;                            // bytes per token per step
     static constexpr int SSTRIDE = MP * TSTRIDE;                  // bytes per step
     static constexpr int GSTRIDE = STEPS * SSTRIDE;               // bytes per group

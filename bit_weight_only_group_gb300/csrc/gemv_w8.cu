@@ -1,0 +1,10 @@
+// Instantiation of the decode / grouped kernels for 8-bit weights.
+#include "gemv_impl.cuh"
+
+namespace qg {
+namespace gemv {
+template qg_status launch_dense<8>(const Problem&, int, cudaStream_t);
+template qg_status launch_multi<8>(const MultiTable&, int, cudaStream_t);
+template qg_status launch_grouped<8>(const MoeTable&, int, int, int, int, cudaStream_t);
+}  // namespace gemv
+}  // namespace qg

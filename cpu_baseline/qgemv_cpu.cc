@@ -134,7 +134,8 @@ void rows(const Weight& w, const float* x, const float* xsum, float* y, int n0, 
             case 3: v = row_affine<3>(w, x, xsum, n); break;
             case 4: v = row_affine<4>(w, x, xsum, n); break;
             case 5: v = row_affine<5>(w, x, xsum, n); break;
-            default: v = row_affine<6>(w, x, xsum, n); break;
+            case 6: v = row_affine<6>(w, x, xsum, n); break;
+            default: v = row_affine<8>(w, x, xsum, n); break;
         }
         if (w.nnz > 0)
             for (int p = w.row_ptr[n]; p < w.row_ptr[n + 1]; p++) v += x[w.col[p]] * half_to_float(w.val[p]);
@@ -160,7 +161,7 @@ int cpuq_gemv(const float* x, int N, int K, int bits, int group, const uint8_t* 
               const uint8_t* zp, const uint16_t* cb, const int32_t* row_ptr, const int32_t* col,
               const uint16_t* val, int nnz, float* y, int threads)
 {
-    if (!x || !y || !packed || N <= 0 || K <= 0 || bits < 2 || bits > 6 || (group != 64 && group != 128) ||
+    if (!x || !y || !packed || N <= 0 || K <= 0 || ((bits < 2 || bits > 6) && bits != 8) || (group != 64 && group != 128) ||
         K % group || (bits == 2 ? !cb : (!scale || !zp)) || (nnz > 0 && (!row_ptr || !col || !val)))
         return -1;
     const Weight w{N, K, bits, group, packed, scale, zp, cb, row_ptr, col, val, nnz};

@@ -13,7 +13,9 @@
  *    excluding the largest-magnitude 0.1 % of weights, which are kept in FP16
  *    and added back after the product  ("70B on one GPU" page, section 2,
  *    "group-wise outlier-aware quantization", steps 1-3);
- *  - widths 2, 3, 4, 5, 6 bits; 2-bit groups use a 4-entry non-uniform
+ *  - widths 2, 3, 4, 5, 6 bits, and 8 bits (a weight-only int8 path, the
+ *    width the pages' GPU unpack targets: "Mixed-width quantization" page,
+ *    section 4.2); 2-bit groups use a 4-entry non-uniform
  *    codebook found by k-means  ("Mixed-width quantization" page, section 2.1 table and 4.1);
  *  - codes packed LSB-first in a little-endian bit stream: 3-bit 8 values
  *    in 3 bytes, 5-bit 8 values in 5 bytes, 6-bit 4 values in 3 bytes,
@@ -69,7 +71,7 @@ typedef enum { QG_Y_F32 = 0, QG_Y_BF16 = 1 } qg_ydtype;
  * array, per-group parameters in others; "Mixed-width quantization" page, section 3.3).
  *
  *  N, K        output and input features.  K % group == 0.
- *  bits        2, 3, 4, 5 or 6.
+ *  bits        2, 3, 4, 5, 6 or 8 (8: one byte per code).
  *  group       64 or 128 consecutive weights along K share a scale/zp
  *              (or, at 2 bits, a codebook).  ng = K / group.
  *  packed      uint8 [N, K*bits/8], row-major; row n holds the K codes of
@@ -104,7 +106,7 @@ typedef struct {
  * 2 + 64/group (2-bit codebook of 4 fp16 entries); "Mixed-width quantization" page, section 2.3
  * gives the same accounting for the scale overhead.
  * Errors: QG_ERR_INVALID_ARG for N, K <= 0, K % group, outlier_frac outside
- * [0, 1); QG_ERR_UNSUPPORTED for bits outside 2..6 or group not 64/128.
+ * [0, 1); QG_ERR_UNSUPPORTED for bits outside {2..6, 8} or group not 64/128.
  */
 QG_API qg_status qpack_query_sizes(int32_t N, int32_t K, int32_t bits, int32_t group, float outlier_frac,
                             size_t* packed_bytes, size_t* scale_bytes, size_t* zp_bytes,

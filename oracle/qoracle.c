@@ -137,7 +137,7 @@ int64_t orc_nnz(int64_t N, int64_t K, float frac)
 static int valid_shape(int64_t N, int64_t K, int bits, int group)
 {
     if (N <= 0 || K <= 0) return 0;
-    if (bits < 2 || bits > 6) return 0;
+    if ((bits < 2 || bits > 6) && bits != 8) return 0;
     if (group != 64 && group != 128) return 0;
     if (K % group) return 0;
     return 1;

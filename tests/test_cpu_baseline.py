@@ -10,7 +10,7 @@ import workloads as wl
 from _parity import check_product
 
 
-@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6])
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
 @pytest.mark.parametrize("group", [64, 128])
 def test_cpu_baseline_matches_oracle(bits, group):
     N, K, frac = 136, 1024, 0.003

@@ -36,7 +36,7 @@ def _check(got, ref):
     assert np.allclose(r[fin], ref["ratio"][fin], rtol=1e-6, atol=0)
 
 
-@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6])
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
 @pytest.mark.parametrize("group", [64, 128])
 def test_diagnostics_against_oracle(qg, bits, group):
     N, K, frac = 200, 1024, 0.002

@@ -30,7 +30,7 @@ def _weights(N, K, bits, group, frac, seed):
     return _cache[key]
 
 
-@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6])
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
 @pytest.mark.parametrize("group", [64, 128])
 @pytest.mark.parametrize("M", [1, 2, 3, 5, 8, 16, 27, 64])
 def test_product_small(qg, bits, group, M):
@@ -120,7 +120,7 @@ def test_tensor_core_path_against_oracle(qg, group, M, N, K):
     assert torch.equal(yb, y.to(torch.bfloat16))
 
 
-@pytest.mark.parametrize("bits", [2, 3, 5, 6])
+@pytest.mark.parametrize("bits", [2, 3, 5, 6, 8])
 @pytest.mark.parametrize("group", [64, 128])
 @pytest.mark.parametrize("M,N,K", [(300, 600, 1024), (129, 200, 384)])
 def test_tensor_core_path_every_width(qg, bits, group, M, N, K):

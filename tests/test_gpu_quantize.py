@@ -24,7 +24,7 @@ def _run(qg, W, bits, group, frac):
     return qw
 
 
-@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6])
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
 @pytest.mark.parametrize("group", [64, 128])
 @pytest.mark.parametrize("N,K,frac", [(96, 512, 0.002), (33, 256, 0.0), (7, 1024, 0.01)])
 def test_quantize_bit_exact_small(qg, bits, group, N, K, frac):

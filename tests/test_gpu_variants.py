@@ -11,7 +11,7 @@ from _parity import assert_quantized_equal, check_product, to_device
 
 pytestmark = pytest.mark.gpu
 
-CASES = [(b, "symmetric") for b in (2, 3, 4, 5, 6)] + [(2, "linear2")]
+CASES = [(b, "symmetric") for b in (2, 3, 4, 5, 6, 8)] + [(2, "linear2")]
 
 
 @pytest.fixture(scope="module")

@@ -190,7 +190,7 @@ def _outlier_mask(q):
     return m
 
 
-@pytest.mark.parametrize("bits", [3, 4, 5, 6])
+@pytest.mark.parametrize("bits", [3, 4, 5, 6, 8])
 @pytest.mark.parametrize("group", [64, 128])
 def test_affine_codes_are_nearest_grid_points(bits, group):
     N, K, frac = 24, 1024, 0.002
@@ -386,7 +386,7 @@ def test_codebook_tie_rules_on_a_closed_form_group():
 
 
 # ---------------------------------------------------------------- the product
-@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6])
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
 def test_linear_is_x_times_dequant_transposed(bits):
     N, K, M = 8, 128, 3
     W = wl.gen_weight(N, K, seed=71, outlier_frac=0.02, outlier_seed=72)
@@ -589,3 +589,10 @@ def test_linear2_constants_are_the_affine_grid():
     assert ((cb == 0).sum(-1) == 1).all()                       # the zero code's constant is exactly 0
     out = _outlier_mask(q)
     assert (oracle.dequant(q)[out] == W.double().numpy()[out]).all()
+
+
+def test_int8_packing_is_one_byte_per_code():
+    # 8 bits: the stream's bytes are the codes themselves
+    codes = np.arange(256, dtype=np.uint8)
+    assert oracle.pack(codes, 8).tolist() == codes.tolist()
+    assert oracle.sizes(4096, 4096, 8, 128, 0.0)["packed"] == 4096 * 4096
