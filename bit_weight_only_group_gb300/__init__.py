@@ -39,6 +39,7 @@ ABI_FUNCTIONS = ("qpack_query_sizes", "qpack_workspace_size", "qpack_quantize", 
                  "qgemm_forward", "qgemm_forward_multi", "qgemm_moe_workspace_size", "qgemm_moe_grouped",
                  "qgemm_moe_grouped_multi",
                  "qgemm_device_status", "qgemm_selftest_bounded_wait", "qdiag_workspace_size", "qdiag_layer",
+                 "qgemm_w8a8_workspace_size", "qgemm_forward_w8a8",
                  "qgemm_last_error")
 
 
@@ -84,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.qgemm_device_status.argtypes = [pi32, i32]
         L.qgemm_selftest_bounded_wait.argtypes = [i32, vp]
         L.qdiag_workspace_size.argtypes = [i32, i32, i32, psz]
+        L.qgemm_w8a8_workspace_size.argtypes = [i32, pq, psz]
+        L.qgemm_forward_w8a8.argtypes = [vp, i32, i32, pq, vp, i32, ctypes.c_int, vp, sz, vp]
         L.qdiag_layer.argtypes = [vp, pq, f32, vp, vp, vp, sz, vp]
         L.qgemm_forward_multi.argtypes = [vp, i32, i32, pq, i32, ctypes.POINTER(vp), pi32, ctypes.c_int, vp, sz, vp]
         for name in ABI_FUNCTIONS[:-1]:
@@ -380,3 +383,25 @@ def qdiag_layer(W: torch.Tensor, qw: QWeight, threshold: float = 8.0, ratio: boo
     if ratio:
         o["ratio"] = r
     return o
+
+
+def qgemm_forward_w8a8(x: torch.Tensor, qw: QWeight, out: torch.Tensor | None = None,
+                       out_dtype: torch.dtype = torch.float32, workspace: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """W8A8 decode product (M <= 16): x [M, K] bf16 quantized to int8 per token
+    inside the call, times the 8-bit weight qw."""
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D bfloat16 CUDA tensor with unit inner stride")
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, qw.N), dtype=out_dtype, device=x.device)
+    yt = Y_BF16 if out.dtype == torch.bfloat16 else Y_F32
+    b = ctypes.c_size_t()
+    d = qw.desc()
+    _check(lib().qgemm_w8a8_workspace_size(M, ctypes.byref(d), ctypes.byref(b)), "qgemm_w8a8_workspace_size")
+    if b.value and (workspace is None or workspace.numel() < b.value):
+        workspace = torch.empty(b.value, dtype=torch.uint8, device=x.device)
+    _check(lib().qgemm_forward_w8a8(_ptr(x), M, x.stride(0), ctypes.byref(d), _ptr(out), out.stride(0), yt,
+                                    _ptr(workspace) if b.value else None, workspace.numel() if b.value else 0,
+                                    _stream(stream)), "qgemm_forward_w8a8")
+    return out

@@ -195,6 +195,36 @@ qg_status qgemm_device_status(int32_t* status, int32_t reset)
     return QG_OK;
 }
 
+qg_status qgemm_w8a8_workspace_size(int32_t M, const qg_qweight* w, size_t* bytes)
+{
+    if (!bytes) return fail(QG_ERR_INVALID_ARG, "qgemm_w8a8_workspace_size: bytes is null");
+    qg_status st = check_qweight(w, "qgemm_w8a8_workspace_size");
+    if (st != QG_OK) return st;
+    if (M < 0 || M > kW8A8MaxM) return fail(QG_ERR_UNSUPPORTED, "qgemm_w8a8: M=%d not in 0..%d", M, kW8A8MaxM);
+    *bytes = M ? w8a8_workspace_bytes(M, w->K) : 0;
+    return QG_OK;
+}
+
+qg_status qgemm_forward_w8a8(const uint16_t* x, int32_t M, int32_t ldx, const qg_qweight* w, void* y, int32_t ldy,
+                             qg_ydtype yt, void* ws, size_t ws_bytes, void* stream)
+{
+    qg_status st = check_qweight(w, "qgemm_forward_w8a8");
+    if (st != QG_OK) return st;
+    if (w->bits != 8) return fail(QG_ERR_UNSUPPORTED, "qgemm_forward_w8a8: weights must be 8-bit (bits=%d)", w->bits);
+    if (M < 0 || M > kW8A8MaxM) return fail(QG_ERR_UNSUPPORTED, "qgemm_forward_w8a8: M=%d not in 0..%d", M, kW8A8MaxM);
+    if (M == 0) return QG_OK;
+    if (!x || !y) return fail(QG_ERR_INVALID_ARG, "qgemm_forward_w8a8: x or y is null");
+    if (ldx < w->K || ldy < w->N) return fail(QG_ERR_INVALID_ARG, "qgemm_forward_w8a8: ldx < K or ldy < N");
+    if (yt != QG_Y_F32 && yt != QG_Y_BF16) return fail(QG_ERR_INVALID_ARG, "qgemm_forward_w8a8: bad y dtype");
+    if (!aligned(x, 2) || !aligned(y, yt == QG_Y_F32 ? 4 : 2))
+        return fail(QG_ERR_ALIGNMENT, "qgemm_forward_w8a8: x or y misaligned");
+    const size_t need = w8a8_workspace_bytes(M, w->K);
+    if (!ws || ws_bytes < need)
+        return fail(QG_ERR_WORKSPACE, "qgemm_forward_w8a8: workspace %zu bytes < %zu", ws ? ws_bytes : (size_t)0, need);
+    if (!aligned(ws, 256)) return fail(QG_ERR_ALIGNMENT, "qgemm_forward_w8a8: workspace must be 256-byte aligned");
+    return launch_w8a8(x, M, ldx, *w, y, ldy, yt, ws, static_cast<cudaStream_t>(stream));
+}
+
 qg_status qdiag_workspace_size(int32_t N, int32_t K, int32_t group, size_t* bytes)
 {
     if (!bytes) return fail(QG_ERR_INVALID_ARG, "qdiag_workspace_size: bytes is null");

@@ -84,6 +84,12 @@ qg_status launch_moe_tc(const uint16_t* x, int T, int k, const qg_qweight* exper
                         qg_ydtype yt, const int* offsets, const int* perm, const int2* items, const int* n_items,
                         int max_items, void* x16p, cudaStream_t s);
 
+// ---------------------------------------------------------------- W8A8 (int8 weights and activations)
+constexpr int kW8A8MaxM = 16;
+size_t w8a8_workspace_bytes(int M, int K);
+qg_status launch_w8a8(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy, qg_ydtype yt,
+                      void* ws, cudaStream_t s);
+
 // ---------------------------------------------------------------- diagnostics
 size_t diag_workspace_bytes(int N, int K, int group);
 qg_status launch_diag(const uint16_t* W, const qg_qweight& w, float threshold, float* ratio, qg_diag* out, void* ws,

@@ -249,6 +249,27 @@ QG_API qg_status qgemm_forward_multi(const uint16_t* x, int32_t M, int32_t ldx, 
                                      void* const* ys, const int32_t* ldys, qg_ydtype yt, void* work,
                                      size_t work_bytes, void* stream);
 
+/*
+ * W8A8 product for decode (M <= 16): int8 weights (bits = 8, affine or
+ * symmetric format, FP16 outliers as usual) and int8 activations quantized
+ * dynamically per token inside the call ("Inference acceleration guide"
+ * page, section 1.2: W8A8 quantizes weights and activations to INT8, the
+ * activations per token; section 1.1: the symmetric range [-127, 127]):
+ *   s_m = max_k |x[m,k]| / 127 (fp32; 1 if the maximum is 0),
+ *   q[m,k] = clamp(round(x[m,k] / s_m), -127, 127)  (fp32 division, round half
+ *   to even),
+ *   y[m, n] = sum_k (q[m,k] s_m) * (w_hat[n,k] + S[n,k]).
+ * Integer sums are exact (32-bit four-way int8 dot products on the CUDA
+ * cores: GB300's int8 tensor-core rate is far below its fp16 rate), scales
+ * and outliers are applied in fp32.  x, y, ldx, ldy, yt as qgemm_forward;
+ * `ws` at least qgemm_w8a8_workspace_size bytes (q and s_m), 256-byte aligned.
+ * Errors: QG_ERR_UNSUPPORTED (bits != 8, M > 16), QG_ERR_INVALID_ARG,
+ * QG_ERR_ALIGNMENT, QG_ERR_WORKSPACE, QG_ERR_CUDA.
+ */
+QG_API qg_status qgemm_w8a8_workspace_size(int32_t M, const qg_qweight* w, size_t* bytes);
+QG_API qg_status qgemm_forward_w8a8(const uint16_t* x, int32_t M, int32_t ldx, const qg_qweight* w, void* y,
+                                    int32_t ldy, qg_ydtype yt, void* ws, size_t ws_bytes, void* stream);
+
 /* Workspace bytes qgemm_moe_grouped (and qgemm_moe_grouped_multi with the
  * same T, k, E and experts[0 .. E-1]) needs.  Host-only. */
 QG_API qg_status qgemm_moe_workspace_size(int32_t T, int32_t k, int32_t E, const qg_qweight* experts,

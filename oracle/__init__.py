@@ -82,6 +82,10 @@ def lib():
         L.orc_dequant_rows.restype = ctypes.c_int
         L.orc_linear_rows.argtypes = [vp, i64, i64, ctypes.POINTER(_QW), i64, i64, vp]
         L.orc_linear_rows.restype = ctypes.c_int
+        L.orc_quantize_act_int8.argtypes = [vp, i64, i64, i64, vp, vp]
+        L.orc_quantize_act_int8.restype = ctypes.c_int
+        L.orc_linear_w8a8.argtypes = [vp, i64, i64, i64, ctypes.POINTER(_QW), i64, i64, vp]
+        L.orc_linear_w8a8.restype = ctypes.c_int
         L.orc_diagnostics.argtypes = [vp, ctypes.POINTER(_QW), ctypes.c_double, vp, vp]
         L.orc_diagnostics.restype = ctypes.c_int
         _lib = L
@@ -252,6 +256,33 @@ def linear(x, q: QWeight, n0: int = 0, n1: int | None = None) -> np.ndarray:
     rc = lib().orc_linear_rows(_p(x), M, K, ctypes.byref(s), n0, n1, _p(y))
     if rc != 0:
         raise ValueError(f"orc_linear_rows failed ({rc})")
+    return y
+
+
+def quantize_act_int8(x):
+    """(q int8 [M, K], s fp32 [M]): per-token symmetric INT8 quantization of bf16 x."""
+    x = as_u16(x)
+    if x.ndim == 1:
+        x = x[None, :]
+    M, K = x.shape
+    q = np.empty((M, K), np.int8)
+    s = np.empty(M, np.float32)
+    lib().orc_quantize_act_int8(_p(np.ascontiguousarray(x)), M, K, K, _p(q), _p(s))
+    return q, s
+
+
+def linear_w8a8(x, q: QWeight, n0: int = 0, n1: int | None = None) -> np.ndarray:
+    """y [M, n1-n0] = (int8-quantized x) . (x_hat + S)[n0:n1]^T in fp64."""
+    x = as_u16(x)
+    if x.ndim == 1:
+        x = x[None, :]
+    M, K = x.shape
+    n1 = q.N if n1 is None else n1
+    y = np.empty((M, n1 - n0), np.float64)
+    s = q._struct()
+    rc = lib().orc_linear_w8a8(_p(np.ascontiguousarray(x)), M, K, K, ctypes.byref(s), n0, n1, _p(y))
+    if rc != 0:
+        raise ValueError(f"orc_linear_w8a8 failed ({rc})")
     return y
 
 

@@ -657,3 +657,61 @@ int orc_diagnostics(const uint16_t *W, const orc_qweight *q, double threshold, d
     free(v); free(codes);
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------ */
+/* W8A8: int8 weights and int8 activations                              */
+/* ------------------------------------------------------------------ */
+
+/* Dynamic per-token activation quantizer ("Inference acceleration guide"
+ * page, section 1.2: W8A8 quantizes the activations as well, dynamically
+ * per token; section 1.1: the symmetric INT8 range [-127, 127]).  For token
+ * m: s[m] = max_k |x[m,k]| / 127 in fp32 (1 if the maximum is 0),
+ * q[m,k] = clamp(round(x[m,k] / s[m]), -127, 127), fp32 division, round half
+ * to even. */
+int orc_quantize_act_int8(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int8_t *q, float *s)
+{
+    for (int64_t m = 0; m < M; m++) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; k++) {
+            float a = fabsf((float)orc_bf16_to_f64(x[m * ldx + k]));
+            if (a > amax) amax = a;
+        }
+        float sm = amax == 0.0f ? 1.0f : amax / 127.0f;
+        for (int64_t k = 0; k < K; k++) {
+            float v = rintf((float)orc_bf16_to_f64(x[m * ldx + k]) / sm);
+            if (v < -127.0f) v = -127.0f;
+            if (v > 127.0f) v = 127.0f;
+            q[m * K + k] = (int8_t)v;
+        }
+        s[m] = sm;
+    }
+    return ORC_OK;
+}
+
+/* y[m, n - n0] = sum_k (q[m,k] * s[m]) * (x_hat[n,k] + S[n,k]) in fp64: the
+ * product of the quantized activations with the layer's weight. */
+int orc_linear_w8a8(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, const orc_qweight *w, int64_t n0,
+                    int64_t n1, double *y)
+{
+    if (n0 < 0 || n1 > w->N || n0 > n1 || ldx < w->K || K != w->K) return ORC_EINVAL;
+    int8_t *q = (int8_t *)malloc((size_t)(M * K));
+    float *s = (float *)malloc(sizeof(float) * (size_t)M);
+    double *row = (double *)malloc(sizeof(double) * (size_t)K);
+    uint8_t *codes = (uint8_t *)malloc((size_t)K);
+    if (!q || !s || !row || !codes) {
+        free(q); free(s); free(row); free(codes);
+        return ORC_ENOMEM;
+    }
+    orc_quantize_act_int8(x, M, K, ldx, q, s);
+    int64_t nn = n1 - n0;
+    for (int64_t n = n0; n < n1; n++) {
+        dequant_row(w, n, codes, row);
+        for (int64_t m = 0; m < M; m++) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; k++) acc += ((double)q[m * K + k] * (double)s[m]) * row[k];
+            y[m * nn + (n - n0)] = acc;
+        }
+    }
+    free(q); free(s); free(row); free(codes);
+    return ORC_OK;
+}

@@ -164,6 +164,19 @@ def test_quantize_mode_validation_without_gpu(qg):
     assert L.qpack_quantize_mode(ctypes.c_void_p(0x400002), 0.0, 1, ctypes.byref(d), ws, need, None) == -3
 
 
+def test_w8a8_validation_without_gpu(qg):
+    L = qg.lib()
+    x, y, ws = ctypes.c_void_p(0x300000), ctypes.c_void_p(0x200000), ctypes.c_void_p(0x600000)
+    d4 = _fake_desc(qg, N=64, K=128)
+    d8 = _fake_desc(qg, N=64, K=128, bits=8)
+    need = ctypes.c_size_t()
+    assert L.qgemm_w8a8_workspace_size(4, ctypes.byref(d8), ctypes.byref(need)) == 0 and need.value > 0
+    assert L.qgemm_forward_w8a8(x, 4, 128, ctypes.byref(d4), y, 64, 0, ws, need.value, None) == -2   # not 8-bit
+    assert L.qgemm_forward_w8a8(x, 17, 128, ctypes.byref(d8), y, 64, 0, ws, need.value, None) == -2  # M > 16
+    assert L.qgemm_forward_w8a8(x, 4, 128, ctypes.byref(d8), y, 64, 0, ws, need.value - 1, None) == -4
+    assert L.qgemm_forward_w8a8(x, 0, 128, ctypes.byref(d8), y, 64, 0, None, 0, None) == 0            # no-op
+
+
 def test_diagnostics_validation_without_gpu(qg):
     L = qg.lib()
     d = _fake_desc(qg, N=64, K=1024)

@@ -596,3 +596,36 @@ def test_int8_packing_is_one_byte_per_code():
     codes = np.arange(256, dtype=np.uint8)
     assert oracle.pack(codes, 8).tolist() == codes.tolist()
     assert oracle.sizes(4096, 4096, 8, 128, 0.0)["packed"] == 4096 * 4096
+
+
+# ---------------------------------------------------------------- W8A8
+def _bf16(vals):
+    import torch
+    return torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16)[None, :]
+
+
+def test_activation_int8_hand_worked():
+    # per-token symmetric INT8 ("Inference acceleration guide" page, sections
+    # 1.1-1.2): amax = 127/64 gives scale 1/64 exactly; 3/128 * 64 = 1.5 -> 2
+    # and 1/128 * 64 = 0.5 -> 0 (ties to even)
+    x = _bf16([1.984375, -1.0, 0.5, 0.0234375, 0.0078125, -1.984375, 0.0])
+    q, s = oracle.quantize_act_int8(x)
+    assert s.tolist() == [1 / 64]
+    assert q[0].tolist() == [127, -64, 32, 2, 0, -127, 0]
+    q0, s0 = oracle.quantize_act_int8(_bf16([0.0, 0.0]))
+    assert s0.tolist() == [1.0] and q0.tolist() == [[0, 0]]
+
+
+def test_w8a8_product_is_the_product_of_the_quantized_activations():
+    N, K = 24, 256
+    W = wl.gen_weight(N, K, seed=101, outlier_frac=0.004, outlier_seed=102)
+    qw = oracle.quantize(W, 8, 128, 0.004)
+    x = wl.gen_x(3, K, seed=103)
+    q, s = oracle.quantize_act_int8(x)
+    xhat = q.astype(np.float64) * s[:, None].astype(np.float64)
+    # the same sum two ways: the oracle's W8A8 product, and dequantize-then-matmul
+    assert np.allclose(oracle.linear_w8a8(x, qw), xhat @ oracle.dequant(qw).T, rtol=1e-12, atol=1e-12)
+    # each activation within half a step of its value, the largest at +-127
+    xf = oracle.bf16_to_f64(x)
+    assert (np.abs(xhat - xf) <= s[:, None] * (0.5 + 2.0 ** -20)).all()
+    assert (np.abs(q).max(1) == 127).all()
