@@ -491,20 +491,34 @@ def run_prefill_widths(qg, P):
     y = torch.empty((M, N), dtype=torch.float32, device=dev)
     out = {}
     t_all0 = time.time()
-    for bits in (2, 3, 4, 5, 6):
+    for bits in (2, 3, 4, 5, 6, 8):
         q = qg.qpack_quantize(W, bits, 128, 0.001)
         ws = torch.empty(qg.qgemm_workspace_size(M, q), dtype=torch.uint8, device=dev)
         g = capture(lambda: qg.qgemm_forward(x, q, out=y, workspace=ws))
         ms, n, clocks = timed_object(g, 0.4)
         tf = 2.0 * M * N * K / (ms / 1e3) / 1e12
+        # the same product from the tile-ordered copy (one-time repack, timed once)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t = qg.qrepack_tiles(q)
+        e0.record()
+        qg.qrepack_tiles(q, out=t)
+        e1.record()
+        torch.cuda.synchronize()
+        rp_us = e0.elapsed_time(e1) * 1e3
+        gt = capture(lambda: qg.qgemm_forward_tiles(x, q, t, out=y, workspace=ws))
+        mst, nt, clocks_t = timed_object(gt, 0.4)
+        tft = 2.0 * M * N * K / (mst / 1e3) / 1e12
         out[f"w{bits}"] = {"TFLOP_s": round(tf, 1), "frac_of_bf16_peak": round(tf / P["bf16"], 4),
-                           "us": round(ms * 1e3, 1), "replays": n, "clocks": clocks}
-        del g, q, ws
+                           "us": round(ms * 1e3, 1), "replays": n, "clocks": clocks,
+                           "tiles_TFLOP_s": round(tft, 1), "tiles_frac_of_bf16_peak": round(tft / P["bf16"], 4),
+                           "tiles_us": round(mst * 1e3, 1), "tiles_clocks": clocks_t, "repack_us": round(rp_us, 1)}
+        del g, gt, q, ws, t
     del W
     torch.cuda.empty_cache()
     return {"metric": "qGEMM TFLOP/s at M=2048 by width", "unit": "TFLOP/s", "by_width": out,
             "config": "W 11008x4096 ~N(0,0.02) + 0.1% outliers, group 128, x bf16 [2048, 4096], y fp32; "
-                      "one product per replay (k_x_to_f16 + k_gemm_tc<bits,128>)",
+                      "one product per replay (k_x_to_f16 + k_gemm_tc<bits,128,planar>); tiles_*: the same product "
+                      "from the tile-ordered copy (k_gemm_tc<bits,128,tiles>), repack_us: the one-time repack",
             "seconds": round(time.time() - t_all0, 1)}
 
 

@@ -40,6 +40,7 @@ ABI_FUNCTIONS = ("qpack_query_sizes", "qpack_workspace_size", "qpack_quantize", 
                  "qgemm_moe_grouped_multi",
                  "qgemm_device_status", "qgemm_selftest_bounded_wait", "qdiag_workspace_size", "qdiag_layer",
                  "qgemm_w8a8_workspace_size", "qgemm_forward_w8a8",
+                 "qrepack_tiles_size", "qrepack_tiles", "qgemm_tiles_workspace_size", "qgemm_forward_tiles",
                  "qgemm_last_error")
 
 
@@ -86,6 +87,10 @@ def lib() -> ctypes.CDLL:
         L.qgemm_selftest_bounded_wait.argtypes = [i32, vp]
         L.qdiag_workspace_size.argtypes = [i32, i32, i32, psz]
         L.qgemm_w8a8_workspace_size.argtypes = [i32, pq, psz]
+        L.qrepack_tiles_size.argtypes = [pq, psz]
+        L.qrepack_tiles.argtypes = [pq, vp, sz, vp]
+        L.qgemm_tiles_workspace_size.argtypes = [i32, pq, psz]
+        L.qgemm_forward_tiles.argtypes = [vp, i32, i32, pq, vp, vp, i32, ctypes.c_int, vp, sz, vp]
         L.qgemm_forward_w8a8.argtypes = [vp, i32, i32, pq, vp, i32, ctypes.c_int, vp, sz, vp]
         L.qdiag_layer.argtypes = [vp, pq, f32, vp, vp, vp, sz, vp]
         L.qgemm_forward_multi.argtypes = [vp, i32, i32, pq, i32, ctypes.POINTER(vp), pi32, ctypes.c_int, vp, sz, vp]
@@ -404,4 +409,36 @@ def qgemm_forward_w8a8(x: torch.Tensor, qw: QWeight, out: torch.Tensor | None = 
     _check(lib().qgemm_forward_w8a8(_ptr(x), M, x.stride(0), ctypes.byref(d), _ptr(out), out.stride(0), yt,
                                     _ptr(workspace) if b.value else None, workspace.numel() if b.value else 0,
                                     _stream(stream)), "qgemm_forward_w8a8")
+    return out
+
+
+def qrepack_tiles(qw: QWeight, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The tile-ordered copy of qw (uint8 CUDA tensor) for qgemm_forward_tiles."""
+    b = ctypes.c_size_t()
+    d = qw.desc()
+    _check(lib().qrepack_tiles_size(ctypes.byref(d), ctypes.byref(b)), "qrepack_tiles_size")
+    if out is None:
+        out = torch.empty(b.value, dtype=torch.uint8, device=qw.packed.device)
+    _check(lib().qrepack_tiles(ctypes.byref(d), _ptr(out), out.numel(), _stream(stream)), "qrepack_tiles")
+    return out
+
+
+def qgemm_forward_tiles(x: torch.Tensor, qw: QWeight, tiles: torch.Tensor, out: torch.Tensor | None = None,
+                        out_dtype: torch.dtype = torch.float32, workspace: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """y = x . (dequant(W) + outliers)^T on the tensor cores from the tile-ordered copy."""
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D bfloat16 CUDA tensor with unit inner stride")
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, qw.N), dtype=out_dtype, device=x.device)
+    yt = Y_BF16 if out.dtype == torch.bfloat16 else Y_F32
+    d = qw.desc()
+    b = ctypes.c_size_t()
+    _check(lib().qgemm_tiles_workspace_size(M, ctypes.byref(d), ctypes.byref(b)), "qgemm_tiles_workspace_size")
+    if b.value and (workspace is None or workspace.numel() < b.value):
+        workspace = torch.empty(b.value, dtype=torch.uint8, device=x.device)
+    _check(lib().qgemm_forward_tiles(_ptr(x), M, x.stride(0), ctypes.byref(d), _ptr(tiles), _ptr(out), out.stride(0),
+                                     yt, _ptr(workspace) if b.value else None, workspace.numel() if b.value else 0,
+                                     _stream(stream)), "qgemm_forward_tiles")
     return out

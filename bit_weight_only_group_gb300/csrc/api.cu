@@ -195,6 +195,56 @@ qg_status qgemm_device_status(int32_t* status, int32_t reset)
     return QG_OK;
 }
 
+qg_status qrepack_tiles_size(const qg_qweight* w, size_t* bytes)
+{
+    if (!bytes) return fail(QG_ERR_INVALID_ARG, "qrepack_tiles_size: bytes is null");
+    qg_status st = check_qweight(w, "qrepack_tiles_size");
+    if (st != QG_OK) return st;
+    *bytes = tiles_bytes(*w);
+    return QG_OK;
+}
+
+qg_status qrepack_tiles(const qg_qweight* w, void* tiles, size_t tiles_bytes_given, void* stream)
+{
+    qg_status st = check_qweight(w, "qrepack_tiles");
+    if (st != QG_OK) return st;
+    if (!tiles) return fail(QG_ERR_INVALID_ARG, "qrepack_tiles: tiles is null");
+    if (!aligned(tiles, 128)) return fail(QG_ERR_ALIGNMENT, "qrepack_tiles: tiles must be 128-byte aligned");
+    if (tiles_bytes_given < tiles_bytes(*w))
+        return fail(QG_ERR_INVALID_ARG, "qrepack_tiles: %zu bytes < %zu", tiles_bytes_given, tiles_bytes(*w));
+    if (!aligned(w->packed, 4)) return fail(QG_ERR_ALIGNMENT, "qrepack_tiles: packed misaligned");
+    return launch_repack(*w, tiles, static_cast<cudaStream_t>(stream));
+}
+
+qg_status qgemm_tiles_workspace_size(int32_t M, const qg_qweight* w, size_t* bytes)
+{
+    if (!bytes) return fail(QG_ERR_INVALID_ARG, "qgemm_tiles_workspace_size: bytes is null");
+    qg_status st = check_qweight(w, "qgemm_tiles_workspace_size");
+    if (st != QG_OK) return st;
+    if (M < 0) return fail(QG_ERR_INVALID_ARG, "qgemm_tiles_workspace_size: M < 0");
+    *bytes = M ? gemm_workspace_bytes(M, *w) : 0;
+    return QG_OK;
+}
+
+qg_status qgemm_forward_tiles(const uint16_t* x, int32_t M, int32_t ldx, const qg_qweight* w, const void* tiles,
+                              void* y, int32_t ldy, qg_ydtype yt, void* ws, size_t ws_bytes, void* stream)
+{
+    qg_status st = check_qweight(w, "qgemm_forward_tiles");
+    if (st != QG_OK) return st;
+    if (M < 0) return fail(QG_ERR_INVALID_ARG, "qgemm_forward_tiles: M < 0");
+    if (M == 0) return QG_OK;
+    if (!x || !y || !tiles) return fail(QG_ERR_INVALID_ARG, "qgemm_forward_tiles: x, y or tiles is null");
+    if (ldx < w->K || ldy < w->N) return fail(QG_ERR_INVALID_ARG, "qgemm_forward_tiles: ldx < K or ldy < N");
+    if (yt != QG_Y_F32 && yt != QG_Y_BF16) return fail(QG_ERR_INVALID_ARG, "qgemm_forward_tiles: bad y dtype");
+    if (!aligned(x, 2) || !aligned(y, yt == QG_Y_F32 ? 4 : 2) || !aligned(tiles, 128))
+        return fail(QG_ERR_ALIGNMENT, "qgemm_forward_tiles: x, y or tiles misaligned");
+    const size_t need = gemm_workspace_bytes(M, *w);
+    if (!ws || ws_bytes < need)
+        return fail(QG_ERR_WORKSPACE, "qgemm_forward_tiles: workspace %zu bytes < %zu", ws ? ws_bytes : (size_t)0, need);
+    if (!aligned(ws, 256)) return fail(QG_ERR_ALIGNMENT, "qgemm_forward_tiles: workspace must be 256-byte aligned");
+    return launch_gemm_tiles(x, M, ldx, *w, tiles, y, ldy, yt, ws, static_cast<cudaStream_t>(stream));
+}
+
 qg_status qgemm_w8a8_workspace_size(int32_t M, const qg_qweight* w, size_t* bytes)
 {
     if (!bytes) return fail(QG_ERR_INVALID_ARG, "qgemm_w8a8_workspace_size: bytes is null");

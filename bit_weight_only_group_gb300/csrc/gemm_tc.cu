@@ -85,15 +85,21 @@ constexpr int kThreads = (kDeqWarps + 3) * 32;
 constexpr int A_BYTES = BM * BK * 2;   // 32 KB fp16
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB fp16
 
-template <int BITS>
+// TILES: the codes and group parameters come from the tile-ordered copy
+// (one contiguous block per 256 rows x 64 k, staged by one bulk copy).
+template <int BITS, bool TILES>
 struct Cfg {
-    static constexpr bool TMA_CODES = BITS == 4;
-    static constexpr int SB = TMA_CODES ? 3 : 4;                        // fp16 weight tiles
-    static constexpr int P_BYTES = TMA_CODES ? BN * PK * BK * BITS / 8 : 0;   // 256 rows x 128 bytes
-    static constexpr int P_ALIGNED = (P_BYTES + 1023) / 1024 * 1024;
+    static constexpr bool TMA_CODES = BITS == 4 && !TILES;
+    static constexpr int SB = TILES || TMA_CODES ? 3 : 4;               // fp16 weight tiles
+    static constexpr int BLOCK = 2048 * BITS + (BITS == 2 ? 2048 : 1024);   // one tile-ordered block
+    static constexpr int P_BYTES = TMA_CODES ? BN * PK * BK * BITS / 8 : TILES ? BLOCK : 0;
+    static constexpr int P_ALIGNED = TMA_CODES ? (P_BYTES + 1023) / 1024 * 1024 : (P_BYTES + 127) / 128 * 128;
     static constexpr int OFF_B = SA * A_BYTES;
     static constexpr int OFF_P = OFF_B + SB * B_BYTES;
-    static constexpr int OFF_BAR = OFF_P + SP * P_ALIGNED;
+    static constexpr int SP_FIT = TILES ? (227 * 1024 - 2048 - OFF_P) / P_ALIGNED : 0;
+    static constexpr int SPN = TMA_CODES ? SP : TILES ? (SP_FIT < 6 ? SP_FIT : 6) : 1;   // packed ring depth
+    static_assert(!TILES || SPN >= 2, "tile ring of at least two blocks");
+    static constexpr int OFF_BAR = OFF_P + (TMA_CODES || TILES ? SPN : 0) * P_ALIGNED;
     static constexpr int OFF_EROW = OFF_BAR + 512;                      // per-row exponents (256 bytes)
     static constexpr int SMEM = OFF_BAR + 1024 /* barriers, exponents */ + 1024 /* alignment */;
 };
@@ -101,6 +107,7 @@ struct Cfg {
 struct Args {
     int M, N, K, ng;
     const uint8_t* packed;   // codes (read directly at widths other than 4)
+    const uint8_t* tiles;    // tile-ordered copy (TILES kernels)
     const uint16_t* scale;
     const uint8_t* zp;
     const uint2* cb;         // 2-bit codebooks: 4 fp16 entries per group
@@ -117,13 +124,14 @@ struct Args {
 
 static_assert(kDeqWarps * 32 == 512, "deq_sync counts 512 dequantization threads");
 
-template <int BITS, int G>
+template <int BITS, int G, bool TILES>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
               const __grid_constant__ Args a)
 {
-    using C = Cfg<BITS>;
+    using C = Cfg<BITS, TILES>;
     constexpr int SB = C::SB;
+    constexpr int SP = C::SPN;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_u32(smem);
@@ -148,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SA; s++) { ptx::mbar_init(full_a(s), 1); ptx::mbar_init(empty_a(s), 1); }
-        if constexpr (C::TMA_CODES)
+        if constexpr (C::TMA_CODES || TILES)
             for (int s = 0; s < SP; s++) { ptx::mbar_init(full_p(s), 1); ptx::mbar_init(empty_p(s), kDeqWarps); }
         for (int s = 0; s < SB; s++) { ptx::mbar_init(full_b(s), kDeqWarps); ptx::mbar_init(empty_b(s), 1); }
         ptx::mbar_init(acc_full, 1);
@@ -191,6 +199,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ptx::mbar_wait(empty_p(s), ph ^ 1u)) { ok = false; break; }
                     ptx::mbar_expect_tx(full_p(s), C::P_BYTES);
                     ptx::tma_load_2d(ptx::smem_u32(p_tile(s)), &wmap, kp * (PK * BK * BITS / 8), n0, full_p(s));
+                    if (++s == SP) { s = 0; ph ^= 1u; }
+                }
+            }
+        } else if constexpr (TILES) {
+            // one bulk copy per K block: the block of this CTA's 256-row tile
+            if (lane == 0) {
+                const uint8_t* base = a.tiles + (size_t)blockIdx.y * KB * C::BLOCK;
+                int s = 0;
+                uint32_t ph = 0;
+                for (int kb = 0; kb < KB; kb++) {
+                    if (!ptx::mbar_wait(empty_p(s), ph ^ 1u)) { ok = false; break; }
+                    ptx::mbar_expect_tx(full_p(s), C::BLOCK);
+                    ptx::bulk_load(ptx::smem_u32(p_tile(s)), base + (size_t)kb * C::BLOCK, C::BLOCK, full_p(s));
                     if (++s == SP) { s = 0; ph ^= 1u; }
                 }
             }
@@ -244,9 +265,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (BITS == 2) return __ldg(cb_row + gi);
             else return make_uint2(f16_times_pow2(__ldg(sp_row + gi), ex), (uint32_t)__ldg(zp_row + gi));
         };
-        prm[0] = load_prm(0);
-        prm[1] = ng > 1 ? load_prm(1) : make_uint2(0u, 0u);
-        prm[2] = ng > 2 ? load_prm(2) : make_uint2(0u, 0u);
+        if constexpr (!TILES) {
+            prm[0] = load_prm(0);
+            prm[1] = ng > 1 ? load_prm(1) : make_uint2(0u, 0u);
+            prm[2] = ng > 2 ? load_prm(2) : make_uint2(0u, 0u);
+        }
         // outlier cursor of this row: the next entry (ocol, oval) and the one
         // after it (ncol, nval), so that consuming an entry never waits for a load
         int op = 0, oe = 0, ocol = 0x7FFFFFFF, ncol = 0x7FFFFFFF;
@@ -316,7 +339,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
 
-        if constexpr (C::TMA_CODES) {
+        if constexpr (TILES) {
+            // codes and parameters of block kb from the tile ring: word i of
+            // this thread's chunk at word i * 512 + threadIdx.x, the row's
+            // parameters after the 512 * BITS code words
+            int sp = 0;
+            uint32_t pp = 0;   // parity of full_p to wait for
+            for (int kb = 0; kb < KB && ok; kb++) {
+                if (!ptx::mbar_wait(full_p(sp), pp)) { ok = false; break; }
+                const uint32_t* pw = reinterpret_cast<const uint32_t*>(p_tile(sp));
+                uint32_t w[BITS];
+#pragma unroll
+                for (int i = 0; i < BITS; i++) w[i] = pw[i * 512 + threadIdx.x];
+                uint32_t pr[16];
+                if constexpr (BITS == 2) {
+                    const uint2 c = reinterpret_cast<const uint2*>(pw + BITS * 512)[r];
+                    const uint32_t lo = __byte_perm(c.x, c.y, 0x6420), hi = __byte_perm(c.x, c.y, 0x7531);
+#pragma unroll
+                    for (int wi = 0; wi < 2; wi++)
+#pragma unroll
+                        for (int jf = 0; jf < 4; jf++) {
+                            const uint32_t f = (w[wi] >> (2 * jf)) & 0x03030303u;
+                            pr[2 * (4 * wi + jf)] = cb_pair<0>(f, lo, hi);
+                            pr[2 * (4 * wi + jf) + 1] = cb_pair<1>(f, lo, hi);
+                        }
+                } else {
+                    const uint32_t pq = pw[BITS * 512 + r];
+                    const uint32_t s2 = __byte_perm(f16_times_pow2(pq & 0xFFFFu, ex), 0u, 0x1010u);
+                    const uint32_t zq = pq >> 16;
+                    gemv::static_for<0, 16>([&](auto ec) {
+                        constexpr int e = decltype(ec)::value;
+                        pr[e] = hmul2_u32(gemv::deq_affine<BITS, 32, e>(w, zq, magic), s2);
+                    });
+                }
+                if (!emit(kb, pr)) { ok = false; break; }
+                // the block goes back to its producer after the shared loads
+                // that read it completed (emit synchronized the warp)
+                if (lane == 0) ptx::mbar_arrive(empty_p(sp));
+                if (++sp == SP) { sp = 0; pp ^= 1u; }
+            }
+        } else if constexpr (C::TMA_CODES) {
             // 4 bits: codes come from the TMA ring (source chunk 2*sub + hk of the packed row)
             uint32_t src_off[PK];
 #pragma unroll
@@ -516,11 +578,11 @@ size_t ws_layout(int M, int K, Ws* w, void* base)
     return total;
 }
 
-template <int BITS, int G>
-qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy, qg_ydtype yt, void* ws,
-              cudaStream_t s)
+template <int BITS, int G, bool TILES>
+qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void* tiles, void* y, int ldy,
+              qg_ydtype yt, void* ws, cudaStream_t s)
 {
-    using C = Cfg<BITS>;
+    using C = Cfg<BITS, TILES>;
     Ws p{};
     ws_layout(M, w.K, &p, ws);
     {
@@ -542,27 +604,29 @@ qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, i
     Args a;
     a.M = M; a.N = w.N; a.K = w.K; a.ng = w.K / G;
     a.packed = w.packed;
+    a.tiles = static_cast<const uint8_t*>(tiles);
     a.scale = w.scale; a.zp = w.zp; a.cb = reinterpret_cast<const uint2*>(w.codebook);
     a.row_ptr = w.out_row_ptr; a.col = w.out_col; a.val = w.out_val; a.nnz = w.nnz;
     a.y = y; a.ldy = ldy; a.y_bf16 = yt == QG_Y_BF16;
     a.status = device_status_ptr();
     a.magic = gemv::kF16Magic;
     {
-        qg_status st2 = gemv::allow_smem(k_gemm_tc<BITS, G>, C::SMEM);
+        qg_status st2 = gemv::allow_smem(k_gemm_tc<BITS, G, TILES>, C::SMEM);
         if (st2 != QG_OK) return st2;
     }
     dim3 grid((unsigned)ceil_div(M, BM), (unsigned)ceil_div(w.N, BN), 1);
-    k_gemm_tc<BITS, G><<<grid, kThreads, C::SMEM, s>>>(xmap, wmap, a);
+    k_gemm_tc<BITS, G, TILES><<<grid, kThreads, C::SMEM, s>>>(xmap, wmap, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
     return QG_OK;
 }
 
-template <int BITS>
-qg_status run_bits(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy, qg_ydtype yt, void* ws,
-                   cudaStream_t s)
+template <int BITS, bool TILES>
+qg_status run_bits(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void* tiles, void* y, int ldy,
+                   qg_ydtype yt, void* ws, cudaStream_t s)
 {
-    return w.group == 64 ? run<BITS, 64>(x, M, ldx, w, y, ldy, yt, ws, s) : run<BITS, 128>(x, M, ldx, w, y, ldy, yt, ws, s);
+    return w.group == 64 ? run<BITS, 64, TILES>(x, M, ldx, w, tiles, y, ldy, yt, ws, s)
+                         : run<BITS, 128, TILES>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
 }
 
 }  // namespace tc
@@ -573,12 +637,25 @@ qg_status launch_gemm(const uint16_t* x, int M, int ldx, const qg_qweight& w, vo
                       void* ws, size_t, cudaStream_t s)
 {
     switch (w.bits) {
-        case 2: return tc::run_bits<2>(x, M, ldx, w, y, ldy, yt, ws, s);
-        case 3: return tc::run_bits<3>(x, M, ldx, w, y, ldy, yt, ws, s);
-        case 4: return tc::run_bits<4>(x, M, ldx, w, y, ldy, yt, ws, s);
-        case 5: return tc::run_bits<5>(x, M, ldx, w, y, ldy, yt, ws, s);
-        case 6: return tc::run_bits<6>(x, M, ldx, w, y, ldy, yt, ws, s);
-        default: return tc::run_bits<8>(x, M, ldx, w, y, ldy, yt, ws, s);
+        case 2: return tc::run_bits<2, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, s);
+        case 3: return tc::run_bits<3, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, s);
+        case 4: return tc::run_bits<4, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, s);
+        case 5: return tc::run_bits<5, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, s);
+        case 6: return tc::run_bits<6, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, s);
+        default: return tc::run_bits<8, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, s);
+    }
+}
+
+qg_status launch_gemm_tiles(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void* tiles, void* y,
+                            int ldy, qg_ydtype yt, void* ws, cudaStream_t s)
+{
+    switch (w.bits) {
+        case 2: return tc::run_bits<2, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
+        case 3: return tc::run_bits<3, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
+        case 4: return tc::run_bits<4, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
+        case 5: return tc::run_bits<5, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
+        case 6: return tc::run_bits<6, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
+        default: return tc::run_bits<8, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
     }
 }
 

@@ -39,8 +39,11 @@ qg_status launch_quantize(const uint16_t* W, float frac, const qg_qweight& w, vo
                           cudaStream_t s, int mode = 0);
 
 // ---------------------------------------------------------------- decode GEMV
-// Largest M the register-dequant kernel handles in one pass.
-constexpr int kGemvMaxM = 64;
+// Largest M the register-dequant (decode) kernel takes; above it the
+// tensor-core kernel runs.  Measured on the 70B-shaped stack: at M = 32 the
+// decode kernel takes 13.3 ms per 20 layers against 20.8 ms on the tensor
+// cores, at M = 64 27.5 ms against 21.0 ms.
+constexpr int kGemvMaxM = 32;
 qg_status launch_gemv(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,
                       qg_ydtype yt, cudaStream_t s);
 
@@ -61,6 +64,22 @@ qg_status launch_gemv_multi(const uint16_t* x, int M, int ldx, const qg_qweight*
 size_t gemm_workspace_bytes(int M, const qg_qweight& w);
 qg_status launch_gemm(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,
                       qg_ydtype yt, void* ws, size_t ws_bytes, cudaStream_t s);
+
+// Tile-ordered copy of a quantized weight for the tensor-core kernel: for
+// every 256-row tile and 64-wide K block, one contiguous block of the
+// block's codes (word i of dequantization thread t = 2 * row + half at word
+// i * 512 + t) followed by its group parameters (one 32-bit word per row:
+// fp16 scale | zero-point << 16; at 2 bits the row's 4 fp16 codebook
+// entries), blocks in (row tile, K block) order.  Rows beyond N are zero.
+constexpr int kTileRows = 256, kTileK = 64;
+__host__ __device__ constexpr size_t tile_block_bytes(int bits) { return (size_t)2048 * bits + (bits == 2 ? 2048 : 1024); }
+inline size_t tiles_bytes(const qg_qweight& w)
+{
+    return (size_t)ceil_div(w.N, kTileRows) * (size_t)(w.K / kTileK) * tile_block_bytes(w.bits);
+}
+qg_status launch_repack(const qg_qweight& w, void* tiles, cudaStream_t s);
+qg_status launch_gemm_tiles(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void* tiles, void* y,
+                            int ldy, qg_ydtype yt, void* ws, cudaStream_t s);
 
 // ---------------------------------------------------------------- grouped MoE
 constexpr int kMoeMaxExperts = 256;

@@ -1,0 +1,73 @@
+// One-time device repack of a quantized weight into the tile-ordered layout
+// the tensor-core kernel streams ("Mixed-width quantization" page, sections
+// 3.1 and 3.3: codes laid out for aligned vector access, the scales beside
+// the codes they scale; "70B on one GPU" page, section 3: weights repacked
+// once, when loaded, for the fused kernel).  Every (256-row tile, 64-wide K
+// block) becomes one contiguous block starting on a 128-byte boundary:
+//   codes   4 * bits words per row pair ... word i of dequantization thread
+//           t = 2 * row + half (codes [32 half, 32 half + 32) of the row in
+//           this K block, LSB-first as in the planar stream) at word
+//           i * 512 + t: a warp's 32 threads read 32 consecutive words;
+//   params  one 32-bit word per row (fp16 scale | zero-point << 16), or at
+//           2 bits the row's four fp16 codebook entries (8 bytes);
+// rows beyond N are zero.  The FP16 outliers stay in their CSR arrays.
+// One CTA of 512 threads per block; a thread moves its chunk's words and
+// (on even threads) the row's parameters.
+#include "qg_internal.h"
+
+namespace qg {
+namespace {
+
+template <int BITS>
+__global__ void __launch_bounds__(512) k_repack(const uint8_t* __restrict__ packed, const uint16_t* __restrict__ scale,
+                                                const uint8_t* __restrict__ zp, const uint2* __restrict__ cb, int N,
+                                                int K, int G, uint8_t* __restrict__ tiles)
+{
+    const int kb = blockIdx.x, nt = blockIdx.y, KB = K / kTileK;
+    const int t = threadIdx.x, r = t >> 1, h = t & 1;
+    const int n = nt * kTileRows + r;
+    uint32_t* blk = reinterpret_cast<uint32_t*>(tiles + ((size_t)nt * KB + kb) * tile_block_bytes(BITS));
+    const bool live = n < N;
+    // the chunk: 4 * BITS bytes at byte (2 kb + h) * 4 * BITS of the row (word aligned)
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(packed + (size_t)n * ((size_t)K * BITS / 8) +
+                                                            (size_t)(2 * kb + h) * 4 * BITS);
+#pragma unroll
+    for (int i = 0; i < BITS; i++) blk[i * 512 + t] = live ? __ldg(src + i) : 0u;
+    if (h == 0) {
+        const int g = kb * kTileK / G, ng = K / G;
+        uint32_t* prm = blk + BITS * 512;
+        if constexpr (BITS == 2) {
+            reinterpret_cast<uint2*>(prm)[r] = live ? __ldg(cb + (size_t)n * ng + g) : make_uint2(0u, 0u);
+        } else {
+            prm[r] = live ? ((uint32_t)__ldg(scale + (size_t)n * ng + g) | ((uint32_t)__ldg(zp + (size_t)n * ng + g) << 16))
+                          : 0u;
+        }
+    }
+}
+
+template <int BITS>
+qg_status repack_bits(const qg_qweight& w, void* tiles, cudaStream_t s)
+{
+    const dim3 grid((unsigned)(w.K / kTileK), (unsigned)ceil_div(w.N, kTileRows));
+    k_repack<BITS><<<grid, 512, 0, s>>>(w.packed, w.scale, w.zp, reinterpret_cast<const uint2*>(w.codebook), w.N,
+                                        w.K, w.group, static_cast<uint8_t*>(tiles));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "repack kernel launch");
+    return QG_OK;
+}
+
+}  // namespace
+
+qg_status launch_repack(const qg_qweight& w, void* tiles, cudaStream_t s)
+{
+    switch (w.bits) {
+        case 2: return repack_bits<2>(w, tiles, s);
+        case 3: return repack_bits<3>(w, tiles, s);
+        case 4: return repack_bits<4>(w, tiles, s);
+        case 5: return repack_bits<5>(w, tiles, s);
+        case 6: return repack_bits<6>(w, tiles, s);
+        default: return repack_bits<8>(w, tiles, s);
+    }
+}
+
+}  // namespace qg

@@ -211,7 +211,7 @@ QG_API qg_status qgemm_workspace_size(int32_t M, const qg_qweight* w, size_t* by
  *   x   bf16 [M, K] row-major with row stride ldx >= K elements (DEVICE).
  *   y   [M, N] row-major with row stride ldy >= N elements, fp32 or bf16
  *       per `yt` (DEVICE).
- * M = 0 is a no-op.  M <= 64 runs the decode kernel (register dequant, split
+ * M = 0 is a no-op.  M <= 32 runs the decode kernel (register dequant, split
  * K across a thread-block cluster); larger M runs the tensor-core kernel
  * (tcgen05 with TMEM accumulators), which converts x to fp16 in the workspace.
  * `ws` may be NULL when qgemm_workspace_size reports 0.
@@ -235,7 +235,7 @@ QG_API qg_status qgemm_forward(const uint16_t* x, int32_t M, int32_t ldx, const 
  * The pages define the single product ("70B on one GPU" page, sections
  * 2-3); this call computes exactly that product for each weight, so each
  * ys[q] equals what qgemm_forward would write for ws[q].  In the decode range
- * (M <= 64) all n products run as one kernel launch over their concatenated
+ * (M <= 32) all n products run as one kernel launch over their concatenated
  * row tiles; above it they run one after the other on the tensor cores in
  * the caller's workspace (size: the largest qgemm_workspace_size of the ws).
  *   x     bf16 [M, K], row stride ldx >= K (DEVICE), shared by all products.
@@ -248,6 +248,43 @@ QG_API qg_status qgemm_forward(const uint16_t* x, int32_t M, int32_t ldx, const 
 QG_API qg_status qgemm_forward_multi(const uint16_t* x, int32_t M, int32_t ldx, const qg_qweight* ws, int32_t n,
                                      void* const* ys, const int32_t* ldys, qg_ydtype yt, void* work,
                                      size_t work_bytes, void* stream);
+
+/*
+ * One-time device repack into the tile-ordered layout the tensor-core
+ * (prefill) kernel streams ("Mixed-width quantization" page, sections 3.1
+ * and 3.3: codes laid out for aligned vector access, the scales next to the
+ * codes they scale -- misalignment costs 5-15 %, cache-line-aligned scales
+ * gain about 8 %; "70B on one GPU" page, section 3: the weights are
+ * repacked once, when the model is loaded, for the fused kernel).
+ * Layout: for every 256-row tile (rows n0 .. n0+255) and 64-wide K block kb,
+ * one contiguous block of tile_block_bytes(bits) = 2048*bits + (bits == 2 ?
+ * 2048 : 1024) bytes, at byte (tile * (K/64) + kb) * tile_block_bytes:
+ *   words [0, 512*bits): word i of thread t = 2*r + h at word i*512 + t,
+ *     where the thread's chunk is the 32 codes [64 kb + 32 h, 64 kb + 32 h +
+ *     32) of row n0 + r as 4*bits bytes of the planar LSB-first stream;
+ *   then per row r: one 32-bit word fp16 scale | zero-point << 16 of the
+ *     group holding the block (bits != 2), or the group's 4 fp16 codebook
+ *     entries (8 bytes, bits == 2).
+ * Rows beyond N are zero.  Every block starts on a 128-byte boundary, so
+ * the kernel stages one block with one bulk copy and reads codes and
+ * parameters from shared memory.  The outlier CSR stays in the descriptor.
+ */
+QG_API qg_status qrepack_tiles_size(const qg_qweight* w, size_t* bytes);
+/* Writes the tile-ordered copy of w into `tiles` (DEVICE, 128-byte aligned,
+ * at least qrepack_tiles_size bytes), stream-ordered.  w is unchanged.
+ * Errors: QG_ERR_INVALID_ARG, QG_ERR_ALIGNMENT, QG_ERR_CUDA. */
+QG_API qg_status qrepack_tiles(const qg_qweight* w, void* tiles, size_t tiles_bytes, void* stream);
+/* Workspace bytes qgemm_forward_tiles needs for M rows of x.  Host-only. */
+QG_API qg_status qgemm_tiles_workspace_size(int32_t M, const qg_qweight* w, size_t* bytes);
+/* qgemm_forward on the tensor cores with the codes and group parameters
+ * read from the tile-ordered copy `tiles` of w (made by qrepack_tiles from
+ * the same w); w supplies the shape, the scales (for the per-row operand
+ * exponent) and the outlier CSR.  Any M >= 1 (every M runs the tensor-core
+ * kernel).  Same result as qgemm_forward's tensor-core path, bit for bit.
+ * Errors: QG_ERR_INVALID_ARG, QG_ERR_ALIGNMENT, QG_ERR_WORKSPACE, QG_ERR_CUDA. */
+QG_API qg_status qgemm_forward_tiles(const uint16_t* x, int32_t M, int32_t ldx, const qg_qweight* w,
+                                     const void* tiles, void* y, int32_t ldy, qg_ydtype yt, void* ws,
+                                     size_t ws_bytes, void* stream);
 
 /*
  * W8A8 product for decode (M <= 16): int8 weights (bits = 8, affine or

@@ -286,6 +286,37 @@ def linear_w8a8(x, q: QWeight, n0: int = 0, n1: int | None = None) -> np.ndarray
     return y
 
 
+def tiles(q: QWeight) -> np.ndarray:
+    """The tile-ordered copy of q, written out block by block from the planar
+    arrays: for each 256-row tile and 64-wide K block, 512 * bits words (word
+    i of thread t = 2r + h at i * 512 + t, the thread's chunk being the 32
+    codes [64 kb + 32 h, 64 kb + 32 h + 32) of row r as 4 * bits bytes of the
+    LSB-first stream), then per row the group's parameter word (fp16 scale |
+    zp << 16) or, at 2 bits, its 4 fp16 codebook entries.  Rows past N stay 0."""
+    b, K, N = q.bits, q.K, q.N
+    KB, NT = K // 64, (N + 255) // 256
+    blk = 2048 * b + (2048 if b == 2 else 1024)
+    out = np.zeros(NT * KB * blk, np.uint8)
+    for nt in range(NT):
+        for kb in range(KB):
+            base = (nt * KB + kb) * blk
+            words = out[base:base + 2048 * b].view(np.uint32).reshape(b, 512)
+            prm = out[base + 2048 * b:base + blk]
+            g = kb * 64 // q.group
+            for r in range(256):
+                n = nt * 256 + r
+                if n >= N:
+                    continue
+                for h in range(2):
+                    lo = (2 * kb + h) * 4 * b
+                    words[:, 2 * r + h] = q.packed[n, lo:lo + 4 * b].view(np.uint32)
+                if b == 2:
+                    prm[8 * r:8 * r + 8] = q.cb[n, g].view(np.uint8)
+                else:
+                    prm[4 * r:4 * r + 4] = np.array([int(q.scale[n, g]) | (int(q.zp[n, g]) << 16)], np.uint32).view(np.uint8)
+    return out
+
+
 def diagnostics(W, q: QWeight, threshold: float = 8.0):
     """Per-layer diagnostics of q against the original fp16 W: dict with
     max_abs_err, rmse, cosine, max_range_ratio, groups_over (threshold) and

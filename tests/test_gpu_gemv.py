@@ -43,7 +43,7 @@ def test_product_small(qg, bits, group, M):
 
 
 @pytest.mark.parametrize("bits", [2, 4, 6])
-@pytest.mark.parametrize("M", [65, 130])
+@pytest.mark.parametrize("M", [33, 64, 65, 130])
 def test_product_above_decode_range(qg, bits, M):
     N, K = 136, 512
     q, wmax = _weights(N, K, bits, 128, 0.002, seed=5)

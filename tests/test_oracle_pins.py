@@ -629,3 +629,37 @@ def test_w8a8_product_is_the_product_of_the_quantized_activations():
     xf = oracle.bf16_to_f64(x)
     assert (np.abs(xhat - xf) <= s[:, None] * (0.5 + 2.0 ** -20)).all()
     assert (np.abs(q).max(1) == 127).all()
+
+
+# ---------------------------------------------------------------- tile-ordered copy
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
+def test_tiles_layout_reads_back_every_code_and_parameter(bits):
+    # read the layout back with the thread/word formula and compare with the
+    # planar stream unpacked by the generic bit loop: every code of every row
+    # (ragged last tile) and the group parameters land where stated
+    N, K, group = 300, 256, 128
+    q = oracle.quantize(wl.gen_weight(N, K, seed=bits), bits, group, 0.0)
+    t = oracle.tiles(q)
+    blk = 2048 * bits + (2048 if bits == 2 else 1024)
+    KB = K // 64
+    assert t.size == ((N + 255) // 256) * KB * blk
+    for n in (0, 1, 255, 256, 299):
+        nt, r = divmod(n, 256)
+        row = oracle.unpack(q.packed[n], K, bits)
+        for kb in range(KB):
+            base = (nt * KB + kb) * blk
+            words = t[base:base + 2048 * bits].view(np.uint32).reshape(bits, 512)
+            for h in range(2):
+                chunk = words[:, 2 * r + h].astype(np.uint32).view(np.uint8)
+                assert oracle.unpack(chunk, 32, bits).tolist() == row[64 * kb + 32 * h:64 * kb + 32 * h + 32].tolist()
+            prm = t[base + 2048 * bits:base + blk]
+            g = 64 * kb // group
+            if bits == 2:
+                assert prm[8 * r:8 * r + 8].view(np.uint16).tolist() == q.cb[n, g].tolist()
+            else:
+                w = int(prm[4 * r:4 * r + 4].view(np.uint32)[0])
+                assert (w & 0xFFFF, w >> 16) == (int(q.scale[n, g]), int(q.zp[n, g]))
+    # rows past N are zero in the last tile
+    base = (1 * KB + 0) * blk
+    words = t[base:base + 2048 * bits].view(np.uint32).reshape(bits, 512)
+    assert (words[:, 2 * 44:] == 0).all()
