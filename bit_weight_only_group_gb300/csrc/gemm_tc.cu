@@ -646,17 +646,23 @@ qg_status launch_gemm(const uint16_t* x, int M, int ldx, const qg_qweight& w, vo
     }
 }
 
-qg_status launch_gemm_tiles(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void* tiles, void* y,
-                            int ldy, qg_ydtype yt, void* ws, cudaStream_t s)
+qg_status launch_x_to_f16(const uint16_t* x, int M, int K, int ldx, int bits, void* x16, cudaStream_t s)
 {
-    switch (w.bits) {
-        case 2: return tc::run_bits<2, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
-        case 3: return tc::run_bits<3, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
-        case 4: return tc::run_bits<4, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
-        case 5: return tc::run_bits<5, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
-        case 6: return tc::run_bits<6, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
-        default: return tc::run_bits<8, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
+    const long long total32 = (long long)M * K / 32;
+    const int blocks = (int)std::min<long long>(ceil_div(total32, 256), (long long)num_sms() * 8);
+    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+    __half* o = static_cast<__half*>(x16);
+    switch (bits) {
+        case 2: tc::k_x_to_f16<2><<<blocks, 256, 0, s>>>(xb, M, K, ldx, o); break;
+        case 3: tc::k_x_to_f16<3><<<blocks, 256, 0, s>>>(xb, M, K, ldx, o); break;
+        case 4: tc::k_x_to_f16<4><<<blocks, 256, 0, s>>>(xb, M, K, ldx, o); break;
+        case 5: tc::k_x_to_f16<5><<<blocks, 256, 0, s>>>(xb, M, K, ldx, o); break;
+        case 6: tc::k_x_to_f16<6><<<blocks, 256, 0, s>>>(xb, M, K, ldx, o); break;
+        default: tc::k_x_to_f16<8><<<blocks, 256, 0, s>>>(xb, M, K, ldx, o); break;
     }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "x conversion launch");
+    return QG_OK;
 }
 
 }  // namespace qg
