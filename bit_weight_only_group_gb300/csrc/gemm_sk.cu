@@ -88,17 +88,18 @@ struct Args {
 // Share of CTA c: units [lo(c), lo(c + 1)).
 __host__ __device__ __forceinline__ long long unit_lo(long long U, int P, int c) { return U * c / P; }
 
-// Segment iterator over a CTA's units: tile t, K blocks [kb0, kb1).
+// Segment iterator over a CTA's units: tile t, K blocks [kb0, kb1).  Unit
+// indices fit in 31 bits (checked on the host).
 struct Seg {
-    long long u, u1;
+    int u, u1;
     int KB;
     int t, kb0, kb1;
     __device__ __forceinline__ bool next()
     {
         if (u >= u1) return false;
-        t = (int)(u / KB);
-        kb0 = (int)(u % KB);
-        kb1 = (int)min((long long)KB, kb0 + (u1 - u));
+        t = u / KB;
+        kb0 = u - t * KB;
+        kb1 = min(KB, kb0 + (u1 - u));
         u += kb1 - kb0;
         return true;
     }
@@ -126,6 +127,28 @@ __device__ __forceinline__ void participants(long long U, int P, int KB, int t, 
     last = lo;
 }
 
+// Store 16 consecutive outputs of token m from column nb: float4 stores
+// when the run is whole and aligned, else one by one within N.
+__device__ __forceinline__ void store16(const Args& a, int m, int nb, const float (&f)[16])
+{
+    if (a.y_bf16) {
+        __nv_bfloat16* yr = reinterpret_cast<__nv_bfloat16*>(a.y) + (size_t)m * a.ldy;
+#pragma unroll
+        for (int q = 0; q < 16; q++)
+            if (nb + q < a.N) yr[nb + q] = __float2bfloat16_rn(f[q]);
+        return;
+    }
+    float* yr = reinterpret_cast<float*>(a.y) + (size_t)m * a.ldy;
+    if (nb + 16 <= a.N && (reinterpret_cast<uintptr_t>(yr + nb) & 15u) == 0) {
+#pragma unroll
+        for (int q = 0; q < 16; q += 4) *reinterpret_cast<float4*>(yr + nb + q) = make_float4(f[q], f[q + 1], f[q + 2], f[q + 3]);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 16; q++)
+            if (nb + q < a.N) yr[nb + q] = f[q];
+    }
+}
+
 template <int BITS, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_sk(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ Args a)
@@ -145,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t acc_full = bars + 8 * (2 * SA + 2 * SP + 2 * SB);
     const uint32_t acc_empty = acc_full + 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * (2 * SA + 2 * SP + 2 * SB + 2));
-    int* bcast = reinterpret_cast<int*>(smem + C::OFF_BAR + 8 * (2 * SA + 2 * SP + 2 * SB + 3));
+    int* bcast = reinterpret_cast<int*>(smem + C::OFF_BAR + 8 * (2 * SA + 2 * SP + 2 * SB + 3));   // 3 ints
     auto a_tile = [&](int s) { return sbase + s * A_BYTES; };
     auto b_tile = [&](int s) { return sbase + C::OFF_B + s * B_BYTES; };
     auto p_tile = [&](int s) { return smem + C::OFF_P + s * C::P_ALIGNED; };
@@ -153,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x;
     const int KB = a.KB;
-    Seg seg0{unit_lo(a.U, a.P, c), unit_lo(a.U, a.P, c + 1), KB, 0, 0, 0};
+    const Seg seg0{(int)unit_lo(a.U, a.P, c), (int)unit_lo(a.U, a.P, c + 1), KB, 0, 0, 0};
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SA; s++) { ptx::mbar_init(full_a(s), 1); ptx::mbar_init(empty_a(s), 1); }
@@ -356,16 +379,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint4 ew = *reinterpret_cast<const uint4*>(e_row + cb);
                     if (ok && m < a.M) {
                         const uint32_t ewa[4] = {ew.x, ew.y, ew.z, ew.w};
-                        const int nb = n0 + cb;
+                        float f[16];
 #pragma unroll
                         for (int q = 0; q < 16; q++) {
                             const int ej = (ewa[q >> 2] >> (8 * (q & 3))) & 0xFF;
-                            const float f = __uint_as_float(v[q]) * __int_as_float((127 + ej) << 23);
-                            if (nb + q < a.N) {
-                                if (a.y_bf16) reinterpret_cast<__nv_bfloat16*>(a.y)[(size_t)m * a.ldy + nb + q] = __float2bfloat16_rn(f);
-                                else reinterpret_cast<float*>(a.y)[(size_t)m * a.ldy + nb + q] = f;
-                            }
+                            f[q] = __uint_as_float(v[q]) * __int_as_float((127 + ej) << 23);
                         }
+                        store16(a, m, n0 + cb, f);
                     }
                 }
                 ptx::tc_fence_before();
@@ -396,11 +416,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) ptx::mbar_arrive(acc_empty);   // TMEM drained: the next segment may start
                 __threadfence();
                 tc::deq_sync();
-                int first, last;
-                participants(a.U, a.P, KB, g.t, first, last);
-                if (threadIdx.x == 0) *bcast = atomicAdd(a.count + g.t, 1);
+                if (threadIdx.x == 0) {
+                    int first, last;
+                    participants(a.U, a.P, KB, g.t, first, last);
+                    bcast[0] = atomicAdd(a.count + g.t, 1);
+                    bcast[1] = first;
+                    bcast[2] = last;
+                }
                 tc::deq_sync();
-                if (*bcast == last - first) {   // every other participant has stored and counted in
+                const int first = bcast[1], last = bcast[2];
+                if (bcast[0] == last - first) {   // every other participant has stored and counted in
                     __threadfence();
 #pragma unroll 1
                     for (int i = 0; i < 8; i++) {
@@ -423,16 +448,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint4 ew = *reinterpret_cast<const uint4*>(e_row + cb);
                         if (ok && m < a.M) {
                             const uint32_t ewa[4] = {ew.x, ew.y, ew.z, ew.w};
-                            const int nb = n0 + cb;
 #pragma unroll
                             for (int q = 0; q < 16; q++) {
                                 const int ej = (ewa[q >> 2] >> (8 * (q & 3))) & 0xFF;
-                                const float f = s16v[q] * __int_as_float((127 + ej) << 23);
-                                if (nb + q < a.N) {
-                                    if (a.y_bf16) reinterpret_cast<__nv_bfloat16*>(a.y)[(size_t)m * a.ldy + nb + q] = __float2bfloat16_rn(f);
-                                    else reinterpret_cast<float*>(a.y)[(size_t)m * a.ldy + nb + q] = f;
-                                }
+                                s16v[q] *= __int_as_float((127 + ej) << 23);
                             }
+                            store16(a, m, n0 + cb, s16v);
                         }
                     }
                 }
@@ -478,6 +499,7 @@ qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void
     using C = Cfg<BITS>;
     const int MT = (int)ceil_div(M, BM), NT = (int)ceil_div(w.N, BN), KB = w.K / BK;
     const long long U = (long long)MT * NT * KB;
+    if (U >= (1LL << 31)) return fail(QG_ERR_UNSUPPORTED, "qgemm_forward_tiles: %lld work units (above 2^31)", U);
     const int P = (int)std::min<long long>(num_sms(), U);
     Ws p{};
     ws_layout(M, w, P, &p, ws);

@@ -1,6 +1,7 @@
 """The one-time device repack into the tile-ordered layout (bytes equal to
-the oracle's layout) and the tensor-core product that streams it (against
-the fp64 oracle, and bit for bit against the planar tensor-core path)."""
+the oracle's layout) and the persistent stream-K tensor-core product that
+streams it: against the fp64 oracle, and bit for bit across repeated calls
+(the partial tiles of split tiles are summed in a fixed order)."""
 import numpy as np
 import pytest
 import torch
@@ -42,8 +43,8 @@ def test_tiles_product(qg, bits, group, M):
     y = qg.qgemm_forward_tiles(x.cuda(), qd, t)
     torch.cuda.synchronize()
     check_product(y, oracle.linear(x, q), x, float(np.abs(oracle.dequant(q)).max()))
-    if M > 32:   # the planar path runs the same tensor-core arithmetic
-        assert torch.equal(qg.qgemm_forward(x.cuda(), qd), y)
+    for _ in range(3):
+        assert torch.equal(qg.qgemm_forward_tiles(x.cuda(), qd, t), y)
 
 
 @pytest.mark.parametrize("bits", [3, 4, 8])
@@ -65,9 +66,10 @@ def test_tiles_full_size_sampled(qg):
     W = wl.gen_weight(N, K, seed=21)
     qw = qg.qpack_quantize(W.cuda(), 4, 128, 0.0)
     x = wl.gen_x(M, K, seed=22)
-    y = qg.qgemm_forward_tiles(x.cuda(), qw, qg.qrepack_tiles(qw))
+    t = qg.qrepack_tiles(qw)
+    y = qg.qgemm_forward_tiles(x.cuda(), qw, t)
     torch.cuda.synchronize()
-    assert torch.equal(y, qg.qgemm_forward(x.cuda(), qw))
+    assert torch.equal(y, qg.qgemm_forward_tiles(x.cuda(), qw, t))
     toks = torch.arange(0, M, 97)
     for n0 in (0, N - 64):
         q = oracle.quantize(W[n0:n0 + 64], 4, 128, 0.0)
