@@ -222,7 +222,7 @@ qg_status qgemm_tiles_workspace_size(int32_t M, const qg_qweight* w, size_t* byt
     qg_status st = check_qweight(w, "qgemm_tiles_workspace_size");
     if (st != QG_OK) return st;
     if (M < 0) return fail(QG_ERR_INVALID_ARG, "qgemm_tiles_workspace_size: M < 0");
-    *bytes = M ? gemm_tiles_workspace_bytes(M, *w) : 0;
+    *bytes = M ? gemm_workspace_bytes(M, *w) : 0;
     return QG_OK;
 }
 
@@ -238,7 +238,7 @@ qg_status qgemm_forward_tiles(const uint16_t* x, int32_t M, int32_t ldx, const q
     if (yt != QG_Y_F32 && yt != QG_Y_BF16) return fail(QG_ERR_INVALID_ARG, "qgemm_forward_tiles: bad y dtype");
     if (!aligned(x, 2) || !aligned(y, yt == QG_Y_F32 ? 4 : 2) || !aligned(tiles, 128))
         return fail(QG_ERR_ALIGNMENT, "qgemm_forward_tiles: x, y or tiles misaligned");
-    const size_t need = gemm_tiles_workspace_bytes(M, *w);
+    const size_t need = gemm_workspace_bytes(M, *w);
     if (!ws || ws_bytes < need)
         return fail(QG_ERR_WORKSPACE, "qgemm_forward_tiles: workspace %zu bytes < %zu", ws ? ws_bytes : (size_t)0, need);
     if (!aligned(ws, 256)) return fail(QG_ERR_ALIGNMENT, "qgemm_forward_tiles: workspace must be 256-byte aligned");

@@ -297,11 +297,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int b = 0; b < 2; b++) {
                 const int kb = kp * PK + grp + b * kGroups;
                 const int gi = min(kb, KB - 1) / KB_PER_G;
-                pq[b] = tc::f16_times_pow2(__ldg(sp_row + gi), ex) | ((uint32_t)__ldg(zp_row + gi) << 16);
+                pq[b] = (uint32_t)__ldg(sp_row + gi) | ((uint32_t)__ldg(zp_row + gi) << 16);   // raw: loads stay in flight
             }
         };
         auto deq_block = [&](const uint4& w, uint32_t pq, unsigned char* at) {
-            const uint32_t sc = pq & 0xFFFFu, zq = pq >> 16;
+            const uint32_t sc = tc::f16_times_pow2(pq & 0xFFFFu, ex), zq = pq >> 16;
             const uint32_t add_lo = zq * 0x00010001u + 0xE400E400u;   // -(1024 + zp)
             const uint32_t add_hi = zq * 0x00100010u + 0xD400D400u;   // -(64 + zp)
             const uint32_t s2 = __byte_perm(sc, 0u, 0x1010u);

@@ -256,14 +256,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (BITS != 2) ex = row_exponent<BITS>(a.scale + (size_t)n * ng, ng, hk);
         if (hk == 0) e_row[r] = (uint8_t)ex;
         // group parameters of the current group and of the next two (loads in
-        // flight): affine (scale bits, zero-point); codebook (two words of 4 fp16)
+        // flight: kept raw until the group is used, the row exponent applied
+        // then): affine (scale bits, zero-point); codebook (two words of 4 fp16)
         const uint16_t* sp_row = a.scale + (size_t)n * ng;
         const uint8_t* zp_row = a.zp + (size_t)n * ng;
         const uint2* cb_row = a.cb + (size_t)n * ng;
         uint2 prm[3];
         auto load_prm = [&](int gi) -> uint2 {
             if constexpr (BITS == 2) return __ldg(cb_row + gi);
-            else return make_uint2(f16_times_pow2(__ldg(sp_row + gi), ex), (uint32_t)__ldg(zp_row + gi));
+            else return make_uint2((uint32_t)__ldg(sp_row + gi), (uint32_t)__ldg(zp_row + gi));
         };
         if constexpr (!TILES) {
             prm[0] = load_prm(0);
@@ -293,16 +294,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 4; j++) dst_off[j] = r * 128 + (((4 * hk + j) ^ rsw) << 4);
         unsigned char* const btile0 = smem + C::OFF_B;
 
-        // the operand of block kb in registers (16 fp16 pairs) -> the fp16 ring,
-        // outliers patched in; returns false if a wait gave up
+        // the fp16 ring: wait for a free slot (acquire), write the block's
+        // operand, then finish (outliers patched in, handed to the MMA warp)
         int sb = 0;
         uint32_t pb = 1;   // parity of empty_b to wait for
-        auto emit = [&](int kb, const uint32_t (&pr)[16]) -> bool {
-            if (!ptx::mbar_wait(empty_b(sb), pb)) return false;
-            unsigned char* bt = btile0 + sb * B_BYTES;
-#pragma unroll
-            for (int j = 0; j < 4; j++)
-                *reinterpret_cast<uint4*>(bt + dst_off[j]) = make_uint4(pr[4 * j], pr[4 * j + 1], pr[4 * j + 2], pr[4 * j + 3]);
+        auto acquire = [&]() -> unsigned char* {
+            return ptx::mbar_wait(empty_b(sb), pb) ? btile0 + sb * B_BYTES : nullptr;
+        };
+        auto finish = [&](int kb, unsigned char* bt) {
             // FP16 outliers in this thread's 32 k; the dense value there is
             // exactly 0 (affine), or the codebook entry nearest 0 (2 bits,
             // whose stored value is the residual)
@@ -327,6 +326,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(full_b(sb));
             if (++sb == SB) { sb = 0; pb ^= 1u; }
+        };
+        // the operand of block kb in registers (16 fp16 pairs) -> the ring;
+        // false if the wait for a free slot gave up
+        auto emit = [&](int kb, const uint32_t (&pr)[16]) -> bool {
+            unsigned char* bt = acquire();
+            if (!bt) return false;
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+                *reinterpret_cast<uint4*>(bt + dst_off[j]) = make_uint4(pr[4 * j], pr[4 * j + 1], pr[4 * j + 2], pr[4 * j + 3]);
+            finish(kb, bt);
             return true;
         };
         // next group: shift the parameter window
@@ -397,16 +406,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t zq = prm[0].y;
                     const uint32_t add_lo = zq * 0x00010001u + 0xE400E400u;   // -(1024 + zp)
                     const uint32_t add_hi = zq * 0x00100010u + 0xD400D400u;   // -(64 + zp)
-                    const uint32_t s2 = __byte_perm(prm[0].x, 0u, 0x1010u);
+                    const uint32_t s2 = __byte_perm(f16_times_pow2(prm[0].x, ex), 0u, 0x1010u);
                     const uint4 w = *reinterpret_cast<const uint4*>(pt + src_off[sub]);
-                    uint32_t pr[16];
-                    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        const uint4 d = deq8_u4(wv[j], add_lo, add_hi, s2, magic);
-                        pr[4 * j] = d.x; pr[4 * j + 1] = d.y; pr[4 * j + 2] = d.z; pr[4 * j + 3] = d.w;
-                    }
-                    if (!emit(kb, pr)) { ok = false; break; }
+                    unsigned char* bt = acquire();
+                    if (!bt) { ok = false; break; }
+                    *reinterpret_cast<uint4*>(bt + dst_off[0]) = deq8_u4(w.x, add_lo, add_hi, s2, magic);
+                    *reinterpret_cast<uint4*>(bt + dst_off[1]) = deq8_u4(w.y, add_lo, add_hi, s2, magic);
+                    *reinterpret_cast<uint4*>(bt + dst_off[2]) = deq8_u4(w.z, add_lo, add_hi, s2, magic);
+                    *reinterpret_cast<uint4*>(bt + dst_off[3]) = deq8_u4(w.w, add_lo, add_hi, s2, magic);
+                    finish(kb, bt);
                     // the packed slot goes back to its producer only after the
                     // stores that consumed its codes (emit synchronized the warp):
                     // a shared load of the whole warp completes in several
@@ -454,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 }
                             });
                         } else {
-                            const uint32_t s2 = __byte_perm(prm[0].x, 0u, 0x1010u);
+                            const uint32_t s2 = __byte_perm(f16_times_pow2(prm[0].x, ex), 0u, 0x1010u);
                             const uint32_t zq = prm[0].y;
                             gemv::static_for<0, 16>([&](auto ec) {
                                 constexpr int e = decltype(ec)::value;
@@ -526,43 +534,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpMma) ptx::tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// Whether the width's operand order is the same permutation inside every
+// block of 8 k positions (as at 4 and 8 bits): then a thread converts 8
+// values with the entries of the first block.
+template <int BITS>
+constexpr bool perm_within_8()
+{
+    for (int e = 0; e < 16; e++) {
+        const gemv::PairE q = gemv::plan_entry(BITS, 32, e), q0 = gemv::plan_entry(BITS, 32, e % 4);
+        if (q0.lo >= 8 || q0.hi >= 8 || q.lo != q0.lo + 8 * (e / 4) || q.hi != q0.hi + 8 * (e / 4)) return false;
+    }
+    return true;
+}
+
 // bf16 [M, ldx] -> fp16 [M, K] (exact for |x| in fp16's range), with the K
 // positions of every block of 32 in the order the weight operand uses: the
 // pair plan of the width puts codes lo and hi of entry e at 2e and 2e + 1.
-// One thread converts one block of 32 (64 bytes in, 64 bytes out).
+// A thread converts a block of 8 (when the order keeps blocks of 8 in place,
+// as at 4 bits) or of 32.
 template <int BITS>
 __global__ void k_x_to_f16(const __nv_bfloat16* __restrict__ x, int M, int K, int ldx, __half* __restrict__ out)
 {
-    const long long total32 = (long long)M * K / 32;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total32;
+    constexpr int R = perm_within_8<BITS>() ? 8 : 32;
+    const long long total = (long long)M * K / R;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
-        const long long e = i * 32;
+        const long long e = i * R;
         const int m = (int)(e / K), k = (int)(e % K);
         const __nv_bfloat16* src = x + (size_t)m * ldx + k;
-        uint32_t v[16];   // the 32 bf16 values, two per word
+        uint32_t v[R / 2];   // the R bf16 values, two per word
         if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
 #pragma unroll
-            for (int j = 0; j < 4; j++) {
+            for (int j = 0; j < R / 8; j++) {
                 const uint4 q = __ldg(reinterpret_cast<const uint4*>(src) + j);
                 v[4 * j] = q.x; v[4 * j + 1] = q.y; v[4 * j + 2] = q.z; v[4 * j + 3] = q.w;
             }
         } else {
             const unsigned short* s16 = reinterpret_cast<const unsigned short*>(src);
 #pragma unroll
-            for (int j = 0; j < 16; j++) v[j] = (uint32_t)__ldg(s16 + 2 * j) | ((uint32_t)__ldg(s16 + 2 * j + 1) << 16);
+            for (int j = 0; j < R / 2; j++) v[j] = (uint32_t)__ldg(s16 + 2 * j) | ((uint32_t)__ldg(s16 + 2 * j + 1) << 16);
         }
         auto f16 = [&](int c) -> uint32_t {   // bf16 -> fp32 (exact) -> fp16
             const uint32_t b = (c & 1) ? (v[c >> 1] & 0xFFFF0000u) : (v[c >> 1] << 16);
             return __half_as_ushort(__float2half_rn(__uint_as_float(b)));
         };
-        uint32_t o[16];
-        gemv::static_for<0, 16>([&](auto ec) {
-            constexpr gemv::PairE q = gemv::plan_entry(BITS, 32, decltype(ec)::value);
-            o[decltype(ec)::value] = f16(q.lo) | (f16(q.hi) << 16);
+        uint32_t o[R / 2];
+        gemv::static_for<0, R / 2>([&](auto ec) {
+            constexpr int pe = decltype(ec)::value;   // pair entry within this thread's block
+            constexpr gemv::PairE q = gemv::plan_entry(BITS, 32, pe);
+            o[pe] = f16(q.lo) | (f16(q.hi) << 16);
         });
         uint4* dst = reinterpret_cast<uint4*>(out + e);
 #pragma unroll
-        for (int j = 0; j < 4; j++) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        for (int j = 0; j < R / 8; j++) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
     }
 }
 
@@ -643,6 +667,19 @@ qg_status launch_gemm(const uint16_t* x, int M, int ldx, const qg_qweight& w, vo
         case 5: return tc::run_bits<5, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, s);
         case 6: return tc::run_bits<6, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, s);
         default: return tc::run_bits<8, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, s);
+    }
+}
+
+qg_status launch_gemm_tiles(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void* tiles, void* y,
+                            int ldy, qg_ydtype yt, void* ws, cudaStream_t s)
+{
+    switch (w.bits) {
+        case 2: return tc::run_bits<2, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
+        case 3: return tc::run_bits<3, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
+        case 4: return tc::run_bits<4, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
+        case 5: return tc::run_bits<5, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
+        case 6: return tc::run_bits<6, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
+        default: return tc::run_bits<8, true>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
     }
 }
 

@@ -78,10 +78,9 @@ inline size_t tiles_bytes(const qg_qweight& w)
     return (size_t)ceil_div(w.N, kTileRows) * (size_t)(w.K / kTileK) * tile_block_bytes(w.bits);
 }
 qg_status launch_repack(const qg_qweight& w, void* tiles, cudaStream_t s);
-// Persistent stream-K tensor-core product over the tile-ordered copy; its
-// workspace holds x in fp16, the partial tiles of split tiles and a counter
-// per tile.
-size_t gemm_tiles_workspace_bytes(int M, const qg_qweight& w);
+// Tensor-core product over the tile-ordered copy (workspace: x in fp16, as
+// gemm_workspace_bytes).
+qg_status launch_x_to_f16(const uint16_t* x, int M, int K, int ldx, int bits, void* x16, cudaStream_t s);
 qg_status launch_gemm_tiles(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void* tiles, void* y,
                             int ldy, qg_ydtype yt, void* ws, cudaStream_t s);
 

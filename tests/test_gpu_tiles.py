@@ -1,7 +1,7 @@
 """The one-time device repack into the tile-ordered layout (bytes equal to
-the oracle's layout) and the persistent stream-K tensor-core product that
-streams it: against the fp64 oracle, and bit for bit across repeated calls
-(the partial tiles of split tiles are summed in a fixed order)."""
+the oracle's layout) and the tensor-core product that streams it: against
+the fp64 oracle, bit for bit against the planar tensor-core path (the same
+arithmetic on the same operands) and across repeated calls."""
 import numpy as np
 import pytest
 import torch
@@ -45,6 +45,8 @@ def test_tiles_product(qg, bits, group, M):
     check_product(y, oracle.linear(x, q), x, float(np.abs(oracle.dequant(q)).max()))
     for _ in range(3):
         assert torch.equal(qg.qgemm_forward_tiles(x.cuda(), qd, t), y)
+    if M > 32:   # the planar tensor-core path computes the same operands in the same order
+        assert torch.equal(qg.qgemm_forward(x.cuda(), qd), y)
 
 
 @pytest.mark.parametrize("bits", [3, 4, 8])
@@ -70,6 +72,7 @@ def test_tiles_full_size_sampled(qg):
     y = qg.qgemm_forward_tiles(x.cuda(), qw, t)
     torch.cuda.synchronize()
     assert torch.equal(y, qg.qgemm_forward_tiles(x.cuda(), qw, t))
+    assert torch.equal(y, qg.qgemm_forward(x.cuda(), qw))
     toks = torch.arange(0, M, 97)
     for n0 in (0, N - 64):
         q = oracle.quantize(W[n0:n0 + 64], 4, 128, 0.0)
