@@ -133,7 +133,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int SB = C::SB;
     constexpr int SP = C::SPN;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived from the shared array by pointer arithmetic (an
+    // integer round trip would leave the compiler a generic pointer)
+    unsigned char* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = ptx::smem_u32(smem);
     const uint32_t bars = sbase + C::OFF_BAR;
     // barriers: full/empty per ring slot, then the accumulator-ready barrier
