@@ -58,11 +58,15 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--layers", type=int, default=80, help="layers of the 70B-shaped stack")
     ap.add_argument("--no-secondary", action="store_true", help="skip the prefill and MoE lines")
-    ap.add_argument("--mode", choices=("all", "decode", "prefill", "moe", "widths"), default="all",
+    ap.add_argument("--mode", choices=("all", "decode", "prefill", "moe", "widths", "case"), default="all",
                     help="run only that measurement and print its object (profiling runs): 'decode' = the "
                          "headline alone; 'prefill' = the 70B layer and the width sweep at M=2048; 'widths' = "
                          "the single layer, the mixed-width sweep and the 7B-shaped stack at M=1, 8, 32")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
+    ap.add_argument("--case", default="gateup1",
+                    help="--mode case: one small case, three calls, for a profiler: gateup<M> (fused 28672x8192 "
+                         "gate/up decode at M), tiles<bits> / planar<bits> (8192x8192 at M=2048), moe (gate/up of "
+                         "the MoE layer), w8a8 (28672x8192 at M=1), diag / repack (28672x8192 INT4)")
     return ap.parse_args()
 
 
@@ -70,8 +74,8 @@ def parse():
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum over the launches
 # of a layer, captured on a 2-layer stack), valid only for the kernel source
 # it was taken on.
-DECODE_TRAFFIC = {"kernel_sha256": "a0a55612a8bb9fef472524400d7228b514bb7911791c9362a1a5b9b73b45cf34",
-                  "bytes_per_layer": 453.862e6}
+DECODE_TRAFFIC = {"kernel_sha256": "fc20486295979214695e23c01cbcdd333f583df66f24d19287c282ae94cfc464",
+                  "bytes_per_layer": 453.863e6}
 
 
 def decode_traffic(n_layers):
@@ -846,6 +850,48 @@ def run_reference(args, world, rank):
     return 0
 
 
+def run_case(qg, name):
+    """One small case of a single kernel family, called three times (for ncu
+    captures: a few hundred MB on the device, one kernel per call)."""
+    dev = torch.device("cuda")
+    if name.startswith("gateup"):
+        M = int(name[6:])
+        qs = [qg.qpack_quantize(wl.gen_weight(28672, 8192, seed=s, device=dev), 4, 128, 0.001) for s in (1, 2)]
+        x = wl.gen_x(M, 8192, device=dev)
+        call = lambda: qg.qgemm_forward_multi(x, qs)
+    elif name.startswith("tiles") or name.startswith("planar"):
+        bits = int(name[5:] if name.startswith("tiles") else name[6:])
+        q = qg.qpack_quantize(wl.gen_weight(8192, 8192, seed=1, device=dev, outlier_frac=0.001), bits, 128, 0.001)
+        x = wl.gen_x(2048, 8192, device=dev)
+        if name.startswith("tiles"):
+            t = qg.qrepack_tiles(q)
+            call = lambda: qg.qgemm_forward_tiles(x, q, t)
+        else:
+            call = lambda: qg.qgemm_forward(x, q)
+    elif name == "moe":
+        cfg = wl.MoE()
+        ex = [[qg.qpack_quantize(wl.gen_weight(cfg.ffn, cfg.hidden, seed=10 * p + e, device=dev), 4, 128, 0.0)
+               for e in range(cfg.n_experts)] for p in range(2)]
+        x = wl.gen_x(cfg.tokens, cfg.hidden, device=dev)
+        topk = wl.gen_topk(cfg.tokens, cfg.top_k, cfg.n_experts).to(dev)
+        call = lambda: qg.qgemm_moe_grouped_multi(x, topk, ex)
+    elif name == "w8a8":
+        q = qg.qpack_quantize(wl.gen_weight(28672, 8192, seed=1, device=dev), 8, 128, 0.0)
+        x = wl.gen_x(1, 8192, device=dev)
+        call = lambda: qg.qgemm_forward_w8a8(x, q)
+    elif name in ("diag", "repack"):
+        W = wl.gen_weight(28672, 8192, seed=1, device=dev, outlier_frac=0.001, distinct_positions=False)
+        q = qg.qpack_quantize(W, 4, 128, 0.001)
+        t = qg.qrepack_tiles(q) if name == "repack" else None
+        call = (lambda: qg.qdiag_layer(W, q)) if name == "diag" else (lambda: qg.qrepack_tiles(q, out=t))
+    else:
+        raise SystemExit(f"unknown case {name}")
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    return {"case": name, "calls": 3}
+
+
 def secondary(line, key, fn, *a):
     try:
         line[key] = fn(*a)
@@ -875,6 +921,8 @@ def main():
                 layers7, qs7 = build_stack7b(qg)
                 out = {"single": run_single_layer(qg, P), "sweep": run_sweep(qg, P),
                        "stack_7b": [run_stack7b(qg, P, layers7, qs7, M) for M in (1, 8, 32)]}
+            elif args.mode == "case":
+                out = run_case(qg, args.case)
             elif args.mode == "decode":
                 dec, qws = run_decode(qg, args, world, rank, P)
                 out = {k: v for k, v in dec.items()}
