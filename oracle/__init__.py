@@ -88,6 +88,17 @@ def lib():
         L.orc_linear_w8a8.restype = ctypes.c_int
         L.orc_diagnostics.argtypes = [vp, ctypes.POINTER(_QW), ctypes.c_double, vp, vp]
         L.orc_diagnostics.restype = ctypes.c_int
+        L.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        L.orc_e4m3_to_f64.restype = ctypes.c_double
+        L.orc_e4m3_ceil_normal.argtypes = [ctypes.c_double]
+        L.orc_e4m3_ceil_normal.restype = ctypes.c_int
+        L.orc_fp8_matrix_exponent.argtypes = [vp, i64]
+        L.orc_fp8_matrix_exponent.restype = ctypes.c_int
+        L.orc_quantize_fp8.argtypes = [vp, i64, i64, ctypes.c_int, ctypes.c_int, f32, ctypes.c_int,
+                                       vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64]
+        L.orc_quantize_fp8.restype = i64
+        L.orc_fp8_expand.argtypes = [vp, i32, i64, i64, vp, vp, vp, vp]
+        L.orc_fp8_expand.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -175,6 +186,13 @@ class QWeight:
     row_ptr: np.ndarray           # int32 [N+1]
     col: np.ndarray               # int32 [nnz]
     val: np.ndarray               # uint16 (fp16) [nnz]
+    # E4M3 scales (``scale_fmt='fp8'``): ``scale`` then holds the fp16 value
+    # each group stores, expanded from these by ``orc_fp8_expand``
+    scale8: np.ndarray | None = None      # uint8 [N, K/group], 0x7F = fp16 fallback
+    scale_exp: int = 0                    # the matrix exponent E
+    fb_row_ptr: np.ndarray | None = None  # int32 [N+1]
+    fb_col: np.ndarray | None = None      # int32 [nfb] group index within the row
+    fb_val: np.ndarray | None = None      # uint16 (fp16) [nfb]
 
     @property
     def nnz(self) -> int:
@@ -204,24 +222,45 @@ def select_outliers(W, frac: float):
 MODES = {"asymmetric": 0, "symmetric": 1, "linear2": 2}
 
 
-def quantize(W, bits: int, group: int, frac: float = 0.0, mode: str = "asymmetric") -> QWeight:
+def quantize(W, bits: int, group: int, frac: float = 0.0, mode: str = "asymmetric",
+             scale_fmt: str = "fp16") -> QWeight:
     """Quantize and pack W [N, K] (fp16).  mode: 'asymmetric' (affine with a
-    zero point at 3-6 bits, k-means codebook at 2), 'symmetric' (no zero
+    zero point at 3-8 bits, k-means codebook at 2), 'symmetric' (no zero
     point: the affine format with the zero point fixed at 2^(b-1); at 2
     bits the constants -s, 0, s, s) or 'linear2' (2 bits only: the affine
-    grid's four constants)."""
+    grid's four constants).  scale_fmt 'fp8' (bits 3-8, asymmetric or
+    symmetric): E4M3 group scales with an fp16 fallback (``orc_quantize_fp8``)."""
     W = as_u16(W)
     N, K = W.shape
     sz = sizes(N, K, bits, group, frac)
     ng = K // group
-    packed = np.empty((N, K * bits // 8), np.uint8)
-    scale = np.empty((N, ng), np.uint16) if bits != 2 else None
-    zp = np.empty((N, ng), np.uint8) if bits != 2 else None
-    cb = np.empty((N, ng, 4), np.uint16) if bits == 2 else None
     n = sz["nnz"]
+    packed = np.empty((N, K * bits // 8), np.uint8)
     row_ptr = np.empty(N + 1, np.int32)
     col = np.empty(max(n, 1), np.int32)
     val = np.empty(max(n, 1), np.uint16)
+    if scale_fmt == "fp8":
+        scale8 = np.empty((N, ng), np.uint8)
+        zp = np.empty((N, ng), np.uint8)
+        E = ctypes.c_int32(0)
+        fb_row_ptr = np.empty(N + 1, np.int32)
+        fb_col = np.empty(N * ng, np.int32)
+        fb_val = np.empty(N * ng, np.uint16)
+        nfb = lib().orc_quantize_fp8(_p(W), N, K, bits, group, float(np.float32(frac)), MODES[mode],
+                                     _p(packed), _p(scale8), _p(zp), _p(row_ptr), _p(col), _p(val),
+                                     ctypes.addressof(E), _p(fb_row_ptr), _p(fb_col), _p(fb_val), N * ng)
+        if nfb < 0:
+            raise ValueError(f"orc_quantize_fp8 failed ({nfb})")
+        scale = np.empty((N, ng), np.uint16)
+        rc = lib().orc_fp8_expand(_p(scale8), E.value, N, ng, _p(fb_row_ptr), _p(fb_col), _p(fb_val), _p(scale))
+        if rc != 0:
+            raise ValueError(f"orc_fp8_expand failed ({rc})")
+        return QWeight(N, K, bits, group, packed, scale, zp, None, row_ptr, col[:n], val[:n],
+                       scale8, E.value, fb_row_ptr, fb_col[:nfb].copy(), fb_val[:nfb].copy())
+    assert scale_fmt == "fp16", scale_fmt
+    scale = np.empty((N, ng), np.uint16) if bits != 2 else None
+    zp = np.empty((N, ng), np.uint8) if bits != 2 else None
+    cb = np.empty((N, ng, 4), np.uint16) if bits == 2 else None
     rc = lib().orc_quantize_mode(_p(W), N, K, bits, group, float(np.float32(frac)), MODES[mode], _p(packed),
                             _p(scale) if scale is not None else None,
                             _p(zp) if zp is not None else None,
@@ -230,6 +269,22 @@ def quantize(W, bits: int, group: int, frac: float = 0.0, mode: str = "asymmetri
     if rc != 0:
         raise ValueError(f"orc_quantize failed ({rc})")
     return QWeight(N, K, bits, group, packed, scale, zp, cb, row_ptr, col[:n], val[:n])
+
+
+def e4m3_value(code: int) -> float:
+    """Value of an E4M3 byte (``orc_e4m3_to_f64``)."""
+    return lib().orc_e4m3_to_f64(code)
+
+
+def e4m3_ceil_normal(t: float) -> int:
+    """Least normal E4M3 code with value >= t, or -1 (``orc_e4m3_ceil_normal``)."""
+    return lib().orc_e4m3_ceil_normal(float(t))
+
+
+def fp8_matrix_exponent(s16) -> int:
+    """Lower median of floor(log2 s) over fp16 scales (``orc_fp8_matrix_exponent``)."""
+    s16 = np.ascontiguousarray(as_u16(s16)).ravel()
+    return lib().orc_fp8_matrix_exponent(_p(s16), s16.size)
 
 
 def dequant(q: QWeight, n0: int = 0, n1: int | None = None) -> np.ndarray:
@@ -286,23 +341,32 @@ def linear_w8a8(x, q: QWeight, n0: int = 0, n1: int | None = None) -> np.ndarray
     return y
 
 
+def tile_param_bytes(bits: int, group: int) -> int:
+    """Parameter bytes per row of one tile block: 4 (fp16 scale | zp << 16)
+    or 8 (2-bit codebook) per group the 64-wide K block touches (two at
+    group 32, else one)."""
+    return (8 if bits == 2 else 4) * (2 if group == 32 else 1)
+
+
 def tiles(q: QWeight) -> np.ndarray:
     """The tile-ordered copy of q, written out block by block from the planar
     arrays: for each 256-row tile and 64-wide K block, 512 * bits words (word
     i of thread t = 2r + h at i * 512 + t, the thread's chunk being the 32
     codes [64 kb + 32 h, 64 kb + 32 h + 32) of row r as 4 * bits bytes of the
-    LSB-first stream), then per row the group's parameter word (fp16 scale |
-    zp << 16) or, at 2 bits, its 4 fp16 codebook entries.  Rows past N stay 0."""
+    LSB-first stream), then per row the parameters of the groups the block
+    touches in ascending order: the parameter word (fp16 scale | zp << 16)
+    or, at 2 bits, the 4 fp16 codebook entries.  Rows past N stay 0."""
     b, K, N = q.bits, q.K, q.N
     KB, NT = K // 64, (N + 255) // 256
-    blk = 2048 * b + (2048 if b == 2 else 1024)
+    pb = tile_param_bytes(b, q.group)
+    blk = 2048 * b + 256 * pb
     out = np.zeros(NT * KB * blk, np.uint8)
     for nt in range(NT):
         for kb in range(KB):
             base = (nt * KB + kb) * blk
             words = out[base:base + 2048 * b].view(np.uint32).reshape(b, 512)
             prm = out[base + 2048 * b:base + blk]
-            g = kb * 64 // q.group
+            groups = sorted({(64 * kb + 32 * h) // q.group for h in range(2)})
             for r in range(256):
                 n = nt * 256 + r
                 if n >= N:
@@ -310,10 +374,13 @@ def tiles(q: QWeight) -> np.ndarray:
                 for h in range(2):
                     lo = (2 * kb + h) * 4 * b
                     words[:, 2 * r + h] = q.packed[n, lo:lo + 4 * b].view(np.uint32)
-                if b == 2:
-                    prm[8 * r:8 * r + 8] = q.cb[n, g].view(np.uint8)
-                else:
-                    prm[4 * r:4 * r + 4] = np.array([int(q.scale[n, g]) | (int(q.zp[n, g]) << 16)], np.uint32).view(np.uint8)
+                for i, g in enumerate(groups):
+                    at = pb * r + (pb // len(groups)) * i
+                    if b == 2:
+                        prm[at:at + 8] = q.cb[n, g].view(np.uint8)
+                    else:
+                        prm[at:at + 4] = np.array([int(q.scale[n, g]) | (int(q.zp[n, g]) << 16)],
+                                                  np.uint32).view(np.uint8)
     return out
 
 

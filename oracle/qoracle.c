@@ -24,6 +24,9 @@
  *    0,6,12,18, 5-bit units of 8 values in 5 bytes with shifts 5i ("Mixed-width quantization"
  *    page, sections 3.1-3.2), the 4-bit value pair as the low/high half of a
  *    byte (section 2.1 table).
+ *  - Group sizes 32, 64 and 128; at 32 the scale may be stored as an 8-bit
+ *    float, groups outside its range keeping an fp16 scale ("Mixed-width
+ *    quantization" page, section 2.3; see orc_quantize_fp8).
  *  - The product accumulates in fp64 here (the pages require at least fp32
  *    accumulation, "Mixed-width quantization" page, section 4.2).
  *
@@ -138,7 +141,7 @@ static int valid_shape(int64_t N, int64_t K, int bits, int group)
 {
     if (N <= 0 || K <= 0) return 0;
     if ((bits < 2 || bits > 6) && bits != 8) return 0;
-    if (group != 64 && group != 128) return 0;
+    if (group != 32 && group != 64 && group != 128) return 0;
     if (K % group) return 0;
     return 1;
 }
@@ -251,13 +254,9 @@ int64_t orc_select_outliers(const uint16_t *W, int64_t N, int64_t K, float frac,
 /* group quantizers                                                     */
 /* ------------------------------------------------------------------ */
 
-/* Affine asymmetric quantizer of one group (b in 3..6, also 4).
- * w: g fp16 values, out: g codes.  Writes the fp16 scale and the u8 zp. */
-static void quant_group_affine(const uint16_t *w, const uint8_t *is_out, int g, int bits,
-                               uint8_t *codes, uint16_t *scale16, uint8_t *zp_out)
+/* Range of a group's non-outlier elements, widened to contain 0. */
+static void group_range(const uint16_t *w, const uint8_t *is_out, int g, float *mn_out, float *mx_out)
 {
-    const int qmin = 0, qmax = (1 << bits) - 1;
-    /* range over the non-outlier elements, widened to contain 0 */
     float mn = 0.0f, mx = 0.0f;
     for (int i = 0; i < g; i++) {
         if (is_out[i]) continue;
@@ -265,14 +264,28 @@ static void quant_group_affine(const uint16_t *w, const uint8_t *is_out, int g, 
         if (v < mn) mn = v;
         if (v > mx) mx = v;
     }
-    uint16_t s16;
-    if (mx == mn) {
-        s16 = 0x3C00; /* 1.0 */
-    } else {
-        float range = mx - mn;
-        float s32 = range / (float)(qmax - qmin);
-        s16 = f32_to_f16(s32, 1);
-    }
+    *mn_out = mn;
+    *mx_out = mx;
+}
+
+/* Affine scale: (max - min) / (qmax - qmin) in fp32, rounded up to fp16
+ * (1.0 when max == min). */
+static uint16_t affine_scale16(float mn, float mx, int bits)
+{
+    const int qmin = 0, qmax = (1 << bits) - 1;
+    if (mx == mn) return 0x3C00; /* 1.0 */
+    float range = mx - mn;
+    float s32 = range / (float)(qmax - qmin);
+    return f32_to_f16(s32, 1);
+}
+
+/* Codes of an affine group for the fp16 scale s16: zp = clamp(qmin -
+ * round(min / scale)), q = clamp(round(w / scale) + zp); q = zp at outliers.
+ * Returns zp. */
+static uint8_t affine_encode(const uint16_t *w, const uint8_t *is_out, int g, int bits, float mn, uint16_t s16,
+                             uint8_t *codes)
+{
+    const int qmin = 0, qmax = (1 << bits) - 1;
     float s = orc_f16_to_f32(s16);
     float r = rintf(mn / s);
     int zp = qmin - (int)r;
@@ -290,8 +303,19 @@ static void quant_group_affine(const uint16_t *w, const uint8_t *is_out, int g, 
         }
         codes[i] = (uint8_t)q;
     }
+    return (uint8_t)zp;
+}
+
+/* Affine asymmetric quantizer of one group (b in 2..8).
+ * w: g fp16 values, out: g codes.  Writes the fp16 scale and the u8 zp. */
+static void quant_group_affine(const uint16_t *w, const uint8_t *is_out, int g, int bits,
+                               uint8_t *codes, uint16_t *scale16, uint8_t *zp_out)
+{
+    float mn, mx;
+    group_range(w, is_out, g, &mn, &mx);
+    uint16_t s16 = affine_scale16(mn, mx, bits);
+    *zp_out = affine_encode(w, is_out, g, bits, mn, s16, codes);
     *scale16 = s16;
-    *zp_out = (uint8_t)zp;
 }
 
 /* Symmetric quantizer of one group, stored in the affine format ("Mixed-
@@ -302,17 +326,22 @@ static void quant_group_affine(const uint16_t *w, const uint8_t *is_out, int g, 
  * largest |w| over the non-outliers: scale = fp16 rounded up of amax / qs
  * (1.0 if amax is 0), q = clamp(round(w / scale), -qs, qs), stored as
  * q + 2^(b-1) with the zero point byte fixed at 2^(b-1); q = 0 at outliers. */
-static void quant_group_symmetric(const uint16_t *w, const uint8_t *is_out, int g, int bits,
-                                  uint8_t *codes, uint16_t *scale16, uint8_t *zp_out)
+static uint16_t symmetric_scale16(const uint16_t *w, const uint8_t *is_out, int g, int bits)
 {
-    const int qs = (1 << (bits - 1)) - 1, zp = 1 << (bits - 1);
+    const int qs = (1 << (bits - 1)) - 1;
     float amax = 0.0f;
     for (int i = 0; i < g; i++) {
         if (is_out[i]) continue;
         float a = fabsf(orc_f16_to_f32(w[i]));
         if (a > amax) amax = a;
     }
-    uint16_t s16 = amax == 0.0f ? 0x3C00 : f32_to_f16(amax / (float)qs, 1);
+    return amax == 0.0f ? 0x3C00 : f32_to_f16(amax / (float)qs, 1);
+}
+
+static uint8_t symmetric_encode(const uint16_t *w, const uint8_t *is_out, int g, int bits, uint16_t s16,
+                                uint8_t *codes)
+{
+    const int qs = (1 << (bits - 1)) - 1, zp = 1 << (bits - 1);
     float s = orc_f16_to_f32(s16);
     for (int i = 0; i < g; i++) {
         int q = 0;
@@ -323,8 +352,15 @@ static void quant_group_symmetric(const uint16_t *w, const uint8_t *is_out, int 
         }
         codes[i] = (uint8_t)(q + zp);
     }
+    return (uint8_t)zp;
+}
+
+static void quant_group_symmetric(const uint16_t *w, const uint8_t *is_out, int g, int bits,
+                                  uint8_t *codes, uint16_t *scale16, uint8_t *zp_out)
+{
+    uint16_t s16 = symmetric_scale16(w, is_out, g, bits);
+    *zp_out = symmetric_encode(w, is_out, g, bits, s16, codes);
     *scale16 = s16;
-    *zp_out = (uint8_t)zp;
 }
 
 /* 2-bit groups on a uniform grid, stored as the four constants a code
@@ -517,6 +553,214 @@ int orc_quantize(const uint16_t *W, int64_t N, int64_t K, int bits, int group, f
                  int32_t *row_ptr, int32_t *col, uint16_t *val)
 {
     return orc_quantize_mode(W, N, K, bits, group, frac, 0, packed, scale, zp, cb, row_ptr, col, val);
+}
+
+/* ------------------------------------------------------------------ */
+/* 8-bit float (E4M3) group scales with an fp16 fallback                */
+/* ------------------------------------------------------------------ */
+/* "Mixed-width quantization" page, section 2.3: the group scale itself may
+ * be stored as an 8-bit float.  Its range is narrower than fp16's, so the
+ * scales of all groups are surveyed first; the groups whose scale falls
+ * outside what the 8-bit format can hold keep an fp16 scale, all others
+ * store 8 bits.  Readings (the page names neither the format nor the
+ * window):
+ *  - the format is E4M3: 1 sign bit, 4 exponent bits with bias 7, 3 fraction
+ *    bits, no infinities, S.1111.111 is NaN, largest finite value 448;
+ *  - one power of two per matrix, 2^E, places the format's range over the
+ *    scales: E is the lower median of floor(log2 s16) over all groups of
+ *    the matrix (the survey), so the typical scale sits near 1 in the
+ *    format's terms and only groups far from it fall out;
+ *  - a group's code is the least normal E4M3 value >= s16 * 2^-E (rounded up,
+ *    like the fp16 scale, so the grid still spans the group's range);
+ *  - the group falls back to fp16 when s16 * 2^-E is below the normal range
+ *    (2^-6), when the rounded value would exceed 448, or when (the rounded
+ *    value) * 2^E is not a normal fp16 number; a fallback group stores code
+ *    0x7F and keeps s16 in a per-row list (row_ptr [N+1], group index,
+ *    fp16 scale), groups ascending;
+ *  - the codes and the zero point are then those of the quantizer above
+ *    with the group's stored scale (the E4M3 value times 2^E, which is an
+ *    fp16 number, or the fallback s16).
+ * 2-bit groups have no single scale (codebooks) and are not covered. */
+
+/* Value of an E4M3 code, written from the format definition. */
+double orc_e4m3_to_f64(uint8_t c)
+{
+    int s = c >> 7, e = (c >> 3) & 0xF, m = c & 7;
+    double v;
+    if (e == 0xF && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);              /* subnormal: m * 2^-9 */
+    else
+        v = ldexp((double)(8 + m), e - 10);    /* (1 + m/8) * 2^(e-7) */
+    return s ? -v : v;
+}
+
+/* The least positive normal E4M3 code whose value is >= t, by scanning the
+ * normal codes in ascending order; -1 if t < 2^-6 or t > 448. */
+int orc_e4m3_ceil_normal(double t)
+{
+    if (!(t >= ldexp(1.0, -6))) return -1;
+    for (int c = 0x08; c <= 0x7E; c++)
+        if (orc_e4m3_to_f64((uint8_t)c) >= t) return c;
+    return -1;
+}
+
+/* floor(log2 v) of a positive finite double. */
+static int floor_log2(double v)
+{
+    int e2;
+    frexp(v, &e2);   /* v in [2^(e2-1), 2^e2) */
+    return e2 - 1;
+}
+
+/* Matrix exponent E: the lower median (element (n-1)/2 in ascending order)
+ * of floor(log2 s16) over the n fp16 scales. */
+int orc_fp8_matrix_exponent(const uint16_t *s16, int64_t n)
+{
+    /* fp16 scales lie in [2^-24, 65504]: floor(log2) in [-24, 15] */
+    int64_t hist[40] = {0};
+    for (int64_t i = 0; i < n; i++) hist[floor_log2(orc_f16_to_f64(s16[i])) + 24]++;
+    int64_t want = (n - 1) / 2, seen = 0;
+    for (int b = 0; b < 40; b++) {
+        seen += hist[b];
+        if (seen > want) return b - 24;
+    }
+    return 0;
+}
+
+/* The stored scale of a group with fp16 scale s16 under exponent E: returns
+ * the E4M3 code and sets *eff to the fp16 value code * 2^E, or returns 0x7F
+ * and sets *eff = s16 (fallback). */
+static uint8_t fp8_store(uint16_t s16, int E, uint16_t *eff)
+{
+    double t = ldexp(orc_f16_to_f64(s16), -E);
+    int c = orc_e4m3_ceil_normal(t);
+    if (c >= 0) {
+        double v = ldexp(orc_e4m3_to_f64((uint8_t)c), E);
+        if (v >= ldexp(1.0, -14) && v <= 65504.0) {
+            *eff = f32_to_f16((float)v, 0);   /* exact: 4 significant bits */
+            return (uint8_t)c;
+        }
+    }
+    *eff = s16;
+    return 0x7F;
+}
+
+/* Quantize with E4M3 scales (bits 3..8; mode 0 asymmetric, 1 symmetric).
+ * Outputs as orc_quantize_mode, with scale8 u8 [N, K/group] in place of the
+ * fp16 scales, *exp_out = E, and the fallback list fb_row_ptr [N+1],
+ * fb_col [fb_cap] (group index within the row), fb_val fp16 [fb_cap].
+ * Returns the number of fallback groups, or a negative ORC_ error
+ * (ORC_ENOMEM also when more than fb_cap groups fall back). */
+int64_t orc_quantize_fp8(const uint16_t *W, int64_t N, int64_t K, int bits, int group, float frac, int mode,
+                         uint8_t *packed, uint8_t *scale8, uint8_t *zp, int32_t *row_ptr, int32_t *col,
+                         uint16_t *val, int32_t *exp_out, int32_t *fb_row_ptr, int32_t *fb_col,
+                         uint16_t *fb_val, int64_t fb_cap)
+{
+    if (!valid_shape(N, K, bits, group) || bits == 2 || frac < 0.0f || frac >= 1.0f) return ORC_EINVAL;
+    if (mode != 0 && mode != 1) return ORC_EINVAL;
+    for (int64_t i = 0; i < N * K; i++)
+        if (!finite16(W[i])) return ORC_ENONFINITE;
+    int64_t ng = K / group;
+    uint8_t *mask = (uint8_t *)malloc((size_t)(N * K));
+    uint8_t *codes = (uint8_t *)malloc((size_t)K);
+    uint16_t *s16 = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(N * ng));
+    if (!mask || !codes || !s16) {
+        free(mask); free(codes); free(s16);
+        return ORC_ENOMEM;
+    }
+    int64_t nnz = select_outliers(W, N, K, frac, mask);
+    if (nnz < 0) {
+        free(mask); free(codes); free(s16);
+        return nnz;
+    }
+    /* 1. the fp16 scale of every group, as the fp16 quantizer finds it */
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t j = 0; j < ng; j++) {
+            const uint16_t *wg = W + n * K + j * group;
+            const uint8_t *mg = mask + n * K + j * group;
+            if (mode == 1) {
+                s16[n * ng + j] = symmetric_scale16(wg, mg, group, bits);
+            } else {
+                float mn, mx;
+                group_range(wg, mg, group, &mn, &mx);
+                s16[n * ng + j] = affine_scale16(mn, mx, bits);
+            }
+        }
+    /* 2. the matrix exponent from all groups' scales */
+    int E = orc_fp8_matrix_exponent(s16, N * ng);
+    /* 3. stored scales, codes with the stored scale, fallback list, outliers */
+    int64_t p = 0, f = 0;
+    for (int64_t n = 0; n < N; n++) {
+        const uint16_t *wr = W + n * K;
+        const uint8_t *mr = mask + n * K;
+        fb_row_ptr[n] = (int32_t)f;
+        for (int64_t j = 0; j < ng; j++) {
+            int64_t k0 = j * group;
+            uint16_t eff;
+            uint8_t c = fp8_store(s16[n * ng + j], E, &eff);
+            scale8[n * ng + j] = c;
+            if (c == 0x7F) {
+                if (f >= fb_cap) {
+                    free(mask); free(codes); free(s16);
+                    return ORC_ENOMEM;
+                }
+                fb_col[f] = (int32_t)j;
+                fb_val[f] = eff;
+                f++;
+            }
+            if (mode == 1) {
+                zp[n * ng + j] = symmetric_encode(wr + k0, mr + k0, group, bits, eff, codes + k0);
+            } else {
+                float mn, mx;
+                group_range(wr + k0, mr + k0, group, &mn, &mx);
+                zp[n * ng + j] = affine_encode(wr + k0, mr + k0, group, bits, mn, eff, codes + k0);
+            }
+        }
+        orc_pack(codes, K, bits, packed + n * (K * bits / 8));
+        row_ptr[n] = (int32_t)p;
+        for (int64_t k = 0; k < K; k++)
+            if (mr[k]) {
+                col[p] = (int32_t)k;
+                val[p] = wr[k];
+                p++;
+            }
+    }
+    row_ptr[N] = (int32_t)p;
+    fb_row_ptr[N] = (int32_t)f;
+    *exp_out = E;
+    free(mask); free(codes); free(s16);
+    return f;
+}
+
+/* The fp16 scale every group stores, from its E4M3 code and the matrix
+ * exponent, or from the row's fallback list for code 0x7F.  Returns
+ * ORC_EINVAL for a code that is not a positive normal E4M3 value, a scale
+ * that is not a normal fp16 number, or a 0x7F group missing from the list. */
+int orc_fp8_expand(const uint8_t *scale8, int32_t E, int64_t N, int64_t ng, const int32_t *fb_row_ptr,
+                   const int32_t *fb_col, const uint16_t *fb_val, uint16_t *s16_out)
+{
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t j = 0; j < ng; j++) {
+            uint8_t c = scale8[n * ng + j];
+            if (c == 0x7F) {
+                int found = 0;
+                for (int32_t q = fb_row_ptr[n]; q < fb_row_ptr[n + 1]; q++)
+                    if (fb_col[q] == j) {
+                        s16_out[n * ng + j] = fb_val[q];
+                        found = 1;
+                        break;
+                    }
+                if (!found) return ORC_EINVAL;
+                continue;
+            }
+            if (c < 0x08 || c > 0x7E) return ORC_EINVAL;
+            double v = ldexp(orc_e4m3_to_f64(c), E);
+            if (!(v >= ldexp(1.0, -14) && v <= 65504.0)) return ORC_EINVAL;
+            s16_out[n * ng + j] = f32_to_f16((float)v, 0);
+        }
+    return ORC_OK;
 }
 
 /* ------------------------------------------------------------------ */

@@ -191,7 +191,7 @@ def _outlier_mask(q):
 
 
 @pytest.mark.parametrize("bits", [3, 4, 5, 6, 8])
-@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("group", [32, 64, 128])
 def test_affine_codes_are_nearest_grid_points(bits, group):
     N, K, frac = 24, 1024, 0.002
     W = wl.gen_weight(N, K, seed=100 + bits, outlier_frac=frac, outlier_seed=200 + group)
@@ -633,14 +633,17 @@ def test_w8a8_product_is_the_product_of_the_quantized_activations():
 
 # ---------------------------------------------------------------- tile-ordered copy
 @pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
-def test_tiles_layout_reads_back_every_code_and_parameter(bits):
+@pytest.mark.parametrize("group", [32, 128])
+def test_tiles_layout_reads_back_every_code_and_parameter(bits, group):
     # read the layout back with the thread/word formula and compare with the
     # planar stream unpacked by the generic bit loop: every code of every row
     # (ragged last tile) and the group parameters land where stated
-    N, K, group = 300, 256, 128
+    N, K = 300, 256
     q = oracle.quantize(wl.gen_weight(N, K, seed=bits), bits, group, 0.0)
     t = oracle.tiles(q)
-    blk = 2048 * bits + (2048 if bits == 2 else 1024)
+    npg = 2 if group == 32 else 1                  # groups one 64-wide K block touches
+    per = 8 if bits == 2 else 4                    # parameter bytes per group
+    blk = 2048 * bits + 256 * per * npg
     KB = K // 64
     assert t.size == ((N + 255) // 256) * KB * blk
     for n in (0, 1, 255, 256, 299):
@@ -653,13 +656,149 @@ def test_tiles_layout_reads_back_every_code_and_parameter(bits):
                 chunk = words[:, 2 * r + h].astype(np.uint32).view(np.uint8)
                 assert oracle.unpack(chunk, 32, bits).tolist() == row[64 * kb + 32 * h:64 * kb + 32 * h + 32].tolist()
             prm = t[base + 2048 * bits:base + blk]
-            g = 64 * kb // group
-            if bits == 2:
-                assert prm[8 * r:8 * r + 8].view(np.uint16).tolist() == q.cb[n, g].tolist()
-            else:
-                w = int(prm[4 * r:4 * r + 4].view(np.uint32)[0])
-                assert (w & 0xFFFF, w >> 16) == (int(q.scale[n, g]), int(q.zp[n, g]))
+            for i in range(npg):
+                g = 64 * kb // group + i
+                at = per * npg * r + per * i
+                if bits == 2:
+                    assert prm[at:at + 8].view(np.uint16).tolist() == q.cb[n, g].tolist()
+                else:
+                    w = int(prm[at:at + 4].view(np.uint32)[0])
+                    assert (w & 0xFFFF, w >> 16) == (int(q.scale[n, g]), int(q.zp[n, g]))
     # rows past N are zero in the last tile
     base = (1 * KB + 0) * blk
     words = t[base:base + 2048 * bits].view(np.uint32).reshape(bits, 512)
     assert (words[:, 2 * 44:] == 0).all()
+
+
+# ---------------------------------------------------------------- group 32 and E4M3 scales
+def test_sizing_block32_effective_bits():
+    # "Mixed-width quantization" page, section 2.3: one fp16 scale per block
+    # of 32 gives 3.5 / 5.5 / 6.5 effective bits at 3 / 5 / 6 bits, and an
+    # 8-bit scale costs 8 bits per 32 weights (0.25 bit)
+    g = _sizing()
+    for bits in (3, 5, 6):
+        s = oracle.sizes(4096, 4096, bits, 32, 0.0)
+        assert (s["packed"] + s["scale"]) * 8 / (4096 * 4096) == g[f"effective_bits_g32_fp16_b{bits}"][0]
+    q = oracle.quantize(wl.gen_weight(64, 1024, seed=5), 3, 32, 0.0, scale_fmt="fp8")
+    assert q.scale8.nbytes * 8 / (64 * 1024) == g["scale_overhead_bits_g32_fp8"][0]
+
+
+def _torch_e4m3(codes):
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    t = torch.tensor(np.asarray(codes, np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def test_e4m3_decode_matches_the_library_format():
+    # every one of the 256 codes decodes as torch's float8_e4m3fn does
+    # (a library routine of the same format); 0x7F and 0xFF are its NaNs
+    codes = np.arange(256)
+    ref = _torch_e4m3(codes)
+    mine = np.array([oracle.e4m3_value(int(c)) for c in codes])
+    nan = np.isnan(ref)
+    assert nan.tolist() == np.isnan(mine).tolist() and nan.sum() == 2 and nan[0x7F] and nan[0xFF]
+    assert (mine[~nan] == ref[~nan]).all()
+    assert oracle.e4m3_value(0x7E) == 448.0 and oracle.e4m3_value(0x08) == 2.0 ** -6
+
+
+def test_e4m3_round_up_is_least_normal_upper_bound():
+    # hand-worked: 1 -> 0x38; 0.3 = 1.2 * 2^-2 rounds up to 1.25 * 2^-2 = 0x2A;
+    # 448 -> 0x7E; just above 448, or below 2^-6, there is no normal code
+    assert oracle.e4m3_ceil_normal(1.0) == 0x38
+    assert oracle.e4m3_ceil_normal(0.3) == 0x2A
+    assert oracle.e4m3_ceil_normal(448.0) == 0x7E
+    assert oracle.e4m3_ceil_normal(448.0001) == -1
+    assert oracle.e4m3_ceil_normal(2.0 ** -6) == 0x08
+    assert oracle.e4m3_ceil_normal(2.0 ** -6 * 0.999) == -1
+    # every t: the chosen value is >= t and the normal code below it is < t,
+    # checked against the library's decode of the codes
+    table = _torch_e4m3(np.arange(0x08, 0x7F))
+    rng = np.random.default_rng(7)
+    for t in np.concatenate([2.0 ** rng.uniform(-6, np.log2(448), 300), table]):
+        c = oracle.e4m3_ceil_normal(float(t))
+        assert table[c - 0x08] >= t
+        assert c == 0x08 or table[c - 0x09] < t
+
+
+def test_fp8_matrix_exponent_is_the_lower_median():
+    h = lambda v: np.array(v, np.float16).view(np.uint16)
+    # floor(log2) of 1, 0.25, 3, 0.5 = 0, -2, 1, -1: sorted -2, -1, 0, 1 -> -1
+    assert oracle.fp8_matrix_exponent(h([1.0, 0.25, 3.0, 0.5])) == -1
+    assert oracle.fp8_matrix_exponent(h([1.0, 0.25, 3.0, 0.5, 100.0])) == 0
+    assert oracle.fp8_matrix_exponent(h([2.0 ** -24, 2.0 ** -20, 65504.0])) == -20   # fp16 subnormals count
+    assert oracle.fp8_matrix_exponent(h([0.75])) == -1
+
+
+def test_fp8_scales_hand_worked():
+    # seven 4-bit groups of 32, asymmetric.  Fp16 scales (range / 15): 0.25,
+    # 0.5, 1, fp16_up(0.3) = 0.30004883, 2^-12, 128, 2^-10; floor(log2) = -2,
+    # -1, 0, -2, -12, 7, -10; sorted -12, -10, -2, -2, -1, 0, 7 -> E = -2.  In
+    # the format's terms (x 4): 1, 2, 4 exact (0x38, 0x40, 0x48); 1.2002
+    # rounds up to 1.25 (0x3A, stored scale 0.3125); 2^-10 is below every
+    # E4M3 value, 512 above 448, and 2^-8 only a subnormal: all three keep fp16.
+    g = 32
+    W = np.zeros((1, 7 * g), np.float32)
+    W[0, 0:2] = [-1.0, 2.75]
+    W[0, g:g + 2] = [-2.5, 5.0]
+    W[0, 2 * g:2 * g + 2] = [-5.0, 10.0]
+    W[0, 3 * g:3 * g + 3] = [-1.5, 3.0, 0.5]
+    W[0, 4 * g:4 * g + 2] = [-5 * 2.0 ** -12, 10 * 2.0 ** -12]
+    W[0, 5 * g:5 * g + 2] = [-640.0, 1280.0]
+    W[0, 6 * g:6 * g + 2] = [-5 * 2.0 ** -10, 10 * 2.0 ** -10]
+    q = oracle.quantize(W.astype(np.float16), 4, g, 0.0, scale_fmt="fp8")
+    assert q.scale_exp == -2
+    assert q.scale8[0].tolist() == [0x38, 0x40, 0x48, 0x3A, 0x7F, 0x7F, 0x7F]
+    assert q.fb_row_ptr.tolist() == [0, 3]
+    assert q.fb_col.tolist() == [4, 5, 6]
+    assert q.fb_val.view(np.float16).tolist() == [2.0 ** -12, 128.0, 2.0 ** -10]
+    assert q.scale[0].view(np.float16).tolist() == [0.25, 0.5, 1.0, 0.3125, 2.0 ** -12, 128.0, 2.0 ** -10]
+    # group 3 with scale 0.3125: zp = -round(-1.5 / 0.3125 = -4.8) = 5;
+    # 3.0 / 0.3125 = 9.6 -> 10 + 5 = 15; 0.5 / 0.3125 = 1.6 -> 2 + 5 = 7
+    codes = oracle.unpack(q.packed[0], 7 * g, 4)
+    assert int(q.zp[0, 3]) == 5
+    assert codes[3 * g:3 * g + 4].tolist() == [0, 15, 7, 5]
+
+
+@pytest.mark.parametrize("mode", ["asymmetric", "symmetric"])
+@pytest.mark.parametrize("bits,group", [(3, 32), (4, 128), (6, 64), (8, 128)])
+def test_fp8_scales_round_up_and_keep_half_step_bound(mode, bits, group):
+    N, K, frac = 48, 1024, 0.002
+    W = wl.gen_weight(N, K, seed=60 + bits, outlier_frac=frac, outlier_seed=61)
+    q16 = oracle.quantize(W, bits, group, frac, mode=mode)
+    q8 = oracle.quantize(W, bits, group, frac, mode=mode, scale_fmt="fp8")
+    s16 = q16.scale.view(np.float16).astype(np.float64)
+    s8 = q8.scale.view(np.float16).astype(np.float64)
+    fb = q8.scale8 == 0x7F
+    # stored scale: the fp16 one where it falls back, else rounded up by less
+    # than one E4M3 step (1/8 relative) from it
+    assert (s8[fb] == s16[fb]).all()
+    assert (s8[~fb] >= s16[~fb]).all() and (s8[~fb] < s16[~fb] * 1.125).all()
+    assert (q8.scale8[~fb] >= 0x08).all() and (q8.scale8[~fb] <= 0x7E).all()
+    # every non-outlier is within half a stored step of its dequantized value
+    out = _outlier_mask(q8)
+    err = np.abs(W.double().numpy() - oracle.dequant(q8))
+    sg = np.repeat(s8, group, axis=1)
+    assert (err[~out] <= sg[~out] * (0.5 + 2.0 ** -20)).all()
+    assert (err[out] == 0).all()
+    # Gaussian weights with their outliers taken out: no group falls back
+    # (the page reports under 0.3 % on real layers)
+    assert fb.mean() < 0.003
+
+
+def test_fp8_fallback_rows_list_every_fallback_group_once():
+    rng = np.random.default_rng(3)
+    N, K, g = 40, 512, 32
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    # groups scaled far down or far up fall outside the window
+    tiny = rng.random((N, K // g)) < 0.05
+    huge = rng.random((N, K // g)) < 0.03
+    f = np.where(tiny, 2.0 ** -11, np.where(huge, 2.0 ** 9, 1.0))
+    W = (W.reshape(N, K // g, g) * f[..., None]).reshape(N, K).astype(np.float16)
+    q = oracle.quantize(W, 5, g, 0.0, scale_fmt="fp8")
+    fb = q.scale8 == 0x7F
+    assert (fb >= (tiny | huge)).all() and fb.sum() == q.fb_col.size
+    for n in range(N):
+        cols = q.fb_col[q.fb_row_ptr[n]:q.fb_row_ptr[n + 1]]
+        assert cols.tolist() == np.nonzero(fb[n])[0].tolist()
