@@ -95,7 +95,8 @@ qg_status check_shape(int64_t N, int64_t K, int bits, int group)
 {
     if (N <= 0 || K <= 0) return fail(QG_ERR_INVALID_ARG, "N and K must be positive (N=%lld K=%lld)", (long long)N, (long long)K);
     if ((bits < 2 || bits > 6) && bits != 8) return fail(QG_ERR_UNSUPPORTED, "bits must be 2..6 or 8 (got %d)", bits);
-    if (group != 64 && group != 128) return fail(QG_ERR_UNSUPPORTED, "group must be 64 or 128 (got %d)", group);
+    if (group != 32 && group != 64 && group != 128)
+        return fail(QG_ERR_UNSUPPORTED, "group must be 32, 64 or 128 (got %d)", group);
     if (K % group) return fail(QG_ERR_INVALID_ARG, "K=%lld is not a multiple of group=%d", (long long)K, group);
     if ((int64_t)N * K > (int64_t)1 << 34) return fail(QG_ERR_INVALID_ARG, "N*K too large");
     return QG_OK;

@@ -43,14 +43,22 @@ __global__ void __launch_bounds__(kThreads) k_diag(const uint16_t* __restrict__ 
     if (gid < (long long)N * ng) {
         const int n = (int)(gid / ng), j = (int)(gid % ng);
         const int k0 = j * G;
-        // codes of the group (8-byte aligned: G * BITS / 8 is a multiple of 8)
+        // codes of the group: 8-byte loads where G * BITS / 8 is a multiple
+        // of 8, else 4-byte ones (group 32 at odd widths)
         uint32_t w[NW + 1];
-        const uint2* pc = reinterpret_cast<const uint2*>(packed + (size_t)n * ((size_t)K * BITS / 8) + (size_t)k0 * BITS / 8);
+        const uint8_t* pg = packed + (size_t)n * ((size_t)K * BITS / 8) + (size_t)k0 * BITS / 8;
+        if constexpr (NW % 2 == 0) {
+            const uint2* pc = reinterpret_cast<const uint2*>(pg);
 #pragma unroll
-        for (int i = 0; i < NW / 2; i++) {
-            const uint2 v = __ldg(pc + i);
-            w[2 * i] = v.x;
-            w[2 * i + 1] = v.y;
+            for (int i = 0; i < NW / 2; i++) {
+                const uint2 v = __ldg(pc + i);
+                w[2 * i] = v.x;
+                w[2 * i + 1] = v.y;
+            }
+        } else {
+            const uint32_t* pc = reinterpret_cast<const uint32_t*>(pg);
+#pragma unroll
+            for (int i = 0; i < NW; i++) w[i] = __ldg(pc + i);
         }
         w[NW] = 0u;
         float s = 0.0f, z = 0.0f;
@@ -197,8 +205,9 @@ template <int BITS>
 qg_status run_bits(const uint16_t* W, const qg_qweight& w, float threshold, float* ratio, qg_diag* out, void* ws,
                    cudaStream_t s)
 {
-    return w.group == 64 ? run<BITS, 64>(W, w, threshold, ratio, out, ws, s)
-                         : run<BITS, 128>(W, w, threshold, ratio, out, ws, s);
+    return w.group == 32   ? run<BITS, 32>(W, w, threshold, ratio, out, ws, s)
+           : w.group == 64 ? run<BITS, 64>(W, w, threshold, ratio, out, ws, s)
+                           : run<BITS, 128>(W, w, threshold, ratio, out, ws, s);
 }
 
 }  // namespace diag

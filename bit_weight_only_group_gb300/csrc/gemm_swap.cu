@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 bool moe_tc_eligible(const qg_qweight* experts, int E, int n)
 {
     return n >= 1 && n <= swap::kMaxProducts && E * n <= swap::kMaxExperts && experts[0].bits == 4 &&
-           experts[0].K % swap::BK == 0;
+           experts[0].group != 32 && experts[0].K % swap::BK == 0;
 }
 
 size_t moe_tc_x16_bytes(int P, int K) { return align_up((size_t)P * K * 2, 256); }

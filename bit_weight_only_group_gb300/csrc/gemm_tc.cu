@@ -87,11 +87,11 @@ constexpr int B_BYTES = BN * BK * 2;   // 32 KB fp16
 
 // TILES: the codes and group parameters come from the tile-ordered copy
 // (one contiguous block per 256 rows x 64 k, staged by one bulk copy).
-template <int BITS, bool TILES>
+template <int BITS, int G, bool TILES>
 struct Cfg {
     static constexpr bool TMA_CODES = BITS == 4 && !TILES;
     static constexpr int SB = TILES || TMA_CODES ? 3 : 4;               // fp16 weight tiles
-    static constexpr int BLOCK = 2048 * BITS + (BITS == 2 ? 2048 : 1024);   // one tile-ordered block
+    static constexpr int BLOCK = (int)tile_block_bytes(BITS, G);         // one tile-ordered block
     static constexpr int P_BYTES = TMA_CODES ? BN * PK * BK * BITS / 8 : TILES ? BLOCK : 0;
     static constexpr int P_ALIGNED = TMA_CODES ? (P_BYTES + 1023) / 1024 * 1024 : (P_BYTES + 127) / 128 * 128;
     static constexpr int OFF_B = SA * A_BYTES;
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
               const __grid_constant__ Args a)
 {
-    using C = Cfg<BITS, TILES>;
+    using C = Cfg<BITS, G, TILES>;
     constexpr int SB = C::SB;
     constexpr int SP = C::SPN;
     extern __shared__ unsigned char smem_raw[];
@@ -252,7 +252,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nr = n0 + r;
         const int n = min(nr, a.N - 1);
         const int ng = a.ng;
-        constexpr int KB_PER_G = G / BK;                // 1 or 2
+        // this thread's group in block kb: kb / KB_PER_G (groups of 64 and
+        // 128 span one or two blocks), or 2 kb + hk at group 32 (each half of
+        // a block is a group of its own); GSTEP apart from one block's to the next
+        constexpr int KB_PER_G = G >= BK ? G / BK : 1;
+        constexpr int GSTEP = G >= BK ? 1 : BK / G;
+        const int g0 = G >= BK ? 0 : hk;
         // power-of-two headroom of this row (affine widths; codebook entries are fp16 already)
         int ex = 0;
         if constexpr (BITS != 2) ex = row_exponent<BITS>(a.scale + (size_t)n * ng, ng, hk);
@@ -269,9 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             else return make_uint2((uint32_t)__ldg(sp_row + gi), (uint32_t)__ldg(zp_row + gi));
         };
         if constexpr (!TILES) {
-            prm[0] = load_prm(0);
-            prm[1] = ng > 1 ? load_prm(1) : make_uint2(0u, 0u);
-            prm[2] = ng > 2 ? load_prm(2) : make_uint2(0u, 0u);
+            prm[0] = load_prm(g0);
+            prm[1] = g0 + GSTEP < ng ? load_prm(g0 + GSTEP) : make_uint2(0u, 0u);
+            prm[2] = g0 + 2 * GSTEP < ng ? load_prm(g0 + 2 * GSTEP) : make_uint2(0u, 0u);
         }
         // outlier cursor of this row: the next entry (ocol, oval) and the one
         // after it (ncol, nval), so that consuming an entry never waits for a load
@@ -343,17 +348,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // next group: shift the parameter window
         auto next_group = [&](int kb) {
             if (kb > 0 && kb % KB_PER_G == 0) {
-                const int gi = kb / KB_PER_G;
+                const int gi = g0 + (kb / KB_PER_G) * GSTEP;
                 prm[0] = prm[1];
                 prm[1] = prm[2];
-                if (gi + 2 < ng) prm[2] = load_prm(gi + 2);
+                if (gi + 2 * GSTEP < ng) prm[2] = load_prm(gi + 2 * GSTEP);
             }
         };
 
         if constexpr (TILES) {
             // codes and parameters of block kb from the tile ring: word i of
             // this thread's chunk at word i * 512 + threadIdx.x, the row's
-            // parameters after the 512 * BITS code words
+            // parameters after the 512 * BITS code words (NPG sets per row:
+            // at group 32 this thread's half of the block has its own)
+            constexpr int NPG = tile_groups_per_block(G);
             int sp = 0;
             uint32_t pp = 0;   // parity of full_p to wait for
             for (int kb = 0; kb < KB && ok; kb++) {
@@ -364,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < BITS; i++) w[i] = pw[i * 512 + threadIdx.x];
                 uint32_t pr[16];
                 if constexpr (BITS == 2) {
-                    const uint2 c = reinterpret_cast<const uint2*>(pw + BITS * 512)[r];
+                    const uint2 c = reinterpret_cast<const uint2*>(pw + BITS * 512)[r * NPG + (NPG == 2 ? hk : 0)];
                     const uint32_t lo = __byte_perm(c.x, c.y, 0x6420), hi = __byte_perm(c.x, c.y, 0x7531);
 #pragma unroll
                     for (int wi = 0; wi < 2; wi++)
@@ -375,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pr[2 * (4 * wi + jf) + 1] = cb_pair<1>(f, lo, hi);
                         }
                 } else {
-                    const uint32_t pq = pw[BITS * 512 + r];
+                    const uint32_t pq = pw[BITS * 512 + r * NPG + (NPG == 2 ? hk : 0)];
                     const uint32_t s2 = __byte_perm(f16_times_pow2(pq & 0xFFFFu, ex), 0u, 0x1010u);
                     const uint32_t zq = pq >> 16;
                     gemv::static_for<0, 16>([&](auto ec) {
@@ -608,7 +615,7 @@ template <int BITS, int G, bool TILES>
 qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void* tiles, void* y, int ldy,
               qg_ydtype yt, void* ws, cudaStream_t s)
 {
-    using C = Cfg<BITS, TILES>;
+    using C = Cfg<BITS, G, TILES>;
     Ws p{};
     ws_layout(M, w.K, &p, ws);
     {
@@ -651,8 +658,9 @@ template <int BITS, bool TILES>
 qg_status run_bits(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void* tiles, void* y, int ldy,
                    qg_ydtype yt, void* ws, cudaStream_t s)
 {
-    return w.group == 64 ? run<BITS, 64, TILES>(x, M, ldx, w, tiles, y, ldy, yt, ws, s)
-                         : run<BITS, 128, TILES>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
+    return w.group == 32   ? run<BITS, 32, TILES>(x, M, ldx, w, tiles, y, ldy, yt, ws, s)
+           : w.group == 64 ? run<BITS, 64, TILES>(x, M, ldx, w, tiles, y, ldy, yt, ws, s)
+                           : run<BITS, 128, TILES>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
 }
 
 }  // namespace tc

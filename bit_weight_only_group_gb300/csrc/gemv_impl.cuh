@@ -65,7 +65,12 @@ __host__ __device__ constexpr PairE plan_entry(int bits, int nc, int e)
         const int j = e / 4, q = e % 4;
         return PairE{8 * j + q, 8 * j + q + 4, (q & 1) * 4, (q & 1) * 4, 32 * j + (q / 2) * 8};
     }
-    if (bits == 2) {   // PRMT pairs: (j, j+4) and (j+8, j+12) within each 16-code word
+    if (bits == 2) {
+        if (nc == 8) {   // PRMT pairs of an 8-code chunk: (s, s+4) and (s+2, s+6) in step s
+            const int st = e / 2, h = e % 2;
+            return PairE{st + 2 * h, st + 2 * h + 4, 0, 0, 0};
+        }
+        // PRMT pairs: (j, j+4) and (j+8, j+12) within each 16-code word
         const int w = e / 8, j = (e % 8) / 2, h = e % 2;
         const int lo = 16 * w + (h ? 8 : 0) + j;
         return PairE{lo, lo + 4, 0, 0, 0};
@@ -84,7 +89,11 @@ __host__ __device__ constexpr PairE plan_entry(int bits, int nc, int e)
         const int lo = 8 * u + q;
         return PairE{lo, lo + 4, (q & 1) ? 7 : 4, (q & 1) ? 3 : 0, 24 * u + (q < 2 ? -4 : 2)};
     }
-    // bits == 5: one pair per window, found by an exhaustive search
+    // bits == 5: one pair per window
+    if (nc == 8) {     // (i, i+4): code i at bit 0 and code i+4 at bit 20 of the window at 5i
+        return PairE{e, e + 4, 0, 4, 5 * e};
+    }
+    // found by an exhaustive search
     if (nc == 16) {
         constexpr PairE t[8] = {{0, 3, 5, 4, -5},  {1, 4, 5, 4, 0},   {2, 6, 1, 5, 9},
                                 {5, 8, 5, 4, 20},  {7, 10, 5, 4, 30}, {9, 13, 1, 5, 44},
@@ -247,17 +256,20 @@ struct Chunk {
 #pragma unroll
             for (int i = 0; i < CB / 4; i++) w[i] = ldg_stream32(p + 4 * i);
         } else {
-            // 2-byte aligned chunk (group 64, odd width): aligned words, then
-            // shift by 16 bits when the chunk starts mid-word.  Every word read
-            // holds at least one byte of this group.
-            constexpr int NWL = (CB + 2 + 3) / 4;
+            // chunk at any byte offset (group 64 odd widths: 2-byte aligned;
+            // group 32 at 3 and 5 bits: byte aligned): the aligned words that
+            // hold its bytes, then a funnel shift by the chunk's offset in
+            // the first word.  Groups start 4-byte aligned and span a whole
+            // number of words, so every word read lies inside this group.
+            constexpr int NWL = (CB + 3 + 3) / 4;
             const uintptr_t a = reinterpret_cast<uintptr_t>(p);
             const uint8_t* base = reinterpret_cast<const uint8_t*>(a & ~uintptr_t(3));
+            const int off = (int)(a & 3u);
             uint32_t raw[NWL + 1];
 #pragma unroll
-            for (int i = 0; i < NWL; i++) raw[i] = ldg_stream32(base + 4 * i);
+            for (int i = 0; i < NWL; i++) raw[i] = (4 * i < off + CB) ? ldg_stream32(base + 4 * i) : 0u;
             raw[NWL] = 0u;
-            const int sh = (int)(a & 3u) * 8;   // 0 or 16
+            const int sh = off * 8;
 #pragma unroll
             for (int i = 0; i < NW; i++) w[i] = __funnelshift_r(raw[i], raw[i + 1], sh);
         }
@@ -456,6 +468,26 @@ __device__ __forceinline__ void mma_group(const uint32_t (&w0)[Chunk<BITS, G>::N
         const uint32_t H0 = __byte_perm(pr[0][0], pr[0][1], 0x7531);
         const uint32_t L1 = __byte_perm(pr[1][0], pr[1][1], 0x6420);
         const uint32_t H1 = __byte_perm(pr[1][0], pr[1][1], 0x7531);
+        if constexpr (C::NC == 8) {
+            // an 8-code chunk (group 32) fills two bytes: step s takes codes
+            // (s, s+4) from bit 2s of bytes 0 and 1 and (s+2, s+6) from bit
+            // 2s + 4, moved into bytes 2 and 3
+            static_for<0, 2>([&](auto sc) {
+                constexpr int s = decltype(sc)::value;
+                const uint32_t f0 = ((w0[0] >> (2 * s)) & 0x0303u) | ((w0[0] << (12 - 2 * s)) & 0x03030000u);
+                const uint32_t f1 = ((w1[0] >> (2 * s)) & 0x0303u) | ((w1[0] << (12 - 2 * s)) & 0x03030000u);
+                const uint32_t s0l = f0 * 0x11u + 0x4040u, s0h = __umulhi(f0, 0x00110000u) + 0x4040u;
+                const uint32_t s1l = f1 * 0x11u + 0x4040u, s1h = __umulhi(f1, 0x00110000u) + 0x4040u;
+                const uint32_t a0 = __byte_perm(L0, H0, s0l), a2 = __byte_perm(L0, H0, s0h);
+                const uint32_t a1 = __byte_perm(L1, H1, s1l), a3 = __byte_perm(L1, H1, s1h);
+#pragma unroll
+                for (int nt = 0; nt < NT; nt++) {
+                    const uint2 b = *reinterpret_cast<const uint2*>(xg[nt] + s * C::SSTRIDE);
+                    mma16816(yacc[nt], a0, a1, a2, a3, b.x, b.y);
+                }
+            });
+            return;
+        }
         static_for<0, NW>([&](auto wc) {
             constexpr int wi = decltype(wc)::value;
             static_for<0, 4>([&](auto jc) {
@@ -1025,28 +1057,64 @@ struct GroupedF {
     static qg_status run(const MoeTable& t, int mi, int ei, cudaStream_t s) { return grouped_mp<BITS, G, MP>(t, mi, ei, s); }
 };
 
-template <int BITS>
-qg_status launch_dense(const Problem& p, int G, cudaStream_t s)
+// One (width, group) pair: each is instantiated in a translation unit of its
+// own (gemv_w<bits>.cu for groups 64 and 128, gemv_w<bits>_g32.cu for 32) so
+// that the heavy template compiles in parallel.
+template <int BITS, int G>
+qg_status dense_g(const Problem& p, cudaStream_t s)
 {
-    const int mp = mp_for(p.M);
-    return G == 64 ? by_mp<BITS, 64, DenseF>(mp, p, s) : by_mp<BITS, 128, DenseF>(mp, p, s);
+    return by_mp<BITS, G, DenseF>(mp_for(p.M), p, s);
 }
 
-template <int BITS>
-qg_status launch_multi(const MultiTable& t, int G, cudaStream_t s)
+template <int BITS, int G>
+qg_status multi_g(const MultiTable& t, cudaStream_t s)
 {
-    const int mp = mp_for(t.p[0].M);
-    return G == 64 ? by_mp<BITS, 64, MultiF>(mp, t, s) : by_mp<BITS, 128, MultiF>(mp, t, s);
+    return by_mp<BITS, G, MultiF>(mp_for(t.p[0].M), t, s);
 }
 
 // t.chunk must equal the padded token count mp.  max_items bounds the
 // device-built item count; expect_items is the typical count (for choosing
 // the K split).
+template <int BITS, int G>
+qg_status grouped_g(const MoeTable& t, int max_items, int expect_items, int mp, cudaStream_t s)
+{
+    return by_mp<BITS, G, GroupedF>(mp, t, max_items, expect_items, s);
+}
+
+#define QG_GEMV_EXTERN(B, G)                                                                      \
+    extern template qg_status dense_g<B, G>(const Problem&, cudaStream_t);                       \
+    extern template qg_status multi_g<B, G>(const MultiTable&, cudaStream_t);                    \
+    extern template qg_status grouped_g<B, G>(const MoeTable&, int, int, int, cudaStream_t);
+#define QG_GEMV_INSTANTIATE(B, G)                                                                 \
+    template qg_status dense_g<B, G>(const Problem&, cudaStream_t);                              \
+    template qg_status multi_g<B, G>(const MultiTable&, cudaStream_t);                           \
+    template qg_status grouped_g<B, G>(const MoeTable&, int, int, int, cudaStream_t);
+#define QG_GEMV_EXTERN_WIDTH(B) QG_GEMV_EXTERN(B, 32) QG_GEMV_EXTERN(B, 64) QG_GEMV_EXTERN(B, 128)
+QG_GEMV_EXTERN_WIDTH(2)
+QG_GEMV_EXTERN_WIDTH(3)
+QG_GEMV_EXTERN_WIDTH(4)
+QG_GEMV_EXTERN_WIDTH(5)
+QG_GEMV_EXTERN_WIDTH(6)
+QG_GEMV_EXTERN_WIDTH(8)
+
+template <int BITS>
+qg_status launch_dense(const Problem& p, int G, cudaStream_t s)
+{
+    return G == 32 ? dense_g<BITS, 32>(p, s) : G == 64 ? dense_g<BITS, 64>(p, s) : dense_g<BITS, 128>(p, s);
+}
+
+template <int BITS>
+qg_status launch_multi(const MultiTable& t, int G, cudaStream_t s)
+{
+    return G == 32 ? multi_g<BITS, 32>(t, s) : G == 64 ? multi_g<BITS, 64>(t, s) : multi_g<BITS, 128>(t, s);
+}
+
 template <int BITS>
 qg_status launch_grouped(const MoeTable& t, int max_items, int expect_items, int G, int mp, cudaStream_t s)
 {
-    return G == 64 ? by_mp<BITS, 64, GroupedF>(mp, t, max_items, expect_items, s)
-                   : by_mp<BITS, 128, GroupedF>(mp, t, max_items, expect_items, s);
+    return G == 32   ? grouped_g<BITS, 32>(t, max_items, expect_items, mp, s)
+           : G == 64 ? grouped_g<BITS, 64>(t, max_items, expect_items, mp, s)
+                     : grouped_g<BITS, 128>(t, max_items, expect_items, mp, s);
 }
 
 }  // namespace gemv

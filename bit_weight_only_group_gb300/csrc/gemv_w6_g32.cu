@@ -1,0 +1,8 @@
+// Instantiation of the decode / grouped kernels for 6-bit weights, group 32.
+#include "gemv_impl.cuh"
+
+namespace qg {
+namespace gemv {
+QG_GEMV_INSTANTIATE(6, 32)
+}  // namespace gemv
+}  // namespace qg

@@ -68,14 +68,19 @@ qg_status launch_gemm(const uint16_t* x, int M, int ldx, const qg_qweight& w, vo
 // Tile-ordered copy of a quantized weight for the tensor-core kernel: for
 // every 256-row tile and 64-wide K block, one contiguous block of the
 // block's codes (word i of dequantization thread t = 2 * row + half at word
-// i * 512 + t) followed by its group parameters (one 32-bit word per row:
-// fp16 scale | zero-point << 16; at 2 bits the row's 4 fp16 codebook
-// entries), blocks in (row tile, K block) order.  Rows beyond N are zero.
+// i * 512 + t) followed by its group parameters (per row, for each group
+// the block touches -- two at group 32, else one -- a 32-bit word fp16
+// scale | zero-point << 16, or at 2 bits the 4 fp16 codebook entries),
+// blocks in (row tile, K block) order.  Rows beyond N are zero.
 constexpr int kTileRows = 256, kTileK = 64;
-__host__ __device__ constexpr size_t tile_block_bytes(int bits) { return (size_t)2048 * bits + (bits == 2 ? 2048 : 1024); }
+__host__ __device__ constexpr int tile_groups_per_block(int group) { return group == 32 ? 2 : 1; }
+__host__ __device__ constexpr size_t tile_block_bytes(int bits, int group)
+{
+    return (size_t)2048 * bits + (size_t)256 * (bits == 2 ? 8 : 4) * tile_groups_per_block(group);
+}
 inline size_t tiles_bytes(const qg_qweight& w)
 {
-    return (size_t)ceil_div(w.N, kTileRows) * (size_t)(w.K / kTileK) * tile_block_bytes(w.bits);
+    return (size_t)ceil_div(w.N, kTileRows) * (size_t)(w.K / kTileK) * tile_block_bytes(w.bits, w.group);
 }
 qg_status launch_repack(const qg_qweight& w, void* tiles, cudaStream_t s);
 // Tensor-core product over the tile-ordered copy (workspace: x in fp16, as

@@ -633,26 +633,26 @@ qg_status launch_quantize(const uint16_t* W, float /*frac*/, const qg_qweight& w
     const int blocks = (int)ceil_div(groups, threads);
     const unsigned short* Wh = reinterpret_cast<const unsigned short*>(W);
     if (w.bits == 2 && mode != 0) {
-        if (w.group == 64)
-            k_quant_uniform2<64><<<blocks, threads, 0, s>>>(Wh, w.N, w.K, mode, rp, w.out_col, w.packed, w.codebook,
-                                                            w.out_val);
-        else
-            k_quant_uniform2<128><<<blocks, threads, 0, s>>>(Wh, w.N, w.K, mode, rp, w.out_col, w.packed, w.codebook,
-                                                             w.out_val);
+        auto run = [&](auto kern) {
+            kern<<<blocks, threads, 0, s>>>(Wh, w.N, w.K, mode, rp, w.out_col, w.packed, w.codebook, w.out_val);
+        };
+        if (w.group == 32) run(k_quant_uniform2<32>);
+        else if (w.group == 64) run(k_quant_uniform2<64>);
+        else run(k_quant_uniform2<128>);
     } else if (w.bits == 2) {
-        if (w.group == 64)
-            k_quant_codebook<64><<<blocks, threads, 0, s>>>(Wh, w.N, w.K, rp, w.out_col, w.packed,
-                                                            w.codebook, w.out_val);
-        else
-            k_quant_codebook<128><<<blocks, threads, 0, s>>>(Wh, w.N, w.K, rp, w.out_col, w.packed,
-                                                             w.codebook, w.out_val);
+        auto run = [&](auto kern) {
+            kern<<<blocks, threads, 0, s>>>(Wh, w.N, w.K, rp, w.out_col, w.packed, w.codebook, w.out_val);
+        };
+        if (w.group == 32) run(k_quant_codebook<32>);
+        else if (w.group == 64) run(k_quant_codebook<64>);
+        else run(k_quant_codebook<128>);
     } else {
-        if (w.group == 64)
-            k_quant_affine<64><<<blocks, threads, 0, s>>>(Wh, w.N, w.K, w.bits, mode, rp, w.out_col, w.packed,
-                                                          w.scale, w.zp);
-        else
-            k_quant_affine<128><<<blocks, threads, 0, s>>>(Wh, w.N, w.K, w.bits, mode, rp, w.out_col, w.packed,
-                                                           w.scale, w.zp);
+        auto run = [&](auto kern) {
+            kern<<<blocks, threads, 0, s>>>(Wh, w.N, w.K, w.bits, mode, rp, w.out_col, w.packed, w.scale, w.zp);
+        };
+        if (w.group == 32) run(k_quant_affine<32>);
+        else if (w.group == 64) run(k_quant_affine<64>);
+        else run(k_quant_affine<128>);
     }
     k_quant_done<<<1, 32, 0, s>>>();
     e = cudaGetLastError();

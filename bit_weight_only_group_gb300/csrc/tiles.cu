@@ -8,11 +8,13 @@
 //           t = 2 * row + half (codes [32 half, 32 half + 32) of the row in
 //           this K block, LSB-first as in the planar stream) at word
 //           i * 512 + t: a warp's 32 threads read 32 consecutive words;
-//   params  one 32-bit word per row (fp16 scale | zero-point << 16), or at
-//           2 bits the row's four fp16 codebook entries (8 bytes);
+//   params  per row, for each group the block touches (two at group 32,
+//           else one) a 32-bit word (fp16 scale | zero-point << 16), or at
+//           2 bits the four fp16 codebook entries (8 bytes);
 // rows beyond N are zero.  The FP16 outliers stay in their CSR arrays.
 // One CTA of 512 threads per block; a thread moves its chunk's words and
-// (on even threads) the row's parameters.
+// the parameters of its chunk's group (at group 32; else the even thread
+// writes the row's one set).
 #include "qg_internal.h"
 
 namespace qg {
@@ -26,21 +28,23 @@ __global__ void __launch_bounds__(512) k_repack(const uint8_t* __restrict__ pack
     const int kb = blockIdx.x, nt = blockIdx.y, KB = K / kTileK;
     const int t = threadIdx.x, r = t >> 1, h = t & 1;
     const int n = nt * kTileRows + r;
-    uint32_t* blk = reinterpret_cast<uint32_t*>(tiles + ((size_t)nt * KB + kb) * tile_block_bytes(BITS));
+    uint32_t* blk = reinterpret_cast<uint32_t*>(tiles + ((size_t)nt * KB + kb) * tile_block_bytes(BITS, G));
     const bool live = n < N;
     // the chunk: 4 * BITS bytes at byte (2 kb + h) * 4 * BITS of the row (word aligned)
     const uint32_t* src = reinterpret_cast<const uint32_t*>(packed + (size_t)n * ((size_t)K * BITS / 8) +
                                                             (size_t)(2 * kb + h) * 4 * BITS);
 #pragma unroll
     for (int i = 0; i < BITS; i++) blk[i * 512 + t] = live ? __ldg(src + i) : 0u;
-    if (h == 0) {
-        const int g = kb * kTileK / G, ng = K / G;
+    const int npg = tile_groups_per_block(G);
+    if (npg == 2 || h == 0) {
+        const int g = (kb * kTileK + 32 * h) / G, ng = K / G;
+        const int slot = r * npg + (npg == 2 ? h : 0);
         uint32_t* prm = blk + BITS * 512;
         if constexpr (BITS == 2) {
-            reinterpret_cast<uint2*>(prm)[r] = live ? __ldg(cb + (size_t)n * ng + g) : make_uint2(0u, 0u);
+            reinterpret_cast<uint2*>(prm)[slot] = live ? __ldg(cb + (size_t)n * ng + g) : make_uint2(0u, 0u);
         } else {
-            prm[r] = live ? ((uint32_t)__ldg(scale + (size_t)n * ng + g) | ((uint32_t)__ldg(zp + (size_t)n * ng + g) << 16))
-                          : 0u;
+            prm[slot] = live ? ((uint32_t)__ldg(scale + (size_t)n * ng + g) | ((uint32_t)__ldg(zp + (size_t)n * ng + g) << 16))
+                             : 0u;
         }
     }
 }

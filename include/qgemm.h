@@ -9,7 +9,9 @@
  *    zero_point = qmin - round(min / scale), q = round(w / scale) +
  *    zero_point, w_hat = (q - zero_point) * scale  ("Inference acceleration guide" page,
  *    section 1.1 "quantization is a lossy mapping");
- *  - statistics per group of consecutive weights along K (64 or 128), after
+ *  - statistics per group of consecutive weights along K (32, 64 or 128;
+ *    the "Mixed-width quantization" page, section 2.3, pairs the narrow
+ *    widths with blocks of 32 and the wide ones with 64 or 128), after
  *    excluding the largest-magnitude 0.1 % of weights, which are kept in FP16
  *    and added back after the product  ("70B on one GPU" page, section 2,
  *    "group-wise outlier-aware quantization", steps 1-3);
@@ -72,7 +74,7 @@ typedef enum { QG_Y_F32 = 0, QG_Y_BF16 = 1 } qg_ydtype;
  *
  *  N, K        output and input features.  K % group == 0.
  *  bits        2, 3, 4, 5, 6 or 8 (8: one byte per code).
- *  group       64 or 128 consecutive weights along K share a scale/zp
+ *  group       32, 64 or 128 consecutive weights along K share a scale/zp
  *              (or, at 2 bits, a codebook).  ng = K / group.
  *  packed      uint8 [N, K*bits/8], row-major; row n holds the K codes of
  *              row n as one LSB-first stream.  16-byte aligned.
@@ -106,7 +108,7 @@ typedef struct {
  * 2 + 64/group (2-bit codebook of 4 fp16 entries); "Mixed-width quantization" page, section 2.3
  * gives the same accounting for the scale overhead.
  * Errors: QG_ERR_INVALID_ARG for N, K <= 0, K % group, outlier_frac outside
- * [0, 1); QG_ERR_UNSUPPORTED for bits outside {2..6, 8} or group not 64/128.
+ * [0, 1); QG_ERR_UNSUPPORTED for bits outside {2..6, 8} or group not 32/64/128.
  */
 QG_API qg_status qpack_query_sizes(int32_t N, int32_t K, int32_t bits, int32_t group, float outlier_frac,
                             size_t* packed_bytes, size_t* scale_bytes, size_t* zp_bytes,
@@ -257,14 +259,15 @@ QG_API qg_status qgemm_forward_multi(const uint16_t* x, int32_t M, int32_t ldx, 
  * gain about 8 %; "70B on one GPU" page, section 3: the weights are
  * repacked once, when the model is loaded, for the fused kernel).
  * Layout: for every 256-row tile (rows n0 .. n0+255) and 64-wide K block kb,
- * one contiguous block of tile_block_bytes(bits) = 2048*bits + (bits == 2 ?
- * 2048 : 1024) bytes, at byte (tile * (K/64) + kb) * tile_block_bytes:
+ * one contiguous block of tile_block_bytes = 2048*bits + 256*P*G bytes
+ * (P = 8 at 2 bits, else 4; G = 2 at group 32, else 1), at byte
+ * (tile * (K/64) + kb) * tile_block_bytes:
  *   words [0, 512*bits): word i of thread t = 2*r + h at word i*512 + t,
  *     where the thread's chunk is the 32 codes [64 kb + 32 h, 64 kb + 32 h +
  *     32) of row n0 + r as 4*bits bytes of the planar LSB-first stream;
- *   then per row r: one 32-bit word fp16 scale | zero-point << 16 of the
- *     group holding the block (bits != 2), or the group's 4 fp16 codebook
- *     entries (8 bytes, bits == 2).
+ *   then per row r, for each of the G groups the block touches (in K
+ *     order): one 32-bit word fp16 scale | zero-point << 16 (bits != 2), or
+ *     the group's 4 fp16 codebook entries (8 bytes, bits == 2).
  * Rows beyond N are zero.  Every block starts on a 128-byte boundary, so
  * the kernel stages one block with one bulk copy and reads codes and
  * parameters from shared memory.  The outlier CSR stays in the descriptor.

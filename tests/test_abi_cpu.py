@@ -37,7 +37,8 @@ def test_every_declared_symbol_is_exported(qg):
 
 @pytest.mark.parametrize("N,K,bits,group,frac", [
     (4096, 4096, 4, 128, 0.0), (4096, 4096, 2, 128, 0.001), (11008, 4096, 3, 64, 0.001),
-    (4096, 11008, 5, 128, 0.001), (1024, 8192, 6, 64, 0.002), (7, 64, 2, 64, 0.5)])
+    (4096, 11008, 5, 128, 0.001), (1024, 8192, 6, 64, 0.002), (7, 64, 2, 64, 0.5), (4096, 4096, 3, 32, 0.001),
+    (96, 256, 2, 32, 0.0)])
 def test_sizes_match_oracle(qg, N, K, bits, group, frac):
     got = qg.qpack_query_sizes(N, K, bits, group, frac)
     ref = oracle.sizes(N, K, bits, group, frac)
@@ -53,7 +54,7 @@ def test_sizes_reject_bad_shapes(qg):
         qg.qpack_query_sizes(64, 128, 7, 64)
     assert e.value.status == -2
     with pytest.raises(qg.QgError) as e:
-        qg.qpack_query_sizes(64, 128, 4, 32)
+        qg.qpack_query_sizes(64, 128, 4, 16)
     assert e.value.status == -2
     with pytest.raises(qg.QgError) as e:
         qg.qpack_query_sizes(64, 128, 4, 64, 1.0)
@@ -88,7 +89,7 @@ def test_host_validation_without_gpu(qg):
     bad = _fake_desc(qg, base=0x100004)
     assert L.qgemm_forward(x, 1, 128, ctypes.byref(bad), y, 64, 0, None, 0, None) == -3
     # unsupported width and group
-    for dd in (_fake_desc(qg, bits=7), _fake_desc(qg, group=32)):
+    for dd in (_fake_desc(qg, bits=7), _fake_desc(qg, group=16)):
         assert L.qgemm_forward(x, 1, 128, ctypes.byref(dd), y, 64, 0, None, 0, None) == -2
     # outliers declared but arrays missing
     assert L.qgemm_forward(x, 1, 128, ctypes.byref(_fake_desc(qg, nnz=3)), y, 64, 0, None, 0, None) == -1
@@ -142,7 +143,7 @@ def test_both_quantizers_refuse_the_same_bad_descriptors(qg):
     d = good(); d.out_col = None; cases.append(("null outlier array", d, 0.001, -1))
     d = good(); d.N, d.K, d.nnz = 1 << 20, 1 << 15, 0; cases.append(("N*K above the product limit", d, 0.0, -1))
     d = good(); d.bits = 7; cases.append(("unsupported width", d, 0.001, -2))
-    d = good(); d.group = 32; cases.append(("unsupported group", d, 0.001, -2))
+    d = good(); d.group = 256; cases.append(("unsupported group", d, 0.001, -2))
     d = good(); cases.append(("outlier_frac out of range", d, 1.5, -1))
     for what, d, frac, expect in cases:
         a = L.qpack_quantize(W, frac, ctypes.byref(d), ws, 1 << 30, None)

@@ -37,7 +37,7 @@ def _check(got, ref):
 
 
 @pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
-@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("group", [32, 64, 128])
 def test_diagnostics_against_oracle(qg, bits, group):
     N, K, frac = 200, 1024, 0.002
     W = wl.gen_weight(N, K, seed=bits + group, outlier_frac=frac, outlier_seed=9)

@@ -31,7 +31,7 @@ def _weights(N, K, bits, group, frac, seed):
 
 
 @pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
-@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("group", [32, 64, 128])
 @pytest.mark.parametrize("M", [1, 2, 3, 5, 8, 16, 27, 64])
 def test_product_small(qg, bits, group, M):
     N, K, frac = 200, 1024, 0.002            # N not a multiple of the 64-row tile
@@ -104,7 +104,7 @@ def test_product_4096(qg, bits, group, M):
     check_product(y, oracle.linear(x, q), x, wmax)
 
 
-@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("group", [32, 64, 128])
 @pytest.mark.parametrize("M,N,K", [(300, 600, 1024), (129, 256, 384), (1000, 700, 512)])
 def test_tensor_core_path_against_oracle(qg, group, M, N, K):
     # M above the decode range runs the tcgen05 kernel (128 x 256 tiles, K in
@@ -121,7 +121,7 @@ def test_tensor_core_path_against_oracle(qg, group, M, N, K):
 
 
 @pytest.mark.parametrize("bits", [2, 3, 5, 6, 8])
-@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("group", [32, 64, 128])
 @pytest.mark.parametrize("M,N,K", [(300, 600, 1024), (129, 200, 384)])
 def test_tensor_core_path_every_width(qg, bits, group, M, N, K):
     # 2/3/5/6-bit weights above the decode range: the tcgen05 kernel with the
@@ -185,7 +185,7 @@ def test_bounded_wait_gives_up_and_reports_timeout(qg):
     assert qg.qgemm_device_status() == 0
 
 
-@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("group", [32, 64, 128])
 def test_tensor_core_path_repeatable(qg, group):
     # the accumulation order of the tensor-core kernel is fixed, so repeated
     # calls must agree bit for bit; a ring slot reused too early shows up here
@@ -215,7 +215,7 @@ def test_tensor_core_path_full_size_sampled(qg):
         check_product(y[toks.cuda(), n0:n1], oracle.linear(x[toks], q, n0, n1), x[toks], wmax)
 
 
-@pytest.mark.parametrize("bits,group,M", [(4, 128, 1), (4, 128, 8), (3, 64, 16), (4, 128, 130)])
+@pytest.mark.parametrize("bits,group,M", [(4, 128, 1), (4, 128, 8), (3, 64, 16), (4, 128, 130), (5, 32, 4), (2, 32, 130)])
 def test_forward_multi_against_oracle(qg, bits, group, M):
     # a fused projection: three weights sharing x (different N, one ragged
     # tile) in one call; each output is the single product of its weight

@@ -24,7 +24,7 @@ def _experts(E, N, K, bits, group, frac, seed):
     return qs, wmax
 
 
-@pytest.mark.parametrize("bits,group", [(4, 128), (2, 64), (5, 128), (8, 64)])
+@pytest.mark.parametrize("bits,group", [(4, 128), (2, 64), (5, 128), (8, 64), (4, 32), (3, 32)])
 @pytest.mark.parametrize("T,k,E", [(37, 2, 4), (128, 2, 8), (3, 3, 5)])
 def test_moe_small(qg, bits, group, T, k, E):
     N, K = 136, 512

@@ -25,7 +25,7 @@ def _run(qg, W, bits, group, frac):
 
 
 @pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
-@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("group", [32, 64, 128])
 @pytest.mark.parametrize("N,K,frac", [(96, 512, 0.002), (33, 256, 0.0), (7, 1024, 0.01)])
 def test_quantize_bit_exact_small(qg, bits, group, N, K, frac):
     W = wl.gen_weight(N, K, seed=1000 + N + bits, outlier_frac=frac, outlier_seed=2000 + group)

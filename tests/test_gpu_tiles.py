@@ -21,7 +21,7 @@ def qg():
 
 
 @pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
-@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("group", [32, 64, 128])
 def test_repack_bytes_equal_the_oracle_layout(qg, bits, group):
     N, K = 300, 512
     q = oracle.quantize(wl.gen_weight(N, K, seed=bits + group, outlier_frac=0.003, outlier_seed=1), bits, group, 0.003)
@@ -31,7 +31,7 @@ def test_repack_bytes_equal_the_oracle_layout(qg, bits, group):
 
 
 @pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
-@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("group", [32, 64, 128])
 @pytest.mark.parametrize("M", [1, 100, 300])
 def test_tiles_product(qg, bits, group, M):
     N, K, frac = 300, 1024, 0.003

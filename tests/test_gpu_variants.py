@@ -22,7 +22,7 @@ def qg():
 
 
 @pytest.mark.parametrize("bits,mode", CASES)
-@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("group", [32, 64, 128])
 @pytest.mark.parametrize("frac", [0.0, 0.003])
 def test_variant_quantize_bit_exact(qg, bits, mode, group, frac):
     W = wl.gen_weight(136, 1024, seed=bits + group, outlier_frac=frac, outlier_seed=5)

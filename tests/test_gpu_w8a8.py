@@ -26,7 +26,7 @@ def _xhat(x):
 
 
 @pytest.mark.parametrize("mode", ["asymmetric", "symmetric"])
-@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("group", [32, 64, 128])
 @pytest.mark.parametrize("M", [1, 2, 3, 8, 16])
 def test_w8a8_against_oracle(qg, mode, group, M):
     N, K, frac = 200, 1024, 0.003
