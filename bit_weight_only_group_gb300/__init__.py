@@ -56,7 +56,9 @@ class QgQWeight(ctypes.Structure):
                 ("group", ctypes.c_int32), ("packed", ctypes.c_void_p), ("scale", ctypes.c_void_p),
                 ("zp", ctypes.c_void_p), ("codebook", ctypes.c_void_p), ("nnz", ctypes.c_int32),
                 ("out_row_ptr", ctypes.c_void_p), ("out_col", ctypes.c_void_p),
-                ("out_val", ctypes.c_void_p)]
+                ("out_val", ctypes.c_void_p), ("scale8", ctypes.c_void_p), ("scale8_exp", ctypes.c_void_p),
+                ("fb_row_ptr", ctypes.c_void_p), ("fb_col", ctypes.c_void_p), ("fb_val", ctypes.c_void_p),
+                ("fb_cap", ctypes.c_int32)]
 
 
 _lib = None
@@ -152,46 +154,70 @@ class QWeight:
     col: torch.Tensor | None             # int32 [nnz]
     val: torch.Tensor | None             # int16 (fp16 bits) [nnz]
     nnz: int = 0
+    # 8-bit (E4M3) scales in place of ``scale``, with the fp16 fallback list
+    scale8: torch.Tensor | None = None       # uint8 [N, K/group], 0x7F = fallback
+    scale8_exp: torch.Tensor | None = None   # int32 [1]: the matrix exponent E
+    fb_row_ptr: torch.Tensor | None = None   # int32 [N+1]
+    fb_col: torch.Tensor | None = None       # int32 [fb_cap]
+    fb_val: torch.Tensor | None = None       # int16 (fp16 bits) [fb_cap]
 
     @staticmethod
-    def empty(N: int, K: int, bits: int, group: int, outlier_frac: float = 0.0, device="cuda") -> "QWeight":
+    def empty(N: int, K: int, bits: int, group: int, outlier_frac: float = 0.0, device="cuda",
+              scale_fmt: str = "fp16", fb_cap: int | None = None) -> "QWeight":
+        """Buffers for a quantized matrix.  scale_fmt 'fp8': 8-bit scales
+        with a fallback list of fb_cap entries (default: 1 % of the groups,
+        at least 64)."""
         sz = qpack_query_sizes(N, K, bits, group, outlier_frac)
         ng = K // group
         u8, i16, i32 = torch.uint8, torch.int16, torch.int32
         nnz = sz["nnz"]
+        f8 = scale_fmt == "fp8"
+        if f8 and fb_cap is None:
+            fb_cap = max(64, N * ng // 100)
         return QWeight(
             N, K, bits, group,
             packed=torch.empty((N, K * bits // 8), dtype=u8, device=device),
-            scale=torch.empty((N, ng), dtype=i16, device=device) if bits != 2 else None,
+            scale=torch.empty((N, ng), dtype=i16, device=device) if bits != 2 and not f8 else None,
             zp=torch.empty((N, ng), dtype=u8, device=device) if bits != 2 else None,
             codebook=torch.empty((N, ng, 4), dtype=i16, device=device) if bits == 2 else None,
             row_ptr=torch.empty(N + 1, dtype=i32, device=device),
             col=torch.empty(max(nnz, 1), dtype=i32, device=device)[:nnz],
             val=torch.empty(max(nnz, 1), dtype=i16, device=device)[:nnz],
-            nnz=nnz)
+            nnz=nnz,
+            scale8=torch.empty((N, ng), dtype=u8, device=device) if f8 else None,
+            scale8_exp=torch.zeros(1, dtype=i32, device=device) if f8 else None,
+            fb_row_ptr=torch.zeros(N + 1, dtype=i32, device=device) if f8 else None,
+            fb_col=torch.empty(max(fb_cap, 1), dtype=i32, device=device)[:fb_cap] if f8 else None,
+            fb_val=torch.empty(max(fb_cap, 1), dtype=i16, device=device)[:fb_cap] if f8 else None)
+
+    @property
+    def fb_cap(self) -> int:
+        return 0 if self.fb_col is None else int(self.fb_col.numel())
 
     def desc(self) -> QgQWeight:
         return QgQWeight(self.N, self.K, self.bits, self.group, _ptr(self.packed), _ptr(self.scale),
                          _ptr(self.zp), _ptr(self.codebook), self.nnz, _ptr(self.row_ptr),
-                         _ptr(self.col), _ptr(self.val))
+                         _ptr(self.col), _ptr(self.val), _ptr(self.scale8), _ptr(self.scale8_exp),
+                         _ptr(self.fb_row_ptr), _ptr(self.fb_col), _ptr(self.fb_val), self.fb_cap)
 
     def nbytes(self) -> int:
         return sum(t.numel() * t.element_size() for t in
-                   (self.packed, self.scale, self.zp, self.codebook, self.row_ptr, self.col, self.val)
+                   (self.packed, self.scale, self.zp, self.codebook, self.row_ptr, self.col, self.val,
+                    self.scale8, self.scale8_exp, self.fb_row_ptr, self.fb_col, self.fb_val)
                    if t is not None)
 
 
 def qpack_quantize(W: torch.Tensor, bits: int, group: int, outlier_frac: float = 0.0,
                    out: QWeight | None = None, workspace: torch.Tensor | None = None, stream=None,
-                   mode: str = "asymmetric") -> QWeight:
+                   mode: str = "asymmetric", scale_fmt: str = "fp16", fb_cap: int | None = None) -> QWeight:
     """Quantize and pack W [N, K] (fp16, CUDA) on the device.  mode:
     'asymmetric' (qpack_quantize), 'symmetric' or 'linear2'
-    (qpack_quantize_mode)."""
+    (qpack_quantize_mode); scale_fmt 'fp8': 8-bit scales (bits 3..8)."""
     if W.dtype != torch.float16 or not W.is_cuda or W.dim() != 2:
         raise ValueError("W must be a 2-D float16 CUDA tensor")
     W = W.contiguous()
     N, K = W.shape
-    qw = out if out is not None else QWeight.empty(N, K, bits, group, outlier_frac, W.device)
+    qw = out if out is not None else QWeight.empty(N, K, bits, group, outlier_frac, W.device, scale_fmt, fb_cap)
     ws_bytes = qpack_workspace_size(N, K)
     ws = workspace if workspace is not None else torch.empty(ws_bytes, dtype=torch.uint8, device=W.device)
     d = qw.desc()
@@ -205,14 +231,14 @@ def qpack_quantize(W: torch.Tensor, bits: int, group: int, outlier_frac: float =
 
 
 def qpack_quantize_noalloc(W: torch.Tensor, bits: int, group: int, outlier_frac: float = 0.0,
-                           out: QWeight | None = None, stream=None) -> QWeight:
+                           out: QWeight | None = None, stream=None, scale_fmt: str = "fp16") -> QWeight:
     """qpack_quantize for callers that cannot allocate device memory: the
     library uses its own fixed scratch array (see include/qgemm.h).  Pass
     ``out`` (allocated beforehand) to keep this call allocation-free."""
     if W.dtype != torch.float16 or not W.is_cuda or W.dim() != 2 or not W.is_contiguous():
         raise ValueError("W must be a contiguous 2-D float16 CUDA tensor")
     N, K = W.shape
-    qw = out if out is not None else QWeight.empty(N, K, bits, group, outlier_frac, W.device)
+    qw = out if out is not None else QWeight.empty(N, K, bits, group, outlier_frac, W.device, scale_fmt)
     f = lib().qpack_quantize_noalloc
     f.argtypes = [ctypes.c_void_p, ctypes.c_float, ctypes.POINTER(QgQWeight), ctypes.c_void_p]
     f.restype = ctypes.c_int

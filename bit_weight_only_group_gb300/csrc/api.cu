@@ -112,8 +112,19 @@ qg_status check_qweight(const qg_qweight* w, const char* who)
     if (!w->packed) return fail(QG_ERR_INVALID_ARG, "%s: packed is null", who);
     if (!aligned(w->packed, 16)) return fail(QG_ERR_ALIGNMENT, "%s: packed must be 16-byte aligned", who);
     if (w->bits == 2) {
+        if (w->scale8) return fail(QG_ERR_INVALID_ARG, "%s: 8-bit scales need bits 3..8 (2 bits use codebooks)", who);
         if (!w->codebook) return fail(QG_ERR_INVALID_ARG, "%s: codebook is null for bits=2", who);
         if (!aligned(w->codebook, 8)) return fail(QG_ERR_ALIGNMENT, "%s: codebook must be 8-byte aligned", who);
+    } else if (w->scale8) {
+        // 8-bit scales with the fp16 fallback list (scale unused)
+        if (!w->zp || !w->scale8_exp || !w->fb_row_ptr)
+            return fail(QG_ERR_INVALID_ARG, "%s: zp, scale8_exp or fb_row_ptr null with 8-bit scales", who);
+        if (w->fb_cap < 0) return fail(QG_ERR_INVALID_ARG, "%s: fb_cap < 0", who);
+        if (w->fb_cap > 0 && (!w->fb_col || !w->fb_val))
+            return fail(QG_ERR_INVALID_ARG, "%s: fallback arrays null with fb_cap=%d", who, w->fb_cap);
+        if (!aligned(w->scale8_exp, 4) || !aligned(w->fb_row_ptr, 4) || !aligned(w->fb_col, 4) ||
+            !aligned(w->fb_val, 2))
+            return fail(QG_ERR_ALIGNMENT, "%s: scale8_exp or fallback arrays misaligned", who);
     } else {
         if (!w->scale || !w->zp) return fail(QG_ERR_INVALID_ARG, "%s: scale/zp null for bits=%d", who, w->bits);
         if (!aligned(w->scale, 2)) return fail(QG_ERR_ALIGNMENT, "%s: scale must be 2-byte aligned", who);

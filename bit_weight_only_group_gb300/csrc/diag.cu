@@ -14,6 +14,7 @@
 #include <cmath>
 
 #include "qg_internal.h"
+#include "scale8.cuh"
 
 namespace qg {
 namespace diag {
@@ -29,7 +30,7 @@ __device__ __forceinline__ float h2f(uint32_t h) { return __half2float(__ushort_
 template <int BITS, int G>
 __global__ void __launch_bounds__(kThreads) k_diag(const uint16_t* __restrict__ W, int N, int K,
                                                     const uint8_t* __restrict__ packed,
-                                                    const uint16_t* __restrict__ scale, const uint8_t* __restrict__ zp,
+                                                    const ScaleSrc sc, const uint8_t* __restrict__ zp,
                                                     const uint2* __restrict__ cb, const int* __restrict__ row_ptr,
                                                     const int* __restrict__ col, const uint16_t* __restrict__ val,
                                                     int nnz, float threshold, float* __restrict__ ratio,
@@ -67,7 +68,7 @@ __global__ void __launch_bounds__(kThreads) k_diag(const uint16_t* __restrict__ 
             const uint2 c = __ldg(cb + (size_t)n * ng + j);
             e4[0] = h2f(c.x & 0xFFFFu); e4[1] = h2f(c.x >> 16); e4[2] = h2f(c.y & 0xFFFFu); e4[3] = h2f(c.y >> 16);
         } else {
-            s = h2f(__ldg(scale + (size_t)n * ng + j));
+            s = h2f(scale_bits(sc, scale_exp(sc), n, ng, j));
             z = (float)__ldg(zp + (size_t)n * ng + j);
         }
         // first outlier of the row at or after column k0 (columns ascend)
@@ -192,7 +193,7 @@ qg_status run(const uint16_t* W, const qg_qweight& w, float threshold, float* ra
 {
     const int P = blocks_for(w.N, w.K, G);
     Partial* part = static_cast<Partial*>(ws);
-    k_diag<BITS, G><<<P, kThreads, 0, s>>>(W, w.N, w.K, w.packed, w.scale, w.zp,
+    k_diag<BITS, G><<<P, kThreads, 0, s>>>(W, w.N, w.K, w.packed, scale_src(w), w.zp,
                                            reinterpret_cast<const uint2*>(w.codebook), w.out_row_ptr, w.out_col,
                                            w.out_val, w.nnz, threshold, ratio, part);
     k_diag_final<<<1, 256, 0, s>>>(part, P, (long long)w.N * w.K, out);

@@ -123,6 +123,12 @@ gemv::Problem make_problem(const uint16_t* x, int M, int ldx, const qg_qweight& 
     p.nnz = w.nnz;
     p.y = y; p.ldy = ldy; p.y_bf16 = yt == QG_Y_BF16;
     p.magic = gemv::kF16Magic;
+    p.scale8 = w.scale8;
+    p.scale8_exp = w.scale8_exp;
+    p.fb_row_ptr = w.fb_row_ptr;
+    p.fb_col = w.fb_col;
+    p.fb_val = w.fb_val;
+    p.fb_cap = w.fb_cap;
     return p;
 }
 
@@ -312,6 +318,12 @@ qg_status launch_moe(const uint16_t* x, int T, const int32_t* topk, int k, const
             t.col[i] = ex[i].out_col;
             t.val[i] = ex[i].out_val;
             t.nnz[i] = ex[i].nnz;
+            t.scale8[i] = ex[i].scale8;
+            t.scale8_exp[i] = ex[i].scale8_exp;
+            t.fb_row_ptr[i] = ex[i].fb_row_ptr;
+            t.fb_col[i] = ex[i].fb_col;
+            t.fb_val[i] = ex[i].fb_val;
+            t.fb_cap[i] = ex[i].fb_cap;
         }
         const int maxi = max_items_for(P, E, t.chunk);
         const int expect = std::min(maxi, (int)ceil_div(P, t.chunk) + E / 2);

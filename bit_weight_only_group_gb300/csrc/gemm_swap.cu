@@ -424,8 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 bool moe_tc_eligible(const qg_qweight* experts, int E, int n)
 {
-    return n >= 1 && n <= swap::kMaxProducts && E * n <= swap::kMaxExperts && experts[0].bits == 4 &&
-           experts[0].group != 32 && experts[0].K % swap::BK == 0;
+    if (!(n >= 1 && n <= swap::kMaxProducts && E * n <= swap::kMaxExperts && experts[0].bits == 4 &&
+          experts[0].group != 32 && experts[0].K % swap::BK == 0))
+        return false;
+    for (int i = 0; i < E * n; i++)   // 8-bit scales take the grouped decode kernel
+        if (experts[i].scale8) return false;
+    return true;
 }
 
 size_t moe_tc_x16_bytes(int P, int K) { return align_up((size_t)P * K * 2, 256); }

@@ -120,6 +120,7 @@ struct Args {
     int y_bf16;
     int* status;
     uint32_t magic;   // gemv::kF16Magic, a run-time value (one logic op per code pair)
+    ScaleSrc sc;      // 8-bit scales when sc.scale8 is set (planar kernels; the tile copy holds fp16)
 };
 
 static_assert(kDeqWarps * 32 == 512, "deq_sync counts 512 dequantization threads");
@@ -260,18 +261,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g0 = G >= BK ? 0 : hk;
         // power-of-two headroom of this row (affine widths; codebook entries are fp16 already)
         int ex = 0;
-        if constexpr (BITS != 2) ex = row_exponent<BITS>(a.scale + (size_t)n * ng, ng, hk);
+        // 8-bit scales: the planar kernels convert each code where it is used
+        // (the tile-ordered copy already holds fp16 scales); both find the
+        // row exponent from the codes
+        const bool has8 = a.sc.scale8 != nullptr;
+        const bool s8 = !TILES && has8;
+        const int E8 = has8 ? __ldg(a.sc.exp) : 0;
+        if constexpr (BITS != 2) {
+            if (has8) ex = row_exponent_8<BITS>(a.sc, E8, n, ng, hk);
+            else ex = row_exponent<BITS>(a.scale + (size_t)n * ng, ng, hk);
+        }
         if (hk == 0) e_row[r] = (uint8_t)ex;
         // group parameters of the current group and of the next two (loads in
         // flight: kept raw until the group is used, the row exponent applied
         // then): affine (scale bits, zero-point); codebook (two words of 4 fp16)
         const uint16_t* sp_row = a.scale + (size_t)n * ng;
+        const uint8_t* s8_row = a.sc.scale8 + (size_t)n * ng;
         const uint8_t* zp_row = a.zp + (size_t)n * ng;
         const uint2* cb_row = a.cb + (size_t)n * ng;
         uint2 prm[3];
         auto load_prm = [&](int gi) -> uint2 {
             if constexpr (BITS == 2) return __ldg(cb_row + gi);
-            else return make_uint2((uint32_t)__ldg(sp_row + gi), (uint32_t)__ldg(zp_row + gi));
+            else return make_uint2(s8 ? (uint32_t)__ldg(s8_row + gi) : (uint32_t)__ldg(sp_row + gi),
+                                   (uint32_t)__ldg(zp_row + gi));
         };
         if constexpr (!TILES) {
             prm[0] = load_prm(g0);
@@ -346,14 +358,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
         // next group: shift the parameter window
+        int gcur = g0;   // group of prm[0]
         auto next_group = [&](int kb) {
             if (kb > 0 && kb % KB_PER_G == 0) {
                 const int gi = g0 + (kb / KB_PER_G) * GSTEP;
+                gcur = gi;
                 prm[0] = prm[1];
                 prm[1] = prm[2];
                 if (gi + 2 * GSTEP < ng) prm[2] = load_prm(gi + 2 * GSTEP);
             }
         };
+        // fp16 scale bits of the current group (an 8-bit code converted here,
+        // where it is used, so that its load stays in flight until then)
+        auto cur_scale = [&]() -> uint32_t { return s8 ? scale8_bits(a.sc, E8, n, gcur, prm[0].x) : prm[0].x; };
 
         if constexpr (TILES) {
             // codes and parameters of block kb from the tile ring: word i of
@@ -415,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t zq = prm[0].y;
                     const uint32_t add_lo = zq * 0x00010001u + 0xE400E400u;   // -(1024 + zp)
                     const uint32_t add_hi = zq * 0x00100010u + 0xD400D400u;   // -(64 + zp)
-                    const uint32_t s2 = __byte_perm(f16_times_pow2(prm[0].x, ex), 0u, 0x1010u);
+                    const uint32_t s2 = __byte_perm(f16_times_pow2(cur_scale(), ex), 0u, 0x1010u);
                     const uint4 w = *reinterpret_cast<const uint4*>(pt + src_off[sub]);
                     unsigned char* bt = acquire();
                     if (!bt) { ok = false; break; }
@@ -471,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 }
                             });
                         } else {
-                            const uint32_t s2 = __byte_perm(f16_times_pow2(prm[0].x, ex), 0u, 0x1010u);
+                            const uint32_t s2 = __byte_perm(f16_times_pow2(cur_scale(), ex), 0u, 0x1010u);
                             const uint32_t zq = prm[0].y;
                             gemv::static_for<0, 16>([&](auto ec) {
                                 constexpr int e = decltype(ec)::value;
@@ -643,6 +660,7 @@ qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void
     a.y = y; a.ldy = ldy; a.y_bf16 = yt == QG_Y_BF16;
     a.status = device_status_ptr();
     a.magic = gemv::kF16Magic;
+    a.sc = scale_src(w);
     {
         qg_status st2 = gemv::allow_smem(k_gemm_tc<BITS, G, TILES>, C::SMEM);
         if (st2 != QG_OK) return st2;

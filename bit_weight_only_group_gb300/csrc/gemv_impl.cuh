@@ -39,6 +39,7 @@
 
 #include "ptx.cuh"
 #include "qg_internal.h"
+#include "scale8.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -312,6 +313,14 @@ struct Problem {
     int ldy;
     int y_bf16;
     uint32_t magic;   // kF16Magic
+    // 8-bit scales (scale8 non-null): E4M3 codes, the matrix exponent and
+    // the fp16 fallback list
+    const uint8_t* scale8;
+    const int* scale8_exp;
+    const int* fb_row_ptr;
+    const int* fb_col;
+    const uint16_t* fb_val;
+    int fb_cap;
 };
 
 __device__ __forceinline__ int x_row(const Problem& p, int m) { return p.rowmap ? p.rowmap[m] / p.xdiv : m; }
@@ -420,6 +429,18 @@ __device__ void stage_prm(const Problem& a, int tile, int g0, int ngr, uint32_t*
 {
     const int ng = a.K / G;
     auto word = [](int gi, int rl) { return (gi * kWarps + rl / 16) * 16 + (rl % 8) * 2 + (rl / 8) % 2; };
+    if (a.scale8) {   // 8-bit scales: each group's fp16 scale bits from its code
+        const ScaleSrc sc{a.scale, a.scale8, a.scale8_exp, a.fb_row_ptr, a.fb_col, a.fb_val, a.fb_cap};
+        const int E = __ldg(a.scale8_exp);
+        for (int it = threadIdx.x; it < kRowsPerCta * ngr; it += nthr) {
+            const int rl = it % kRowsPerCta, gi = it / kRowsPerCta;
+            const int n = min(tile * kRowsPerCta + rl, a.N - 1);
+            const size_t idx = (size_t)n * ng + g0 + gi;
+            const uint32_t c = __ldg(a.scale8 + idx);
+            ps[word(gi, rl)] = scale8_bits(sc, E, n, g0 + gi, c) | ((uint32_t)__ldg(a.zp + idx) << 16);
+        }
+        return;
+    }
     const bool vec = ng % 8 == 0 && g0 % 8 == 0 && (reinterpret_cast<uintptr_t>(a.scale) & 15u) == 0 &&
                      (reinterpret_cast<uintptr_t>(a.zp) & 7u) == 0;
     if (vec) {
@@ -886,6 +907,13 @@ struct MoeTable {
     const int* col[kMoeMaxExperts];
     const uint16_t* val[kMoeMaxExperts];
     int nnz[kMoeMaxExperts];
+    // 8-bit scales (all experts alike: scale8 null for none)
+    const uint8_t* scale8[kMoeMaxExperts];
+    const int* scale8_exp[kMoeMaxExperts];
+    const int* fb_row_ptr[kMoeMaxExperts];
+    const int* fb_col[kMoeMaxExperts];
+    const uint16_t* fb_val[kMoeMaxExperts];
+    int fb_cap[kMoeMaxExperts];
 };
 
 template <int BITS, int G, int MP>
@@ -904,6 +932,8 @@ __global__ void __launch_bounds__(kWarps * 32) k_gemv_moe(const __grid_constant_
     p.row_ptr = t.row_ptr[e]; p.col = t.col[e]; p.val = t.val[e]; p.nnz = t.nnz[e];
     p.y = t.y; p.ldy = t.N; p.y_bf16 = t.y_bf16;
     p.magic = t.magic;
+    p.scale8 = t.scale8[e]; p.scale8_exp = t.scale8_exp[e];
+    p.fb_row_ptr = t.fb_row_ptr[e]; p.fb_col = t.fb_col[e]; p.fb_val = t.fb_val[e]; p.fb_cap = t.fb_cap[e];
     gemv_body<BITS, G, MP>(p, splits, gpsplit, blockIdx.x);
 }
 

@@ -21,10 +21,22 @@
 //   5. k_compact     one warp per row writes CSR columns/values in k order;
 //   6. k_quant_*     one thread per (row, group): group statistics, scale /
 //                    zero-point or codebook, codes, packing.
+// With 8-bit (E4M3) scales ("Mixed-width quantization" page, section 2.3),
+// step 6 is bracketed by:
+//   k_fp8_hist       one thread per group: its fp16 scale, a histogram of
+//                    floor(log2 scale) over the matrix;
+//   k_fp8_exp        one thread: E = the histogram's lower median;
+//   k_quant_affine   stores the E4M3 code (or the fallback mark) and codes
+//                    the group with the stored scale;
+//   k_fb_count       one warp per row counts its fallback groups;
+//   k_fb_scan        one block: exclusive scan -> fallback CSR row pointer;
+//   k_fb_fill        one warp per row lists its fallback groups and their
+//                    fp16 scales.
 #include <atomic>
 #include <cuda_fp16.h>
 
 #include "qg_internal.h"
+#include "scale8.cuh"
 
 namespace qg {
 namespace {
@@ -39,12 +51,17 @@ struct SelParams {
     unsigned pad;
 };
 
+// 8-bit scales: 40 bins of floor(log2 scale) in [-24, 15], then E
+constexpr int kF8Bins = 40;
+constexpr int kF8Words = 64;
+
 struct QuantWs {
     unsigned* hist;
     SelParams* sel;
     unsigned* cnt_gt;
     unsigned* cnt_eq;
     unsigned* take_eq;
+    unsigned* f8;   // [kF8Words]: histogram, then E at kF8Bins
 };
 
 size_t ws_layout(int N, QuantWs* p, void* base)
@@ -60,6 +77,7 @@ size_t ws_layout(int N, QuantWs* p, void* base)
     size_t o_gt = take(sizeof(unsigned) * (size_t)N);
     size_t o_eq = take(sizeof(unsigned) * (size_t)N);
     size_t o_take = take(sizeof(unsigned) * (size_t)N);
+    size_t o_f8 = take(sizeof(unsigned) * kF8Words);
     if (p && base) {
         char* b = static_cast<char*>(base);
         p->hist = reinterpret_cast<unsigned*>(b + o_hist);
@@ -67,6 +85,7 @@ size_t ws_layout(int N, QuantWs* p, void* base)
         p->cnt_gt = reinterpret_cast<unsigned*>(b + o_gt);
         p->cnt_eq = reinterpret_cast<unsigned*>(b + o_eq);
         p->take_eq = reinterpret_cast<unsigned*>(b + o_take);
+        p->f8 = reinterpret_cast<unsigned*>(b + o_f8);
     }
     return off;
 }
@@ -337,7 +356,7 @@ __device__ __forceinline__ bool is_out(const unsigned (&om)[G / 32], int i)
 // clamp(-round(min / scale), 0, qmax).
 template <int G>
 __device__ __forceinline__ void affine_params(const unsigned short* __restrict__ src, const unsigned (&om)[G / 32],
-                                              int qmax, unsigned short* s16_out, int* zp_out)
+                                              int qmax, unsigned short* s16_out, int* zp_out, float* mn_out = nullptr)
 {
     float mn = 0.0f, mx = 0.0f;
     for_group<G>(src, [&](int i, unsigned short h) {
@@ -358,6 +377,56 @@ __device__ __forceinline__ void affine_params(const unsigned short* __restrict__
     int zp = -(int)r;
     *zp_out = zp < 0 ? 0 : (zp > qmax ? qmax : zp);
     *s16_out = s16;
+    if (mn_out) *mn_out = mn;
+}
+
+// fp16 scale of an affine (sym == 0) or symmetric (sym == 1) group, as the
+// quantizer below finds it.
+template <int G>
+__device__ __forceinline__ unsigned short group_scale16(const unsigned short* __restrict__ src,
+                                                        const unsigned (&om)[G / 32], int bits, int sym);
+
+// floor(log2 h) of a positive finite fp16 number h.
+__device__ __forceinline__ int f16_floor_log2(unsigned h)
+{
+    const int e5 = (h >> 10) & 31;
+    if (e5) return e5 - 15;
+    return (31 - __clz(h & 1023u)) - 24;
+}
+
+// E4M3 storage of the fp16 scale s16 under the matrix exponent E: the least
+// normal E4M3 value >= s16 * 2^-E (code returned, *eff = fp16 bits of that
+// value times 2^E), or kScale8Fallback with *eff = s16 when s16 * 2^-E is
+// below 2^-6, the rounded value above 448, or value * 2^E off fp16's normal
+// range.  Integer arithmetic on the fp16 fields: s16 = (mant / 1024) *
+// 2^lg with mant in [1024, 2048), rounded up to 3 fraction bits.
+__device__ __forceinline__ unsigned e4m3_store(unsigned s16, int E, unsigned* eff)
+{
+    const int e5 = (s16 >> 10) & 31;
+    const unsigned m10 = s16 & 1023u;
+    int lg;
+    unsigned mant;
+    if (e5) {
+        lg = e5 - 15;
+        mant = 1024u + m10;
+    } else {
+        const int hb = 31 - __clz(m10);
+        lg = hb - 24;
+        mant = m10 << (10 - hb);
+    }
+    int ex = lg - E;
+    *eff = s16;
+    if (ex < -6) return kScale8Fallback;
+    unsigned m3 = (mant - 1024u + 127u) >> 7;   // ceil of the fraction in eighths
+    if (m3 == 8u) {
+        m3 = 0u;
+        ++ex;
+    }
+    if (ex > 8 || (ex == 8 && m3 == 7u)) return kScale8Fallback;
+    const int fe = ex + E;
+    if (fe < -14 || fe > 15) return kScale8Fallback;
+    *eff = ((unsigned)(fe + 15) << 10) | (m3 << 7);
+    return ((unsigned)(ex + 7) << 3) | m3;
 }
 
 // Largest |w| over the group's non-outliers.
@@ -375,11 +444,14 @@ __device__ __forceinline__ float group_amax(const unsigned short* __restrict__ s
 // range); sym == 1: symmetric, integer range [-qs, qs] with qs = 2^(b-1) - 1,
 // scale rounded up from amax / qs (1.0 if amax is 0), codes q + 2^(b-1) with
 // the zero point fixed at 2^(b-1).  Outliers take the zero point's code.
+// With scale8 set, the group's scale is stored as 8 bits (e4m3_store under
+// the exponent *f8_exp) and the codes use the stored scale.
 template <int G>
 __global__ void k_quant_affine(const unsigned short* __restrict__ W, int N, int K, int bits, int sym,
                                const int* __restrict__ row_ptr, const int* __restrict__ col,
                                unsigned char* __restrict__ packed, unsigned short* __restrict__ scale,
-                               unsigned char* __restrict__ zp_out)
+                               unsigned char* __restrict__ zp_out, const unsigned* __restrict__ f8_exp,
+                               unsigned char* __restrict__ scale8)
 {
     const int ng = K / G;
     const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -401,9 +473,22 @@ __global__ void k_quant_affine(const unsigned short* __restrict__ W, int N, int 
         qlo = zp - qs;
         qhi = zp + qs;
     } else {
-        affine_params<G>(src, om, qmax, &s16, &zp);
+        float mn;
+        affine_params<G>(src, om, qmax, &s16, &zp, &mn);
         qlo = 0;
         qhi = qmax;
+        if (scale8) {   // zero point of the stored scale
+            unsigned eff;
+            e4m3_store(s16, (int)__ldg(f8_exp), &eff);
+            const float r = rintf(__fdiv_rn(mn, h2f((unsigned short)eff)));
+            zp = -(int)r;
+            zp = zp < 0 ? 0 : (zp > qmax ? qmax : zp);
+        }
+    }
+    if (scale8) {
+        unsigned eff;
+        scale8[gid] = (unsigned char)e4m3_store(s16, (int)__ldg(f8_exp), &eff);
+        s16 = (unsigned short)eff;
     }
     const float s = h2f(s16);
     BitWriter bw{reinterpret_cast<unsigned*>(packed + ((size_t)n * K + k0) * bits / 8), 0ull, 0};
@@ -417,8 +502,138 @@ __global__ void k_quant_affine(const unsigned short* __restrict__ W, int N, int 
         }
         bw.put((unsigned)q, bits);
     });
-    scale[gid] = s16;
+    if (!scale8) scale[gid] = s16;
     zp_out[gid] = (unsigned char)zp;
+}
+
+template <int G>
+__device__ __forceinline__ unsigned short group_scale16(const unsigned short* __restrict__ src,
+                                                        const unsigned (&om)[G / 32], int bits, int sym)
+{
+    if (sym) {
+        const int qs = (1 << (bits - 1)) - 1;
+        const float amax = group_amax<G>(src, om);
+        return amax == 0.0f ? (unsigned short)0x3C00 : __half_as_ushort(__float2half_ru(__fdiv_rn(amax, (float)qs)));
+    }
+    unsigned short s16;
+    int zp;
+    affine_params<G>(src, om, (1 << bits) - 1, &s16, &zp);
+    return s16;
+}
+
+// ---------------------------------------------------------------- 8-bit scales
+// Histogram of floor(log2 s16) over every group's fp16 scale (bins -24..15).
+template <int G>
+__global__ void k_fp8_hist(const unsigned short* __restrict__ W, int N, int K, int bits, int sym,
+                           const int* __restrict__ row_ptr, const int* __restrict__ col, unsigned* __restrict__ hist)
+{
+    __shared__ unsigned sh[kF8Bins];
+    for (int i = threadIdx.x; i < kF8Bins; i += blockDim.x) sh[i] = 0u;
+    __syncthreads();
+    const int ng = K / G;
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gid < (long long)N * ng) {
+        const int n = (int)(gid / ng), j = (int)(gid % ng);
+        unsigned om[G / 32];
+        int first;
+        group_outliers<G>(row_ptr, col, n, j * G, om, &first);
+        const unsigned short s16 = group_scale16<G>(W + (size_t)n * K + j * G, om, bits, sym);
+        atomicAdd(&sh[f16_floor_log2(s16) + 24], 1u);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kF8Bins; i += blockDim.x)
+        if (sh[i]) atomicAdd(&hist[i], sh[i]);
+}
+
+// E = the lower median (element (count - 1) / 2 in ascending order).
+__global__ void k_fp8_exp(unsigned* __restrict__ f8, unsigned long long count, int* __restrict__ exp_out)
+{
+    const unsigned long long want = (count - 1) / 2;
+    unsigned long long seen = 0;
+    int E = 0;
+    for (int b = 0; b < kF8Bins; b++) {
+        seen += f8[b];
+        if (seen > want) {
+            E = b - 24;
+            break;
+        }
+    }
+    f8[kF8Bins] = (unsigned)E;
+    *exp_out = E;
+}
+
+// Number of fallback groups of every row (one warp per row).
+__global__ void k_fb_count(const unsigned char* __restrict__ scale8, int N, int ng, unsigned* __restrict__ cnt)
+{
+    const int warp = (int)((blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+    if (warp >= N) return;
+    const unsigned char* r = scale8 + (size_t)warp * ng;
+    unsigned c = 0;
+    for (int j = lane; j < ng; j += 32) c += r[j] == kScale8Fallback;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (lane == 0) cnt[warp] = c;
+}
+
+// Exclusive scan of the row counts into the fallback CSR row pointer (one
+// block); more groups than the list holds sets the status word.
+__global__ void __launch_bounds__(1024) k_fb_scan(const unsigned* __restrict__ cnt, int N, int* __restrict__ fb_row_ptr,
+                                                  int cap, int* status)
+{
+    __shared__ unsigned long long part[1024];
+    const int t = threadIdx.x;
+    const long long per = (N + 1023) / 1024;
+    const long long b0 = (long long)t * per, b1 = min((long long)N, b0 + per);
+    unsigned long long sum = 0;
+    for (long long i = b0; i < b1; i++) sum += cnt[i];
+    part[t] = sum;
+    __syncthreads();
+    for (int o = 1; o < 1024; o <<= 1) {   // inclusive scan of the per-thread sums
+        const unsigned long long v = t >= o ? part[t - o] : 0ull;
+        __syncthreads();
+        part[t] += v;
+        __syncthreads();
+    }
+    unsigned long long run = part[t] - sum;
+    for (long long i = b0; i < b1; i++) {
+        fb_row_ptr[i] = (int)run;
+        run += cnt[i];
+    }
+    if (t == 1023) {
+        fb_row_ptr[N] = (int)part[1023];
+        if (part[1023] > (unsigned long long)cap && status) atomicExch(status, (int)QG_ERR_WORKSPACE);
+    }
+}
+
+// The fallback list of every row (one warp per row): group index and fp16
+// scale of each group stored as kScale8Fallback, in ascending order; entries
+// beyond the capacity are not written.
+template <int G>
+__global__ void k_fb_fill(const unsigned short* __restrict__ W, int N, int K, int bits, int sym,
+                          const int* __restrict__ row_ptr, const int* __restrict__ col,
+                          const unsigned char* __restrict__ scale8, const int* __restrict__ fb_row_ptr,
+                          int* __restrict__ fb_col, unsigned short* __restrict__ fb_val, int cap)
+{
+    const int warp = (int)((blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+    if (warp >= N) return;
+    const int n = warp, ng = K / G;
+    int base = fb_row_ptr[n];
+    for (int j0 = 0; j0 < ng; j0 += 32) {
+        const int j = j0 + lane;
+        const bool fb = j < ng && scale8[(size_t)n * ng + j] == kScale8Fallback;
+        const unsigned m = __ballot_sync(0xffffffffu, fb);
+        if (fb) {
+            const int at = base + __popc(m & ((1u << lane) - 1u));
+            if (at < cap) {
+                unsigned om[G / 32];
+                int first;
+                group_outliers<G>(row_ptr, col, n, j * G, om, &first);
+                fb_col[at] = j;
+                fb_val[at] = group_scale16<G>(W + (size_t)n * K + j * G, om, bits, sym);
+            }
+        }
+        base += __popc(m);
+    }
 }
 
 // 2-bit groups on a uniform grid, stored as the four constants a code
@@ -646,13 +861,40 @@ qg_status launch_quantize(const uint16_t* W, float /*frac*/, const qg_qweight& w
         if (w.group == 32) run(k_quant_codebook<32>);
         else if (w.group == 64) run(k_quant_codebook<64>);
         else run(k_quant_codebook<128>);
-    } else {
+    } else if (!w.scale8) {
         auto run = [&](auto kern) {
-            kern<<<blocks, threads, 0, s>>>(Wh, w.N, w.K, w.bits, mode, rp, w.out_col, w.packed, w.scale, w.zp);
+            kern<<<blocks, threads, 0, s>>>(Wh, w.N, w.K, w.bits, mode, rp, w.out_col, w.packed, w.scale, w.zp,
+                                            nullptr, nullptr);
         };
         if (w.group == 32) run(k_quant_affine<32>);
         else if (w.group == 64) run(k_quant_affine<64>);
         else run(k_quant_affine<128>);
+    } else {
+        // 8-bit scales: histogram -> E -> quantize -> fallback list
+        e = cudaMemsetAsync(p.f8, 0, sizeof(unsigned) * kF8Words, s);
+        if (e != cudaSuccess) return cuda_fail(e, "memset scale histogram");
+        auto hist = [&](auto kern) { kern<<<blocks, threads, 0, s>>>(Wh, w.N, w.K, w.bits, mode, rp, w.out_col, p.f8); };
+        if (w.group == 32) hist(k_fp8_hist<32>);
+        else if (w.group == 64) hist(k_fp8_hist<64>);
+        else hist(k_fp8_hist<128>);
+        k_fp8_exp<<<1, 1, 0, s>>>(p.f8, (unsigned long long)groups, w.scale8_exp);
+        auto run = [&](auto kern) {
+            kern<<<blocks, threads, 0, s>>>(Wh, w.N, w.K, w.bits, mode, rp, w.out_col, w.packed, w.scale, w.zp,
+                                            p.f8 + kF8Bins, w.scale8);
+        };
+        if (w.group == 32) run(k_quant_affine<32>);
+        else if (w.group == 64) run(k_quant_affine<64>);
+        else run(k_quant_affine<128>);
+        const int row_blocks = (int)ceil_div(w.N, 8);
+        k_fb_count<<<row_blocks, 256, 0, s>>>(w.scale8, w.N, w.K / w.group, p.cnt_gt);
+        k_fb_scan<<<1, 1024, 0, s>>>(p.cnt_gt, w.N, w.fb_row_ptr, w.fb_cap, device_status_ptr());
+        auto fill = [&](auto kern) {
+            kern<<<row_blocks, 256, 0, s>>>(Wh, w.N, w.K, w.bits, mode, rp, w.out_col, w.scale8, w.fb_row_ptr,
+                                            w.fb_col, w.fb_val, w.fb_cap);
+        };
+        if (w.group == 32) fill(k_fb_fill<32>);
+        else if (w.group == 64) fill(k_fb_fill<64>);
+        else fill(k_fb_fill<128>);
     }
     k_quant_done<<<1, 32, 0, s>>>();
     e = cudaGetLastError();

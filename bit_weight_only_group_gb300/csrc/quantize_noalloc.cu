@@ -25,8 +25,9 @@ namespace qg {
 namespace {
 
 // 1 MiB: the histogram takes 128 KiB; the per-row counters take 12 bytes per
-// row, so matrices with outliers up to about 76,000 rows fit.  Without
-// outliers the quantizer touches no scratch, and any size is accepted.
+// row, so matrices with outliers (or 8-bit scales) up to about 76,000 rows
+// fit.  Without either the quantizer touches no scratch, and any size is
+// accepted.
 constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -74,12 +75,13 @@ extern "C" QG_API qg_status qpack_quantize_noalloc(const uint16_t* W, float outl
     if (st != QG_OK) return st;
     const qg_qweight& w = *out;
     void* scratch = nullptr;
-    if (w.nnz > 0) {   // only the outlier selection uses scratch
+    if (w.nnz > 0 || w.scale8) {   // only the outlier selection and the 8-bit scales use scratch
         const size_t need = quantize_workspace_bytes(w.N, w.K);
         if (need > kNoAllocScratchBytes)
             return fail(QG_ERR_WORKSPACE,
-                        "qpack_quantize_noalloc: N=%d with outliers needs %zu bytes of scratch, above the fixed "
-                        "%zu-byte array (use qpack_quantize with a workspace)", w.N, need, kNoAllocScratchBytes);
+                        "qpack_quantize_noalloc: N=%d with outliers or 8-bit scales needs %zu bytes of scratch, "
+                        "above the fixed %zu-byte array (use qpack_quantize with a workspace)", w.N, need,
+                        kNoAllocScratchBytes);
         st = scratch_address(&scratch);
         if (st != QG_OK) return st;
     }

@@ -67,6 +67,19 @@ __device__ __forceinline__ int chunk_pos(int c)
 // it is stored.  The two threads of a row (lanes 2i and 2i + 1 of a warp
 // whose lanes all call this) each scan half of the row's groups.
 template <int BITS>
+__device__ __forceinline__ int row_exponent_of_max(uint32_t m)
+{
+    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    float b = __half2float(__ushort_as_half((uint16_t)m)) * (float)((1 << BITS) - 1);
+    int e = 0;
+    while (b > 65504.0f && e < 30) {
+        b *= 0.5f;
+        ++e;
+    }
+    return e;
+}
+
+template <int BITS>
 __device__ __forceinline__ int row_exponent(const uint16_t* srow, int ng, int hk)
 {
     uint32_t m = 0;
@@ -82,14 +95,25 @@ __device__ __forceinline__ int row_exponent(const uint16_t* srow, int ng, int hk
         for (int g = hk; g < ng; g += 2) m = max(m, (uint32_t)(__ldg(srow + g) & 0x7FFFu));
     }
     m = max(m & 0xFFFFu, m >> 16);
-    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-    float b = __half2float(__ushort_as_half((uint16_t)m)) * (float)((1 << BITS) - 1);
-    int e = 0;
-    while (b > 65504.0f && e < 30) {
-        b *= 0.5f;
-        ++e;
+    return row_exponent_of_max<BITS>(m);
+}
+
+// The same for a row with 8-bit scales: the largest stored scale is the
+// largest normal code's (the fp16 value grows with the code) or one of the
+// row's fallback scales.
+template <int BITS>
+__device__ __forceinline__ int row_exponent_8(const ScaleSrc& sc, int E, int n, int ng, int hk)
+{
+    const uint8_t* crow = sc.scale8 + (size_t)n * ng;
+    uint32_t c = 0;
+    for (int g = hk; g < ng; g += 2) {
+        const uint32_t v = __ldg(crow + g);
+        if (v != kScale8Fallback) c = max(c, v);
     }
-    return e;
+    uint32_t m = c ? e4m3_scale_bits(c, E) : 0u;
+    const int p1 = min(__ldg(sc.fb_row_ptr + n + 1), sc.fb_cap);
+    for (int p = min(__ldg(sc.fb_row_ptr + n), sc.fb_cap) + hk; p < p1; p += 2) m = max(m, (uint32_t)__ldg(sc.fb_val + p));
+    return row_exponent_of_max<BITS>(m);
 }
 
 // fp16 value h times 2^-e (exact while the result stays a normal number).

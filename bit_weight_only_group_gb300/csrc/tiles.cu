@@ -9,19 +9,21 @@
 //           this K block, LSB-first as in the planar stream) at word
 //           i * 512 + t: a warp's 32 threads read 32 consecutive words;
 //   params  per row, for each group the block touches (two at group 32,
-//           else one) a 32-bit word (fp16 scale | zero-point << 16), or at
-//           2 bits the four fp16 codebook entries (8 bytes);
+//           else one) a 32-bit word (fp16 scale | zero-point << 16; an
+//           8-bit scale is converted to its fp16 value here), or at 2 bits
+//           the four fp16 codebook entries (8 bytes);
 // rows beyond N are zero.  The FP16 outliers stay in their CSR arrays.
 // One CTA of 512 threads per block; a thread moves its chunk's words and
 // the parameters of its chunk's group (at group 32; else the even thread
 // writes the row's one set).
 #include "qg_internal.h"
+#include "scale8.cuh"
 
 namespace qg {
 namespace {
 
 template <int BITS>
-__global__ void __launch_bounds__(512) k_repack(const uint8_t* __restrict__ packed, const uint16_t* __restrict__ scale,
+__global__ void __launch_bounds__(512) k_repack(const uint8_t* __restrict__ packed, const ScaleSrc sc,
                                                 const uint8_t* __restrict__ zp, const uint2* __restrict__ cb, int N,
                                                 int K, int G, uint8_t* __restrict__ tiles)
 {
@@ -43,7 +45,7 @@ __global__ void __launch_bounds__(512) k_repack(const uint8_t* __restrict__ pack
         if constexpr (BITS == 2) {
             reinterpret_cast<uint2*>(prm)[slot] = live ? __ldg(cb + (size_t)n * ng + g) : make_uint2(0u, 0u);
         } else {
-            prm[slot] = live ? ((uint32_t)__ldg(scale + (size_t)n * ng + g) | ((uint32_t)__ldg(zp + (size_t)n * ng + g) << 16))
+            prm[slot] = live ? (scale_bits(sc, scale_exp(sc), n, ng, g) | ((uint32_t)__ldg(zp + (size_t)n * ng + g) << 16))
                              : 0u;
         }
     }
@@ -53,7 +55,7 @@ template <int BITS>
 qg_status repack_bits(const qg_qweight& w, void* tiles, cudaStream_t s)
 {
     const dim3 grid((unsigned)(w.K / kTileK), (unsigned)ceil_div(w.N, kTileRows));
-    k_repack<BITS><<<grid, 512, 0, s>>>(w.packed, w.scale, w.zp, reinterpret_cast<const uint2*>(w.codebook), w.N,
+    k_repack<BITS><<<grid, 512, 0, s>>>(w.packed, scale_src(w), w.zp, reinterpret_cast<const uint2*>(w.codebook), w.N,
                                         w.K, w.group, static_cast<uint8_t*>(tiles));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "repack kernel launch");

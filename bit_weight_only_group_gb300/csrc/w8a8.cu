@@ -63,7 +63,7 @@ __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c)
 template <int MT>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
     k_w8a8(const int8_t* __restrict__ xq, const float* __restrict__ sx, int M, int N, int K, int G,
-           const uint8_t* __restrict__ packed, const uint16_t* __restrict__ scale, const uint8_t* __restrict__ zp,
+           const uint8_t* __restrict__ packed, const ScaleSrc sc, const uint8_t* __restrict__ zp,
            const int* __restrict__ row_ptr, const int* __restrict__ col, const uint16_t* __restrict__ val, int nnz,
            void* __restrict__ y, int ldy, int y_bf16)
 {
@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
     const int n = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
     if (n >= N) return;   // whole warp
     const int ng = K / G;
+    const int E8 = scale_exp(sc);
     const uint8_t* wr = packed + (size_t)n * K;
     float acc[MT];
 #pragma unroll
@@ -79,7 +80,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
     for (int k = lane * 16; k < K; k += 512) {
         const uint4 wv = gemv::ldg_stream128(wr + k);
         const int g = k / G;   // a 16-code run lies in one group (G is a multiple of 16)
-        const float sw = __half2float(__ushort_as_half(__ldg(scale + (size_t)n * ng + g)));
+        const float sw = __half2float(__ushort_as_half((uint16_t)scale_bits(sc, E8, n, ng, g)));
         const int z = __ldg(zp + (size_t)n * ng + g);
 #pragma unroll
         for (int m = 0; m < MT; m++) {
@@ -135,7 +136,7 @@ template <int MT>
 qg_status run(const Ws& p, int M, const qg_qweight& w, void* y, int ldy, qg_ydtype yt, cudaStream_t s)
 {
     const int blocks = (int)ceil_div(w.N, kWarpsPerCta);
-    k_w8a8<MT><<<blocks, kWarpsPerCta * 32, 0, s>>>(p.q, p.s, M, w.N, w.K, w.group, w.packed, w.scale, w.zp,
+    k_w8a8<MT><<<blocks, kWarpsPerCta * 32, 0, s>>>(p.q, p.s, M, w.N, w.K, w.group, w.packed, scale_src(w), w.zp,
                                                     w.out_row_ptr, w.out_col, w.out_val, w.nnz, y, ldy,
                                                     yt == QG_Y_BF16);
     cudaError_t e = cudaGetLastError();

@@ -86,7 +86,26 @@ typedef enum { QG_Y_F32 = 0, QG_Y_BF16 = 1 } qg_ydtype;
  *  out_row_ptr int32 [N+1] CSR row pointer (may be NULL when nnz == 0).
  *  out_col     int32 [nnz] column of each outlier, ascending within a row.
  *  out_val     fp16 [nnz]  the value added back at (row, col): the weight
- *              itself (bits 3..6) or the residual w - codebook entry (2 bits).
+ *              itself (bits 3..8) or the residual w - codebook entry (2 bits).
+ *
+ * Optional 8-bit float group scales with an fp16 fallback ("Mixed-width
+ * quantization" page, section 2.3: the scale stored as an 8-bit float,
+ * groups whose scale the 8-bit format cannot hold kept at fp16).  When
+ * scale8 is not NULL (bits 3..8) it replaces `scale`, which may be NULL:
+ *  scale8      uint8 [N, ng]: the E4M3 code (1 sign, 4 exponent bits with
+ *              bias 7, 3 fraction bits; only positive normal codes 0x08 ..
+ *              0x7E occur) of the group's scale times 2^-E, or 0x7F: the
+ *              group keeps an fp16 scale, found in the fallback list.  The
+ *              group's scale is then code value * 2^E, an fp16 number.
+ *  scale8_exp  int32 [1]: the matrix exponent E (written by the quantizer).
+ *              4-byte aligned.
+ *  fb_row_ptr  int32 [N+1] the fallback list's CSR row pointer.
+ *  fb_col      int32 [fb_cap] group index j of each fallback group,
+ *              ascending within a row.
+ *  fb_val      fp16 [fb_cap] that group's fp16 scale.
+ *  fb_cap      capacity of fb_col / fb_val (entries); the quantizer reports
+ *              more fallback groups than that through the device status
+ *              word (QG_ERR_WORKSPACE, see qgemm_device_status).
  */
 typedef struct {
     int32_t N, K, bits, group;
@@ -98,6 +117,12 @@ typedef struct {
     int32_t* out_row_ptr;
     int32_t* out_col;
     uint16_t* out_val;
+    uint8_t* scale8;
+    int32_t* scale8_exp;
+    int32_t* fb_row_ptr;
+    int32_t* fb_col;
+    uint16_t* fb_val;
+    int32_t fb_cap;
 } qg_qweight;
 
 /*
@@ -136,6 +161,16 @@ QG_API qg_status qpack_workspace_size(int32_t N, int32_t K, size_t* bytes);
  *   3. codes packed LSB-first along K.
  * All rounding is IEEE round-to-nearest-even except the scale (toward +inf);
  * the results are bit-exact and deterministic.
+ * With out->scale8 set (bits 3..8), step 2 stores 8-bit scales: the fp16
+ * scale s16 of every group is found as above; E = the lower median of
+ * floor(log2 s16) over all N * ng groups; a group's code is the least normal
+ * E4M3 value >= s16 * 2^-E; the group falls back (code 0x7F, s16 in the
+ * fallback list) when s16 * 2^-E < 2^-6, when that value would exceed 448,
+ * or when value * 2^E is not a normal fp16 number; zp and q are then
+ * computed with the group's stored scale.  When more groups fall back than
+ * out->fb_cap, the first fb_cap are listed, fb_row_ptr still counts all of
+ * them, and the device status word becomes QG_ERR_WORKSPACE: the weight must
+ * not be used.
  * `ws` must hold qpack_workspace_size bytes (256-byte aligned).  Errors:
  * QG_ERR_INVALID_ARG (nulls, sizes, nnz mismatch), QG_ERR_ALIGNMENT,
  * QG_ERR_WORKSPACE, QG_ERR_CUDA.  Non-finite W gives unspecified output.

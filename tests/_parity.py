@@ -18,13 +18,26 @@ def to_device(q: oracle.QWeight, device="cuda"):
     return qg.QWeight(
         q.N, q.K, q.bits, q.group,
         packed=t(q.packed, np.uint8),
-        scale=t(q.scale, np.int16) if q.scale is not None else None,
+        scale=t(q.scale, np.int16) if q.scale is not None and q.scale8 is None else None,
         zp=t(q.zp, np.uint8) if q.zp is not None else None,
         codebook=t(q.cb, np.int16) if q.cb is not None else None,
         row_ptr=t(q.row_ptr, np.int32),
         col=t(q.col, np.int32) if q.nnz else torch.empty(0, dtype=torch.int32, device=device),
         val=t(q.val, np.int16) if q.nnz else torch.empty(0, dtype=torch.int16, device=device),
-        nnz=q.nnz)
+        nnz=q.nnz, **_fp8_fields(q, t, device))
+
+
+def _fp8_fields(q, t, device):
+    """The 8-bit scale arrays of an oracle weight (its fp16 ``scale`` then
+    only expands them and is not sent)."""
+    if q.scale8 is None:
+        return {}
+    nfb = int(q.fb_col.size)
+    return dict(scale8=t(q.scale8, np.uint8),
+                scale8_exp=torch.tensor([q.scale_exp], dtype=torch.int32, device=device),
+                fb_row_ptr=t(q.fb_row_ptr, np.int32),
+                fb_col=t(q.fb_col, np.int32) if nfb else torch.empty(0, dtype=torch.int32, device=device),
+                fb_val=t(q.fb_val, np.int16) if nfb else torch.empty(0, dtype=torch.int16, device=device))
 
 
 def to_host(qw) -> dict:
@@ -33,6 +46,8 @@ def to_host(qw) -> dict:
     out["row_ptr"] = c(qw.row_ptr)
     out["col"] = c(qw.col)
     out["val"] = c(qw.val)
+    for k in ("scale8", "scale8_exp", "fb_row_ptr", "fb_col", "fb_val"):
+        out[k] = c(getattr(qw, k))
     return out
 
 
@@ -41,6 +56,14 @@ def assert_quantized_equal(qw, ref: oracle.QWeight):
     assert np.array_equal(h["packed"], ref.packed), "packed bytes differ"
     if ref.bits == 2:
         assert np.array_equal(h["cb"].view(np.uint16), ref.cb), "codebooks differ"
+    elif ref.scale8 is not None:
+        assert int(h["scale8_exp"][0]) == ref.scale_exp, "matrix exponents differ"
+        assert np.array_equal(h["scale8"], ref.scale8), "8-bit scales differ"
+        assert np.array_equal(h["fb_row_ptr"], ref.fb_row_ptr), "fallback row pointers differ"
+        nfb = ref.fb_col.size
+        assert np.array_equal(h["fb_col"][:nfb], ref.fb_col), "fallback groups differ"
+        assert np.array_equal(h["fb_val"][:nfb].view(np.uint16), ref.fb_val), "fallback scales differ"
+        assert np.array_equal(h["zp"], ref.zp), "zero-points differ"
     else:
         assert np.array_equal(h["scale"].view(np.uint16), ref.scale), "scales differ"
         assert np.array_equal(h["zp"], ref.zp), "zero-points differ"

@@ -72,6 +72,36 @@ def _fake_desc(qg, N=64, K=128, bits=4, group=64, nnz=0, base=0x100000):
     return d
 
 
+def test_scale8_descriptor_checks_without_gpu(qg):
+    # 8-bit scales: the products and the quantizers refuse a descriptor whose
+    # 8-bit scale arrays are missing or misaligned, before any launch
+    L = qg.lib()
+    y = ctypes.c_void_p(0x200000)
+    x = ctypes.c_void_p(0x300000)
+
+    def d8(**kw):
+        d = _fake_desc(qg)
+        d.scale = None
+        d.scale8, d.scale8_exp, d.fb_row_ptr = 0x140000, 0x150000, 0x160000
+        d.fb_col, d.fb_val, d.fb_cap = 0x170000, 0x180000, 16
+        for k, v in kw.items():
+            setattr(d, k, v)
+        return d
+
+    cases = [(d8(scale8_exp=None), -1), (d8(fb_row_ptr=None), -1), (d8(fb_col=None), -1),
+             (d8(fb_cap=-1), -1), (d8(scale8_exp=0x150002), -3), (d8(fb_val=0x180001), -3),
+             (d8(zp=None), -1)]
+    d2 = _fake_desc(qg, bits=2)
+    d2.scale8 = 0x140000
+    cases.append((d2, -1))
+    for d, expect in cases:
+        assert L.qgemm_forward(x, 1, 128, ctypes.byref(d), y, 64, 0, None, 0, None) == expect, qg.last_error()
+        assert L.qpack_quantize(x, 0.0, ctypes.byref(d), None, 0, None) == expect
+    # fb_cap = 0 needs no list arrays
+    ok = d8(fb_col=None, fb_val=None, fb_cap=0)
+    assert L.qpack_quantize(x, 0.0, ctypes.byref(ok), None, 0, None) == -4   # passes the checks, lacks workspace
+
+
 def test_host_validation_without_gpu(qg):
     L = qg.lib()
     d = _fake_desc(qg)

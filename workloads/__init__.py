@@ -198,6 +198,18 @@ def gen_extreme_weight(N: int, K: int, group: int, seed: int = SEED_W) -> torch.
     return w.to(torch.float16)
 
 
+def gen_spread_scale_weight(N: int, K: int, group: int, seed: int = SEED_W, tiny: float = 0.05,
+                            huge: float = 0.03) -> torch.Tensor:
+    """W [N, K] fp16 ~ N(0, 0.02) with a seeded share of its groups scaled by
+    2^-11 (``tiny``) and by 2^9 (``huge``): group scales spread over about
+    twenty binades."""
+    w = gen_weight(N, K, seed=seed).float().reshape(N, K // group, group)
+    g = _gen(seed + 7, "cpu")
+    u = torch.rand((N, K // group), generator=g)
+    f = torch.where(u < tiny, 2.0 ** -11, torch.where(u > 1.0 - huge, 2.0 ** 9, 1.0))
+    return (w * f[..., None]).reshape(N, K).to(torch.float16)
+
+
 def gen_x(M: int, K: int, seed: int = SEED_X, device="cpu") -> torch.Tensor:
     """x [M, K] bf16 ~ N(0, 1)."""
     g = _gen(seed, device)
