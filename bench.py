@@ -30,6 +30,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import dataclasses
 import json
 import math
 import os
@@ -58,7 +59,7 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--layers", type=int, default=80, help="layers of the 70B-shaped stack")
     ap.add_argument("--no-secondary", action="store_true", help="skip the prefill and MoE lines")
-    ap.add_argument("--mode", choices=("all", "decode", "prefill", "moe", "widths", "case"), default="all",
+    ap.add_argument("--mode", choices=("all", "decode", "prefill", "moe", "widths", "variants", "case"), default="all",
                     help="run only that measurement and print its object (profiling runs): 'decode' = the "
                          "headline alone; 'prefill' = the 70B layer and the width sweep at M=2048; 'widths' = "
                          "the single layer, the mixed-width sweep and the 7B-shaped stack at M=1, 8, 32")
@@ -74,8 +75,8 @@ def parse():
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum over the launches
 # of a layer, captured on a 2-layer stack), valid only for the kernel source
 # it was taken on.
-DECODE_TRAFFIC = {"kernel_sha256": "fc20486295979214695e23c01cbcdd333f583df66f24d19287c282ae94cfc464",
-                  "bytes_per_layer": 453.863e6}
+DECODE_TRAFFIC = {"kernel_sha256": "d2040d2ea725e654f30164a04954c6bb581e241617480fa0fecf89d5c7b9ad61",
+                  "bytes_per_layer": 453.895e6}
 
 
 def decode_traffic(n_layers):
@@ -588,11 +589,10 @@ def run_moe(qg, args):
 
 def weight_copies(qg, q, min_bytes=600e6):
     """q and clones of it, together larger than L2 several times over."""
-    clone = lambda t: None if t is None else t.clone()
     copies = max(4, int(math.ceil(min_bytes / q.nbytes())))
-    return [q] + [qg.QWeight(q.N, q.K, q.bits, q.group, q.packed.clone(), clone(q.scale), clone(q.zp),
-                             clone(q.codebook), q.row_ptr.clone(), q.col.clone(), q.val.clone(), q.nnz)
-                  for _ in range(copies - 1)]
+    fields = {f.name: getattr(q, f.name) for f in dataclasses.fields(q)}
+    clone = lambda: qg.QWeight(**{k: v.clone() if torch.is_tensor(v) else v for k, v in fields.items()})
+    return [q] + [clone() for _ in range(copies - 1)]
 
 
 def layer_rate(qg, cs, M, P, seconds=0.15):
@@ -654,6 +654,54 @@ def run_sweep(qg, P):
             "config": "W 4096x4096 and 11008x4096 ~N(0,0.02) + 0.1% outliers, widths {2 (codebook),3,5,6} x groups "
                       "{64,128}; x bf16 [M, K]; weight copies above 600 MB per graph",
             "seconds": round(time.time() - t0, 1)}
+
+
+VARIANTS = [  # (name, bits, group, mode, scale format)
+    ("b4_g128", 4, 128, "asymmetric", "fp16"),
+    ("b4_g128_fp8", 4, 128, "asymmetric", "fp8"),
+    ("b3_g32", 3, 32, "asymmetric", "fp16"),
+    ("b3_g32_fp8", 3, 32, "asymmetric", "fp8"),
+    ("b3_g32_sym_fp8", 3, 32, "symmetric", "fp8"),
+    ("b2_g32", 2, 32, "asymmetric", "fp16"),
+    ("b2_g128_sym", 2, 128, "symmetric", "fp16"),
+    ("b2_g128_linear", 2, 128, "linear2", "fp16"),
+]
+
+
+def run_variants(qg, P):
+    """The format variants (group 32, E4M3 scales with the fp16 fallback,
+    symmetric and linear 2-bit) on one 11008 x 4096 matrix with 0.1 %
+    outliers: decode at M = 1 over weight copies above L2, and the
+    tensor-core product at M = 2048 from the tile-ordered copy."""
+    dev = torch.device("cuda")
+    N, K, frac = 11008, 4096, 0.001
+    W = wl.gen_weight(N, K, outlier_frac=frac, device=dev, distinct_positions=False)
+    x = wl.gen_x(2048, K, device=dev)
+    rows = {}
+    for name, bits, group, mode, fmt in VARIANTS:
+        q = qg.qpack_quantize(W, bits, group, frac, mode=mode, scale_fmt=fmt)
+        cs = weight_copies(qg, q)
+        r = layer_rate(qg, cs, 1, P)
+        del cs
+        t = qg.qrepack_tiles(q)
+        y = torch.empty((2048, N), device=dev)
+        g = capture(lambda: qg.qgemm_forward_tiles(x, q, t, out=y))
+        ms, n, clocks = timed_object(g, 0.15)
+        del g, t, y
+        r.update(eff_bits=round(q.nbytes() * 8 / (N * K), 3),
+                 prefill_TFLOP_s=round(2 * 2048 * N * K / ms / 1e9, 1), prefill_us=round(ms * 1e3, 1),
+                 prefill_clocks=clocks)
+        if fmt == "fp8":
+            r["fallback_groups"] = int(q.fb_row_ptr[-1].item())
+        rows[name] = r
+        del q
+        torch.cuda.empty_cache()
+    del W, x
+    return {"metric": "format variants: decode GB/s at M=1, tensor-core TFLOP/s at M=2048", "unit": "GB/s",
+            "rows": rows,
+            "config": "W 11008x4096 ~N(0,0.02) + 0.1% outliers; decode over weight copies above 600 MB per graph "
+                      "(packed_GBps = codes only, all_GBps = every byte of the layer); prefill from the tile-ordered "
+                      "copy, x bf16 [2048, 4096]"}
 
 
 def run_quantize(qg, P):
@@ -921,6 +969,8 @@ def main():
                 layers7, qs7 = build_stack7b(qg)
                 out = {"single": run_single_layer(qg, P), "sweep": run_sweep(qg, P),
                        "stack_7b": [run_stack7b(qg, P, layers7, qs7, M) for M in (1, 8, 32)]}
+            elif args.mode == "variants":
+                out = run_variants(qg, P)
             elif args.mode == "case":
                 out = run_case(qg, args.case)
             elif args.mode == "decode":
@@ -956,6 +1006,7 @@ def main():
                 secondary(line, key, run_stack7b, qg, P, layers7, qs7, M)
             secondary(line, "single_layer", run_single_layer, qg, P)
             secondary(line, "mixed_sweep", run_sweep, qg, P)
+            secondary(line, "format_variants", run_variants, qg, P)
             secondary(line, "quantize", run_quantize, qg, P)
             secondary(line, "cpu_fused_baseline", run_cpu_fused, qg, args.cpu_seconds, qs7, layers7)
             del qs7

@@ -399,7 +399,7 @@ qg_status qgemm_forward_multi(const uint16_t* x, int32_t M, int32_t ldx, const q
         if (!aligned(ys[q], yt == QG_Y_F32 ? 4 : 2)) return fail(QG_ERR_ALIGNMENT, "qgemm_forward_multi: ys[%d] misaligned", q);
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (M <= kGemvMaxM) return launch_gemv_multi(x, M, ldx, ws, n, ys, ldys, yt, s);
+    if (M <= kGemvMaxM) return launch_gemv_multi(x, M, ldx, ws, n, ys, ldys, yt, work, work_bytes, s);
     // above the decode range: one tensor-core product after the other in the caller's workspace
     for (int q = 0; q < n; q++) {
         const size_t need = gemm_workspace_bytes(M, ws[q]);
@@ -418,7 +418,7 @@ qg_status qgemm_workspace_size(int32_t M, const qg_qweight* w, size_t* bytes)
     qg_status st = check_qweight(w, "qgemm_workspace_size");
     if (st != QG_OK) return st;
     if (M < 0) return fail(QG_ERR_INVALID_ARG, "M < 0");
-    *bytes = M <= kGemvMaxM ? 0 : gemm_workspace_bytes(M, *w);
+    *bytes = M <= kGemvMaxM ? gemv_workspace_bytes(M, w->K) : gemm_workspace_bytes(M, *w);
     return QG_OK;
 }
 
@@ -436,7 +436,7 @@ qg_status qgemm_forward(const uint16_t* x, int32_t M, int32_t ldx, const qg_qwei
     if (!aligned(x, 2) || !aligned(y, yt == QG_Y_F32 ? 4 : 2))
         return fail(QG_ERR_ALIGNMENT, "qgemm_forward: x or y misaligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (M <= kGemvMaxM) return launch_gemv(x, M, ldx, *w, y, ldy, yt, s);
+    if (M <= kGemvMaxM) return launch_gemv(x, M, ldx, *w, y, ldy, yt, ws, ws_bytes, s);
     const size_t need = gemm_workspace_bytes(M, *w);
     if (need && (!ws || ws_bytes < need))
         return fail(QG_ERR_WORKSPACE, "qgemm_forward: workspace %zu bytes < %zu", ws ? ws_bytes : (size_t)0, need);

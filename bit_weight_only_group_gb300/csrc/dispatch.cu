@@ -129,6 +129,8 @@ gemv::Problem make_problem(const uint16_t* x, int M, int ldx, const qg_qweight& 
     p.fb_col = w.fb_col;
     p.fb_val = w.fb_val;
     p.fb_cap = w.fb_cap;
+    p.xfrag = nullptr;
+    p.status = device_status_ptr();
     return p;
 }
 
@@ -238,14 +240,24 @@ size_t moe_ws_layout(int T, int k, int E, int n, const qg_qweight* experts, MoeW
 
 }  // namespace
 
-qg_status launch_gemv(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,
-                      qg_ydtype yt, cudaStream_t s)
+// The caller's workspace as the fragment-order copy of x, when M calls for it
+// and it is large enough (else null: the CTAs convert x themselves).
+static const unsigned char* xfrag_buffer(int M, int K, void* ws, size_t ws_bytes)
 {
-    return dense_by_bits(make_problem(x, M, ldx, w, y, ldy, yt), w.bits, w.group, s);
+    const size_t need = gemv_workspace_bytes(M, K);
+    return need && ws && ws_bytes >= need && aligned(ws, 256) ? static_cast<const unsigned char*>(ws) : nullptr;
+}
+
+qg_status launch_gemv(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,
+                      qg_ydtype yt, void* ws, size_t ws_bytes, cudaStream_t s)
+{
+    gemv::Problem p = make_problem(x, M, ldx, w, y, ldy, yt);
+    p.xfrag = xfrag_buffer(M, w.K, ws, ws_bytes);
+    return dense_by_bits(p, w.bits, w.group, s);
 }
 
 qg_status launch_gemv_multi(const uint16_t* x, int M, int ldx, const qg_qweight* ws, int n, void* const* ys,
-                            const int32_t* ldys, qg_ydtype yt, cudaStream_t s)
+                            const int32_t* ldys, qg_ydtype yt, void* work, size_t work_bytes, cudaStream_t s)
 {
     static_assert(kMultiMax == gemv::kMultiMax, "one limit on products per launch");
     gemv::MultiTable t;
@@ -254,6 +266,7 @@ qg_status launch_gemv_multi(const uint16_t* x, int M, int ldx, const qg_qweight*
     t.tile_start[0] = 0;
     for (int q = 0; q < n; q++) {
         t.p[q] = make_problem(x, M, ldx, ws[q], ys[q], ldys[q], yt);
+        t.p[q].xfrag = xfrag_buffer(M, ws[q].K, work, work_bytes);   // one copy of x for every product
         t.tile_start[q + 1] = t.tile_start[q] + (int)ceil_div(ws[q].N, gemv::kRowsPerCta);
     }
     for (int q = n; q < gemv::kMultiMax; q++) t.tile_start[q + 1] = t.tile_start[n];

@@ -321,6 +321,10 @@ struct Problem {
     const int* fb_col;
     const uint16_t* fb_val;
     int fb_cap;
+    // x already in fp16 B-fragment order (k_x_frag, once per call; null: each
+    // CTA converts its own x blocks), and the device status word
+    const unsigned char* xfrag;
+    int* status;
 };
 
 __device__ __forceinline__ int x_row(const Problem& p, int m) { return p.rowmap ? p.rowmap[m] / p.xdiv : m; }
@@ -335,8 +339,12 @@ struct Cfg {
     static constexpr int STEPS = G / 16;
     static constexpr int NT = (MP + 7) / 8;                       // n8 token tiles
     static constexpr int NTOK = 8 * NT;
-    // prefetch depth (groups) of the register ring
-    static constexpr int D_CLAMP = (MP <= 16 && NW < 8) ? 4 : 2;   // 8-word chunks (8 bits, group 128): 2
+    // prefetch depth (groups) of the register ring: 8-word chunks (8 bits,
+    // group 128) take 2; a group of 32 is a quarter of a 128-group's bytes,
+    // so its ring is deeper (16 one-word chunks, 8 two-word chunks or 2-bit
+    // groups, whose codebooks ride the ring) to keep as many bytes in flight
+    static constexpr int D_CLAMP = G == 32 ? (MP <= 16 ? (BITS == 2 || NW > 1 ? 8 : 16) : 4)
+                                           : ((MP <= 16 && NW < 8) ? 4 : 2);
     static constexpr int TSTRIDE = 32;                            // bytes per token per step
     static constexpr int SSTRIDE = MP * TSTRIDE;                  // bytes per step
     static constexpr int GSTRIDE = STEPS * SSTRIDE;               // bytes per group
@@ -361,57 +369,119 @@ struct Cfg {
         const int xs = (gpsplit < XG ? gpsplit : XG) * BSTRIDE;
         return ((xs > RED_BYTES ? xs : RED_BYTES) + 15) / 16 * 16;
     }
-    static int smem(int gpsplit, int S) { return slot_offset(gpsplit) + (S > 1 ? SLOT_BYTES : 0); }
+    // the mbarrier of the x-block bulk copies, after the slots
+    __host__ __device__ static int mbar_offset(int gpsplit, int S) { return slot_offset(gpsplit) + (S > 1 ? SLOT_BYTES : 0); }
+    static int smem(int gpsplit, int S) { return mbar_offset(gpsplit, S) + 16; }
 };
+
+// One x item (token m, thread slot t of one group): the thread's NC
+// contiguous bf16 values at xr, converted to fp16 and stored as STEPS 8-byte
+// entries at dst + s * SSTRIDE, each holding the 4 values whose k positions
+// match the A-fragment codes of thread t in step s.  16-byte loads when xr
+// is 16-byte aligned.
+template <int BITS, int G, int MP, typename Dst>
+__device__ __forceinline__ void x_frag_item(const __nv_bfloat16* xr, Dst* dst)
+{
+    using C = Cfg<BITS, G, MP>;
+    constexpr int NV = C::NC / 2;
+    uint32_t v[NV];
+    if ((reinterpret_cast<uintptr_t>(xr) & 15u) == 0) {
+#pragma unroll
+        for (int i = 0; i < C::NC / 8; i++) {
+            const uint4 q = __ldg(reinterpret_cast<const uint4*>(xr) + i);
+            v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+        }
+    } else {
+        const unsigned short* x16 = reinterpret_cast<const unsigned short*>(xr);
+#pragma unroll
+        for (int i = 0; i < NV; i++)
+            v[i] = (uint32_t)__ldg(x16 + 2 * i) | ((uint32_t)__ldg(x16 + 2 * i + 1) << 16);
+    }
+    auto f16 = [&](int c) -> uint32_t {   // bf16 -> fp32 (exact) -> fp16
+        const uint32_t bits = (c & 1) ? (v[c >> 1] & 0xFFFF0000u) : (v[c >> 1] << 16);
+        return __half_as_ushort(__float2half_rn(__uint_as_float(bits)));
+    };
+    static_for<0, C::STEPS>([&](auto sc) {
+        constexpr int s = decltype(sc)::value;
+        constexpr PairE e0 = plan_entry(BITS, C::NC, 2 * s);
+        constexpr PairE e1 = plan_entry(BITS, C::NC, 2 * s + 1);
+        *reinterpret_cast<uint2*>(reinterpret_cast<unsigned char*>(dst) + s * C::SSTRIDE) =
+            make_uint2(f16(e0.lo) | (f16(e0.hi) << 16), f16(e1.lo) | (f16(e1.hi) << 16));
+    });
+}
 
 // Stage x[:, kbase : kbase + ngr*G] as fp16 in MMA B-fragment order: the
 // 8-byte entry (group, step, token m, t) holds the 4 values of token m whose k
 // positions match the A-fragment codes of thread t in that step.  One item
-// = (group, token, t): 16-byte loads of the thread's NC contiguous bf16
-// values, then one 8-byte store per step.  Tokens M..MP-1 are not written:
-// the MMA columns that read them are never stored.
+// = (group, token, t).  Tokens M..MP-1 are not written: the MMA columns that
+// read them are never stored.
 template <int BITS, int G, int MP>
 __device__ void stage_x(const Problem& a, int kbase, int ngr, unsigned char* xs, int nthr)
 {
     using C = Cfg<BITS, G, MP>;
-    constexpr int NV = C::NC / 2;
     const int M = a.M;
     const int items = ngr * M * 4;
-    auto load = [&](int it, uint32_t (&v)[NV]) {
+    for (int it = threadIdx.x; it < items; it += nthr) {
         const int t = it & 3, m = (it >> 2) % M, gi = (it >> 2) / M;
         const __nv_bfloat16* xr = a.x + (size_t)x_row(a, m) * a.ldx + kbase + gi * G + t * C::NC;
-        if ((reinterpret_cast<uintptr_t>(xr) & 15u) == 0) {
-#pragma unroll
-            for (int i = 0; i < C::NC / 8; i++) {
-                const uint4 q = __ldg(reinterpret_cast<const uint4*>(xr) + i);
-                v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
-            }
+        x_frag_item<BITS, G, MP>(xr, xs + (size_t)gi * C::GSTRIDE + m * C::TSTRIDE + t * 8);
+    }
+}
+
+// The same x block from the fragment-order copy of x (a.xfrag, written once
+// per call by k_x_frag in exactly the staged layout, group after group): one
+// bulk copy by thread 0, completing on the CTA's mbarrier, which every thread
+// then waits on (bounded; a wait that gives up sets the status word and the
+// kernel carries on, so that no thread leaves a barrier the others reach).
+template <int BITS, int G, int MP>
+__device__ void stage_x_bulk(const Problem& a, int g0, int ngr, unsigned char* xs, uint32_t bar, uint32_t& phase)
+{
+    using C = Cfg<BITS, G, MP>;
+    if (threadIdx.x == 0) {
+        const uint32_t bytes = (uint32_t)ngr * C::GSTRIDE;
+        ptx::fence_proxy_async();   // the block's earlier generic accesses before the async write
+        ptx::mbar_expect_tx(bar, bytes);
+        ptx::bulk_load(ptx::smem_u32(xs), a.xfrag + (size_t)g0 * C::GSTRIDE, bytes, bar);
+    }
+    if (!ptx::mbar_wait(bar, phase) && a.status) atomicExch(a.status, (int)QG_ERR_TIMEOUT);
+    phase ^= 1u;
+}
+
+// Programmatic dependent launch.  The dense decode kernels are launched with
+// programmatic stream serialization, so that the next one can be resident and
+// have its first weight groups in registers while this one drains: a kernel
+// reads only weight data (codes, group parameters, outlier CSR) before
+// griddepcontrol.wait, which returns once the grids it depends on have
+// completed and their writes are visible; x and y are touched only after it.
+// The kernel immediately preceding a decode product on its stream therefore
+// must not write that product's weights (the quantizer ends with an empty
+// kernel for this reason).  Dependents are released after the main loop.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// x [M, K] to fp16 B-fragment order for every group, tokens padded to MP
+// with zeros: entry (group, step, token, t) at group * GSTRIDE + step *
+// SSTRIDE + token * TSTRIDE + t * 8, the layout a decode CTA stages.  It lets
+// dependents launch at once (their weight loads overlap this kernel) and
+// waits for the kernel that wrote x before reading it.
+template <int BITS, int G, int MP>
+__global__ void __launch_bounds__(256) k_x_frag(const __nv_bfloat16* __restrict__ x, int ldx, int M, int K,
+                                                unsigned char* __restrict__ out)
+{
+    using C = Cfg<BITS, G, MP>;
+    pdl_release();
+    pdl_wait();
+    const long long items = (long long)(K / G) * MP * 4;
+    for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < items;
+         it += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(it & 3), m = (int)((it >> 2) % MP), gi = (int)((it >> 2) / MP);
+        unsigned char* dst = out + (size_t)gi * C::GSTRIDE + m * C::TSTRIDE + t * 8;
+        if (m < M) {
+            x_frag_item<BITS, G, MP>(x + (size_t)m * ldx + gi * G + t * C::NC, dst);
         } else {
-            const unsigned short* x16 = reinterpret_cast<const unsigned short*>(xr);
 #pragma unroll
-            for (int i = 0; i < NV; i++)
-                v[i] = (uint32_t)__ldg(x16 + 2 * i) | ((uint32_t)__ldg(x16 + 2 * i + 1) << 16);
+            for (int s = 0; s < C::STEPS; s++) *reinterpret_cast<uint2*>(dst + s * C::SSTRIDE) = make_uint2(0u, 0u);
         }
-    };
-    auto store = [&](int it, const uint32_t (&v)[NV]) {
-        const int t = it & 3, m = (it >> 2) % M, gi = (it >> 2) / M;
-        auto f16 = [&](int c) -> uint32_t {   // bf16 -> fp32 (exact) -> fp16
-            const uint32_t bits = (c & 1) ? (v[c >> 1] & 0xFFFF0000u) : (v[c >> 1] << 16);
-            return __half_as_ushort(__float2half_rn(__uint_as_float(bits)));
-        };
-        unsigned char* dst = xs + (size_t)gi * C::GSTRIDE + m * C::TSTRIDE + t * 8;
-        static_for<0, C::STEPS>([&](auto sc) {
-            constexpr int s = decltype(sc)::value;
-            constexpr PairE e0 = plan_entry(BITS, C::NC, 2 * s);
-            constexpr PairE e1 = plan_entry(BITS, C::NC, 2 * s + 1);
-            *reinterpret_cast<uint2*>(dst + s * C::SSTRIDE) =
-                make_uint2(f16(e0.lo) | (f16(e0.hi) << 16), f16(e1.lo) | (f16(e1.hi) << 16));
-        });
-    };
-    for (int it = threadIdx.x; it < items; it += nthr) {
-        uint32_t v[NV];
-        load(it, v);
-        store(it, v);
     }
 }
 
@@ -555,17 +625,6 @@ __device__ __forceinline__ void mma_group(const uint32_t (&w0)[Chunk<BITS, G>::N
     }
 }
 
-// Programmatic dependent launch.  The dense decode kernels are launched with
-// programmatic stream serialization, so that the next one can be resident and
-// have its first weight groups in registers while this one drains: a kernel
-// reads only weight data (codes, group parameters, outlier CSR) before
-// griddepcontrol.wait, which returns once the grids it depends on have
-// completed and their writes are visible; x and y are touched only after it.
-// The kernel immediately preceding a decode product on its stream therefore
-// must not write that product's weights (the quantizer ends with an empty
-// kernel for this reason).  Dependents are released after the main loop.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Cluster barrier in two halves, and an fp32 add into another CTA's shared
 // memory (distributed shared memory of the thread-block cluster).
@@ -795,12 +854,27 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     OutCursor oc;
     oc.init(a, splits, tile);
 
+    // x from the fragment-order copy: one bulk copy per x block on this mbarrier
+    const bool xpre = a.xfrag != nullptr;
+    const uint32_t xbar = ptx::smem_u32(smem + C::mbar_offset(gpsplit, splits));
+    uint32_t xphase = 0;
+    if (xpre) {
+        if (threadIdx.x == 0) {
+            ptx::mbar_init(xbar, 1);
+            ptx::fence_mbar_init();
+        }
+        __syncthreads();
+    }
+
     uint32_t* const pblock = reinterpret_cast<uint32_t*>(smem + C::prm_offset(gpsplit));
     if constexpr (BITS != 2)   // weight data: staged before the dependency wait
         if (ngrp > 0) stage_prm<BITS, G>(a, tile, g_begin, min(C::XG, ngrp), pblock, blockDim.x);
 
     pdl_wait();   // weight loads are in flight; x may come from the preceding kernel
-    if (ngrp > 0) stage_x<BITS, G, MP>(a, g_begin * G, min(C::XG, ngrp), smem, blockDim.x);
+    if (ngrp > 0) {
+        if (xpre) stage_x_bulk<BITS, G, MP>(a, g_begin, min(C::XG, ngrp), smem, xbar, xphase);
+        else stage_x<BITS, G, MP>(a, g_begin * G, min(C::XG, ngrp), smem, blockDim.x);
+    }
     __syncthreads();
     oc.fetch(a);
 
@@ -810,7 +884,8 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     for (int jj = 0; jj < ngrp; jj += D) {
         if (jj == xnext) {
             __syncthreads();
-            stage_x<BITS, G, MP>(a, (g_begin + jj) * G, min(C::XG, ngrp - jj), smem, blockDim.x);
+            if (xpre) stage_x_bulk<BITS, G, MP>(a, g_begin + jj, min(C::XG, ngrp - jj), smem, xbar, xphase);
+            else stage_x<BITS, G, MP>(a, (g_begin + jj) * G, min(C::XG, ngrp - jj), smem, blockDim.x);
             if constexpr (BITS != 2) stage_prm<BITS, G>(a, tile, g_begin + jj, min(C::XG, ngrp - jj), pblock, blockDim.x);
             __syncthreads();
             xnext += C::XG;
@@ -820,7 +895,7 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
         const unsigned char* xb[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; nt++) xb[nt] = smem + xoff + xlo[nt];
-        if constexpr (BITS != 2) {
+        if constexpr (BITS != 2 && G != 32) {
             static_for<0, D>([&](auto dc) {
                 constexpr int d = decltype(dc)::value;
                 if (jj + d < ngrp) {   // only staged groups lie inside the block
@@ -838,7 +913,13 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
                     const unsigned char* xg[NT];
 #pragma unroll
                     for (int nt = 0; nt < NT; nt++) xg[nt] = xb[nt] + d * C::GSTRIDE;
-                    if constexpr (Chunk<BITS, G>::SPLIT) {
+                    if constexpr (BITS != 2 && G == 32) {
+                        // group 32: the group's parameters straight from the
+                        // staged block (a ring of them would not fit in registers)
+                        const uint2 v = *reinterpret_cast<const uint2*>(ps + pw + d * kWarps * 16);
+                        const uint32_t pg[2][2] = {{v.x, v.x >> 16}, {v.y, v.y >> 16}};
+                        mma_group<BITS, G, MP>(wr[d][0], wr[d][1], pg, xg, yacc, magic);
+                    } else if constexpr (Chunk<BITS, G>::SPLIT) {
                         uint32_t s0[NW], s1[NW];
                         Chunk<BITS, G>::order(wr[d][0], s0, odd_chunk);
                         Chunk<BITS, G>::order(wr[d][1], s1, odd_chunk);
@@ -934,6 +1015,8 @@ __global__ void __launch_bounds__(kWarps * 32) k_gemv_moe(const __grid_constant_
     p.magic = t.magic;
     p.scale8 = t.scale8[e]; p.scale8_exp = t.scale8_exp[e];
     p.fb_row_ptr = t.fb_row_ptr[e]; p.fb_col = t.fb_col[e]; p.fb_val = t.fb_val[e]; p.fb_cap = t.fb_cap[e];
+    p.xfrag = nullptr;   // routed rows: each CTA gathers and converts its x blocks
+    p.status = nullptr;
     gemv_body<BITS, G, MP>(p, splits, gpsplit, blockIdx.x);
 }
 
@@ -1022,9 +1105,36 @@ size_t decode_smem(int gps, int S)
     return (size_t)std::max(need, smem_for_cap(S > 1 ? 4 : 3));
 }
 
+// The fragment-order copy of x for products launched next (one per call,
+// shared by the products of a fused call): k_x_frag with programmatic
+// serialization, so that it overlaps the tail of the preceding product.
+template <int BITS, int G, int MP>
+qg_status launch_x_frag(const Problem& p, cudaStream_t s)
+{
+    const long long items = (long long)(p.K / G) * MP * 4;
+    const int blocks = (int)std::max<long long>(1, std::min<long long>(ceil_div(items, 256), 2LL * num_sms()));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_x_frag<BITS, G, MP>, p.x, p.ldx, p.M, p.K,
+                                       const_cast<unsigned char*>(p.xfrag));
+    if (e != cudaSuccess) return cuda_fail(e, "x conversion kernel launch");
+    return QG_OK;
+}
+
 template <int BITS, int G, int MP>
 qg_status dense_mp(const Problem& p, cudaStream_t s)
 {
+    if (p.xfrag) {
+        qg_status st = launch_x_frag<BITS, G, MP>(p, s);
+        if (st != QG_OK) return st;
+    }
     const int ng = p.K / G;
     const int tiles = (int)ceil_div(p.N, kRowsPerCta);
     const int S = choose_splits(tiles, ng);
@@ -1040,6 +1150,10 @@ qg_status dense_mp(const Problem& p, cudaStream_t s)
 template <int BITS, int G, int MP>
 qg_status multi_mp(const MultiTable& t, cudaStream_t s)
 {
+    if (t.p[0].xfrag) {
+        qg_status st = launch_x_frag<BITS, G, MP>(t.p[0], s);
+        if (st != QG_OK) return st;
+    }
     const int ng = t.p[0].K / G;
     const int tiles = t.tile_start[t.n];
     const int S = choose_splits(tiles, ng);

@@ -44,8 +44,19 @@ qg_status launch_quantize(const uint16_t* W, float frac, const qg_qweight& w, vo
 // decode kernel takes 13.3 ms per 20 layers against 20.8 ms on the tensor
 // cores, at M = 64 27.5 ms against 21.0 ms.
 constexpr int kGemvMaxM = 32;
+// From this M on, a decode call converts x once into the fp16 fragment order
+// the CTAs stage (in the caller's workspace) and the CTAs bulk-copy their x
+// blocks, instead of every CTA converting them.
+constexpr int kXFragMinM = 8;
+inline int padded_tokens(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : 64; }
+// Workspace of a decode call: the fragment-order copy of x (0 below kXFragMinM).
+inline size_t gemv_workspace_bytes(int M, int K)
+{
+    return M >= kXFragMinM ? align_up((size_t)2 * K * padded_tokens(M), 256) : 0;
+}
+// ws: the decode workspace, or null (or too small): each CTA then converts its own x blocks.
 qg_status launch_gemv(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,
-                      qg_ydtype yt, cudaStream_t s);
+                      qg_ydtype yt, void* ws, size_t ws_bytes, cudaStream_t s);
 
 // Device status word of the library's kernels with bounded waits (nullptr if
 // it has no address on the current device) and its synchronous read
@@ -58,7 +69,7 @@ qg_status launch_wait_selftest(uint32_t limit, cudaStream_t s);
 // Up to kMultiMax products sharing x (same M, K, bits, group) in one decode launch.
 constexpr int kMultiMax = 4;
 qg_status launch_gemv_multi(const uint16_t* x, int M, int ldx, const qg_qweight* ws, int n, void* const* ys,
-                            const int32_t* ldys, qg_ydtype yt, cudaStream_t s);
+                            const int32_t* ldys, qg_ydtype yt, void* work, size_t work_bytes, cudaStream_t s);
 
 // ---------------------------------------------------------------- tensor-core GEMM
 size_t gemm_workspace_bytes(int M, const qg_qweight& w);

@@ -268,3 +268,36 @@ def test_decode_long_k_with_outliers(qg, M):
     y = qg.qgemm_forward(x.cuda(), to_device(q))
     torch.cuda.synchronize()
     check_product(y, oracle.linear(x, q), x, wmax)
+
+
+def _forward_raw(qg, x, qd, ws):
+    """qgemm_forward through the C ABI with an explicit workspace (None: none)."""
+    import ctypes
+    M, K = x.shape
+    y = torch.empty((M, qd.N), dtype=torch.float32, device="cuda")
+    d = qd.desc()
+    st = qg.lib().qgemm_forward(x.data_ptr(), M, K, ctypes.byref(d), y.data_ptr(), qd.N, 0,
+                                None if ws is None else ws.data_ptr(), 0 if ws is None else ws.numel(), None)
+    assert st == 0, qg.last_error()
+    return y
+
+
+@pytest.mark.parametrize("bits,group", [(4, 128), (2, 128), (3, 64), (5, 32), (8, 128), (6, 32)])
+@pytest.mark.parametrize("M", [8, 13, 16, 27, 32])
+def test_decode_converted_x_matches_per_cta_staging(qg, bits, group, M):
+    # from M = 8 the call converts x once into fragment order in the workspace
+    # and the CTAs bulk-copy it; without a workspace every CTA converts its own
+    # x blocks: the operands, and so the results, are the same bit for bit
+    N, K = 200, 2048
+    q, wmax = _weights(N, K, bits, group, 0.002, seed=3 * bits + group)
+    qd = to_device(q)
+    x = wl.gen_x(M, K, seed=M + 100).cuda()
+    need = qg.qgemm_workspace_size(M, qd)
+    assert need >= 2 * K * M
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    y_conv = _forward_raw(qg, x, qd, ws)
+    y_cta = _forward_raw(qg, x, qd, None)
+    torch.cuda.synchronize()
+    assert torch.equal(y_conv, y_cta)
+    check_product(y_conv, oracle.linear(x.cpu(), q), x.cpu(), wmax)
+    assert qg.qgemm_device_status() == 0
