@@ -251,11 +251,17 @@ QG_API qg_status qgemm_workspace_size(int32_t M, const qg_qweight* w, size_t* by
  * M = 0 is a no-op.  M <= 32 runs the decode kernel (register dequant, split
  * K across a thread-block cluster); larger M runs the tensor-core kernel
  * (tcgen05 with TMEM accumulators), which converts x to fp16 in the workspace.
- * `ws` may be NULL when qgemm_workspace_size reports 0.
+ * From M = 8 the decode call also uses the workspace: x is converted once
+ * into the fp16 fragment order the kernel stages (2 * K * Mpad bytes, Mpad
+ * the next of 8, 16, 32), and every CTA copies its blocks of it; with no or a
+ * smaller workspace each CTA converts its own blocks instead, with the same
+ * result, more slowly.  `ws` may be NULL when qgemm_workspace_size reports 0.
+ * |x| must stay below 65520: x is converted to fp16 on every path.
  * Ordering: the decode kernel is launched with programmatic dependent launch,
  * so it may start, and read the weight buffers (packed, scale, zp, codebook,
- * outlier CSR), before the kernel launched just before it on the same stream
- * has finished; it reads x and writes y only after that kernel has completed.
+ * outlier CSR, 8-bit scale arrays), before the kernel launched just before it
+ * on the same stream has finished; it reads x and writes y only after that
+ * kernel has completed.
  * The kernel launched immediately before qgemm_forward on the stream must
  * therefore not write w's buffers (qpack_quantize ends with an empty kernel,
  * and copies are not kernels, so quantizing or uploading on the same stream
