@@ -66,7 +66,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
     ap.add_argument("--case", default="gateup1",
                     help="--mode case: one small case, three calls, for a profiler: gateup<M> (fused 28672x8192 "
-                         "gate/up decode at M), tiles<bits> / planar<bits> (8192x8192 at M=2048), moe (gate/up of "
+                         "gate/up decode at M), tiles<bits>[m<M>] / planar<bits>[m<M>] (8192x8192 at M=2048 or M), moe (gate/up of "
                          "the MoE layer), w8a8 (28672x8192 at M=1), diag / repack (28672x8192 INT4)")
     return ap.parse_args()
 
@@ -908,9 +908,10 @@ def run_case(qg, name):
         x = wl.gen_x(M, 8192, device=dev)
         call = lambda: qg.qgemm_forward_multi(x, qs)
     elif name.startswith("tiles") or name.startswith("planar"):
-        bits = int(name[5:] if name.startswith("tiles") else name[6:])
+        spec = name[5:] if name.startswith("tiles") else name[6:]   # <bits> or <bits>m<M>
+        bits, M = (int(spec.split("m")[0]), int(spec.split("m")[1])) if "m" in spec else (int(spec), 2048)
         q = qg.qpack_quantize(wl.gen_weight(8192, 8192, seed=1, device=dev, outlier_frac=0.001), bits, 128, 0.001)
-        x = wl.gen_x(2048, 8192, device=dev)
+        x = wl.gen_x(M, 8192, device=dev)
         if name.startswith("tiles"):
             t = qg.qrepack_tiles(q)
             call = lambda: qg.qgemm_forward_tiles(x, q, t)

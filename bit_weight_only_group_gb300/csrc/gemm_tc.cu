@@ -121,9 +121,40 @@ struct Args {
     int* status;
     uint32_t magic;   // gemv::kF16Magic, a run-time value (one logic op per code pair)
     ScaleSrc sc;      // 8-bit scales when sc.scale8 is set (planar kernels; the tile copy holds fp16)
+    // split K (gridDim.z > 1): CTA z takes K blocks [z * kbs, (z + 1) * kbs),
+    // writes its fp32 partial tile to part (z-th slab of M x ldp), and the last
+    // of a tile's CTAs to finish (tile_cnt) sums the slabs in z order into y
+    int kbs;
+    float* part;
+    int ldp;
+    unsigned* tile_cnt;
 };
 
 static_assert(kDeqWarps * 32 == 512, "deq_sync counts 512 dequantization threads");
+
+// 16 consecutive y values of token m from column nb (fp32 or bf16 per a.y_bf16;
+// nothing at or past N).
+__device__ __forceinline__ void store_y16(const Args& a, int m, int nb, const uint32_t (&v)[16])
+{
+    if (a.y_bf16) {
+        __nv_bfloat16* yr = reinterpret_cast<__nv_bfloat16*>(a.y) + (size_t)m * a.ldy;
+#pragma unroll
+        for (int j = 0; j < 16; j++)
+            if (nb + j < a.N) yr[nb + j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+    } else {
+        float* yr = reinterpret_cast<float*>(a.y) + (size_t)m * a.ldy;
+        if (nb + 16 <= a.N && ((reinterpret_cast<uintptr_t>(yr + nb) & 15u) == 0)) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+                *reinterpret_cast<float4*>(yr + nb + j) = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                                                      __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; j++)
+                if (nb + j < a.N) yr[nb + j] = __uint_as_float(v[j]);
+        }
+    }
+}
 
 template <int BITS, int G, bool TILES>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -155,7 +186,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
-    const int KB = a.K / BK;
+    // this CTA's K blocks [kb0, kb1); kbs is a multiple of the packed tile's PK blocks
+    const int kb0 = (int)blockIdx.z * a.kbs, kb1 = min(a.K / BK, kb0 + a.kbs);
+    const int KB = kb1;   // loops run kb0 .. KB - 1
+    // tokens m0 + 128 .. m0 + 255 exist: both accumulators; else only the first
+    const bool two = a.M - m0 > MH;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SA; s++) { ptx::mbar_init(full_a(s), 1); ptx::mbar_init(empty_a(s), 1); }
@@ -184,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
-            for (int kb = 0; kb < KB; kb++) {
+            for (int kb = kb0; kb < KB; kb++) {
                 if (!ptx::mbar_wait(empty_a(s), ph ^ 1u)) { ok = false; break; }
                 ptx::mbar_expect_tx(full_a(s), A_BYTES);
                 ptx::tma_load_2d(a_tile(s), &xmap, kb * BK, m0, full_a(s));
@@ -198,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int KP = (KB + PK - 1) / PK;
                 int s = 0;
                 uint32_t ph = 0;
-                for (int kp = 0; kp < KP; kp++) {
+                for (int kp = kb0 / PK; kp < KP; kp++) {
                     if (!ptx::mbar_wait(empty_p(s), ph ^ 1u)) { ok = false; break; }
                     ptx::mbar_expect_tx(full_p(s), C::P_BYTES);
                     ptx::tma_load_2d(ptx::smem_u32(p_tile(s)), &wmap, kp * (PK * BK * BITS / 8), n0, full_p(s));
@@ -208,10 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if constexpr (TILES) {
             // one bulk copy per K block: the block of this CTA's 256-row tile
             if (lane == 0) {
-                const uint8_t* base = a.tiles + (size_t)blockIdx.y * KB * C::BLOCK;
+                const uint8_t* base = a.tiles + (size_t)blockIdx.y * (a.K / BK) * C::BLOCK;
                 int s = 0;
                 uint32_t ph = 0;
-                for (int kb = 0; kb < KB; kb++) {
+                for (int kb = kb0; kb < KB; kb++) {
                     if (!ptx::mbar_wait(empty_p(s), ph ^ 1u)) { ok = false; break; }
                     ptx::mbar_expect_tx(full_p(s), C::BLOCK);
                     ptx::bulk_load(ptx::smem_u32(p_tile(s)), base + (size_t)kb * C::BLOCK, C::BLOCK, full_p(s));
@@ -225,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t adesc0 = ptx::sw128_desc(a_tile(0)), bdesc0 = ptx::sw128_desc(b_tile(0));
         int sa = 0, sb = 0;
         uint32_t pa = 0, pb = 0;
-        for (int kb = 0; kb < KB; kb++) {
+        for (int kb = kb0; kb < KB; kb++) {
             ok = __all_sync(0xffffffffu, ptx::mbar_wait(full_a(sa), pa) && ptx::mbar_wait(full_b(sb), pb));
             if (!ok) break;
             ptx::tc_fence_after();
@@ -236,8 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = bdesc0 + (uint64_t)((sb * B_BYTES) >> 4);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; kk++) {
-                ptx::mma_f16_elect(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
-                ptx::mma_f16_elect(tmem + BN, ad + ((MH * 128) >> 4) + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                const bool acc = ((kb - kb0) | kk) != 0;
+                ptx::mma_f16_elect(tmem, ad + 2 * kk, bd + 2 * kk, idesc, acc);
+                if (two) ptx::mma_f16_elect(tmem + BN, ad + ((MH * 128) >> 4) + 2 * kk, bd + 2 * kk, idesc, acc);
             }
             ptx::tc_commit_elect(empty_a(sa));
             ptx::tc_commit_elect(empty_b(sb));
@@ -285,10 +321,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             else return make_uint2(s8 ? (uint32_t)__ldg(s8_row + gi) : (uint32_t)__ldg(sp_row + gi),
                                    (uint32_t)__ldg(zp_row + gi));
         };
+        const int gs = g0 + (kb0 / KB_PER_G) * GSTEP;   // group of block kb0
         if constexpr (!TILES) {
-            prm[0] = load_prm(g0);
-            prm[1] = g0 + GSTEP < ng ? load_prm(g0 + GSTEP) : make_uint2(0u, 0u);
-            prm[2] = g0 + 2 * GSTEP < ng ? load_prm(g0 + 2 * GSTEP) : make_uint2(0u, 0u);
+            prm[0] = load_prm(gs);
+            prm[1] = gs + GSTEP < ng ? load_prm(gs + GSTEP) : make_uint2(0u, 0u);
+            prm[2] = gs + 2 * GSTEP < ng ? load_prm(gs + 2 * GSTEP) : make_uint2(0u, 0u);
         }
         // outlier cursor of this row: the next entry (ocol, oval) and the one
         // after it (ncol, nval), so that consuming an entry never waits for a load
@@ -297,6 +334,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (a.nnz > 0 && nr < a.N) {
             op = a.row_ptr[n];
             oe = a.row_ptr[n + 1];
+            if (kb0 > 0) {   // first entry at or after column kb0 * BK
+                int hi = oe;
+                while (op < hi) {
+                    const int mid = (op + hi) >> 1;
+                    if (a.col[mid] < kb0 * BK) op = mid + 1;
+                    else hi = mid;
+                }
+            }
             if (op < oe) {
                 ocol = a.col[op];
                 oval = a.val[op];
@@ -358,9 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
         // next group: shift the parameter window
-        int gcur = g0;   // group of prm[0]
+        int gcur = gs;   // group of prm[0]
         auto next_group = [&](int kb) {
-            if (kb > 0 && kb % KB_PER_G == 0) {
+            if (kb > kb0 && kb % KB_PER_G == 0) {
                 const int gi = g0 + (kb / KB_PER_G) * GSTEP;
                 gcur = gi;
                 prm[0] = prm[1];
@@ -380,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr int NPG = tile_groups_per_block(G);
             int sp = 0;
             uint32_t pp = 0;   // parity of full_p to wait for
-            for (int kb = 0; kb < KB && ok; kb++) {
+            for (int kb = kb0; kb < KB && ok; kb++) {
                 if (!ptx::mbar_wait(full_p(sp), pp)) { ok = false; break; }
                 const uint32_t* pw = reinterpret_cast<const uint32_t*>(p_tile(sp));
                 uint32_t w[BITS];
@@ -421,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int KP = (KB + PK - 1) / PK;
             int sp = 0;
             uint32_t pp = 0;   // parity of full_p to wait for
-            for (int kp = 0; kp < KP && ok; kp++) {
+            for (int kp = kb0 / PK; kp < KP && ok; kp++) {
                 const unsigned char* pt = p_tile(sp);
                 if (!ptx::mbar_wait(full_p(sp), pp)) { ok = false; break; }
 #pragma unroll
@@ -460,12 +505,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t wr[DG][NW];
             gemv::static_for<0, DG>([&](auto dc) {
                 constexpr int d = decltype(dc)::value;
-                if (d < KB) Ch::load(prow + d * 8 * BITS, wr[d]);
+                if (kb0 + d < KB) Ch::load(prow + (kb0 + d) * 8 * BITS, wr[d]);
             });
-            for (int kb0 = 0; kb0 < KB && ok; kb0 += DG) {
+            for (int kbd = kb0; kbd < KB && ok; kbd += DG) {
                 gemv::static_for<0, DG>([&](auto dc) {
                     constexpr int d = decltype(dc)::value;
-                    const int kb = kb0 + d;
+                    const int kb = kbd + d;
                     if (ok && kb < KB) {
                         next_group(kb);
                         uint32_t w[NW];
@@ -508,10 +553,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // warp w reads TMEM lanes 32 (w % 4) .. (the lanes a warp may
             // access) and a quarter of the 512 columns
             const int q = warp & 3, quarter = warp >> 2;
+            const bool split = gridDim.z > 1;
 #pragma unroll 1
             for (int i = 0; i < 8; i++) {
                 const int col = 128 * quarter + 16 * i;       // 0..511
                 const int half = col / BN, cb = col % BN;
+                if (half && !two) continue;                   // no tokens in the second accumulator
                 const int m = m0 + MH * half + 32 * q + lane;
                 uint32_t v[16];
                 ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, v);
@@ -527,25 +574,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (m < a.M) {
-                    const int nb = n0 + cb;
-                    if (a.y_bf16) {
-                        __nv_bfloat16* yr = reinterpret_cast<__nv_bfloat16*>(a.y) + (size_t)m * a.ldy;
+                    if (split) {   // the partial tile to this CTA's slab (ldp covers whole tiles)
+                        float* pr = a.part + ((size_t)blockIdx.z * a.M + m) * a.ldp + n0 + cb;
 #pragma unroll
-                        for (int j = 0; j < 16; j++)
-                            if (nb + j < a.N) yr[nb + j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                        for (int j = 0; j < 16; j += 4)
+                            __stcg(reinterpret_cast<float4*>(pr + j),
+                                   make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                               __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])));
                     } else {
-                        float* yr = reinterpret_cast<float*>(a.y) + (size_t)m * a.ldy;
-                        if (nb + 16 <= a.N && ((reinterpret_cast<uintptr_t>(yr + nb) & 15u) == 0)) {
+                        store_y16(a, m, n0 + cb, v);
+                    }
+                }
+            }
+            if (split) {
+                // the last CTA of this tile to get here sums the slabs in z order:
+                // partial stores, then a fence, then the count (no CTA waits on another)
+                __threadfence();
+                deq_sync();
+                uint32_t* last = reinterpret_cast<uint32_t*>(e_row + BN);
+                if (threadIdx.x == 0) {
+                    unsigned* cnt = a.tile_cnt + blockIdx.y * gridDim.x + blockIdx.x;
+                    const unsigned prev = atomicAdd(cnt, 1u);
+                    *last = prev + 1 == gridDim.z;
+                    if (*last) *cnt = 0u;   // ready for the next call
+                }
+                deq_sync();
+                if (*last) {
+                    __threadfence();
+#pragma unroll 1
+                    for (int i = 0; i < 8; i++) {
+                        const int col = 128 * quarter + 16 * i;
+                        const int half = col / BN, cb = col % BN;
+                        if (half && !two) continue;
+                        const int m = m0 + MH * half + 32 * q + lane;
+                        if (m >= a.M) continue;
+                        float acc[16];
 #pragma unroll
-                            for (int j = 0; j < 16; j += 4)
-                                *reinterpret_cast<float4*>(yr + nb + j) =
-                                    make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                                __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-                        } else {
+                        for (int j = 0; j < 16; j++) acc[j] = 0.0f;
+                        for (int z = 0; z < (int)gridDim.z; z++) {
+                            const float* pr = a.part + ((size_t)z * a.M + m) * a.ldp + n0 + cb;
 #pragma unroll
-                            for (int j = 0; j < 16; j++)
-                                if (nb + j < a.N) yr[nb + j] = __uint_as_float(v[j]);
+                            for (int j = 0; j < 16; j += 4) {
+                                const float4 t = __ldcg(reinterpret_cast<const float4*>(pr + j));
+                                acc[j] += t.x; acc[j + 1] += t.y; acc[j + 2] += t.z; acc[j + 3] += t.w;
+                            }
                         }
+                        uint32_t v[16];
+#pragma unroll
+                        for (int j = 0; j < 16; j++) v[j] = __float_as_uint(acc[j]);
+                        store_y16(a, m, n0 + cb, v);
                     }
                 }
             }
@@ -617,15 +694,64 @@ __global__ void k_x_to_f16(const __nv_bfloat16* __restrict__ x, int M, int K, in
 }
 
 // Workspace: x converted to fp16 (K order permuted), M x K.
+// Split K applies to products of at most kSplitMaxM tokens (one token tile,
+// whose grid of 256-row tiles is too small to fill the GPU); at most
+// kMaxSplit CTAs share a tile.
+constexpr int kSplitMaxM = 128, kMaxSplit = 8;
+
+// Workspace: x converted to fp16 (K order permuted), M x K; for small M also
+// the partial slabs (kMaxSplit x M x ldp fp32) and one counter per tile.
 struct Ws {
     __half* x16;
+    float* part;
+    unsigned* cnt;
+    int ldp;
 };
 
-size_t ws_layout(int M, int K, Ws* w, void* base)
+size_t ws_layout(int M, int N, int K, Ws* w, void* base)
 {
-    const size_t total = align_up((size_t)M * K * 2, 256);
-    if (w && base) w->x16 = reinterpret_cast<__half*>(base);
+    const size_t x16 = align_up((size_t)M * K * 2, 256);
+    size_t total = x16, o_part = 0, o_cnt = 0;
+    const int ldp = (int)ceil_div(N, BN) * BN;
+    if (M <= kSplitMaxM) {
+        o_part = total;
+        total += align_up((size_t)kMaxSplit * M * ldp * 4, 256);
+        o_cnt = total;
+        total += align_up((size_t)ceil_div(M, BM) * ceil_div(N, BN) * 4, 256);
+    }
+    if (w && base) {
+        char* b = static_cast<char*>(base);
+        w->x16 = reinterpret_cast<__half*>(b);
+        w->part = M <= kSplitMaxM ? reinterpret_cast<float*>(b + o_part) : nullptr;
+        w->cnt = M <= kSplitMaxM ? reinterpret_cast<unsigned*>(b + o_cnt) : nullptr;
+        w->ldp = ldp;
+    }
     return total;
+}
+
+// K splits of a launch: none above kSplitMaxM tokens; else the count (at
+// most kMaxSplit, at least 8 K blocks each, a whole number of packed tiles)
+// whose waves of one-CTA-per-SM grids end soonest.  Returns the split count
+// and sets *kbs to the K blocks per split.
+int choose_ksplit(int M, int tiles, int KB, int* kbs)
+{
+    *kbs = KB;
+    if (M > kSplitMaxM || KB < 16) return 1;
+    const int sms = num_sms();
+    int best = 1;
+    long long best_cost = ceil_div(tiles, sms) * (long long)KB;
+    for (int s = 2; s <= kMaxSplit; s++) {
+        const int k = (int)(ceil_div(ceil_div(KB, s), PK) * PK);
+        if (k < 8) break;
+        const int se = (int)ceil_div(KB, k);
+        const long long cost = ceil_div((long long)tiles * se, sms) * (long long)k;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = se;
+            *kbs = k;
+        }
+    }
+    return best;
 }
 
 template <int BITS, int G, bool TILES>
@@ -634,7 +760,7 @@ qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void
 {
     using C = Cfg<BITS, G, TILES>;
     Ws p{};
-    ws_layout(M, w.K, &p, ws);
+    ws_layout(M, w.N, w.K, &p, ws);
     {
         const long long total32 = (long long)M * w.K / 32;
         const int blocks = (int)std::min<long long>(ceil_div(total32, 256), (long long)num_sms() * 8);
@@ -665,7 +791,16 @@ qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void
         qg_status st2 = gemv::allow_smem(k_gemm_tc<BITS, G, TILES>, C::SMEM);
         if (st2 != QG_OK) return st2;
     }
-    dim3 grid((unsigned)ceil_div(M, BM), (unsigned)ceil_div(w.N, BN), 1);
+    const int tm = (int)ceil_div(M, BM), tn = (int)ceil_div(w.N, BN);
+    const int splits = choose_ksplit(M, tm * tn, w.K / BK, &a.kbs);
+    a.part = p.part;
+    a.ldp = p.ldp;
+    a.tile_cnt = p.cnt;
+    if (splits > 1) {
+        cudaError_t e0 = cudaMemsetAsync(p.cnt, 0, sizeof(unsigned) * (size_t)tm * tn, s);
+        if (e0 != cudaSuccess) return cuda_fail(e0, "split counters memset");
+    }
+    dim3 grid((unsigned)tm, (unsigned)tn, (unsigned)splits);
     k_gemm_tc<BITS, G, TILES><<<grid, kThreads, C::SMEM, s>>>(xmap, wmap, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
@@ -683,7 +818,7 @@ qg_status run_bits(const uint16_t* x, int M, int ldx, const qg_qweight& w, const
 
 }  // namespace tc
 
-size_t gemm_workspace_bytes(int M, const qg_qweight& w) { return tc::ws_layout(M, w.K, nullptr, nullptr); }
+size_t gemm_workspace_bytes(int M, const qg_qweight& w) { return tc::ws_layout(M, w.N, w.K, nullptr, nullptr); }
 
 qg_status launch_gemm(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy, qg_ydtype yt,
                       void* ws, size_t, cudaStream_t s)

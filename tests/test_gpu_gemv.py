@@ -215,7 +215,8 @@ def test_tensor_core_path_full_size_sampled(qg):
         check_product(y[toks.cuda(), n0:n1], oracle.linear(x[toks], q, n0, n1), x[toks], wmax)
 
 
-@pytest.mark.parametrize("bits,group,M", [(4, 128, 1), (4, 128, 8), (3, 64, 16), (4, 128, 130), (5, 32, 4), (2, 32, 130)])
+@pytest.mark.parametrize("bits,group,M", [(4, 128, 1), (4, 128, 8), (3, 64, 16), (4, 128, 130), (5, 32, 4), (2, 32, 130),
+                                          (4, 128, 64), (6, 64, 100)])
 def test_forward_multi_against_oracle(qg, bits, group, M):
     # a fused projection: three weights sharing x (different N, one ragged
     # tile) in one call; each output is the single product of its weight
@@ -283,7 +284,7 @@ def _forward_raw(qg, x, qd, ws):
 
 
 @pytest.mark.parametrize("bits,group", [(4, 128), (2, 128), (3, 64), (5, 32), (8, 128), (6, 32)])
-@pytest.mark.parametrize("M", [8, 13, 16, 27, 32])
+@pytest.mark.parametrize("M", [8, 13, 16, 21, 24])
 def test_decode_converted_x_matches_per_cta_staging(qg, bits, group, M):
     # from M = 8 the call converts x once into fragment order in the workspace
     # and the CTAs bulk-copy it; without a workspace every CTA converts its own
@@ -300,4 +301,26 @@ def test_decode_converted_x_matches_per_cta_staging(qg, bits, group, M):
     torch.cuda.synchronize()
     assert torch.equal(y_conv, y_cta)
     check_product(y_conv, oracle.linear(x.cpu(), q), x.cpu(), wmax)
+    assert qg.qgemm_device_status() == 0
+
+
+@pytest.mark.parametrize("bits,group,M,ytype", [(4, 128, 64, torch.float32), (5, 32, 40, torch.bfloat16),
+                                                (2, 128, 128, torch.float32), (3, 64, 33, torch.float32)])
+def test_tensor_core_split_k_against_oracle_and_repeatable(qg, bits, group, M, ytype):
+    # up to 128 tokens the tensor-core kernel splits K over several CTAs per
+    # tile; the last CTA of a tile sums the partial tiles in a fixed order, so
+    # the result is repeatable bit for bit, and matches the oracle
+    N, K = 600, 4096
+    q, wmax = _weights(N, K, bits, group, 0.003, seed=M + bits)
+    qd = to_device(q)
+    x = wl.gen_x(M, K, seed=M).cuda()
+    y0 = qg.qgemm_forward(x, qd, out_dtype=ytype)
+    for _ in range(10):
+        assert torch.equal(qg.qgemm_forward(x, qd, out_dtype=ytype), y0)
+    torch.cuda.synchronize()
+    if ytype == torch.float32:
+        check_product(y0, oracle.linear(x.cpu(), q), x.cpu(), wmax)
+    else:
+        y32 = qg.qgemm_forward(x, qd)
+        assert torch.equal(y0, y32.to(torch.bfloat16))
     assert qg.qgemm_device_status() == 0
