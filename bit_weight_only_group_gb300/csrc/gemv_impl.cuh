@@ -225,10 +225,42 @@ struct Chunk {
     // in stream order when the group is used (odd lanes: the 4-byte word
     // first).
     static constexpr bool SPLIT = CB % 8 == 4 && CB > 4;
+    // Group 32 with chunks off word boundaries (2, 3, 5, 6 bits): the group
+    // is BITS whole words per row, and lane t of a row's 4 lanes loads its
+    // words t and t + 4; each thread gathers the (at most two) words holding
+    // its chunk from those lanes with shuffles when the group is used
+    // (assemble).  Loading each chunk's own words instead read most bytes
+    // two or three times through L2 (2.1x the L2 sectors of group 128).
+    static constexpr bool SHUF = G == 32 && CB % 4 != 0;
     __device__ __forceinline__ static void order(const uint32_t (&r)[NW], uint32_t (&w)[NW], bool odd)
     {
 #pragma unroll
         for (int i = 0; i < NW; i++) w[i] = odd ? r[(i + NW - 1) % NW] : r[i];
+    }
+    // SHUF: the lane's words t and t + 4 of the group (p is the chunk at byte
+    // t * CB of the group; the words of a group lie inside it)
+    __device__ __forceinline__ static void load_words(const uint8_t* p, int t, uint32_t (&r)[NW])
+    {
+        const uint32_t* g = reinterpret_cast<const uint32_t*>(p - t * CB);
+        r[0] = t < BITS ? ldg_stream32(g + t) : 0u;
+        if constexpr (NW > 1) r[1] = t + 4 < BITS ? ldg_stream32(g + t + 4) : 0u;
+    }
+    // SHUF: this thread's chunk words from the loaded words of its row's lanes
+    // (every lane of the warp calls it)
+    __device__ __forceinline__ static void assemble(const uint32_t (&r)[NW], uint32_t (&w)[NW], int lane)
+    {
+        const int t = lane & 3, byte0 = t * CB, wa = byte0 >> 2, sh = (byte0 & 3) * 8;
+        const int srcA = (lane & ~3) | (wa & 3), srcB = (lane & ~3) | ((wa + 1) & 3);
+        uint32_t a = __shfl_sync(0xffffffffu, r[0], srcA);
+        uint32_t b = __shfl_sync(0xffffffffu, r[0], srcB);
+        if constexpr (NW > 1) {
+            const uint32_t a1 = __shfl_sync(0xffffffffu, r[1], srcA);
+            const uint32_t b1 = __shfl_sync(0xffffffffu, r[1], srcB);
+            a = wa < 4 ? a : a1;
+            b = wa + 1 < 4 ? b : b1;
+        }
+        w[0] = __funnelshift_r(a, b, sh);
+        if constexpr (NW > 1) w[1] = sh ? b >> sh : b;
     }
     __device__ __forceinline__ static void load(const uint8_t* p, uint32_t (&w)[NW])
     {
@@ -833,8 +865,13 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     // ring with the codes; affine parameters are staged per x block)
     auto issue = [&](auto slot_c, auto rel_c) {
         constexpr int SLOT = decltype(slot_c)::value, REL = decltype(rel_c)::value;
-        Chunk<BITS, G>::load(p0 + REL * GB, wr[SLOT][0]);
-        Chunk<BITS, G>::load(p1 + REL * GB, wr[SLOT][1]);
+        if constexpr (Chunk<BITS, G>::SHUF) {
+            Chunk<BITS, G>::load_words(p0 + REL * GB, t, wr[SLOT][0]);
+            Chunk<BITS, G>::load_words(p1 + REL * GB, t, wr[SLOT][1]);
+        } else {
+            Chunk<BITS, G>::load(p0 + REL * GB, wr[SLOT][0]);
+            Chunk<BITS, G>::load(p1 + REL * GB, wr[SLOT][1]);
+        }
         if constexpr (BITS == 2) {
             const uint2 c0 = __ldg(cq0 + REL), c1 = __ldg(cq1 + REL);
             prm[SLOT][0][0] = c0.x; prm[SLOT][0][1] = c0.y;
@@ -918,7 +955,19 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
                         // staged block (a ring of them would not fit in registers)
                         const uint2 v = *reinterpret_cast<const uint2*>(ps + pw + d * kWarps * 16);
                         const uint32_t pg[2][2] = {{v.x, v.x >> 16}, {v.y, v.y >> 16}};
-                        mma_group<BITS, G, MP>(wr[d][0], wr[d][1], pg, xg, yacc, magic);
+                        if constexpr (Chunk<BITS, G>::SHUF) {
+                            uint32_t s0[NW], s1[NW];
+                            Chunk<BITS, G>::assemble(wr[d][0], s0, lane);
+                            Chunk<BITS, G>::assemble(wr[d][1], s1, lane);
+                            mma_group<BITS, G, MP>(s0, s1, pg, xg, yacc, magic);
+                        } else {
+                            mma_group<BITS, G, MP>(wr[d][0], wr[d][1], pg, xg, yacc, magic);
+                        }
+                    } else if constexpr (BITS == 2 && Chunk<BITS, G>::SHUF) {
+                        uint32_t s0[NW], s1[NW];
+                        Chunk<BITS, G>::assemble(wr[d][0], s0, lane);
+                        Chunk<BITS, G>::assemble(wr[d][1], s1, lane);
+                        mma_group<BITS, G, MP>(s0, s1, prm[d], xg, yacc, magic);
                     } else if constexpr (Chunk<BITS, G>::SPLIT) {
                         uint32_t s0[NW], s1[NW];
                         Chunk<BITS, G>::order(wr[d][0], s0, odd_chunk);
