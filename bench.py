@@ -66,7 +66,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
     ap.add_argument("--case", default="gateup1",
                     help="--mode case: one small case, three calls, for a profiler: gateup<M> (fused 28672x8192 "
-                         "gate/up decode at M), tiles<bits>[m<M>] / planar<bits>[m<M>] (8192x8192 at M=2048 or M), moe (gate/up of "
+                         "gate/up decode at M), decode<bits>g<group> (11008x4096 at M=1), tiles<bits>[m<M>] / planar<bits>[m<M>] "
+                         "(8192x8192 at M=2048 or M), moe (gate/up of "
                          "the MoE layer), w8a8 (28672x8192 at M=1), diag / repack (28672x8192 INT4)")
     return ap.parse_args()
 
@@ -75,8 +76,8 @@ def parse():
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum over the launches
 # of a layer, captured on a 2-layer stack), valid only for the kernel source
 # it was taken on.
-DECODE_TRAFFIC = {"kernel_sha256": "d2040d2ea725e654f30164a04954c6bb581e241617480fa0fecf89d5c7b9ad61",
-                  "bytes_per_layer": 453.895e6}
+DECODE_TRAFFIC = {"kernel_sha256": "c8ab2896b3e27e4446b8f876fe14824eba178210038c4c10e8aec8dc9448f74f",
+                  "bytes_per_layer": 453.950e6}
 
 
 def decode_traffic(n_layers):
@@ -917,6 +918,11 @@ def run_case(qg, name):
             call = lambda: qg.qgemm_forward_tiles(x, q, t)
         else:
             call = lambda: qg.qgemm_forward(x, q)
+    elif name.startswith("decode"):   # decode<bits>g<group>: 11008 x 4096 at M = 1
+        bits, group = (int(v) for v in name[6:].split("g"))
+        q = qg.qpack_quantize(wl.gen_weight(11008, 4096, seed=1, device=dev, outlier_frac=0.001), bits, group, 0.001)
+        x = wl.gen_x(1, 4096, device=dev)
+        call = lambda: qg.qgemm_forward(x, q)
     elif name == "moe":
         cfg = wl.MoE()
         ex = [[qg.qpack_quantize(wl.gen_weight(cfg.ffn, cfg.hidden, seed=10 * p + e, device=dev), 4, 128, 0.0)
