@@ -487,7 +487,7 @@ __device__ void stage_x_bulk(const Problem& a, int g0, int ngr, unsigned char* x
 // completed and their writes are visible; x and y are touched only after it.
 // The kernel immediately preceding a decode product on its stream therefore
 // must not write that product's weights (the quantizer ends with an empty
-// kernel for this reason).  Dependents are released after the main loop.
+// kernel for this reason).  Dependents are released when the main loop starts.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
@@ -915,6 +915,13 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     __syncthreads();
     oc.fetch(a);
 
+    // dependents may launch now: every CTA of this grid has started, and a
+    // dependent CTA cannot pass its own dependency wait (so cannot release the
+    // grid after it) before this grid has finished; its weight loads overlap
+    // this grid's main loop and tail (about 2 % on the 70B stack against
+    // releasing after the main loop)
+    pdl_release();
+
     int xnext = C::XG;      // group index (relative) at which x is staged next
     uint32_t xoff = 0;      // byte offset of group jj inside the x block
     int pw = 0;             // word offset of group jj inside the parameter block
@@ -985,7 +992,6 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
         pw += D * kWarps * 16;
     }
 
-    pdl_release();
     tile_epilogue<BITS, G, MP>(a, splits, C::slot_offset(gpsplit), tile, yacc, oc);
 }
 
