@@ -41,7 +41,7 @@ ABI_FUNCTIONS = ("qpack_query_sizes", "qpack_workspace_size", "qpack_quantize", 
                  "qgemm_device_status", "qgemm_selftest_bounded_wait", "qdiag_workspace_size", "qdiag_layer",
                  "qgemm_w8a8_workspace_size", "qgemm_forward_w8a8",
                  "qrepack_tiles_size", "qrepack_tiles", "qgemm_tiles_workspace_size", "qgemm_forward_tiles",
-                 "qgemm_last_error")
+                 "qgemm_set_dependent_launch", "qgemm_last_error")
 
 
 class QgError(RuntimeError):
@@ -370,6 +370,12 @@ def qgemm_moe_grouped_multi(x: torch.Tensor, topk_ids: torch.Tensor, experts_per
     _check(lib().qgemm_moe_grouped_multi(_ptr(x), T, _ptr(topk_ids), k, arr, E, n, ys, yt, _ptr(workspace),
                                          workspace.numel(), _stream(stream)), "qgemm_moe_grouped_multi")
     return outs
+
+
+def qgemm_set_dependent_launch(enable: bool) -> None:
+    """Programmatic dependent launch of the decode kernels, process-wide."""
+    lib().qgemm_set_dependent_launch.argtypes = [ctypes.c_int32]
+    _check(lib().qgemm_set_dependent_launch(1 if enable else 0), "qgemm_set_dependent_launch")
 
 
 def qgemm_device_status(reset: bool = False) -> int:

@@ -189,6 +189,10 @@ unsigned long long current_context_id()
     return id + 1;   // never 0 for a live context
 }
 
+// Programmatic dependent launch of the decode kernels (qgemm_set_dependent_launch).
+std::atomic<int> g_dependent_launch{1};
+bool dependent_launch_enabled() { return g_dependent_launch.load(std::memory_order_relaxed) != 0; }
+
 }  // namespace qg
 
 using namespace qg;
@@ -196,6 +200,12 @@ using namespace qg;
 extern "C" {
 
 const char* qgemm_last_error(void) { return g_err; }
+
+qg_status qgemm_set_dependent_launch(int32_t enable)
+{
+    qg::g_dependent_launch.store(enable ? 1 : 0, std::memory_order_relaxed);
+    return QG_OK;
+}
 
 qg_status qgemm_device_status(int32_t* status, int32_t reset)
 {

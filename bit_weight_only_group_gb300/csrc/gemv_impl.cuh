@@ -1140,7 +1140,7 @@ qg_status launch_cluster(K kernel, dim3 grid, int S, unsigned threads, size_t sm
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 2 : 1;
+    cfg.numAttrs = pdl && dependent_launch_enabled() ? 2 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     return QG_OK;
@@ -1176,7 +1176,7 @@ qg_status launch_x_frag(const Problem& p, cudaStream_t s)
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = dependent_launch_enabled() ? 1 : 0;
     cudaError_t e = cudaLaunchKernelEx(&cfg, k_x_frag<BITS, G, MP>, p.x, p.ldx, p.M, p.K,
                                        const_cast<unsigned char*>(p.xfrag));
     if (e != cudaSuccess) return cuda_fail(e, "x conversion kernel launch");

@@ -407,6 +407,18 @@ QG_API qg_status qgemm_moe_grouped_multi(const uint16_t* x, int32_t T, const int
 QG_API qg_status qgemm_device_status(int32_t* status, int32_t reset);
 
 /*
+ * Programmatic dependent launch of the decode kernels, process-wide
+ * (default on).  On, a decode product may start, and read its weight
+ * buffers, before the kernel launched just before it on the stream has
+ * finished (see qgemm_forward's ordering note).  enable = 0 turns this off
+ * for every later call: each decode kernel then starts only after the
+ * previous kernel on its stream has finished, so the product may follow a
+ * kernel that writes its weights (a device-side copy or repack of them).
+ * The results are the same either way.  Host-only; never fails.
+ */
+QG_API qg_status qgemm_set_dependent_launch(int32_t enable);
+
+/*
  * Diagnostics of one quantized layer against its original weights
  * ("Mixed-width quantization" page, section 6.1: unpack the quantized weights
  * and compare them element by element with the original fp16 weights --

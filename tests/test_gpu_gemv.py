@@ -324,3 +324,26 @@ def test_tensor_core_split_k_against_oracle_and_repeatable(qg, bits, group, M, y
         y32 = qg.qgemm_forward(x, qd)
         assert torch.equal(y0, y32.to(torch.bfloat16))
     assert qg.qgemm_device_status() == 0
+
+
+def test_decode_without_dependent_launch_gives_the_same_result(qg):
+    # with programmatic dependent launch off, the decode kernels wait for the
+    # previous kernel on the stream before they start; the products are the
+    # same bit for bit (a device-side copy of the weights may precede them)
+    N, K = 512, 2048
+    q, wmax = _weights(N, K, 4, 128, 0.002, seed=77)
+    qd = to_device(q)
+    for M in (1, 16):
+        x = wl.gen_x(M, K, seed=M + 7).cuda()
+        y_on = qg.qgemm_forward(x, qd)
+        try:
+            qg.qgemm_set_dependent_launch(False)
+            packed = qd.packed.clone()
+            qd.packed.zero_()
+            qd.packed.copy_(packed)          # a kernel writing the weights just before the product
+            y_off = qg.qgemm_forward(x, qd)
+        finally:
+            qg.qgemm_set_dependent_launch(True)
+        torch.cuda.synchronize()
+        assert torch.equal(y_on, y_off)
+        check_product(y_off, oracle.linear(x.cpu(), q), x.cpu(), wmax)
