@@ -82,6 +82,10 @@ constexpr int DG = 4;                   // K blocks of codes in flight per threa
 constexpr int kDeqWarps = 16;
 constexpr int kWarpA = kDeqWarps, kWarpP = kDeqWarps + 1, kWarpMma = kDeqWarps + 2;
 constexpr int kThreads = (kDeqWarps + 3) * 32;
+// Split K applies to products of at most kSplitMaxM tokens (one token tile,
+// whose grid of 256-row tiles is too small to fill the GPU); at most
+// kMaxSplit CTAs share a tile.
+constexpr int kSplitMaxM = 128, kMaxSplit = 8;
 constexpr int A_BYTES = BM * BK * 2;   // 32 KB fp16
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB fp16
 
@@ -131,6 +135,27 @@ struct Args {
 };
 
 static_assert(kDeqWarps * 32 == 512, "deq_sync counts 512 dequantization threads");
+
+// 4 consecutive y values of token m from column nb (nothing at or past N).
+__device__ __forceinline__ void store_y4(const Args& a, int m, int nb, float4 v)
+{
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+    if (a.y_bf16) {
+        __nv_bfloat16* yr = reinterpret_cast<__nv_bfloat16*>(a.y) + (size_t)m * a.ldy;
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            if (nb + j < a.N) yr[nb + j] = __float2bfloat16_rn(vv[j]);
+    } else {
+        float* yr = reinterpret_cast<float*>(a.y) + (size_t)m * a.ldy;
+        if (nb + 4 <= a.N && ((reinterpret_cast<uintptr_t>(yr + nb) & 15u) == 0)) {
+            *reinterpret_cast<float4*>(yr + nb) = v;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+                if (nb + j < a.N) yr[nb + j] = vv[j];
+        }
+    }
+}
 
 // 16 consecutive y values of token m from column nb (fp32 or bf16 per a.y_bf16;
 // nothing at or past N).
@@ -600,29 +625,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 deq_sync();
                 if (*last) {
+                    // every thread takes whole float4 columns of the tile's
+                    // tokens, all S slabs' loads of one in flight together
                     __threadfence();
-#pragma unroll 1
-                    for (int i = 0; i < 8; i++) {
-                        const int col = 128 * quarter + 16 * i;
-                        const int half = col / BN, cb = col % BN;
-                        if (half && !two) continue;
-                        const int m = m0 + MH * half + 32 * q + lane;
-                        if (m >= a.M) continue;
-                        float acc[16];
+                    const int mt = min(a.M - m0, two ? BM : MH);
+                    const int nitems = mt * (BN / 4);
+                    for (int it = threadIdx.x; it < nitems; it += kDeqWarps * 32) {
+                        const int m = m0 + it / (BN / 4), nb = n0 + 4 * (it % (BN / 4));
+                        const float* pr = a.part + (size_t)m * a.ldp + nb;
+                        const size_t zs = (size_t)a.M * a.ldp;
+                        float4 t[kMaxSplit];
 #pragma unroll
-                        for (int j = 0; j < 16; j++) acc[j] = 0.0f;
-                        for (int z = 0; z < (int)gridDim.z; z++) {
-                            const float* pr = a.part + ((size_t)z * a.M + m) * a.ldp + n0 + cb;
+                        for (int z = 0; z < kMaxSplit; z++)
+                            if (z < (int)gridDim.z) t[z] = __ldcg(reinterpret_cast<const float4*>(pr + z * zs));
+                        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-                            for (int j = 0; j < 16; j += 4) {
-                                const float4 t = __ldcg(reinterpret_cast<const float4*>(pr + j));
-                                acc[j] += t.x; acc[j + 1] += t.y; acc[j + 2] += t.z; acc[j + 3] += t.w;
+                        for (int z = 0; z < kMaxSplit; z++)
+                            if (z < (int)gridDim.z) {
+                                acc.x += t[z].x; acc.y += t[z].y; acc.z += t[z].z; acc.w += t[z].w;
                             }
-                        }
-                        uint32_t v[16];
-#pragma unroll
-                        for (int j = 0; j < 16; j++) v[j] = __float_as_uint(acc[j]);
-                        store_y16(a, m, n0 + cb, v);
+                        store_y4(a, m, nb, acc);
                     }
                 }
             }
@@ -694,10 +716,6 @@ __global__ void k_x_to_f16(const __nv_bfloat16* __restrict__ x, int M, int K, in
 }
 
 // Workspace: x converted to fp16 (K order permuted), M x K.
-// Split K applies to products of at most kSplitMaxM tokens (one token tile,
-// whose grid of 256-row tiles is too small to fill the GPU); at most
-// kMaxSplit CTAs share a tile.
-constexpr int kSplitMaxM = 128, kMaxSplit = 8;
 
 // Workspace: x converted to fp16 (K order permuted), M x K; for small M also
 // the partial slabs (kMaxSplit x M x ldp fp32) and one counter per tile.
