@@ -84,8 +84,9 @@ constexpr int kWarpA = kDeqWarps, kWarpP = kDeqWarps + 1, kWarpMma = kDeqWarps +
 constexpr int kThreads = (kDeqWarps + 3) * 32;
 // Split K applies to products of at most kSplitMaxM tokens (one token tile,
 // whose grid of 256-row tiles is too small to fill the GPU); at most
-// kMaxSplit CTAs share a tile.
-constexpr int kSplitMaxM = 128, kMaxSplit = 8;
+// kMaxSplit CTAs share a tile, and at most kSplitSlabRows / M (the partial
+// slabs of a split take S x M rows of workspace).
+constexpr int kSplitMaxM = 256, kMaxSplit = 8, kSplitSlabRows = 1024;
 constexpr int A_BYTES = BM * BK * 2;   // 32 KB fp16
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB fp16
 
@@ -718,7 +719,7 @@ __global__ void k_x_to_f16(const __nv_bfloat16* __restrict__ x, int M, int K, in
 // Workspace: x converted to fp16 (K order permuted), M x K.
 
 // Workspace: x converted to fp16 (K order permuted), M x K; for small M also
-// the partial slabs (kMaxSplit x M x ldp fp32) and one counter per tile.
+// the partial slabs (S_max x M x ldp fp32) and one counter per tile.
 struct Ws {
     __half* x16;
     float* part;
@@ -733,7 +734,7 @@ size_t ws_layout(int M, int N, int K, Ws* w, void* base)
     const int ldp = (int)ceil_div(N, BN) * BN;
     if (M <= kSplitMaxM) {
         o_part = total;
-        total += align_up((size_t)kMaxSplit * M * ldp * 4, 256);
+        total += align_up((size_t)std::min(kMaxSplit, kSplitSlabRows / M) * M * ldp * 4, 256);
         o_cnt = total;
         total += align_up((size_t)ceil_div(M, BM) * ceil_div(N, BN) * 4, 256);
     }
@@ -748,7 +749,8 @@ size_t ws_layout(int M, int N, int K, Ws* w, void* base)
 }
 
 // K splits of a launch: none above kSplitMaxM tokens; else the count (at
-// most kMaxSplit, at least 8 K blocks each, a whole number of packed tiles)
+// most min(kMaxSplit, kSplitSlabRows / M), at least 8 K blocks each, a whole
+// number of packed tiles)
 // whose waves of one-CTA-per-SM grids end soonest.  Returns the split count
 // and sets *kbs to the K blocks per split.
 int choose_ksplit(int M, int tiles, int KB, int* kbs)
@@ -758,7 +760,7 @@ int choose_ksplit(int M, int tiles, int KB, int* kbs)
     const int sms = num_sms();
     int best = 1;
     long long best_cost = ceil_div(tiles, sms) * (long long)KB;
-    for (int s = 2; s <= kMaxSplit; s++) {
+    for (int s = 2; s <= std::min(kMaxSplit, kSplitSlabRows / M); s++) {
         const int k = (int)(ceil_div(ceil_div(KB, s), PK) * PK);
         if (k < 8) break;
         const int se = (int)ceil_div(KB, k);

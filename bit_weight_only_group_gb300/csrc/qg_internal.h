@@ -40,13 +40,12 @@ qg_status launch_quantize(const uint16_t* W, float frac, const qg_qweight& w, vo
 
 // ---------------------------------------------------------------- decode GEMV
 // Largest M the register-dequant (decode) kernel takes; above it the
-// tensor-core kernel runs (split over K up to 128 tokens).  Measured: on two
-// 70B-shaped INT4 layers (L2 flushed) M = 16 decode 0.615 ms against 1.008 on
-// the tensor cores, M = 32 1.267 against 1.104 (tile-ordered copy); on the
-// 7B-shaped mixed-width stack at M = 32 the decode kernel is the faster one
-// (352 against 271 GB/s: the planar tensor-core path loads odd-width codes
-// per thread), so the decode range keeps M <= 32.
-constexpr int kGemvMaxM = 32;
+// tensor-core kernel runs (split over K up to 256 tokens).  Measured with
+// the tensor-core kernel's split K: on two 70B-shaped INT4 layers (L2
+// flushed) M = 16 decode 0.614 ms against 0.885 on the tensor cores, M = 24
+// 1.125 against 1.043 (planar), M = 32 1.295 against 1.055; on the 7B-shaped
+// mixed-width stack at M = 32, 354 GB/s on the decode kernel against 361.
+constexpr int kGemvMaxM = 16;
 // From this M on, a decode call converts x once into the fp16 fragment order
 // the CTAs stage (in the caller's workspace) and the CTAs bulk-copy their x
 // blocks, instead of every CTA converting them.

@@ -248,14 +248,14 @@ QG_API qg_status qgemm_workspace_size(int32_t M, const qg_qweight* w, size_t* by
  *   x   bf16 [M, K] row-major with row stride ldx >= K elements (DEVICE).
  *   y   [M, N] row-major with row stride ldy >= N elements, fp32 or bf16
  *       per `yt` (DEVICE).
- * M = 0 is a no-op.  M <= 32 runs the decode kernel (register dequant, split
+ * M = 0 is a no-op.  M <= 16 runs the decode kernel (register dequant, split
  * K across a thread-block cluster); larger M runs the tensor-core kernel
  * (tcgen05 with TMEM accumulators), which converts x to fp16 in the workspace;
- * up to M = 128 it also splits K over several CTAs per tile, whose partial
+ * up to M = 256 it also splits K over several CTAs per tile, whose partial
  * tiles (in the workspace) the last CTA of the tile sums in a fixed order.
  * From M = 8 the decode call also uses the workspace: x is converted once
  * into the fp16 fragment order the kernel stages (2 * K * Mpad bytes, Mpad
- * 8, 16 or 32), and every CTA copies its blocks of it; with no or a
+ * 8 or 16), and every CTA copies its blocks of it; with no or a
  * smaller workspace each CTA converts its own blocks instead, with the same
  * result, more slowly.  `ws` may be NULL when qgemm_workspace_size reports 0.
  * |x| must stay below 65520: x is converted to fp16 on every path.
@@ -280,7 +280,7 @@ QG_API qg_status qgemm_forward(const uint16_t* x, int32_t M, int32_t ldx, const 
  * The pages define the single product ("70B on one GPU" page, sections
  * 2-3); this call computes exactly that product for each weight, so each
  * ys[q] equals what qgemm_forward would write for ws[q].  In the decode range
- * (M <= 32) all n products run as one kernel launch over their concatenated
+ * (M <= 16) all n products run as one kernel launch over their concatenated
  * row tiles; above it they run one after the other on the tensor cores in
  * the caller's workspace (size: the largest qgemm_workspace_size of the ws).
  *   x     bf16 [M, K], row stride ldx >= K (DEVICE), shared by all products.
