@@ -131,6 +131,7 @@ gemv::Problem make_problem(const uint16_t* x, int M, int ldx, const qg_qweight& 
     p.fb_cap = w.fb_cap;
     p.xfrag = nullptr;
     p.status = device_status_ptr();
+    p.xg = p.xp_off = p.xslot_off = p.xbar_off = 0;
     return p;
 }
 

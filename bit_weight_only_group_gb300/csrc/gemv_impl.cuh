@@ -357,6 +357,10 @@ struct Problem {
     // CTA converts its own x blocks), and the device status word
     const unsigned char* xfrag;
     int* status;
+    // shared-memory layout with xfrag (host-computed, xpre_layout): two x
+    // buffers of xg groups each, then the parameters of all the split's
+    // groups at xp_off, the split-K slots at xslot_off, two mbarriers at xbar_off
+    int xg, xp_off, xslot_off, xbar_off;
 };
 
 __device__ __forceinline__ int x_row(const Problem& p, int m) { return p.rowmap ? p.rowmap[m] / p.xdiv : m; }
@@ -460,21 +464,24 @@ __device__ void stage_x(const Problem& a, int kbase, int ngr, unsigned char* xs,
     }
 }
 
-// The same x block from the fragment-order copy of x (a.xfrag, written once
-// per call by k_x_frag in exactly the staged layout, group after group): one
-// bulk copy by thread 0, completing on the CTA's mbarrier, which every thread
-// then waits on (bounded; a wait that gives up sets the status word and the
-// kernel carries on, so that no thread leaves a barrier the others reach).
+// An x block from the fragment-order copy of x (a.xfrag, written once per
+// call by k_x_frag in exactly the staged layout, group after group): one
+// bulk copy by thread 0 into buffer xs, completing on mbarrier bar.
 template <int BITS, int G, int MP>
-__device__ void stage_x_bulk(const Problem& a, int g0, int ngr, unsigned char* xs, uint32_t bar, uint32_t& phase)
+__device__ __forceinline__ void x_bulk_issue(const Problem& a, int g0, int ngr, unsigned char* xs, uint32_t bar)
 {
     using C = Cfg<BITS, G, MP>;
-    if (threadIdx.x == 0) {
-        const uint32_t bytes = (uint32_t)ngr * C::GSTRIDE;
-        ptx::fence_proxy_async();   // the block's earlier generic accesses before the async write
-        ptx::mbar_expect_tx(bar, bytes);
-        ptx::bulk_load(ptx::smem_u32(xs), a.xfrag + (size_t)g0 * C::GSTRIDE, bytes, bar);
-    }
+    const uint32_t bytes = (uint32_t)ngr * C::GSTRIDE;
+    ptx::fence_proxy_async();   // the buffer's earlier generic accesses before the async write
+    ptx::mbar_expect_tx(bar, bytes);
+    ptx::bulk_load(ptx::smem_u32(xs), a.xfrag + (size_t)g0 * C::GSTRIDE, bytes, bar);
+}
+
+// Every thread waits for the copy on bar (bounded; a wait that gives up sets
+// the status word and the kernel carries on, so that no thread leaves a
+// barrier the others reach).
+__device__ __forceinline__ void x_bulk_wait(const Problem& a, uint32_t bar, uint32_t& phase)
+{
     if (!ptx::mbar_wait(bar, phase) && a.status) atomicExch(a.status, (int)QG_ERR_TIMEOUT);
     phase ^= 1u;
 }
@@ -845,8 +852,14 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     const size_t pidx0 = (size_t)r0 * ng + g_begin, pidx1 = (size_t)r1 * ng + g_begin;
     const uint2* cq0 = a.cb + pidx0;
     const uint2* cq1 = a.cb + pidx1;
+    // x from the fragment-order copy (xpre): double-buffered x blocks of a.xg
+    // groups and every group's parameters staged once; else x blocks of XG
+    // groups converted by the CTA, parameters staged per block
+    const bool xpre = a.xfrag != nullptr;
+    const int XGB = xpre ? a.xg : C::XG;
+    const int poff = xpre ? a.xp_off : C::prm_offset(gpsplit);
     // affine: the staged group parameters, this thread's words of block group 0
-    const uint32_t* const ps = reinterpret_cast<const uint32_t*>(smem + C::prm_offset(gpsplit)) + warp * 16 + gq * 2;
+    const uint32_t* const ps = reinterpret_cast<const uint32_t*>(smem + poff) + warp * 16 + gq * 2;
 
     const bool odd_chunk = ((t * CB) & 4) != 0;   // the chunk starts 4 bytes past an 8-byte boundary
     // this lane's B-fragment slot (token clamped to MP-1; its column is discarded)
@@ -891,26 +904,35 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     OutCursor oc;
     oc.init(a, splits, tile);
 
-    // x from the fragment-order copy: one bulk copy per x block on this mbarrier
-    const bool xpre = a.xfrag != nullptr;
-    const uint32_t xbar = ptx::smem_u32(smem + C::mbar_offset(gpsplit, splits));
-    uint32_t xphase = 0;
+    // xpre: mbarriers of the two x buffers
+    const uint32_t xbar0 = ptx::smem_u32(smem + (xpre ? a.xbar_off : 0));
+    uint32_t xph[2] = {0u, 0u};
+    int xcur = 0;   // buffer of the current x block
+    auto xbuf = [&](int b) { return smem + (size_t)b * XGB * C::GSTRIDE; };
     if (xpre) {
         if (threadIdx.x == 0) {
-            ptx::mbar_init(xbar, 1);
+            ptx::mbar_init(xbar0, 1);
+            ptx::mbar_init(xbar0 + 8, 1);
             ptx::fence_mbar_init();
         }
         __syncthreads();
     }
 
-    uint32_t* const pblock = reinterpret_cast<uint32_t*>(smem + C::prm_offset(gpsplit));
+    uint32_t* const pblock = reinterpret_cast<uint32_t*>(smem + poff);
     if constexpr (BITS != 2)   // weight data: staged before the dependency wait
-        if (ngrp > 0) stage_prm<BITS, G>(a, tile, g_begin, min(C::XG, ngrp), pblock, blockDim.x);
+        if (ngrp > 0) stage_prm<BITS, G>(a, tile, g_begin, xpre ? ngrp : min(C::XG, ngrp), pblock, blockDim.x);
 
     pdl_wait();   // weight loads are in flight; x may come from the preceding kernel
     if (ngrp > 0) {
-        if (xpre) stage_x_bulk<BITS, G, MP>(a, g_begin, min(C::XG, ngrp), smem, xbar, xphase);
-        else stage_x<BITS, G, MP>(a, g_begin * G, min(C::XG, ngrp), smem, blockDim.x);
+        if (xpre) {
+            if (threadIdx.x == 0) {
+                x_bulk_issue<BITS, G, MP>(a, g_begin, min(XGB, ngrp), xbuf(0), xbar0);
+                if (ngrp > XGB) x_bulk_issue<BITS, G, MP>(a, g_begin + XGB, min(XGB, ngrp - XGB), xbuf(1), xbar0 + 8);
+            }
+            x_bulk_wait(a, xbar0, xph[0]);
+        } else {
+            stage_x<BITS, G, MP>(a, g_begin * G, min(C::XG, ngrp), smem, blockDim.x);
+        }
     }
     __syncthreads();
     oc.fetch(a);
@@ -922,19 +944,29 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
     // releasing after the main loop)
     pdl_release();
 
-    int xnext = C::XG;      // group index (relative) at which x is staged next
-    uint32_t xoff = 0;      // byte offset of group jj inside the x block
+    int xnext = XGB;        // group index (relative) at which the next x block starts
+    uint32_t xoff = 0;      // byte offset of group jj inside the shared memory of x
     int pw = 0;             // word offset of group jj inside the parameter block
     for (int jj = 0; jj < ngrp; jj += D) {
         if (jj == xnext) {
             __syncthreads();
-            if (xpre) stage_x_bulk<BITS, G, MP>(a, g_begin + jj, min(C::XG, ngrp - jj), smem, xbar, xphase);
-            else stage_x<BITS, G, MP>(a, (g_begin + jj) * G, min(C::XG, ngrp - jj), smem, blockDim.x);
-            if constexpr (BITS != 2) stage_prm<BITS, G>(a, tile, g_begin + jj, min(C::XG, ngrp - jj), pblock, blockDim.x);
-            __syncthreads();
-            xnext += C::XG;
-            xoff = 0;
-            pw = 0;
+            if (xpre) {
+                // the finished buffer takes the block after next; the next one
+                // was copied during the previous block
+                if (threadIdx.x == 0 && jj + XGB < ngrp)
+                    x_bulk_issue<BITS, G, MP>(a, g_begin + jj + XGB, min(XGB, ngrp - jj - XGB), xbuf(xcur),
+                                              xbar0 + 8 * xcur);
+                xcur ^= 1;
+                x_bulk_wait(a, xbar0 + 8 * xcur, xph[xcur]);
+                xoff = (uint32_t)(xcur * XGB * C::GSTRIDE);
+            } else {
+                stage_x<BITS, G, MP>(a, (g_begin + jj) * G, min(C::XG, ngrp - jj), smem, blockDim.x);
+                if constexpr (BITS != 2) stage_prm<BITS, G>(a, tile, g_begin + jj, min(C::XG, ngrp - jj), pblock, blockDim.x);
+                __syncthreads();
+                xoff = 0;
+                pw = 0;
+            }
+            xnext += XGB;
         }
         const unsigned char* xb[NT];
 #pragma unroll
@@ -992,7 +1024,7 @@ __device__ __forceinline__ void gemv_body(const Problem& a, int splits, int gpsp
         pw += D * kWarps * 16;
     }
 
-    tile_epilogue<BITS, G, MP>(a, splits, C::slot_offset(gpsplit), tile, yacc, oc);
+    tile_epilogue<BITS, G, MP>(a, splits, xpre ? a.xslot_off : C::slot_offset(gpsplit), tile, yacc, oc);
 }
 
 template <int BITS, int G, int MP>
@@ -1183,39 +1215,79 @@ qg_status launch_x_frag(const Problem& p, cudaStream_t s)
     return QG_OK;
 }
 
+// Shared-memory layout of a launch with the fragment-order copy of x, inside
+// the per-SM cap's share: two x buffers of xg groups, the parameters of all
+// gps groups, the split-K slots, two mbarriers.  Sets p's layout fields and
+// returns the dynamic shared memory, or 0 if two buffers of D groups do not fit.
 template <int BITS, int G, int MP>
-qg_status dense_mp(const Problem& p, cudaStream_t s)
+size_t xpre_layout(int gps, int S, Problem& p)
 {
-    if (p.xfrag) {
-        qg_status st = launch_x_frag<BITS, G, MP>(p, s);
-        if (st != QG_OK) return st;
-    }
+    using C = Cfg<BITS, G, MP>;
+    const int cap = smem_for_cap(S > 1 ? 4 : 3);
+    const int pbytes = gps * C::PSTRIDE;
+    const int slots = S > 1 ? C::SLOT_BYTES : 0;
+    const int avail = cap - pbytes - slots - 32;
+    int xg = avail > 0 ? avail / (2 * C::GSTRIDE) / C::D * C::D : 0;
+    if (xg < C::D) return 0;
+    xg = std::min(xg, (int)ceil_div(gps, C::D) * C::D);
+    p.xg = xg;
+    p.xp_off = 2 * xg * C::GSTRIDE;
+    p.xslot_off = (std::max(p.xp_off + pbytes, C::RED_BYTES) + 15) / 16 * 16;
+    p.xbar_off = p.xslot_off + slots;
+    return (size_t)std::max(p.xbar_off + 16, cap);
+}
+
+template <int BITS, int G, int MP>
+qg_status dense_mp(const Problem& p0, cudaStream_t s)
+{
+    Problem p = p0;
     const int ng = p.K / G;
     const int tiles = (int)ceil_div(p.N, kRowsPerCta);
     const int S = choose_splits(tiles, ng);
     const dim3 grid((unsigned)tiles, (unsigned)S, 1);
     const int gps = (int)ceil_div(ng, S);
+    size_t smem = decode_smem<BITS, G, MP>(gps, S);
+    if (p.xfrag) {
+        const size_t sx = xpre_layout<BITS, G, MP>(gps, S, p);
+        if (sx) {
+            smem = sx;
+            qg_status st = launch_x_frag<BITS, G, MP>(p, s);
+            if (st != QG_OK) return st;
+        } else {
+            p.xfrag = nullptr;   // no room for two x buffers: the CTAs convert x
+        }
+    }
     // programmatic dependent launch: the next product's CTAs start their weight
     // loads while this one drains (the per-SM caps of decode_smem keep them
     // from crowding the SMs this launch still uses)
-    return launch_cluster(k_gemv<BITS, G, MP>, grid, S, kWarps * 32, decode_smem<BITS, G, MP>(gps, S), true, s, p,
-                          S, gps);
+    return launch_cluster(k_gemv<BITS, G, MP>, grid, S, kWarps * 32, smem, true, s, p, S, gps);
 }
 
 template <int BITS, int G, int MP>
-qg_status multi_mp(const MultiTable& t, cudaStream_t s)
+qg_status multi_mp(const MultiTable& t0, cudaStream_t s)
 {
-    if (t.p[0].xfrag) {
-        qg_status st = launch_x_frag<BITS, G, MP>(t.p[0], s);
-        if (st != QG_OK) return st;
-    }
+    MultiTable t = t0;
     const int ng = t.p[0].K / G;
     const int tiles = t.tile_start[t.n];
     const int S = choose_splits(tiles, ng);
     const dim3 grid((unsigned)tiles, (unsigned)S, 1);
     const int gps = (int)ceil_div(ng, S);
-    return launch_cluster(k_gemv_multi<BITS, G, MP>, grid, S, kWarps * 32, decode_smem<BITS, G, MP>(gps, S), true,
-                          s, t, S, gps);
+    size_t smem = decode_smem<BITS, G, MP>(gps, S);
+    if (t.p[0].xfrag) {
+        const size_t sx = xpre_layout<BITS, G, MP>(gps, S, t.p[0]);
+        for (int q = 1; q < t.n; q++) {   // one launch, one layout
+            t.p[q].xg = t.p[0].xg; t.p[q].xp_off = t.p[0].xp_off;
+            t.p[q].xslot_off = t.p[0].xslot_off; t.p[q].xbar_off = t.p[0].xbar_off;
+        }
+        if (sx) {
+            smem = sx;
+            qg_status st = launch_x_frag<BITS, G, MP>(t.p[0], s);
+            if (st != QG_OK) return st;
+        } else {
+            for (int q = 0; q < t.n; q++) t.p[q].xfrag = nullptr;
+        }
+    }
+    return launch_cluster(k_gemv_multi<BITS, G, MP>, grid, S, kWarps * 32, smem, true, s, t, S, gps);
 }
 
 template <int BITS, int G, int MP>
