@@ -490,13 +490,17 @@ def run_prefill(qg, args, P):
                       "0.1% outliers, M=2048; weights in the tile-ordered copy (qrepack_tiles once, at load; "
                       "qgemm_forward_tiles per product)",
             "frac_of_bf16_peak": round(tflops_t / P["bf16"], 4),
+            "frac_of_bf16_sustained": round(tflops_t / P["bf16_sust"], 4),
             "planar": {"value": round(tflops, 1), "frac_of_bf16_peak": round(tflops / P["bf16"], 4),
                        "ms_per_step": round(ms, 4), "replays": n, "clocks": clocks,
                        "config": "the same layer from the planar layout (qgemm_forward per product)"},
-            "roofline": {"bound": "tensor", "achieved": round(tflops_t, 1), "peak": P["bf16"], "unit": "TFLOP/s",
-                         "frac": round(tflops_t / P["bf16"], 4), "traffic": None,
+            # the layer's products run back to back for the whole timed region
+            # (power cap active): the sustained measured peak is the denominator
+            "roofline": {"bound": "tensor", "achieved": round(tflops_t, 1), "peak": P["bf16_sust"], "unit": "TFLOP/s",
+                         "frac": round(tflops_t / P["bf16_sust"], 4), "traffic": None,
                          "kernel": "k_gemm_tc<4,128,tiles> (tcgen05, TMEM accumulators)",
-                         "peak_source": P["src"] + " bf16_tflops (burst: fp16 and bf16 share the tensor rate)"}}
+                         "peak_source": P["src"] + " bf16_tflops_sustained (kernels timed inside a long step; "
+                                        "fp16 and bf16 share the tensor rate)"}}
 
 
 def run_prefill_widths(qg, P):
