@@ -126,34 +126,53 @@ struct Args {
     int* status;
     uint32_t magic;   // gemv::kF16Magic, a run-time value (one logic op per code pair)
     ScaleSrc sc;      // 8-bit scales when sc.scale8 is set (planar kernels; the tile copy holds fp16)
-    // split K (gridDim.z > 1): CTA z takes K blocks [z * kbs, (z + 1) * kbs),
-    // writes its fp32 partial tile to part (z-th slab of M x ldp), and the last
-    // of a tile's CTAs to finish (tile_cnt) sums the slabs in z order into y
+    // split K (gridDim.z > 1): CTA z takes K blocks [z * kbs, (z + 1) * kbs)
+    // and writes its fp32 partial tile to part (z-th slab of M x ldp);
+    // k_split_sum then adds the slabs in z order into y
     int kbs;
     float* part;
     int ldp;
-    unsigned* tile_cnt;
 };
 
 static_assert(kDeqWarps * 32 == 512, "deq_sync counts 512 dequantization threads");
 
-// 4 consecutive y values of token m from column nb (nothing at or past N).
-__device__ __forceinline__ void store_y4(const Args& a, int m, int nb, float4 v)
+// y from the partial slabs of a split-K launch: every thread sums one float4
+// column of one token over the S slabs in z order (fixed: the result is
+// repeatable bit for bit) and stores it, fp32 or bf16, nothing at or past N.
+__global__ void __launch_bounds__(256) k_split_sum(const float* __restrict__ part, int S, int M, int N, int ldp,
+                                                   void* __restrict__ y, int ldy, int y_bf16)
 {
-    const float vv[4] = {v.x, v.y, v.z, v.w};
-    if (a.y_bf16) {
-        __nv_bfloat16* yr = reinterpret_cast<__nv_bfloat16*>(a.y) + (size_t)m * a.ldy;
+    const int cols = (N + 3) / 4;
+    const long long items = (long long)M * cols;
+    const size_t zs = (size_t)M * ldp;
+    for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < items;
+         it += (long long)gridDim.x * blockDim.x) {
+        const int m = (int)(it / cols), nb = 4 * (int)(it % cols);
+        const float* pr = part + (size_t)m * ldp + nb;
+        float4 t[kMaxSplit];
 #pragma unroll
-        for (int j = 0; j < 4; j++)
-            if (nb + j < a.N) yr[nb + j] = __float2bfloat16_rn(vv[j]);
-    } else {
-        float* yr = reinterpret_cast<float*>(a.y) + (size_t)m * a.ldy;
-        if (nb + 4 <= a.N && ((reinterpret_cast<uintptr_t>(yr + nb) & 15u) == 0)) {
-            *reinterpret_cast<float4*>(yr + nb) = v;
-        } else {
+        for (int z = 0; z < kMaxSplit; z++)
+            if (z < S) t[z] = __ldcg(reinterpret_cast<const float4*>(pr + z * zs));
+        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int z = 0; z < kMaxSplit; z++)
+            if (z < S) {
+                v[0] += t[z].x; v[1] += t[z].y; v[2] += t[z].z; v[3] += t[z].w;
+            }
+        if (y_bf16) {
+            __nv_bfloat16* yr = reinterpret_cast<__nv_bfloat16*>(y) + (size_t)m * ldy;
 #pragma unroll
             for (int j = 0; j < 4; j++)
-                if (nb + j < a.N) yr[nb + j] = vv[j];
+                if (nb + j < N) yr[nb + j] = __float2bfloat16_rn(v[j]);
+        } else {
+            float* yr = reinterpret_cast<float*>(y) + (size_t)m * ldy;
+            if (nb + 4 <= N && ((reinterpret_cast<uintptr_t>(yr + nb) & 15u) == 0)) {
+                *reinterpret_cast<float4*>(yr + nb) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; j++)
+                    if (nb + j < N) yr[nb + j] = v[j];
+            }
         }
     }
 }
@@ -612,43 +631,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (split) {
-                // the last CTA of this tile to get here sums the slabs in z order:
-                // partial stores, then a fence, then the count (no CTA waits on another)
-                __threadfence();
-                deq_sync();
-                uint32_t* last = reinterpret_cast<uint32_t*>(e_row + BN);
-                if (threadIdx.x == 0) {
-                    unsigned* cnt = a.tile_cnt + blockIdx.y * gridDim.x + blockIdx.x;
-                    const unsigned prev = atomicAdd(cnt, 1u);
-                    *last = prev + 1 == gridDim.z;
-                    if (*last) *cnt = 0u;   // ready for the next call
-                }
-                deq_sync();
-                if (*last) {
-                    // every thread takes whole float4 columns of the tile's
-                    // tokens, all S slabs' loads of one in flight together
-                    __threadfence();
-                    const int mt = min(a.M - m0, two ? BM : MH);
-                    const int nitems = mt * (BN / 4);
-                    for (int it = threadIdx.x; it < nitems; it += kDeqWarps * 32) {
-                        const int m = m0 + it / (BN / 4), nb = n0 + 4 * (it % (BN / 4));
-                        const float* pr = a.part + (size_t)m * a.ldp + nb;
-                        const size_t zs = (size_t)a.M * a.ldp;
-                        float4 t[kMaxSplit];
-#pragma unroll
-                        for (int z = 0; z < kMaxSplit; z++)
-                            if (z < (int)gridDim.z) t[z] = __ldcg(reinterpret_cast<const float4*>(pr + z * zs));
-                        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll
-                        for (int z = 0; z < kMaxSplit; z++)
-                            if (z < (int)gridDim.z) {
-                                acc.x += t[z].x; acc.y += t[z].y; acc.z += t[z].z; acc.w += t[z].w;
-                            }
-                        store_y4(a, m, nb, acc);
-                    }
-                }
-            }
         } else {
             ok = false;
         }
@@ -719,30 +701,26 @@ __global__ void k_x_to_f16(const __nv_bfloat16* __restrict__ x, int M, int K, in
 // Workspace: x converted to fp16 (K order permuted), M x K.
 
 // Workspace: x converted to fp16 (K order permuted), M x K; for small M also
-// the partial slabs (S_max x M x ldp fp32) and one counter per tile.
+// the partial slabs (S_max x M x ldp fp32).
 struct Ws {
     __half* x16;
     float* part;
-    unsigned* cnt;
     int ldp;
 };
 
 size_t ws_layout(int M, int N, int K, Ws* w, void* base)
 {
     const size_t x16 = align_up((size_t)M * K * 2, 256);
-    size_t total = x16, o_part = 0, o_cnt = 0;
+    size_t total = x16, o_part = 0;
     const int ldp = (int)ceil_div(N, BN) * BN;
     if (M <= kSplitMaxM) {
         o_part = total;
         total += align_up((size_t)std::min(kMaxSplit, kSplitSlabRows / M) * M * ldp * 4, 256);
-        o_cnt = total;
-        total += align_up((size_t)ceil_div(M, BM) * ceil_div(N, BN) * 4, 256);
     }
     if (w && base) {
         char* b = static_cast<char*>(base);
         w->x16 = reinterpret_cast<__half*>(b);
         w->part = M <= kSplitMaxM ? reinterpret_cast<float*>(b + o_part) : nullptr;
-        w->cnt = M <= kSplitMaxM ? reinterpret_cast<unsigned*>(b + o_cnt) : nullptr;
         w->ldp = ldp;
     }
     return total;
@@ -815,13 +793,13 @@ qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void
     const int splits = choose_ksplit(M, tm * tn, w.K / BK, &a.kbs);
     a.part = p.part;
     a.ldp = p.ldp;
-    a.tile_cnt = p.cnt;
-    if (splits > 1) {
-        cudaError_t e0 = cudaMemsetAsync(p.cnt, 0, sizeof(unsigned) * (size_t)tm * tn, s);
-        if (e0 != cudaSuccess) return cuda_fail(e0, "split counters memset");
-    }
     dim3 grid((unsigned)tm, (unsigned)tn, (unsigned)splits);
     k_gemm_tc<BITS, G, TILES><<<grid, kThreads, C::SMEM, s>>>(xmap, wmap, a);
+    if (splits > 1) {
+        const long long items = (long long)M * ceil_div(w.N, 4);
+        const int blocks = (int)std::min<long long>(ceil_div(items, 256), 4LL * num_sms());
+        k_split_sum<<<blocks, 256, 0, s>>>(p.part, splits, M, w.N, p.ldp, y, ldy, yt == QG_Y_BF16);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
     return QG_OK;
