@@ -42,7 +42,9 @@ __device__ __forceinline__ uint32_t e4m3_scale_bits(uint32_t c, int E)
 
 // fp16 scale bits of fallback group j of row n (0 if the list lacks it: a
 // list that overflowed its capacity is searched only within the capacity).
-__device__ __forceinline__ uint32_t fallback_scale_bits(const ScaleSrc& s, int n, int j)
+// Not inlined: the path is rare, and its loop would weigh on the registers
+// of the loops that convert scales as they use them.
+static __device__ __noinline__ uint32_t fallback_scale_bits(const ScaleSrc& s, int n, int j)
 {
     int lo = min(__ldg(s.fb_row_ptr + n), s.fb_cap);
     const int end = min(__ldg(s.fb_row_ptr + n + 1), s.fb_cap);
