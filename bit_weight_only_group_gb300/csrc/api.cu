@@ -410,13 +410,15 @@ qg_status qgemm_forward_multi(const uint16_t* x, int32_t M, int32_t ldx, const q
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (M <= kGemvMaxM) return launch_gemv_multi(x, M, ldx, ws, n, ys, ldys, yt, work, work_bytes, s);
-    // above the decode range: one tensor-core product after the other in the caller's workspace
+    // above the decode range: one tensor-core product after the other in the
+    // caller's workspace, x converted to fp16 by the first (same K and width:
+    // the same operand order) and read by all
     for (int q = 0; q < n; q++) {
         const size_t need = gemm_workspace_bytes(M, ws[q]);
         if (need && (!work || work_bytes < need))
             return fail(QG_ERR_WORKSPACE, "qgemm_forward_multi: workspace %zu bytes < %zu", work ? work_bytes : (size_t)0, need);
         if (need && !aligned(work, 256)) return fail(QG_ERR_ALIGNMENT, "qgemm_forward_multi: workspace must be 256-byte aligned");
-        qg_status st = launch_gemm(x, M, ldx, ws[q], ys[q], ldys[q], yt, work, work_bytes, s);
+        qg_status st = launch_gemm(x, M, ldx, ws[q], ys[q], ldys[q], yt, work, work_bytes, q == 0, s);
         if (st != QG_OK) return st;
     }
     return QG_OK;
@@ -451,7 +453,7 @@ qg_status qgemm_forward(const uint16_t* x, int32_t M, int32_t ldx, const qg_qwei
     if (need && (!ws || ws_bytes < need))
         return fail(QG_ERR_WORKSPACE, "qgemm_forward: workspace %zu bytes < %zu", ws ? ws_bytes : (size_t)0, need);
     if (need && !aligned(ws, 256)) return fail(QG_ERR_ALIGNMENT, "qgemm_forward: workspace must be 256-byte aligned");
-    return launch_gemm(x, M, ldx, *w, y, ldy, yt, ws, ws_bytes, s);
+    return launch_gemm(x, M, ldx, *w, y, ldy, yt, ws, ws_bytes, true, s);
 }
 
 qg_status qgemm_moe_workspace_size(int32_t T, int32_t k, int32_t E, const qg_qweight* experts,

@@ -32,35 +32,16 @@ qg_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, 
 size_t gemm_workspace_bytes(int M, const qg_qweight& w) { return tc::ws_layout(M, w.N, w.K, nullptr, nullptr); }
 
 qg_status launch_gemm(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy, qg_ydtype yt,
-                      void* ws, size_t, cudaStream_t s)
+                      void* ws, size_t, bool convert_x, cudaStream_t s)
 {
     switch (w.bits) {
-        case 2: return tc::run_bits<2, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, s);
-        case 3: return tc::run_bits<3, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, s);
-        case 4: return tc::run_bits<4, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, s);
-        case 5: return tc::run_bits<5, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, s);
-        case 6: return tc::run_bits<6, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, s);
-        default: return tc::run_bits<8, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, s);
+        case 2: return tc::run_bits<2, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, convert_x, s);
+        case 3: return tc::run_bits<3, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, convert_x, s);
+        case 4: return tc::run_bits<4, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, convert_x, s);
+        case 5: return tc::run_bits<5, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, convert_x, s);
+        case 6: return tc::run_bits<6, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, convert_x, s);
+        default: return tc::run_bits<8, false>(x, M, ldx, w, nullptr, y, ldy, yt, ws, convert_x, s);
     }
-}
-
-qg_status launch_x_to_f16(const uint16_t* x, int M, int K, int ldx, int bits, void* x16, cudaStream_t s)
-{
-    const long long total32 = (long long)M * K / 32;
-    const int blocks = (int)std::min<long long>(ceil_div(total32, 256), (long long)num_sms() * 8);
-    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
-    __half* o = static_cast<__half*>(x16);
-    switch (bits) {
-        case 2: tc::k_x_to_f16<2><<<blocks, 256, 0, s>>>(xb, M, K, ldx, o); break;
-        case 3: tc::k_x_to_f16<3><<<blocks, 256, 0, s>>>(xb, M, K, ldx, o); break;
-        case 4: tc::k_x_to_f16<4><<<blocks, 256, 0, s>>>(xb, M, K, ldx, o); break;
-        case 5: tc::k_x_to_f16<5><<<blocks, 256, 0, s>>>(xb, M, K, ldx, o); break;
-        case 6: tc::k_x_to_f16<6><<<blocks, 256, 0, s>>>(xb, M, K, ldx, o); break;
-        default: tc::k_x_to_f16<8><<<blocks, 256, 0, s>>>(xb, M, K, ldx, o); break;
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "x conversion launch");
-    return QG_OK;
 }
 
 }  // namespace qg

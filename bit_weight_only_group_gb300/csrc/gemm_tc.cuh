@@ -42,6 +42,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <utility>
 
 #include "gemv_impl.cuh"
 #include "ptx.cuh"
@@ -125,6 +126,8 @@ static_assert(kDeqWarps * 32 == 512, "deq_sync counts 512 dequantization threads
 static __global__ void __launch_bounds__(256) k_split_sum(const float* __restrict__ part, int S, int M, int N, int ldp,
                                                    void* __restrict__ y, int ldy, int y_bf16)
 {
+    gemv::pdl_release();
+    gemv::pdl_wait();   // the slabs come from the kernel just before
     const int cols = (N + 3) / 4;
     const long long items = (long long)M * cols;
     const size_t zs = (size_t)M * ldp;
@@ -241,9 +244,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
+    // programmatic dependent launch: the next kernel on the stream may start
+    // once every CTA got here (it waits for this grid before touching what
+    // this grid writes); x, y and the slabs are touched only after pdl_wait
+    gemv::pdl_release();
 
     if (warp == kWarpA) {
         // ------------------------------------------------ x tiles (TMA)
+        gemv::pdl_wait();   // x in fp16 comes from the kernel just before
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
@@ -575,6 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         // ------------------------------------------------ epilogue: TMEM -> y
+        gemv::pdl_wait();   // (long done: the x tiles came after it) before y and the slabs are written
         deq_sync();   // every row's exponent is in shared memory
         if (ok && ptx::mbar_wait(acc_full, 0)) {
             ptx::tc_fence_after();
@@ -646,6 +655,8 @@ constexpr bool perm_within_8()
 template <int BITS>
 __global__ void k_x_to_f16(const __nv_bfloat16* __restrict__ x, int M, int K, int ldx, __half* __restrict__ out)
 {
+    gemv::pdl_release();
+    gemv::pdl_wait();   // x may come from the kernel just before; out may still be read by it
     constexpr int R = perm_within_8<BITS>() ? 8 : 32;
     const long long total = (long long)M * K / R;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -680,8 +691,6 @@ __global__ void k_x_to_f16(const __nv_bfloat16* __restrict__ x, int M, int K, in
         for (int j = 0; j < R / 8; j++) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
     }
 }
-
-// Workspace: x converted to fp16 (K order permuted), M x K.
 
 // Workspace: x converted to fp16 (K order permuted), M x K; for small M also
 // the partial slabs (S_max x M x ldp fp32).
@@ -735,17 +744,41 @@ inline int choose_ksplit(int M, int tiles, int KB, int* kbs)
     return best;
 }
 
+// Launch with programmatic stream serialization when dependent launch is on
+// (every kernel launched this way releases its dependents and waits for the
+// kernel before it on its own).
+template <typename... KArgs, typename... Act>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, int threads, size_t smem, cudaStream_t s,
+                              Act&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent_launch_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...);
+}
+
+// One product.  convert_x = false: x is already in the workspace in fp16 (a
+// fused call's later products, which share the first one's conversion).
 template <int BITS, int G, bool TILES, bool S8>
 qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void* tiles, void* y, int ldy,
-              qg_ydtype yt, void* ws, cudaStream_t s)
+              qg_ydtype yt, void* ws, bool convert_x, cudaStream_t s)
 {
     using C = Cfg<BITS, G, TILES>;
     Ws p{};
     ws_layout(M, w.N, w.K, &p, ws);
-    {
+    if (convert_x) {
         const long long total32 = (long long)M * w.K / 32;
         const int blocks = (int)std::min<long long>(ceil_div(total32, 256), (long long)num_sms() * 8);
-        k_x_to_f16<BITS><<<blocks, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), M, w.K, ldx, p.x16);
+        const cudaError_t e = launch_pdl(k_x_to_f16<BITS>, dim3((unsigned)blocks), 256, 0, s,
+                                         reinterpret_cast<const __nv_bfloat16*>(x), M, w.K, ldx, p.x16);
+        if (e != cudaSuccess) return cuda_fail(e, "x conversion launch");
     }
     CUtensorMap xmap, wmap;
     qg_status st = encode_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.x16, (uint64_t)w.K, (uint64_t)M,
@@ -777,30 +810,31 @@ qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void
     a.part = p.part;
     a.ldp = p.ldp;
     dim3 grid((unsigned)tm, (unsigned)tn, (unsigned)splits);
-    k_gemm_tc<BITS, G, TILES, S8><<<grid, kThreads, C::SMEM, s>>>(xmap, wmap, a);
+    cudaError_t e = launch_pdl(k_gemm_tc<BITS, G, TILES, S8>, grid, kThreads, C::SMEM, s, xmap, wmap, a);
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
     if (splits > 1) {
         const long long items = (long long)M * ceil_div(w.N, 4);
         const int blocks = (int)std::min<long long>(ceil_div(items, 256), 4LL * num_sms());
-        k_split_sum<<<blocks, 256, 0, s>>>(p.part, splits, M, w.N, p.ldp, y, ldy, yt == QG_Y_BF16);
+        e = launch_pdl(k_split_sum, dim3((unsigned)blocks), 256, 0, s, (const float*)p.part, splits, M, w.N, p.ldp, y,
+                       ldy, (int)(yt == QG_Y_BF16));
+        if (e != cudaSuccess) return cuda_fail(e, "split-K sum launch");
     }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
     return QG_OK;
 }
 
 template <int BITS, bool TILES>
 qg_status run_bits(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void* tiles, void* y, int ldy,
-                   qg_ydtype yt, void* ws, cudaStream_t s)
+                   qg_ydtype yt, void* ws, bool convert_x, cudaStream_t s)
 {
     // planar kernels with 8-bit scales convert them as they use them (their own
     // instantiation); the tile-ordered copy always holds fp16 scales
     if (!TILES && w.scale8)
-        return w.group == 32   ? run<BITS, 32, TILES, !TILES>(x, M, ldx, w, tiles, y, ldy, yt, ws, s)
-               : w.group == 64 ? run<BITS, 64, TILES, !TILES>(x, M, ldx, w, tiles, y, ldy, yt, ws, s)
-                               : run<BITS, 128, TILES, !TILES>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
-    return w.group == 32   ? run<BITS, 32, TILES, false>(x, M, ldx, w, tiles, y, ldy, yt, ws, s)
-           : w.group == 64 ? run<BITS, 64, TILES, false>(x, M, ldx, w, tiles, y, ldy, yt, ws, s)
-                           : run<BITS, 128, TILES, false>(x, M, ldx, w, tiles, y, ldy, yt, ws, s);
+        return w.group == 32   ? run<BITS, 32, TILES, !TILES>(x, M, ldx, w, tiles, y, ldy, yt, ws, convert_x, s)
+               : w.group == 64 ? run<BITS, 64, TILES, !TILES>(x, M, ldx, w, tiles, y, ldy, yt, ws, convert_x, s)
+                               : run<BITS, 128, TILES, !TILES>(x, M, ldx, w, tiles, y, ldy, yt, ws, convert_x, s);
+    return w.group == 32   ? run<BITS, 32, TILES, false>(x, M, ldx, w, tiles, y, ldy, yt, ws, convert_x, s)
+           : w.group == 64 ? run<BITS, 64, TILES, false>(x, M, ldx, w, tiles, y, ldy, yt, ws, convert_x, s)
+                           : run<BITS, 128, TILES, false>(x, M, ldx, w, tiles, y, ldy, yt, ws, convert_x, s);
 }
 
 }  // namespace tc

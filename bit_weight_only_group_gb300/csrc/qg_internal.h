@@ -77,8 +77,10 @@ qg_status launch_gemv_multi(const uint16_t* x, int M, int ldx, const qg_qweight*
 
 // ---------------------------------------------------------------- tensor-core GEMM
 size_t gemm_workspace_bytes(int M, const qg_qweight& w);
+// convert_x = false: x is already in the workspace in fp16 (the later
+// products of a fused call, after the first one converted it).
 qg_status launch_gemm(const uint16_t* x, int M, int ldx, const qg_qweight& w, void* y, int ldy,
-                      qg_ydtype yt, void* ws, size_t ws_bytes, cudaStream_t s);
+                      qg_ydtype yt, void* ws, size_t ws_bytes, bool convert_x, cudaStream_t s);
 
 // Tile-ordered copy of a quantized weight for the tensor-core kernel: for
 // every 256-row tile and 64-wide K block, one contiguous block of the
@@ -100,7 +102,6 @@ inline size_t tiles_bytes(const qg_qweight& w)
 qg_status launch_repack(const qg_qweight& w, void* tiles, cudaStream_t s);
 // Tensor-core product over the tile-ordered copy (workspace: x in fp16, as
 // gemm_workspace_bytes).
-qg_status launch_x_to_f16(const uint16_t* x, int M, int K, int ldx, int bits, void* x16, cudaStream_t s);
 qg_status launch_gemm_tiles(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void* tiles, void* y,
                             int ldy, qg_ydtype yt, void* ws, cudaStream_t s);
 

@@ -252,18 +252,18 @@ QG_API qg_status qgemm_workspace_size(int32_t M, const qg_qweight* w, size_t* by
  * K across a thread-block cluster); larger M runs the tensor-core kernel
  * (tcgen05 with TMEM accumulators), which converts x to fp16 in the workspace;
  * up to M = 256 it also splits K over several CTAs per tile, whose partial
- * tiles (in the workspace) the last CTA of the tile sums in a fixed order.
+ * tiles (in the workspace) a second small kernel sums in a fixed order.
  * From M = 8 the decode call also uses the workspace: x is converted once
  * into the fp16 fragment order the kernel stages (2 * K * Mpad bytes, Mpad
  * 8 or 16), and every CTA copies its blocks of it; with no or a
  * smaller workspace each CTA converts its own blocks instead, with the same
  * result, more slowly.  `ws` may be NULL when qgemm_workspace_size reports 0.
  * |x| must stay below 65520: x is converted to fp16 on every path.
- * Ordering: the decode kernel is launched with programmatic dependent launch,
- * so it may start, and read the weight buffers (packed, scale, zp, codebook,
- * outlier CSR, 8-bit scale arrays), before the kernel launched just before it
- * on the same stream has finished; it reads x and writes y only after that
- * kernel has completed.
+ * Ordering: the product's kernels are launched with programmatic dependent
+ * launch, so a product may start, and read the weight buffers (packed,
+ * scale, zp, codebook, outlier CSR, 8-bit scale arrays), before the kernel
+ * launched just before it on the same stream has finished; it reads x and
+ * writes y and the workspace only after that kernel has completed.
  * The kernel launched immediately before qgemm_forward on the stream must
  * therefore not write w's buffers (qpack_quantize ends with an empty kernel,
  * and copies are not kernels, so quantizing or uploading on the same stream
@@ -282,7 +282,8 @@ QG_API qg_status qgemm_forward(const uint16_t* x, int32_t M, int32_t ldx, const 
  * ys[q] equals what qgemm_forward would write for ws[q].  In the decode range
  * (M <= 16) all n products run as one kernel launch over their concatenated
  * row tiles; above it they run one after the other on the tensor cores in
- * the caller's workspace (size: the largest qgemm_workspace_size of the ws).
+ * the caller's workspace (size: the largest qgemm_workspace_size of the ws),
+ * with x converted to fp16 once for all of them.
  *   x     bf16 [M, K], row stride ldx >= K (DEVICE), shared by all products.
  *   ws    host array of n descriptors, 1 <= n <= 4, same K, bits and group.
  *   ys    host array of n DEVICE pointers, ys[q] [M, ws[q].N] with row stride
@@ -407,14 +408,15 @@ QG_API qg_status qgemm_moe_grouped_multi(const uint16_t* x, int32_t T, const int
 QG_API qg_status qgemm_device_status(int32_t* status, int32_t reset);
 
 /*
- * Programmatic dependent launch of the decode kernels, process-wide
- * (default on).  On, a decode product may start, and read its weight
- * buffers, before the kernel launched just before it on the stream has
- * finished (see qgemm_forward's ordering note).  enable = 0 turns this off
- * for every later call: each decode kernel then starts only after the
- * previous kernel on its stream has finished, so the product may follow a
- * kernel that writes its weights (a device-side copy or repack of them).
- * The results are the same either way.  Host-only; never fails.
+ * Programmatic dependent launch of the dense products (decode and
+ * tensor-core kernels, with their x conversion and split-K sum), process-wide
+ * (default on).  On, a product may start, and read its weight buffers,
+ * before the kernel launched just before it on the stream has finished (see
+ * qgemm_forward's ordering note).  enable = 0 turns this off for every later
+ * call: each kernel then starts only after the previous kernel on its
+ * stream has finished, so the product may follow a kernel that writes its
+ * weights (a device-side copy or repack of them).  The results are the same
+ * either way.  Host-only; never fails.
  */
 QG_API qg_status qgemm_set_dependent_launch(int32_t enable);
 

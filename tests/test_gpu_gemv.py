@@ -216,7 +216,7 @@ def test_tensor_core_path_full_size_sampled(qg):
 
 
 @pytest.mark.parametrize("bits,group,M", [(4, 128, 1), (4, 128, 8), (3, 64, 16), (4, 128, 130), (5, 32, 4), (2, 32, 130),
-                                          (4, 128, 64), (6, 64, 100)])
+                                          (4, 128, 64), (6, 64, 100), (3, 64, 300)])
 def test_forward_multi_against_oracle(qg, bits, group, M):
     # a fused projection: three weights sharing x (different N, one ragged
     # tile) in one call; each output is the single product of its weight
@@ -224,10 +224,16 @@ def test_forward_multi_against_oracle(qg, bits, group, M):
     shapes = [(512, 11), (128, 12), (200, 13)]
     qs = [_weights(N, K, bits, group, 0.002, seed=sd) for N, sd in shapes]
     x = wl.gen_x(M, K, seed=M + 5)
-    ys = qg.qgemm_forward_multi(x.cuda(), [to_device(q) for q, _ in qs])
+    qds = [to_device(q) for q, _ in qs]
+    ys = qg.qgemm_forward_multi(x.cuda(), qds)
     torch.cuda.synchronize()
     for (q, wmax), y in zip(qs, ys):
         check_product(y, oracle.linear(x, q), x, wmax)
+    if M > 16:
+        # on the tensor cores the later products read the first one's
+        # conversion of x and run the single call's kernels: equal bit for bit
+        for qd, y in zip(qds, ys):
+            assert torch.equal(y, qg.qgemm_forward(x.cuda(), qd))
 
 
 def test_decode_full_size_sampled(qg):
@@ -310,8 +316,8 @@ def test_decode_converted_x_matches_per_cta_staging(qg, bits, group, M):
                                                 (8, 32, 256, torch.bfloat16)])
 def test_tensor_core_split_k_against_oracle_and_repeatable(qg, bits, group, M, ytype):
     # up to 256 tokens the tensor-core kernel splits K over several CTAs per
-    # tile; the last CTA of a tile sums the partial tiles in a fixed order, so
-    # the result is repeatable bit for bit, and matches the oracle
+    # tile; a second kernel sums the partial tiles in a fixed order, so the
+    # result is repeatable bit for bit, and matches the oracle
     N, K = 600, 4096
     q, wmax = _weights(N, K, bits, group, 0.003, seed=M + bits)
     qd = to_device(q)
@@ -329,13 +335,14 @@ def test_tensor_core_split_k_against_oracle_and_repeatable(qg, bits, group, M, y
 
 
 def test_decode_without_dependent_launch_gives_the_same_result(qg):
-    # with programmatic dependent launch off, the decode kernels wait for the
-    # previous kernel on the stream before they start; the products are the
-    # same bit for bit (a device-side copy of the weights may precede them)
+    # with programmatic dependent launch off, the kernels of a product wait
+    # for the previous kernel on the stream before they start; the products
+    # are the same bit for bit (a device-side copy of the weights may precede
+    # them).  M = 64 is the split-K tensor-core chain, M = 300 the unsplit one.
     N, K = 512, 2048
     q, wmax = _weights(N, K, 4, 128, 0.002, seed=77)
     qd = to_device(q)
-    for M in (1, 16):
+    for M in (1, 16, 64, 300):
         x = wl.gen_x(M, K, seed=M + 7).cuda()
         y_on = qg.qgemm_forward(x, qd)
         try:
