@@ -116,6 +116,11 @@ struct Args {
     int kbs;
     float* part;
     int ldp;
+    // bytes of one x tile load: the TMA box holds min(256, M rounded up to 8)
+    // token rows, so that few tokens do not fill the tile with zeros (rows
+    // past the box keep stale values; they feed only accumulator rows of
+    // tokens >= M, which are never stored)
+    uint32_t x_bytes;
 };
 
 static_assert(kDeqWarps * 32 == 512, "deq_sync counts 512 dequantization threads");
@@ -257,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             for (int kb = kb0; kb < KB; kb++) {
                 if (!ptx::mbar_wait(empty_a(s), ph ^ 1u)) { ok = false; break; }
-                ptx::mbar_expect_tx(full_a(s), A_BYTES);
+                ptx::mbar_expect_tx(full_a(s), a.x_bytes);
                 ptx::tma_load_2d(a_tile(s), &xmap, kb * BK, m0, full_a(s));
                 if (++s == SA) { s = 0; ph ^= 1u; }
             }
@@ -781,8 +786,9 @@ qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void
         if (e != cudaSuccess) return cuda_fail(e, "x conversion launch");
     }
     CUtensorMap xmap, wmap;
+    const int x_rows = std::min(BM, (M + 7) & ~7);   // a whole number of 8-row swizzle atoms
     qg_status st = encode_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.x16, (uint64_t)w.K, (uint64_t)M,
-                             (uint64_t)w.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+                             (uint64_t)w.K * 2, BK, (uint32_t)x_rows, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != QG_OK) return st;
     if constexpr (C::TMA_CODES) {
         st = encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.packed, (uint64_t)w.K * BITS / 8, (uint64_t)w.N,
@@ -801,6 +807,7 @@ qg_status run(const uint16_t* x, int M, int ldx, const qg_qweight& w, const void
     a.status = device_status_ptr();
     a.magic = gemv::kF16Magic;
     a.sc = scale_src(w);
+    a.x_bytes = (uint32_t)x_rows * BK * 2;
     {
         qg_status st2 = gemv::allow_smem(k_gemm_tc<BITS, G, TILES, S8>, C::SMEM);
         if (st2 != QG_OK) return st2;
