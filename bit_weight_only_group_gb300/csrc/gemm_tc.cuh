@@ -593,38 +593,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && ptx::mbar_wait(acc_full, 0)) {
             ptx::tc_fence_after();
             // warp w reads TMEM lanes 32 (w % 4) .. (the lanes a warp may
-            // access) and a quarter of the 512 columns
+            // access) and a quarter of the 512 columns, or, with tokens in the
+            // first accumulator only, an eighth: its 256 columns over all 16
+            // warps.  Two 16-column loads are in flight per wait.
             const int q = warp & 3, quarter = warp >> 2;
             const bool split = gridDim.z > 1;
+            const int span = two ? 128 : 64;   // columns per warp
 #pragma unroll 1
-            for (int i = 0; i < 8; i++) {
-                const int col = 128 * quarter + 16 * i;       // 0..511
-                const int half = col / BN, cb = col % BN;
-                if (half && !two) continue;                   // no tokens in the second accumulator
-                const int m = m0 + MH * half + 32 * q + lane;
-                uint32_t v[16];
-                ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, v);
+            for (int i = 0; i < span / 16; i += 2) {
+                uint32_t v[2][16];
+                const int col0 = span * quarter + 16 * i;   // 0..511
+                ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col0, v[0]);
+                ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(col0 + 16), v[1]);
                 ptx::tmem_ld_wait();
-                // rows built at scale * 2^-e: multiply back by 2^e (exact)
-                const uint4 ew = *reinterpret_cast<const uint4*>(e_row + cb);
-                if (ew.x | ew.y | ew.z | ew.w) {
-                    const uint32_t ewa[4] = {ew.x, ew.y, ew.z, ew.w};
 #pragma unroll
-                    for (int j = 0; j < 16; j++) {
-                        const int ej = (ewa[j >> 2] >> (8 * (j & 3))) & 0xFF;
-                        v[j] = __float_as_uint(__uint_as_float(v[j]) * __int_as_float((127 + ej) << 23));
+                for (int u = 0; u < 2; u++) {
+                    const int col = col0 + 16 * u;
+                    const int half = col / BN, cb = col % BN;
+                    const int m = m0 + MH * half + 32 * q + lane;
+                    // rows built at scale * 2^-e: multiply back by 2^e (exact)
+                    const uint4 ew = *reinterpret_cast<const uint4*>(e_row + cb);
+                    if (ew.x | ew.y | ew.z | ew.w) {
+                        const uint32_t ewa[4] = {ew.x, ew.y, ew.z, ew.w};
+#pragma unroll
+                        for (int j = 0; j < 16; j++) {
+                            const int ej = (ewa[j >> 2] >> (8 * (j & 3))) & 0xFF;
+                            v[u][j] = __float_as_uint(__uint_as_float(v[u][j]) * __int_as_float((127 + ej) << 23));
+                        }
                     }
-                }
-                if (m < a.M) {
-                    if (split) {   // the partial tile to this CTA's slab (ldp covers whole tiles)
-                        float* pr = a.part + ((size_t)blockIdx.z * a.M + m) * a.ldp + n0 + cb;
+                    if (m < a.M) {
+                        if (split) {   // the partial tile to this CTA's slab (ldp covers whole tiles)
+                            float* pr = a.part + ((size_t)blockIdx.z * a.M + m) * a.ldp + n0 + cb;
 #pragma unroll
-                        for (int j = 0; j < 16; j += 4)
-                            __stcg(reinterpret_cast<float4*>(pr + j),
-                                   make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                               __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])));
-                    } else {
-                        store_y16(a, m, n0 + cb, v);
+                            for (int j = 0; j < 16; j += 4)
+                                __stcg(reinterpret_cast<float4*>(pr + j),
+                                       make_float4(__uint_as_float(v[u][j]), __uint_as_float(v[u][j + 1]),
+                                                   __uint_as_float(v[u][j + 2]), __uint_as_float(v[u][j + 3])));
+                        } else {
+                            store_y16(a, m, n0 + cb, v[u]);
+                        }
                     }
                 }
             }
