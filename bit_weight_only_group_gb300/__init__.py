@@ -373,7 +373,7 @@ def qgemm_moe_grouped_multi(x: torch.Tensor, topk_ids: torch.Tensor, experts_per
 
 
 def qgemm_set_dependent_launch(enable: bool) -> None:
-    """Programmatic dependent launch of the decode kernels, process-wide."""
+    """Programmatic dependent launch of the dense products (decode and tensor-core kernels), process-wide."""
     lib().qgemm_set_dependent_launch.argtypes = [ctypes.c_int32]
     _check(lib().qgemm_set_dependent_launch(1 if enable else 0), "qgemm_set_dependent_launch")
 

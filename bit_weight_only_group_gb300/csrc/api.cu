@@ -189,7 +189,8 @@ unsigned long long current_context_id()
     return id + 1;   // never 0 for a live context
 }
 
-// Programmatic dependent launch of the decode kernels (qgemm_set_dependent_launch).
+// Programmatic dependent launch of the dense products: decode and tensor-core
+// kernels (qgemm_set_dependent_launch).
 std::atomic<int> g_dependent_launch{1};
 bool dependent_launch_enabled() { return g_dependent_launch.load(std::memory_order_relaxed) != 0; }
 

@@ -64,7 +64,8 @@ qg_status launch_gemv(const uint16_t* x, int M, int ldx, const qg_qweight& w, vo
 // it has no address on the current device) and its synchronous read
 // (optionally cleared).
 int* device_status_ptr();
-// Programmatic dependent launch of the decode kernels (qgemm_set_dependent_launch).
+// Programmatic dependent launch of the decode and tensor-core kernels
+// (qgemm_set_dependent_launch).
 bool dependent_launch_enabled();
 qg_status read_device_status(int* out, int reset);
 // A kernel whose one mbarrier wait (limit polls) must give up (QG_ERR_TIMEOUT).
