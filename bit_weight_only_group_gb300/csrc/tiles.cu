@@ -62,18 +62,30 @@ qg_status repack_bits(const qg_qweight& w, void* tiles, cudaStream_t s)
     return QG_OK;
 }
 
+// Launched after the repack: a product that reads the copy next on the
+// stream may start its code loads before the kernel just before it has
+// finished (programmatic dependent launch), so that kernel must not be the
+// one that wrote the copy.
+__global__ void k_repack_done() {}
+
 }  // namespace
 
 qg_status launch_repack(const qg_qweight& w, void* tiles, cudaStream_t s)
 {
+    qg_status st;
     switch (w.bits) {
-        case 2: return repack_bits<2>(w, tiles, s);
-        case 3: return repack_bits<3>(w, tiles, s);
-        case 4: return repack_bits<4>(w, tiles, s);
-        case 5: return repack_bits<5>(w, tiles, s);
-        case 6: return repack_bits<6>(w, tiles, s);
-        default: return repack_bits<8>(w, tiles, s);
+        case 2: st = repack_bits<2>(w, tiles, s); break;
+        case 3: st = repack_bits<3>(w, tiles, s); break;
+        case 4: st = repack_bits<4>(w, tiles, s); break;
+        case 5: st = repack_bits<5>(w, tiles, s); break;
+        case 6: st = repack_bits<6>(w, tiles, s); break;
+        default: st = repack_bits<8>(w, tiles, s); break;
     }
+    if (st != QG_OK) return st;
+    k_repack_done<<<1, 32, 0, s>>>();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "repack launch");
+    return QG_OK;
 }
 
 }  // namespace qg

@@ -328,6 +328,8 @@ QG_API qg_status qgemm_tiles_workspace_size(int32_t M, const qg_qweight* w, size
  * the same w); w supplies the shape, the scales (for the per-row operand
  * exponent) and the outlier CSR.  Any M >= 1 (every M runs the tensor-core
  * kernel).  Same result as qgemm_forward's tensor-core path, bit for bit.
+ * Ordering as for qgemm_forward (the kernel launched just before must not
+ * write w's buffers or `tiles`; qrepack_tiles is safe).
  * Errors: QG_ERR_INVALID_ARG, QG_ERR_ALIGNMENT, QG_ERR_WORKSPACE, QG_ERR_CUDA. */
 QG_API qg_status qgemm_forward_tiles(const uint16_t* x, int32_t M, int32_t ldx, const qg_qweight* w,
                                      const void* tiles, void* y, int32_t ldy, qg_ydtype yt, void* ws,
